@@ -1,0 +1,249 @@
+"""CPU oracle for the rate-adaptive KV-cache block quantizer.
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, by __graft_entry__.smoke() and by
+the cpu_baseline / reference leg of bench.py.  The product package never
+imports it, and it never imports the product package.  It wraps the plain fp64
+C implementation in kvq_oracle.c (see that file for the page passages each step
+follows and for the readings of the open points).
+
+Arrays: x is a uint16 numpy array of binary16 bit patterns, shape [S, T, D].
+"""
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = C.CDLL(path)
+        i64, i32, u64, dbl = C.c_int64, C.c_int32, C.c_uint64, C.c_double
+        vp = C.c_void_p
+        L.kvqo_hash32.restype = C.c_uint32
+        L.kvqo_hash32.argtypes = [u64, u64]
+        L.kvqo_hash_many.restype = None
+        L.kvqo_hash_many.argtypes = [u64, u64, i64, vp]
+        L.kvqo_set_threads.restype = C.c_int
+        L.kvqo_set_threads.argtypes = [C.c_int]
+        L.kvqo_f16_to_double.restype = dbl
+        L.kvqo_f16_to_double.argtypes = [C.c_uint16]
+        L.kvqo_double_to_f16.restype = C.c_uint16
+        L.kvqo_double_to_f16.argtypes = [dbl, C.POINTER(C.c_int)]
+        L.kvqo_num_blocks.restype = i64
+        L.kvqo_num_blocks.argtypes = [i64, i64, C.c_int, C.c_int]
+        L.kvqo_flat_index.restype = i64
+        L.kvqo_flat_index.argtypes = [i64, C.c_int, C.c_int, i64, C.c_int]
+        L.kvqo_stats.restype = None
+        L.kvqo_stats.argtypes = [vp, i64, i64, C.c_int, C.c_int, i64, i64,
+                                 vp, vp, vp, vp]
+        L.kvqo_allocate_bisect.restype = C.c_int
+        L.kvqo_allocate_bisect.argtypes = [vp, i64, i64, C.c_int, C.c_int, vp,
+                                           i64, C.c_int, dbl, vp, vp, vp, vp,
+                                           vp, vp, vp, vp, vp]
+        L.kvqo_allocate_at.restype = C.c_int
+        L.kvqo_allocate_at.argtypes = [vp, i64, i64, C.c_int, C.c_int, vp, i64,
+                                       C.c_int, dbl, dbl, dbl, vp, vp, vp, vp,
+                                       vp, vp, vp, vp]
+        L.kvqo_rate_at.restype = dbl
+        L.kvqo_rate_at.argtypes = [vp, i64, i64, C.c_int, C.c_int, vp, i64,
+                                   C.c_int, dbl]
+        L.kvqo_block_tables.restype = C.c_int
+        L.kvqo_block_tables.argtypes = [vp, i64, C.c_int, C.c_int, i64, vp, vp,
+                                        vp, vp]
+        L.kvqo_chain_cost.restype = None
+        L.kvqo_chain_cost.argtypes = [vp, i64, C.c_int, C.c_int, i64,
+                                      C.c_uint32, vp, vp]
+        L.kvqo_quantize.restype = None
+        L.kvqo_quantize.argtypes = [vp, i64, i64, C.c_int, C.c_int, vp, vp, u64,
+                                    u64, i64, i64, vp]
+        L.kvqo_dequantize.restype = C.c_int
+        L.kvqo_dequantize.argtypes = [vp, vp, i64, i64, C.c_int, C.c_int, i64,
+                                      i64, vp]
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _x(x):
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float16:
+        x = x.view(np.uint16)
+    assert x.dtype == np.uint16 and x.ndim == 3, "x must be [S,T,D] binary16"
+    return x
+
+
+def _ids(ids):
+    if ids is None:
+        return None
+    return np.ascontiguousarray(np.asarray(ids, dtype=np.int64))
+
+
+def set_threads(n: int) -> int:
+    return lib().kvqo_set_threads(int(n))
+
+
+def hash32(seed: int, i: int) -> int:
+    return lib().kvqo_hash32(seed, i)
+
+
+def hash_many(seed: int, i0: int, n: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint32)
+    lib().kvqo_hash_many(seed, i0, n, _p(out))
+    return out
+
+
+def f16_to_double(h: int) -> float:
+    return lib().kvqo_f16_to_double(h)
+
+
+def double_to_f16(v: float):
+    ok = C.c_int(0)
+    h = lib().kvqo_double_to_f16(v, C.byref(ok))
+    return h, bool(ok.value)
+
+
+def num_blocks(S, T, D, G) -> int:
+    return lib().kvqo_num_blocks(S, T, D, G)
+
+
+def flat_index(T, D, G, b, e) -> int:
+    return lib().kvqo_flat_index(T, D, G, b, e)
+
+
+def stats(x, G, b0=0, nb=None):
+    """Candidates, m', atom moments (n, s1, t1, e) and the non-finite flag."""
+    x = _x(x)
+    S, T, D = x.shape
+    if nb is None:
+        nb = num_blocks(S, T, D, G) - b0
+    cand = np.zeros((nb, 17))
+    mp = np.zeros(nb, dtype=np.int32)
+    atoms = np.zeros((nb, 16, 4))
+    bad = np.zeros(nb, dtype=np.int32)
+    lib().kvqo_stats(_p(x), S, T, D, G, b0, nb, _p(cand), _p(mp), _p(atoms),
+                     _p(bad))
+    return {"cand": cand, "mprime": mp, "atoms": atoms, "nonfinite": bad}
+
+
+def _alloc_out(nb):
+    return {
+        "codebook": np.zeros((nb, 16), dtype=np.float32),
+        "k": np.zeros(nb, dtype=np.uint8),
+        "D_r": np.zeros(nb),
+        "H_r": np.zeros(nb),
+        "gap": np.zeros(nb),
+        "mask": np.zeros(nb, dtype=np.uint32),
+        "totals": np.zeros(3),
+    }
+
+
+def allocate_bisect(x, G, s, budget_bits, ids=None):
+    """Global lambda by the 40-step bisection, and the per-block choice there.
+    Returns a dict with lambda, bracket (lo, hi), status and per-block arrays
+    (ids order)."""
+    x = _x(x)
+    S, T, D = x.shape
+    ids = _ids(ids)
+    nb = num_blocks(S, T, D, G) if ids is None else len(ids)
+    out = _alloc_out(nb)
+    lam = np.zeros(1)
+    bracket = np.zeros(2)
+    st = lib().kvqo_allocate_bisect(
+        _p(x), S, T, D, G, _p(ids), nb, s, float(budget_bits), _p(lam),
+        _p(bracket), _p(out["codebook"]), _p(out["k"]), _p(out["D_r"]),
+        _p(out["H_r"]), _p(out["gap"]), _p(out["mask"]), _p(out["totals"]))
+    out.update(status=st, **{"lambda": float(lam[0])},
+               bracket=(float(bracket[0]), float(bracket[1])))
+    return out
+
+
+def allocate_at(x, G, s, lam, eta=0.0, budget_bits=0.0, ids=None):
+    """Per-block choice at a fixed lambda; lambda_next is the subgradient
+    update max(0, lambda + eta (R - budget_bits))."""
+    x = _x(x)
+    S, T, D = x.shape
+    ids = _ids(ids)
+    nb = num_blocks(S, T, D, G) if ids is None else len(ids)
+    out = _alloc_out(nb)
+    nxt = np.zeros(1)
+    st = lib().kvqo_allocate_at(
+        _p(x), S, T, D, G, _p(ids), nb, s, float(lam), float(eta),
+        float(budget_bits), _p(nxt), _p(out["codebook"]), _p(out["k"]),
+        _p(out["D_r"]), _p(out["H_r"]), _p(out["gap"]), _p(out["mask"]),
+        _p(out["totals"]))
+    out.update(status=st, lambda_next=float(nxt[0]), **{"lambda": float(lam)})
+    return out
+
+
+def rate_at(x, G, s, lam, ids=None) -> float:
+    x = _x(x)
+    S, T, D = x.shape
+    ids = _ids(ids)
+    nb = num_blocks(S, T, D, G) if ids is None else len(ids)
+    return lib().kvqo_rate_at(_p(x), S, T, D, G, _p(ids), nb, s, float(lam))
+
+
+def block_tables(x, G, b):
+    """(m', cand[17], Dpq, Mup, Mdn) of block b, each table 17x17."""
+    x = _x(x)
+    S, T, D = x.shape
+    cand = np.zeros(17)
+    Dpq, Mup, Mdn = (np.zeros((17, 17)) for _ in range(3))
+    mp = lib().kvqo_block_tables(_p(x), T, D, G, b, _p(cand), _p(Dpq),
+                                 _p(Mup), _p(Mdn))
+    return mp, cand, Dpq, Mup, Mdn
+
+
+def chain_cost(x, G, b, mask):
+    """(D_r, d_r H_r) of the chain `mask` (bit j = candidate j) of block b."""
+    x = _x(x)
+    S, T, D = x.shape
+    Dr = np.zeros(1)
+    Rr = np.zeros(1)
+    lib().kvqo_chain_cost(_p(x), T, D, G, b, int(mask), _p(Dr), _p(Rr))
+    return float(Dr[0]), float(Rr[0])
+
+
+def quantize(x, G, codebook, k, seed, index_base=0, b0=0, nb=None):
+    """Packed 4-bit codes [nb, d/2] of blocks [b0, b0+nb); codebook/k are
+    indexed from b0."""
+    x = _x(x)
+    S, T, D = x.shape
+    if nb is None:
+        nb = num_blocks(S, T, D, G) - b0
+    codebook = np.ascontiguousarray(codebook, dtype=np.float32)
+    k = np.ascontiguousarray(k, dtype=np.uint8)
+    codes = np.zeros((nb, 16 * G), dtype=np.uint8)
+    lib().kvqo_quantize(_p(x), S, T, D, G, _p(codebook), _p(k), int(seed),
+                        int(index_base), b0, nb, _p(codes))
+    return codes
+
+
+def dequantize(codes, codebook, shape, G, b0=0, nb=None, y=None):
+    """binary16 reconstruction written into y ([S,T,D] uint16) for blocks
+    [b0, b0+nb)."""
+    S, T, D = shape
+    if nb is None:
+        nb = num_blocks(S, T, D, G) - b0
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    codebook = np.ascontiguousarray(codebook, dtype=np.float32)
+    if y is None:
+        y = np.zeros((S, T, D), dtype=np.uint16)
+    bad = lib().kvqo_dequantize(_p(codes), _p(codebook), S, T, D, G, b0, nb,
+                                _p(y))
+    if bad:
+        raise ValueError("codebook level not representable in binary16")
+    return y
+
+
+if os.environ.get("KVQ_ORACLE_THREADS"):
+    set_threads(int(os.environ["KVQ_ORACLE_THREADS"]))
