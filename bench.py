@@ -1,0 +1,370 @@
+"""Throughput of the write-time KV-cache quantizer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = kvq_stats + kvq_allocate (40-step lambda bisection) + kvq_quantize
+over one [S, T, D] binary16 K/V tensor already resident in HBM: the
+Llama-3-8B-shaped single-layer prefill (K and V, 8 KV heads each, 8192
+tokens, head dim 128; blocks of one head x 32 tokens; s = 16; B = 2.5 bits per
+entry).  L2 is flushed (a 256 MB write) before every timed step, outside the
+timed interval.  The metric is binary16 input bytes quantized per second.
+
+Also reported on the same line: per-kernel times, the roofline of the dominant
+kernel (algorithmic bytes / measured time / measured HBM peak), an end-to-end
+figure through the C ABI with pinned host buffers (host->device copy of the
+input and device->host copy of codes, codebooks and totals inside the timed
+region), the number of our kernel launches, SM clocks sampled during the
+timed region, and the CPU oracle timed on a bounded sample (cpu_baseline).
+
+Multi-GPU (torchrun): every rank quantizes its own independent tensor
+(replicas: the method has no cross-tensor exchange); value = all ranks' bytes
+/ the slowest rank's time.
+
+--impl reference times the CPU oracle (the only reference implementation: the
+method's pages publish no code) on the host cores, on bounded samples of the
+same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fp16 KV GB/s quantized at budget B (1 B300) and fraction of HBM roofline"
+WORKLOAD = "llama3_8b_layer"
+WORKLOAD_DESC = ("Llama-3-8B-shaped single-layer prefill: K and V, 8 KV heads x 8192 tokens x "
+                 "128 dims fp16 (S=16 streams); K = N(0,1) x per-channel lognormal(0,0.5) with 4 "
+                 "outlier channels x10, V = Student-t(5); blocks = head x 32 tokens (4096 blocks "
+                 "of 4096), s=16, B=2.5 bits/entry, seed 0")
+CPU_SAMPLE_BLOCKS = 192
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(w, x_np, budget_per_entry, nblocks=CPU_SAMPLE_BLOCKS, seed=0):
+    """The oracle, as it stands, on a bounded sample: `nblocks` whole blocks
+    (half from K streams, half from V streams), full path (stats, 40-step
+    bisection at the same bits/entry, quantize).  Returns (GB/s, seconds,
+    threads, description)."""
+    import numpy as np
+    import oracle
+    nTB = w.T // 32
+    per = nblocks // 2
+    half = w.S // 2
+    sel = []
+    for s0 in (0, half):
+        for i in range(per):
+            sel.append((s0 + i % half, i // half))
+    sl = np.stack([x_np[h, 32 * tb:32 * tb + 32, :] for h, tb in sel])   # [n, 32, D]
+    threads = oracle.set_threads(0)
+    t0 = time.perf_counter()
+    oracle.stats(sl, w.G)
+    r = oracle.allocate_bisect(sl, w.G, w.s, budget_per_entry * sl.size)
+    oracle.quantize(sl, w.G, r["codebook"], r["k"], seed, 0)
+    dt = time.perf_counter() - t0
+    return sl.nbytes / dt / 1e9, dt, threads, (
+        "%d blocks (%d K + %d V slabs of 32 tokens x 128) of the workload, full path at the same "
+        "bits/entry; %d bytes" % (len(sel), per, per, sl.nbytes))
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle on bounded samples (rank 0 only)."""
+    if rank != 0:
+        return
+    import numpy as np
+    from rate_adaptive_kv_block_b300 import synth
+    w = synth.workload(WORKLOAD)
+    x = synth.make_numpy(w, seed=0)
+    B = w.budgets[0]
+    for _ in range(args.warmup):
+        cpu_baseline(w, x, B, nblocks=32)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        gbs, dt, thr, desc = cpu_baseline(w, x, B, nblocks=args.ref_blocks)
+        vals.append(gbs)
+        secs.append(dt)
+    value = sum(args.ref_blocks * 8192 for _ in vals) / sum(secs) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * sum(secs) / len(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": WORKLOAD_DESC, "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": thr, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-blocks", type=int, default=CPU_SAMPLE_BLOCKS)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import numpy as np
+    import torch
+    from rate_adaptive_kv_block_b300 import kvq, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+
+    w = synth.workload(WORKLOAD)
+    x_np = synth.make_numpy(w, seed=rank)
+    x = torch.from_numpy(x_np.view(np.int16)).view(torch.float16).to(dev)
+    L = kvq.Layout(w.S, w.T, w.D, w.G)
+    B = w.budgets[0] * w.entries
+    s = w.s
+    buf = kvq.Buffers(L, s, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    in_bytes = x.numel() * 2
+    nb = L.nblocks
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        kvq.kvq_stats(x, L, buf.stats, buf.status_stats)
+        if ev is not None:
+            ev[1].record(stream)
+        kvq.kvq_allocate(buf.stats, L, s, B, kvq.KVQ_BISECT40, 0.0, buf.lam, buf.workspace,
+                         buf.codebook, buf.k, buf.D_r, buf.H_r, buf.totals, buf.status)
+        if ev is not None:
+            ev[2].record(stream)
+        kvq.kvq_quantize(x, L, buf.codebook, buf.k, 0, 0, buf.codes)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st = int(buf.status.item())
+    if st != 0:
+        raise SystemExit("allocation status %d (%s)" % (st, kvq.kvq_status_string(st)))
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            step(evs[i])
+        torch.cuda.synchronize()
+    t_stats = [e[0].elapsed_time(e[1]) for e in evs]
+    t_alloc = [e[1].elapsed_time(e[2]) for e in evs]
+    t_quant = [e[2].elapsed_time(e[3]) for e in evs]
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    tot_ms = sum(t_step)
+    if pg:
+        t = torch.tensor([tot_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    value = world * args.steps * in_bytes / (tot_ms * 1e-3) / 1e9
+
+    # quantize alone with a cold L2 (the gated kernel), same launch configuration
+    qe = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        qe[i][0].record(stream)
+        kvq.kvq_quantize(x, L, buf.codebook, buf.k, 0, 0, buf.codes)
+        qe[i][1].record(stream)
+    se = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        se[i][0].record(stream)
+        kvq.kvq_stats(x, L, buf.stats, buf.status_stats)
+        se[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_qcold = [a.elapsed_time(b) for a, b in qe]
+    t_scold = [a.elapsed_time(b) for a, b in se]
+
+    # end to end through the C ABI with pinned host buffers
+    x_host = torch.from_numpy(x_np.view(np.int16)).view(torch.float16).pin_memory()
+    codes_h = torch.empty(buf.codes.shape, dtype=torch.uint8).pin_memory()
+    cb_h = torch.empty(buf.codebook.shape, dtype=torch.float32).pin_memory()
+    k_h = torch.empty(buf.k.shape, dtype=torch.uint8).pin_memory()
+    tot_h = torch.empty(3, dtype=torch.float64).pin_memory()
+    h2d = x_host.numel() * 2
+    d2h = codes_h.numel() + cb_h.numel() * 4 + k_h.numel() + 24
+    xe = torch.empty_like(x)
+
+    def e2e_step():
+        xe.copy_(x_host, non_blocking=True)
+        kvq.kvq_stats(xe, L, buf.stats, buf.status_stats)
+        kvq.kvq_allocate(buf.stats, L, s, B, kvq.KVQ_BISECT40, 0.0, buf.lam, buf.workspace,
+                         buf.codebook, buf.k, buf.D_r, buf.H_r, buf.totals, buf.status)
+        kvq.kvq_quantize(xe, L, buf.codebook, buf.k, 0, 0, buf.codes)
+        codes_h.copy_(buf.codes, non_blocking=True)
+        cb_h.copy_(buf.codebook, non_blocking=True)
+        k_h.copy_(buf.k, non_blocking=True)
+        tot_h.copy_(buf.totals, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        ee[i][0].record(stream)
+        e2e_step()
+        ee[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_e2e = sum(a.elapsed_time(b) for a, b in ee)
+    if pg:
+        t = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        t_e2e = float(t.item())
+    e2e_val = world * args.steps * in_bytes / (t_e2e * 1e-3) / 1e9
+
+    hbm, src = peaks()
+    mean = lambda v: sum(v) / len(v)
+    # algorithmic bytes per launch (per entry / per block figures)
+    q_bytes = in_bytes + in_bytes // 4 + nb * (64 + 1)
+    s_bytes = in_bytes + nb * 384
+    kern = {
+        "stats_ms": mean(t_stats), "allocate_ms": mean(t_alloc), "quantize_ms": mean(t_quant),
+        "stats_cold_ms": mean(t_scold), "quantize_cold_ms": mean(t_qcold),
+        "stats_cold_GBps": s_bytes / (mean(t_scold) * 1e-3) / 1e9,
+        "quantize_cold_GBps": q_bytes / (mean(t_qcold) * 1e-3) / 1e9,
+    }
+    kern["quantize_cold_frac_hbm"] = kern["quantize_cold_GBps"] / hbm
+    kern["stats_cold_frac_hbm"] = kern["stats_cold_GBps"] / hbm
+    shares = {"stats": mean(t_stats), "allocate": mean(t_alloc), "quantize": mean(t_quant)}
+    dominant = max(shares, key=shares.get)
+    if dominant == "allocate":
+        roof = {"kernel": "kvq_allocate (search rounds)", "bound": "alu",
+                "achieved": None, "peak": None, "unit": "TFLOP/s", "frac": None,
+                "traffic": None, "note": "see DESIGN.md: the lambda search is ALU/latency bound; "
+                "HBM kernels listed under kernels"}
+    elif dominant == "stats":
+        a = kern["stats_cold_GBps"]
+        roof = {"kernel": "kvq_stats", "bound": "hbm", "achieved": a, "peak": hbm, "unit": "GB/s",
+                "frac": a / hbm, "traffic": None, "peak_source": src}
+    else:
+        a = kern["quantize_cold_GBps"]
+        roof = {"kernel": "kvq_quantize", "bound": "hbm", "achieved": a, "peak": hbm,
+                "unit": "GB/s", "frac": a / hbm, "traffic": None, "peak_source": src}
+
+    launches_per_step = 1 + (2 + 9 + 1) + 1
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, dt, thr, desc = cpu_baseline(w, x_np, w.budgets[0])
+        cpu = {"value": gbs, "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc,
+               "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "l2": "flushed (256 MB write) before each step",
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "tokens_per_s": world * args.steps * w.T / (tot_ms * 1e-3),
+            "lambda": float(buf.lam.item()), "rate_bits_per_entry": float(buf.totals[0].item()) / w.entries,
+            "kernels": kern,
+            "roofline": roof,
+            "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+/*
+ * kvq.h -- C ABI of the B300 (sm_103a) write-time KV-cache quantizer.
+ *
+ * What it computes ("Rate-adaptive KV-cache quantizer", synthcore idea 2502):
+ * the cache is cut into blocks (one attention head x 32 tokens, or one head x
+ * 32 tokens x a feature group -- "Implementation notes"); every block r of
+ * d_r entries gets its own codebook Q_r of k <= s levels, chosen to minimise
+ * D_r + lambda d_r H_r ("Mathematical statement", "Key formulas": the
+ * Lagrangian), where D_r is the expected squared error of unbiased
+ * stochastic interpolation between neighbouring levels and H_r the entropy
+ * of the expected codepoint frequencies; one global lambda makes
+ * sum_r d_r H_r <= B.  The entries are then rounded at random to one of their
+ * two neighbouring levels with the unbiased probabilities of "Key formulas"
+ * and stored as 4-bit codes plus a per-block fp32 codebook.
+ *
+ * Call sequence (all on one CUDA stream, asynchronous, no host sync inside):
+ *     kvq_stats      -> per-block candidate levels and interval statistics
+ *     kvq_allocate   -> lambda, per-block codebook / k / D_r / H_r
+ *     kvq_quantize   -> packed codes
+ *     kvq_dequantize -> binary16 reconstruction ("decode before attention")
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" are CUDA device memory owned by the caller; the
+ *     library allocates nothing and keeps no pointer after the call returns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - Return value: KVQ_OK, KVQ_ERR_INVALID_ARG (arguments rejected on the
+ *     host before anything is launched; nothing is written) or KVQ_ERR_CUDA
+ *     (a launch failed).  Conditions that depend on the data (non-finite
+ *     inputs, an infeasible budget) are written by the kernels to the
+ *     caller's device `status` word; read it after synchronising.
+ *   - Device buffers must be 16-byte aligned.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define KVQ_OK 0
+#define KVQ_ERR_INVALID_ARG 1
+#define KVQ_ERR_CUDA 2
+#define KVQ_ERR_NONFINITE 3   /* device status: a block holds NaN or +-Inf */
+#define KVQ_ERR_INFEASIBLE 4  /* device status: budget unreachable         */
+
+/* lambda modes of kvq_allocate */
+#define KVQ_BISECT40 0        /* global lambda by the 40-step bisection      */
+#define KVQ_SUBGRADIENT 1     /* one subgradient step from a given lambda    */
+
+#define KVQ_CANDIDATES 17     /* order-statistic candidate levels per block  */
+#define KVQ_MAX_LEVELS 16     /* codes are 4 bits                            */
+
+/*
+ * Shape of one K or V tensor: [S, T, D] row-major binary16, S streams (layer
+ * x K/V x head, or any other flattening), T tokens per stream, D features.
+ * A block is 32 consecutive tokens x `group` consecutive features of one
+ * stream; d = 32 * group entries.  Blocks are numbered row-major over
+ * (stream, token block, feature group); inside a block entry e is
+ * (token - 32 * token_block) * group + (feature - group_index * group).
+ * Requirements: S >= 0, T >= 0 and T % 32 == 0, group in {8,16,32,64,128},
+ * D % group == 0, D / group <= 32.
+ */
+typedef struct kvq_layout {
+    int64_t S;
+    int64_t T;
+    int32_t D;
+    int32_t group;
+} kvq_layout;
+
+/* Number of blocks S * (T/32) * (D/group); -1 if the layout is invalid. */
+int64_t kvq_num_blocks(kvq_layout L);
+
+/* Bytes of the per-block statistics table written by kvq_stats (384 bytes per
+ * block); 0 if the layout is invalid. */
+size_t kvq_stats_bytes(kvq_layout L);
+
+/* Bytes of device scratch that kvq_allocate needs for this layout and s; 0
+ * if the arguments are invalid. */
+size_t kvq_workspace_bytes(kvq_layout L, int s);
+
+/*
+ * kvq_stats -- candidate alphabet and interval statistics of every block
+ * ("Implementation notes": build a candidate alphabet from the block's
+ * minimum, maximum and quantiles; compute D_r from interval statistics).
+ *   x       device, [S,T,D] binary16 (read once).
+ *   m       number of candidates; must be KVQ_CANDIDATES (17): the order
+ *           statistics at 0-based sorted ranks floor((j(d-1)+8)/16),
+ *           j = 0..16 (minimum and maximum included), equal values merged.
+ *   stats   device, kvq_stats_bytes(L) bytes, written: per block the merged
+ *           candidates and, for each gap between consecutive candidates, the
+ *           count and first moments of the entries in it.  Its layout is
+ *           private to this library; pass it to kvq_allocate unchanged.
+ *   status  device int32, set to KVQ_OK, or KVQ_ERR_NONFINITE if any entry is
+ *           NaN or infinite (the results of such blocks are unspecified).
+ */
+int kvq_stats(const uint16_t *x, kvq_layout L, int m, void *stats,
+              int32_t *status, void *stream);
+
+/*
+ * kvq_allocate -- per-block codebooks and the global lambda ("Mathematical
+ * statement": minimise sum_r D_r subject to sum_r d_r H_r <= B, |Q_r| <= s;
+ * with lambda the blocks decouple into argmin_Q D_r + lambda d_r H_r).
+ * Every block gets the exact minimiser over all subsets of its candidates
+ * that contain the minimum and the maximum and have 2 <= k <= s levels
+ * (k = 1 for a constant block).  Reads only `stats` (never x again).
+ *   s            2..16, maximum levels per block.
+ *   budget_bits  B, in bits, for the whole tensor (e.g. 2.5 * S*T*D); >= 0.
+ *   mode         KVQ_BISECT40: R(0) <= B gives lambda = 0; else
+ *                hi = max_r (c_max - c_min)^2, doubled (at most 30 times)
+ *                until R(hi) <= B, then 40 bisection steps on [0, hi];
+ *                lambda = the feasible end.  If R stays above B the
+ *                allocation at the last hi is returned and the status is
+ *                KVQ_ERR_INFEASIBLE.
+ *                KVQ_SUBGRADIENT ("Key formulas": lambda <- max{0, lambda +
+ *                eta (sum_r d_r H_r - B)}): the choice is made at the given
+ *                lambda; on return *lambda holds the updated value.
+ *   eta          step of KVQ_SUBGRADIENT (ignored by KVQ_BISECT40); >= 0.
+ *   lambda       device double; KVQ_SUBGRADIENT: in = lambda_t, out =
+ *                lambda_{t+1}; KVQ_BISECT40: out = lambda.
+ *   workspace    device, kvq_workspace_bytes(L, s) bytes of scratch.
+ *   codebook     device float [nblocks][16]: levels in increasing order,
+ *                slots k..15 repeat the largest level.
+ *   k            device uint8 [nblocks]: number of levels.
+ *   D_r          device float [nblocks]: expected squared error of the block.
+ *   H_r          device float [nblocks]: entropy (bits per entry) of the
+ *                expected codepoint frequencies.
+ *   totals       device double [3]: sum_r d_r H_r, sum_r D_r, and the lambda
+ *                the codebooks were chosen at.
+ *   status       device int32: KVQ_OK, KVQ_ERR_NONFINITE, KVQ_ERR_INFEASIBLE.
+ */
+int kvq_allocate(const void *stats, kvq_layout L, int s, double budget_bits,
+                 int mode, double eta, double *lambda, void *workspace,
+                 float *codebook, uint8_t *k, float *D_r, float *H_r,
+                 double *totals, int32_t *status, void *stream);
+
+/*
+ * kvq_quantize -- unbiased stochastic interpolation and 4-bit packing ("Key
+ * formulas": P(q_{i+1} | x) = (x - q_i)/(q_{i+1} - q_i)).  For entry x of
+ * block r with levels q_0 < ... < q_{k-1}: i = the largest index with
+ * q_i <= x, capped at k-2; u = hash(seed, index_base + flat index) >> 8; the
+ * code is i+1 iff fl(u 2^-24 * (q_{i+1} - q_i)) < fl(x - q_i) in fp32
+ * round-to-nearest (no fused multiply-add), else i; k = 1 gives code 0.
+ * hash(seed, n) is the SplitMix64 generator seeded with `seed`: output
+ * number n>>1, its high 32 bits for even n, low 32 bits for odd n.
+ *   x           device [S,T,D] binary16.
+ *   codebook, k as written by kvq_allocate.
+ *   seed        any 64-bit value.
+ *   index_base  even, and index_base + S*T*D <= 2^40.
+ *   codes       device uint8 [nblocks][16*group]: byte e/2 of block r holds
+ *               entry e in its low nibble (e even) or high nibble (e odd).
+ */
+int kvq_quantize(const uint16_t *x, kvq_layout L, const float *codebook,
+                 const uint8_t *k, uint64_t seed, uint64_t index_base,
+                 uint8_t *codes, void *stream);
+
+/*
+ * kvq_dequantize -- decode before attention ("Implementation notes"):
+ * y = codebook[r][code] written as binary16 (exact: every level is a
+ * binary16 value of the block).
+ *   codes, codebook  as above; y  device [S,T,D] binary16, written.
+ */
+int kvq_dequantize(const uint8_t *codes, const float *codebook, kvq_layout L,
+                   uint16_t *y, void *stream);
+
+/* Text of a status code. */
+const char *kvq_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

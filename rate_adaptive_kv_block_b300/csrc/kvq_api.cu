@@ -1,0 +1,130 @@
+// C ABI of libkvq (declared in include/kvq.h): argument validation on the
+// host, then stream-ordered launches.  Nothing here allocates memory.
+#include <math.h>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+int launch_stats(const uint16_t *x, const kvq_layout &L, void *stats, int32_t *status,
+                 cudaStream_t st);
+int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget, int mode,
+                    double eta, double *lambda, void *workspace, float *codebook, uint8_t *k,
+                    float *Dr, float *Hr, double *totals, int32_t *status, cudaStream_t st);
+int launch_quantize(const uint16_t *x, const kvq_layout &L, const float *codebook,
+                    const uint8_t *k, uint64_t seed, uint64_t index_base, uint8_t *codes,
+                    cudaStream_t st);
+int launch_dequantize(const uint8_t *codes, const float *codebook, const kvq_layout &L,
+                      uint16_t *y, cudaStream_t st);
+size_t workspace_bytes(int64_t nb, int s);
+int allocate_init();
+
+static bool layout_ok(const kvq_layout &L) {
+    if (L.S < 0 || L.T < 0 || L.T % 32 != 0) return false;
+    const int G = L.group;
+    if (!(G == 8 || G == 16 || G == 32 || G == 64 || G == 128)) return false;
+    if (L.D <= 0 || L.D % G != 0 || L.D / G > 32) return false;
+    // element count must fit comfortably in 64-bit index arithmetic
+    if (L.S > 0 && L.T > 0 && (double)L.S * (double)L.T * (double)L.D > 9.0e15) return false;
+    return true;
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Per-device one-time set-up (function attributes are per device).
+static int init_once() {
+    static int state[64];
+    static bool done[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return KVQ_ERR_CUDA;
+    if (dev >= 64) return allocate_init();
+    if (!done[dev]) {
+        state[dev] = allocate_init();
+        done[dev] = true;
+    }
+    return state[dev];
+}
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+int64_t kvq_num_blocks(kvq_layout L) { return layout_ok(L) ? num_blocks(L) : -1; }
+
+size_t kvq_stats_bytes(kvq_layout L) {
+    return layout_ok(L) ? (size_t)num_blocks(L) * sizeof(StatsRow) : 0;
+}
+
+size_t kvq_workspace_bytes(kvq_layout L, int s) {
+    if (!layout_ok(L) || s < 2 || s > kMaxLev) return 0;
+    return workspace_bytes(num_blocks(L), s);
+}
+
+int kvq_stats(const uint16_t *x, kvq_layout L, int m, void *stats, int32_t *status,
+              void *stream) {
+    if (!layout_ok(L) || m != kCand || !status) return KVQ_ERR_INVALID_ARG;
+    const int64_t nb = num_blocks(L);
+    if (nb > 0 && (!x || !stats || !aligned16(x) || !aligned16(stats))) return KVQ_ERR_INVALID_ARG;
+    if (nb > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
+    return launch_stats(x, L, stats, status, static_cast<cudaStream_t>(stream));
+}
+
+int kvq_allocate(const void *stats, kvq_layout L, int s, double budget_bits, int mode,
+                 double eta, double *lambda, void *workspace, float *codebook, uint8_t *k,
+                 float *D_r, float *H_r, double *totals, int32_t *status, void *stream) {
+    if (!layout_ok(L) || s < 2 || s > kMaxLev) return KVQ_ERR_INVALID_ARG;
+    if (!(budget_bits >= 0.0) || !isfinite(budget_bits)) return KVQ_ERR_INVALID_ARG;
+    if (mode != KVQ_BISECT40 && mode != KVQ_SUBGRADIENT) return KVQ_ERR_INVALID_ARG;
+    if (!(eta >= 0.0) || !isfinite(eta)) return KVQ_ERR_INVALID_ARG;
+    if (!lambda || !totals || !status) return KVQ_ERR_INVALID_ARG;
+    const int64_t nb = num_blocks(L);
+    if (nb > 0) {
+        if (!stats || !workspace || !codebook || !k || !D_r || !H_r) return KVQ_ERR_INVALID_ARG;
+        if (!aligned16(stats) || !aligned16(workspace) || !aligned16(codebook))
+            return KVQ_ERR_INVALID_ARG;
+        if (nb > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
+    }
+    if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
+    return launch_allocate(stats, L, s, budget_bits, mode, eta, lambda, workspace, codebook, k,
+                           D_r, H_r, totals, status, static_cast<cudaStream_t>(stream));
+}
+
+int kvq_quantize(const uint16_t *x, kvq_layout L, const float *codebook, const uint8_t *k,
+                 uint64_t seed, uint64_t index_base, uint8_t *codes, void *stream) {
+    if (!layout_ok(L)) return KVQ_ERR_INVALID_ARG;
+    if (index_base & 1u) return KVQ_ERR_INVALID_ARG;
+    const uint64_t n = (uint64_t)L.S * (uint64_t)L.T * (uint64_t)L.D;
+    if (index_base > (1ull << 40) || n > (1ull << 40) - index_base) return KVQ_ERR_INVALID_ARG;
+    if (n > 0) {
+        if (!x || !codebook || !k || !codes) return KVQ_ERR_INVALID_ARG;
+        if (!aligned16(x) || !aligned16(codebook) || !aligned16(codes)) return KVQ_ERR_INVALID_ARG;
+        if (L.S * (L.T / 32) > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
+    }
+    return launch_quantize(x, L, codebook, k, seed, index_base, codes,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int kvq_dequantize(const uint8_t *codes, const float *codebook, kvq_layout L, uint16_t *y,
+                   void *stream) {
+    if (!layout_ok(L)) return KVQ_ERR_INVALID_ARG;
+    const int64_t nb = num_blocks(L);
+    if (nb > 0) {
+        if (!codes || !codebook || !y) return KVQ_ERR_INVALID_ARG;
+        if (!aligned16(codes) || !aligned16(codebook) || !aligned16(y)) return KVQ_ERR_INVALID_ARG;
+        if (L.S * (L.T / 32) > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
+    }
+    return launch_dequantize(codes, codebook, L, y, static_cast<cudaStream_t>(stream));
+}
+
+const char *kvq_status_string(int status) {
+    switch (status) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_CUDA: return "CUDA launch error";
+    case KVQ_ERR_NONFINITE: return "non-finite input entry";
+    case KVQ_ERR_INFEASIBLE: return "budget infeasible";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

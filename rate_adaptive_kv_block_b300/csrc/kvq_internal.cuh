@@ -1,0 +1,121 @@
+// Internal definitions shared by the CUDA translation units of libkvq.
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kCand = 17;       // order-statistic candidates per block
+constexpr int kMaxLev = 16;     // levels per block (4-bit codes)
+constexpr int kPairs = 136;     // slot pairs j < l over 17 slots
+constexpr int kTriples = 680;   // slot triples i < j < l
+
+// ---------------------------------------------------------------- stats row
+// One row per block, written by kvq_stats, read by kvq_allocate.  Atom p
+// (p = 0 .. m'-2) holds the entries c_p <= x < c_{p+1} (the last atom also
+// the entries equal to the maximum): n, s1 = sum(x - c_p),
+// t1 = sum(c_{p+1} - x), e = sum((x - c_p)(c_{p+1} - x)).
+struct StatsRow {
+    float c[kCand];      // merged candidates, padded with the maximum
+    int32_t mprime;      // number of distinct candidates (1..17)
+    int32_t flags;       // bit 0: a non-finite entry
+    int32_t d;           // entries in the block
+    float n[16];
+    float s1[16];
+    float t1[16];
+    float e[16];
+    float pad[12];
+};
+static_assert(sizeof(StatsRow) == 384, "stats row is 384 bytes");
+constexpr int kFlagNonfinite = 1;
+
+// ------------------------------------------------------------- table layout
+// Per-block, lambda-independent DP tables, in "slot" space: the m'
+// candidates sit in slots 0 .. m'-2 and 16 (the maximum always in slot 16);
+// slots m'-1 .. 15 are unused ("dummy") when m' < 17.
+//   Dp(j,l)    expected squared error of entries in [q_j, q_l)  (+inf for
+//              a dummy slot)
+//   hh(i,j,l)  h(Mup(i,j) + Mdn(j,l)): entropy term of level j between
+//              levels i and l, h(M) = -M log2(M/d)
+//   h0(l)      h(Mdn(0,l)): term of the first level
+//   hend(i)    h(Mup(i,16)): term of the last level
+// Pair (j,l) is stored at pair_off(j) + l-j-1; triple (i,j,l) at
+// trip_off(i,j) + l-j-1, so the entries of one (i,j) are contiguous in l.
+__host__ __device__ constexpr int pair_off(int j) { return 16 * j - j * (j - 1) / 2; }
+__host__ __device__ constexpr int trip_base(int j) {
+    // sum_{j'=1}^{j-1} j' (16 - j')
+    return 16 * (j - 1) * j / 2 - (j - 1) * j * (2 * j - 1) / 6;
+}
+__host__ __device__ constexpr int trip_off(int i, int j) { return trip_base(j) + i * (16 - j); }
+static_assert(trip_base(16) == kTriples, "triple count");
+static_assert(pair_off(16) == kPairs, "pair count");
+
+constexpr int kTblD = 0;
+constexpr int kTblHH = kTblD + kPairs;        // 136
+constexpr int kTblH0 = kTblHH + kTriples;     // 816
+constexpr int kTblHend = kTblH0 + 17;         // 833
+constexpr int kTblC = kTblHend + 17;          // 850: level value per slot
+constexpr int kTblHdr = kTblC + 17;           // 867: m', d, flags (int bits)
+constexpr int kTblStride = 872;               // floats per block (3488 B)
+static_assert(kTblStride % 4 == 0, "16-byte rows");
+
+// ---------------------------------------------------- allocation control
+// Lives at the start of the kvq_allocate workspace.
+struct Ctrl {
+    double budget;          // B (bits)
+    double eta;             // subgradient step
+    double lo, hi;          // bisection interval
+    double lambda;          // lambda of the emitted choice
+    double R_hi;            // sum_r d_r H_r at hi (as the search summed it)
+    unsigned long long hi0_bits;   // max_r (c_max - c_min)^2 (double bits)
+    int32_t phase;          // kPhase*
+    int32_t step;           // bisection steps done
+    int32_t hi_probe;       // probe of the last round that is hi, or -1
+    int32_t status;
+    int32_t flags;          // OR of block flags
+    int32_t mode;
+    uint32_t ticket;        // last-CTA-done counter of the search rounds
+    uint32_t ticket_emit;   // same, emit kernel
+    int32_t pad[4];
+};
+constexpr int kPhaseBracket = 0;
+constexpr int kPhaseBisect = 1;
+constexpr int kPhaseDone = 2;
+constexpr int kPhaseFixed = 3;   // subgradient: one round at a given lambda
+constexpr int kProbes = 32;      // lambda values per search round (one per lane)
+constexpr int kBisectSteps = 40;
+constexpr int kLevelsPerRound = 5;   // 31 tree nodes = 5 bisection levels
+constexpr int kMaxDoublings = 30;
+
+// ------------------------------------------------------------ binary16 keys
+// Order-preserving 16-bit key of a binary16 value (-0 folded into +0):
+// negative values map below 0x8000, non-negative at or above it.
+__device__ __forceinline__ uint32_t f16_key(uint32_t h) {
+    h = (h == 0x8000u) ? 0u : h;
+    return (h & 0x8000u) ? (~h & 0xffffu) : (h | 0x8000u);
+}
+__device__ __forceinline__ uint32_t key_to_bits(uint32_t key) {
+    return (key & 0x8000u) ? (key & 0x7fffu) : (~key & 0xffffu);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __half2float(__ushort_as_half((unsigned short)key_to_bits(key)));
+}
+// spacing of consecutive keys inside the 256-key bin b (binary16 ulp there)
+__device__ __forceinline__ float bin_ulp(uint32_t b) {
+    uint32_t e = (key_to_bits(b << 8) >> 10) & 31u;
+    return e == 0 ? 5.9604644775390625e-8f : __int_as_float((int)((e - 25 + 127) << 23));
+}
+
+// -------------------------------------------------------------- block map
+struct BlockPos {
+    int64_t stream, tblock;
+    int group;
+};
+__host__ __device__ __forceinline__ int64_t num_blocks(const kvq_layout &L) {
+    return L.S * (L.T / 32) * (int64_t)(L.D / L.group);
+}
+
+}  // namespace kvq

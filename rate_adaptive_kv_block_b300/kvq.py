@@ -1,0 +1,177 @@
+"""Python binding of libkvq (include/kvq.h): argument marshalling only.
+
+Every function has the name of the C entry point it calls and takes torch
+tensors that live on the current CUDA device; it passes their data pointers,
+the layout and torch's current stream, and raises on a non-OK return code.
+All work happens in the CUDA kernels; there is no CPU fallback: if the
+library is missing or cannot be loaded the first call raises.
+"""
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import torch
+
+_LIB = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvq.so")
+_lib = None
+
+KVQ_OK = 0
+KVQ_ERR_INVALID_ARG = 1
+KVQ_ERR_CUDA = 2
+KVQ_ERR_NONFINITE = 3
+KVQ_ERR_INFEASIBLE = 4
+KVQ_BISECT40 = 0
+KVQ_SUBGRADIENT = 1
+STATS_ROW_BYTES = 384
+
+
+class _Layout(C.Structure):
+    _fields_ = [("S", C.c_int64), ("T", C.c_int64), ("D", C.c_int32), ("group", C.c_int32)]
+
+
+@dataclass(frozen=True)
+class Layout:
+    """[S, T, D] binary16 tensor cut into blocks of 32 tokens x `group`
+    features."""
+    S: int
+    T: int
+    D: int
+    group: int
+
+    def c(self):
+        return _Layout(self.S, self.T, self.D, self.group)
+
+    @property
+    def d(self) -> int:
+        return 32 * self.group
+
+    @property
+    def nblocks(self) -> int:
+        return self.S * (self.T // 32) * (self.D // self.group)
+
+
+class KvqError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _LIB
+
+
+def lib():
+    """Load libkvq.so (building it first if it is absent)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB):
+            from . import build as _b
+            _b.build()
+        L = C.CDLL(_LIB)
+        vp, i32, i64, u64, dbl = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_double
+        L.kvq_num_blocks.restype = i64
+        L.kvq_num_blocks.argtypes = [_Layout]
+        L.kvq_stats_bytes.restype = C.c_size_t
+        L.kvq_stats_bytes.argtypes = [_Layout]
+        L.kvq_workspace_bytes.restype = C.c_size_t
+        L.kvq_workspace_bytes.argtypes = [_Layout, C.c_int]
+        L.kvq_stats.restype = C.c_int
+        L.kvq_stats.argtypes = [vp, _Layout, C.c_int, vp, vp, vp]
+        L.kvq_allocate.restype = C.c_int
+        L.kvq_allocate.argtypes = [vp, _Layout, C.c_int, dbl, C.c_int, dbl, vp, vp, vp, vp,
+                                   vp, vp, vp, vp, vp]
+        L.kvq_quantize.restype = C.c_int
+        L.kvq_quantize.argtypes = [vp, _Layout, vp, vp, u64, u64, vp, vp]
+        L.kvq_dequantize.restype = C.c_int
+        L.kvq_dequantize.argtypes = [vp, vp, _Layout, vp, vp]
+        L.kvq_status_string.restype = C.c_char_p
+        L.kvq_status_string.argtypes = [C.c_int]
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != KVQ_OK:
+        raise KvqError("%s: %s" % (what, kvq_status_string(rc)))
+
+
+def kvq_status_string(status: int) -> str:
+    return lib().kvq_status_string(int(status)).decode()
+
+
+def kvq_num_blocks(L: Layout) -> int:
+    return lib().kvq_num_blocks(L.c())
+
+
+def kvq_stats_bytes(L: Layout) -> int:
+    return lib().kvq_stats_bytes(L.c())
+
+
+def kvq_workspace_bytes(L: Layout, s: int) -> int:
+    return lib().kvq_workspace_bytes(L.c(), int(s))
+
+
+def kvq_stats(x, L: Layout, stats, status, m: int = 17, stream=None):
+    _check(lib().kvq_stats(_ptr(x), L.c(), int(m), _ptr(stats), _ptr(status), _stream(stream)),
+           "kvq_stats")
+
+
+def kvq_allocate(stats, L: Layout, s: int, budget_bits: float, mode: int, eta: float, lam,
+                 workspace, codebook, k, D_r, H_r, totals, status, stream=None):
+    _check(lib().kvq_allocate(_ptr(stats), L.c(), int(s), float(budget_bits), int(mode),
+                              float(eta), _ptr(lam), _ptr(workspace), _ptr(codebook), _ptr(k),
+                              _ptr(D_r), _ptr(H_r), _ptr(totals), _ptr(status),
+                              _stream(stream)), "kvq_allocate")
+
+
+def kvq_quantize(x, L: Layout, codebook, k, seed: int, index_base: int, codes, stream=None):
+    _check(lib().kvq_quantize(_ptr(x), L.c(), _ptr(codebook), _ptr(k), int(seed),
+                              int(index_base), _ptr(codes), _stream(stream)), "kvq_quantize")
+
+
+def kvq_dequantize(codes, codebook, L: Layout, y, stream=None):
+    _check(lib().kvq_dequantize(_ptr(codes), _ptr(codebook), L.c(), _ptr(y), _stream(stream)),
+           "kvq_dequantize")
+
+
+class Buffers:
+    """Device buffers of one quantization of a layout (torch allocations)."""
+
+    def __init__(self, L: Layout, s: int, device="cuda"):
+        nb = L.nblocks
+        dev = torch.device(device)
+        self.L, self.s = L, s
+        self.stats = torch.empty(kvq_stats_bytes(L), dtype=torch.uint8, device=dev)
+        self.workspace = torch.empty(max(kvq_workspace_bytes(L, s), 16), dtype=torch.uint8,
+                                     device=dev)
+        self.codebook = torch.empty((nb, 16), dtype=torch.float32, device=dev)
+        self.k = torch.empty(nb, dtype=torch.uint8, device=dev)
+        self.D_r = torch.empty(nb, dtype=torch.float32, device=dev)
+        self.H_r = torch.empty(nb, dtype=torch.float32, device=dev)
+        self.totals = torch.zeros(3, dtype=torch.float64, device=dev)
+        self.lam = torch.zeros(1, dtype=torch.float64, device=dev)
+        self.status_stats = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.codes = torch.empty((nb, 16 * L.group), dtype=torch.uint8, device=dev)
+
+
+def quantize(x, L: Layout, budget_bits: float, s: int, seed: int = 0, index_base: int = 0,
+             mode: int = KVQ_BISECT40, eta: float = 0.0, buf: Buffers = None, stream=None):
+    """kvq_stats + kvq_allocate + kvq_quantize on x (a [S,T,D] float16 CUDA
+    tensor).  Returns the Buffers (codes, codebook, k, D_r, H_r, totals,
+    lambda, statuses), all still on the device."""
+    if buf is None:
+        buf = Buffers(L, s, x.device)
+    kvq_stats(x, L, buf.stats, buf.status_stats, stream=stream)
+    kvq_allocate(buf.stats, L, s, budget_bits, mode, eta, buf.lam, buf.workspace, buf.codebook,
+                 buf.k, buf.D_r, buf.H_r, buf.totals, buf.status, stream=stream)
+    kvq_quantize(x, L, buf.codebook, buf.k, seed, index_base, buf.codes, stream=stream)
+    return buf

@@ -1,0 +1,78 @@
+"""The C-ABI library loads, exports every entry point include/kvq.h declares,
+and rejects bad arguments on the host before touching the GPU (no compute
+call runs here)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from rate_adaptive_kv_block_b300 import build as kbuild
+from rate_adaptive_kv_block_b300 import kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z_]+)\s*\(", src)))
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    path = kbuild.build()
+    lib = C.CDLL(path)
+    names = declared_functions()
+    assert {"kvq_stats", "kvq_allocate", "kvq_quantize", "kvq_dequantize"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_sizes_and_layout_validation():
+    L = kvq.Layout(16, 8192, 128, 128)
+    assert kvq.kvq_num_blocks(L) == 4096
+    assert kvq.kvq_stats_bytes(L) == 4096 * 384
+    assert kvq.kvq_workspace_bytes(L, 16) > 4096 * 872 * 4
+    assert kvq.kvq_workspace_bytes(L, 1) == 0 and kvq.kvq_workspace_bytes(L, 17) == 0
+    assert kvq.kvq_num_blocks(kvq.Layout(16, 8200, 128, 128)) == -1      # T % 32
+    assert kvq.kvq_num_blocks(kvq.Layout(16, 8192, 128, 48)) == -1       # group
+    assert kvq.kvq_num_blocks(kvq.Layout(16, 8192, 96, 64)) == -1        # D % group
+    assert kvq.kvq_num_blocks(kvq.Layout(1, 32, 8 * 33, 8)) == -1        # > 32 groups
+    assert kvq.kvq_num_blocks(kvq.Layout(0, 32, 128, 32)) == 0
+    assert kvq.kvq_status_string(3) == "non-finite input entry"
+
+
+class _Fake:
+    """Stands in for a device tensor: only data_ptr() is used by the binding."""
+    def __init__(self, p):
+        self.p = p
+
+    def data_ptr(self):
+        return self.p
+
+
+class _Stream:
+    cuda_stream = 0
+
+
+def test_host_validation_rejects_bad_arguments():
+    L = kvq.Layout(2, 64, 128, 128)
+    p, odd = _Fake(1 << 20), _Fake((1 << 20) + 8)
+    s = _Stream()
+    bad = kvq.KVQ_ERR_INVALID_ARG
+    lib = kvq.lib()
+    st = kvq._stream
+    assert lib.kvq_stats(C.c_void_p(p.p), L.c(), 16, C.c_void_p(p.p), C.c_void_p(p.p), st(s)) == bad
+    assert lib.kvq_stats(C.c_void_p(odd.p), L.c(), 17, C.c_void_p(p.p), C.c_void_p(p.p), st(s)) == bad
+    assert lib.kvq_stats(C.c_void_p(p.p), L.c(), 17, C.c_void_p(p.p), None, st(s)) == bad
+    args = [C.c_void_p(p.p)] * 9
+    for s_, B, mode, eta in [(1, 1.0, 0, 0.0), (17, 1.0, 0, 0.0), (8, -1.0, 0, 0.0),
+                             (8, float("nan"), 0, 0.0), (8, 1.0, 2, 0.0), (8, 1.0, 1, -1.0)]:
+        assert lib.kvq_allocate(C.c_void_p(p.p), L.c(), s_, B, mode, eta, *args, st(s)) == bad
+    assert lib.kvq_quantize(C.c_void_p(p.p), L.c(), C.c_void_p(p.p), C.c_void_p(p.p), 0, 1,
+                            C.c_void_p(p.p), st(s)) == bad                     # odd base
+    assert lib.kvq_quantize(C.c_void_p(p.p), L.c(), C.c_void_p(p.p), C.c_void_p(p.p), 0,
+                            (1 << 40) - 1000, C.c_void_p(p.p), st(s)) == bad   # 2^40 cap
+    assert lib.kvq_dequantize(None, C.c_void_p(p.p), L.c(), C.c_void_p(p.p), st(s)) == bad
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_stats(p, L, p, p, m=16, stream=s)

@@ -1,0 +1,227 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Inputs are the seeded synthetic workloads of rate_adaptive_kv_block_b300.synth
+at sizes the oracle finishes in seconds (several thousand blocks, both block
+shapes, s < 16 and s = 16), the bench workload at its full size, and the
+multi-GB workloads at full size on sampled 32-token slabs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gpu_common as gc
+from rate_adaptive_kv_block_b300 import kvq, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+# ------------------------------------------------------------------ stats
+
+EDGE_BLOCKS = {
+    "constant": lambda r: np.full((32, 128), 0.75),
+    "two_values": lambda r: np.where(r.random((32, 128)) < 0.3, -1.0, 2.0),
+    "ties": lambda r: np.round(r.standard_normal((32, 128)) * 4) / 4,
+    "signed_zero": lambda r: np.where(r.random((32, 128)) < 0.5, -0.0, 0.0) + (r.random((32, 128)) < 0.1) * r.standard_normal((32, 128)),
+    "subnormal": lambda r: r.standard_normal((32, 128)) * 1e-6,
+    "huge": lambda r: np.clip(r.standard_normal((32, 128)) * 3e4, -65504, 65504),
+    "negative": lambda r: -np.abs(r.standard_normal((32, 128))) - 1,
+    "one_outlier": lambda r: np.where(np.arange(32 * 128).reshape(32, 128) == 77, 1000.0, r.standard_normal((32, 128)) * 0.01),
+}
+
+
+def _edge_tensor():
+    r = np.random.default_rng(5)
+    blocks = [f(r) for f in EDGE_BLOCKS.values()]
+    x = np.stack(blocks).astype(np.float16)          # [nb, 32, 128]: one block each
+    return x.view(np.uint16)
+
+
+@pytest.mark.parametrize("name,T,S", [("k_head_small", None, None),
+                                      ("llama3_8b_layer", 1024, None),
+                                      ("hadamard_groups", 512, None)])
+def test_stats_matches_oracle(name, T, S):
+    _need_gpu()
+    w = synth.workload(name, T=T, S=S)
+    x = synth.make_numpy(w, seed=1)
+    g = gc.run(x, w.G, w.s, w.budgets[0] * x.size)
+    gc.check_stats(g, oracle.stats(x, w.G))
+    assert g["status_stats"] == 0
+
+
+def test_stats_edge_blocks():
+    _need_gpu()
+    x = _edge_tensor()
+    g = gc.run(x, 128, 16, 2.0 * x.size)
+    ora = oracle.stats(x, 128)
+    gc.check_stats(g, ora)
+    assert ora["mprime"][0] == 1 and ora["mprime"][1] == 2
+
+
+# --------------------------------------------------- quantize / dequantize
+
+@pytest.mark.parametrize("name,T,G", [("llama3_8b_layer", 512, 128), ("hadamard_groups", 256, 32)])
+def test_quantize_bit_exact_with_given_codebooks(name, T, G):
+    _need_gpu()
+    w = synth.workload(name, T=T)
+    x = synth.make_numpy(w, seed=2)
+    lam = 0.03
+    at = oracle.allocate_at(x, G, 16, lam)
+    L = kvq.Layout(*x.shape, G)
+    xd = gc.to_dev(x)
+    cb = torch.from_numpy(at["codebook"]).cuda()
+    kk = torch.from_numpy(at["k"]).cuda()
+    codes = torch.empty((L.nblocks, 16 * G), dtype=torch.uint8, device="cuda")
+    for seed, base in [(0, 0), (12345, 2), (2**63 + 7, 2**39)]:
+        kvq.kvq_quantize(xd, L, cb, kk, seed, base, codes)
+        ref = oracle.quantize(x, G, at["codebook"], at["k"], seed, base)
+        assert np.array_equal(codes.cpu().numpy(), ref)
+    y = torch.empty_like(xd)
+    kvq.kvq_dequantize(codes, cb, L, y)
+    ref_y = oracle.dequantize(codes.cpu().numpy(), at["codebook"], x.shape, G)
+    assert np.array_equal(gc.to_np(y), ref_y)
+
+
+# ------------------------------------------------------------ allocation
+
+ALLOC_CASES = [
+    # name, T override, S override, s, budget index
+    ("k_head_small", None, None, 8, 0),          # s < 16: general DP path
+    ("llama3_8b_layer", None, None, 16, 0),      # the benchmark workload, full size
+    ("full_model_cache", 2048, 32, 16, 0),
+    ("decode_admission", None, 2048, 16, 0),
+    ("hadamard_groups", 1024, None, 16, 0),
+    ("hadamard_groups", 1024, None, 16, 1),
+    ("hadamard_groups", 1024, None, 16, 2),
+    ("hadamard_groups", 1024, None, 16, 3),
+]
+
+
+@pytest.mark.parametrize("name,T,S,s,bi", ALLOC_CASES)
+def test_allocate_and_quantize_match_oracle(name, T, S, s, bi):
+    _need_gpu()
+    w = synth.workload(name, T=T, S=S)
+    x = synth.make_numpy(w, seed=0)
+    B = w.budgets[bi] * x.size
+    g = gc.run(x, w.G, s, B, seed=7, index_base=1 << 20)
+    assert g["status"] == 0 and g["status_stats"] == 0
+    ob = oracle.allocate_bisect(x, w.G, s, B)
+    lam_o, lam_g = ob["lambda"], g["lambda"]
+    assert abs(lam_g - lam_o) <= gc.LAM_REL * abs(lam_o), (lam_g, lam_o)
+    assert g["totals"][2] == lam_g
+    assert g["totals"][0] <= B
+    at, nontie = gc.check_choice(g, x, w.G, s, lam_g)
+    assert nontie.mean() > 0.9
+    assert g["totals"][0] == pytest.approx(at["totals"][0], rel=1e-4)
+    assert g["totals"][1] == pytest.approx(at["totals"][1], rel=1e-4)
+    gc.check_codes(g, x, w.G, 7, 1 << 20)
+    assert np.array_equal(g["y"], oracle.dequantize(g["codes"], g["codebook"], x.shape, w.G))
+
+
+def test_budget_large_gives_lambda_zero_and_s_levels():
+    _need_gpu()
+    w = synth.workload("k_head_small", T=64)
+    x = synth.make_numpy(w, seed=3)
+    g = gc.run(x, w.G, 6, 16.0 * x.size)
+    assert g["lambda"] == 0.0 and g["status"] == 0
+    assert np.all(g["k"] == 6)
+    gc.check_choice(g, x, w.G, 6, 0.0)
+
+
+def test_infeasible_and_nonfinite_status():
+    _need_gpu()
+    w = synth.workload("k_head_small", T=64)
+    x = synth.make_numpy(w, seed=4)
+    g = gc.run(x, w.G, 8, 0.0)
+    assert g["status"] == kvq.KVQ_ERR_INFEASIBLE
+    ob = oracle.allocate_bisect(x, w.G, 8, 0.0)
+    assert ob["status"] == 4 and g["lambda"] == pytest.approx(ob["lambda"], rel=1e-12)
+    xb = x.copy()
+    xb[1, 40, 3] = 0x7C00                  # +inf
+    g = gc.run(xb, w.G, 8, 3.0 * x.size)
+    assert g["status_stats"] == kvq.KVQ_ERR_NONFINITE
+    assert g["status"] == kvq.KVQ_ERR_NONFINITE
+
+
+def test_empty_layout():
+    _need_gpu()
+    L = kvq.Layout(0, 64, 128, 128)
+    buf = kvq.Buffers(L, 16)
+    x = torch.empty((0, 64, 128), dtype=torch.float16, device="cuda")
+    buf.status.fill_(9)
+    kvq.quantize(x, L, 100.0, 16, buf=buf)
+    torch.cuda.synchronize()
+    assert int(buf.status.item()) == 0 and float(buf.totals[0].item()) == 0.0
+
+
+# ---------------------------------------------- decode-time subgradient lambda
+
+def test_subgradient_steps_match_one_step_map():
+    _need_gpu()
+    w = synth.workload("decode_admission", S=1024)
+    B = w.budgets[0] * w.entries
+    x0 = synth.make_numpy(w, seed=100)
+    g = gc.run(x0, w.G, 16, B)                          # step 0: bisection warm start
+    lam = g["lambda"]
+    for t in range(1, 4):
+        x = synth.make_numpy(w, seed=100 + t)
+        g = gc.run(x, w.G, 16, B, seed=t, mode=kvq.KVQ_SUBGRADIENT, eta=w.eta, lam0=lam)
+        assert g["status"] == 0
+        assert g["totals"][2] == lam                      # chosen at lambda_t
+        at, nontie = gc.check_choice(g, x, w.G, 16, lam)
+        R = g["totals"][0]
+        assert R == pytest.approx(at["totals"][0], rel=1e-4)
+        assert g["lambda"] == max(0.0, lam + w.eta * (R - B))
+        o = oracle.allocate_at(x, w.G, 16, lam, w.eta, B)
+        assert g["lambda"] == pytest.approx(o["lambda_next"], rel=1e-4, abs=w.eta * 1e-4 * B)
+        gc.check_codes(g, x, w.G, t, 0)
+        lam = g["lambda"]
+
+
+# ------------------------------------------------ full sizes, sampled slabs
+
+FULL = [("full_model_cache", 0), ("decode_admission", 0), ("hadamard_groups", 0),
+        ("hadamard_groups", 3)]
+
+
+@pytest.mark.parametrize("name,bi", FULL)
+def test_full_size_sampled_slabs(name, bi):
+    _need_gpu()
+    w = synth.workload(name)
+    xd = synth.make_torch(w, seed=0)
+    B = w.budgets[bi] * w.entries
+    g_buf = kvq.Buffers(kvq.Layout(w.S, w.T, w.D, w.G), w.s)
+    L = g_buf.L
+    kvq.quantize(xd, L, B, w.s, seed=11, index_base=0, buf=g_buf)
+    torch.cuda.synchronize()
+    assert int(g_buf.status.item()) == 0
+    tot = g_buf.totals.cpu().numpy()
+    assert tot[0] <= B
+    lam = float(g_buf.lam.item())
+    rng = np.random.default_rng(1)
+    nTB, nG = w.T // 32, w.D // w.G
+    slabs = rng.choice(w.S * nTB, size=6, replace=False)
+    rows = g_buf.stats.view(torch.float32).view(-1, 96)
+    for sl in slabs:
+        h, tb = divmod(int(sl), nTB)
+        xs = gc.to_np(xd[h, 32 * tb:32 * tb + 32, :].unsqueeze(0))
+        gid = np.arange(nG) + int(sl) * nG
+        gidt = torch.from_numpy(gid).cuda()
+        r = rows[gidt].cpu().numpy()
+        g = {
+            "cand": r[:, :17].astype(np.float64), "mprime": r[:, 17].view(np.int32).copy(),
+            "flags": r[:, 18].view(np.int32).copy(),
+            "atoms": np.stack([r[:, 20:36], r[:, 36:52], r[:, 52:68], r[:, 68:84]], axis=-1).astype(np.float64),
+            "codebook": g_buf.codebook[gidt].cpu().numpy(), "k": g_buf.k[gidt].cpu().numpy(),
+            "D_r": g_buf.D_r[gidt].cpu().numpy().astype(np.float64),
+            "H_r": g_buf.H_r[gidt].cpu().numpy().astype(np.float64),
+            "codes": g_buf.codes[gidt].cpu().numpy(),
+        }
+        gc.check_stats(g, oracle.stats(xs, w.G))
+        gc.check_choice(g, xs, w.G, w.s, lam)
+        gc.check_codes(g, xs, w.G, 11, (h * w.T + 32 * tb) * w.D)
