@@ -6,8 +6,9 @@ One step = kvq_stats + kvq_allocate (40-step lambda bisection) + kvq_quantize
 over one [S, T, D] binary16 K/V tensor already resident in HBM: the
 Llama-3-8B-shaped single-layer prefill (K and V, 8 KV heads each, 8192
 tokens, head dim 128; blocks of one head x 32 tokens; s = 16; B = 2.5 bits per
-entry).  L2 is flushed (a 256 MB write) before every timed step, outside the
-timed interval.  The metric is binary16 input bytes quantized per second.
+entry).  L2 is flushed before every timed step, outside the timed interval
+(a 256 MB write, then a 256 MB read so the write's dirty lines are written
+back before timing starts).  The metric is binary16 input bytes quantized per second.
 
 Also reported on the same line: per-kernel times, the roofline of the dominant
 kernel (algorithmic bytes / measured time / measured HBM peak), an end-to-end
@@ -30,7 +31,6 @@ import os
 import statistics
 import subprocess
 import sys
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -66,28 +66,34 @@ class ClockSampler:
         self.lines = []
 
     def __enter__(self):
+        import tempfile
+        self.path = tempfile.mktemp(prefix="kvq_clocks_", suffix=".csv")
         try:
+            # nvidia-smi writes each sample line itself (-f), so nothing is
+            # lost in a pipe buffer when it is stopped
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
         except OSError:
             self.proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *a):
         if self.proc is not None:
+            time.sleep(0.15)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            try:
+                with open(self.path) as f:
+                    self.lines = [ln.strip() for ln in f if ln.strip()]
+                os.unlink(self.path)
+            except OSError:
+                pass
 
     def summary(self):
         sm, mx, reasons = [], None, set()
@@ -206,6 +212,14 @@ def main():
     s = w.s
     buf = kvq.Buffers(L, s, dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def flush_l2(i):
+        # write 256 MB (evicts the input), then read 256 MB so the dirty lines
+        # of the write are written back before the timed interval starts
+        flush.fill_(i & 0xff)
+        torch.sum(flush_r, dim=0, keepdim=True, out=sink)
     stream = torch.cuda.current_stream()
     in_bytes = x.numel() * 2
     nb = L.nblocks
@@ -225,7 +239,7 @@ def main():
             ev[3].record(stream)
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush_l2(0)
         step()
     torch.cuda.synchronize()
     st = int(buf.status.item())
@@ -238,7 +252,7 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
-            flush.fill_(i & 0xff)
+            flush_l2(i)
             step(evs[i])
         torch.cuda.synchronize()
     t_stats = [e[0].elapsed_time(e[1]) for e in evs]
@@ -255,13 +269,13 @@ def main():
     # quantize alone with a cold L2 (the gated kernel), same launch configuration
     qe = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.fill_(i & 0xff)
+        flush_l2(i)
         qe[i][0].record(stream)
         kvq.kvq_quantize(x, L, buf.codebook, buf.k, 0, 0, buf.codes)
         qe[i][1].record(stream)
     se = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.fill_(i & 0xff)
+        flush_l2(i)
         se[i][0].record(stream)
         kvq.kvq_stats(x, L, buf.stats, buf.status_stats)
         se[i][1].record(stream)
@@ -295,7 +309,7 @@ def main():
     torch.cuda.synchronize()
     ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.fill_(i & 0xff)
+        flush_l2(i)
         ee[i][0].record(stream)
         e2e_step()
         ee[i][1].record(stream)
@@ -349,7 +363,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "l2": "flushed (256 MB write) before each step",
+            "config": {"workload": WORKLOAD_DESC, "l2": "flushed before each step (256 MB write then 256 MB read, outside the timed interval)",
                        "parallelism": "replicas" if world > 1 else "single"},
             "tokens_per_s": world * args.steps * w.T / (tot_ms * 1e-3),
             "lambda": float(buf.lam.item()), "rate_bits_per_entry": float(buf.totals[0].item()) / w.entries,

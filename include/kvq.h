@@ -62,7 +62,7 @@ extern "C" {
  * (stream, token block, feature group); inside a block entry e is
  * (token - 32 * token_block) * group + (feature - group_index * group).
  * Requirements: S >= 0, T >= 0 and T % 32 == 0, group in {8,16,32,64,128},
- * D % group == 0, D / group <= 32.
+ * D a power of two <= 2048, D % group == 0, D / group <= 32.
  */
 typedef struct kvq_layout {
     int64_t S;

@@ -43,34 +43,30 @@ constexpr int kEmitThreads = 256;
 struct Workspace {
     Ctrl *ctrl;
     float *tables;        // [nblk][kTblStride]
-    float *rates;         // [nblk][32]
-    uint32_t *masks;      // [nblk][32]
-    float *rate_hi;       // [nblk]
-    uint32_t *mask_hi;    // [nblk]
-    double *partial;      // [max CTAs][32]
+    float *rates;         // [nblk][32]   d_r H_r per probe (last round)
+    uint32_t *masks;      // [nblk][32]   chain per probe (last round)
+    float *rate_lo;       // [nblk]       d_r H_r at lo
+    float *rate_hi;       // [nblk]       d_r H_r at hi
+    uint32_t *mask_hi;    // [nblk]       chain at hi
+    uint8_t *act;         // [nblk]       evaluated in the last round
     double *epartial;     // [emit CTAs][2]
 };
 
 static size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 
-static size_t round_ctas(int64_t nb, int s) {
-    const int w = s >= 16 ? kRoundWarps : kRoundWarpsGen;
-    return (size_t)((nb + w - 1) / w);
-}
-
 size_t workspace_bytes(int64_t nb, int s) {
+    (void)s;
     size_t b = align_up(sizeof(Ctrl));
     b += align_up((size_t)nb * kTblStride * sizeof(float));
     b += align_up((size_t)nb * 32 * sizeof(float));
     b += align_up((size_t)nb * 32 * sizeof(uint32_t));
-    b += align_up((size_t)nb * sizeof(float));
-    b += align_up((size_t)nb * sizeof(uint32_t));
-    b += align_up(round_ctas(nb, s) * 32 * sizeof(double));
+    b += 3 * align_up((size_t)nb * sizeof(float));
+    b += align_up((size_t)nb);
     b += align_up((size_t)((nb + kEmitThreads - 1) / kEmitThreads) * 2 * sizeof(double));
     return b;
 }
 
-static Workspace carve(void *base, int64_t nb, int s) {
+static Workspace carve(void *base, int64_t nb) {
     char *p = static_cast<char *>(base);
     Workspace w;
     w.ctrl = reinterpret_cast<Ctrl *>(p);
@@ -81,12 +77,14 @@ static Workspace carve(void *base, int64_t nb, int s) {
     p += align_up((size_t)nb * 32 * sizeof(float));
     w.masks = reinterpret_cast<uint32_t *>(p);
     p += align_up((size_t)nb * 32 * sizeof(uint32_t));
+    w.rate_lo = reinterpret_cast<float *>(p);
+    p += align_up((size_t)nb * sizeof(float));
     w.rate_hi = reinterpret_cast<float *>(p);
     p += align_up((size_t)nb * sizeof(float));
     w.mask_hi = reinterpret_cast<uint32_t *>(p);
     p += align_up((size_t)nb * sizeof(uint32_t));
-    w.partial = reinterpret_cast<double *>(p);
-    p += align_up(round_ctas(nb, s) * 32 * sizeof(double));
+    w.act = reinterpret_cast<uint8_t *>(p);
+    p += align_up((size_t)nb);
     w.epartial = reinterpret_cast<double *>(p);
     return w;
 }
@@ -105,6 +103,8 @@ __global__ void ctrl_init_kernel(Ctrl *c, double budget, double eta, int mode,
     c->phase = (mode == KVQ_SUBGRADIENT) ? kPhaseFixed : kPhaseBracket;
     c->step = 0;
     c->hi_probe = -1;
+    c->lo_probe = -1;
+    for (int i = 0; i < 32; ++i) c->acc[i] = 0ull;
     c->status = KVQ_OK;
     c->flags = 0;
     c->mode = mode;
@@ -113,6 +113,29 @@ __global__ void ctrl_init_kernel(Ctrl *c, double budget, double eta, int mode,
 }
 
 // -------------------------------------------------------------------- tables
+// Decode of a padded hh entry: (i, j, l) packed as i | j << 8 | l << 16
+// (l = 17 marks padding), and of a padded Dp entry: j | l << 8.
+struct DecodeTables {
+    uint32_t trip[kHHFloats];
+    uint32_t pair[kDpFloats];
+};
+constexpr DecodeTables make_decode() {
+    DecodeTables t{};
+    for (int j = 1; j < 16; ++j)
+        for (int i = 0; i < j; ++i)
+            for (int k = 0; k < pad4(16 - j); ++k) {
+                const int l = j + 1 + k;
+                t.trip[trip_off(i, j) + k] = (uint32_t)i | ((uint32_t)j << 8) | ((uint32_t)(l < 17 ? l : 17) << 16);
+            }
+    for (int j = 0; j < 16; ++j)
+        for (int k = 0; k < pad4(16 - j); ++k) {
+            const int l = j + 1 + k;
+            t.pair[dp_off(j) + k] = (uint32_t)j | ((uint32_t)(l < 17 ? l : 17) << 8);
+        }
+    return t;
+}
+__device__ constexpr DecodeTables kDecode = make_decode();
+
 __device__ __forceinline__ float hterm(float M, float inv_d) {
     // entropy term of a level with expected count M out of d: -M log2(M/d)
     return M > 0.f ? -M * log2f(M * inv_d) : 0.f;
@@ -163,7 +186,7 @@ tables_kernel(const StatsRow *__restrict__ stats, int64_t nb, float *__restrict_
         }
         const float W = bq - a;
         const int sj = slot_of(P), sl = slot_of(Q);
-        const int o = pair_off(sj) + sl - sj - 1;
+        const int o = pidx(sj, sl);
         sDp[w][o] = Dv;
         sUp[w][o] = Us / W;
         sDn[w][o] = Ls / W;
@@ -171,23 +194,26 @@ tables_kernel(const StatsRow *__restrict__ stats, int64_t nb, float *__restrict_
     __syncwarp();
     float *tb = tables + b * kTblStride;
     auto real = [&](int t) { return t < mp - 1 || t == 16; };
-    for (int i = lane; i < kPairs; i += 32) tb[kTblD + i] = sDp[w][i];
-    // triples (slot space)
-    for (int idx = lane; idx < kTriples; idx += 32) {
-        int j = 1;
-        while (idx >= trip_base(j + 1)) ++j;
-        const int r = idx - trip_base(j);
-        const int i = r / (16 - j), l = j + 1 + r % (16 - j);
+    // Dp rows, padded
+    for (int idx = lane; idx < kDpFloats; idx += 32) {
+        const uint32_t dc = kDecode.pair[idx];
+        const int j = dc & 255, l = dc >> 8;
+        tb[kTblD + idx] = l < 17 ? sDp[w][pidx(j, l)] : INF;
+    }
+    // hh rows (slot space), padded
+    for (int idx = lane; idx < kHHFloats; idx += 32) {
+        const uint32_t dc = kDecode.trip[idx];
+        const int i = dc & 255, j = (dc >> 8) & 255, l = dc >> 16;
         float v = 0.f;
-        if (mp > 1 && real(i) && real(j) && real(l))
-            v = hterm(sUp[w][pair_off(i) + j - i - 1] + sDn[w][pair_off(j) + l - j - 1], inv_d);
+        if (l < 17 && mp > 1 && real(i) && real(j) && real(l))
+            v = hterm(sUp[w][pidx(i, j)] + sDn[w][pidx(j, l)], inv_d);
         tb[kTblHH + idx] = v;
     }
-    if (lane < 17) {
+    if (lane < 20) {
         const int t = lane;
         float h0 = 0.f, he = 0.f;
-        if (mp > 1 && t >= 1 && real(t)) h0 = hterm(sDn[w][pair_off(0) + t - 1], inv_d);
-        if (mp > 1 && t <= 15 && real(t)) he = hterm(sUp[w][pair_off(t) + 16 - t - 1], inv_d);
+        if (mp > 1 && t >= 1 && t < 17 && real(t)) h0 = hterm(sDn[w][pidx(0, t)], inv_d);
+        if (mp > 1 && t <= 15 && real(t)) he = hterm(sUp[w][pidx(t, 16)], inv_d);
         tb[kTblH0 + t] = h0;
         tb[kTblHend + t] = he;
         float cv = 0.f;
@@ -200,8 +226,7 @@ tables_kernel(const StatsRow *__restrict__ stats, int64_t nb, float *__restrict_
         tb[kTblHdr + 0] = __int_as_float(mp);
         tb[kTblHdr + 1] = __int_as_float(d);
         tb[kTblHdr + 2] = __int_as_float(flags);
-        tb[kTblHdr + 3] = 0.f;
-        tb[kTblHdr + 4] = 0.f;
+        tb[kTblHdr + 3] = 0.f;   // the row ends at kTblHdr + 3
         const double wd = (double)row[mp - 1] - (double)row[0];
         const double w2 = wd * wd;
         if (w2 == w2) atomicMax(&ctrl->hi0_bits, (unsigned long long)__double_as_longlong(w2));
@@ -237,56 +262,113 @@ __device__ __forceinline__ double probe_lambda(const Ctrl &c, double hi0, int la
 // State value G(j,l): distortion of the intervals up to (j,l) plus lambda
 // times the entropy terms of the levels before l.  Lane-private state in
 // shared memory, [pair][lane].  Returns the chain's d_r H_r and its mask.
+__device__ __forceinline__ float hh_at(const float *tb, int i, int j, int l) {
+    return tb[kTblHH + trip_off(i, j) + l - j - 1];
+}
+__device__ __forceinline__ float dp_at(const float *tb, int j, int l) {
+    return tb[kTblD + dp_off(j) + l - j - 1];
+}
+
+// One stage of the forward pass: all states (j, l), l = j+1 .. 16, from the
+// states (i, j) of the earlier stages (compile-time j, so every index is an
+// immediate and the accumulators stay in registers).
+template <int J>
+__device__ __forceinline__ void dp_a_stage(const float *__restrict__ tb, float lam,
+                                           float *__restrict__ sG1, float *__restrict__ sG0,
+                                           int lane) {
+    constexpr int n = 16 - J;          // targets l = J+1 .. 16
+    constexpr int nq = (n + 3) / 4;
+    const float INF = __int_as_float(0x7f800000);
+    float acc[n];
+    float acc0 = INF;
+    {
+        const float g0 = sG0[J * 32 + lane];
+        const float4 *h4 = reinterpret_cast<const float4 *>(tb + kTblHH + trip_off(J - 1, J));
+#pragma unroll
+        for (int q = 0; q < nq; ++q) {
+            const float4 h = h4[q];
+            const float hs[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * q + r;
+                if (t < n) {
+                    if (t == 0) acc0 = fmaf(lam, hs[r], g0);
+                    else acc[t] = fmaf(lam, hs[r], g0);
+                }
+            }
+        }
+        acc[0] = INF;
+    }
+#pragma unroll
+    for (int i = 0; i < J; ++i) {
+        const float g = sG1[pidx(i, J) * 32 + lane];
+        const float4 *h4 = reinterpret_cast<const float4 *>(tb + kTblHH + trip_off(i, J));
+#pragma unroll
+        for (int q = 0; q < nq; ++q) {
+            const float4 h = h4[q];
+            const float hs[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * q + r;
+                if (t < n) acc[t] = fminf(acc[t], fmaf(lam, hs[r], g));
+            }
+        }
+    }
+    const float4 *d4 = reinterpret_cast<const float4 *>(tb + kTblD + dp_off(J));
+#pragma unroll
+    for (int q = 0; q < nq; ++q) {
+        const float4 dd = d4[q];
+        const float ds[4] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int t = 4 * q + r;
+            if (t < n) {
+                if (t == 0) sG0[(J + 1) * 32 + lane] = acc0 + ds[r];
+                sG1[pidx(J, J + 1 + t) * 32 + lane] = acc[t] + ds[r];
+            }
+        }
+    }
+    if constexpr (J < 15) dp_a_stage<J + 1>(tb, lam, sG1, sG0, lane);
+}
+
 __device__ __forceinline__ void dp_path_a(const float *__restrict__ tb, float lam, int C,
                                           float *__restrict__ sG1, float *__restrict__ sG0,
                                           int lane, float &rate, uint32_t &mask) {
     const float INF = __int_as_float(0x7f800000);
-#define G1(p) sG1[(p) * 32 + lane]
+#define G1(j, l) sG1[pidx(j, l) * 32 + lane]
 #define G0(j) sG0[(j) * 32 + lane]
     // chains (0, l)
+    {
+        float dv[16], hv[16];
 #pragma unroll
-    for (int l = 1; l < 17; ++l) {
-        const float v = fmaf(lam, tb[kTblH0 + l], tb[kTblD + pair_off(0) + l - 1]);
-        if (l == 1) { G0(1) = v; G1(pair_off(0)) = INF; }
-        else G1(pair_off(0) + l - 1) = v;
-    }
-#pragma unroll
-    for (int j = 1; j < 16; ++j) {
-        float acc[16];
-        float acc0;
-        {
-            const float g0 = G0(j);
-            const float *h = tb + kTblHH + trip_off(j - 1, j);
-            acc0 = fmaf(lam, h[0], g0);
-#pragma unroll
-            for (int t = 1; t < 16 - j; ++t) acc[t] = fmaf(lam, h[t], g0);
-            acc[0] = INF;
+        for (int t = 0; t < 4; ++t) {
+            const float4 a = reinterpret_cast<const float4 *>(tb + kTblD + dp_off(0))[t];
+            const float4 h = reinterpret_cast<const float4 *>(tb + kTblH0)[t];
+            dv[4 * t] = a.x; dv[4 * t + 1] = a.y; dv[4 * t + 2] = a.z; dv[4 * t + 3] = a.w;
+            hv[4 * t] = h.x; hv[4 * t + 1] = h.y; hv[4 * t + 2] = h.z; hv[4 * t + 3] = h.w;
         }
+        const float h16 = tb[kTblH0 + 16];
 #pragma unroll
-        for (int i = 0; i < j; ++i) {
-            const float g = G1(pair_off(i) + j - i - 1);
-            const float *h = tb + kTblHH + trip_off(i, j);
-#pragma unroll
-            for (int t = 0; t < 16 - j; ++t) acc[t] = fminf(acc[t], fmaf(lam, h[t], g));
+        for (int l = 1; l < 17; ++l) {
+            const float v = fmaf(lam, l < 16 ? hv[l] : h16, dv[l - 1]);
+            if (l == 1) { G0(1) = v; G1(0, 1) = INF; }
+            else G1(0, l) = v;
         }
-        const float *Dj = tb + kTblD + pair_off(j);
-        G0(j + 1) = acc0 + Dj[0];
-#pragma unroll
-        for (int t = 0; t < 16 - j; ++t) G1(pair_off(j) + t) = acc[t] + Dj[t];
     }
+    dp_a_stage<1>(tb, lam, sG1, sG0, lane);
     // final level (slot 16)
     float best = INF;
     int bi = -1;
     if (C == 0) best = fmaf(lam, tb[kTblHend + 15], G0(16));
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const float v = fmaf(lam, tb[kTblHend + i], G1(pair_off(i) + 16 - i - 1));
+        const float v = fmaf(lam, tb[kTblHend + i], G1(i, 16));
         if (v < best) { best = v; bi = i; }
     }
     if (bi < 0) {   // the chain through every slot
         mask = 0x1ffffu;
         float r = tb[kTblH0 + 1];
-        for (int j = 1; j < 16; ++j) r += tb[kTblHH + trip_off(j - 1, j)];
+        for (int j = 1; j < 16; ++j) r += hh_at(tb, j - 1, j, j + 1);
         rate = r + tb[kTblHend + 15];
         return;
     }
@@ -297,27 +379,25 @@ __device__ __forceinline__ void dp_path_a(const float *__restrict__ tb, float la
     int j = bi, l = 16;
     bool from_start = true;
     for (int guard = 0; guard < 17 && j > 0; ++guard) {
-        const int tl = l - j - 1;
-        const float cg0 = fmaf(lam, tb[kTblHH + trip_off(j - 1, j) + tl], G0(j));
+        const float cg0 = fmaf(lam, hh_at(tb, j - 1, j, l), G0(j));
         float acc = (l >= j + 2) ? cg0 : INF;
-        for (int i = 0; i < j; ++i)
-            acc = fminf(acc, fmaf(lam, tb[kTblHH + trip_off(i, j) + tl], G1(pair_off(i) + j - i - 1)));
+        for (int i = 0; i < j; ++i) acc = fminf(acc, fmaf(lam, hh_at(tb, i, j, l), G1(i, j)));
         if (l >= j + 2 && cg0 == acc) {           // the no-skip prefix 0..j
-            r += tb[kTblHH + trip_off(j - 1, j) + tl];
+            r += hh_at(tb, j - 1, j, l);
             m |= (1u << (j + 1)) - 1u;
             r += tb[kTblH0 + 1];
-            for (int t = 1; t < j; ++t) r += tb[kTblHH + trip_off(t - 1, t)];
+            for (int t = 1; t < j; ++t) r += hh_at(tb, t - 1, t, t + 1);
             from_start = false;
             break;
         }
         int pred = -1;
         for (int i = 0; i < j; ++i)
-            if (fmaf(lam, tb[kTblHH + trip_off(i, j) + tl], G1(pair_off(i) + j - i - 1)) == acc) {
+            if (fmaf(lam, hh_at(tb, i, j, l), G1(i, j)) == acc) {
                 pred = i;
                 break;
             }
         if (pred < 0) { from_start = false; break; }   // non-finite data only
-        r += tb[kTblHH + trip_off(pred, j) + tl];
+        r += hh_at(tb, pred, j, l);
         m |= 1u << pred;
         l = j;
         j = pred;
@@ -342,27 +422,26 @@ __device__ void dp_path_b(const float *__restrict__ tb, float lam, int s,
     const float INF = __int_as_float(0x7f800000);
     for (int p = 0; p < kPairs; ++p) sG[p * 32 + lane] = INF;
     for (int l = 1; l < 17; ++l) {
-        const int p = pair_off(0) + l - 1;
-        sG[p * 32 + lane] = fmaf(lam, tb[kTblH0 + l], tb[kTblD + p]);
+        const int p = pidx(0, l);
+        sG[p * 32 + lane] = fmaf(lam, tb[kTblH0 + l], dp_at(tb, 0, l));
         sR[p * 32 + lane] = tb[kTblH0 + l];
         sM[p * 32 + lane] = 1u | (1u << l);
     }
     for (int it = 0; it < s - 2; ++it) {
         for (int j = 15; j >= 1; --j) {
             for (int l = j + 1; l < 17; ++l) {
-                const int pjl = pair_off(j) + l - j - 1;
+                const int pjl = pidx(j, l);
                 float best = sG[pjl * 32 + lane];
-                const float dv = tb[kTblD + pjl];
+                const float dv = dp_at(tb, j, l);
                 int bi = -1;
                 for (int i = 0; i < j; ++i) {
-                    const float c = fmaf(lam, tb[kTblHH + trip_off(i, j) + l - j - 1],
-                                         sG[(pair_off(i) + j - i - 1) * 32 + lane]) + dv;
+                    const float c = fmaf(lam, hh_at(tb, i, j, l), sG[pidx(i, j) * 32 + lane]) + dv;
                     if (c < best) { best = c; bi = i; }
                 }
                 if (bi >= 0) {
-                    const int pij = pair_off(bi) + j - bi - 1;
+                    const int pij = pidx(bi, j);
                     sG[pjl * 32 + lane] = best;
-                    sR[pjl * 32 + lane] = sR[pij * 32 + lane] + tb[kTblHH + trip_off(bi, j) + l - j - 1];
+                    sR[pjl * 32 + lane] = sR[pij * 32 + lane] + hh_at(tb, bi, j, l);
                     sM[pjl * 32 + lane] = sM[pij * 32 + lane] | (1u << l);
                 }
             }
@@ -371,10 +450,10 @@ __device__ void dp_path_b(const float *__restrict__ tb, float lam, int s,
     float best = INF;
     int bi = 0;
     for (int i = 0; i < 16; ++i) {
-        const float v = fmaf(lam, tb[kTblHend + i], sG[(pair_off(i) + 16 - i - 1) * 32 + lane]);
+        const float v = fmaf(lam, tb[kTblHend + i], sG[pidx(i, 16) * 32 + lane]);
         if (v < best) { best = v; bi = i; }
     }
-    const int p = pair_off(bi) + 16 - bi - 1;
+    const int p = pidx(bi, 16);
     rate = sR[p * 32 + lane] + tb[kTblHend + bi];
     mask = sM[p * 32 + lane];
 }
@@ -395,8 +474,8 @@ template <bool GENERAL>
 __global__ void __launch_bounds__(RoundCfg<GENERAL>::kWarps * 32)
 search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restrict__ ctrl,
                     float *__restrict__ rates, uint32_t *__restrict__ masks,
-                    float *__restrict__ rate_hi, uint32_t *__restrict__ mask_hi,
-                    double *__restrict__ partial) {
+                    float *__restrict__ rate_lo, float *__restrict__ rate_hi,
+                    uint32_t *__restrict__ mask_hi, uint8_t *__restrict__ act) {
     using Cfg = RoundCfg<GENERAL>;
     constexpr int W = Cfg::kWarps;
     extern __shared__ __align__(16) float smem[];
@@ -411,46 +490,65 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
     const int64_t b = (int64_t)blockIdx.x * W + w;
     float my_rate = 0.f;
     if (b < nb) {
-        // the previous round's chain at hi becomes this block's chain at hi
-        if (c.hi_probe >= 0) {
+        // carry the previous round's results at the new lo / hi
+        bool active = true;
+        if (c.phase == kPhaseBisect) {
+            // lane 0 alone touches the per-block state, then broadcasts
+            float rl = 0.f, rh = 0.f;
             if (lane == 0) {
-                rate_hi[b] = rates[b * 32 + c.hi_probe];
-                mask_hi[b] = masks[b * 32 + c.hi_probe];
+                const bool was = act[b] != 0;
+                rl = rate_lo[b];
+                rh = rate_hi[b];
+                if (was && c.lo_probe >= 0) rl = rates[b * 32 + c.lo_probe];
+                if (was && c.hi_probe >= 0) {
+                    rh = rates[b * 32 + c.hi_probe];
+                    mask_hi[b] = masks[b * 32 + c.hi_probe];
+                }
+                rate_lo[b] = rl;
+                rate_hi[b] = rh;
             }
+            rl = __shfl_sync(0xffffffffu, rl, 0);
+            rh = __shfl_sync(0xffffffffu, rh, 0);
+            // the rate is non-increasing in lambda: equal at both ends means
+            // constant on [lo, hi], and so is the chosen chain
+            active = rl != rh;
+            my_rate = rh;
+        }
+        if (lane == 0) act[b] = active ? 1 : 0;
+        if (active) {
+            const float4 *src = reinterpret_cast<const float4 *>(tables + b * kTblStride);
+            float4 *dst = reinterpret_cast<float4 *>(sTbl);
+            for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
             __syncwarp();
-        }
-        const float4 *src = reinterpret_cast<const float4 *>(tables + b * kTblStride);
-        float4 *dst = reinterpret_cast<float4 *>(sTbl);
-        for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
-        __syncwarp();
-        const double hi0 = __longlong_as_double((long long)c.hi0_bits);
-        const float lam = (float)probe_lambda(c, hi0, lane);
-        const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
-        float rate;
-        uint32_t mask;
-        if (mp <= 1) {
-            rate = 0.f;
-            mask = 1u;
-        } else {
-            const int C = mp > s ? mp - s : 0;
-            if (!GENERAL || C == 0 || (C == 1 && mp == 17)) {
-                dp_path_a(sTbl, lam, C, sState, sState + kPairs * 32, lane, rate, mask);
+            const double hi0 = __longlong_as_double((long long)c.hi0_bits);
+            const float lam = (float)probe_lambda(c, hi0, lane);
+            const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
+            float rate;
+            uint32_t mask;
+            if (mp <= 1) {
+                rate = 0.f;
+                mask = 1u;
             } else {
-                dp_path_b(sTbl, lam, s, sState, sState + kPairs * 32,
-                          reinterpret_cast<uint32_t *>(sState + 2 * kPairs * 32), lane, rate,
-                          mask);
+                const int C = mp > s ? mp - s : 0;
+                if (!GENERAL || C == 0 || (C == 1 && mp == 17)) {
+                    dp_path_a(sTbl, lam, C, sState, sState + kPairs * 32, lane, rate, mask);
+                } else {
+                    dp_path_b(sTbl, lam, s, sState, sState + kPairs * 32,
+                              reinterpret_cast<uint32_t *>(sState + 2 * kPairs * 32), lane, rate,
+                              mask);
+                }
             }
+            rates[b * 32 + lane] = rate;
+            masks[b * 32 + lane] = mask;
+            my_rate = rate;
         }
-        rates[b * 32 + lane] = rate;
-        masks[b * 32 + lane] = mask;
-        my_rate = rate;
     }
     sRate[w * 32 + lane] = my_rate;
     __syncthreads();
     if (threadIdx.x < 32) {
         double sum = 0.0;
         for (int k = 0; k < W; ++k) sum += (double)sRate[k * 32 + threadIdx.x];
-        partial[(size_t)blockIdx.x * 32 + threadIdx.x] = sum;
+        atomicAdd(&ctrl->acc[threadIdx.x], (unsigned long long)llrint(sum * kRateScale));
         __threadfence();
     }
     __syncthreads();
@@ -462,21 +560,11 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
     if (!is_last) return;
     __threadfence();
 
-    // ---- last CTA: fixed-order sums per probe, then advance the search
-    __shared__ double sSum[W][32];
-    {
-        const int p = threadIdx.x & 31, part = threadIdx.x >> 5;
-        double sum = 0.0;
-        for (unsigned cta = part; cta < gridDim.x; cta += W)
-            sum += __ldcg(&partial[(size_t)cta * 32 + p]);
-        sSum[part][p] = sum;
-    }
-    __syncthreads();
+    // ---- last CTA: read the sums, advance the search
     __shared__ double R[32];
     if (threadIdx.x < 32) {
-        double sum = 0.0;
-        for (int k = 0; k < W; ++k) sum += sSum[k][threadIdx.x];
-        R[threadIdx.x] = sum;
+        const unsigned long long a = atomicExch(&ctrl->acc[threadIdx.x], 0ull);
+        R[threadIdx.x] = (double)a / kRateScale;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -485,6 +573,7 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
         const double hi0 = __longlong_as_double((long long)n.hi0_bits);
         n.ticket = 0u;
         n.hi_probe = -1;
+        n.lo_probe = -1;
         if (n.phase == kPhaseFixed) {
             n.hi_probe = 0;
             n.R_hi = R[0];
@@ -498,15 +587,15 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
             } else {
                 int t = 1;
                 while (t < 32 && !(R[t] <= B)) ++t;
+                n.lo = 0.0;
+                n.lo_probe = 0;
                 if (t < 32) {
-                    n.lo = 0.0;
                     n.hi = ldexp(hi0, t - 1);
                     n.hi_probe = t;
                     n.R_hi = R[t];
                     n.phase = kPhaseBisect;
                     n.step = 0;
                 } else {
-                    n.lo = 0.0;
                     n.hi = n.lambda = ldexp(hi0, kMaxDoublings);
                     n.hi_probe = 31;
                     n.R_hi = R[31];
@@ -526,6 +615,7 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
                     cur -= half;
                 } else {
                     a = mid;
+                    n.lo_probe = cur - 1;
                     cur += half;
                 }
                 half >>= 1;
@@ -538,6 +628,7 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
                 n.phase = kPhaseDone;
             }
         }
+        for (int i = 0; i < 32; ++i) n.acc[i] = 0ull;
         *ctrl = n;
         __threadfence();
     }
@@ -548,9 +639,10 @@ __global__ void __launch_bounds__(kEmitThreads)
 emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctrl,
             const float *__restrict__ rates, const uint32_t *__restrict__ masks,
             const float *__restrict__ rate_hi, const uint32_t *__restrict__ mask_hi,
-            double *__restrict__ epartial, float *__restrict__ codebook, uint8_t *__restrict__ kout,
-            float *__restrict__ Dr, float *__restrict__ Hr, double *__restrict__ totals,
-            double *__restrict__ lambda_out, int32_t *__restrict__ status) {
+            const uint8_t *__restrict__ act, double *__restrict__ epartial,
+            float *__restrict__ codebook, uint8_t *__restrict__ kout, float *__restrict__ Dr,
+            float *__restrict__ Hr, double *__restrict__ totals, double *__restrict__ lambda_out,
+            int32_t *__restrict__ status) {
     const Ctrl c = *ctrl;
     const int64_t b = (int64_t)blockIdx.x * kEmitThreads + threadIdx.x;
     double myD = 0.0;
@@ -558,7 +650,7 @@ emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctr
         const float *tb = tables + b * kTblStride;
         uint32_t mask;
         float rate;
-        if (c.hi_probe >= 0) {
+        if (c.hi_probe >= 0 && act[b]) {
             mask = masks[b * 32 + c.hi_probe];
             rate = rates[b * 32 + c.hi_probe];
         } else {
@@ -573,7 +665,7 @@ emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctr
         for (int t = 0; t < 17; ++t) {
             if (!(mask >> t & 1u)) continue;
             q[k < 16 ? k : 15] = tb[kTblC + t];
-            if (prev >= 0) Dsum += tb[kTblD + pair_off(prev) + t - prev - 1];
+            if (prev >= 0) Dsum += dp_at(tb, prev, t);
             prev = t;
             ++k;
         }
@@ -588,7 +680,7 @@ emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctr
         Hr[b] = rate / (float)d;
         myD = (double)Dsum;
     }
-    // fixed-order block reduction
+    // fixed-order block reduction of sum D_r
     __shared__ double sD[kEmitThreads / 32];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
@@ -653,7 +745,7 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
         empty_alloc_kernel<<<1, 32, 0, st>>>(totals, lambda, status, mode, eta, budget);
         return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
     }
-    Workspace ws = carve(workspace, nb, s);
+    Workspace ws = carve(workspace, nb);
     ctrl_init_kernel<<<1, 32, 0, st>>>(ws.ctrl, budget, eta, mode, lambda);
     const unsigned tgrid = (unsigned)((nb + kTablesWarps - 1) / kTablesWarps);
     tables_kernel<<<tgrid, kTablesWarps * 32, 0, st>>>(static_cast<const StatsRow *>(stats), nb,
@@ -665,18 +757,20 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
             using Cfg = RoundCfg<true>;
             const unsigned grid = (unsigned)((nb + Cfg::kWarps - 1) / Cfg::kWarps);
             search_round_kernel<true><<<grid, Cfg::kWarps * 32, Cfg::kSmem, st>>>(
-                ws.tables, nb, s, ws.ctrl, ws.rates, ws.masks, ws.rate_hi, ws.mask_hi, ws.partial);
+                ws.tables, nb, s, ws.ctrl, ws.rates, ws.masks, ws.rate_lo, ws.rate_hi, ws.mask_hi,
+                ws.act);
         } else {
             using Cfg = RoundCfg<false>;
             const unsigned grid = (unsigned)((nb + Cfg::kWarps - 1) / Cfg::kWarps);
             search_round_kernel<false><<<grid, Cfg::kWarps * 32, Cfg::kSmem, st>>>(
-                ws.tables, nb, s, ws.ctrl, ws.rates, ws.masks, ws.rate_hi, ws.mask_hi, ws.partial);
+                ws.tables, nb, s, ws.ctrl, ws.rates, ws.masks, ws.rate_lo, ws.rate_hi, ws.mask_hi,
+                ws.act);
         }
     }
     const unsigned egrid = (unsigned)((nb + kEmitThreads - 1) / kEmitThreads);
     emit_kernel<<<egrid, kEmitThreads, 0, st>>>(ws.tables, nb, ws.ctrl, ws.rates, ws.masks,
-                                                ws.rate_hi, ws.mask_hi, ws.epartial, codebook, k,
-                                                Dr, Hr, totals, lambda, status);
+                                                ws.rate_hi, ws.mask_hi, ws.act, ws.epartial,
+                                                codebook, k, Dr, Hr, totals, lambda, status);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

@@ -23,6 +23,7 @@ static bool layout_ok(const kvq_layout &L) {
     const int G = L.group;
     if (!(G == 8 || G == 16 || G == 32 || G == 64 || G == 128)) return false;
     if (L.D <= 0 || L.D % G != 0 || L.D / G > 32) return false;
+    if ((L.D & (L.D - 1)) != 0 || L.D > 2048) return false;   // power of two
     // element count must fit comfortably in 64-bit index arithmetic
     if (L.S > 0 && L.T > 0 && (double)L.S * (double)L.T * (double)L.D > 9.0e15) return false;
     return true;

@@ -42,25 +42,50 @@ constexpr int kFlagNonfinite = 1;
 //              levels i and l, h(M) = -M log2(M/d)
 //   h0(l)      h(Mdn(0,l)): term of the first level
 //   hend(i)    h(Mup(i,16)): term of the last level
-// Pair (j,l) is stored at pair_off(j) + l-j-1; triple (i,j,l) at
-// trip_off(i,j) + l-j-1, so the entries of one (i,j) are contiguous in l.
-__host__ __device__ constexpr int pair_off(int j) { return 16 * j - j * (j - 1) / 2; }
-__host__ __device__ constexpr int trip_base(int j) {
-    // sum_{j'=1}^{j-1} j' (16 - j')
-    return 16 * (j - 1) * j / 2 - (j - 1) * j * (2 * j - 1) / 6;
+// Row j of Dp holds l = j+1 .. 16 and row (i,j) of hh holds l = j+1 .. 16,
+// each padded to a multiple of 4 floats so rows start on 16 bytes.
+// pidx(j,l) is the compact index of a pair (lane-private DP state).
+__host__ __device__ constexpr int pad4(int n) { return (n + 3) & ~3; }
+// Closed forms (row j holds 16 - j entries padded to 16 - 4 floor(j/4)):
+//   dp_off(j)    = sum_{j' < j} pad4(16 - j')
+//   trip_base(j) = sum_{1 <= j' < j} j' pad4(16 - j')
+__host__ __device__ constexpr int dp_off(int j) {
+    const int q = j >> 2, r = j & 3;
+    return 64 * q - 8 * q * (q - 1) + r * (16 - 4 * q);
 }
-__host__ __device__ constexpr int trip_off(int i, int j) { return trip_base(j) + i * (16 - j); }
-static_assert(trip_base(16) == kTriples, "triple count");
-static_assert(pair_off(16) == kPairs, "pair count");
+__host__ __device__ constexpr int trip_base(int j) {
+    const int q = j >> 2, r = j & 3;
+    const int full = q == 0 ? 0 : q == 1 ? 96 : q == 2 ? 360 : q == 3 ? 664 : 880;
+    return full + (16 - 4 * q) * (4 * q * r + r * (r - 1) / 2);
+}
+__host__ __device__ constexpr int trip_off(int i, int j) { return trip_base(j) + i * (16 - 4 * (j >> 2)); }
+__host__ __device__ constexpr int pidx(int j, int l) { return 16 * j - j * (j - 1) / 2 + l - j - 1; }
+// the closed forms agree with the sums they stand for
+__host__ __device__ constexpr bool check_offsets() {
+    int a = 0, b = 0;
+    for (int j = 0; j <= 16; ++j) {
+        if (dp_off(j) != a) return false;
+        if (j >= 1 && trip_base(j) != b) return false;
+        if (j < 16) a += pad4(16 - j);
+        if (j >= 1 && j < 16) b += j * pad4(16 - j);
+        if (j < 16 && 16 - 4 * (j >> 2) != pad4(16 - j)) return false;
+    }
+    return true;
+}
+static_assert(check_offsets(), "table offsets");
+constexpr int kDpFloats = dp_off(16);          // 160
+constexpr int kHHFloats = trip_base(16);       // 880
+static_assert(kDpFloats == 160 && kHHFloats == 880, "padded table sizes");
+static_assert(pidx(15, 16) == kPairs - 1, "pair count");
 
 constexpr int kTblD = 0;
-constexpr int kTblHH = kTblD + kPairs;        // 136
-constexpr int kTblH0 = kTblHH + kTriples;     // 816
-constexpr int kTblHend = kTblH0 + 17;         // 833
-constexpr int kTblC = kTblHend + 17;          // 850: level value per slot
-constexpr int kTblHdr = kTblC + 17;           // 867: m', d, flags (int bits)
-constexpr int kTblStride = 872;               // floats per block (3488 B)
-static_assert(kTblStride % 4 == 0, "16-byte rows");
+constexpr int kTblHH = kTblD + kDpFloats;     // 160
+constexpr int kTblH0 = kTblHH + kHHFloats;    // 1040
+constexpr int kTblHend = kTblH0 + 20;         // 1060
+constexpr int kTblC = kTblHend + 20;          // 1080: level value per slot
+constexpr int kTblHdr = kTblC + 20;           // 1100: m', d, flags (int bits)
+constexpr int kTblStride = 1104;              // floats per block (4416 B)
+static_assert(kTblStride % 4 == 0 && kTblHH % 4 == 0 && kTblH0 % 4 == 0, "16-byte rows");
 
 // ---------------------------------------------------- allocation control
 // Lives at the start of the kvq_allocate workspace.
@@ -77,10 +102,15 @@ struct Ctrl {
     int32_t status;
     int32_t flags;          // OR of block flags
     int32_t mode;
+    int32_t lo_probe;       // probe of the last round that is lo, or -1
     uint32_t ticket;        // last-CTA-done counter of the search rounds
     uint32_t ticket_emit;   // same, emit kernel
-    int32_t pad[4];
+    int32_t pad[3];
+    // per-probe sum of d_r H_r over blocks, fixed point (2^-20 bit units):
+    // integer adds are exact, so the sum does not depend on arrival order
+    unsigned long long acc[32];
 };
+constexpr double kRateScale = 1048576.0;   // 2^20
 constexpr int kPhaseBracket = 0;
 constexpr int kPhaseBisect = 1;
 constexpr int kPhaseDone = 2;

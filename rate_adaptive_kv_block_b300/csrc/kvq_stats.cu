@@ -4,40 +4,47 @@
 // maximum and quantiles; D_r from interval statistics).
 //
 // One CTA of 256 threads per block.  The block's binary16 entries are read
-// once from HBM with 16-byte loads and kept in registers.  Order statistics
-// come from a two-level radix select on the order-preserving 16-bit key:
-//   pass 1  one 64-bit shared atomic per entry into the 256 bins of the key's
-//           high byte; the word packs count (bits 48..60), sum of the low
-//           byte j (28..47) and sum of j^2 (0..27) -- exact integers, no
-//           field can carry into the next for d <= 4096;
+// once from HBM with 16-byte loads; their order-preserving 16-bit keys stay in
+// registers.  Order statistics come from a two-level radix select:
+//   pass 1  each warp histograms its own entries by the key's high byte into a
+//           private 256-bin table: one 32-bit shared atomic adds
+//           (1 << 22) | j (count in bits 22..31, sum of the low byte j in
+//           0..21; a warp holds at most 512 entries, so neither field can
+//           overflow) and a second adds j^2.  The 8 tables are merged per bin;
 //   scan    bin prefix counts locate the bin of each of the 17 ranks;
 //   pass 2  entries of those (<= 17) bins count their low byte in a second
 //           histogram (two 16-bit counters per 32-bit word);
 //   select  one warp per selected bin finds the exact key of each rank and
-//           the prefix sums of (1, j, j^2) below it.
+//           the prefix sums of (1, j, j^2) below it (a count scan, then two
+//           warp reductions).
 // Inside a bin the value is affine in j (one binade quarter: fixed sign and
-// exponent), so the atom moments follow from those integer sums without
-// touching the entries again.  Every fp32 term added is non-negative, so the
-// moments carry no cancellation.
+// exponent), so the atom moments follow from those exact integer sums without
+// touching the entries again: half a warp per atom sums its bins with a
+// fixed-order tree.  Every fp32 term added is non-negative, so there is no cancellation.
+// Non-finite entries are the keys of the four lowest and four highest bins.
 #include "kvq_internal.cuh"
 
 namespace kvq {
 
 constexpr int kStatsThreads = 256;
+constexpr int kStatsWarps = kStatsThreads / 32;
 
 struct StatsSmem {
-    unsigned long long l1[256];
+    uint32_t h1a[kStatsWarps][256];   // per warp: (count << 22) | sum j
+    uint32_t h1b[kStatsWarps][256];   // per warp: sum j^2
+    int32_t cnt[256];
+    uint32_t s1[256], s2[256];
     uint32_t l2[17][128];
-    int32_t pre[256];
     uint8_t binslot[256];
-    int32_t warp_tot[8];
+    int32_t warp_tot[kStatsWarps];
     int32_t rank_bin[17], rank_res[17], rank_slot[17];
+    int32_t slot_first[17], slot_nrank[17];
     int32_t rank_key[17], rank_p0[17], rank_cnt[17];
     uint32_t rank_p1[17], rank_p2[17];
     int32_t dkey[17], dp0[17], dcnt[17];
     uint32_t dp1[17], dp2[17];
     float dc[17];
-    int32_t mprime, nslots, flags;
+    int32_t mprime, nslots;
     float an[16], as1[16], at1[16], ae[16];
 };
 
@@ -89,22 +96,17 @@ template <int UNITS>
 __global__ void __launch_bounds__(kStatsThreads)
 stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsRow *__restrict__ out,
              int32_t *__restrict__ status) {
-    __shared__ StatsSmem sm;
-    const int tid = threadIdx.x;
+    __shared__ __align__(16) StatsSmem sm;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = L.group, D = L.D;
     const int d = 32 * G;
     const int nG = D / G;
     const int64_t blk = blockIdx.x;
     const int g = (int)(blk % nG);
-    const int64_t tbk = blk / nG;                       // stream * nTB + token block
+    const int64_t tbk = blk / nG;                       // stream * (T/32) + token block
     const int units = d / 8, upr = G / 8;               // 8-entry units, units per row
 
-    // zero histograms
-    sm.l1[tid] = 0ull;
-    for (int i = tid; i < 17 * 128; i += kStatsThreads) (&sm.l2[0][0])[i] = 0u;
-    if (tid == 0) sm.flags = 0;
-
-    // ---- load: UNITS 16-byte units per thread, kept in registers
+    // ---- load: UNITS 16-byte units per thread
     uint4 raw[UNITS];
 #pragma unroll
     for (int k = 0; k < UNITS; ++k) {
@@ -116,191 +118,227 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsRow *__restrict_
             raw[k] = __ldg(reinterpret_cast<const uint4 *>(x + off));
         }
     }
+    // zero the tables while the loads are in flight
+    {
+        uint4 *z = reinterpret_cast<uint4 *>(&sm.h1a[0][0]);
+        for (int i = tid; i < 2 * kStatsWarps * 256 / 4; i += kStatsThreads) z[i] = make_uint4(0, 0, 0, 0);
+        uint4 *z2 = reinterpret_cast<uint4 *>(&sm.l2[0][0]);
+        for (int i = tid; i < 17 * 128 / 4; i += kStatsThreads) z2[i] = make_uint4(0, 0, 0, 0);
+    }
     __syncthreads();
 
-    // ---- pass 1: level-1 histogram with exact (count, sum j, sum j^2)
-    int bad = 0;
+    // ---- keys (two per register) and pass 1 into the warp's own table
+    uint32_t keys[UNITS][4];
 #pragma unroll
     for (int k = 0; k < UNITS; ++k) {
         const int u = tid + k * kStatsThreads;
-        if (u >= units) continue;
         const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const uint32_t h = (w4[q >> 1] >> ((q & 1) * 16)) & 0xffffu;
-            bad |= ((h & 0x7c00u) == 0x7c00u);
-            const uint32_t key = f16_key(h);
-            const uint32_t j = key & 255u;
-            atomicAdd(&sm.l1[key >> 8],
-                      (1ull << 48) | ((unsigned long long)j << 28) | (unsigned long long)(j * j));
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t k0 = f16_key(w4[q] & 0xffffu), k1 = f16_key(w4[q] >> 16);
+            keys[k][q] = k0 | (k1 << 16);
+            if (u < units) {
+                atomicAdd(&sm.h1a[warp][k0 >> 8], (1u << 22) | (k0 & 255u));
+                atomicAdd(&sm.h1b[warp][k0 >> 8], (k0 & 255u) * (k0 & 255u));
+                atomicAdd(&sm.h1a[warp][k1 >> 8], (1u << 22) | (k1 & 255u));
+                atomicAdd(&sm.h1b[warp][k1 >> 8], (k1 & 255u) * (k1 & 255u));
+            }
         }
     }
-    if (bad) atomicOr(&sm.flags, kFlagNonfinite);
     __syncthreads();
 
-    // ---- bin prefix counts, ranks -> bins, bins -> slots
-    const unsigned long long v1 = sm.l1[tid];
-    const int cnt = (int)(v1 >> 48);
+    // ---- merge the warp tables (thread = bin), prefix counts, rank -> bin
+    int cnt = 0;
+    uint32_t S1 = 0, S2 = 0;
+#pragma unroll
+    for (int w = 0; w < kStatsWarps; ++w) {
+        const uint32_t a = sm.h1a[w][tid];
+        cnt += (int)(a >> 22);
+        S1 += a & 0x3fffffu;
+        S2 += sm.h1b[w][tid];
+    }
+    sm.cnt[tid] = cnt;
+    sm.s1[tid] = S1;
+    sm.s2[tid] = S2;
     int total;
     const int pre = block_excl_scan(cnt, sm.warp_tot, total);
-    sm.pre[tid] = pre;
-    bool tgt = false;
-#pragma unroll
-    for (int j = 0; j < kCand; ++j) {
-        const int r = (j * (d - 1) + 8) >> 4;
-        if (r >= pre && r < pre + cnt) {
-            tgt = true;
-            sm.rank_bin[j] = tid;
-            sm.rank_res[j] = r - pre;
-        }
+    // ranks r_j = floor((j (d-1) + 8) / 16) inside [pre, pre + cnt):
+    // r_j >= pre  <=>  j (d-1) >= 16 pre - 8;  r_j < pre + cnt  <=>
+    // j (d-1) <= 16 (pre + cnt) - 9
+    int jlo = 17, jhi = -1;
+    if (cnt > 0) {
+        const int dm1 = d - 1;
+        const int a = 16 * pre - 8, bnd = 16 * (pre + cnt) - 9;
+        jlo = a <= 0 ? 0 : (a + dm1 - 1) / dm1;
+        jhi = bnd < 0 ? -1 : min(bnd / dm1, kCand - 1);
+    }
+    const bool tgt = jlo <= jhi;
+    for (int j = jlo; j <= jhi; ++j) {
+        sm.rank_bin[j] = tid;
+        sm.rank_res[j] = ((j * (d - 1) + 8) >> 4) - pre;
     }
     int nslots;
     const int slot = block_excl_scan(tgt ? 1 : 0, sm.warp_tot, nslots);
     sm.binslot[tid] = tgt ? (uint8_t)slot : (uint8_t)0xff;
+    if (tgt) {
+        sm.slot_first[slot] = jlo;
+        sm.slot_nrank[slot] = jhi - jlo + 1;
+    }
     if (tid == 0) sm.nslots = nslots;
     __syncthreads();
-    if (tid < kCand) sm.rank_slot[tid] = sm.binslot[sm.rank_bin[tid]];
 
     // ---- pass 2: per-key counts inside the selected bins
 #pragma unroll
     for (int k = 0; k < UNITS; ++k) {
         const int u = tid + k * kStatsThreads;
         if (u >= units) continue;
-        const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const uint32_t key = f16_key((w4[q >> 1] >> ((q & 1) * 16)) & 0xffffu);
-            const uint32_t s = sm.binslot[key >> 8];
-            if (s != 0xffu) atomicAdd(&sm.l2[s][(key & 255u) >> 1], 1u << ((key & 1u) * 16));
+            const uint32_t key = (keys[k][q >> 1] >> ((q & 1) * 16)) & 0xffffu;
+            const uint32_t sl = sm.binslot[key >> 8];
+            if (sl != 0xffu) atomicAdd(&sm.l2[sl][(key & 255u) >> 1], 1u << ((key & 1u) * 16));
         }
     }
     __syncthreads();
 
-    // ---- exact key of every rank + prefix sums below it inside its bin
-    {
-        const int lane = tid & 31, w = tid >> 5;
-        for (int s = w; s < sm.nslots; s += kStatsThreads / 32) {
-            uint32_t c8[8];
-            uint32_t n = 0, S1 = 0, S2 = 0;
+    // ---- exact key of every rank + prefix sums (count, sum j, sum j^2) of
+    //      the keys below it inside its bin: one warp per selected bin, lane l
+    //      holds keys 8l .. 8l+7
+    for (int sl = warp; sl < sm.nslots; sl += kStatsWarps) {
+        const uint4 wd = reinterpret_cast<const uint4 *>(sm.l2[sl])[lane];
+        const uint32_t c8[8] = {wd.x & 0xffffu, wd.x >> 16, wd.y & 0xffffu, wd.y >> 16,
+                                wd.z & 0xffffu, wd.z >> 16, wd.w & 0xffffu, wd.w >> 16};
+        const uint32_t pairsum = wd.x + wd.y + wd.z + wd.w;   // two 16-bit sums
+        const uint32_t n = (pairsum & 0xffffu) + (pairsum >> 16);
+        uint32_t en = n;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t wd = sm.l2[s][lane * 4 + q];
-                c8[2 * q] = wd & 0xffffu;
-                c8[2 * q + 1] = wd >> 16;
-            }
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t a = __shfl_up_sync(0xffffffffu, en, o);
+            if (lane >= o) en += a;
+        }
+        en -= n;                                                // exclusive
+        uint32_t P1 = 0, P2 = 0;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint32_t jj = lane * 8 + q;
-                n += c8[q];
-                S1 += c8[q] * jj;
-                S2 += c8[q] * jj * jj;
-            }
-            uint32_t en = n, e1 = S1, e2 = S2;   // inclusive scans
+        for (int q = 0; q < 8; ++q) {
+            const uint32_t jj = lane * 8 + q;
+            P1 += c8[q] * jj;
+            P2 += c8[q] * jj * jj;
+        }
+        const int j0 = sm.slot_first[sl], nr = sm.slot_nrank[sl];
+        for (int j = j0; j < j0 + nr; ++j) {
+            const uint32_t res = (uint32_t)sm.rank_res[j];
+            const bool mine = res >= en && res < en + n;
+            const int L = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+            const uint32_t b1 = __reduce_add_sync(0xffffffffu, lane < L ? P1 : 0u);
+            const uint32_t b2 = __reduce_add_sync(0xffffffffu, lane < L ? P2 : 0u);
+            if (lane == L) {
+                uint32_t cum = en, p1 = b1, p2 = b2;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t a = __shfl_up_sync(0xffffffffu, en, o);
-                const uint32_t b = __shfl_up_sync(0xffffffffu, e1, o);
-                const uint32_t c = __shfl_up_sync(0xffffffffu, e2, o);
-                if (lane >= o) { en += a; e1 += b; e2 += c; }
-            }
-            en -= n; e1 -= S1; e2 -= S2;         // exclusive
-            for (int j = 0; j < kCand; ++j) {
-                if (sm.rank_slot[j] != s) continue;
-                const uint32_t res = (uint32_t)sm.rank_res[j];
-                if (res >= en && res < en + n) {
-                    uint32_t cum = en, p1 = e1, p2 = e2;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint32_t jj = lane * 8 + q;
-                        if (res < cum + c8[q]) {
-                            sm.rank_key[j] = (sm.rank_bin[j] << 8) | (int)jj;
-                            sm.rank_p0[j] = (int)cum;
-                            sm.rank_p1[j] = p1;
-                            sm.rank_p2[j] = p2;
-                            sm.rank_cnt[j] = (int)c8[q];
-                            break;
-                        }
-                        cum += c8[q];
-                        p1 += c8[q] * jj;
-                        p2 += c8[q] * jj * jj;
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t jj = lane * 8 + q;
+                    if (res < cum + c8[q]) {
+                        sm.rank_key[j] = (sm.rank_bin[j] << 8) | (int)jj;
+                        sm.rank_p0[j] = (int)cum;
+                        sm.rank_p1[j] = p1;
+                        sm.rank_p2[j] = p2;
+                        sm.rank_cnt[j] = (int)c8[q];
+                        break;
                     }
+                    cum += c8[q];
+                    p1 += c8[q] * jj;
+                    p2 += c8[q] * jj * jj;
                 }
             }
         }
     }
     __syncthreads();
 
-    // ---- merge equal candidates
-    if (tid == 0) {
-        int mp = 0;
-        for (int j = 0; j < kCand; ++j) {
-            const int key = sm.rank_key[j];
-            if (mp == 0 || key != sm.dkey[mp - 1]) {
-                sm.dkey[mp] = key;
-                sm.dp0[mp] = sm.rank_p0[j];
-                sm.dp1[mp] = sm.rank_p1[j];
-                sm.dp2[mp] = sm.rank_p2[j];
-                sm.dcnt[mp] = sm.rank_cnt[j];
-                sm.dc[mp] = key_value((uint32_t)key);
-                ++mp;
-            }
+    // ---- merge equal candidates (warp 0, lane j = rank j)
+    if (warp == 0) {
+        const int key = lane < kCand ? sm.rank_key[lane] : -1;
+        const int prev = (lane >= 1 && lane < kCand) ? sm.rank_key[lane - 1] : -2;
+        const bool first = lane < kCand && key != prev;
+        const uint32_t bal = __ballot_sync(0xffffffffu, first);
+        if (first) {
+            const int p = __popc(bal & ((1u << lane) - 1u));
+            sm.dkey[p] = key;
+            sm.dp0[p] = sm.rank_p0[lane];
+            sm.dp1[p] = sm.rank_p1[lane];
+            sm.dp2[p] = sm.rank_p2[lane];
+            sm.dcnt[p] = sm.rank_cnt[lane];
+            sm.dc[p] = key_value((uint32_t)key);
         }
-        sm.mprime = mp;
+        if (lane == 0) sm.mprime = __popc(bal);
     }
     __syncthreads();
 
-    // ---- atom moments, one thread per atom, bins in increasing order
+    // ---- atom moments: half a warp per atom (16 atoms in one pass over the 8
+    //      warps).  Sub-lane 0 takes the piece above the atom's lower
+    //      candidate (or the whole atom when both candidates share a bin),
+    //      sub-lane 1 the piece below its upper candidate, sub-lanes 2..15 the
+    //      bins strictly between; a fixed-order 16-lane tree sums them.
     const int mp = sm.mprime;
-    if (tid < 16) {
+    {
+        const int p = 2 * warp + (lane >> 4), sub = lane & 15;
         float an = 0.f, as1 = 0.f, at1 = 0.f, ae = 0.f;
-        const int p = tid;
         if (p < mp - 1) {
             const bool last = (p == mp - 2);
             const uint32_t Klo = (uint32_t)sm.dkey[p], Khi = (uint32_t)sm.dkey[p + 1];
             const uint32_t blo = Klo >> 8, bhi = Khi >> 8;
-            const int jlo = (int)(Klo & 255u), jhi = (int)(Khi & 255u);
             const float cp = sm.dc[p], cq = sm.dc[p + 1];
-            // prefix sums (over keys < X of X's bin) at the two ends
-            const uint32_t lo0 = sm.dp0[p], lo1 = sm.dp1[p], lo2 = sm.dp2[p];
-            uint32_t hi0 = sm.dp0[p + 1], hi1 = sm.dp1[p + 1], hi2 = sm.dp2[p + 1];
-            int jend = jhi - 1;
-            if (last) {   // the maximum itself belongs to the last atom
-                const uint32_t c = (uint32_t)sm.dcnt[p + 1];
-                hi0 += c;
-                hi1 += c * (uint32_t)jhi;
-                hi2 += c * (uint32_t)jhi * (uint32_t)jhi;
-                jend = jhi;
-            }
-            if (blo == bhi) {
-                add_piece(blo, jlo, jend, hi0 - lo0, hi1 - lo1, hi2 - lo2, cp, cq, an, as1, at1, ae);
-            } else {
-                const unsigned long long t = sm.l1[blo];
-                add_piece(blo, jlo, 255, (uint32_t)(t >> 48) - lo0,
-                          (uint32_t)((t >> 28) & 0xfffffu) - lo1, (uint32_t)(t & 0xfffffffu) - lo2,
-                          cp, cq, an, as1, at1, ae);
-                for (uint32_t b = blo + 1; b < bhi; ++b) {
-                    const unsigned long long v = sm.l1[b];
-                    if ((v >> 48) == 0) continue;
-                    add_piece(b, 0, 255, (uint32_t)(v >> 48), (uint32_t)((v >> 28) & 0xfffffu),
-                              (uint32_t)(v & 0xfffffffu), cp, cq, an, as1, at1, ae);
+            if (sub >= 2) {
+                for (uint32_t b = blo + (uint32_t)sub - 1u; b < bhi; b += 14u) {
+                    const int c = sm.cnt[b];
+                    if (c) add_piece(b, 0, 255, (uint32_t)c, sm.s1[b], sm.s2[b], cp, cq, an, as1, at1, ae);
                 }
-                if (jend >= 0) add_piece(bhi, 0, jend, hi0, hi1, hi2, cp, cq, an, as1, at1, ae);
+            } else {
+                const int jlo = (int)(Klo & 255u), jhi = (int)(Khi & 255u);
+                const uint32_t lo0 = sm.dp0[p], lo1 = sm.dp1[p], lo2 = sm.dp2[p];
+                uint32_t hi0 = sm.dp0[p + 1], hi1 = sm.dp1[p + 1], hi2 = sm.dp2[p + 1];
+                int jend = jhi - 1;
+                if (last) {   // the maximum itself belongs to the last atom
+                    const uint32_t c = (uint32_t)sm.dcnt[p + 1];
+                    hi0 += c;
+                    hi1 += c * (uint32_t)jhi;
+                    hi2 += c * (uint32_t)jhi * (uint32_t)jhi;
+                    jend = jhi;
+                }
+                if (sub == 0) {
+                    if (blo == bhi)
+                        add_piece(blo, jlo, jend, hi0 - lo0, hi1 - lo1, hi2 - lo2, cp, cq, an, as1, at1, ae);
+                    else
+                        add_piece(blo, jlo, 255, (uint32_t)sm.cnt[blo] - lo0, sm.s1[blo] - lo1,
+                                  sm.s2[blo] - lo2, cp, cq, an, as1, at1, ae);
+                } else if (blo != bhi && jend >= 0) {
+                    add_piece(bhi, 0, jend, hi0, hi1, hi2, cp, cq, an, as1, at1, ae);
+                }
             }
         }
-        sm.an[tid] = an;
-        sm.as1[tid] = as1;
-        sm.at1[tid] = at1;
-        sm.ae[tid] = ae;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+            an += __shfl_down_sync(0xffffffffu, an, o, 16);
+            as1 += __shfl_down_sync(0xffffffffu, as1, o, 16);
+            at1 += __shfl_down_sync(0xffffffffu, at1, o, 16);
+            ae += __shfl_down_sync(0xffffffffu, ae, o, 16);
+        }
+        if (sub == 0 && p < 16) {
+            sm.an[p] = an;
+            sm.as1[p] = as1;
+            sm.at1[p] = at1;
+            sm.ae[p] = ae;
+        }
     }
     __syncthreads();
 
-    // ---- write the row (96 words)
+    // ---- write the row (96 words); non-finite keys live in bins 0..3, 252..255
+    const bool bad = (sm.cnt[0] | sm.cnt[1] | sm.cnt[2] | sm.cnt[3] | sm.cnt[252] | sm.cnt[253] |
+                      sm.cnt[254] | sm.cnt[255]) != 0;
     if (tid < 96) {
         float *row = reinterpret_cast<float *>(out + blk);
         float v = 0.f;
         if (tid < 17) v = sm.dc[tid < mp ? tid : mp - 1];
         else if (tid == 17) v = __int_as_float(mp);
-        else if (tid == 18) v = __int_as_float(sm.flags);
+        else if (tid == 18) v = __int_as_float(bad ? kFlagNonfinite : 0);
         else if (tid == 19) v = __int_as_float(d);
         else if (tid < 36) v = sm.an[tid - 20];
         else if (tid < 52) v = sm.as1[tid - 36];
@@ -308,7 +346,7 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsRow *__restrict_
         else if (tid < 84) v = sm.ae[tid - 68];
         row[tid] = v;
     }
-    if (tid == 0 && sm.flags) atomicMax(status, (int32_t)KVQ_ERR_NONFINITE);
+    if (tid == 0 && bad) atomicMax(status, (int32_t)KVQ_ERR_NONFINITE);
 }
 
 int launch_stats(const uint16_t *x, const kvq_layout &L, void *stats, int32_t *status,
