@@ -37,7 +37,7 @@ namespace kvq {
 constexpr int kTablesWarps = 4;
 constexpr int kRoundWarps = 4;        // s >= 16: DP path A only
 constexpr int kRoundWarpsGen = 2;     // s < 16: path B possible
-constexpr int kEmitThreads = 256;
+constexpr int kEmitWarps = 4;
 
 // ---------------------------------------------------------------- workspace
 struct Workspace {
@@ -49,7 +49,7 @@ struct Workspace {
     float *rate_hi;       // [nblk]       d_r H_r at hi
     uint32_t *mask_hi;    // [nblk]       chain at hi
     uint8_t *act;         // [nblk]       evaluated in the last round
-    double *epartial;     // [emit CTAs][2]
+    double *epartial;     // [emit CTAs]
 };
 
 static size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -62,7 +62,7 @@ size_t workspace_bytes(int64_t nb, int s) {
     b += align_up((size_t)nb * 32 * sizeof(uint32_t));
     b += 3 * align_up((size_t)nb * sizeof(float));
     b += align_up((size_t)nb);
-    b += align_up((size_t)((nb + kEmitThreads - 1) / kEmitThreads) * 2 * sizeof(double));
+    b += align_up((size_t)((nb + kEmitWarps - 1) / kEmitWarps) * sizeof(double));
     return b;
 }
 
@@ -93,23 +93,18 @@ static Workspace carve(void *base, int64_t nb) {
 __global__ void ctrl_init_kernel(Ctrl *c, double budget, double eta, int mode,
                                  const double *lambda_in) {
     if (threadIdx.x != 0) return;
+    search_init(c->s);
     c->budget = budget;
     c->eta = eta;
-    c->lo = 0.0;
-    c->hi = 0.0;
-    c->lambda = (mode == KVQ_SUBGRADIENT) ? *lambda_in : 0.0;
-    c->R_hi = 0.0;
+    c->fixed = (mode == KVQ_SUBGRADIENT) ? 1 : 0;
+    c->lambda_fixed = c->fixed ? *lambda_in : 0.0;
     c->hi0_bits = 0ull;
-    c->phase = (mode == KVQ_SUBGRADIENT) ? kPhaseFixed : kPhaseBracket;
-    c->step = 0;
-    c->hi_probe = -1;
-    c->lo_probe = -1;
-    for (int i = 0; i < 32; ++i) c->acc[i] = 0ull;
     c->status = KVQ_OK;
     c->flags = 0;
     c->mode = mode;
     c->ticket = 0u;
     c->ticket_emit = 0u;
+    for (int i = 0; i < 32; ++i) c->acc[i] = 0ull;
 }
 
 // -------------------------------------------------------------------- tables
@@ -235,23 +230,20 @@ tables_kernel(const StatsRow *__restrict__ stats, int64_t nb, float *__restrict_
 }
 
 // ------------------------------------------------------- probe lambda values
-// In-order position pos (1..31) of the 5-level bisection tree under [lo, hi],
-// with the midpoints formed exactly as the sequential bisection forms them.
-__device__ __forceinline__ double tree_node(double lo, double hi, int pos) {
-    int cur = 16, half = 8;
-    double a = lo, b = hi;
-    for (;;) {
-        const double mid = 0.5 * (a + b);
-        if (pos == cur) return mid;
-        if (pos < cur) { b = mid; cur -= half; } else { a = mid; cur += half; }
-        half >>= 1;
+__device__ __forceinline__ double probe_lambda(const Ctrl *c, int lane) {
+    if (c->fixed) return c->lambda_fixed;
+    const int ph = c->s.phase;
+    const double hi0 = __longlong_as_double((long long)c->hi0_bits);
+    if (ph == kSearchBracket) {
+        if (lane == 0) return 0.0;
+        if (lane <= kSearchFirstDoublings) return ldexp(hi0, lane - 1);
+        return search_grid(hi0, lane - kSearchFirstDoublings);
     }
-}
-
-__device__ __forceinline__ double probe_lambda(const Ctrl &c, double hi0, int lane) {
-    if (c.phase == kPhaseBracket) return lane == 0 ? 0.0 : ldexp(hi0, lane - 1);
-    if (c.phase == kPhaseFixed) return c.lambda;
-    return lane == 31 ? c.hi : tree_node(c.lo, c.hi, lane + 1);
+    if (ph == kSearchDouble) {
+        const int t = kSearchFirstDoublings + lane;
+        return ldexp(hi0, t <= kSearchMaxDoublings ? t : kSearchMaxDoublings);
+    }
+    return c->s.probe[lane < c->s.nprobe ? lane : 0];
 }
 
 // ---------------------------------------------------------------- DP path A
@@ -331,9 +323,66 @@ __device__ __forceinline__ void dp_a_stage(const float *__restrict__ tb, float l
     if constexpr (J < 15) dp_a_stage<J + 1>(tb, lam, sG1, sG0, lane);
 }
 
+// Walk back one stage: if the chain's current state is (J, l), find the
+// predecessor whose candidate is the minimum (recomputed with the same
+// operations, so the comparison is exact) and add level J's entropy term.
+template <int J>
+__device__ __forceinline__ void dp_a_back(const float *__restrict__ tb, float lam,
+                                          const float *__restrict__ sG1,
+                                          const float *__restrict__ sG0,
+                                          const float *__restrict__ diag, int lane, int &cj,
+                                          int &cl, float &r, uint32_t &m, bool &open) {
+    if (open && cj == J) {
+        const float INF = __int_as_float(0x7f800000);
+        const float *hrow = tb + kTblHH + (cl - J - 1);    // hh(., J, cl) at trip_off(., J)
+        float best = INF, hsel = 0.f;
+        int arg = -2;
+        if (cl >= J + 2) {
+            hsel = hrow[trip_off(J - 1, J)];
+            best = fmaf(lam, hsel, sG0[J * 32 + lane]);
+            arg = -1;
+        }
+#pragma unroll
+        for (int i = 0; i < J; ++i) {
+            const float h = hrow[trip_off(i, J)];
+            const float c = fmaf(lam, h, sG1[pidx(i, J) * 32 + lane]);
+            if (c < best) { best = c; arg = i; hsel = h; }
+        }
+        if (arg == -1) {                 // the no-skip prefix 0, 1, .., J
+            r += hsel + diag[J];
+            m |= (1u << (J + 1)) - 1u;
+            open = false;
+        } else if (arg >= 0) {
+            r += hsel;
+            m |= 1u << arg;
+            cl = J;
+            cj = arg;
+        } else {
+            open = false;                // non-finite data only
+        }
+    }
+    if constexpr (J > 1) dp_a_back<J - 1>(tb, lam, sG1, sG0, diag, lane, cj, cl, r, m, open);
+}
+
+// diag[J] = entropy terms of levels 0 .. J-1 of the chain 0, 1, .., J
+__device__ __forceinline__ void dp_a_diag(const float *__restrict__ tb, float *__restrict__ diag,
+                                          int lane) {
+    float v = 0.f;
+    if (lane == 0) v = tb[kTblH0 + 1];
+    else if (lane < 16) v = tb[kTblHH + trip_off(lane - 1, lane)];     // hh(lane-1, lane, lane+1)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+    }
+    if (lane < 16) diag[lane + 1] = v;
+    __syncwarp();
+}
+
 __device__ __forceinline__ void dp_path_a(const float *__restrict__ tb, float lam, int C,
                                           float *__restrict__ sG1, float *__restrict__ sG0,
-                                          int lane, float &rate, uint32_t &mask) {
+                                          const float *__restrict__ diag, int lane, float &rate,
+                                          uint32_t &mask) {
     const float INF = __int_as_float(0x7f800000);
 #define G1(j, l) sG1[pidx(j, l) * 32 + lane]
 #define G0(j) sG0[(j) * 32 + lane]
@@ -367,43 +416,16 @@ __device__ __forceinline__ void dp_path_a(const float *__restrict__ tb, float la
     }
     if (bi < 0) {   // the chain through every slot
         mask = 0x1ffffu;
-        float r = tb[kTblH0 + 1];
-        for (int j = 1; j < 16; ++j) r += hh_at(tb, j - 1, j, j + 1);
-        rate = r + tb[kTblHend + 15];
+        rate = diag[16] + tb[kTblHend + 15];
         return;
     }
-    // walk back: at state (j, l) find the predecessor whose candidate equals
-    // the minimum (recomputed with the same operations, so equality is exact)
     uint32_t m = (1u << 16) | (1u << bi);
     float r = tb[kTblHend + bi];
-    int j = bi, l = 16;
-    bool from_start = true;
-    for (int guard = 0; guard < 17 && j > 0; ++guard) {
-        const float cg0 = fmaf(lam, hh_at(tb, j - 1, j, l), G0(j));
-        float acc = (l >= j + 2) ? cg0 : INF;
-        for (int i = 0; i < j; ++i) acc = fminf(acc, fmaf(lam, hh_at(tb, i, j, l), G1(i, j)));
-        if (l >= j + 2 && cg0 == acc) {           // the no-skip prefix 0..j
-            r += hh_at(tb, j - 1, j, l);
-            m |= (1u << (j + 1)) - 1u;
-            r += tb[kTblH0 + 1];
-            for (int t = 1; t < j; ++t) r += hh_at(tb, t - 1, t, t + 1);
-            from_start = false;
-            break;
-        }
-        int pred = -1;
-        for (int i = 0; i < j; ++i)
-            if (fmaf(lam, hh_at(tb, i, j, l), G1(i, j)) == acc) {
-                pred = i;
-                break;
-            }
-        if (pred < 0) { from_start = false; break; }   // non-finite data only
-        r += hh_at(tb, pred, j, l);
-        m |= 1u << pred;
-        l = j;
-        j = pred;
-    }
-    if (from_start && j == 0) {
-        r += tb[kTblH0 + l];
+    int cj = bi, cl = 16;
+    bool open = true;
+    dp_a_back<15>(tb, lam, sG1, sG0, diag, lane, cj, cl, r, m, open);
+    if (open && cj == 0) {
+        r += tb[kTblH0 + cl];
         m |= 1u;
     }
     rate = r;
@@ -467,7 +489,7 @@ struct RoundCfg {
     static constexpr int kStateFloats = (GENERAL ? 3 * kPairs : kPairs + 17) * 32;
     static constexpr size_t kSmem =
         (size_t)kWarps * (kTblStride + kStateFloats) * sizeof(float) +
-        (size_t)kWarps * 32 * sizeof(float);
+        (size_t)kWarps * 32 * sizeof(float) + (size_t)kWarps * 32 * sizeof(float);
 };
 
 template <bool GENERAL>
@@ -479,12 +501,14 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
     using Cfg = RoundCfg<GENERAL>;
     constexpr int W = Cfg::kWarps;
     extern __shared__ __align__(16) float smem[];
-    const Ctrl c = *ctrl;
-    if (c.phase == kPhaseDone) return;
+    if (ctrl->s.phase == kSearchDone) return;
+    const int fixed = ctrl->fixed, phase = ctrl->s.phase;
+    const int xa_probe = ctrl->s.xa_probe, xb_probe = ctrl->s.xb_probe;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     float *sTbl = smem + w * kTblStride;
     float *sState = smem + W * kTblStride + w * Cfg::kStateFloats;
     float *sRate = smem + W * (kTblStride + Cfg::kStateFloats);
+    float *sDiag = sRate + W * 32 + w * 32;
     __shared__ bool is_last;
 
     const int64_t b = (int64_t)blockIdx.x * W + w;
@@ -492,27 +516,28 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
     if (b < nb) {
         // carry the previous round's results at the new lo / hi
         bool active = true;
-        if (c.phase == kPhaseBisect) {
-            // lane 0 alone touches the per-block state, then broadcasts
-            float rl = 0.f, rh = 0.f;
+        if (!fixed && phase == kSearchWalk) {
+            // carry the last round's results at the new window ends (lane 0
+            // alone touches the per-block state, then broadcasts)
+            float ra = 0.f, rb = 0.f;
             if (lane == 0) {
                 const bool was = act[b] != 0;
-                rl = rate_lo[b];
-                rh = rate_hi[b];
-                if (was && c.lo_probe >= 0) rl = rates[b * 32 + c.lo_probe];
-                if (was && c.hi_probe >= 0) {
-                    rh = rates[b * 32 + c.hi_probe];
-                    mask_hi[b] = masks[b * 32 + c.hi_probe];
+                ra = rate_lo[b];
+                rb = rate_hi[b];
+                if (was && xa_probe >= 0) ra = rates[b * 32 + xa_probe];
+                if (was && xb_probe >= 0) {
+                    rb = rates[b * 32 + xb_probe];
+                    mask_hi[b] = masks[b * 32 + xb_probe];
                 }
-                rate_lo[b] = rl;
-                rate_hi[b] = rh;
+                rate_lo[b] = ra;
+                rate_hi[b] = rb;
             }
-            rl = __shfl_sync(0xffffffffu, rl, 0);
-            rh = __shfl_sync(0xffffffffu, rh, 0);
-            // the rate is non-increasing in lambda: equal at both ends means
-            // constant on [lo, hi], and so is the chosen chain
-            active = rl != rh;
-            my_rate = rh;
+            ra = __shfl_sync(0xffffffffu, ra, 0);
+            rb = __shfl_sync(0xffffffffu, rb, 0);
+            // the rate is non-increasing in lambda: equal at both window ends
+            // means constant inside the window, and so is the chosen chain
+            active = ra != rb;
+            my_rate = rb;
         }
         if (lane == 0) act[b] = active ? 1 : 0;
         if (active) {
@@ -520,8 +545,7 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
             float4 *dst = reinterpret_cast<float4 *>(sTbl);
             for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
             __syncwarp();
-            const double hi0 = __longlong_as_double((long long)c.hi0_bits);
-            const float lam = (float)probe_lambda(c, hi0, lane);
+            const float lam = (float)probe_lambda(ctrl, lane);
             const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
             float rate;
             uint32_t mask;
@@ -531,7 +555,9 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
             } else {
                 const int C = mp > s ? mp - s : 0;
                 if (!GENERAL || C == 0 || (C == 1 && mp == 17)) {
-                    dp_path_a(sTbl, lam, C, sState, sState + kPairs * 32, lane, rate, mask);
+                    dp_a_diag(sTbl, sDiag, lane);
+                    dp_path_a(sTbl, lam, C, sState, sState + kPairs * 32, sDiag, lane, rate,
+                              mask);
                 } else {
                     dp_path_b(sTbl, lam, s, sState, sState + kPairs * 32,
                               reinterpret_cast<uint32_t *>(sState + 2 * kPairs * 32), lane, rate,
@@ -567,75 +593,78 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
         R[threadIdx.x] = (double)a / kRateScale;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        Ctrl n = *ctrl;
-        const double B = n.budget;
-        const double hi0 = __longlong_as_double((long long)n.hi0_bits);
-        n.ticket = 0u;
-        n.hi_probe = -1;
-        n.lo_probe = -1;
-        if (n.phase == kPhaseFixed) {
-            n.hi_probe = 0;
-            n.R_hi = R[0];
-            n.phase = kPhaseDone;
-        } else if (n.phase == kPhaseBracket) {
-            if (R[0] <= B) {
-                n.lo = n.hi = n.lambda = 0.0;
-                n.hi_probe = 0;
-                n.R_hi = R[0];
-                n.phase = kPhaseDone;
-            } else {
-                int t = 1;
-                while (t < 32 && !(R[t] <= B)) ++t;
-                n.lo = 0.0;
-                n.lo_probe = 0;
-                if (t < 32) {
-                    n.hi = ldexp(hi0, t - 1);
-                    n.hi_probe = t;
-                    n.R_hi = R[t];
-                    n.phase = kPhaseBisect;
-                    n.step = 0;
-                } else {
-                    n.hi = n.lambda = ldexp(hi0, kMaxDoublings);
-                    n.hi_probe = 31;
-                    n.R_hi = R[31];
-                    n.status = KVQ_ERR_INFEASIBLE;
-                    n.phase = kPhaseDone;
-                }
+
+    // warp 0 advances the search: one lane per probe folds the evaluations
+    // into the window (exact min / max reductions), every lane walks, and
+    // lane L generates the probes along decision path L
+    __shared__ SearchState sS;
+    __shared__ double sProbe[kSearchProbes];
+    if (threadIdx.x < 32) {
+        const int L = threadIdx.x;
+        if (L == 0) search_copy_scalars(sS, ctrl->s);
+        sS.probe[L] = ctrl->s.probe[L];
+        __syncwarp();
+        const double B = ctrl->budget;
+        if (ctrl->fixed) {
+            if (L == 0) {
+                sS.xb_probe = 0;
+                sS.R_xb = R[0];
+                sS.lambda = ctrl->lambda_fixed;
+                sS.phase = kSearchDone;
+                sS.rounds += 1;
             }
-        } else {   // bisection: 5 steps down the evaluated tree
-            double a = n.lo, bb = n.hi;
-            int cur = 16, half = 8;
-            for (int lev = 0; lev < kLevelsPerRound && n.step < kBisectSteps; ++lev) {
-                const double mid = 0.5 * (a + bb);
-                if (R[cur - 1] <= B) {
-                    bb = mid;
-                    n.hi_probe = cur - 1;
-                    n.R_hi = R[cur - 1];
-                    cur -= half;
-                } else {
-                    a = mid;
-                    n.lo_probe = cur - 1;
-                    cur += half;
-                }
-                half >>= 1;
-                ++n.step;
+        } else {
+            if (L == 0) sS.hi0 = __longlong_as_double((long long)ctrl->hi0_bits);
+            __syncwarp();
+            const bool inr = L < sS.nprobe;
+            const double v = search_probe(sS, L);
+            const bool feas = inr && R[L] <= B;
+            double vb = feas ? v : INFINITY;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) vb = fmin(vb, __shfl_xor_sync(0xffffffffu, vb, o));
+            const uint32_t mb = __ballot_sync(0xffffffffu, feas && v == vb);
+            const int ib = mb ? __ffs(mb) - 1 : -1;
+            const double xbn = (ib >= 0 && vb < sS.xb) ? vb : sS.xb;
+            const bool inf = inr && !(R[L] <= B) && v < xbn;
+            double va = inf ? v : -INFINITY;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) va = fmax(va, __shfl_xor_sync(0xffffffffu, va, o));
+            const uint32_t ma = __ballot_sync(0xffffffffu, inf && v == va);
+            const int ia = ma ? __ffs(ma) - 1 : -1;
+            SearchState st;                       // every lane walks the same path
+            search_copy_scalars(st, sS);
+            search_window(st, vb, ib, ib >= 0 ? R[ib] : 0.0, va, ia);
+            const int go = search_advance(st, R, B);
+            if (go) {
+                sProbe[L] = search_first_unknown(st);
+                __syncwarp();
+                search_path(st, L, sProbe);
+                __syncwarp();
+                sS.probe[L] = sProbe[L];
             }
-            n.lo = a;
-            n.hi = bb;
-            if (n.step >= kBisectSteps) {
-                n.lambda = n.hi;
-                n.phase = kPhaseDone;
+            __syncwarp();
+            if (L == 0) {
+                search_copy_scalars(sS, st);
+                if (st.infeasible) ctrl->status = KVQ_ERR_INFEASIBLE;
             }
         }
-        for (int i = 0; i < 32; ++i) n.acc[i] = 0ull;
-        *ctrl = n;
+        __syncwarp();
+        if (L == 0) {
+            search_copy_scalars(ctrl->s, sS);
+            ctrl->ticket = 0u;
+        }
+        ctrl->s.probe[L] = sS.probe[L];
         __threadfence();
     }
 }
 
 // -------------------------------------------------------------------- emit
-__global__ void __launch_bounds__(kEmitThreads)
+// One warp per block, lane t = slot t: the chain at the final lambda becomes
+// the codebook (levels in slot order), k, D_r (sum of the chain's interval
+// distortions, reduced in a fixed tree) and H_r.  Sum D_r: per CTA in warp
+// order, then the last CTA adds the CTA partials with all its threads in a
+// fixed pattern.
+__global__ void __launch_bounds__(kEmitWarps * 32)
 emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctrl,
             const float *__restrict__ rates, const uint32_t *__restrict__ masks,
             const float *__restrict__ rate_hi, const uint32_t *__restrict__ mask_hi,
@@ -643,82 +672,90 @@ emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctr
             float *__restrict__ codebook, uint8_t *__restrict__ kout, float *__restrict__ Dr,
             float *__restrict__ Hr, double *__restrict__ totals, double *__restrict__ lambda_out,
             int32_t *__restrict__ status) {
-    const Ctrl c = *ctrl;
-    const int64_t b = (int64_t)blockIdx.x * kEmitThreads + threadIdx.x;
-    double myD = 0.0;
+    const int xb_probe = ctrl->s.xb_probe;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t b = (int64_t)blockIdx.x * kEmitWarps + w;
+    __shared__ double sD[kEmitWarps];
+    __shared__ bool is_last;
+    double Dblk = 0.0;
     if (b < nb) {
         const float *tb = tables + b * kTblStride;
         uint32_t mask;
         float rate;
-        if (c.hi_probe >= 0 && act[b]) {
-            mask = masks[b * 32 + c.hi_probe];
-            rate = rates[b * 32 + c.hi_probe];
+        if (xb_probe >= 0 && act[b]) {
+            mask = masks[b * 32 + xb_probe];
+            rate = rates[b * 32 + xb_probe];
         } else {
             mask = mask_hi[b];
             rate = rate_hi[b];
         }
-        const int d = __float_as_int(tb[kTblHdr + 1]);
-        float q[16];
-        int k = 0;
-        float Dsum = 0.f;
-        int prev = -1;
-        for (int t = 0; t < 17; ++t) {
-            if (!(mask >> t & 1u)) continue;
-            q[k < 16 ? k : 15] = tb[kTblC + t];
-            if (prev >= 0) Dsum += dp_at(tb, prev, t);
-            prev = t;
-            ++k;
+        mask &= 0x1ffffu;
+        if (mask == 0u) mask = 1u;
+        const int k = min(__popc(mask), 16);
+        const bool in = lane < 17 && (mask >> lane & 1u);
+        const int pos = __popc(mask & ((1u << lane) - 1u));
+        float dv = 0.f;
+        if (in) {
+            const uint32_t above = lane < 16 ? (mask >> (lane + 1)) : 0u;
+            if (above) {
+                const int nxt = lane + __ffs(above);
+                dv = dp_at(tb, lane, nxt);
+            }
+            const float q = tb[kTblC + lane];
+            if (pos < 16) codebook[b * 16 + pos] = q;
+            if (pos == k - 1)
+                for (int t = k; t < 16; ++t) codebook[b * 16 + t] = q;
         }
-        if (k > 16) k = 16;   // cannot happen for s <= 16
-        if (k == 0) { k = 1; q[0] = tb[kTblC]; }
-        for (int t = k; t < 16; ++t) q[t] = q[k - 1];
-        float4 *cb = reinterpret_cast<float4 *>(codebook + b * 16);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) cb[t] = make_float4(q[4 * t], q[4 * t + 1], q[4 * t + 2], q[4 * t + 3]);
-        kout[b] = (uint8_t)k;
-        Dr[b] = Dsum;
-        Hr[b] = rate / (float)d;
-        myD = (double)Dsum;
+        for (int o = 16; o > 0; o >>= 1) dv += __shfl_down_sync(0xffffffffu, dv, o);
+        if (lane == 0) {
+            const int d = __float_as_int(tb[kTblHdr + 1]);
+            kout[b] = (uint8_t)k;
+            Dr[b] = dv;
+            Hr[b] = rate / (float)d;
+        }
+        Dblk = (double)dv;
     }
-    // fixed-order block reduction of sum D_r
-    __shared__ double sD[kEmitThreads / 32];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) myD += __shfl_down_sync(0xffffffffu, myD, o);
-    if (lane == 0) sD[w] = myD;
+    if (lane == 0) sD[w] = Dblk;
     __syncthreads();
-    __shared__ bool is_last;
     if (threadIdx.x == 0) {
         double dd = 0.0;
-        for (int k = 0; k < kEmitThreads / 32; ++k) dd += sD[k];
-        epartial[2 * blockIdx.x] = 0.0;
-        epartial[2 * blockIdx.x + 1] = dd;
+        for (int k = 0; k < kEmitWarps; ++k) dd += sD[k];
+        epartial[blockIdx.x] = dd;
         __threadfence();
         const unsigned t = atomicAdd(&ctrl->ticket_emit, 1u);
         is_last = (t == gridDim.x - 1);
     }
     __syncthreads();
-    if (!is_last || threadIdx.x != 0) return;
+    if (!is_last) return;
     __threadfence();
+    __shared__ double sPart[kEmitWarps * 32];
+    {
+        double acc = 0.0;
+        for (unsigned k = threadIdx.x; k < gridDim.x; k += kEmitWarps * 32)
+            acc += __ldcg(&epartial[k]);
+        sPart[threadIdx.x] = acc;
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
     double dd = 0.0;
-    for (unsigned k = 0; k < gridDim.x; ++k) dd += __ldcg(&epartial[2 * k + 1]);
-    Ctrl n = *ctrl;
-    const double R = n.R_hi;   // the rate the search tested (same per-block rates)
-    const double lam = n.lambda;
+    for (int k = 0; k < kEmitWarps * 32; ++k) dd += sPart[k];
+    Ctrl *n = ctrl;
+    const double R = n->s.R_xb;   // the rate the search tested (same per-block rates)
+    const double lam = n->s.lambda;
     totals[0] = R;
     totals[1] = dd;
     totals[2] = lam;
-    if (n.mode == KVQ_SUBGRADIENT) {
-        const double nl = lam + n.eta * (R - n.budget);
+    if (n->mode == KVQ_SUBGRADIENT) {
+        const double nl = lam + n->eta * (R - n->budget);
         *lambda_out = nl > 0.0 ? nl : 0.0;
     } else {
         *lambda_out = lam;
     }
-    int st = n.status;
-    if (n.flags & kFlagNonfinite) st = KVQ_ERR_NONFINITE;
+    int st = n->status;
+    if (n->flags & kFlagNonfinite) st = KVQ_ERR_NONFINITE;
     *status = st;
-    n.ticket_emit = 0u;
-    *ctrl = n;
+    n->ticket_emit = 0u;
 }
 
 __global__ void empty_alloc_kernel(double *totals, double *lambda_out, int32_t *status, int mode,
@@ -750,7 +787,9 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
     const unsigned tgrid = (unsigned)((nb + kTablesWarps - 1) / kTablesWarps);
     tables_kernel<<<tgrid, kTablesWarps * 32, 0, st>>>(static_cast<const StatsRow *>(stats), nb,
                                                        ws.tables, ws.ctrl);
-    const int rounds = (mode == KVQ_SUBGRADIENT) ? 1 : 1 + kBisectSteps / kLevelsPerRound;
+    // bracket + (rarely) the extra doublings + at most 8 walk rounds (each
+    // takes >= 5 bisection steps); rounds after the search is done return at once
+    const int rounds = (mode == KVQ_SUBGRADIENT) ? 1 : 2 + kSearchSteps / 5;
     const bool general = s < 16;
     for (int r = 0; r < rounds; ++r) {
         if (general) {
@@ -767,8 +806,8 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
                 ws.act);
         }
     }
-    const unsigned egrid = (unsigned)((nb + kEmitThreads - 1) / kEmitThreads);
-    emit_kernel<<<egrid, kEmitThreads, 0, st>>>(ws.tables, nb, ws.ctrl, ws.rates, ws.masks,
+    const unsigned egrid = (unsigned)((nb + kEmitWarps - 1) / kEmitWarps);
+    emit_kernel<<<egrid, kEmitWarps * 32, 0, st>>>(ws.tables, nb, ws.ctrl, ws.rates, ws.masks,
                                                 ws.rate_hi, ws.mask_hi, ws.act, ws.epartial,
                                                 codebook, k, Dr, Hr, totals, lambda, status);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include "kvq.h"
+#include "kvq_search.h"
 
 namespace kvq {
 
@@ -90,35 +91,22 @@ static_assert(kTblStride % 4 == 0 && kTblHH % 4 == 0 && kTblH0 % 4 == 0, "16-byt
 // ---------------------------------------------------- allocation control
 // Lives at the start of the kvq_allocate workspace.
 struct Ctrl {
+    SearchState s;          // lambda search (kvq_search.h)
     double budget;          // B (bits)
     double eta;             // subgradient step
-    double lo, hi;          // bisection interval
-    double lambda;          // lambda of the emitted choice
-    double R_hi;            // sum_r d_r H_r at hi (as the search summed it)
+    double lambda_fixed;    // KVQ_SUBGRADIENT: the lambda of this step
     unsigned long long hi0_bits;   // max_r (c_max - c_min)^2 (double bits)
-    int32_t phase;          // kPhase*
-    int32_t step;           // bisection steps done
-    int32_t hi_probe;       // probe of the last round that is hi, or -1
+    int32_t fixed;          // 1: one round at lambda_fixed
     int32_t status;
     int32_t flags;          // OR of block flags
     int32_t mode;
-    int32_t lo_probe;       // probe of the last round that is lo, or -1
     uint32_t ticket;        // last-CTA-done counter of the search rounds
     uint32_t ticket_emit;   // same, emit kernel
-    int32_t pad[3];
     // per-probe sum of d_r H_r over blocks, fixed point (2^-20 bit units):
     // integer adds are exact, so the sum does not depend on arrival order
     unsigned long long acc[32];
 };
 constexpr double kRateScale = 1048576.0;   // 2^20
-constexpr int kPhaseBracket = 0;
-constexpr int kPhaseBisect = 1;
-constexpr int kPhaseDone = 2;
-constexpr int kPhaseFixed = 3;   // subgradient: one round at a given lambda
-constexpr int kProbes = 32;      // lambda values per search round (one per lane)
-constexpr int kBisectSteps = 40;
-constexpr int kLevelsPerRound = 5;   // 31 tree nodes = 5 bisection levels
-constexpr int kMaxDoublings = 30;
 
 // ------------------------------------------------------------ binary16 keys
 // Order-preserving 16-bit key of a binary16 value (-0 folded into +0):

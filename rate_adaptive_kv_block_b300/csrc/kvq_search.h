@@ -1,0 +1,235 @@
+// Search control for the global lambda: the fixed 40-step bisection, walked
+// with as few rounds of evaluations as possible.
+//
+// The problem ("Rate-adaptive KV-cache quantizer", "Mathematical statement")
+// is separable given lambda, and the total rate R(lambda) = sum_r d_r H_r of
+// the per-block minimisers is non-increasing in lambda.  The lambda that the
+// bisection returns is fixed by the predicate P(lambda) = [R(lambda) <= B] at
+// the midpoints it visits:
+//   R(0) <= B  -> lambda = 0;
+//   hi = hi0 * 2^t, t the first of 0..30 with P true (none: infeasible);
+//   40 times: mid = 0.5 (lo + hi); P(mid) ? hi = mid : lo = mid;
+//   lambda = hi.
+// Each round evaluates R at up to 32 lambdas at once (one per lane of the
+// DP).  Every evaluated lambda tightens a window (xa, xb): xa the largest
+// lambda known infeasible, xb the smallest known feasible.  Because R is
+// monotone, a midpoint at or above xb is feasible and one at or below xa is
+// not, so the walk only stops at midpoints strictly inside the window; the
+// next round evaluates those, breadth first over the walk's possible paths.
+// Round 0 probes lambda = 0, the first doublings of hi0 and a geometric grid
+// below hi0, which brackets the answer within a factor 2^1.5 at once.
+//
+// Plain C++ usable on the host (tests) and the device (last CTA of a round).
+#pragma once
+#include <math.h>
+#include <stdint.h>
+
+#ifndef KVQ_HD
+#ifdef __CUDACC__
+#define KVQ_HD __host__ __device__
+#else
+#define KVQ_HD
+#endif
+#endif
+
+namespace kvq {
+
+constexpr int kSearchProbes = 32;
+constexpr int kSearchSteps = 40;
+constexpr int kSearchMaxDoublings = 30;
+constexpr int kSearchFirstDoublings = 3;       // hi0 * 2^0 .. 2^2 in round 0
+
+enum SearchPhase : int32_t {
+    kSearchBracket = 0,   // round 0: 0, hi0 * 2^{0,1,2}, geometric grid
+    kSearchDouble = 1,    // hi0 * 2^3 .. 2^30 (only if round 0 found no feasible hi)
+    kSearchWalk = 2,      // bisection walk
+    kSearchDone = 3,
+};
+
+struct SearchState {
+    double hi0;           // max_r (c_max - c_min)^2
+    double lo, hi;        // bisection interval
+    double xa, xb;        // known infeasible (largest) / feasible (smallest)
+    double R_xb;          // R at xb
+    double lambda;        // the answer once done
+    double probe[kSearchProbes];   // lambdas of the next round (walk phase)
+    int32_t phase;
+    int32_t step;         // bisection steps taken
+    int32_t nprobe;       // probes in use this round
+    int32_t xa_probe;     // probe of the last round that became xa, or -1
+    int32_t xb_probe;     // probe of the last round that became xb, or -1
+    int32_t infeasible;
+    int32_t rounds;
+};
+
+KVQ_HD inline void search_init(SearchState &s) {
+    s.hi0 = 0.0;
+    s.lo = s.hi = 0.0;
+    s.xa = -1.0;
+    s.xb = INFINITY;
+    s.R_xb = 0.0;
+    s.lambda = 0.0;
+    for (int i = 0; i < kSearchProbes; ++i) s.probe[i] = 0.0;
+    s.phase = kSearchBracket;
+    s.step = 0;
+    s.nprobe = kSearchProbes;
+    s.xa_probe = s.xb_probe = -1;
+    s.infeasible = 0;
+    s.rounds = 0;
+}
+
+// hi0 * 2^(-1.5 k), from exact operations: a power-of-two scaling, times
+// sqrt(1/2) (one correctly rounded constant) when k is odd
+KVQ_HD inline double search_grid(double hi0, int k) {
+    const double odd = 0.70710678118654752440;
+    return (k & 1) ? ldexp(hi0 * odd, -(3 * k - 1) / 2) : ldexp(hi0, -(3 * k) / 2);
+}
+
+// lambda evaluated by probe p this round
+KVQ_HD inline double search_probe(const SearchState &s, int p) {
+    if (s.phase == kSearchBracket) {
+        if (p == 0) return 0.0;
+        if (p <= kSearchFirstDoublings) return ldexp(s.hi0, p - 1);
+        return search_grid(s.hi0, p - kSearchFirstDoublings);
+    }
+    if (s.phase == kSearchDouble) {
+        const int t = kSearchFirstDoublings + p;
+        return ldexp(s.hi0, t <= kSearchMaxDoublings ? t : kSearchMaxDoublings);
+    }
+    return s.probe[p < s.nprobe ? p : 0];
+}
+
+// P(mid) if it follows from the window, else -1
+KVQ_HD inline int search_known(const SearchState &s, double mid) {
+    if (mid >= s.xb) return 1;
+    if (mid <= s.xa) return 0;
+    return -1;
+}
+
+// The update is split so that a warp can run it with one lane per probe:
+//   search_window   fold the round's evaluations into (xa, xb)
+//   search_advance  bracket decisions and the walk (cheap, sequential)
+//   search_path     probe generation: lane L follows the decision bits of L
+//                   through the unknown midpoints; the node reached after u
+//                   unknown decisions with prefix bits p gets id 2^u - 1 + p,
+//                   so the 32 paths together write the 31 unknown nodes of
+//                   the next 5 unknown levels (breadth-first set)
+// search_update runs the three in order on one thread (host tests); the
+// device runs the same functions across a warp.
+
+// (xb, its probe) = smallest feasible evaluation; (xa, its probe) = largest
+// infeasible evaluation below xb.  Infeasible evaluations above xb contradict
+// monotonicity (a rounding tie) and are ignored.
+KVQ_HD inline void search_window(SearchState &s, double vb, int ib, double Rb, double va, int ia) {
+    s.xa_probe = s.xb_probe = -1;
+    if (ib >= 0 && vb < s.xb) { s.xb = vb; s.xb_probe = ib; s.R_xb = Rb; }
+    if (ia >= 0 && va > s.xa && va < s.xb) { s.xa = va; s.xa_probe = ia; }
+}
+
+// Bracket decisions and the walk.  Returns 1 if probes must be generated.
+KVQ_HD inline int search_advance(SearchState &s, const double *R, double B) {
+    s.rounds += 1;
+    if (s.phase == kSearchBracket || s.phase == kSearchDouble) {
+        if (s.phase == kSearchBracket && R[0] <= B) {          // lambda = 0
+            s.lo = s.hi = s.lambda = 0.0;
+            s.xb = 0.0;
+            s.xb_probe = 0;
+            s.R_xb = R[0];
+            s.phase = kSearchDone;
+            return 0;
+        }
+        int t = -1;
+        const int pmax = s.phase == kSearchBracket ? kSearchFirstDoublings
+                                                   : kSearchMaxDoublings - kSearchFirstDoublings;
+        for (int p = (s.phase == kSearchBracket ? 1 : 0); p <= pmax && p < s.nprobe; ++p) {
+            const int tt = s.phase == kSearchBracket ? p - 1 : kSearchFirstDoublings + p;
+            if (R[p] <= B) { t = tt; break; }
+        }
+        if (t < 0) {
+            if (s.phase == kSearchBracket) {
+                s.phase = kSearchDouble;
+                s.nprobe = kSearchMaxDoublings - kSearchFirstDoublings + 1;   // 2^3 .. 2^30
+                return 0;
+            }
+            // infeasible at hi0 * 2^30: keep the choice there
+            s.lo = 0.0;
+            s.hi = s.lambda = ldexp(s.hi0, kSearchMaxDoublings);
+            s.xb_probe = s.nprobe - 1;
+            s.R_xb = R[s.nprobe - 1];
+            s.infeasible = 1;
+            s.phase = kSearchDone;
+            return 0;
+        }
+        s.lo = 0.0;
+        s.hi = ldexp(s.hi0, t);
+        s.step = 0;
+        s.phase = kSearchWalk;
+    }
+    while (s.step < kSearchSteps) {
+        const double mid = 0.5 * (s.lo + s.hi);
+        const int k = search_known(s, mid);
+        if (k < 0) break;
+        if (k) s.hi = mid; else s.lo = mid;
+        ++s.step;
+    }
+    if (s.step >= kSearchSteps) {
+        s.lambda = s.hi;
+        s.phase = kSearchDone;
+        return 0;
+    }
+    s.nprobe = kSearchProbes - 1;
+    return 1;
+}
+
+// The first unknown midpoint (all paths start there).
+KVQ_HD inline double search_first_unknown(const SearchState &s) { return 0.5 * (s.lo + s.hi); }
+
+// Path of lane L: writes the unknown midpoints it meets into probe[id].
+KVQ_HD inline void search_path(const SearchState &s, int L, double *probe) {
+    double a = s.lo, b = s.hi;
+    int u = 0, pre = 0;
+    for (int dep = s.step; dep < kSearchSteps && u < 5; ++dep) {
+        const double mid = 0.5 * (a + b);
+        int k = search_known(s, mid);
+        if (k < 0) {
+            probe[(1 << u) - 1 + pre] = mid;
+            k = ((L >> (4 - u)) & 1) ? 0 : 1;   // bit 1: take the infeasible branch
+            pre = 2 * pre + (k ? 0 : 1);
+            ++u;
+        }
+        if (k) b = mid; else a = mid;
+    }
+}
+
+// Copy every field but the probe array.
+KVQ_HD inline void search_copy_scalars(SearchState &d, const SearchState &s) {
+    d.hi0 = s.hi0; d.lo = s.lo; d.hi = s.hi; d.xa = s.xa; d.xb = s.xb; d.R_xb = s.R_xb;
+    d.lambda = s.lambda; d.phase = s.phase; d.step = s.step; d.nprobe = s.nprobe;
+    d.xa_probe = s.xa_probe; d.xb_probe = s.xb_probe; d.infeasible = s.infeasible;
+    d.rounds = s.rounds;
+}
+
+// Single-thread version (host tests).
+KVQ_HD inline void search_update(SearchState &s, const double *R, double B) {
+    int ib = -1, ia = -1;
+    double vb = INFINITY, va = -INFINITY, Rb = 0.0;
+    for (int p = 0; p < s.nprobe; ++p) {
+        const double v = search_probe(s, p);
+        if (R[p] <= B && v < vb) { vb = v; ib = p; Rb = R[p]; }
+    }
+    const double xb_next = (ib >= 0 && vb < s.xb) ? vb : s.xb;
+    for (int p = 0; p < s.nprobe; ++p) {
+        const double v = search_probe(s, p);
+        if (!(R[p] <= B) && v > va && v < xb_next) { va = v; ia = p; }
+    }
+    search_window(s, vb, ib, Rb, va, ia);
+    if (search_advance(s, R, B)) {
+        double probe[kSearchProbes];
+        const double first = search_first_unknown(s);
+        for (int p = 0; p < kSearchProbes; ++p) probe[p] = first;
+        for (int L = 0; L < kSearchProbes; ++L) search_path(s, L, probe);
+        for (int p = 0; p < kSearchProbes; ++p) s.probe[p] = probe[p];
+    }
+}
+
+}  // namespace kvq
