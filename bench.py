@@ -42,7 +42,7 @@ WORKLOAD_DESC = ("Llama-3-8B-shaped single-layer prefill: K and V, 8 KV heads x 
                  "128 dims fp16 (S=16 streams); K = N(0,1) x per-channel lognormal(0,0.5) with 4 "
                  "outlier channels x10, V = Student-t(5); blocks = head x 32 tokens (4096 blocks "
                  "of 4096), s=16, B=2.5 bits/entry, seed 0")
-CPU_SAMPLE_BLOCKS = 192
+CPU_SAMPLE_BLOCKS = 4096
 
 
 def peaks():
@@ -138,8 +138,9 @@ def cpu_baseline(w, x_np, budget_per_entry, nblocks=CPU_SAMPLE_BLOCKS, seed=0):
     oracle.quantize(sl, w.G, r["codebook"], r["k"], seed, 0)
     dt = time.perf_counter() - t0
     return sl.nbytes / dt / 1e9, dt, threads, (
-        "%d blocks (%d K + %d V slabs of 32 tokens x 128) of the workload, full path at the same "
-        "bits/entry; %d bytes" % (len(sel), per, per, sl.nbytes))
+        "%d blocks (%d K + %d V slabs of 32 tokens x 128; all of them when %d) of the workload, "
+        "full path (stats, 40-step bisection at the same bits/entry, quantize); %d bytes"
+        % (len(sel), per, per, w.nblocks, sl.nbytes))
 
 
 def run_reference(args, rank, world):
@@ -179,7 +180,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-blocks", type=int, default=CPU_SAMPLE_BLOCKS)
+    ap.add_argument("--ref-blocks", type=int, default=1024)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -336,11 +337,21 @@ def main():
     kern["stats_cold_frac_hbm"] = kern["stats_cold_GBps"] / hbm
     shares = {"stats": mean(t_stats), "allocate": mean(t_alloc), "quantize": mean(t_quant)}
     dominant = max(shares, key=shares.get)
+    clk = clk_summary = clk.summary()
+    sm_mhz = clk_summary["sm_mhz"] or 2032.0
+    rep = kvq.kvq_allocate_report(buf.workspace)
+    kern["search_rounds"] = rep["rounds"]
+    kern["search_active_blocks"] = rep["active"]
+    # exact DP of one block at one lambda: 680 (i < j < l) level triples, one
+    # fp32 multiply-add and one min each
+    dp_ops = sum(rep["active"]) * 32 * 680 * 2
     if dominant == "allocate":
-        roof = {"kernel": "kvq_allocate (search rounds)", "bound": "alu",
-                "achieved": None, "peak": None, "unit": "TFLOP/s", "frac": None,
-                "traffic": None, "note": "see DESIGN.md: the lambda search is ALU/latency bound; "
-                "HBM kernels listed under kernels"}
+        peak = 148 * 128 * sm_mhz * 1e6 / 1e12          # fp32 lane ops, T/s
+        a = dp_ops / (mean(t_alloc) * 1e-3) / 1e12
+        roof = {"kernel": "kvq_allocate (search rounds)", "bound": "alu", "achieved": a,
+                "peak": peak, "unit": "T fp32 lane-op/s", "frac": a / peak, "traffic": None,
+                "work": "%d DP block-lambda evaluations x 680 triples x 2 ops" % (sum(rep["active"]) * 32),
+                "peak_source": "148 SMs x 128 fp32 lanes x median SM clock"}
     elif dominant == "stats":
         a = kern["stats_cold_GBps"]
         roof = {"kernel": "kvq_stats", "bound": "hbm", "achieved": a, "peak": hbm, "unit": "GB/s",
@@ -372,7 +383,7 @@ def main():
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
-            "clocks": clk.summary(),
+            "clocks": clk_summary,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -74,7 +74,7 @@ typedef struct kvq_layout {
 /* Number of blocks S * (T/32) * (D/group); -1 if the layout is invalid. */
 int64_t kvq_num_blocks(kvq_layout L);
 
-/* Bytes of the per-block statistics table written by kvq_stats (384 bytes per
+/* Bytes of the statistics buffer written by kvq_stats (256 + 4800 bytes per
  * block); 0 if the layout is invalid. */
 size_t kvq_stats_bytes(kvq_layout L);
 
@@ -91,9 +91,11 @@ size_t kvq_workspace_bytes(kvq_layout L, int s);
  *           statistics at 0-based sorted ranks floor((j(d-1)+8)/16),
  *           j = 0..16 (minimum and maximum included), equal values merged.
  *   stats   device, kvq_stats_bytes(L) bytes, written: per block the merged
- *           candidates and, for each gap between consecutive candidates, the
- *           count and first moments of the entries in it.  Its layout is
- *           private to this library; pass it to kvq_allocate unchanged.
+ *           candidates, for each gap between consecutive candidates the count
+ *           and first moments of the entries in it, and the block's
+ *           lambda-independent interval distortions and entropy terms.  Its
+ *           layout is private to this library; pass it to kvq_allocate
+ *           unchanged.
  *   status  device int32, set to KVQ_OK, or KVQ_ERR_NONFINITE if any entry is
  *           NaN or infinite (the results of such blocks are unspecified).
  */
@@ -165,6 +167,26 @@ int kvq_quantize(const uint16_t *x, kvq_layout L, const float *codebook,
  */
 int kvq_dequantize(const uint8_t *codes, const float *codebook, kvq_layout L,
                    uint16_t *y, void *stream);
+
+/*
+ * kvq_allocate_report -- what the last kvq_allocate on this workspace did
+ * (diagnostics; no counterpart on the method's page).  Synchronous: waits
+ * for the copy of the control block to the host.
+ *   rounds     rounds of DP evaluations the lambda search ran (each round
+ *              evaluates every block whose rate can still change at up to
+ *              32 lambdas, one per lane)
+ *   active[i]  blocks evaluated in round i (i < 16)
+ *   lambda, xa, xb  the answer, and the largest infeasible / smallest
+ *              feasible lambda evaluated (the codebooks are the choice at xb)
+ *   steps      bisection steps taken (40 unless lambda = 0 or infeasible)
+ */
+typedef struct kvq_report {
+    int32_t rounds;
+    int32_t steps;
+    uint32_t active[16];
+    double lambda, xa, xb;
+} kvq_report;
+int kvq_allocate_report(const void *workspace, kvq_report *report);
 
 /* Text of a status code. */
 const char *kvq_status_string(int status);

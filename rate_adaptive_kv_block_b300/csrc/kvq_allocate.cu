@@ -9,9 +9,9 @@
 //
 // Kernels (all on the caller's stream, no host synchronisation):
 //   ctrl_init      reset the control word in the workspace
-//   tables         per block, from the stats row: the lambda-independent DP
-//                  tables (interval distortion, entropy terms), in "slot"
-//                  space (see kvq_internal.cuh); max_r (c_max - c_min)^2
+//   (the lambda-independent DP tables of every block -- interval distortion
+//   and entropy terms in "slot" space, see kvq_internal.cuh -- come from
+//   kvq_stats, with max_r (c_max - c_min)^2 in the stats header)
 //   search_round   one warp per block, one lane per probe lambda: each lane
 //                  runs the whole exact DP at its own lambda, so the warp
 //                  evaluates 32 lambdas with no cross-lane traffic and the
@@ -34,7 +34,6 @@
 
 namespace kvq {
 
-constexpr int kTablesWarps = 4;
 constexpr int kRoundWarps = 4;        // s >= 16: DP path A only
 constexpr int kRoundWarpsGen = 2;     // s < 16: path B possible
 constexpr int kEmitWarps = 4;
@@ -42,13 +41,13 @@ constexpr int kEmitWarps = 4;
 // ---------------------------------------------------------------- workspace
 struct Workspace {
     Ctrl *ctrl;
-    float *tables;        // [nblk][kTblStride]
     float *rates;         // [nblk][32]   d_r H_r per probe (last round)
     uint32_t *masks;      // [nblk][32]   chain per probe (last round)
-    float *rate_lo;       // [nblk]       d_r H_r at lo
-    float *rate_hi;       // [nblk]       d_r H_r at hi
-    uint32_t *mask_hi;    // [nblk]       chain at hi
-    uint8_t *act;         // [nblk]       evaluated in the last round
+    float *rate_lo;       // [nblk]       d_r H_r at xa
+    float *rate_hi;       // [nblk]       d_r H_r at xb
+    uint32_t *mask_hi;    // [nblk]       chain at xb
+    int32_t *evr;         // [nblk]       round that last evaluated the block
+    int32_t *list;        // [2][nblk]    candidate lists (ping-pong)
     double *epartial;     // [emit CTAs]
 };
 
@@ -57,11 +56,11 @@ static size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 size_t workspace_bytes(int64_t nb, int s) {
     (void)s;
     size_t b = align_up(sizeof(Ctrl));
-    b += align_up((size_t)nb * kTblStride * sizeof(float));
     b += align_up((size_t)nb * 32 * sizeof(float));
     b += align_up((size_t)nb * 32 * sizeof(uint32_t));
     b += 3 * align_up((size_t)nb * sizeof(float));
-    b += align_up((size_t)nb);
+    b += align_up((size_t)nb * sizeof(int32_t));
+    b += align_up((size_t)nb * 2 * sizeof(int32_t));
     b += align_up((size_t)((nb + kEmitWarps - 1) / kEmitWarps) * sizeof(double));
     return b;
 }
@@ -71,8 +70,6 @@ static Workspace carve(void *base, int64_t nb) {
     Workspace w;
     w.ctrl = reinterpret_cast<Ctrl *>(p);
     p += align_up(sizeof(Ctrl));
-    w.tables = reinterpret_cast<float *>(p);
-    p += align_up((size_t)nb * kTblStride * sizeof(float));
     w.rates = reinterpret_cast<float *>(p);
     p += align_up((size_t)nb * 32 * sizeof(float));
     w.masks = reinterpret_cast<uint32_t *>(p);
@@ -83,150 +80,39 @@ static Workspace carve(void *base, int64_t nb) {
     p += align_up((size_t)nb * sizeof(float));
     w.mask_hi = reinterpret_cast<uint32_t *>(p);
     p += align_up((size_t)nb * sizeof(uint32_t));
-    w.act = reinterpret_cast<uint8_t *>(p);
-    p += align_up((size_t)nb);
+    w.evr = reinterpret_cast<int32_t *>(p);
+    p += align_up((size_t)nb * sizeof(int32_t));
+    w.list = reinterpret_cast<int32_t *>(p);
+    p += align_up((size_t)nb * 2 * sizeof(int32_t));
     w.epartial = reinterpret_cast<double *>(p);
     return w;
 }
 
 // ---------------------------------------------------------------- ctrl init
-__global__ void ctrl_init_kernel(Ctrl *c, double budget, double eta, int mode,
-                                 const double *lambda_in) {
+// pilot round over 1/16 of the blocks when there are at least this many
+constexpr int64_t kPilotMinBlocks = 1024;
+constexpr int kPilotStride = 16;
+
+__global__ void ctrl_init_kernel(Ctrl *c, const StatsHeader *hdr, double budget, double eta,
+                                 int mode, const double *lambda_in, int64_t nb) {
     if (threadIdx.x != 0) return;
     search_init(c->s);
+    c->nb = nb;
+    if (mode != KVQ_SUBGRADIENT && nb >= kPilotMinBlocks) search_set_pilot(c->s, nb, kPilotStride);
     c->budget = budget;
     c->eta = eta;
     c->fixed = (mode == KVQ_SUBGRADIENT) ? 1 : 0;
     c->lambda_fixed = c->fixed ? *lambda_in : 0.0;
-    c->hi0_bits = 0ull;
+    c->hi0_bits = hdr->hi0_bits;
     c->status = KVQ_OK;
-    c->flags = 0;
+    c->flags = (int32_t)hdr->flags;
     c->mode = mode;
     c->ticket = 0u;
     c->ticket_emit = 0u;
     for (int i = 0; i < 32; ++i) c->acc[i] = 0ull;
-}
-
-// -------------------------------------------------------------------- tables
-// Decode of a padded hh entry: (i, j, l) packed as i | j << 8 | l << 16
-// (l = 17 marks padding), and of a padded Dp entry: j | l << 8.
-struct DecodeTables {
-    uint32_t trip[kHHFloats];
-    uint32_t pair[kDpFloats];
-};
-constexpr DecodeTables make_decode() {
-    DecodeTables t{};
-    for (int j = 1; j < 16; ++j)
-        for (int i = 0; i < j; ++i)
-            for (int k = 0; k < pad4(16 - j); ++k) {
-                const int l = j + 1 + k;
-                t.trip[trip_off(i, j) + k] = (uint32_t)i | ((uint32_t)j << 8) | ((uint32_t)(l < 17 ? l : 17) << 16);
-            }
-    for (int j = 0; j < 16; ++j)
-        for (int k = 0; k < pad4(16 - j); ++k) {
-            const int l = j + 1 + k;
-            t.pair[dp_off(j) + k] = (uint32_t)j | ((uint32_t)(l < 17 ? l : 17) << 8);
-        }
-    return t;
-}
-__device__ constexpr DecodeTables kDecode = make_decode();
-
-__device__ __forceinline__ float hterm(float M, float inv_d) {
-    // entropy term of a level with expected count M out of d: -M log2(M/d)
-    return M > 0.f ? -M * log2f(M * inv_d) : 0.f;
-}
-
-__global__ void __launch_bounds__(kTablesWarps * 32)
-tables_kernel(const StatsRow *__restrict__ stats, int64_t nb, float *__restrict__ tables,
-              Ctrl *__restrict__ ctrl) {
-    __shared__ float sRow[kTablesWarps][96];
-    __shared__ float sDp[kTablesWarps][kPairs];
-    __shared__ float sUp[kTablesWarps][kPairs];
-    __shared__ float sDn[kTablesWarps][kPairs];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t b = (int64_t)blockIdx.x * kTablesWarps + w;
-    if (b >= nb) return;
-    const float *src = reinterpret_cast<const float *>(stats + b);
-    for (int i = lane; i < 96; i += 32) sRow[w][i] = src[i];
-    __syncwarp();
-    const float *row = sRow[w];
-    const int mp = min(max(__float_as_int(row[17]), 1), kCand);
-    const int flags = __float_as_int(row[18]);
-    const int d = __float_as_int(row[19]);
-    const float inv_d = 1.0f / (float)d;
-    const float INF = __int_as_float(0x7f800000);
-    // candidate index -> slot
-    auto slot_of = [&](int t) { return t == mp - 1 ? 16 : t; };
-
-    for (int i = lane; i < kPairs; i += 32) {
-        sDp[w][i] = INF;
-        sUp[w][i] = 0.f;
-        sDn[w][i] = 0.f;
-    }
-    __syncwarp();
-    // pairs of real candidates P < Q: sums over the atoms P .. Q-1
-    const int npr = mp * (mp - 1) / 2;
-    for (int idx = lane; idx < npr; idx += 32) {
-        int P = 0, rem = idx;
-        while (rem >= mp - 1 - P) { rem -= mp - 1 - P; ++P; }
-        const int Q = P + 1 + rem;
-        const float a = row[P], bq = row[Q];
-        float Dv = 0.f, Us = 0.f, Ls = 0.f;
-        for (int p = P; p < Q; ++p) {
-            const float n = row[20 + p], s1 = row[36 + p], t1 = row[52 + p], e = row[68 + p];
-            const float A = row[p] - a, B = bq - row[p + 1];
-            Dv += n * A * B + A * t1 + B * s1 + e;
-            Us += s1 + n * A;
-            Ls += t1 + n * B;
-        }
-        const float W = bq - a;
-        const int sj = slot_of(P), sl = slot_of(Q);
-        const int o = pidx(sj, sl);
-        sDp[w][o] = Dv;
-        sUp[w][o] = Us / W;
-        sDn[w][o] = Ls / W;
-    }
-    __syncwarp();
-    float *tb = tables + b * kTblStride;
-    auto real = [&](int t) { return t < mp - 1 || t == 16; };
-    // Dp rows, padded
-    for (int idx = lane; idx < kDpFloats; idx += 32) {
-        const uint32_t dc = kDecode.pair[idx];
-        const int j = dc & 255, l = dc >> 8;
-        tb[kTblD + idx] = l < 17 ? sDp[w][pidx(j, l)] : INF;
-    }
-    // hh rows (slot space), padded
-    for (int idx = lane; idx < kHHFloats; idx += 32) {
-        const uint32_t dc = kDecode.trip[idx];
-        const int i = dc & 255, j = (dc >> 8) & 255, l = dc >> 16;
-        float v = 0.f;
-        if (l < 17 && mp > 1 && real(i) && real(j) && real(l))
-            v = hterm(sUp[w][pidx(i, j)] + sDn[w][pidx(j, l)], inv_d);
-        tb[kTblHH + idx] = v;
-    }
-    if (lane < 20) {
-        const int t = lane;
-        float h0 = 0.f, he = 0.f;
-        if (mp > 1 && t >= 1 && t < 17 && real(t)) h0 = hterm(sDn[w][pidx(0, t)], inv_d);
-        if (mp > 1 && t <= 15 && real(t)) he = hterm(sUp[w][pidx(t, 16)], inv_d);
-        tb[kTblH0 + t] = h0;
-        tb[kTblHend + t] = he;
-        float cv = 0.f;
-        if (mp == 1) cv = (t == 0) ? row[0] : 0.f;
-        else if (t < mp - 1) cv = row[t];
-        else if (t == 16) cv = row[mp - 1];
-        tb[kTblC + t] = cv;
-    }
-    if (lane == 0) {
-        tb[kTblHdr + 0] = __int_as_float(mp);
-        tb[kTblHdr + 1] = __int_as_float(d);
-        tb[kTblHdr + 2] = __int_as_float(flags);
-        tb[kTblHdr + 3] = 0.f;   // the row ends at kTblHdr + 3
-        const double wd = (double)row[mp - 1] - (double)row[0];
-        const double w2 = wd * wd;
-        if (w2 == w2) atomicMax(&ctrl->hi0_bits, (unsigned long long)__double_as_longlong(w2));
-        if (flags) atomicOr(&ctrl->flags, flags);
-    }
+    for (int i = 0; i < 16; ++i) c->active[i] = 0u;
+    c->Rxb_fx = 0;
+    c->cnt[0] = c->cnt[1] = 0u;
 }
 
 // ------------------------------------------------------- probe lambda values
@@ -234,9 +120,10 @@ __device__ __forceinline__ double probe_lambda(const Ctrl *c, int lane) {
     if (c->fixed) return c->lambda_fixed;
     const int ph = c->s.phase;
     const double hi0 = __longlong_as_double((long long)c->hi0_bits);
-    if (ph == kSearchBracket) {
+    if (ph == kSearchBracket || ph == kSearchPilot) {
         if (lane == 0) return 0.0;
         if (lane <= kSearchFirstDoublings) return ldexp(hi0, lane - 1);
+        if (ph == kSearchBracket && c->s.have_grid) return c->s.probe[lane];
         return search_grid(hi0, lane - kSearchFirstDoublings);
     }
     if (ph == kSearchDouble) {
@@ -489,43 +376,61 @@ struct RoundCfg {
     static constexpr int kStateFloats = (GENERAL ? 3 * kPairs : kPairs + 17) * 32;
     static constexpr size_t kSmem =
         (size_t)kWarps * (kTblStride + kStateFloats) * sizeof(float) +
-        (size_t)kWarps * 32 * sizeof(float) + (size_t)kWarps * 32 * sizeof(float);
+        (size_t)kWarps * 32 * sizeof(long long) + (size_t)kWarps * 32 * sizeof(float);
 };
 
+// One round.  Persistent: the grid's warps take the round's blocks in turn
+// (all blocks in the bracket rounds, a sample in the pilot round, in the walk
+// only the blocks evaluated in the previous round -- a block that was not
+// is constant across the window and stays so).  Each lane accumulates, per
+// probe, the change of its blocks' d_r H_r against their value at xb, in
+// fixed point; the control adds the sums to the total at xb.
 template <bool GENERAL>
 __global__ void __launch_bounds__(RoundCfg<GENERAL>::kWarps * 32)
 search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restrict__ ctrl,
                     float *__restrict__ rates, uint32_t *__restrict__ masks,
                     float *__restrict__ rate_lo, float *__restrict__ rate_hi,
-                    uint32_t *__restrict__ mask_hi, uint8_t *__restrict__ act) {
+                    uint32_t *__restrict__ mask_hi, int32_t *__restrict__ evr,
+                    int32_t *__restrict__ list) {
     using Cfg = RoundCfg<GENERAL>;
     constexpr int W = Cfg::kWarps;
     extern __shared__ __align__(16) float smem[];
     if (ctrl->s.phase == kSearchDone) return;
     const int fixed = ctrl->fixed, phase = ctrl->s.phase;
     const int xa_probe = ctrl->s.xa_probe, xb_probe = ctrl->s.xb_probe;
+    const int round = ctrl->s.rounds;
+    const bool walk = !fixed && phase == kSearchWalk;
+    const bool pilot = !fixed && phase == kSearchPilot;
+    const int stride = ctrl->s.pilot_stride;
+    const int32_t *lin = list + (size_t)(round & 1) * nb;
+    int32_t *lout = list + (size_t)((round + 1) & 1) * nb;
+    const int64_t nitems = walk ? (int64_t)ctrl->cnt[round & 1]
+                                : pilot ? (int64_t)ctrl->s.pilot_blocks : nb;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     float *sTbl = smem + w * kTblStride;
     float *sState = smem + W * kTblStride + w * Cfg::kStateFloats;
-    float *sRate = smem + W * (kTblStride + Cfg::kStateFloats);
-    float *sDiag = sRate + W * 32 + w * 32;
+    long long *sSum = reinterpret_cast<long long *>(smem + W * (kTblStride + Cfg::kStateFloats));
+    float *sDiag = reinterpret_cast<float *>(sSum + W * 32) + w * 32;
     __shared__ bool is_last;
-
-    const int64_t b = (int64_t)blockIdx.x * W + w;
-    float my_rate = 0.f;
-    if (b < nb) {
-        // carry the previous round's results at the new lo / hi
+    __shared__ uint32_t sAct;
+    if (threadIdx.x == 0) sAct = 0u;
+    const float lam = (float)probe_lambda(ctrl, lane);
+    long long my_sum = 0;
+    uint32_t my_act = 0;
+    for (int64_t it = (int64_t)blockIdx.x * W + w; it < nitems; it += (int64_t)gridDim.x * W) {
+        const int64_t b = walk ? (int64_t)lin[it] : pilot ? it * stride : it;
+        float rb = 0.f;
         bool active = true;
-        if (!fixed && phase == kSearchWalk) {
-            // carry the last round's results at the new window ends (lane 0
-            // alone touches the per-block state, then broadcasts)
-            float ra = 0.f, rb = 0.f;
+        if (walk) {
+            // the block was evaluated in the previous round: carry its results
+            // at the new window ends (lane 0 alone touches the per-block
+            // state, then broadcasts)
+            float ra = 0.f;
             if (lane == 0) {
-                const bool was = act[b] != 0;
                 ra = rate_lo[b];
                 rb = rate_hi[b];
-                if (was && xa_probe >= 0) ra = rates[b * 32 + xa_probe];
-                if (was && xb_probe >= 0) {
+                if (xa_probe >= 0) ra = rates[b * 32 + xa_probe];
+                if (xb_probe >= 0) {
                     rb = rates[b * 32 + xb_probe];
                     mask_hi[b] = masks[b * 32 + xb_probe];
                 }
@@ -537,48 +442,51 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
             // the rate is non-increasing in lambda: equal at both window ends
             // means constant inside the window, and so is the chosen chain
             active = ra != rb;
-            my_rate = rb;
         }
-        if (lane == 0) act[b] = active ? 1 : 0;
-        if (active) {
-            const float4 *src = reinterpret_cast<const float4 *>(tables + b * kTblStride);
-            float4 *dst = reinterpret_cast<float4 *>(sTbl);
-            for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
-            __syncwarp();
-            const float lam = (float)probe_lambda(ctrl, lane);
-            const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
-            float rate;
-            uint32_t mask;
-            if (mp <= 1) {
-                rate = 0.f;
-                mask = 1u;
+        if (!active) continue;
+        const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
+        float4 *dst = reinterpret_cast<float4 *>(sTbl);
+        for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
+        __syncwarp();
+        const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
+        float rate;
+        uint32_t mask;
+        if (mp <= 1) {
+            rate = 0.f;
+            mask = 1u;
+        } else {
+            const int C = mp > s ? mp - s : 0;
+            if (!GENERAL || C == 0 || (C == 1 && mp == 17)) {
+                dp_a_diag(sTbl, sDiag, lane);
+                dp_path_a(sTbl, lam, C, sState, sState + kPairs * 32, sDiag, lane, rate, mask);
             } else {
-                const int C = mp > s ? mp - s : 0;
-                if (!GENERAL || C == 0 || (C == 1 && mp == 17)) {
-                    dp_a_diag(sTbl, sDiag, lane);
-                    dp_path_a(sTbl, lam, C, sState, sState + kPairs * 32, sDiag, lane, rate,
-                              mask);
-                } else {
-                    dp_path_b(sTbl, lam, s, sState, sState + kPairs * 32,
-                              reinterpret_cast<uint32_t *>(sState + 2 * kPairs * 32), lane, rate,
-                              mask);
-                }
+                dp_path_b(sTbl, lam, s, sState, sState + kPairs * 32,
+                          reinterpret_cast<uint32_t *>(sState + 2 * kPairs * 32), lane, rate,
+                          mask);
             }
-            rates[b * 32 + lane] = rate;
-            masks[b * 32 + lane] = mask;
-            my_rate = rate;
         }
+        rates[b * 32 + lane] = rate;
+        masks[b * 32 + lane] = mask;
+        my_sum += llrint((double)rate * kRateScale) - llrint((double)rb * kRateScale);
+        if (lane == 0) {
+            evr[b] = round;
+            if (!pilot) lout[atomicAdd(&ctrl->cnt[(round + 1) & 1], 1u)] = (int32_t)b;
+        }
+        ++my_act;
+        __syncwarp();
     }
-    sRate[w * 32 + lane] = my_rate;
+    sSum[w * 32 + lane] = my_sum;
     __syncthreads();
+    if (lane == 0 && my_act) atomicAdd(&sAct, my_act);
     if (threadIdx.x < 32) {
-        double sum = 0.0;
-        for (int k = 0; k < W; ++k) sum += (double)sRate[k * 32 + threadIdx.x];
-        atomicAdd(&ctrl->acc[threadIdx.x], (unsigned long long)llrint(sum * kRateScale));
+        long long sum = 0;
+        for (int k = 0; k < W; ++k) sum += sSum[k * 32 + threadIdx.x];
+        if (sum) atomicAdd(&ctrl->acc[threadIdx.x], (unsigned long long)sum);
         __threadfence();
     }
     __syncthreads();
     if (threadIdx.x == 0) {
+        if (sAct) atomicAdd(&ctrl->active[min(round, 15)], sAct);
         const unsigned t = atomicAdd(&ctrl->ticket, 1u);
         is_last = (t == gridDim.x - 1);
     }
@@ -588,9 +496,12 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
 
     // ---- last CTA: read the sums, advance the search
     __shared__ double R[32];
+    __shared__ long long Rfx[32];
+    const long long base = walk ? ctrl->Rxb_fx : 0;
     if (threadIdx.x < 32) {
-        const unsigned long long a = atomicExch(&ctrl->acc[threadIdx.x], 0ull);
-        R[threadIdx.x] = (double)a / kRateScale;
+        const long long a = (long long)atomicExch(&ctrl->acc[threadIdx.x], 0ull);
+        Rfx[threadIdx.x] = base + a;
+        R[threadIdx.x] = (double)(base + a) / kRateScale;
     }
     __syncthreads();
 
@@ -613,6 +524,14 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
                 sS.phase = kSearchDone;
                 sS.rounds += 1;
             }
+        } else if (sS.phase == kSearchPilot) {
+            __shared__ double sEst;
+            if (L == 0) {
+                sS.hi0 = __longlong_as_double((long long)ctrl->hi0_bits);
+                sEst = search_pilot_estimate(sS, R, B, ctrl->nb);
+            }
+            __syncwarp();
+            if (sS.have_grid && L > kSearchFirstDoublings) sS.probe[L] = search_pilot_probe(sEst, L);
         } else {
             if (L == 0) sS.hi0 = __longlong_as_double((long long)ctrl->hi0_bits);
             __syncwarp();
@@ -650,7 +569,9 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
         }
         __syncwarp();
         if (L == 0) {
+            if (!ctrl->fixed && sS.xb_probe >= 0) ctrl->Rxb_fx = Rfx[sS.xb_probe];
             search_copy_scalars(ctrl->s, sS);
+            ctrl->cnt[round & 1] = 0u;     // consumed; next round appends here
             ctrl->ticket = 0u;
         }
         ctrl->s.probe[L] = sS.probe[L];
@@ -668,21 +589,22 @@ __global__ void __launch_bounds__(kEmitWarps * 32)
 emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctrl,
             const float *__restrict__ rates, const uint32_t *__restrict__ masks,
             const float *__restrict__ rate_hi, const uint32_t *__restrict__ mask_hi,
-            const uint8_t *__restrict__ act, double *__restrict__ epartial,
+            const int32_t *__restrict__ evr, double *__restrict__ epartial,
             float *__restrict__ codebook, uint8_t *__restrict__ kout, float *__restrict__ Dr,
             float *__restrict__ Hr, double *__restrict__ totals, double *__restrict__ lambda_out,
             int32_t *__restrict__ status) {
     const int xb_probe = ctrl->s.xb_probe;
+    const int last_round = ctrl->s.rounds - 1;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t b = (int64_t)blockIdx.x * kEmitWarps + w;
     __shared__ double sD[kEmitWarps];
     __shared__ bool is_last;
     double Dblk = 0.0;
     if (b < nb) {
-        const float *tb = tables + b * kTblStride;
+        const float *tb = tables + b * kRecFloats + kRecTbl;
         uint32_t mask;
         float rate;
-        if (xb_probe >= 0 && act[b]) {
+        if (xb_probe >= 0 && evr[b] == last_round) {
             mask = masks[b * 32 + xb_probe];
             rate = rates[b * 32 + xb_probe];
         } else {
@@ -783,34 +705,51 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
         return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
     }
     Workspace ws = carve(workspace, nb);
-    ctrl_init_kernel<<<1, 32, 0, st>>>(ws.ctrl, budget, eta, mode, lambda);
-    const unsigned tgrid = (unsigned)((nb + kTablesWarps - 1) / kTablesWarps);
-    tables_kernel<<<tgrid, kTablesWarps * 32, 0, st>>>(static_cast<const StatsRow *>(stats), nb,
-                                                       ws.tables, ws.ctrl);
-    // bracket + (rarely) the extra doublings + at most 8 walk rounds (each
-    // takes >= 5 bisection steps); rounds after the search is done return at once
-    const int rounds = (mode == KVQ_SUBGRADIENT) ? 1 : 2 + kSearchSteps / 5;
+    const StatsHeader *hdr = static_cast<const StatsHeader *>(stats);
+    const float *recs = reinterpret_cast<const float *>(static_cast<const char *>(stats) +
+                                                        sizeof(StatsHeader));
+    ctrl_init_kernel<<<1, 32, 0, st>>>(ws.ctrl, hdr, budget, eta, mode, lambda, nb);
+    const int rounds = (mode == KVQ_SUBGRADIENT) ? 1 : 3 + kSearchSteps / 5;
     const bool general = s < 16;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     for (int r = 0; r < rounds; ++r) {
+        // persistent grid: two CTAs per SM (the shared-memory limit)
         if (general) {
             using Cfg = RoundCfg<true>;
-            const unsigned grid = (unsigned)((nb + Cfg::kWarps - 1) / Cfg::kWarps);
+            const int64_t need = (nb + Cfg::kWarps - 1) / Cfg::kWarps;
+            const unsigned grid = (unsigned)(need < 2 * sms ? need : 2 * sms);
             search_round_kernel<true><<<grid, Cfg::kWarps * 32, Cfg::kSmem, st>>>(
-                ws.tables, nb, s, ws.ctrl, ws.rates, ws.masks, ws.rate_lo, ws.rate_hi, ws.mask_hi,
-                ws.act);
+                recs, nb, s, ws.ctrl, ws.rates, ws.masks, ws.rate_lo, ws.rate_hi, ws.mask_hi,
+                ws.evr, ws.list);
         } else {
             using Cfg = RoundCfg<false>;
-            const unsigned grid = (unsigned)((nb + Cfg::kWarps - 1) / Cfg::kWarps);
+            const int64_t need = (nb + Cfg::kWarps - 1) / Cfg::kWarps;
+            const unsigned grid = (unsigned)(need < 2 * sms ? need : 2 * sms);
             search_round_kernel<false><<<grid, Cfg::kWarps * 32, Cfg::kSmem, st>>>(
-                ws.tables, nb, s, ws.ctrl, ws.rates, ws.masks, ws.rate_lo, ws.rate_hi, ws.mask_hi,
-                ws.act);
+                recs, nb, s, ws.ctrl, ws.rates, ws.masks, ws.rate_lo, ws.rate_hi, ws.mask_hi,
+                ws.evr, ws.list);
         }
     }
     const unsigned egrid = (unsigned)((nb + kEmitWarps - 1) / kEmitWarps);
-    emit_kernel<<<egrid, kEmitWarps * 32, 0, st>>>(ws.tables, nb, ws.ctrl, ws.rates, ws.masks,
-                                                ws.rate_hi, ws.mask_hi, ws.act, ws.epartial,
+    emit_kernel<<<egrid, kEmitWarps * 32, 0, st>>>(recs, nb, ws.ctrl, ws.rates, ws.masks,
+                                                ws.rate_hi, ws.mask_hi, ws.evr, ws.epartial,
                                                 codebook, k, Dr, Hr, totals, lambda, status);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+int allocate_report(const void *workspace, kvq_report *r) {
+    Ctrl c;
+    if (cudaMemcpy(&c, workspace, sizeof(Ctrl), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    r->rounds = c.s.rounds;
+    for (int i = 0; i < 16; ++i) r->active[i] = c.active[i];
+    r->lambda = c.s.lambda;
+    r->xa = c.s.xa;
+    r->xb = c.s.xb;
+    r->steps = c.s.step;
+    return KVQ_OK;
 }
 
 int allocate_init() {

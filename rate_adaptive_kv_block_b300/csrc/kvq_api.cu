@@ -17,6 +17,7 @@ int launch_dequantize(const uint8_t *codes, const float *codebook, const kvq_lay
                       uint16_t *y, cudaStream_t st);
 size_t workspace_bytes(int64_t nb, int s);
 int allocate_init();
+int allocate_report(const void *workspace, kvq_report *r);
 
 static bool layout_ok(const kvq_layout &L) {
     if (L.S < 0 || L.T < 0 || L.T % 32 != 0) return false;
@@ -53,7 +54,8 @@ extern "C" {
 int64_t kvq_num_blocks(kvq_layout L) { return layout_ok(L) ? num_blocks(L) : -1; }
 
 size_t kvq_stats_bytes(kvq_layout L) {
-    return layout_ok(L) ? (size_t)num_blocks(L) * sizeof(StatsRow) : 0;
+    return layout_ok(L) ? sizeof(StatsHeader) + (size_t)num_blocks(L) * kRecFloats * sizeof(float)
+                        : 0;
 }
 
 size_t kvq_workspace_bytes(kvq_layout L, int s) {
@@ -115,6 +117,11 @@ int kvq_dequantize(const uint8_t *codes, const float *codebook, kvq_layout L, ui
         if (L.S * (L.T / 32) > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
     }
     return launch_dequantize(codes, codebook, L, y, static_cast<cudaStream_t>(stream));
+}
+
+int kvq_allocate_report(const void *workspace, kvq_report *report) {
+    if (!workspace || !report) return KVQ_ERR_INVALID_ARG;
+    return allocate_report(workspace, report);
 }
 
 const char *kvq_status_string(int status) {

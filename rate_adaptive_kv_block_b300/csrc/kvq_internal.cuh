@@ -79,6 +79,17 @@ constexpr int kHHFloats = trip_base(16);       // 880
 static_assert(kDpFloats == 160 && kHHFloats == 880, "padded table sizes");
 static_assert(pidx(15, 16) == kPairs - 1, "pair count");
 
+// Output of kvq_stats: a 256-byte header, then one 4800-byte record per
+// block: the stats row (96 floats) and the DP tables (1104 floats).
+struct StatsHeader {
+    unsigned long long hi0_bits;   // max_r (c_max - c_min)^2 (double bits, atomic max)
+    uint32_t flags;                // OR of the block flags
+    uint32_t pad[61];
+};
+static_assert(sizeof(StatsHeader) == 256, "stats header is 256 bytes");
+constexpr int kRecFloats = 1200;
+constexpr int kRecTbl = 96;
+
 constexpr int kTblD = 0;
 constexpr int kTblHH = kTblD + kDpFloats;     // 160
 constexpr int kTblH0 = kTblHH + kHHFloats;    // 1040
@@ -87,6 +98,30 @@ constexpr int kTblC = kTblHend + 20;          // 1080: level value per slot
 constexpr int kTblHdr = kTblC + 20;           // 1100: m', d, flags (int bits)
 constexpr int kTblStride = 1104;              // floats per block (4416 B)
 static_assert(kTblStride % 4 == 0 && kTblHH % 4 == 0 && kTblH0 % 4 == 0, "16-byte rows");
+
+// Decode of a padded hh entry: (i, j, l) packed as i | j << 8 | l << 16
+// (l = 17 marks padding), and of a padded Dp entry: j | l << 8.
+struct DecodeTables {
+    uint32_t trip[kHHFloats];
+    uint32_t pair[kDpFloats];
+};
+constexpr DecodeTables make_decode() {
+    DecodeTables t{};
+    for (int j = 1; j < 16; ++j)
+        for (int i = 0; i < j; ++i)
+            for (int k = 0; k < pad4(16 - j); ++k) {
+                const int l = j + 1 + k;
+                t.trip[trip_off(i, j) + k] =
+                    (uint32_t)i | ((uint32_t)j << 8) | ((uint32_t)(l < 17 ? l : 17) << 16);
+            }
+    for (int j = 0; j < 16; ++j)
+        for (int k = 0; k < pad4(16 - j); ++k) {
+            const int l = j + 1 + k;
+            t.pair[dp_off(j) + k] = (uint32_t)j | ((uint32_t)(l < 17 ? l : 17) << 8);
+        }
+    return t;
+}
+static __device__ constexpr DecodeTables kDecode = make_decode();
 
 // ---------------------------------------------------- allocation control
 // Lives at the start of the kvq_allocate workspace.
@@ -102,6 +137,12 @@ struct Ctrl {
     int32_t mode;
     uint32_t ticket;        // last-CTA-done counter of the search rounds
     uint32_t ticket_emit;   // same, emit kernel
+    uint32_t active[16];    // blocks evaluated in each round (diagnostics)
+    int64_t nb;             // blocks
+    // sum over all blocks of d_r H_r at xb, fixed point; the rounds of the
+    // walk add to it the change of each re-evaluated block
+    long long Rxb_fx;
+    uint32_t cnt[2];        // lengths of the two candidate lists
     // per-probe sum of d_r H_r over blocks, fixed point (2^-20 bit units):
     // integer adds are exact, so the sum does not depend on arrival order
     unsigned long long acc[32];

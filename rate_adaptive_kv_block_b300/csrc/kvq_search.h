@@ -40,6 +40,7 @@ constexpr int kSearchMaxDoublings = 30;
 constexpr int kSearchFirstDoublings = 3;       // hi0 * 2^0 .. 2^2 in round 0
 
 enum SearchPhase : int32_t {
+    kSearchPilot = 4,     // a sample of the blocks at the round-0 probes (estimate only)
     kSearchBracket = 0,   // round 0: 0, hi0 * 2^{0,1,2}, geometric grid
     kSearchDouble = 1,    // hi0 * 2^3 .. 2^30 (only if round 0 found no feasible hi)
     kSearchWalk = 2,      // bisection walk
@@ -60,6 +61,10 @@ struct SearchState {
     int32_t xb_probe;     // probe of the last round that became xb, or -1
     int32_t infeasible;
     int32_t rounds;
+    int32_t pilot_stride;     // pilot round: every pilot_stride-th block (0: no pilot)
+    int32_t pilot_blocks;     // blocks the pilot evaluated
+    int32_t have_grid;        // round 0 uses probe[4..31] (set by the pilot)
+    int32_t pad;
 };
 
 KVQ_HD inline void search_init(SearchState &s) {
@@ -76,6 +81,19 @@ KVQ_HD inline void search_init(SearchState &s) {
     s.xa_probe = s.xb_probe = -1;
     s.infeasible = 0;
     s.rounds = 0;
+    s.pilot_stride = 0;
+    s.pilot_blocks = 0;
+    s.have_grid = 0;
+    s.pad = 0;
+}
+
+// Start with a pilot round over every stride-th of nb blocks (stride <= 0: none).
+KVQ_HD inline void search_set_pilot(SearchState &s, int64_t nb, int stride) {
+    if (stride > 1 && nb >= 4 * (int64_t)stride) {
+        s.pilot_stride = stride;
+        s.pilot_blocks = (int32_t)((nb + stride - 1) / stride);
+        s.phase = kSearchPilot;
+    }
 }
 
 // hi0 * 2^(-1.5 k), from exact operations: a power-of-two scaling, times
@@ -85,11 +103,18 @@ KVQ_HD inline double search_grid(double hi0, int k) {
     return (k & 1) ? ldexp(hi0 * odd, -(3 * k - 1) / 2) : ldexp(hi0, -(3 * k) / 2);
 }
 
+// Fine grid of round 0 around an estimate: est * f^((2k - 27) / 27), k = 0..27
+KVQ_HD inline double search_fine(double est, int k) {
+    const double f = 1.35;
+    return est * pow(f, (double)(2 * k - 27) / 27.0);
+}
+
 // lambda evaluated by probe p this round
 KVQ_HD inline double search_probe(const SearchState &s, int p) {
-    if (s.phase == kSearchBracket) {
+    if (s.phase == kSearchBracket || s.phase == kSearchPilot) {
         if (p == 0) return 0.0;
         if (p <= kSearchFirstDoublings) return ldexp(s.hi0, p - 1);
+        if (s.phase == kSearchBracket && s.have_grid) return s.probe[p];
         return search_grid(s.hi0, p - kSearchFirstDoublings);
     }
     if (s.phase == kSearchDouble) {
@@ -201,16 +226,63 @@ KVQ_HD inline void search_path(const SearchState &s, int L, double *probe) {
     }
 }
 
+// Pilot round: estimate where R crosses B from the sample's rates (scaled to
+// all blocks); round 0 then puts its fine grid there.  Nothing is concluded
+// from the sample: the window only moves on evaluations of every block.
+// Returns the estimate, or 0 when there is none (round 0 keeps its default
+// grid).
+KVQ_HD inline double search_pilot_estimate(SearchState &s, const double *R, double B, int64_t nb) {
+    s.rounds += 1;
+    s.xa_probe = s.xb_probe = -1;
+    const double scale = (double)nb / (double)(s.pilot_blocks > 0 ? s.pilot_blocks : 1);
+    int ib = -1;
+    double vb = INFINITY, Rb = 0.0;
+    for (int p = 0; p < kSearchProbes; ++p) {
+        const double v = search_probe(s, p), r = R[p] * scale;
+        if (r <= B && v < vb) { vb = v; ib = p; Rb = r; }
+    }
+    int ia = -1;
+    double va = -1.0, Ra = 0.0;
+    for (int p = 0; p < kSearchProbes; ++p) {
+        const double v = search_probe(s, p), r = R[p] * scale;
+        if (!(r <= B) && v < vb && v > va) { va = v; ia = p; Ra = r; }
+    }
+    s.phase = kSearchBracket;
+    s.have_grid = 0;
+    if (ib <= 0 || !(vb > 0.0)) return 0.0;       // lambda = 0 likely, or no feasible probe
+    double est;
+    if (ia <= 0 || !(va > 0.0)) est = 0.5 * vb;
+    else {
+        const double t = (Ra - B) / (Ra - Rb);        // log-linear interpolation
+        est = va * pow(vb / va, t > 0.0 ? (t < 1.0 ? t : 1.0) : 0.0);
+    }
+    s.have_grid = 1;
+    return est;
+}
+
+// Probe p of round 0 around the estimate (p > kSearchFirstDoublings).
+KVQ_HD inline double search_pilot_probe(double est, int p) {
+    return search_fine(est, p - 1 - kSearchFirstDoublings);
+}
+
 // Copy every field but the probe array.
 KVQ_HD inline void search_copy_scalars(SearchState &d, const SearchState &s) {
     d.hi0 = s.hi0; d.lo = s.lo; d.hi = s.hi; d.xa = s.xa; d.xb = s.xb; d.R_xb = s.R_xb;
     d.lambda = s.lambda; d.phase = s.phase; d.step = s.step; d.nprobe = s.nprobe;
     d.xa_probe = s.xa_probe; d.xb_probe = s.xb_probe; d.infeasible = s.infeasible;
-    d.rounds = s.rounds;
+    d.rounds = s.rounds; d.pilot_stride = s.pilot_stride; d.pilot_blocks = s.pilot_blocks;
+    d.have_grid = s.have_grid;
 }
 
-// Single-thread version (host tests).
-KVQ_HD inline void search_update(SearchState &s, const double *R, double B) {
+// Single-thread version (host tests).  nb: number of blocks (pilot scaling).
+KVQ_HD inline void search_update(SearchState &s, const double *R, double B, int64_t nb = 0) {
+    if (s.phase == kSearchPilot) {
+        const double est = search_pilot_estimate(s, R, B, nb);
+        if (s.have_grid)
+            for (int p = 1 + kSearchFirstDoublings; p < kSearchProbes; ++p)
+                s.probe[p] = search_pilot_probe(est, p);
+        return;
+    }
     int ib = -1, ia = -1;
     double vb = INFINITY, va = -INFINITY, Rb = 0.0;
     for (int p = 0; p < s.nprobe; ++p) {

@@ -20,7 +20,9 @@
 // Inside a bin the value is affine in j (one binade quarter: fixed sign and
 // exponent), so the atom moments follow from those exact integer sums without
 // touching the entries again: half a warp per atom sums its bins with a
-// fixed-order tree.  Every fp32 term added is non-negative, so there is no cancellation.
+// fixed-order tree.  The CTA then builds the block's lambda-independent DP
+// tables (interval distortion and entropy terms, one entropy log2 per level
+// triple) and writes them with the stats row as the block's record.  Every fp32 term added is non-negative, so there is no cancellation.
 // Non-finite entries are the keys of the four lowest and four highest bins.
 #include "kvq_internal.cuh"
 
@@ -46,6 +48,7 @@ struct StatsSmem {
     float dc[17];
     int32_t mprime, nslots;
     float an[16], as1[16], at1[16], ae[16];
+    float pDp[kPairs], pUp[kPairs], pDn[kPairs];   // pair tables, slot space
 };
 
 __device__ __forceinline__ int block_excl_scan(int v, int32_t *warp_tot, int &total) {
@@ -94,8 +97,8 @@ __device__ __forceinline__ void add_piece(uint32_t b, int j0, int j1, uint32_t n
 
 template <int UNITS>
 __global__ void __launch_bounds__(kStatsThreads)
-stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsRow *__restrict__ out,
-             int32_t *__restrict__ status) {
+stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsHeader *__restrict__ hdr,
+             float *__restrict__ recs, int32_t *__restrict__ status) {
     __shared__ __align__(16) StatsSmem sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = L.group, D = L.D;
@@ -124,6 +127,11 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsRow *__restrict_
         for (int i = tid; i < 2 * kStatsWarps * 256 / 4; i += kStatsThreads) z[i] = make_uint4(0, 0, 0, 0);
         uint4 *z2 = reinterpret_cast<uint4 *>(&sm.l2[0][0]);
         for (int i = tid; i < 17 * 128 / 4; i += kStatsThreads) z2[i] = make_uint4(0, 0, 0, 0);
+        if (tid < kPairs) {
+            sm.pDp[tid] = __int_as_float(0x7f800000);   // +inf: no such pair
+            sm.pUp[tid] = 0.f;
+            sm.pDn[tid] = 0.f;
+        }
     }
     __syncthreads();
 
@@ -330,11 +338,42 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsRow *__restrict_
     }
     __syncthreads();
 
-    // ---- write the row (96 words); non-finite keys live in bins 0..3, 252..255
+    // ---- pair tables in slot space (candidates 0 .. m'-2 in slots 0 .., the
+    //      maximum in slot 16): for a = c_P < b = c_Q, over the atoms p of
+    //      [a, b) with A = c_p - a, B = b - c_{p+1}:
+    //        D = sum n A B + A t1 + B s1 + e      (sum of (b - x)(x - a))
+    //        Mup = sum (s1 + n A) / (b - a)        (expected count sent to b)
+    //        Mdn = sum (t1 + n B) / (b - a)        (expected count sent to a)
+    //      every term non-negative
+    const int npr = mp * (mp - 1) / 2;
+    if (tid < npr) {
+        int P = 0, rem = tid;
+        while (rem >= mp - 1 - P) { rem -= mp - 1 - P; ++P; }
+        const int Q = P + 1 + rem;
+        const float a = sm.dc[P], bq = sm.dc[Q];
+        float Dv = 0.f, Us = 0.f, Ls = 0.f;
+        for (int p = P; p < Q; ++p) {
+            const float n = sm.an[p], s1 = sm.as1[p], t1 = sm.at1[p], e = sm.ae[p];
+            const float A = sm.dc[p] - a, Bq = bq - sm.dc[p + 1];
+            Dv += n * A * Bq + A * t1 + Bq * s1 + e;
+            Us += s1 + n * A;
+            Ls += t1 + n * Bq;
+        }
+        const float W = bq - a;
+        const int sj = P == mp - 1 ? 16 : P, sl = Q == mp - 1 ? 16 : Q;
+        const int o = pidx(sj, sl);
+        sm.pDp[o] = Dv;
+        sm.pUp[o] = Us / W;
+        sm.pDn[o] = Ls / W;
+    }
+    __syncthreads();
+
+    // ---- the record: stats row, then the DP tables
+    //      (non-finite keys live in bins 0..3 and 252..255)
     const bool bad = (sm.cnt[0] | sm.cnt[1] | sm.cnt[2] | sm.cnt[3] | sm.cnt[252] | sm.cnt[253] |
                       sm.cnt[254] | sm.cnt[255]) != 0;
+    float *rec = recs + blk * kRecFloats;
     if (tid < 96) {
-        float *row = reinterpret_cast<float *>(out + blk);
         float v = 0.f;
         if (tid < 17) v = sm.dc[tid < mp ? tid : mp - 1];
         else if (tid == 17) v = __int_as_float(mp);
@@ -344,23 +383,65 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsRow *__restrict_
         else if (tid < 52) v = sm.as1[tid - 36];
         else if (tid < 68) v = sm.at1[tid - 52];
         else if (tid < 84) v = sm.ae[tid - 68];
-        row[tid] = v;
+        rec[tid] = v;
     }
-    if (tid == 0 && bad) atomicMax(status, (int32_t)KVQ_ERR_NONFINITE);
+    float *tb = rec + kRecTbl;
+    const float inv_d = 1.0f / (float)d;
+    auto real = [&](int t) { return t < mp - 1 || t == 16; };
+    auto hterm = [&](float M) { return M > 0.f ? -M * log2f(M * inv_d) : 0.f; };
+    for (int idx = tid; idx < kDpFloats; idx += kStatsThreads) {
+        const uint32_t dcd = kDecode.pair[idx];
+        const int j = dcd & 255, l = dcd >> 8;
+        tb[kTblD + idx] = l < 17 ? sm.pDp[pidx(j, l)] : __int_as_float(0x7f800000);
+    }
+    for (int idx = tid; idx < kHHFloats; idx += kStatsThreads) {
+        const uint32_t dcd = kDecode.trip[idx];
+        const int i = dcd & 255, j = (dcd >> 8) & 255, l = dcd >> 16;
+        float v = 0.f;
+        if (l < 17 && mp > 1 && real(i) && real(j) && real(l))
+            v = hterm(sm.pUp[pidx(i, j)] + sm.pDn[pidx(j, l)]);
+        tb[kTblHH + idx] = v;
+    }
+    if (tid < 20) {
+        const int t = tid;
+        float h0 = 0.f, he = 0.f;
+        if (mp > 1 && t >= 1 && t < 17 && real(t)) h0 = hterm(sm.pDn[pidx(0, t)]);
+        if (mp > 1 && t <= 15 && real(t)) he = hterm(sm.pUp[pidx(t, 16)]);
+        tb[kTblH0 + t] = h0;
+        tb[kTblHend + t] = he;
+        float cv = 0.f;
+        if (mp == 1) cv = (t == 0) ? sm.dc[0] : 0.f;
+        else if (t < mp - 1) cv = sm.dc[t];
+        else if (t == 16) cv = sm.dc[mp - 1];
+        tb[kTblC + t] = cv;
+    } else if (tid < 24) {
+        const int t = tid - 20;
+        tb[kTblHdr + t] = __int_as_float(t == 0 ? mp : t == 1 ? d : t == 2 ? (bad ? kFlagNonfinite : 0) : 0);
+    } else if (tid == 32) {
+        const double wd = (double)sm.dc[mp - 1] - (double)sm.dc[0];
+        const double w2 = wd * wd;
+        if (w2 == w2) atomicMax(&hdr->hi0_bits, (unsigned long long)__double_as_longlong(w2));
+        if (bad) {
+            atomicOr(&hdr->flags, (uint32_t)kFlagNonfinite);
+            atomicMax(status, (int32_t)KVQ_ERR_NONFINITE);
+        }
+    }
 }
 
 int launch_stats(const uint16_t *x, const kvq_layout &L, void *stats, int32_t *status,
                  cudaStream_t st) {
     const int64_t nb = num_blocks(L);
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (cudaMemsetAsync(stats, 0, sizeof(StatsHeader), st) != cudaSuccess) return KVQ_ERR_CUDA;
     if (nb == 0) return KVQ_OK;
     const int units = 4 * L.group;   // 8-entry units per block
-    StatsRow *out = static_cast<StatsRow *>(stats);
+    StatsHeader *hdr = static_cast<StatsHeader *>(stats);
+    float *recs = reinterpret_cast<float *>(static_cast<char *>(stats) + sizeof(StatsHeader));
     const dim3 grid((unsigned)nb);
     if (units <= kStatsThreads)
-        stats_kernel<1><<<grid, kStatsThreads, 0, st>>>(x, L, out, status);
+        stats_kernel<1><<<grid, kStatsThreads, 0, st>>>(x, L, hdr, recs, status);
     else
-        stats_kernel<2><<<grid, kStatsThreads, 0, st>>>(x, L, out, status);
+        stats_kernel<2><<<grid, kStatsThreads, 0, st>>>(x, L, hdr, recs, status);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

@@ -22,7 +22,11 @@ KVQ_ERR_NONFINITE = 3
 KVQ_ERR_INFEASIBLE = 4
 KVQ_BISECT40 = 0
 KVQ_SUBGRADIENT = 1
-STATS_ROW_BYTES = 384
+# kvq_stats output: a 256-byte header, then per block a 4800-byte record whose
+# first 96 floats are the stats row (candidates, m', flags, d, atom moments)
+STATS_HEADER_BYTES = 256
+STATS_RECORD_FLOATS = 1200
+STATS_ROW_FLOATS = 96
 
 
 class _Layout(C.Structure):
@@ -48,6 +52,11 @@ class Layout:
     @property
     def nblocks(self) -> int:
         return self.S * (self.T // 32) * (self.D // self.group)
+
+
+class _Report(C.Structure):
+    _fields_ = [("rounds", C.c_int32), ("steps", C.c_int32), ("active", C.c_uint32 * 16),
+                ("lambda_", C.c_double), ("xa", C.c_double), ("xb", C.c_double)]
 
 
 class KvqError(RuntimeError):
@@ -82,6 +91,8 @@ def lib():
         L.kvq_quantize.argtypes = [vp, _Layout, vp, vp, u64, u64, vp, vp]
         L.kvq_dequantize.restype = C.c_int
         L.kvq_dequantize.argtypes = [vp, vp, _Layout, vp, vp]
+        L.kvq_allocate_report.restype = C.c_int
+        L.kvq_allocate_report.argtypes = [vp, C.POINTER(_Report)]
         L.kvq_status_string.restype = C.c_char_p
         L.kvq_status_string.argtypes = [C.c_int]
         _lib = L
@@ -140,6 +151,20 @@ def kvq_quantize(x, L: Layout, codebook, k, seed: int, index_base: int, codes, s
 def kvq_dequantize(codes, codebook, L: Layout, y, stream=None):
     _check(lib().kvq_dequantize(_ptr(codes), _ptr(codebook), L.c(), _ptr(y), _stream(stream)),
            "kvq_dequantize")
+
+
+def stats_rows(stats):
+    """View of the per-block stats rows inside a kvq_stats buffer: a
+    [nblocks, 96] float32 tensor (same device)."""
+    recs = stats[STATS_HEADER_BYTES:].view(torch.float32).view(-1, STATS_RECORD_FLOATS)
+    return recs[:, :STATS_ROW_FLOATS]
+
+
+def kvq_allocate_report(workspace) -> dict:
+    r = _Report()
+    _check(lib().kvq_allocate_report(_ptr(workspace), C.byref(r)), "kvq_allocate_report")
+    return {"rounds": r.rounds, "steps": r.steps, "active": list(r.active)[:max(r.rounds, 0)],
+            "lambda": r.lambda_, "xa": r.xa, "xb": r.xb}
 
 
 class Buffers:

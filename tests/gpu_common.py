@@ -40,7 +40,7 @@ def run(x, G, s, budget, seed=0, index_base=0, mode=kvq.KVQ_BISECT40, eta=0.0, l
     y = torch.empty_like(xd)
     kvq.kvq_dequantize(buf.codes, buf.codebook, L, y)
     torch.cuda.synchronize()
-    rows = buf.stats.view(torch.float32).view(-1, 96).cpu().numpy()
+    rows = kvq.stats_rows(buf.stats).cpu().numpy()
     return {
         "L": L,
         "rows": rows,

@@ -31,8 +31,8 @@ def test_library_builds_and_exports_every_declared_symbol():
 def test_sizes_and_layout_validation():
     L = kvq.Layout(16, 8192, 128, 128)
     assert kvq.kvq_num_blocks(L) == 4096
-    assert kvq.kvq_stats_bytes(L) == 4096 * 384
-    assert kvq.kvq_workspace_bytes(L, 16) > 4096 * 872 * 4
+    assert kvq.kvq_stats_bytes(L) == 256 + 4096 * 4800
+    assert kvq.kvq_workspace_bytes(L, 16) > 4096 * 32 * 8
     assert kvq.kvq_workspace_bytes(L, 1) == 0 and kvq.kvq_workspace_bytes(L, 17) == 0
     assert kvq.kvq_num_blocks(kvq.Layout(16, 8200, 128, 128)) == -1      # T % 32
     assert kvq.kvq_num_blocks(kvq.Layout(16, 8192, 128, 48)) == -1       # group

@@ -211,7 +211,7 @@ def test_full_size_sampled_slabs(name, bi):
     rng = np.random.default_rng(1)
     nTB, nG = w.T // 32, w.D // w.G
     slabs = rng.choice(w.S * nTB, size=6, replace=False)
-    rows = g_buf.stats.view(torch.float32).view(-1, 96)
+    rows = kvq.stats_rows(g_buf.stats)
     for sl in slabs:
         h, tb = divmod(int(sl), nTB)
         xs = gc.to_np(xd[h, 32 * tb:32 * tb + 32, :].unsqueeze(0))

@@ -20,17 +20,25 @@ static double Rfun(double lam, int nbp, const double *bl, const double *br, doub
     for (int i = 0; i < nbp; ++i) if (lam >= bl[i]) r = br[i];
     return r;
 }
+// pilot_bias < 0: no pilot; else the pilot sees R * (1 + pilot_bias) on 1/16 of the blocks
 extern "C" int kvqs_run(double hi0, double B, int nbp, const double *bl, const double *br,
-                        double R0, double *out) {
+                        double R0, double *out, double pilot_bias) {
     kvq::SearchState s;
     kvq::search_init(s);
     s.hi0 = hi0;
+    const int64_t nb = 4096;
+    if (pilot_bias >= 0.0 || pilot_bias <= -1.0) {}
+    if (pilot_bias > -1.0) kvq::search_set_pilot(s, nb, 16);
     int r = 0;
     for (; r < 64 && s.phase != kvq::kSearchDone; ++r) {
         double R[kvq::kSearchProbes];
-        for (int p = 0; p < kvq::kSearchProbes; ++p)
-            R[p] = p < s.nprobe ? Rfun(kvq::search_probe(s, p), nbp, bl, br, R0) : 0.0;
-        kvq::search_update(s, R, B);
+        const bool pilot = s.phase == kvq::kSearchPilot;
+        for (int p = 0; p < kvq::kSearchProbes; ++p) {
+            double v = p < s.nprobe || pilot ? Rfun(kvq::search_probe(s, p), nbp, bl, br, R0) : 0.0;
+            if (pilot) v = v * (1.0 + pilot_bias) * (double)s.pilot_blocks / (double)nb;
+            R[p] = v;
+        }
+        kvq::search_update(s, R, B, nb);
     }
     out[0] = s.lambda; out[1] = s.xb; out[2] = s.R_xb; out[3] = r;
     out[4] = s.infeasible; out[5] = s.step;
@@ -51,7 +59,7 @@ def lib():
     L = C.CDLL(so)
     L.kvqs_run.restype = C.c_int
     L.kvqs_run.argtypes = [C.c_double, C.c_double, C.c_int, C.c_void_p, C.c_void_p, C.c_double,
-                           C.c_void_p]
+                           C.c_void_p, C.c_double]
     return L
 
 
@@ -84,11 +92,11 @@ def bisect40(hi0, B, bl, br, R0):
     return hi, 0
 
 
-def run(lib, hi0, B, bl, br, R0):
+def run(lib, hi0, B, bl, br, R0, pilot=-2.0):
     out = (C.c_double * 6)()
     a = (C.c_double * len(bl))(*bl)
     b = (C.c_double * len(br))(*br)
-    rc = lib.kvqs_run(hi0, B, len(bl), a, b, R0, out)
+    rc = lib.kvqs_run(hi0, B, len(bl), a, b, R0, out, pilot)
     assert rc == 0
     return list(out)
 
@@ -124,6 +132,20 @@ def test_same_lambda_as_sequential_bisection(lib):
             assert lam == 0.0 or want - hi0 * 2 ** -39 <= xb <= want
         rounds.append(nr)
     assert sum(rounds) / len(rounds) < 8
+
+
+@pytest.mark.parametrize("bias", [0.0, 0.05, -0.05, 0.4, -0.4])
+def test_pilot_estimate_never_changes_lambda(lib, bias):
+    # the pilot (a biased estimate of R on a sample of blocks) only places the
+    # probes of round 0; the answer is the sequential bisection's either way
+    rng = random.Random(5)
+    for _ in range(800):
+        hi0, bl, br, R0 = random_case(rng)
+        B = rng.uniform(0, R0)
+        want, infeasible = bisect40(hi0, B, bl, br, R0)
+        out = run(lib, hi0, B, bl, br, R0, pilot=bias)
+        assert out[0] == want
+        assert out[4] == infeasible
 
 
 def test_budget_at_zero_lambda_and_large_hi(lib):
