@@ -46,6 +46,7 @@ extern "C" {
 #define KVQ_ERR_CUDA 2
 #define KVQ_ERR_NONFINITE 3   /* device status: a block holds NaN or +-Inf */
 #define KVQ_ERR_INFEASIBLE 4  /* device status: budget unreachable         */
+#define KVQ_ERR_TOO_LARGE 5   /* kvq_allocate_static: layout over its limit  */
 
 /* lambda modes of kvq_allocate */
 #define KVQ_BISECT40 0        /* global lambda by the 40-step bisection      */
@@ -138,6 +139,33 @@ int kvq_allocate(const void *stats, kvq_layout L, int s, double budget_bits,
                  int mode, double eta, double *lambda, void *workspace,
                  float *codebook, uint8_t *k, float *D_r, float *H_r,
                  double *totals, int32_t *status, void *stream);
+
+/*
+ * kvq_allocate_static -- kvq_allocate without a caller-provided workspace.
+ * The method's page has no counterpart: this is a convenience for callers
+ * that must not allocate device memory at the point of the call -- code that
+ * runs inside a caching allocator's own hooks, a memory-capped serving
+ * process whose pool is fully reserved, or a C caller with no allocator at
+ * all.  Arguments, results and statuses are those of kvq_allocate.
+ *
+ * The scratch is a fixed array of KVQ_STATIC_WORKSPACE_BYTES (8 MiB) in the
+ * library's device memory, present on every GPU that loads the library until
+ * the process exits.  It holds layouts whose kvq_workspace_bytes(L, s) is at
+ * most that size (29 742 blocks: 7.6 million entries with group 8, 122
+ * million with group 128); larger layouts return KVQ_ERR_TOO_LARGE without
+ * launching anything.
+ * Nothing is allocated: the first call on each device looks up the array's
+ * address once (cudaGetSymbolAddress) -- make that first call outside any
+ * stream capture.  Every call on a device shares the one array, so calls that
+ * can overlap in time (different streams, different host threads without a
+ * dependency between them) race on it and corrupt each other's results;
+ * serialise them.
+ */
+#define KVQ_STATIC_WORKSPACE_BYTES (8u << 20)
+int kvq_allocate_static(const void *stats, kvq_layout L, int s, double budget_bits,
+                        int mode, double eta, double *lambda, float *codebook,
+                        uint8_t *k, float *D_r, float *H_r, double *totals,
+                        int32_t *status, void *stream);
 
 /*
  * kvq_quantize -- unbiased stochastic interpolation and 4-bit packing ("Key

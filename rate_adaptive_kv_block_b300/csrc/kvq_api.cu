@@ -2,6 +2,8 @@
 // host, then stream-ordered launches.  Nothing here allocates memory.
 #include <math.h>
 
+#include <mutex>
+
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -43,6 +45,32 @@ static int init_once() {
         state[dev] = allocate_init();
         done[dev] = true;
     }
+    return state[dev];
+}
+
+// Scratch of kvq_allocate_static: a fixed array in the module's global
+// memory, created when a device loads the library and held until the process
+// exits.  One copy per device; every call on that device shares it.
+static __device__ __align__(256) unsigned char g_static_workspace[KVQ_STATIC_WORKSPACE_BYTES];
+
+// Device address of g_static_workspace on the current device, looked up once
+// per device (cudaGetSymbolAddress; no allocation).
+static int static_workspace(void **out) {
+    static std::mutex mu;
+    static void *addr[64];
+    static int state[64];
+    static bool done[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
+    std::lock_guard<std::mutex> g(mu);
+    if (!done[dev]) {
+        void *p = nullptr;
+        state[dev] = cudaGetSymbolAddress(&p, g_static_workspace) == cudaSuccess ? KVQ_OK
+                                                                                 : KVQ_ERR_CUDA;
+        addr[dev] = p;
+        done[dev] = true;
+    }
+    *out = addr[dev];
     return state[dev];
 }
 }  // namespace kvq
@@ -92,6 +120,20 @@ int kvq_allocate(const void *stats, kvq_layout L, int s, double budget_bits, int
                            D_r, H_r, totals, status, static_cast<cudaStream_t>(stream));
 }
 
+int kvq_allocate_static(const void *stats, kvq_layout L, int s, double budget_bits, int mode,
+                        double eta, double *lambda, float *codebook, uint8_t *k, float *D_r,
+                        float *H_r, double *totals, int32_t *status, void *stream) {
+    if (!layout_ok(L) || s < 2 || s > kMaxLev) return KVQ_ERR_INVALID_ARG;
+    if (workspace_bytes(num_blocks(L), s) > (size_t)KVQ_STATIC_WORKSPACE_BYTES)
+        return KVQ_ERR_TOO_LARGE;
+    void *ws = nullptr;
+    if (static_workspace(&ws) != KVQ_OK || !ws) return KVQ_ERR_CUDA;
+    // the control block at the start of the scratch is reset by the first
+    // kernel of kvq_allocate; nothing else in it is read before it is written
+    return kvq_allocate(stats, L, s, budget_bits, mode, eta, lambda, ws, codebook, k, D_r, H_r,
+                        totals, status, stream);
+}
+
 int kvq_quantize(const uint16_t *x, kvq_layout L, const float *codebook, const uint8_t *k,
                  uint64_t seed, uint64_t index_base, uint8_t *codes, void *stream) {
     if (!layout_ok(L)) return KVQ_ERR_INVALID_ARG;
@@ -131,6 +173,7 @@ const char *kvq_status_string(int status) {
     case KVQ_ERR_CUDA: return "CUDA launch error";
     case KVQ_ERR_NONFINITE: return "non-finite input entry";
     case KVQ_ERR_INFEASIBLE: return "budget infeasible";
+    case KVQ_ERR_TOO_LARGE: return "layout needs more scratch than the static workspace holds";
     default: return "unknown status";
     }
 }

@@ -20,6 +20,8 @@ KVQ_ERR_INVALID_ARG = 1
 KVQ_ERR_CUDA = 2
 KVQ_ERR_NONFINITE = 3
 KVQ_ERR_INFEASIBLE = 4
+KVQ_ERR_TOO_LARGE = 5
+KVQ_STATIC_WORKSPACE_BYTES = 8 << 20
 KVQ_BISECT40 = 0
 KVQ_SUBGRADIENT = 1
 # kvq_stats output: a 256-byte header, then per block a 4800-byte record whose
@@ -87,6 +89,9 @@ def lib():
         L.kvq_allocate.restype = C.c_int
         L.kvq_allocate.argtypes = [vp, _Layout, C.c_int, dbl, C.c_int, dbl, vp, vp, vp, vp,
                                    vp, vp, vp, vp, vp]
+        L.kvq_allocate_static.restype = C.c_int
+        L.kvq_allocate_static.argtypes = [vp, _Layout, C.c_int, dbl, C.c_int, dbl, vp, vp, vp,
+                                          vp, vp, vp, vp, vp]
         L.kvq_quantize.restype = C.c_int
         L.kvq_quantize.argtypes = [vp, _Layout, vp, vp, u64, u64, vp, vp]
         L.kvq_dequantize.restype = C.c_int
@@ -141,6 +146,19 @@ def kvq_allocate(stats, L: Layout, s: int, budget_bits: float, mode: int, eta: f
                               float(eta), _ptr(lam), _ptr(workspace), _ptr(codebook), _ptr(k),
                               _ptr(D_r), _ptr(H_r), _ptr(totals), _ptr(status),
                               _stream(stream)), "kvq_allocate")
+
+
+def kvq_allocate_static(stats, L: Layout, s: int, budget_bits: float, mode: int, eta: float,
+                        lam, codebook, k, D_r, H_r, totals, status, stream=None):
+    """kvq_allocate with the library's fixed device scratch instead of a
+    caller-provided workspace, for callers that cannot allocate device memory
+    at the call.  Layouts needing more than KVQ_STATIC_WORKSPACE_BYTES of
+    scratch raise KvqError (KVQ_ERR_TOO_LARGE); calls that overlap in time on
+    one device share the scratch and must be serialised."""
+    _check(lib().kvq_allocate_static(_ptr(stats), L.c(), int(s), float(budget_bits), int(mode),
+                                     float(eta), _ptr(lam), _ptr(codebook), _ptr(k), _ptr(D_r),
+                                     _ptr(H_r), _ptr(totals), _ptr(status), _stream(stream)),
+           "kvq_allocate_static")
 
 
 def kvq_quantize(x, L: Layout, codebook, k, seed: int, index_base: int, codes, stream=None):
