@@ -6,15 +6,17 @@ One step = kvq_stats + kvq_allocate (40-step lambda bisection) + kvq_quantize
 over one [S, T, D] binary16 K/V tensor already resident in HBM: the
 Llama-3-8B-shaped single-layer prefill (K and V, 8 KV heads each, 8192
 tokens, head dim 128; blocks of one head x 32 tokens; s = 16; B = 2.5 bits per
-entry).  L2 is flushed before every timed step, outside the timed interval
-(a 256 MB write, then a 256 MB read so the write's dirty lines are written
-back before timing starts).  The metric is binary16 input bytes quantized per second.
+entry).  The step is captured once as a CUDA graph and replayed; L2 is
+flushed before every timed step, outside the timed interval (a 256 MB write,
+then a 256 MB read so the write's dirty lines are written back before timing
+starts).  The metric is binary16 input bytes quantized per second.  The same
+step launched eagerly is timed too, with per-kernel events.
 
 Also reported on the same line: per-kernel times, the roofline of the dominant
 kernel (algorithmic bytes / measured time / measured HBM peak), an end-to-end
 figure through the C ABI with pinned host buffers (host->device copy of the
-input and device->host copy of codes, codebooks and totals inside the timed
-region), the number of our kernel launches, SM clocks sampled during the
+input and device->host copy of codes, codebooks, k and totals inside the timed
+region, pipelined over three streams), the number of our kernel launches, SM clocks sampled during the
 timed region, and the CPU oracle timed on a bounded sample (cpu_baseline).
 
 Multi-GPU (torchrun): every rank quantizes its own independent tensor
@@ -239,6 +241,8 @@ def main():
         if ev is not None:
             ev[3].record(stream)
 
+    # the whole step captured once as a CUDA graph (the C-ABI calls are
+    # stream-ordered and capture-safe after their first call on a device)
     for _ in range(args.warmup):
         flush_l2(0)
         step()
@@ -246,20 +250,42 @@ def main():
     st = int(buf.status.item())
     if st != 0:
         raise SystemExit("allocation status %d (%s)" % (st, kvq.kvq_status_string(st)))
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    if pg:
-        pg.barrier()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
     torch.cuda.synchronize()
+
+    def timed(run, n):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for i in range(n):
+            flush_l2(i)
+            ev[i][0].record(stream)
+            run()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
     with ClockSampler(local) as clk:
+        for i in range(args.warmup):
+            flush_l2(i)
+            graph.replay()
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        t_step = timed(graph.replay, args.steps)
+        # the same step launched eagerly, with per-kernel events
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
         for i in range(args.steps):
             flush_l2(i)
             step(evs[i])
         torch.cuda.synchronize()
+    st = int(buf.status.item())
+    if st != 0:
+        raise SystemExit("allocation status %d (%s)" % (st, kvq.kvq_status_string(st)))
     t_stats = [e[0].elapsed_time(e[1]) for e in evs]
     t_alloc = [e[1].elapsed_time(e[2]) for e in evs]
     t_quant = [e[2].elapsed_time(e[3]) for e in evs]
-    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    t_eager = [e[0].elapsed_time(e[3]) for e in evs]
     tot_ms = sum(t_step)
     if pg:
         t = torch.tensor([tot_ms], device=dev, dtype=torch.float64)
@@ -267,60 +293,78 @@ def main():
         tot_ms = float(t.item())
     value = world * args.steps * in_bytes / (tot_ms * 1e-3) / 1e9
 
-    # quantize alone with a cold L2 (the gated kernel), same launch configuration
-    qe = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush_l2(i)
-        qe[i][0].record(stream)
-        kvq.kvq_quantize(x, L, buf.codebook, buf.k, 0, 0, buf.codes)
-        qe[i][1].record(stream)
-    se = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush_l2(i)
-        se[i][0].record(stream)
-        kvq.kvq_stats(x, L, buf.stats, buf.status_stats)
-        se[i][1].record(stream)
-    torch.cuda.synchronize()
-    t_qcold = [a.elapsed_time(b) for a, b in qe]
-    t_scold = [a.elapsed_time(b) for a, b in se]
+    # each kernel alone with a cold L2, same launch configuration
+    t_qcold = timed(lambda: kvq.kvq_quantize(x, L, buf.codebook, buf.k, 0, 0, buf.codes),
+                    args.steps)
+    t_scold = timed(lambda: kvq.kvq_stats(x, L, buf.stats, buf.status_stats), args.steps)
+    t_acold = timed(lambda: kvq.kvq_allocate(buf.stats, L, s, B, kvq.KVQ_BISECT40, 0.0, buf.lam,
+                                             buf.workspace, buf.codebook, buf.k, buf.D_r,
+                                             buf.H_r, buf.totals, buf.status), args.steps)
 
-    # end to end through the C ABI with pinned host buffers
+    # End to end through the C ABI from pinned host memory, pipelined over
+    # three streams the way a serving loop would run it: step i's input copy
+    # overlaps step i-1's kernels and step i-2's result copy.  Every step
+    # copies its whole input in and its codes, codebooks, k and totals out;
+    # the L2 flush runs on the compute stream before each step, inside the
+    # timed interval.  Two sets of device and host buffers alternate.
     x_host = torch.from_numpy(x_np.view(np.int16)).view(torch.float16).pin_memory()
-    codes_h = torch.empty(buf.codes.shape, dtype=torch.uint8).pin_memory()
-    cb_h = torch.empty(buf.codebook.shape, dtype=torch.float32).pin_memory()
-    k_h = torch.empty(buf.k.shape, dtype=torch.uint8).pin_memory()
-    tot_h = torch.empty(3, dtype=torch.float64).pin_memory()
+    bufs = [buf, kvq.Buffers(L, s, dev)]
+    xes = [torch.empty_like(x), torch.empty_like(x)]
+    outs_h = [dict(codes=torch.empty(buf.codes.shape, dtype=torch.uint8).pin_memory(),
+                   codebook=torch.empty(buf.codebook.shape, dtype=torch.float32).pin_memory(),
+                   k=torch.empty(buf.k.shape, dtype=torch.uint8).pin_memory(),
+                   totals=torch.empty(3, dtype=torch.float64).pin_memory()) for _ in range(2)]
     h2d = x_host.numel() * 2
-    d2h = codes_h.numel() + cb_h.numel() * 4 + k_h.numel() + 24
-    xe = torch.empty_like(x)
+    d2h = sum(t.numel() * t.element_size() for t in outs_h[0].values())
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        xe.copy_(x_host, non_blocking=True)
-        kvq.kvq_stats(xe, L, buf.stats, buf.status_stats)
-        kvq.kvq_allocate(buf.stats, L, s, B, kvq.KVQ_BISECT40, 0.0, buf.lam, buf.workspace,
-                         buf.codebook, buf.k, buf.D_r, buf.H_r, buf.totals, buf.status)
-        kvq.kvq_quantize(xe, L, buf.codebook, buf.k, 0, 0, buf.codes)
-        codes_h.copy_(buf.codes, non_blocking=True)
-        cb_h.copy_(buf.codebook, non_blocking=True)
-        k_h.copy_(buf.k, non_blocking=True)
-        tot_h.copy_(buf.totals, non_blocking=True)
+    def e2e_run(n):
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(s_in)
+        s_cmp.wait_event(t0)
+        s_out.wait_event(t0)
+        for i in range(n):
+            j = i & 1
+            b, xe, oh = bufs[j], xes[j], outs_h[j]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_cmp[j])         # step i-2 is done reading xe
+                xe.copy_(x_host, non_blocking=True)
+                ev_in[j].record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(ev_in[j])
+                if i >= 2:
+                    s_cmp.wait_event(ev_out[j])       # step i-2's results are copied out
+                flush_l2(i)
+                kvq.kvq_stats(xe, L, b.stats, b.status_stats, stream=s_cmp)
+                kvq.kvq_allocate(b.stats, L, s, B, kvq.KVQ_BISECT40, 0.0, b.lam, b.workspace,
+                                 b.codebook, b.k, b.D_r, b.H_r, b.totals, b.status, stream=s_cmp)
+                kvq.kvq_quantize(xe, L, b.codebook, b.k, 0, 0, b.codes, stream=s_cmp)
+                ev_cmp[j].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_cmp[j])
+                for key in ("codes", "codebook", "k", "totals"):
+                    oh[key].copy_(getattr(b, key), non_blocking=True)
+                ev_out[j].record(s_out)
+        t1.record(s_out)                              # after the last result copy
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
 
-    for _ in range(args.warmup):
-        e2e_step()
-    torch.cuda.synchronize()
-    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush_l2(i)
-        ee[i][0].record(stream)
-        e2e_step()
-        ee[i][1].record(stream)
-    torch.cuda.synchronize()
-    t_e2e = sum(a.elapsed_time(b) for a, b in ee)
+    ref_codes = buf.codes.cpu()
+    e2e_run(args.warmup)
+    t_e2e = e2e_run(args.steps)
     if pg:
         t = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         t_e2e = float(t.item())
     e2e_val = world * args.steps * in_bytes / (t_e2e * 1e-3) / 1e9
+    if not torch.equal(outs_h[(args.steps - 1) & 1]["codes"], ref_codes):
+        raise SystemExit("end-to-end codes differ from the device-resident run")
 
     hbm, src = peaks()
     mean = lambda v: sum(v) / len(v)
@@ -328,8 +372,11 @@ def main():
     q_bytes = in_bytes + in_bytes // 4 + nb * (64 + 1)
     s_bytes = in_bytes + nb * 384
     kern = {
+        "step_ms_graph_median": statistics.median(t_step), "step_ms_graph_min": min(t_step),
+        "step_ms_eager_mean": mean(t_eager), "step_ms_eager_median": statistics.median(t_eager),
         "stats_ms": mean(t_stats), "allocate_ms": mean(t_alloc), "quantize_ms": mean(t_quant),
         "stats_cold_ms": mean(t_scold), "quantize_cold_ms": mean(t_qcold),
+        "allocate_cold_ms": mean(t_acold),
         "stats_cold_GBps": s_bytes / (mean(t_scold) * 1e-3) / 1e9,
         "quantize_cold_GBps": q_bytes / (mean(t_qcold) * 1e-3) / 1e9,
     }
@@ -361,7 +408,8 @@ def main():
         roof = {"kernel": "kvq_quantize", "bound": "hbm", "achieved": a, "peak": hbm,
                 "unit": "GB/s", "frac": a / hbm, "traffic": None, "peak_source": src}
 
-    launches_per_step = 1 + (2 + 9 + 1) + 1
+    # kvq_stats 1; kvq_allocate: ctrl_init, 3 + 40/5 search rounds, emit; kvq_quantize 1
+    launches_per_step = 1 + (1 + (3 + 40 // 5) + 1) + 1
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         gbs, dt, thr, desc = cpu_baseline(w, x_np, w.budgets[0])
@@ -375,13 +423,16 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": WORKLOAD_DESC, "l2": "flushed before each step (256 MB write then 256 MB read, outside the timed interval)",
+                       "launch": "whole step as one CUDA graph replay",
                        "parallelism": "replicas" if world > 1 else "single"},
             "tokens_per_s": world * args.steps * w.T / (tot_ms * 1e-3),
             "lambda": float(buf.lam.item()), "rate_bits_per_entry": float(buf.totals[0].item()) / w.entries,
             "kernels": kern,
             "roofline": roof,
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "how": "C-ABI calls from pinned host memory, input copy / kernels / result "
+                           "copy pipelined on 3 streams, L2 flush inside each step"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk_summary,
             "cpu_baseline": cpu,

@@ -100,6 +100,7 @@ __global__ void ctrl_init_kernel(Ctrl *c, const StatsHeader *hdr, double budget,
     c->nb = nb;
     if (mode != KVQ_SUBGRADIENT && nb >= kPilotMinBlocks) search_set_pilot(c->s, nb, kPilotStride);
     c->budget = budget;
+    c->budget_fx = budget_fx(budget);
     c->eta = eta;
     c->fixed = (mode == KVQ_SUBGRADIENT) ? 1 : 0;
     c->lambda_fixed = c->fixed ? *lambda_in : 0.0;
@@ -412,72 +413,100 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
     long long *sSum = reinterpret_cast<long long *>(smem + W * (kTblStride + Cfg::kStateFloats));
     float *sDiag = reinterpret_cast<float *>(sSum + W * 32) + w * 32;
     __shared__ bool is_last;
-    __shared__ uint32_t sAct;
+    __shared__ uint32_t sAct, sN;
+    __shared__ int32_t sList[W * 32];
+    __shared__ float sRb[W * 32];
     if (threadIdx.x == 0) sAct = 0u;
     const float lam = (float)probe_lambda(ctrl, lane);
     long long my_sum = 0;
-    uint32_t my_act = 0;
-    for (int64_t it = (int64_t)blockIdx.x * W + w; it < nitems; it += (int64_t)gridDim.x * W) {
-        const int64_t b = walk ? (int64_t)lin[it] : pilot ? it * stride : it;
-        float rb = 0.f;
-        bool active = true;
-        if (walk) {
-            // the block was evaluated in the previous round: carry its results
-            // at the new window ends (lane 0 alone touches the per-block
-            // state, then broadcasts)
-            float ra = 0.f;
-            if (lane == 0) {
-                ra = rate_lo[b];
-                rb = rate_hi[b];
-                if (xa_probe >= 0) ra = rates[b * 32 + xa_probe];
+    // Items in chunks of one per thread: item it = blockIdx.x + gridDim.x *
+    // (c * blockDim.x + threadIdx.x), so consecutive CTAs take consecutive
+    // items.  Phase A (a thread per item) carries the walk's per-block state
+    // to the new window ends and keeps the blocks whose rate can still
+    // change; phase B (a warp per kept block) runs the DP.
+    for (int64_t c0 = 0; (int64_t)blockIdx.x + (int64_t)gridDim.x * c0 < nitems;
+         c0 += blockDim.x) {
+        if (threadIdx.x == 0) sN = 0u;
+        __syncthreads();
+        const int64_t it = (int64_t)blockIdx.x + (int64_t)gridDim.x * (c0 + threadIdx.x);
+        bool act = false;
+        int32_t bsel = 0;
+        if (it < nitems) {
+            act = true;
+            if (walk) {
+                // evaluated in the previous round: its rates at the new window
+                // ends; the rate is non-increasing in lambda, so equal rates
+                // at both ends mean the chain is constant inside the window
+                const int32_t b = lin[it];
+                float ra = rate_lo[b], rb = rate_hi[b];
+                if (xa_probe >= 0) ra = rates[(int64_t)b * 32 + xa_probe];
                 if (xb_probe >= 0) {
-                    rb = rates[b * 32 + xb_probe];
-                    mask_hi[b] = masks[b * 32 + xb_probe];
+                    rb = rates[(int64_t)b * 32 + xb_probe];
+                    mask_hi[b] = masks[(int64_t)b * 32 + xb_probe];
                 }
                 rate_lo[b] = ra;
                 rate_hi[b] = rb;
-            }
-            ra = __shfl_sync(0xffffffffu, ra, 0);
-            rb = __shfl_sync(0xffffffffu, rb, 0);
-            // the rate is non-increasing in lambda: equal at both window ends
-            // means constant inside the window, and so is the chosen chain
-            active = ra != rb;
-        }
-        if (!active) continue;
-        const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
-        float4 *dst = reinterpret_cast<float4 *>(sTbl);
-        for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
-        __syncwarp();
-        const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
-        float rate;
-        uint32_t mask;
-        if (mp <= 1) {
-            rate = 0.f;
-            mask = 1u;
-        } else {
-            const int C = mp > s ? mp - s : 0;
-            if (!GENERAL || C == 0 || (C == 1 && mp == 17)) {
-                dp_a_diag(sTbl, sDiag, lane);
-                dp_path_a(sTbl, lam, C, sState, sState + kPairs * 32, sDiag, lane, rate, mask);
+                act = ra != rb;
+                bsel = b;
+                if (act) {
+                    const uint32_t slot = atomicAdd(&sN, 1u);
+                    sList[slot] = b;
+                    sRb[slot] = rb;
+                }
             } else {
-                dp_path_b(sTbl, lam, s, sState, sState + kPairs * 32,
-                          reinterpret_cast<uint32_t *>(sState + 2 * kPairs * 32), lane, rate,
-                          mask);
+                bsel = (int32_t)(pilot ? it * stride : it);
+                const uint32_t slot = atomicAdd(&sN, 1u);
+                sList[slot] = bsel;
+                sRb[slot] = 0.f;
             }
+            if (act) evr[bsel] = round;
         }
-        rates[b * 32 + lane] = rate;
-        masks[b * 32 + lane] = mask;
-        my_sum += llrint((double)rate * kRateScale) - llrint((double)rb * kRateScale);
-        if (lane == 0) {
-            evr[b] = round;
-            if (!pilot) lout[atomicAdd(&ctrl->cnt[(round + 1) & 1], 1u)] = (int32_t)b;
+        // room in the next round's list: one atomic per warp; the entries are
+        // written after the DP, so its latency is hidden
+        uint32_t lbase = 0, lrank = 0;
+        if (!pilot) {
+            const uint32_t am = __ballot_sync(0xffffffffu, act);
+            lrank = __popc(am & ((1u << lane) - 1u));
+            if (lane == 0 && am) lbase = atomicAdd(&ctrl->cnt[(round + 1) & 1], (uint32_t)__popc(am));
+            lbase = __shfl_sync(0xffffffffu, lbase, 0);
         }
-        ++my_act;
-        __syncwarp();
+        __syncthreads();
+        const uint32_t n = sN;
+        for (uint32_t q = w; q < n; q += W) {
+            const int64_t b = sList[q];
+            const float rb = sRb[q];
+            const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
+            float4 *dst = reinterpret_cast<float4 *>(sTbl);
+            for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
+            __syncwarp();
+            const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
+            float rate;
+            uint32_t mask;
+            if (mp <= 1) {
+                rate = 0.f;
+                mask = 1u;
+            } else {
+                const int C = mp > s ? mp - s : 0;
+                if (!GENERAL || C == 0 || (C == 1 && mp == 17)) {
+                    dp_a_diag(sTbl, sDiag, lane);
+                    dp_path_a(sTbl, lam, C, sState, sState + kPairs * 32, sDiag, lane, rate, mask);
+                } else {
+                    dp_path_b(sTbl, lam, s, sState, sState + kPairs * 32,
+                              reinterpret_cast<uint32_t *>(sState + 2 * kPairs * 32), lane, rate,
+                              mask);
+                }
+            }
+            rates[b * 32 + lane] = rate;
+            masks[b * 32 + lane] = mask;
+            my_sum += llrint((double)rate * kRateScale) - llrint((double)rb * kRateScale);
+            __syncwarp();
+        }
+        if (!pilot && act) lout[lbase + lrank] = bsel;
+        if (threadIdx.x == 0) sAct += n;
+        __syncthreads();
     }
     sSum[w * 32 + lane] = my_sum;
     __syncthreads();
-    if (lane == 0 && my_act) atomicAdd(&sAct, my_act);
     if (threadIdx.x < 32) {
         long long sum = 0;
         for (int k = 0; k < W; ++k) sum += sSum[k * 32 + threadIdx.x];
@@ -494,89 +523,136 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
     if (!is_last) return;
     __threadfence();
 
-    // ---- last CTA: read the sums, advance the search
-    __shared__ double R[32];
-    __shared__ long long Rfx[32];
-    const long long base = walk ? ctrl->Rxb_fx : 0;
-    if (threadIdx.x < 32) {
-        const long long a = (long long)atomicExch(&ctrl->acc[threadIdx.x], 0ull);
-        Rfx[threadIdx.x] = base + a;
-        R[threadIdx.x] = (double)(base + a) / kRateScale;
+    // ---- last CTA: stage the whole control block in shared memory with one
+    // coalesced read (L2, past L1: other CTAs updated it with atomics), then
+    // advance the search there and write back what changed
+    __shared__ __align__(16) Ctrl sC;
+    {
+        const int4 *src = reinterpret_cast<const int4 *>(ctrl);
+        int4 *dst = reinterpret_cast<int4 *>(&sC);
+        for (int i = threadIdx.x; i < (int)(sizeof(Ctrl) / 16); i += blockDim.x)
+            dst[i] = __ldcg(src + i);
     }
     __syncthreads();
-
-    // warp 0 advances the search: one lane per probe folds the evaluations
-    // into the window (exact min / max reductions), every lane walks, and
-    // lane L generates the probes along decision path L
-    __shared__ SearchState sS;
-    __shared__ double sProbe[kSearchProbes];
-    if (threadIdx.x < 32) {
-        const int L = threadIdx.x;
-        if (L == 0) search_copy_scalars(sS, ctrl->s);
-        sS.probe[L] = ctrl->s.probe[L];
+    if (threadIdx.x >= 32) return;
+    const int L = threadIdx.x;
+    SearchState &S = sC.s;
+    __shared__ long long Rfx[32];
+    const long long myR = (walk ? sC.Rxb_fx : 0) + (long long)sC.acc[L];
+    Rfx[L] = myR;
+    ctrl->acc[L] = 0ull;
+    const long long Bfx = sC.budget_fx;
+    if (L == 0) S.hi0 = __longlong_as_double((long long)sC.hi0_bits);
+    __syncwarp();
+    if (sC.fixed) {
+        if (L == 0) {
+            S.xb_probe = 0;
+            S.R_xb = myR;
+            S.lambda = sC.lambda_fixed;
+            S.phase = kSearchDone;
+            S.rounds += 1;
+        }
+    } else if (S.phase == kSearchPilot) {
+        // one lane per probe: the sample's rates scaled to all blocks, the
+        // smallest feasible probe and the largest infeasible one below it
+        // (first lane on ties, as a sequential scan)
+        const double B = sC.budget;
+        const double scale =
+            (double)sC.nb / (double)(S.pilot_blocks > 0 ? S.pilot_blocks : 1) / kRateScale;
+        const double v = search_probe(S, L), r = (double)myR * scale;
+        const bool feas = r <= B;
+        const uint64_t kv = okey(v);
+        uint64_t kb = feas ? kv : ~0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t y = __shfl_xor_sync(0xffffffffu, kb, o);
+            kb = y < kb ? y : kb;
+        }
+        const uint32_t mb = __ballot_sync(0xffffffffu, feas && kv == kb);
+        const int ib = mb ? __ffs(mb) - 1 : -1;
+        const bool cand = !feas && v > -1.0 && (ib < 0 || kv < kb);
+        uint64_t ka = cand ? kv : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t y = __shfl_xor_sync(0xffffffffu, ka, o);
+            ka = y > ka ? y : ka;
+        }
+        const uint32_t ma = __ballot_sync(0xffffffffu, cand && kv == ka);
+        const int ia = ma ? __ffs(ma) - 1 : -1;
+        const double vb = __shfl_sync(0xffffffffu, v, ib >= 0 ? ib : 0);
+        const double Rb = __shfl_sync(0xffffffffu, r, ib >= 0 ? ib : 0);
+        const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
+        const double Ra = __shfl_sync(0xffffffffu, r, ia >= 0 ? ia : 0);
+        SearchState st;                       // every lane computes the same estimate
+        search_copy_scalars(st, S);
+        const double est = search_pilot_finish(st, ib, ib >= 0 ? vb : INFINITY, ib >= 0 ? Rb : 0.0,
+                                               ia, ia >= 0 ? va : -1.0, ia >= 0 ? Ra : 0.0, B);
         __syncwarp();
-        const double B = ctrl->budget;
-        if (ctrl->fixed) {
-            if (L == 0) {
-                sS.xb_probe = 0;
-                sS.R_xb = R[0];
-                sS.lambda = ctrl->lambda_fixed;
-                sS.phase = kSearchDone;
-                sS.rounds += 1;
-            }
-        } else if (sS.phase == kSearchPilot) {
-            __shared__ double sEst;
-            if (L == 0) {
-                sS.hi0 = __longlong_as_double((long long)ctrl->hi0_bits);
-                sEst = search_pilot_estimate(sS, R, B, ctrl->nb);
-            }
-            __syncwarp();
-            if (sS.have_grid && L > kSearchFirstDoublings) sS.probe[L] = search_pilot_probe(sEst, L);
-        } else {
-            if (L == 0) sS.hi0 = __longlong_as_double((long long)ctrl->hi0_bits);
-            __syncwarp();
-            const bool inr = L < sS.nprobe;
-            const double v = search_probe(sS, L);
-            const bool feas = inr && R[L] <= B;
-            double vb = feas ? v : INFINITY;
+        if (st.have_grid && L > kSearchFirstDoublings) S.probe[L] = search_pilot_probe(est, L);
+        __syncwarp();
+        if (L == 0) search_copy_scalars(S, st);
+    } else {
+        // one lane per probe folds the evaluations into the window (exact
+        // min / max of order keys), every lane walks, and lane L generates
+        // the probes along decision path L
+        const bool inr = L < S.nprobe;
+        const double v = search_probe(S, L);
+        const uint64_t kv = okey(v);
+        const bool feas = inr && myR <= Bfx;
+        uint64_t kb = feas ? kv : ~0ull;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) vb = fmin(vb, __shfl_xor_sync(0xffffffffu, vb, o));
-            const uint32_t mb = __ballot_sync(0xffffffffu, feas && v == vb);
-            const int ib = mb ? __ffs(mb) - 1 : -1;
-            const double xbn = (ib >= 0 && vb < sS.xb) ? vb : sS.xb;
-            const bool inf = inr && !(R[L] <= B) && v < xbn;
-            double va = inf ? v : -INFINITY;
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t y = __shfl_xor_sync(0xffffffffu, kb, o);
+            kb = y < kb ? y : kb;
+        }
+        const uint32_t mb = __ballot_sync(0xffffffffu, feas && kv == kb);
+        const int ib = mb ? __ffs(mb) - 1 : -1;
+        const double vb = __shfl_sync(0xffffffffu, v, ib >= 0 ? ib : 0);
+        const uint64_t kxb = okey(S.xb);
+        const uint64_t kxbn = (ib >= 0 && kb < kxb) ? kb : kxb;
+        const bool inf = inr && !feas && kv < kxbn;
+        uint64_t ka = inf ? kv : 0ull;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) va = fmax(va, __shfl_xor_sync(0xffffffffu, va, o));
-            const uint32_t ma = __ballot_sync(0xffffffffu, inf && v == va);
-            const int ia = ma ? __ffs(ma) - 1 : -1;
-            SearchState st;                       // every lane walks the same path
-            search_copy_scalars(st, sS);
-            search_window(st, vb, ib, ib >= 0 ? R[ib] : 0.0, va, ia);
-            const int go = search_advance(st, R, B);
-            if (go) {
-                sProbe[L] = search_first_unknown(st);
-                __syncwarp();
-                search_path(st, L, sProbe);
-                __syncwarp();
-                sS.probe[L] = sProbe[L];
-            }
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t y = __shfl_xor_sync(0xffffffffu, ka, o);
+            ka = y > ka ? y : ka;
+        }
+        const uint32_t ma = __ballot_sync(0xffffffffu, inf && kv == ka);
+        const int ia = ma ? __ffs(ma) - 1 : -1;
+        const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
+        SearchState st;                       // every lane walks the same path
+        search_copy_scalars(st, S);
+        search_window(st, ib >= 0 ? vb : INFINITY, ib, ib >= 0 ? Rfx[ib] : 0, va, ia);
+        const int go = search_advance(st, Rfx, Bfx);
+        __syncwarp();
+        if (go) {
+            __shared__ double sProbe[kSearchProbes];
+            sProbe[L] = search_first_unknown(st);
             __syncwarp();
-            if (L == 0) {
-                search_copy_scalars(sS, st);
-                if (st.infeasible) ctrl->status = KVQ_ERR_INFEASIBLE;
-            }
+            search_path(st, L, sProbe);
+            __syncwarp();
+            S.probe[L] = sProbe[L];
         }
         __syncwarp();
         if (L == 0) {
-            if (!ctrl->fixed && sS.xb_probe >= 0) ctrl->Rxb_fx = Rfx[sS.xb_probe];
-            search_copy_scalars(ctrl->s, sS);
-            ctrl->cnt[round & 1] = 0u;     // consumed; next round appends here
-            ctrl->ticket = 0u;
+            search_copy_scalars(S, st);
+            if (st.infeasible) ctrl->status = KVQ_ERR_INFEASIBLE;
         }
-        ctrl->s.probe[L] = sS.probe[L];
-        __threadfence();
     }
+    __syncwarp();
+    if (L == 0) {
+        if (!sC.fixed && S.xb_probe >= 0) ctrl->Rxb_fx = Rfx[S.xb_probe];
+        ctrl->cnt[round & 1] = 0u;     // consumed; the next round appends here
+        ctrl->ticket = 0u;
+    }
+    {
+        // the search state back to global memory, 16 bytes per lane
+        static_assert(sizeof(SearchState) % 16 == 0, "search state in 16-byte pieces");
+        const int4 *src = reinterpret_cast<const int4 *>(&S);
+        int4 *dst = reinterpret_cast<int4 *>(&ctrl->s);
+        for (int i = L; i < (int)(sizeof(SearchState) / 16); i += 32) dst[i] = src[i];
+    }
+    __threadfence();
 }
 
 // -------------------------------------------------------------------- emit
@@ -584,7 +660,7 @@ search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *_
 // the codebook (levels in slot order), k, D_r (sum of the chain's interval
 // distortions, reduced in a fixed tree) and H_r.  Sum D_r: per CTA in warp
 // order, then the last CTA adds the CTA partials with all its threads in a
-// fixed pattern.
+// fixed pattern and a fixed shuffle tree.
 __global__ void __launch_bounds__(kEmitWarps * 32)
 emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctrl,
             const float *__restrict__ rates, const uint32_t *__restrict__ masks,
@@ -659,11 +735,16 @@ emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctr
         sPart[threadIdx.x] = acc;
     }
     __syncthreads();
-    if (threadIdx.x != 0) return;
+    if (threadIdx.x >= 32) return;
+    // fixed tree: lane l adds its column of four, then a shuffle tree
     double dd = 0.0;
-    for (int k = 0; k < kEmitWarps * 32; ++k) dd += sPart[k];
+#pragma unroll
+    for (int k = 0; k < kEmitWarps; ++k) dd += sPart[k * 32 + threadIdx.x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dd += __shfl_down_sync(0xffffffffu, dd, o);
+    if (threadIdx.x != 0) return;
     Ctrl *n = ctrl;
-    const double R = n->s.R_xb;   // the rate the search tested (same per-block rates)
+    const double R = (double)n->s.R_xb / kRateScale;   // the rate the search tested
     const double lam = n->s.lambda;
     totals[0] = R;
     totals[1] = dd;

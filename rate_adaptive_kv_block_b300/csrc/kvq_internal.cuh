@@ -125,9 +125,10 @@ static __device__ constexpr DecodeTables kDecode = make_decode();
 
 // ---------------------------------------------------- allocation control
 // Lives at the start of the kvq_allocate workspace.
-struct Ctrl {
+struct alignas(16) Ctrl {
     SearchState s;          // lambda search (kvq_search.h)
     double budget;          // B (bits)
+    long long budget_fx;    // floor(B 2^20): R <= B iff R_fx <= budget_fx
     double eta;             // subgradient step
     double lambda_fixed;    // KVQ_SUBGRADIENT: the lambda of this step
     unsigned long long hi0_bits;   // max_r (c_max - c_min)^2 (double bits)
@@ -147,6 +148,7 @@ struct Ctrl {
     // integer adds are exact, so the sum does not depend on arrival order
     unsigned long long acc[32];
 };
+static_assert(sizeof(Ctrl) % 16 == 0, "control block in 16-byte pieces");
 constexpr double kRateScale = 1048576.0;   // 2^20
 
 // ------------------------------------------------------------ binary16 keys

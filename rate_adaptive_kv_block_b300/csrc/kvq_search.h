@@ -19,10 +19,20 @@
 // Round 0 probes lambda = 0, the first doublings of hi0 and a geometric grid
 // below hi0, which brackets the answer within a factor 2^1.5 at once.
 //
+// Rates are sums of per-block d_r H_r in fixed point (integers in units of
+// 2^-20 bit) and the budget is compared as floor(B 2^20), so R <= B is an
+// integer comparison with the same outcome as the real one.  The walk's
+// midpoints 0.5 (lo + hi) are binary64 values computed with integer
+// operations that round exactly as the binary64 sum does (half_sum), and
+// lambdas are compared through order-preserving integer keys: the control
+// runs on a GPU whose double-precision unit is slow, and every one of these
+// steps is on the search's critical path.
+//
 // Plain C++ usable on the host (tests) and the device (last CTA of a round).
 #pragma once
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
 
 #ifndef KVQ_HD
 #ifdef __CUDACC__
@@ -47,12 +57,12 @@ enum SearchPhase : int32_t {
     kSearchDone = 3,
 };
 
-struct SearchState {
+struct alignas(16) SearchState {
     double hi0;           // max_r (c_max - c_min)^2
     double lo, hi;        // bisection interval
     double xa, xb;        // known infeasible (largest) / feasible (smallest)
-    double R_xb;          // R at xb
     double lambda;        // the answer once done
+    long long R_xb;       // R at xb (fixed point)
     double probe[kSearchProbes];   // lambdas of the next round (walk phase)
     int32_t phase;
     int32_t step;         // bisection steps taken
@@ -67,12 +77,99 @@ struct SearchState {
     int32_t pad;
 };
 
+// ------------------------------------------------------- binary64 helpers
+KVQ_HD inline uint64_t dbits(double x) {
+    uint64_t u;
+    memcpy(&u, &x, 8);
+    return u;
+}
+KVQ_HD inline double dfrom(uint64_t u) {
+    double x;
+    memcpy(&x, &u, 8);
+    return x;
+}
+
+// Order-preserving key: okey(a) < okey(b) iff a < b (finite or infinite, not
+// NaN; -0 sorts just below +0, which no caller distinguishes).
+KVQ_HD inline uint64_t okey(double x) {
+    const uint64_t u = dbits(x);
+    return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+}
+
+// 0.5 * (a + b) for finite a, b >= 0, bit for bit as binary64 arithmetic
+// with round-to-nearest-even computes it: the sum rounded once, then halved
+// (exact for normal results).  Integer operations only; inputs outside the
+// fast path (a subnormal operand, a result that would not stay normal) take
+// the floating-point expression itself.
+KVQ_HD inline double half_sum(double a, double b) {
+    uint64_t ua = dbits(a), ub = dbits(b);
+    if (ua > ub) { const uint64_t t = ua; ua = ub; ub = t; }     // a <= b (non-negative)
+    const int eb = (int)(ub >> 52);
+    const int ea = (int)(ua >> 52);
+    const uint64_t frac = (1ull << 52) - 1;
+    if (eb == 0 || eb >= 2046 || (ea == 0 && ua != 0) || (ub >> 63) || (ua >> 63))
+        return 0.5 * (dfrom(ua) + dfrom(ub));
+    uint64_t sig;
+    int e;
+    if (ua == 0) {
+        sig = (ub & frac) | (1ull << 52);
+        e = eb;
+    } else {
+        const int d = eb - ea;
+        if (d >= 54) {                       // a below half an ulp of b
+            sig = (ub & frac) | (1ull << 52);
+            e = eb;
+        } else {
+            const uint64_t ma = ((ua & frac) | (1ull << 52)) << 10;   // bit 62 leading
+            const uint64_t mb = ((ub & frac) | (1ull << 52)) << 10;
+            uint64_t sticky = d ? ((ma & ((1ull << d) - 1)) != 0) : 0;
+            uint64_t m = mb + (ma >> d);                              // < 2^64
+            e = eb;
+            if (m >> 63) {
+                sticky |= m & 1ull;
+                m >>= 1;
+                ++e;
+            }
+            sig = m >> 10;                                            // 53 bits
+            const uint64_t r = m & 0x3ffull;
+            const bool up = r > 0x200ull || (r == 0x200ull && (sticky || (sig & 1ull)));
+            if (up) {
+                ++sig;
+                if (sig >> 53) {
+                    sig >>= 1;
+                    ++e;
+                }
+            }
+        }
+    }
+    if (e - 1 < 1 || e - 1 >= 2047) return 0.5 * (dfrom(ua) + dfrom(ub));
+    return dfrom(((uint64_t)(e - 1) << 52) | (sig & frac));
+}
+
+// x * 2^t for x = 0 or normal x > 0 whose result stays normal (exponent
+// arithmetic); anything else goes through ldexp.
+KVQ_HD inline double pow2_scale(double x, int t) {
+    const uint64_t u = dbits(x);
+    const int e = (int)(u >> 52);
+    if (u == 0) return 0.0;
+    if ((u >> 63) || e == 0 || e + t < 1 || e + t > 2046) return ldexp(x, t);
+    return dfrom(u + ((uint64_t)(int64_t)t << 52));
+}
+
+// floor(B 2^20) clamped to the int64 range: R <= B iff R_fx <= this, for
+// every fixed-point rate R_fx (B >= 0).
+KVQ_HD inline long long budget_fx(double B) {
+    const double v = floor(B * 1048576.0);
+    if (!(v < 9.2e18)) return 0x7fffffffffffffffll;
+    return (long long)v;
+}
+
 KVQ_HD inline void search_init(SearchState &s) {
     s.hi0 = 0.0;
     s.lo = s.hi = 0.0;
     s.xa = -1.0;
     s.xb = INFINITY;
-    s.R_xb = 0.0;
+    s.R_xb = 0;
     s.lambda = 0.0;
     for (int i = 0; i < kSearchProbes; ++i) s.probe[i] = 0.0;
     s.phase = kSearchBracket;
@@ -96,39 +193,43 @@ KVQ_HD inline void search_set_pilot(SearchState &s, int64_t nb, int stride) {
     }
 }
 
-// hi0 * 2^(-1.5 k), from exact operations: a power-of-two scaling, times
-// sqrt(1/2) (one correctly rounded constant) when k is odd
+// hi0 * 2^(-1.5 k): a power-of-two scaling, times sqrt(1/2) (one correctly
+// rounded constant) when k is odd
 KVQ_HD inline double search_grid(double hi0, int k) {
     const double odd = 0.70710678118654752440;
-    return (k & 1) ? ldexp(hi0 * odd, -(3 * k - 1) / 2) : ldexp(hi0, -(3 * k) / 2);
+    return (k & 1) ? pow2_scale(hi0 * odd, -(3 * k - 1) / 2) : pow2_scale(hi0, -(3 * k) / 2);
 }
 
-// Fine grid of round 0 around an estimate: est * f^((2k - 27) / 27), k = 0..27
+// Fine grid of round 0 around an estimate: est * 1.35^((2k - 27) / 27),
+// k = 0..27, the factor in single precision (the grid only places probes).
 KVQ_HD inline double search_fine(double est, int k) {
-    const double f = 1.35;
-    return est * pow(f, (double)(2 * k - 27) / 27.0);
+    const float e = (float)(2 * k - 27) * (0.43295940727610627f / 27.0f);   // log2(1.35) / 27
+    return est * (double)exp2f(e);
 }
 
 // lambda evaluated by probe p this round
 KVQ_HD inline double search_probe(const SearchState &s, int p) {
     if (s.phase == kSearchBracket || s.phase == kSearchPilot) {
         if (p == 0) return 0.0;
-        if (p <= kSearchFirstDoublings) return ldexp(s.hi0, p - 1);
+        if (p <= kSearchFirstDoublings) return pow2_scale(s.hi0, p - 1);
         if (s.phase == kSearchBracket && s.have_grid) return s.probe[p];
         return search_grid(s.hi0, p - kSearchFirstDoublings);
     }
     if (s.phase == kSearchDouble) {
         const int t = kSearchFirstDoublings + p;
-        return ldexp(s.hi0, t <= kSearchMaxDoublings ? t : kSearchMaxDoublings);
+        return pow2_scale(s.hi0, t <= kSearchMaxDoublings ? t : kSearchMaxDoublings);
     }
     return s.probe[p < s.nprobe ? p : 0];
 }
 
-// P(mid) if it follows from the window, else -1
-KVQ_HD inline int search_known(const SearchState &s, double mid) {
-    if (mid >= s.xb) return 1;
-    if (mid <= s.xa) return 0;
+// P(mid) if it follows from the window (keys of xa, xb), else -1
+KVQ_HD inline int search_known_k(uint64_t kmid, uint64_t kxa, uint64_t kxb) {
+    if (kmid >= kxb) return 1;
+    if (kmid <= kxa) return 0;
     return -1;
+}
+KVQ_HD inline int search_known(const SearchState &s, double mid) {
+    return search_known_k(okey(mid), okey(s.xa), okey(s.xb));
 }
 
 // The update is split so that a warp can run it with one lane per probe:
@@ -145,17 +246,18 @@ KVQ_HD inline int search_known(const SearchState &s, double mid) {
 // (xb, its probe) = smallest feasible evaluation; (xa, its probe) = largest
 // infeasible evaluation below xb.  Infeasible evaluations above xb contradict
 // monotonicity (a rounding tie) and are ignored.
-KVQ_HD inline void search_window(SearchState &s, double vb, int ib, double Rb, double va, int ia) {
+KVQ_HD inline void search_window(SearchState &s, double vb, int ib, long long Rb, double va,
+                                 int ia) {
     s.xa_probe = s.xb_probe = -1;
-    if (ib >= 0 && vb < s.xb) { s.xb = vb; s.xb_probe = ib; s.R_xb = Rb; }
-    if (ia >= 0 && va > s.xa && va < s.xb) { s.xa = va; s.xa_probe = ia; }
+    if (ib >= 0 && okey(vb) < okey(s.xb)) { s.xb = vb; s.xb_probe = ib; s.R_xb = Rb; }
+    if (ia >= 0 && okey(va) > okey(s.xa) && okey(va) < okey(s.xb)) { s.xa = va; s.xa_probe = ia; }
 }
 
 // Bracket decisions and the walk.  Returns 1 if probes must be generated.
-KVQ_HD inline int search_advance(SearchState &s, const double *R, double B) {
+KVQ_HD inline int search_advance(SearchState &s, const long long *R, long long Bfx) {
     s.rounds += 1;
     if (s.phase == kSearchBracket || s.phase == kSearchDouble) {
-        if (s.phase == kSearchBracket && R[0] <= B) {          // lambda = 0
+        if (s.phase == kSearchBracket && R[0] <= Bfx) {          // lambda = 0
             s.lo = s.hi = s.lambda = 0.0;
             s.xb = 0.0;
             s.xb_probe = 0;
@@ -168,7 +270,7 @@ KVQ_HD inline int search_advance(SearchState &s, const double *R, double B) {
                                                    : kSearchMaxDoublings - kSearchFirstDoublings;
         for (int p = (s.phase == kSearchBracket ? 1 : 0); p <= pmax && p < s.nprobe; ++p) {
             const int tt = s.phase == kSearchBracket ? p - 1 : kSearchFirstDoublings + p;
-            if (R[p] <= B) { t = tt; break; }
+            if (R[p] <= Bfx) { t = tt; break; }
         }
         if (t < 0) {
             if (s.phase == kSearchBracket) {
@@ -178,7 +280,7 @@ KVQ_HD inline int search_advance(SearchState &s, const double *R, double B) {
             }
             // infeasible at hi0 * 2^30: keep the choice there
             s.lo = 0.0;
-            s.hi = s.lambda = ldexp(s.hi0, kSearchMaxDoublings);
+            s.hi = s.lambda = pow2_scale(s.hi0, kSearchMaxDoublings);
             s.xb_probe = s.nprobe - 1;
             s.R_xb = R[s.nprobe - 1];
             s.infeasible = 1;
@@ -186,13 +288,14 @@ KVQ_HD inline int search_advance(SearchState &s, const double *R, double B) {
             return 0;
         }
         s.lo = 0.0;
-        s.hi = ldexp(s.hi0, t);
+        s.hi = pow2_scale(s.hi0, t);
         s.step = 0;
         s.phase = kSearchWalk;
     }
+    const uint64_t kxa = okey(s.xa), kxb = okey(s.xb);
     while (s.step < kSearchSteps) {
-        const double mid = 0.5 * (s.lo + s.hi);
-        const int k = search_known(s, mid);
+        const double mid = half_sum(s.lo, s.hi);
+        const int k = search_known_k(okey(mid), kxa, kxb);
         if (k < 0) break;
         if (k) s.hi = mid; else s.lo = mid;
         ++s.step;
@@ -207,15 +310,16 @@ KVQ_HD inline int search_advance(SearchState &s, const double *R, double B) {
 }
 
 // The first unknown midpoint (all paths start there).
-KVQ_HD inline double search_first_unknown(const SearchState &s) { return 0.5 * (s.lo + s.hi); }
+KVQ_HD inline double search_first_unknown(const SearchState &s) { return half_sum(s.lo, s.hi); }
 
 // Path of lane L: writes the unknown midpoints it meets into probe[id].
 KVQ_HD inline void search_path(const SearchState &s, int L, double *probe) {
+    const uint64_t kxa = okey(s.xa), kxb = okey(s.xb);
     double a = s.lo, b = s.hi;
     int u = 0, pre = 0;
     for (int dep = s.step; dep < kSearchSteps && u < 5; ++dep) {
-        const double mid = 0.5 * (a + b);
-        int k = search_known(s, mid);
+        const double mid = half_sum(a, b);
+        int k = search_known_k(okey(mid), kxa, kxb);
         if (k < 0) {
             probe[(1 << u) - 1 + pre] = mid;
             k = ((L >> (4 - u)) & 1) ? 0 : 1;   // bit 1: take the infeasible branch
@@ -229,35 +333,46 @@ KVQ_HD inline void search_path(const SearchState &s, int L, double *probe) {
 // Pilot round: estimate where R crosses B from the sample's rates (scaled to
 // all blocks); round 0 then puts its fine grid there.  Nothing is concluded
 // from the sample: the window only moves on evaluations of every block.
-// Returns the estimate, or 0 when there is none (round 0 keeps its default
-// grid).
-KVQ_HD inline double search_pilot_estimate(SearchState &s, const double *R, double B, int64_t nb) {
+// The estimate from the pilot's smallest feasible probe (ib, vb, Rb) and
+// largest infeasible probe below it (ia, va, Ra), rates scaled to all blocks
+// (bits); ib / ia = -1 when there is none.  Single precision: the estimate
+// only places probes.
+KVQ_HD inline double search_pilot_finish(SearchState &s, int ib, double vb, double Rb, int ia,
+                                         double va, double Ra, double B) {
     s.rounds += 1;
     s.xa_probe = s.xb_probe = -1;
-    const double scale = (double)nb / (double)(s.pilot_blocks > 0 ? s.pilot_blocks : 1);
-    int ib = -1;
-    double vb = INFINITY, Rb = 0.0;
-    for (int p = 0; p < kSearchProbes; ++p) {
-        const double v = search_probe(s, p), r = R[p] * scale;
-        if (r <= B && v < vb) { vb = v; ib = p; Rb = r; }
-    }
-    int ia = -1;
-    double va = -1.0, Ra = 0.0;
-    for (int p = 0; p < kSearchProbes; ++p) {
-        const double v = search_probe(s, p), r = R[p] * scale;
-        if (!(r <= B) && v < vb && v > va) { va = v; ia = p; Ra = r; }
-    }
     s.phase = kSearchBracket;
     s.have_grid = 0;
     if (ib <= 0 || !(vb > 0.0)) return 0.0;       // lambda = 0 likely, or no feasible probe
     double est;
     if (ia <= 0 || !(va > 0.0)) est = 0.5 * vb;
     else {
-        const double t = (Ra - B) / (Ra - Rb);        // log-linear interpolation
-        est = va * pow(vb / va, t > 0.0 ? (t < 1.0 ? t : 1.0) : 0.0);
+        const float fa = (float)Ra, fb = (float)Rb, fB = (float)B;
+        float t = (fa - fB) / (fa - fb);              // log-linear interpolation
+        t = t > 0.f ? (t < 1.f ? t : 1.f) : 0.f;
+        est = va * (double)exp2f(t * log2f((float)(vb / va)));
     }
     s.have_grid = 1;
     return est;
+}
+
+KVQ_HD inline double search_pilot_estimate(SearchState &s, const long long *R, double B,
+                                           int64_t nb) {
+    const double scale =
+        (double)nb / (double)(s.pilot_blocks > 0 ? s.pilot_blocks : 1) / 1048576.0;
+    int ib = -1;
+    double vb = INFINITY, Rb = 0.0;
+    for (int p = 0; p < kSearchProbes; ++p) {
+        const double v = search_probe(s, p), r = (double)R[p] * scale;
+        if (r <= B && v < vb) { vb = v; ib = p; Rb = r; }
+    }
+    int ia = -1;
+    double va = -1.0, Ra = 0.0;
+    for (int p = 0; p < kSearchProbes; ++p) {
+        const double v = search_probe(s, p), r = (double)R[p] * scale;
+        if (!(r <= B) && v < vb && v > va) { va = v; ia = p; Ra = r; }
+    }
+    return search_pilot_finish(s, ib, vb, Rb, ia, va, Ra, B);
 }
 
 // Probe p of round 0 around the estimate (p > kSearchFirstDoublings).
@@ -274,8 +389,9 @@ KVQ_HD inline void search_copy_scalars(SearchState &d, const SearchState &s) {
     d.have_grid = s.have_grid;
 }
 
-// Single-thread version (host tests).  nb: number of blocks (pilot scaling).
-KVQ_HD inline void search_update(SearchState &s, const double *R, double B, int64_t nb = 0) {
+// Single-thread version (host tests).  R: fixed-point rates; B: the budget in
+// bits; nb: number of blocks (pilot scaling).
+KVQ_HD inline void search_update(SearchState &s, const long long *R, double B, int64_t nb = 0) {
     if (s.phase == kSearchPilot) {
         const double est = search_pilot_estimate(s, R, B, nb);
         if (s.have_grid)
@@ -283,19 +399,21 @@ KVQ_HD inline void search_update(SearchState &s, const double *R, double B, int6
                 s.probe[p] = search_pilot_probe(est, p);
         return;
     }
+    const long long Bfx = budget_fx(B);
     int ib = -1, ia = -1;
-    double vb = INFINITY, va = -INFINITY, Rb = 0.0;
+    double vb = INFINITY, va = -INFINITY;
+    long long Rb = 0;
     for (int p = 0; p < s.nprobe; ++p) {
         const double v = search_probe(s, p);
-        if (R[p] <= B && v < vb) { vb = v; ib = p; Rb = R[p]; }
+        if (R[p] <= Bfx && okey(v) < okey(vb)) { vb = v; ib = p; Rb = R[p]; }
     }
-    const double xb_next = (ib >= 0 && vb < s.xb) ? vb : s.xb;
+    const double xb_next = (ib >= 0 && okey(vb) < okey(s.xb)) ? vb : s.xb;
     for (int p = 0; p < s.nprobe; ++p) {
         const double v = search_probe(s, p);
-        if (!(R[p] <= B) && v > va && v < xb_next) { va = v; ia = p; }
+        if (!(R[p] <= Bfx) && okey(v) > okey(va) && okey(v) < okey(xb_next)) { va = v; ia = p; }
     }
     search_window(s, vb, ib, Rb, va, ia);
-    if (search_advance(s, R, B)) {
+    if (search_advance(s, R, Bfx)) {
         double probe[kSearchProbes];
         const double first = search_first_unknown(s);
         for (int p = 0; p < kSearchProbes; ++p) probe[p] = first;

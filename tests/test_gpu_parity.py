@@ -230,3 +230,31 @@ def test_full_size_sampled_slabs(name, bi):
         gc.check_stats(g, oracle.stats(xs, w.G))
         gc.check_choice(g, xs, w.G, w.s, lam)
         gc.check_codes(g, xs, w.G, 11, (h * w.T + 32 * tb) * w.D)
+
+
+# ------------------------------------------------------ CUDA graph capture
+
+def test_graph_capture_replays_the_eager_results():
+    """The three calls captured as one CUDA graph (after a first eager call on
+    the device) and replayed on new data give the eager results bit for bit."""
+    _need_gpu()
+    w = synth.workload("llama3_8b_layer", T=1024)
+    L = kvq.Layout(w.S, w.T, w.D, w.G)
+    B = w.budgets[0] * w.entries
+    xd = synth.make_torch(w, seed=31)
+    gbuf = kvq.Buffers(L, w.s)
+    kvq.quantize(xd, L, B, w.s, seed=5, buf=gbuf)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        kvq.quantize(xd, L, B, w.s, seed=5, buf=gbuf)
+    for sd in (32, 33):
+        xn = synth.make_torch(w, seed=sd)
+        xd.copy_(xn)
+        graph.replay()
+        ebuf = kvq.Buffers(L, w.s)
+        kvq.quantize(xn, L, B, w.s, seed=5, buf=ebuf)
+        torch.cuda.synchronize()
+        for key in ("codebook", "k", "D_r", "H_r", "totals", "lam", "status", "codes"):
+            a, b = getattr(gbuf, key), getattr(ebuf, key)
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), key

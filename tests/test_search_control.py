@@ -1,13 +1,16 @@
 """The lambda-search control (csrc/kvq_search.h, compiled for the host here)
 walks exactly the fixed 40-step bisection: on monotone step functions R it
 returns the same lambda as the sequential bisection, bit for bit, whatever the
-breakpoints; and it needs far fewer rounds of evaluations than 40."""
+breakpoints; and it needs far fewer rounds of evaluations than 40.  Its
+integer helpers round and compare exactly as binary64 arithmetic does."""
 import ctypes as C
 import os
 import random
+import struct
 import subprocess
 import tempfile
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -15,6 +18,29 @@ CSRC = os.path.join(ROOT, "rate_adaptive_kv_block_b300", "csrc")
 
 SHIM = r'''
 #include "kvq_search.h"
+#include <math.h>
+static long long fx(double r) { return llround(r * 1048576.0); }
+// mismatches of half_sum against the floating-point expression over n pairs
+extern "C" long kvqs_half_sum_check(const double *a, const double *b, long n, long *first) {
+    long bad = 0;
+    *first = -1;
+    for (long i = 0; i < n; ++i) {
+        const double want = 0.5 * (a[i] + b[i]);
+        const double got = kvq::half_sum(a[i], b[i]);
+        if (kvq::dbits(want) != kvq::dbits(got)) { if (*first < 0) *first = i; ++bad; }
+    }
+    return bad;
+}
+extern "C" long kvqs_okey_check(const double *a, const double *b, long n) {
+    long bad = 0;
+    for (long i = 0; i < n; ++i) {
+        if ((kvq::okey(a[i]) < kvq::okey(b[i])) != (a[i] < b[i])) ++bad;
+        if ((kvq::okey(a[i]) == kvq::okey(b[i])) != (kvq::dbits(a[i]) == kvq::dbits(b[i]))) ++bad;
+    }
+    return bad;
+}
+extern "C" double kvqs_pow2_scale(double x, int t) { return kvq::pow2_scale(x, t); }
+extern "C" long long kvqs_budget_fx(double B) { return kvq::budget_fx(B); }
 static double Rfun(double lam, int nbp, const double *bl, const double *br, double R0) {
     double r = R0;
     for (int i = 0; i < nbp; ++i) if (lam >= bl[i]) r = br[i];
@@ -31,16 +57,16 @@ extern "C" int kvqs_run(double hi0, double B, int nbp, const double *bl, const d
     if (pilot_bias > -1.0) kvq::search_set_pilot(s, nb, 16);
     int r = 0;
     for (; r < 64 && s.phase != kvq::kSearchDone; ++r) {
-        double R[kvq::kSearchProbes];
+        long long R[kvq::kSearchProbes];
         const bool pilot = s.phase == kvq::kSearchPilot;
         for (int p = 0; p < kvq::kSearchProbes; ++p) {
             double v = p < s.nprobe || pilot ? Rfun(kvq::search_probe(s, p), nbp, bl, br, R0) : 0.0;
             if (pilot) v = v * (1.0 + pilot_bias) * (double)s.pilot_blocks / (double)nb;
-            R[p] = v;
+            R[p] = fx(v);
         }
         kvq::search_update(s, R, B, nb);
     }
-    out[0] = s.lambda; out[1] = s.xb; out[2] = s.R_xb; out[3] = r;
+    out[0] = s.lambda; out[1] = s.xb; out[2] = (double)s.R_xb / 1048576.0; out[3] = r;
     out[4] = s.infeasible; out[5] = s.step;
     return s.phase == kvq::kSearchDone ? 0 : 1;
 }
@@ -57,6 +83,14 @@ def lib():
     subprocess.check_call(["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fPIC", "-shared",
                            "-I", CSRC, "-o", so, src])
     L = C.CDLL(so)
+    L.kvqs_half_sum_check.restype = C.c_long
+    L.kvqs_half_sum_check.argtypes = [C.c_void_p, C.c_void_p, C.c_long, C.POINTER(C.c_long)]
+    L.kvqs_okey_check.restype = C.c_long
+    L.kvqs_okey_check.argtypes = [C.c_void_p, C.c_void_p, C.c_long]
+    L.kvqs_pow2_scale.restype = C.c_double
+    L.kvqs_pow2_scale.argtypes = [C.c_double, C.c_int]
+    L.kvqs_budget_fx.restype = C.c_longlong
+    L.kvqs_budget_fx.argtypes = [C.c_double]
     L.kvqs_run.restype = C.c_int
     L.kvqs_run.argtypes = [C.c_double, C.c_double, C.c_int, C.c_void_p, C.c_void_p, C.c_double,
                            C.c_void_p, C.c_double]
@@ -110,7 +144,8 @@ def random_case(rng):
     br, r = [], R0
     for _ in bl:
         r -= rng.uniform(0, 2 * R0 / n)
-        br.append(max(r, 0.0))
+        # rates are fixed-point sums (multiples of 2^-20 bit)
+        br.append(round(max(r, 0.0) * 2 ** 20) / 2 ** 20)
     return hi0, bl, br, R0
 
 
@@ -163,3 +198,82 @@ def test_budget_at_zero_lambda_and_large_hi(lib):
     # hi0 = 0 (all blocks constant): R = 0 <= B
     out = run(lib, 0.0, 0.0, [], [], 0.0)
     assert out[0] == 0.0
+
+
+def _d(u):
+    return struct.unpack("<d", struct.pack("<Q", u))[0]
+
+
+def _pairs(rng, n):
+    """Non-negative binary64 pairs that exercise every rounding case of
+    a + b: random exponent gaps 0..60, random and extreme significands,
+    exact half-ulp ties with odd and even b, carries, zeros, and a > b."""
+    e = rng.integers(900, 1150, n)
+    gap = rng.integers(0, 61, n)
+    fa = rng.integers(0, 1 << 52, n, dtype=np.uint64)
+    fb = rng.integers(0, 1 << 52, n, dtype=np.uint64)
+    kind = rng.integers(0, 6, n)
+    ones = np.uint64((1 << 52) - 1)
+    fa = np.where(kind == 1, ones, fa)                       # all-ones: carries
+    fb = np.where(kind == 1, ones, fb)
+    fa = np.where(kind == 2, np.uint64(0), fa)               # a a power of two
+    ub = (e.astype(np.uint64) << np.uint64(52)) | fb
+    ua = (np.maximum(e - gap, 1).astype(np.uint64) << np.uint64(52)) | fa
+    # ties: a exactly half an ulp of b (gap 53, a a power of two), b odd or even
+    tie = kind == 3
+    ua = np.where(tie, ((e - 53).astype(np.uint64) << np.uint64(52)), ua)
+    ub = np.where(tie & (rng.integers(0, 2, n) == 1), ub | np.uint64(1), ub)
+    a = ua.view(np.float64).copy()
+    b = ub.view(np.float64).copy()
+    a = np.where(kind == 4, 0.0, a)                          # lo = 0
+    swap = rng.integers(0, 2, n) == 1                        # either order
+    a2 = np.where(swap, b, a)
+    b2 = np.where(swap, a, b)
+    a2 = np.where(kind == 5, b2, a2)                         # a == b
+    return np.ascontiguousarray(a2), np.ascontiguousarray(b2)
+
+
+def test_half_sum_rounds_as_binary64(lib):
+    rng = np.random.default_rng(3)
+    a, b = _pairs(rng, 400000)
+    first = C.c_long()
+    bad = lib.kvqs_half_sum_check(a.ctypes.data, b.ctypes.data, len(a), C.byref(first))
+    assert bad == 0, (bad, a[first.value], b[first.value])
+    # the midpoints of real bisections over random brackets
+    xs, ys = [], []
+    r = random.Random(1)
+    for _ in range(2000):
+        lo, hi = 0.0, r.uniform(1e-9, 1e9)
+        for _ in range(40):
+            mid = 0.5 * (lo + hi)
+            xs.append(lo)
+            ys.append(hi)
+            if r.random() < 0.5:
+                hi = mid
+            else:
+                lo = mid
+    xa, ya = np.array(xs), np.array(ys)
+    assert lib.kvqs_half_sum_check(xa.ctypes.data, ya.ctypes.data, len(xa), C.byref(first)) == 0
+
+
+def test_okey_orders_as_binary64(lib):
+    rng = np.random.default_rng(4)
+    a = rng.standard_normal(200000) * 10.0 ** rng.integers(-30, 30, 200000)
+    b = np.where(rng.random(200000) < 0.2, a, rng.standard_normal(200000) * 1e3)
+    a[:4] = [np.inf, -np.inf, -1.0, 0.0]
+    b[:4] = [1e308, -1e308, -1.0, 1e-300]
+    assert lib.kvqs_okey_check(a.ctypes.data, b.ctypes.data, len(a)) == 0
+
+
+def test_pow2_scale_and_budget_fixed_point(lib):
+    for x in (0.0, 1.0, 3.7e-12, 1.234e10, _d(0x0010000000000000), _d(1)):
+        for t in (-40, -3, 0, 5, 30):
+            assert lib.kvqs_pow2_scale(x, t) == np.ldexp(x, t)
+    assert lib.kvqs_budget_fx(2.5) == 2621440
+    assert lib.kvqs_budget_fx(0.1) == int(np.floor(0.1 * 2 ** 20))
+    assert lib.kvqs_budget_fx(1e300) == 2 ** 63 - 1
+    for B in (0.0, 3.0, 83886080.0, 123456.789):
+        fxB = lib.kvqs_budget_fx(B)
+        # R <= B  iff  R_fx <= floor(B 2^20), for integer R_fx
+        for R in (fxB - 1, fxB, fxB + 1):
+            assert (R / 2 ** 20 <= B) == (R <= fxB)

@@ -102,10 +102,16 @@ def test_static_scratch_back_to_back_on_one_stream():
 
 def test_static_scratch_limit_rejected_on_host():
     """Layouts over the fixed scratch size fail before any CUDA call."""
-    big = kvq.Layout(1, 32 * 29743, 8, 8)
+    lo, hi = 1, 1 << 20                  # largest number of 8-entry-wide blocks that fits
+    while lo < hi:
+        m = (lo + hi + 1) // 2
+        if kvq.kvq_workspace_bytes(kvq.Layout(1, 32 * m, 8, 8), 16) <= kvq.KVQ_STATIC_WORKSPACE_BYTES:
+            lo = m
+        else:
+            hi = m - 1
+    assert 29000 <= lo <= 30000          # the limit the header states
+    big = kvq.Layout(1, 32 * (lo + 1), 8, 8)
     assert kvq.kvq_workspace_bytes(big, 16) > kvq.KVQ_STATIC_WORKSPACE_BYTES
-    fits = kvq.Layout(1, 32 * 29742, 8, 8)
-    assert kvq.kvq_workspace_bytes(fits, 16) <= kvq.KVQ_STATIC_WORKSPACE_BYTES
     rc = kvq.lib().kvq_allocate_static(None, big.c(), 16, 1.0, kvq.KVQ_BISECT40, 0.0, None,
                                        None, None, None, None, None, None, None)
     assert rc == kvq.KVQ_ERR_TOO_LARGE
