@@ -47,6 +47,7 @@ extern "C" {
 #define KVQ_ERR_NONFINITE 3   /* device status: a block holds NaN or +-Inf */
 #define KVQ_ERR_INFEASIBLE 4  /* device status: budget unreachable         */
 #define KVQ_ERR_TOO_LARGE 5   /* kvq_allocate_static: layout over its limit  */
+#define KVQ_ERR_TIMEOUT 6     /* device status: a grid-wide wait gave up     */
 
 /* lambda modes of kvq_allocate */
 #define KVQ_BISECT40 0        /* global lambda by the 40-step bisection      */

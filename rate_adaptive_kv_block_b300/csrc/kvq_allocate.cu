@@ -36,7 +36,13 @@ namespace kvq {
 
 constexpr int kRoundWarps = 4;        // s >= 16: DP path A only
 constexpr int kRoundWarpsGen = 2;     // s < 16: path B possible
-constexpr int kEmitWarps = 4;
+constexpr int kMaxGrid = 4096;        // CTAs of the persistent search kernel (at most)
+
+// CTAs of the persistent search kernel resident at once, per device (set by
+// allocate_init, which the API runs once per device before the first launch)
+constexpr int kMaxDevices = 64;
+static int g_resident[kMaxDevices];
+static int g_resident_gen[kMaxDevices];
 
 // ---------------------------------------------------------------- workspace
 struct Workspace {
@@ -48,7 +54,7 @@ struct Workspace {
     uint32_t *mask_hi;    // [nblk]       chain at xb
     int32_t *evr;         // [nblk]       round that last evaluated the block
     int32_t *list;        // [2][nblk]    candidate lists (ping-pong)
-    double *epartial;     // [emit CTAs]
+    double *epartial;     // [grid]       per-CTA sums of D_r
 };
 
 static size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -61,7 +67,7 @@ size_t workspace_bytes(int64_t nb, int s) {
     b += 3 * align_up((size_t)nb * sizeof(float));
     b += align_up((size_t)nb * sizeof(int32_t));
     b += align_up((size_t)nb * 2 * sizeof(int32_t));
-    b += align_up((size_t)((nb + kEmitWarps - 1) / kEmitWarps) * sizeof(double));
+    b += align_up((size_t)(nb < kMaxGrid ? nb : kMaxGrid) * sizeof(double));
     return b;
 }
 
@@ -97,6 +103,7 @@ __global__ void ctrl_init_kernel(Ctrl *c, const StatsHeader *hdr, double budget,
                                  int mode, const double *lambda_in, int64_t nb) {
     if (threadIdx.x != 0) return;
     search_init(c->s);
+    c->s.hi0 = __longlong_as_double((long long)hdr->hi0_bits);
     c->nb = nb;
     if (mode != KVQ_SUBGRADIENT && nb >= kPilotMinBlocks) search_set_pilot(c->s, nb, kPilotStride);
     c->budget = budget;
@@ -110,28 +117,12 @@ __global__ void ctrl_init_kernel(Ctrl *c, const StatsHeader *hdr, double budget,
     c->mode = mode;
     c->ticket = 0u;
     c->ticket_emit = 0u;
+    c->gen = 0u;
+    c->err = 0u;
     for (int i = 0; i < 32; ++i) c->acc[i] = 0ull;
     for (int i = 0; i < 16; ++i) c->active[i] = 0u;
     c->Rxb_fx = 0;
     c->cnt[0] = c->cnt[1] = 0u;
-}
-
-// ------------------------------------------------------- probe lambda values
-__device__ __forceinline__ double probe_lambda(const Ctrl *c, int lane) {
-    if (c->fixed) return c->lambda_fixed;
-    const int ph = c->s.phase;
-    const double hi0 = __longlong_as_double((long long)c->hi0_bits);
-    if (ph == kSearchBracket || ph == kSearchPilot) {
-        if (lane == 0) return 0.0;
-        if (lane <= kSearchFirstDoublings) return ldexp(hi0, lane - 1);
-        if (ph == kSearchBracket && c->s.have_grid) return c->s.probe[lane];
-        return search_grid(hi0, lane - kSearchFirstDoublings);
-    }
-    if (ph == kSearchDouble) {
-        const int t = kSearchFirstDoublings + lane;
-        return ldexp(hi0, t <= kSearchMaxDoublings ? t : kSearchMaxDoublings);
-    }
-    return c->s.probe[lane < c->s.nprobe ? lane : 0];
 }
 
 // ---------------------------------------------------------------- DP path A
@@ -368,7 +359,7 @@ __device__ void dp_path_b(const float *__restrict__ tb, float lam, int s,
     mask = sM[p * 32 + lane];
 }
 
-// ------------------------------------------------------------- search round
+// ------------------------------------------------------------ search kernel
 template <bool GENERAL>
 struct RoundCfg {
     static constexpr int kWarps = GENERAL ? kRoundWarpsGen : kRoundWarps;
@@ -380,312 +371,363 @@ struct RoundCfg {
         (size_t)kWarps * 32 * sizeof(long long) + (size_t)kWarps * 32 * sizeof(float);
 };
 
-// One round.  Persistent: the grid's warps take the round's blocks in turn
-// (all blocks in the bracket rounds, a sample in the pilot round, in the walk
-// only the blocks evaluated in the previous round -- a block that was not
-// is constant across the window and stays so).  Each lane accumulates, per
-// probe, the change of its blocks' d_r H_r against their value at xb, in
-// fixed point; the control adds the sums to the total at xb.
+// Grid-wide hand-over between rounds: the last CTA of a round publishes the
+// next round's state and then the generation number with a release store;
+// the other CTAs wait for it with acquire loads.  Every CTA of the grid is
+// resident (cooperative launch), and the wait is bounded all the same.
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+constexpr uint32_t kSpinLimit = 1u << 22;     // polls, at most
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // and at most one second
+constexpr int kMaxRounds = 16;
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Stage the control block in shared memory with coalesced 16-byte loads from
+// L2 (other CTAs write it during the kernel; L1 is not coherent).
+__device__ __forceinline__ void stage_ctrl(Ctrl &dst, const Ctrl *src) {
+    const int4 *s4 = reinterpret_cast<const int4 *>(src);
+    int4 *d4 = reinterpret_cast<int4 *>(&dst);
+    for (int i = threadIdx.x; i < (int)(sizeof(Ctrl) / 16); i += blockDim.x) d4[i] = __ldcg(s4 + i);
+}
+
+// The whole search and the emit in one persistent, cooperative launch.
+//
+// Each round: the grid's warps take the round's blocks (all blocks in the
+// bracket rounds, a sample in the pilot round, in the walk only the blocks
+// evaluated in the previous round -- a block that was not is constant across
+// the window and stays so).  Each lane accumulates, per probe, the change of
+// its blocks' d_r H_r against their value at xb, in fixed point; the last
+// CTA to finish adds the sums to the total at xb and advances the search;
+// the next round starts when it publishes the new state.
+//
+// Emit (after the last round), one warp per block, lane t = slot t: the
+// chain at the final lambda becomes the codebook (levels in slot order), k,
+// D_r (sum of the chain's interval distortions, reduced in a fixed tree) and
+// H_r.  Sum D_r: per CTA in warp and block order, then the last CTA adds the
+// CTA partials in a fixed pattern and a fixed shuffle tree.
 template <bool GENERAL>
 __global__ void __launch_bounds__(RoundCfg<GENERAL>::kWarps * 32)
-search_round_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restrict__ ctrl,
-                    float *__restrict__ rates, uint32_t *__restrict__ masks,
-                    float *__restrict__ rate_lo, float *__restrict__ rate_hi,
-                    uint32_t *__restrict__ mask_hi, int32_t *__restrict__ evr,
-                    int32_t *__restrict__ list) {
+search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restrict__ ctrl,
+              float *__restrict__ rates, uint32_t *__restrict__ masks,
+              float *__restrict__ rate_lo, float *__restrict__ rate_hi,
+              uint32_t *__restrict__ mask_hi, int32_t *__restrict__ evr,
+              int32_t *__restrict__ list, double *__restrict__ epartial,
+              float *__restrict__ codebook, uint8_t *__restrict__ kout, float *__restrict__ Dr,
+              float *__restrict__ Hr, double *__restrict__ totals, double *__restrict__ lambda_out,
+              int32_t *__restrict__ status) {
     using Cfg = RoundCfg<GENERAL>;
     constexpr int W = Cfg::kWarps;
     extern __shared__ __align__(16) float smem[];
-    if (ctrl->s.phase == kSearchDone) return;
-    const int fixed = ctrl->fixed, phase = ctrl->s.phase;
-    const int xa_probe = ctrl->s.xa_probe, xb_probe = ctrl->s.xb_probe;
-    const int round = ctrl->s.rounds;
-    const bool walk = !fixed && phase == kSearchWalk;
-    const bool pilot = !fixed && phase == kSearchPilot;
-    const int stride = ctrl->s.pilot_stride;
-    const int32_t *lin = list + (size_t)(round & 1) * nb;
-    int32_t *lout = list + (size_t)((round + 1) & 1) * nb;
-    const int64_t nitems = walk ? (int64_t)ctrl->cnt[round & 1]
-                                : pilot ? (int64_t)ctrl->s.pilot_blocks : nb;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     float *sTbl = smem + w * kTblStride;
     float *sState = smem + W * kTblStride + w * Cfg::kStateFloats;
     long long *sSum = reinterpret_cast<long long *>(smem + W * (kTblStride + Cfg::kStateFloats));
     float *sDiag = reinterpret_cast<float *>(sSum + W * 32) + w * 32;
-    __shared__ bool is_last;
+    __shared__ __align__(16) Ctrl sC;
+    __shared__ bool is_last, timed_out;
     __shared__ uint32_t sAct, sN;
     __shared__ int32_t sList[W * 32];
     __shared__ float sRb[W * 32];
-    if (threadIdx.x == 0) sAct = 0u;
-    const float lam = (float)probe_lambda(ctrl, lane);
-    long long my_sum = 0;
-    // Items in chunks of one per thread: item it = blockIdx.x + gridDim.x *
-    // (c * blockDim.x + threadIdx.x), so consecutive CTAs take consecutive
-    // items.  Phase A (a thread per item) carries the walk's per-block state
-    // to the new window ends and keeps the blocks whose rate can still
-    // change; phase B (a warp per kept block) runs the DP.
-    for (int64_t c0 = 0; (int64_t)blockIdx.x + (int64_t)gridDim.x * c0 < nitems;
-         c0 += blockDim.x) {
-        if (threadIdx.x == 0) sN = 0u;
+
+    for (int iter = 0; iter < kMaxRounds; ++iter) {
+        stage_ctrl(sC, ctrl);
+        if (threadIdx.x == 0) sAct = 0u;
         __syncthreads();
-        const int64_t it = (int64_t)blockIdx.x + (int64_t)gridDim.x * (c0 + threadIdx.x);
-        bool act = false;
-        int32_t bsel = 0;
-        if (it < nitems) {
-            act = true;
-            if (walk) {
-                // evaluated in the previous round: its rates at the new window
-                // ends; the rate is non-increasing in lambda, so equal rates
-                // at both ends mean the chain is constant inside the window
-                const int32_t b = lin[it];
-                float ra = rate_lo[b], rb = rate_hi[b];
-                if (xa_probe >= 0) ra = rates[(int64_t)b * 32 + xa_probe];
-                if (xb_probe >= 0) {
-                    rb = rates[(int64_t)b * 32 + xb_probe];
-                    mask_hi[b] = masks[(int64_t)b * 32 + xb_probe];
-                }
-                rate_lo[b] = ra;
-                rate_hi[b] = rb;
-                act = ra != rb;
-                bsel = b;
-                if (act) {
-                    const uint32_t slot = atomicAdd(&sN, 1u);
-                    sList[slot] = b;
-                    sRb[slot] = rb;
-                }
-            } else {
-                bsel = (int32_t)(pilot ? it * stride : it);
-                const uint32_t slot = atomicAdd(&sN, 1u);
-                sList[slot] = bsel;
-                sRb[slot] = 0.f;
-            }
-            if (act) evr[bsel] = round;
-        }
-        // room in the next round's list: one atomic per warp; the entries are
-        // written after the DP, so its latency is hidden
-        uint32_t lbase = 0, lrank = 0;
-        if (!pilot) {
-            const uint32_t am = __ballot_sync(0xffffffffu, act);
-            lrank = __popc(am & ((1u << lane) - 1u));
-            if (lane == 0 && am) lbase = atomicAdd(&ctrl->cnt[(round + 1) & 1], (uint32_t)__popc(am));
-            lbase = __shfl_sync(0xffffffffu, lbase, 0);
-        }
-        __syncthreads();
-        const uint32_t n = sN;
-        for (uint32_t q = w; q < n; q += W) {
-            const int64_t b = sList[q];
-            const float rb = sRb[q];
-            const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
-            float4 *dst = reinterpret_cast<float4 *>(sTbl);
-            for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
-            __syncwarp();
-            const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
-            float rate;
-            uint32_t mask;
-            if (mp <= 1) {
-                rate = 0.f;
-                mask = 1u;
-            } else {
-                const int C = mp > s ? mp - s : 0;
-                if (!GENERAL || C == 0 || (C == 1 && mp == 17)) {
-                    dp_a_diag(sTbl, sDiag, lane);
-                    dp_path_a(sTbl, lam, C, sState, sState + kPairs * 32, sDiag, lane, rate, mask);
+        if (sC.s.phase == kSearchDone) break;
+        const int fixed = sC.fixed, phase = sC.s.phase;
+        const int xa_probe = sC.s.xa_probe, xb_probe = sC.s.xb_probe;
+        const int round = sC.s.rounds;
+        const bool walk = !fixed && phase == kSearchWalk;
+        const bool pilot = !fixed && phase == kSearchPilot;
+        const int stride = sC.s.pilot_stride;
+        const int32_t *lin = list + (size_t)(round & 1) * nb;
+        int32_t *lout = list + (size_t)((round + 1) & 1) * nb;
+        const int64_t nitems = walk ? (int64_t)sC.cnt[round & 1]
+                                    : pilot ? (int64_t)sC.s.pilot_blocks : nb;
+        const float lam = (float)(fixed ? sC.lambda_fixed : search_probe(sC.s, lane));
+        long long my_sum = 0;
+        // Items in chunks of one per thread: item it = blockIdx.x + gridDim.x
+        // * (c * blockDim.x + threadIdx.x), so consecutive CTAs take
+        // consecutive items.  Phase A (a thread per item) carries the walk's
+        // per-block state to the new window ends and keeps the blocks whose
+        // rate can still change; phase B (a warp per kept block) runs the DP.
+        for (int64_t c0 = 0; (int64_t)blockIdx.x + (int64_t)gridDim.x * c0 < nitems;
+             c0 += blockDim.x) {
+            if (threadIdx.x == 0) sN = 0u;
+            __syncthreads();
+            const int64_t it = (int64_t)blockIdx.x + (int64_t)gridDim.x * (c0 + threadIdx.x);
+            bool act = false;
+            int32_t bsel = 0;
+            if (it < nitems) {
+                act = true;
+                if (walk) {
+                    // evaluated in the previous round: its rates at the new
+                    // window ends; the rate is non-increasing in lambda, so
+                    // equal rates at both ends mean the chain is constant
+                    // inside the window
+                    const int32_t b = __ldcg(&lin[it]);
+                    float ra = __ldcg(&rate_lo[b]), rb = __ldcg(&rate_hi[b]);
+                    if (xa_probe >= 0) ra = __ldcg(&rates[(int64_t)b * 32 + xa_probe]);
+                    if (xb_probe >= 0) {
+                        rb = __ldcg(&rates[(int64_t)b * 32 + xb_probe]);
+                        mask_hi[b] = __ldcg(&masks[(int64_t)b * 32 + xb_probe]);
+                    }
+                    rate_lo[b] = ra;
+                    rate_hi[b] = rb;
+                    act = ra != rb;
+                    bsel = b;
+                    if (act) {
+                        const uint32_t slot = atomicAdd(&sN, 1u);
+                        sList[slot] = b;
+                        sRb[slot] = rb;
+                    }
                 } else {
-                    dp_path_b(sTbl, lam, s, sState, sState + kPairs * 32,
-                              reinterpret_cast<uint32_t *>(sState + 2 * kPairs * 32), lane, rate,
-                              mask);
+                    bsel = (int32_t)(pilot ? it * stride : it);
+                    const uint32_t slot = atomicAdd(&sN, 1u);
+                    sList[slot] = bsel;
+                    sRb[slot] = 0.f;
+                }
+                if (act) evr[bsel] = round;
+            }
+            // room in the next round's list: one atomic per warp; the entries
+            // are written after the DP, so its latency is hidden
+            uint32_t lbase = 0, lrank = 0;
+            if (!pilot) {
+                const uint32_t am = __ballot_sync(0xffffffffu, act);
+                lrank = __popc(am & ((1u << lane) - 1u));
+                if (lane == 0 && am)
+                    lbase = atomicAdd(&ctrl->cnt[(round + 1) & 1], (uint32_t)__popc(am));
+                lbase = __shfl_sync(0xffffffffu, lbase, 0);
+            }
+            __syncthreads();
+            const uint32_t n = sN;
+            for (uint32_t q = w; q < n; q += W) {
+                const int64_t b = sList[q];
+                const float rb = sRb[q];
+                const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
+                float4 *dst = reinterpret_cast<float4 *>(sTbl);
+                for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
+                __syncwarp();
+                const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
+                float rate;
+                uint32_t mask;
+                if (mp <= 1) {
+                    rate = 0.f;
+                    mask = 1u;
+                } else {
+                    const int C = mp > s ? mp - s : 0;
+                    if (!GENERAL || C == 0 || (C == 1 && mp == 17)) {
+                        dp_a_diag(sTbl, sDiag, lane);
+                        dp_path_a(sTbl, lam, C, sState, sState + kPairs * 32, sDiag, lane, rate, mask);
+                    } else {
+                        dp_path_b(sTbl, lam, s, sState, sState + kPairs * 32,
+                                  reinterpret_cast<uint32_t *>(sState + 2 * kPairs * 32), lane, rate,
+                                  mask);
+                    }
+                }
+                rates[b * 32 + lane] = rate;
+                masks[b * 32 + lane] = mask;
+                my_sum += llrint((double)rate * kRateScale) - llrint((double)rb * kRateScale);
+                __syncwarp();
+            }
+            if (!pilot && act) lout[lbase + lrank] = bsel;
+            if (threadIdx.x == 0) sAct += n;
+            __syncthreads();
+        }
+        sSum[w * 32 + lane] = my_sum;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            long long sum = 0;
+            for (int k = 0; k < W; ++k) sum += sSum[k * 32 + threadIdx.x];
+            if (sum) atomicAdd(&ctrl->acc[threadIdx.x], (unsigned long long)sum);
+            __threadfence();
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            if (sAct) atomicAdd(&ctrl->active[min(round, 15)], sAct);
+            const unsigned t = atomicAdd(&ctrl->ticket, 1u);
+            is_last = (t == gridDim.x - 1);
+            timed_out = false;
+        }
+        __syncthreads();
+        if (is_last) {
+            // ---- last CTA: stage the control block again (the sums are
+            // final now), advance the search in shared memory, write back
+            // what changed, then release the other CTAs
+            __threadfence();
+            stage_ctrl(sC, ctrl);
+            __syncthreads();
+            if (threadIdx.x < 32) {
+                const int L = threadIdx.x;
+                SearchState &S = sC.s;
+                __shared__ long long Rfx[32];
+                const long long myR = (walk ? sC.Rxb_fx : 0) + (long long)sC.acc[L];
+                Rfx[L] = myR;
+                ctrl->acc[L] = 0ull;
+                const long long Bfx = sC.budget_fx;
+                if (L == 0) S.hi0 = __longlong_as_double((long long)sC.hi0_bits);
+                __syncwarp();
+                if (sC.fixed) {
+                    if (L == 0) {
+                        S.xb_probe = 0;
+                        S.R_xb = myR;
+                        S.lambda = sC.lambda_fixed;
+                        S.phase = kSearchDone;
+                        S.rounds += 1;
+                    }
+                } else if (S.phase == kSearchPilot) {
+                    // one lane per probe: the sample's rates scaled to all blocks, the
+                    // smallest feasible probe and the largest infeasible one below it
+                    // (first lane on ties, as a sequential scan)
+                    const double B = sC.budget;
+                    const double scale =
+                        (double)sC.nb / (double)(S.pilot_blocks > 0 ? S.pilot_blocks : 1) / kRateScale;
+                    const double v = search_probe(S, L), r = (double)myR * scale;
+                    const bool feas = r <= B;
+                    const uint64_t kv = okey(v);
+                    uint64_t kb = feas ? kv : ~0ull;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const uint64_t y = __shfl_xor_sync(0xffffffffu, kb, o);
+                        kb = y < kb ? y : kb;
+                    }
+                    const uint32_t mb = __ballot_sync(0xffffffffu, feas && kv == kb);
+                    const int ib = mb ? __ffs(mb) - 1 : -1;
+                    const bool cand = !feas && v > -1.0 && (ib < 0 || kv < kb);
+                    uint64_t ka = cand ? kv : 0ull;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const uint64_t y = __shfl_xor_sync(0xffffffffu, ka, o);
+                        ka = y > ka ? y : ka;
+                    }
+                    const uint32_t ma = __ballot_sync(0xffffffffu, cand && kv == ka);
+                    const int ia = ma ? __ffs(ma) - 1 : -1;
+                    const double vb = __shfl_sync(0xffffffffu, v, ib >= 0 ? ib : 0);
+                    const double Rb = __shfl_sync(0xffffffffu, r, ib >= 0 ? ib : 0);
+                    const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
+                    const double Ra = __shfl_sync(0xffffffffu, r, ia >= 0 ? ia : 0);
+                    SearchState st;                       // every lane computes the same estimate
+                    search_copy_scalars(st, S);
+                    const double est = search_pilot_finish(st, ib, ib >= 0 ? vb : INFINITY, ib >= 0 ? Rb : 0.0,
+                                                           ia, ia >= 0 ? va : -1.0, ia >= 0 ? Ra : 0.0, B);
+                    __syncwarp();
+                    if (st.have_grid && L > kSearchFirstDoublings) S.probe[L] = search_pilot_probe(est, L);
+                    __syncwarp();
+                    if (L == 0) search_copy_scalars(S, st);
+                } else {
+                    // one lane per probe folds the evaluations into the window (exact
+                    // min / max of order keys), every lane walks, and lane L generates
+                    // the probes along decision path L
+                    const bool inr = L < S.nprobe;
+                    const double v = search_probe(S, L);
+                    const uint64_t kv = okey(v);
+                    const bool feas = inr && myR <= Bfx;
+                    uint64_t kb = feas ? kv : ~0ull;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const uint64_t y = __shfl_xor_sync(0xffffffffu, kb, o);
+                        kb = y < kb ? y : kb;
+                    }
+                    const uint32_t mb = __ballot_sync(0xffffffffu, feas && kv == kb);
+                    const int ib = mb ? __ffs(mb) - 1 : -1;
+                    const double vb = __shfl_sync(0xffffffffu, v, ib >= 0 ? ib : 0);
+                    const uint64_t kxb = okey(S.xb);
+                    const uint64_t kxbn = (ib >= 0 && kb < kxb) ? kb : kxb;
+                    const bool inf = inr && !feas && kv < kxbn;
+                    uint64_t ka = inf ? kv : 0ull;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const uint64_t y = __shfl_xor_sync(0xffffffffu, ka, o);
+                        ka = y > ka ? y : ka;
+                    }
+                    const uint32_t ma = __ballot_sync(0xffffffffu, inf && kv == ka);
+                    const int ia = ma ? __ffs(ma) - 1 : -1;
+                    const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
+                    SearchState st;                       // every lane walks the same path
+                    search_copy_scalars(st, S);
+                    search_window(st, ib >= 0 ? vb : INFINITY, ib, ib >= 0 ? Rfx[ib] : 0, va, ia);
+                    const int go = search_advance(st, Rfx, Bfx);
+                    __syncwarp();
+                    if (go) {
+                        __shared__ double sProbe[kSearchProbes];
+                        sProbe[L] = search_first_unknown(st);
+                        __syncwarp();
+                        search_path(st, L, sProbe);
+                        __syncwarp();
+                        S.probe[L] = sProbe[L];
+                    }
+                    __syncwarp();
+                    if (L == 0) {
+                        search_copy_scalars(S, st);
+                        if (st.infeasible) ctrl->status = KVQ_ERR_INFEASIBLE;
+                    }
+                }
+                __syncwarp();
+                if (L == 0) {
+                    if (!sC.fixed && S.xb_probe >= 0) ctrl->Rxb_fx = Rfx[S.xb_probe];
+                    ctrl->cnt[round & 1] = 0u;     // consumed; the next round appends here
+                    ctrl->ticket = 0u;
+                }
+                {
+                    // the search state back to global memory, 16 bytes per lane
+                    static_assert(sizeof(SearchState) % 16 == 0, "search state in 16-byte pieces");
+                    const int4 *src = reinterpret_cast<const int4 *>(&S);
+                    int4 *dst = reinterpret_cast<int4 *>(&ctrl->s);
+                    for (int i = L; i < (int)(sizeof(SearchState) / 16); i += 32) dst[i] = src[i];
+                }
+                __threadfence();
+                __syncwarp();
+                if (L == 0) st_release_u32(&ctrl->gen, (uint32_t)(iter + 1));
+            }
+            __syncthreads();
+        } else {
+            if (threadIdx.x == 0) {
+                uint32_t spins = 0;
+                const unsigned long long t0 = global_ns();
+                while (ld_acquire_u32(&ctrl->gen) < (uint32_t)(iter + 1)) {
+                    if (++spins > kSpinLimit || global_ns() - t0 > kWaitLimitNs) {
+                        timed_out = true;
+                        break;
+                    }
+                    __nanosleep(64);
                 }
             }
-            rates[b * 32 + lane] = rate;
-            masks[b * 32 + lane] = mask;
-            my_sum += llrint((double)rate * kRateScale) - llrint((double)rb * kRateScale);
-            __syncwarp();
+            __syncthreads();
+            if (timed_out) {
+                if (threadIdx.x == 0) {
+                    atomicExch(&ctrl->err, 1u);
+                    *status = KVQ_ERR_TIMEOUT;
+                }
+                return;
+            }
         }
-        if (!pilot && act) lout[lbase + lrank] = bsel;
-        if (threadIdx.x == 0) sAct += n;
-        __syncthreads();
     }
-    sSum[w * 32 + lane] = my_sum;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        long long sum = 0;
-        for (int k = 0; k < W; ++k) sum += sSum[k * 32 + threadIdx.x];
-        if (sum) atomicAdd(&ctrl->acc[threadIdx.x], (unsigned long long)sum);
-        __threadfence();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        if (sAct) atomicAdd(&ctrl->active[min(round, 15)], sAct);
-        const unsigned t = atomicAdd(&ctrl->ticket, 1u);
-        is_last = (t == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
 
-    // ---- last CTA: stage the whole control block in shared memory with one
-    // coalesced read (L2, past L1: other CTAs updated it with atomics), then
-    // advance the search there and write back what changed
-    __shared__ __align__(16) Ctrl sC;
-    {
-        const int4 *src = reinterpret_cast<const int4 *>(ctrl);
-        int4 *dst = reinterpret_cast<int4 *>(&sC);
-        for (int i = threadIdx.x; i < (int)(sizeof(Ctrl) / 16); i += blockDim.x)
-            dst[i] = __ldcg(src + i);
-    }
-    __syncthreads();
-    if (threadIdx.x >= 32) return;
-    const int L = threadIdx.x;
-    SearchState &S = sC.s;
-    __shared__ long long Rfx[32];
-    const long long myR = (walk ? sC.Rxb_fx : 0) + (long long)sC.acc[L];
-    Rfx[L] = myR;
-    ctrl->acc[L] = 0ull;
-    const long long Bfx = sC.budget_fx;
-    if (L == 0) S.hi0 = __longlong_as_double((long long)sC.hi0_bits);
-    __syncwarp();
-    if (sC.fixed) {
-        if (L == 0) {
-            S.xb_probe = 0;
-            S.R_xb = myR;
-            S.lambda = sC.lambda_fixed;
-            S.phase = kSearchDone;
-            S.rounds += 1;
-        }
-    } else if (S.phase == kSearchPilot) {
-        // one lane per probe: the sample's rates scaled to all blocks, the
-        // smallest feasible probe and the largest infeasible one below it
-        // (first lane on ties, as a sequential scan)
-        const double B = sC.budget;
-        const double scale =
-            (double)sC.nb / (double)(S.pilot_blocks > 0 ? S.pilot_blocks : 1) / kRateScale;
-        const double v = search_probe(S, L), r = (double)myR * scale;
-        const bool feas = r <= B;
-        const uint64_t kv = okey(v);
-        uint64_t kb = feas ? kv : ~0ull;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const uint64_t y = __shfl_xor_sync(0xffffffffu, kb, o);
-            kb = y < kb ? y : kb;
-        }
-        const uint32_t mb = __ballot_sync(0xffffffffu, feas && kv == kb);
-        const int ib = mb ? __ffs(mb) - 1 : -1;
-        const bool cand = !feas && v > -1.0 && (ib < 0 || kv < kb);
-        uint64_t ka = cand ? kv : 0ull;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const uint64_t y = __shfl_xor_sync(0xffffffffu, ka, o);
-            ka = y > ka ? y : ka;
-        }
-        const uint32_t ma = __ballot_sync(0xffffffffu, cand && kv == ka);
-        const int ia = ma ? __ffs(ma) - 1 : -1;
-        const double vb = __shfl_sync(0xffffffffu, v, ib >= 0 ? ib : 0);
-        const double Rb = __shfl_sync(0xffffffffu, r, ib >= 0 ? ib : 0);
-        const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
-        const double Ra = __shfl_sync(0xffffffffu, r, ia >= 0 ? ia : 0);
-        SearchState st;                       // every lane computes the same estimate
-        search_copy_scalars(st, S);
-        const double est = search_pilot_finish(st, ib, ib >= 0 ? vb : INFINITY, ib >= 0 ? Rb : 0.0,
-                                               ia, ia >= 0 ? va : -1.0, ia >= 0 ? Ra : 0.0, B);
-        __syncwarp();
-        if (st.have_grid && L > kSearchFirstDoublings) S.probe[L] = search_pilot_probe(est, L);
-        __syncwarp();
-        if (L == 0) search_copy_scalars(S, st);
-    } else {
-        // one lane per probe folds the evaluations into the window (exact
-        // min / max of order keys), every lane walks, and lane L generates
-        // the probes along decision path L
-        const bool inr = L < S.nprobe;
-        const double v = search_probe(S, L);
-        const uint64_t kv = okey(v);
-        const bool feas = inr && myR <= Bfx;
-        uint64_t kb = feas ? kv : ~0ull;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const uint64_t y = __shfl_xor_sync(0xffffffffu, kb, o);
-            kb = y < kb ? y : kb;
-        }
-        const uint32_t mb = __ballot_sync(0xffffffffu, feas && kv == kb);
-        const int ib = mb ? __ffs(mb) - 1 : -1;
-        const double vb = __shfl_sync(0xffffffffu, v, ib >= 0 ? ib : 0);
-        const uint64_t kxb = okey(S.xb);
-        const uint64_t kxbn = (ib >= 0 && kb < kxb) ? kb : kxb;
-        const bool inf = inr && !feas && kv < kxbn;
-        uint64_t ka = inf ? kv : 0ull;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const uint64_t y = __shfl_xor_sync(0xffffffffu, ka, o);
-            ka = y > ka ? y : ka;
-        }
-        const uint32_t ma = __ballot_sync(0xffffffffu, inf && kv == ka);
-        const int ia = ma ? __ffs(ma) - 1 : -1;
-        const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
-        SearchState st;                       // every lane walks the same path
-        search_copy_scalars(st, S);
-        search_window(st, ib >= 0 ? vb : INFINITY, ib, ib >= 0 ? Rfx[ib] : 0, va, ia);
-        const int go = search_advance(st, Rfx, Bfx);
-        __syncwarp();
-        if (go) {
-            __shared__ double sProbe[kSearchProbes];
-            sProbe[L] = search_first_unknown(st);
-            __syncwarp();
-            search_path(st, L, sProbe);
-            __syncwarp();
-            S.probe[L] = sProbe[L];
-        }
-        __syncwarp();
-        if (L == 0) {
-            search_copy_scalars(S, st);
-            if (st.infeasible) ctrl->status = KVQ_ERR_INFEASIBLE;
-        }
-    }
-    __syncwarp();
-    if (L == 0) {
-        if (!sC.fixed && S.xb_probe >= 0) ctrl->Rxb_fx = Rfx[S.xb_probe];
-        ctrl->cnt[round & 1] = 0u;     // consumed; the next round appends here
-        ctrl->ticket = 0u;
-    }
-    {
-        // the search state back to global memory, 16 bytes per lane
-        static_assert(sizeof(SearchState) % 16 == 0, "search state in 16-byte pieces");
-        const int4 *src = reinterpret_cast<const int4 *>(&S);
-        int4 *dst = reinterpret_cast<int4 *>(&ctrl->s);
-        for (int i = L; i < (int)(sizeof(SearchState) / 16); i += 32) dst[i] = src[i];
-    }
-    __threadfence();
-}
-
-// -------------------------------------------------------------------- emit
-// One warp per block, lane t = slot t: the chain at the final lambda becomes
-// the codebook (levels in slot order), k, D_r (sum of the chain's interval
-// distortions, reduced in a fixed tree) and H_r.  Sum D_r: per CTA in warp
-// order, then the last CTA adds the CTA partials with all its threads in a
-// fixed pattern and a fixed shuffle tree.
-__global__ void __launch_bounds__(kEmitWarps * 32)
-emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctrl,
-            const float *__restrict__ rates, const uint32_t *__restrict__ masks,
-            const float *__restrict__ rate_hi, const uint32_t *__restrict__ mask_hi,
-            const int32_t *__restrict__ evr, double *__restrict__ epartial,
-            float *__restrict__ codebook, uint8_t *__restrict__ kout, float *__restrict__ Dr,
-            float *__restrict__ Hr, double *__restrict__ totals, double *__restrict__ lambda_out,
-            int32_t *__restrict__ status) {
-    const int xb_probe = ctrl->s.xb_probe;
-    const int last_round = ctrl->s.rounds - 1;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t b = (int64_t)blockIdx.x * kEmitWarps + w;
-    __shared__ double sD[kEmitWarps];
-    __shared__ bool is_last;
-    double Dblk = 0.0;
-    if (b < nb) {
+    // ---- emit (sC holds the final state)
+    const int xb_probe = sC.s.xb_probe;
+    const int last_round = sC.s.rounds - 1;
+    __shared__ double sD[W];
+    double Dsum = 0.0;                 // this warp's blocks, in order
+    for (int64_t b = (int64_t)blockIdx.x * W + w; b < nb; b += (int64_t)gridDim.x * W) {
         const float *tb = tables + b * kRecFloats + kRecTbl;
         uint32_t mask;
         float rate;
-        if (xb_probe >= 0 && evr[b] == last_round) {
-            mask = masks[b * 32 + xb_probe];
-            rate = rates[b * 32 + xb_probe];
+        if (xb_probe >= 0 && __ldcg(&evr[b]) == last_round) {
+            mask = __ldcg(&masks[b * 32 + xb_probe]);
+            rate = __ldcg(&rates[b * 32 + xb_probe]);
         } else {
-            mask = mask_hi[b];
-            rate = rate_hi[b];
+            mask = __ldcg(&mask_hi[b]);
+            rate = __ldcg(&rate_hi[b]);
         }
         mask &= 0x1ffffu;
         if (mask == 0u) mask = 1u;
@@ -712,13 +754,13 @@ emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctr
             Dr[b] = dv;
             Hr[b] = rate / (float)d;
         }
-        Dblk = (double)dv;
+        Dsum += (double)dv;
     }
-    if (lane == 0) sD[w] = Dblk;
+    if (lane == 0) sD[w] = Dsum;
     __syncthreads();
     if (threadIdx.x == 0) {
         double dd = 0.0;
-        for (int k = 0; k < kEmitWarps; ++k) dd += sD[k];
+        for (int k = 0; k < W; ++k) dd += sD[k];
         epartial[blockIdx.x] = dd;
         __threadfence();
         const unsigned t = atomicAdd(&ctrl->ticket_emit, 1u);
@@ -727,23 +769,22 @@ emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctr
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    __shared__ double sPart[kEmitWarps * 32];
+    __shared__ double sPart[W * 32];
     {
         double acc = 0.0;
-        for (unsigned k = threadIdx.x; k < gridDim.x; k += kEmitWarps * 32)
-            acc += __ldcg(&epartial[k]);
+        for (unsigned k = threadIdx.x; k < gridDim.x; k += W * 32) acc += __ldcg(&epartial[k]);
         sPart[threadIdx.x] = acc;
     }
     __syncthreads();
     if (threadIdx.x >= 32) return;
-    // fixed tree: lane l adds its column of four, then a shuffle tree
+    // fixed tree: lane l adds its column, then a shuffle tree
     double dd = 0.0;
 #pragma unroll
-    for (int k = 0; k < kEmitWarps; ++k) dd += sPart[k * 32 + threadIdx.x];
+    for (int k = 0; k < W; ++k) dd += sPart[k * 32 + threadIdx.x];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dd += __shfl_down_sync(0xffffffffu, dd, o);
     if (threadIdx.x != 0) return;
-    Ctrl *n = ctrl;
+    const Ctrl *n = &sC;
     const double R = (double)n->s.R_xb / kRateScale;   // the rate the search tested
     const double lam = n->s.lambda;
     totals[0] = R;
@@ -757,8 +798,9 @@ emit_kernel(const float *__restrict__ tables, int64_t nb, Ctrl *__restrict__ ctr
     }
     int st = n->status;
     if (n->flags & kFlagNonfinite) st = KVQ_ERR_NONFINITE;
+    if (__ldcg(&ctrl->err)) st = KVQ_ERR_TIMEOUT;
     *status = st;
-    n->ticket_emit = 0u;
+    ctrl->ticket_emit = 0u;
 }
 
 __global__ void empty_alloc_kernel(double *totals, double *lambda_out, int32_t *status, int mode,
@@ -790,33 +832,33 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
     const float *recs = reinterpret_cast<const float *>(static_cast<const char *>(stats) +
                                                         sizeof(StatsHeader));
     ctrl_init_kernel<<<1, 32, 0, st>>>(ws.ctrl, hdr, budget, eta, mode, lambda, nb);
-    const int rounds = (mode == KVQ_SUBGRADIENT) ? 1 : 3 + kSearchSteps / 5;
+    if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
     const bool general = s < 16;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    for (int r = 0; r < rounds; ++r) {
-        // persistent grid: two CTAs per SM (the shared-memory limit)
-        if (general) {
-            using Cfg = RoundCfg<true>;
-            const int64_t need = (nb + Cfg::kWarps - 1) / Cfg::kWarps;
-            const unsigned grid = (unsigned)(need < 2 * sms ? need : 2 * sms);
-            search_round_kernel<true><<<grid, Cfg::kWarps * 32, Cfg::kSmem, st>>>(
-                recs, nb, s, ws.ctrl, ws.rates, ws.masks, ws.rate_lo, ws.rate_hi, ws.mask_hi,
-                ws.evr, ws.list);
-        } else {
-            using Cfg = RoundCfg<false>;
-            const int64_t need = (nb + Cfg::kWarps - 1) / Cfg::kWarps;
-            const unsigned grid = (unsigned)(need < 2 * sms ? need : 2 * sms);
-            search_round_kernel<false><<<grid, Cfg::kWarps * 32, Cfg::kSmem, st>>>(
-                recs, nb, s, ws.ctrl, ws.rates, ws.masks, ws.rate_lo, ws.rate_hi, ws.mask_hi,
-                ws.evr, ws.list);
-        }
-    }
-    const unsigned egrid = (unsigned)((nb + kEmitWarps - 1) / kEmitWarps);
-    emit_kernel<<<egrid, kEmitWarps * 32, 0, st>>>(recs, nb, ws.ctrl, ws.rates, ws.masks,
-                                                ws.rate_hi, ws.mask_hi, ws.evr, ws.epartial,
-                                                codebook, k, Dr, Hr, totals, lambda, status);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+    const int resident = general ? g_resident_gen[dev] : g_resident[dev];
+    const int W = general ? RoundCfg<true>::kWarps : RoundCfg<false>::kWarps;
+    const int64_t need = (nb + W - 1) / W;
+    int64_t grid = need < resident ? need : resident;
+    if (grid > kMaxGrid) grid = kMaxGrid;
+    if (grid < 1) return KVQ_ERR_CUDA;
+    void *args[] = {(void *)&recs, (void *)&nb, (void *)&s, (void *)&ws.ctrl, (void *)&ws.rates,
+                    (void *)&ws.masks, (void *)&ws.rate_lo, (void *)&ws.rate_hi,
+                    (void *)&ws.mask_hi, (void *)&ws.evr, (void *)&ws.list, (void *)&ws.epartial,
+                    (void *)&codebook, (void *)&k, (void *)&Dr, (void *)&Hr, (void *)&totals,
+                    (void *)&lambda, (void *)&status};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)(W * 32));
+    cfg.dynamicSmemBytes = general ? RoundCfg<true>::kSmem : RoundCfg<false>::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;       // every CTA resident: the rounds hand over
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const void *fn = general ? (const void *)search_kernel<true> : (const void *)search_kernel<false>;
+    if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return KVQ_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
@@ -834,13 +876,28 @@ int allocate_report(const void *workspace, kvq_report *r) {
 }
 
 int allocate_init() {
-    // opt in to more than 48 KB of dynamic shared memory for the search rounds
-    if (cudaFuncSetAttribute(search_round_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // more than 48 KB of dynamic shared memory for the search kernel, and the
+    // number of its CTAs that fit on the device at once (the cooperative grid)
+    int dev = 0, sms = 0, occ = 0, occg = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+    if (cudaFuncSetAttribute(search_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)RoundCfg<false>::kSmem) != cudaSuccess)
         return KVQ_ERR_CUDA;
-    if (cudaFuncSetAttribute(search_round_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(search_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)RoundCfg<true>::kSmem) != cudaSuccess)
         return KVQ_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, search_kernel<false>,
+                                                      RoundCfg<false>::kWarps * 32,
+                                                      RoundCfg<false>::kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occg, search_kernel<true>,
+                                                      RoundCfg<true>::kWarps * 32,
+                                                      RoundCfg<true>::kSmem) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    if (occ < 1 || occg < 1) return KVQ_ERR_CUDA;
+    g_resident[dev] = occ * sms;
+    g_resident_gen[dev] = occg * sms;
     return KVQ_OK;
 }
 

@@ -173,6 +173,7 @@ const char *kvq_status_string(int status) {
     case KVQ_ERR_CUDA: return "CUDA launch error";
     case KVQ_ERR_NONFINITE: return "non-finite input entry";
     case KVQ_ERR_INFEASIBLE: return "budget infeasible";
+    case KVQ_ERR_TIMEOUT: return "device wait timed out";
     case KVQ_ERR_TOO_LARGE: return "layout needs more scratch than the static workspace holds";
     default: return "unknown status";
     }

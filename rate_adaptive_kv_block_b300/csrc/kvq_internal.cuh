@@ -137,7 +137,9 @@ struct alignas(16) Ctrl {
     int32_t flags;          // OR of block flags
     int32_t mode;
     uint32_t ticket;        // last-CTA-done counter of the search rounds
-    uint32_t ticket_emit;   // same, emit kernel
+    uint32_t ticket_emit;   // same, emit
+    uint32_t gen;           // rounds released to the grid (persistent search kernel)
+    uint32_t err;           // a CTA gave up waiting for a release
     uint32_t active[16];    // blocks evaluated in each round (diagnostics)
     int64_t nb;             // blocks
     // sum over all blocks of d_r H_r at xb, fixed point; the rounds of the

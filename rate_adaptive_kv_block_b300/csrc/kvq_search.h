@@ -99,16 +99,13 @@ KVQ_HD inline uint64_t okey(double x) {
 // 0.5 * (a + b) for finite a, b >= 0, bit for bit as binary64 arithmetic
 // with round-to-nearest-even computes it: the sum rounded once, then halved
 // (exact for normal results).  Integer operations only; inputs outside the
-// fast path (a subnormal operand, a result that would not stay normal) take
+// fast paths (a subnormal operand, a result that would not stay normal) take
 // the floating-point expression itself.
-KVQ_HD inline double half_sum(double a, double b) {
-    uint64_t ua = dbits(a), ub = dbits(b);
-    if (ua > ub) { const uint64_t t = ua; ua = ub; ub = t; }     // a <= b (non-negative)
+KVQ_HD inline double half_sum_general(uint64_t ua, uint64_t ub) {
+    // ua <= ub, both non-negative and normal (or ua == 0)
+    const uint64_t frac = (1ull << 52) - 1;
     const int eb = (int)(ub >> 52);
     const int ea = (int)(ua >> 52);
-    const uint64_t frac = (1ull << 52) - 1;
-    if (eb == 0 || eb >= 2046 || (ea == 0 && ua != 0) || (ub >> 63) || (ua >> 63))
-        return 0.5 * (dfrom(ua) + dfrom(ub));
     uint64_t sig;
     int e;
     if (ua == 0) {
@@ -144,6 +141,44 @@ KVQ_HD inline double half_sum(double a, double b) {
     }
     if (e - 1 < 1 || e - 1 >= 2047) return 0.5 * (dfrom(ua) + dfrom(ub));
     return dfrom(((uint64_t)(e - 1) << 52) | (sig & frac));
+}
+
+KVQ_HD inline double half_sum(double a, double b) {
+    uint64_t ua = dbits(a), ub = dbits(b);
+    if (ua > ub) { const uint64_t t = ua; ua = ub; ub = t; }     // a <= b (non-negative)
+    const int eb = (int)(ub >> 52);
+    const int ea = (int)(ua >> 52);
+    if (eb <= 1 || eb >= 2046 || (ub >> 63) || (ea == 0 && ua != 0))
+        return 0.5 * (dfrom(ua) + dfrom(ub));
+    const uint64_t frac = (1ull << 52) - 1;
+    // the bisection's own cases: lo = 0 (halve hi), or lo and hi within a
+    // binade of each other (exponents equal or one apart)
+    if (ua == 0) return dfrom(ub - (1ull << 52));
+    const int d = eb - ea;
+    if (d <= 1) {
+        const uint64_t ma = (ua & frac) | (1ull << 52);
+        const uint64_t mb = (ub & frac) | (1ull << 52);
+        const uint64_t lost = d ? (ma & 1ull) : 0ull;               // bit shifted out of a
+        const uint64_t m = mb + (ma >> d);                          // 53 or 54 bits
+        uint64_t sig;
+        int e;                                                      // exponent of the half sum
+        if (m >> 53) {                                              // sum in [2^53, 2^54)
+            sig = m >> 1;
+            const uint64_t g = m & 1ull;                            // half an ulp
+            if (g && (lost || (sig & 1ull))) ++sig;
+            e = eb;
+        } else {                                                    // d = 1, no carry
+            sig = m;
+            if (lost && (sig & 1ull)) ++sig;                        // exact tie: to even
+            e = eb - 1;
+        }
+        if (sig >> 53) {
+            sig >>= 1;
+            ++e;
+        }
+        return dfrom(((uint64_t)e << 52) | (sig & frac));
+    }
+    return half_sum_general(ua, ub);
 }
 
 // x * 2^t for x = 0 or normal x > 0 whose result stays normal (exponent

@@ -21,6 +21,7 @@ KVQ_ERR_CUDA = 2
 KVQ_ERR_NONFINITE = 3
 KVQ_ERR_INFEASIBLE = 4
 KVQ_ERR_TOO_LARGE = 5
+KVQ_ERR_TIMEOUT = 6
 KVQ_STATIC_WORKSPACE_BYTES = 8 << 20
 KVQ_BISECT40 = 0
 KVQ_SUBGRADIENT = 1
