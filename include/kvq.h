@@ -178,15 +178,20 @@ int kvq_allocate_static(const void *stats, kvq_layout L, int s, double budget_bi
  * hash(seed, n) is the SplitMix64 generator seeded with `seed`: output
  * number n>>1, its high 32 bits for even n, low 32 bits for odd n.
  *   x           device [S,T,D] binary16.
- *   codebook, k as written by kvq_allocate.
+ *   codebook, k as written by kvq_allocate (k must be the number of distinct
+ *               levels, with slots k..15 repeating the largest: the kernel
+ *               takes k from the codebook itself).
  *   seed        any 64-bit value.
  *   index_base  even, and index_base + S*T*D <= 2^40.
  *   codes       device uint8 [nblocks][16*group]: byte e/2 of block r holds
  *               entry e in its low nibble (e even) or high nibble (e odd).
+ *   status      device int32 or NULL: set to KVQ_ERR_TIMEOUT if a copy into
+ *               shared memory never completed (the codes are then
+ *               incomplete); left unchanged otherwise.
  */
 int kvq_quantize(const uint16_t *x, kvq_layout L, const float *codebook,
                  const uint8_t *k, uint64_t seed, uint64_t index_base,
-                 uint8_t *codes, void *stream);
+                 uint8_t *codes, int32_t *status, void *stream);
 
 /*
  * kvq_dequantize -- decode before attention ("Implementation notes"):

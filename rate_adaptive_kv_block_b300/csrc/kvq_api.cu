@@ -14,7 +14,8 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
                     float *Dr, float *Hr, double *totals, int32_t *status, cudaStream_t st);
 int launch_quantize(const uint16_t *x, const kvq_layout &L, const float *codebook,
                     const uint8_t *k, uint64_t seed, uint64_t index_base, uint8_t *codes,
-                    cudaStream_t st);
+                    int32_t *status, cudaStream_t st);
+int quantize_init();
 int launch_dequantize(const uint8_t *codes, const float *codebook, const kvq_layout &L,
                       uint16_t *y, cudaStream_t st);
 size_t workspace_bytes(int64_t nb, int s);
@@ -40,9 +41,10 @@ static int init_once() {
     static bool done[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return KVQ_ERR_CUDA;
-    if (dev >= 64) return allocate_init();
+    if (dev >= 64) return KVQ_ERR_CUDA;
     if (!done[dev]) {
         state[dev] = allocate_init();
+        if (state[dev] == KVQ_OK) state[dev] = quantize_init();
         done[dev] = true;
     }
     return state[dev];
@@ -135,7 +137,8 @@ int kvq_allocate_static(const void *stats, kvq_layout L, int s, double budget_bi
 }
 
 int kvq_quantize(const uint16_t *x, kvq_layout L, const float *codebook, const uint8_t *k,
-                 uint64_t seed, uint64_t index_base, uint8_t *codes, void *stream) {
+                 uint64_t seed, uint64_t index_base, uint8_t *codes, int32_t *status,
+                 void *stream) {
     if (!layout_ok(L)) return KVQ_ERR_INVALID_ARG;
     if (index_base & 1u) return KVQ_ERR_INVALID_ARG;
     const uint64_t n = (uint64_t)L.S * (uint64_t)L.T * (uint64_t)L.D;
@@ -145,7 +148,8 @@ int kvq_quantize(const uint16_t *x, kvq_layout L, const float *codebook, const u
         if (!aligned16(x) || !aligned16(codebook) || !aligned16(codes)) return KVQ_ERR_INVALID_ARG;
         if (L.S * (L.T / 32) > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
     }
-    return launch_quantize(x, L, codebook, k, seed, index_base, codes,
+    if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
+    return launch_quantize(x, L, codebook, k, seed, index_base, codes, status,
                            static_cast<cudaStream_t>(stream));
 }
 

@@ -3,134 +3,267 @@
 // formulas": P(q_{i+1} | x) = (x - q_i)/(q_{i+1} - q_i); "Implementation
 // notes": store the codebook and the symbol stream; decode before attention).
 //
-// One CTA per 32-token slab of one stream (32 x D binary16, contiguous), so
-// both passes stream HBM with 16-byte loads and stores.  The slab holds D/G
-// blocks; their codebooks are staged in shared memory once per slab.  Every
-// fp32 operation of the rounding decision is an explicit round-to-nearest
-// intrinsic, so no multiply-add contraction can change a code.
+// kvq_quantize is a persistent kernel that streams the tensor through shared
+// memory: a tile is 32 tokens x Dc features of one stream (Dc = min(D, 256)),
+// copied by the bulk-copy (TMA) engine into a ring of stages, each completing
+// on its own mbarrier, several tiles ahead of the warps that consume it; the
+// tile's codebooks ride in the same copy.  Per tile, 16 threads per block turn
+// the codebook into the interval thresholds and the (-q_i, w_i) table; every
+// thread then handles fixed 8-feature columns of the tile.  Per pair of
+// entries (binary16x2): the interval index is a 4-level binary search over
+// the 15 thresholds (padded with +inf) with packed half2 comparisons and
+// bitwise selects, the rounding decision uses packed fp32 add / multiply
+// (explicit round-to-nearest, so no multiply-add contraction can change a
+// code), and one SplitMix64 output gives both uniforms.
 #include "kvq_internal.cuh"
 
 namespace kvq {
 
-constexpr int kQThreads = 256;
-constexpr int kMaxGroups = 32;
+constexpr int kQThreads = 128;
+constexpr int kQStages = 4;
+constexpr int kQMaxCols = 256;               // features per tile (at most)
+constexpr int kQMaxGroups = kQMaxCols / 8;   // blocks per tile (at most)
+constexpr uint32_t kQWaitLimit = 1u << 22;   // mbarrier polls before giving up
 
-// SplitMix64 output function (Steele, Lea, Flood 2014).
-__device__ __forceinline__ uint64_t splitmix_mix(uint64_t z) {
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    return z ^ (z >> 31);
+// SplitMix64 output function (Steele, Lea, Flood 2014), written on the two
+// 32-bit halves (hi:lo) of the state so that each step is one funnel shift,
+// one xor or one 32-bit multiply-add: returns the output's high and low words.
+__device__ __forceinline__ void splitmix_mix(uint32_t lo, uint32_t hi, uint32_t &ohi,
+                                             uint32_t &olo) {
+    // z ^= z >> 30; z *= 0xBF58476D1CE4E5B9
+    lo ^= __funnelshift_r(lo, hi, 30);
+    hi ^= hi >> 30;
+    const uint32_t nlo0 = lo * 0x1CE4E5B9u;
+    const uint32_t nhi0 = __umulhi(lo, 0x1CE4E5B9u) + lo * 0xBF58476Du + hi * 0x1CE4E5B9u;
+    // z ^= z >> 27; z *= 0x94D049BB133111EB
+    const uint32_t nlo = nlo0 ^ __funnelshift_r(nlo0, nhi0, 27);
+    const uint32_t nhi = nhi0 ^ (nhi0 >> 27);
+    lo = nlo * 0x133111EBu;
+    hi = __umulhi(nlo, 0x133111EBu) + nlo * 0x94D049BBu + nhi * 0x133111EBu;
+    // z ^= z >> 31
+    olo = lo ^ __funnelshift_r(lo, hi, 31);
+    ohi = hi ^ (hi >> 31);
 }
 constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;
 
-struct QSmem {
-    __half2 thr[kMaxGroups][16];   // (q_j, q_j) for 1 <= j <= k-2, +inf beyond
-    float2 qw[kMaxGroups][16];     // (q_i, (q_{i+1} - q_i) * 2^-24); k = 1: (q_0, +inf)
-    int kmax;
-};
-
-// Interval index of two binary16 entries at once: the number of thresholds
-// q_1 .. q_{k-2} at or below each entry, counted in a half2 accumulator that
-// starts at 1024 (binary16 integers 1024..2047 are exact and their low byte
-// is the count).  The comparisons and adds run on the fp16 FMA datapath.
-template <int NT>
-__device__ __forceinline__ void count_below(const __half2 (&xh)[4], const __half2 *th, int nthr,
-                                            uint32_t (&cnt)[4]) {
-    const __half2 base = __floats2half2_rn(1024.f, 1024.f);
-    __half2 c[4] = {base, base, base, base};
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-        if (j < nthr) {
-            const __half2 t = th[j];
-#pragma unroll
-            for (int p = 0; p < 4; ++p) c[p] = __hadd2(c[p], __hge2(xh[p], t));
-        }
-    }
-#pragma unroll
-    for (int p = 0; p < 4; ++p) cnt[p] = *reinterpret_cast<const uint32_t *>(&c[p]);
+__device__ __forceinline__ __half2 as_h2(uint32_t u) {
+    __half2 h;
+    memcpy(&h, &u, 4);
+    return h;
 }
 
-// One CTA per 32-token slab; thread t always handles the same 8 features
-// (column unit t % (D/8)) on rows t / (D/8), t / (D/8) + 256 / (D/8), ...
-// (D / 8 divides 256 for D a power of two <= 2048).
-__global__ void __launch_bounds__(kQThreads)
-quantize_kernel(const uint16_t *__restrict__ x, kvq_layout L, const float *__restrict__ codebook,
-                const uint8_t *__restrict__ kk, uint64_t seed, uint64_t index_base,
-                uint8_t *__restrict__ codes, int log2_upr) {
-    __shared__ __align__(16) QSmem sm;
-    const int D = L.D, G = L.group, nG = D / G;
-    const int64_t slab = blockIdx.x;                 // stream * (T/32) + token block
-    const int64_t blk0 = slab * nG;
-    const int hb = 16 * G;                           // code bytes per block
-    if (threadIdx.x == 0) sm.kmax = 0;
-    __syncthreads();
-    const float INF = __int_as_float(0x7f800000);
-    for (int i = threadIdx.x; i < nG * 16; i += kQThreads) {
-        const int g = i >> 4, j = i & 15;
-        const float *q = codebook + (blk0 + g) * 16;
-        const int k = kk[blk0 + g];
-        const float qj = q[j];
-        const float t = (j >= 1 && j <= k - 2) ? qj : INF;
-        sm.thr[g][j] = __floats2half2_rn(t, t);     // exact: levels are binary16 values
-        const float qn = q[j < 15 ? j + 1 : 15];
-        float ws = 0.f;
-        if (k <= 1) ws = INF;                       // k = 1: never move up
-        else if (j <= k - 2) ws = __fmul_rn(__fsub_rn(qn, qj), 5.9604644775390625e-8f);  // 2^-24, exact
-        sm.qw[g][j] = make_float2(qj, ws);
-        if (j == 0) atomicMax(&sm.kmax, k);
+// ------------------------------------------------------------- mbarriers
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// true once the phase with this parity has completed; false after the limit
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kQWaitLimit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n"
+            " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(smem_addr(bar)), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+// bulk copy global -> shared, completing on `bar` (16-byte aligned, size % 16 == 0)
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// --------------------------------------------------------------- tiles
+struct QGeom {
+    int D, G, Dc;          // features, block width, tile width (powers of two)
+    int nchunk;            // tiles per 32-token slab
+    int ngt;               // blocks per tile
+    int upr_log2;          // log2(Dc / 8)
+    int chunk_log2;        // log2(nchunk)
+    int g_log2;            // log2(G)
+    int bps_log2;          // log2(D / G): blocks per slab
+    uint32_t x_bytes;      // 64 * Dc
+    uint32_t cb_bytes;     // 64 * ngt
+    uint32_t stage_bytes;  // x_bytes + cb_bytes, rounded to 128
+};
+
+// Issue the copies of tile t into stage buffer `buf`.
+__device__ __forceinline__ void issue_tile(const QGeom &g, int64_t t, const uint16_t *x,
+                                           const float *codebook, char *buf, uint64_t *bar) {
+    const int64_t slab = t >> g.chunk_log2;
+    const int chunk = (int)(t & (g.nchunk - 1));
+    mbar_expect_tx(bar, g.x_bytes + g.cb_bytes);
+    const uint16_t *src = x + slab * 32 * (int64_t)g.D + (int64_t)chunk * g.Dc;
+    if (g.Dc == g.D) {
+        bulk_g2s(buf, src, g.x_bytes, bar);                 // the slab is contiguous
+    } else {
+        for (int r = 0; r < 32; ++r)
+            bulk_g2s(buf + r * g.Dc * 2, src + (int64_t)r * g.D, (uint32_t)(g.Dc * 2), bar);
+    }
+    const int64_t blk0 = (slab << g.bps_log2) + (int64_t)chunk * g.ngt;
+    bulk_g2s(buf + g.x_bytes, codebook + blk0 * 16, g.cb_bytes, bar);
+}
+
+struct QTables {
+    __half2 thr[kQMaxGroups][16];   // (q_j, q_j) for 1 <= j <= k-2, +inf beyond; [0] unused
+    float2 qw[kQMaxGroups][16];     // (-q_i, (q_{i+1} - q_i) * 2^-24); k = 1: (-q_0, +inf)
+};
+
+__global__ void __launch_bounds__(kQThreads, 6)
+quantize_kernel(const uint16_t *__restrict__ x, const float *__restrict__ codebook, QGeom g,
+                int64_t ntiles, uint64_t seed, uint64_t index_base, uint8_t *__restrict__ codes,
+                int32_t *__restrict__ status) {
+    extern __shared__ __align__(128) char qsm[];
+    __shared__ __align__(8) uint64_t bars[kQStages];
+    __shared__ __align__(16) QTables tb;
+    __shared__ bool failed;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int s = 0; s < kQStages; ++s) mbar_init(&bars[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        failed = false;
     }
     __syncthreads();
-    const int upr = 1 << log2_upr;                  // 8-entry units per row
-    const int cu = threadIdx.x & (upr - 1);
-    const int row0 = threadIdx.x >> log2_upr, rstep = kQThreads >> log2_upr;
-    const int f0 = cu * 8;
-    const int g = f0 / G;
-    const int nthr = sm.kmax - 2;
-    __half2 th[14];
+    // prologue: the first kQStages tiles of this CTA in flight
+    if (tid == 0) {
+        for (int s = 0; s < kQStages; ++s) {
+            const int64_t t = (int64_t)blockIdx.x + (int64_t)s * gridDim.x;
+            if (t < ntiles) issue_tile(g, t, x, codebook, qsm + s * g.stage_bytes, &bars[s]);
+        }
+    }
+    const float INF = __int_as_float(0x7f800000);
+    const int upr = 1 << g.upr_log2;
+    const int cu = tid & (upr - 1);
+    const int row0 = tid >> g.upr_log2, rstep = kQThreads >> g.upr_log2;
+    const int f0 = cu * 8;                       // column inside the tile
+    const int gt = f0 >> g.g_log2;               // block inside the tile
+    const int hb = 16 * g.G;                     // code bytes per block
+    uint32_t n = 0;                              // tiles consumed by this CTA
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++n) {
+        const uint32_t s = n % kQStages;
+        char *buf = qsm + s * g.stage_bytes;
+        if (!mbar_wait(&bars[s], (n / kQStages) & 1u)) {
+            if (tid == 0) failed = true;
+        }
+        __syncthreads();
+        if (failed) break;
+        // codebook -> thresholds and decision table (16 threads per block)
+        const float *cb = reinterpret_cast<const float *>(buf + g.x_bytes);
+        for (int i = tid; i < g.ngt * 16; i += kQThreads) {
+            const int b = i >> 4, j = i & 15;
+            const float *q = cb + b * 16;
+            const float top = q[15];
+            int k = 1;
 #pragma unroll
-    for (int j = 0; j < 14; ++j) th[j] = sm.thr[g][j + 1];
-    const float2 *qw = sm.qw[g];
-    uint8_t *cbase = codes + (blk0 + g) * hb + (f0 % G) / 2;
-    const int64_t flat0 = (slab * 32 + row0) * (int64_t)D + f0;
-    uint64_t z = seed + ((index_base + (uint64_t)flat0) / 2 + 1) * kGolden;
-    const uint64_t zstep = (uint64_t)(rstep * D / 2) * kGolden;
-    for (int row = row0; row < 32; row += rstep, z += zstep) {
-        const int64_t flat = (slab * 32 + row) * (int64_t)D + f0;
-        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(x + flat));
-        __half2 xh[4];
-        xh[0] = *reinterpret_cast<const __half2 *>(&raw.x);
-        xh[1] = *reinterpret_cast<const __half2 *>(&raw.y);
-        xh[2] = *reinterpret_cast<const __half2 *>(&raw.z);
-        xh[3] = *reinterpret_cast<const __half2 *>(&raw.w);
-        uint32_t cnt[4];
-        count_below<14>(xh, th, nthr, cnt);
-        uint32_t packed = 0;
-        uint64_t zz = z;
+            for (int m = 0; m < 15; ++m) k += q[m] < top ? 1 : 0;
+            const float qj = q[j];
+            const float th = (j >= 1 && j <= k - 2) ? qj : INF;
+            tb.thr[b][j] = __floats2half2_rn(th, th);     // exact: levels are binary16 values
+            const float qn = q[j < 15 ? j + 1 : 15];
+            float ws = 0.f;
+            if (k <= 1) ws = INF;                         // k = 1: never move up
+            else if (j <= k - 2) ws = __fmul_rn(__fsub_rn(qn, qj), 5.9604644775390625e-8f);  // 2^-24
+            tb.qw[b][j] = make_float2(-qj, ws);
+        }
+        __syncthreads();
+        // this thread's block: 15 thresholds in registers
+        uint32_t T[16];
 #pragma unroll
-        for (int pr = 0; pr < 4; ++pr) {
-            const uint64_t hz = splitmix_mix(zz);
-            zz += kGolden;
-            const uint32_t hsh[2] = {(uint32_t)(hz >> 32), (uint32_t)hz};
-            const float2 xf = __half22float2(xh[pr]);
-            const float xv[2] = {xf.x, xf.y};
+        for (int j = 1; j < 16; ++j) {
+            const __half2 h = tb.thr[gt][j];
+            memcpy(&T[j], &h, 4);
+        }
+        const float2 *qw = tb.qw[gt];
+        const int64_t slab = t >> g.chunk_log2;
+        const int chunk = (int)(t & (g.nchunk - 1));
+        const int col = chunk * g.Dc + f0;                      // feature of the first entry
+        const int64_t blk = (slab << g.bps_log2) + (col >> g.g_log2);
+        uint8_t *cbase = codes + blk * hb + ((col & (g.G - 1)) >> 1);
+        uint64_t z = seed + ((index_base + (uint64_t)((slab * 32 + row0) * (int64_t)g.D + col)) / 2 + 1) * kGolden;
+        const uint64_t zstep = (uint64_t)(rstep * g.D / 2) * kGolden;
+        for (int row = row0; row < 32; row += rstep, z += zstep) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(buf + (row * g.Dc + f0) * 2);
+            const uint32_t xw0 = raw.x, xw1 = raw.y, xw2 = raw.z, xw3 = raw.w;
+            uint32_t packed = 0;
+            uint64_t zz = z;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int i = (int)((cnt[pr] >> (16 * q)) & 0xffu);
-                const float2 a = qw[i];
-                const float r = __fsub_rn(xv[q], a.x);
-                const float tw = __fmul_rn((float)(hsh[q] >> 8), a.y);
-                const uint32_t code = (uint32_t)i + (tw < r ? 1u : 0u);
-                packed |= code << (4 * (2 * pr + q));
+            for (int pr = 0; pr < 4; ++pr) {
+                const __half2 X = as_h2(pr == 0 ? xw0 : pr == 1 ? xw1 : pr == 2 ? xw2 : xw3);
+                // interval index of both halves: 4-level binary search over
+                // T1..T15 (sorted, +inf padded); m* are 0xffff-per-half masks
+                const uint32_t m1 = __hge2_mask(X, as_h2(T[8]));
+                const uint32_t t2 = (T[12] & m1) | (T[4] & ~m1);
+                const uint32_t m2 = __hge2_mask(X, as_h2(t2));
+                const uint32_t a3 = (T[6] & m2) | (T[2] & ~m2), b3 = (T[14] & m2) | (T[10] & ~m2);
+                const uint32_t t3 = (b3 & m1) | (a3 & ~m1);
+                const uint32_t m3 = __hge2_mask(X, as_h2(t3));
+                const uint32_t a4 = (T[3] & m3) | (T[1] & ~m3), b4 = (T[7] & m3) | (T[5] & ~m3);
+                const uint32_t c4 = (T[11] & m3) | (T[9] & ~m3), d4 = (T[15] & m3) | (T[13] & ~m3);
+                const uint32_t lo4 = (b4 & m2) | (a4 & ~m2), hi4 = (d4 & m2) | (c4 & ~m2);
+                const uint32_t t4 = (hi4 & m1) | (lo4 & ~m1);
+                const uint32_t m4 = __hge2_mask(X, as_h2(t4));
+                const uint32_t idx = (m1 & 0x00080008u) | (m2 & 0x00040004u) | (m3 & 0x00020002u) |
+                                     (m4 & 0x00010001u);
+                const int i0 = (int)(idx & 15u), i1 = (int)(idx >> 16);
+                const float2 e0 = qw[i0], e1 = qw[i1];
+                uint32_t hhi, hlo;
+                splitmix_mix((uint32_t)zz, (uint32_t)(zz >> 32), hhi, hlo);
+                zz += kGolden;
+                const float2 xf = __half22float2(X);
+                const float2 r = __fadd2_rn(xf, make_float2(e0.x, e1.x));          // x - q_i
+                const float2 u = make_float2((float)(hhi >> 8), (float)(hlo >> 8));
+                const float2 tw = __fmul2_rn(u, make_float2(e0.y, e1.y));
+                const uint32_t c0 = (uint32_t)i0 + (tw.x < r.x ? 1u : 0u);
+                const uint32_t c1 = (uint32_t)i1 + (tw.y < r.y ? 1u : 0u);
+                packed |= (c0 | (c1 << 4)) << (8 * pr);
+            }
+            *reinterpret_cast<uint32_t *>(cbase + (int64_t)row * (g.G / 2)) = packed;
+        }
+        __syncthreads();                         // every thread is done with this stage
+        if (tid == 0) {
+            const int64_t tn = t + (int64_t)kQStages * gridDim.x;
+            if (tn < ntiles) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue_tile(g, tn, x, codebook, buf, &bars[s]);
             }
         }
-        *reinterpret_cast<uint32_t *>(cbase + (int64_t)row * (G / 2)) = packed;
+    }
+    if (failed) {
+        // a copy never completed: report it, and give the copies this CTA
+        // issued a bounded chance to land before the shared memory is released
+        if (tid == 0) {
+            if (status) atomicExch(status, KVQ_ERR_TIMEOUT);
+            for (uint32_t k = 0; k < kQStages; ++k) {
+                const uint32_t nk = n + k;
+                const int64_t tk = (int64_t)blockIdx.x + (int64_t)nk * gridDim.x;
+                if (tk < ntiles) mbar_wait(&bars[nk % kQStages], (nk / kQStages) & 1u);
+            }
+        }
+        __syncthreads();
     }
 }
 
 __global__ void __launch_bounds__(kQThreads)
 dequantize_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ codebook,
                   kvq_layout L, uint16_t *__restrict__ y) {
-    __shared__ uint16_t sq[kMaxGroups][16];
+    __shared__ uint16_t sq[32][16];
     const int D = L.D, G = L.group, nG = D / G;
     const int64_t slab = blockIdx.x;
     const int64_t blk0 = slab * nG;
@@ -154,15 +287,58 @@ dequantize_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ c
     }
 }
 
+static int g_quant_grid[64];
+
+static QGeom geometry(const kvq_layout &L) {
+    QGeom g;
+    g.D = L.D;
+    g.G = L.group;
+    g.Dc = L.D < kQMaxCols ? L.D : kQMaxCols;
+    g.nchunk = L.D / g.Dc;
+    g.ngt = g.Dc / g.G;
+    auto lg2 = [](int v) { int l = 0; while ((1 << l) < v) ++l; return l; };
+    g.upr_log2 = lg2(g.Dc / 8);
+    g.chunk_log2 = lg2(g.nchunk);
+    g.g_log2 = lg2(g.G);
+    g.bps_log2 = lg2(g.D / g.G);
+    g.x_bytes = (uint32_t)(64 * g.Dc);
+    g.cb_bytes = (uint32_t)(64 * g.ngt);
+    g.stage_bytes = (g.x_bytes + g.cb_bytes + 127u) & ~127u;
+    return g;
+}
+
+int quantize_init() {
+    int dev = 0, sms = 0, occ = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
+    const int smem = kQStages * ((64 * kQMaxCols + 64 * kQMaxGroups + 127) & ~127);
+    if (cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return KVQ_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    // the grid for the llama-shaped tile size (8 KB + codebook per stage)
+    const int smem128 = kQStages * ((64 * 128 + 64 + 127) & ~127);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quantize_kernel, kQThreads, smem128) !=
+        cudaSuccess)
+        return KVQ_ERR_CUDA;
+    g_quant_grid[dev] = (occ < 1 ? 1 : occ) * sms;
+    return KVQ_OK;
+}
+
 int launch_quantize(const uint16_t *x, const kvq_layout &L, const float *codebook,
                     const uint8_t *k, uint64_t seed, uint64_t index_base, uint8_t *codes,
-                    cudaStream_t st) {
-    const int64_t slabs = L.S * (L.T / 32);
-    if (slabs == 0) return KVQ_OK;
-    int log2_upr = 0;
-    while ((1 << log2_upr) < L.D / 8) ++log2_upr;
-    quantize_kernel<<<(unsigned)slabs, kQThreads, 0, st>>>(x, L, codebook, k, seed, index_base,
-                                                          codes, log2_upr);
+                    int32_t *status, cudaStream_t st) {
+    (void)k;   // the kernel reads k from the codebook (slots k..15 repeat the top level)
+    const QGeom g = geometry(L);
+    const int64_t ntiles = L.S * (L.T / 32) * g.nchunk;
+    if (ntiles == 0) return KVQ_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
+    int64_t grid = g_quant_grid[dev] > 0 ? g_quant_grid[dev] : 148;
+    if (grid > ntiles) grid = ntiles;
+    const size_t smem = (size_t)kQStages * g.stage_bytes;
+    quantize_kernel<<<(unsigned)grid, kQThreads, smem, st>>>(x, codebook, g, ntiles, seed,
+                                                             index_base, codes, status);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

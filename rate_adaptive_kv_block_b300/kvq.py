@@ -94,7 +94,7 @@ def lib():
         L.kvq_allocate_static.argtypes = [vp, _Layout, C.c_int, dbl, C.c_int, dbl, vp, vp, vp,
                                           vp, vp, vp, vp, vp]
         L.kvq_quantize.restype = C.c_int
-        L.kvq_quantize.argtypes = [vp, _Layout, vp, vp, u64, u64, vp, vp]
+        L.kvq_quantize.argtypes = [vp, _Layout, vp, vp, u64, u64, vp, vp, vp]
         L.kvq_dequantize.restype = C.c_int
         L.kvq_dequantize.argtypes = [vp, vp, _Layout, vp, vp]
         L.kvq_allocate_report.restype = C.c_int
@@ -162,9 +162,11 @@ def kvq_allocate_static(stats, L: Layout, s: int, budget_bits: float, mode: int,
            "kvq_allocate_static")
 
 
-def kvq_quantize(x, L: Layout, codebook, k, seed: int, index_base: int, codes, stream=None):
+def kvq_quantize(x, L: Layout, codebook, k, seed: int, index_base: int, codes, status=None,
+                 stream=None):
     _check(lib().kvq_quantize(_ptr(x), L.c(), _ptr(codebook), _ptr(k), int(seed),
-                              int(index_base), _ptr(codes), _stream(stream)), "kvq_quantize")
+                              int(index_base), _ptr(codes), _ptr(status), _stream(stream)),
+           "kvq_quantize")
 
 
 def kvq_dequantize(codes, codebook, L: Layout, y, stream=None):
@@ -204,6 +206,7 @@ class Buffers:
         self.lam = torch.zeros(1, dtype=torch.float64, device=dev)
         self.status_stats = torch.zeros(1, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.status_quant = torch.zeros(1, dtype=torch.int32, device=dev)
         self.codes = torch.empty((nb, 16 * L.group), dtype=torch.uint8, device=dev)
 
 
@@ -217,5 +220,6 @@ def quantize(x, L: Layout, budget_bits: float, s: int, seed: int = 0, index_base
     kvq_stats(x, L, buf.stats, buf.status_stats, stream=stream)
     kvq_allocate(buf.stats, L, s, budget_bits, mode, eta, buf.lam, buf.workspace, buf.codebook,
                  buf.k, buf.D_r, buf.H_r, buf.totals, buf.status, stream=stream)
-    kvq_quantize(x, L, buf.codebook, buf.k, seed, index_base, buf.codes, stream=stream)
+    kvq_quantize(x, L, buf.codebook, buf.k, seed, index_base, buf.codes, buf.status_quant,
+                 stream=stream)
     return buf
