@@ -104,6 +104,7 @@ __global__ void ctrl_init_kernel(Ctrl *c, const StatsHeader *hdr, double budget,
     if (threadIdx.x != 0) return;
     search_init(c->s);
     c->s.hi0 = __longlong_as_double((long long)hdr->hi0_bits);
+    c->s.f32_lambda = 1;      // the DP runs at float(lambda)
     c->nb = nb;
     if (mode != KVQ_SUBGRADIENT && nb >= kPilotMinBlocks) search_set_pilot(c->s, nb, kPilotStride);
     c->budget = budget;
@@ -173,15 +174,19 @@ __device__ __forceinline__ void dp_a_stage(const float *__restrict__ tb, float l
 #pragma unroll
     for (int i = 0; i < J; ++i) {
         const float g = sG1[pidx(i, J) * 32 + lane];
+        const float2 g2 = make_float2(g, g), l2 = make_float2(lam, lam);
         const float4 *h4 = reinterpret_cast<const float4 *>(tb + kTblHH + trip_off(i, J));
 #pragma unroll
         for (int q = 0; q < nq; ++q) {
             const float4 h = h4[q];
-            const float hs[4] = {h.x, h.y, h.z, h.w};
+            // two targets per packed fused multiply-add (same rounding as fmaf)
+            const float2 c01 = __ffma2_rn(l2, make_float2(h.x, h.y), g2);
+            const float2 c23 = __ffma2_rn(l2, make_float2(h.z, h.w), g2);
+            const float cs[4] = {c01.x, c01.y, c23.x, c23.y};
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int t = 4 * q + r;
-                if (t < n) acc[t] = fminf(acc[t], fmaf(lam, hs[r], g));
+                if (t < n) acc[t] = fminf(acc[t], cs[r]);
             }
         }
     }
@@ -416,7 +421,7 @@ __device__ __forceinline__ void stage_ctrl(Ctrl &dst, const Ctrl *src) {
 // H_r.  Sum D_r: per CTA in warp and block order, then the last CTA adds the
 // CTA partials in a fixed pattern and a fixed shuffle tree.
 template <bool GENERAL>
-__global__ void __launch_bounds__(RoundCfg<GENERAL>::kWarps * 32)
+__global__ void __launch_bounds__(RoundCfg<GENERAL>::kWarps * 32, 1)
 search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restrict__ ctrl,
               float *__restrict__ rates, uint32_t *__restrict__ masks,
               float *__restrict__ rate_lo, float *__restrict__ rate_hi,

@@ -74,7 +74,7 @@ struct alignas(16) SearchState {
     int32_t pilot_stride;     // pilot round: every pilot_stride-th block (0: no pilot)
     int32_t pilot_blocks;     // blocks the pilot evaluated
     int32_t have_grid;        // round 0 uses probe[4..31] (set by the pilot)
-    int32_t pad;
+    int32_t f32_lambda;       // R depends on lambda only through its binary32 rounding
 };
 
 // ------------------------------------------------------- binary64 helpers
@@ -216,7 +216,7 @@ KVQ_HD inline void search_init(SearchState &s) {
     s.pilot_stride = 0;
     s.pilot_blocks = 0;
     s.have_grid = 0;
-    s.pad = 0;
+    s.f32_lambda = 0;
 }
 
 // Start with a pilot round over every stride-th of nb blocks (stride <= 0: none).
@@ -257,14 +257,39 @@ KVQ_HD inline double search_probe(const SearchState &s, int p) {
     return s.probe[p < s.nprobe ? p : 0];
 }
 
-// P(mid) if it follows from the window (keys of xa, xb), else -1
-KVQ_HD inline int search_known_k(uint64_t kmid, uint64_t kxa, uint64_t kxb) {
-    if (kmid >= kxb) return 1;
-    if (kmid <= kxa) return 0;
+// What the window (xa, xb) fixes about the predicate at a midpoint: order
+// keys of both ends, and, when R depends on lambda only through its binary32
+// rounding (the GPU evaluates the DP at float(lambda)), the binary32 values
+// of both ends: a midpoint that rounds to float(xb) is feasible, one that
+// rounds to float(xa) is not.
+struct SearchWindow {
+    uint64_t kxa, kxb;
+    float fxa, fxb;
+    int f32;
+};
+KVQ_HD inline SearchWindow search_window_of(const SearchState &s) {
+    SearchWindow w;
+    w.kxa = okey(s.xa);
+    w.kxb = okey(s.xb);
+    w.fxa = (float)s.xa;
+    w.fxb = (float)s.xb;
+    w.f32 = s.f32_lambda;
+    return w;
+}
+// P(mid) if it follows from the window, else -1
+KVQ_HD inline int search_known_w(const SearchWindow &w, double mid) {
+    const uint64_t km = okey(mid);
+    if (km >= w.kxb) return 1;
+    if (km <= w.kxa) return 0;
+    if (w.f32) {
+        const float fm = (float)mid;
+        if (fm == w.fxb) return 1;
+        if (fm == w.fxa) return 0;
+    }
     return -1;
 }
 KVQ_HD inline int search_known(const SearchState &s, double mid) {
-    return search_known_k(okey(mid), okey(s.xa), okey(s.xb));
+    return search_known_w(search_window_of(s), mid);
 }
 
 // The update is split so that a warp can run it with one lane per probe:
@@ -327,10 +352,10 @@ KVQ_HD inline int search_advance(SearchState &s, const long long *R, long long B
         s.step = 0;
         s.phase = kSearchWalk;
     }
-    const uint64_t kxa = okey(s.xa), kxb = okey(s.xb);
+    const SearchWindow win = search_window_of(s);
     while (s.step < kSearchSteps) {
         const double mid = half_sum(s.lo, s.hi);
-        const int k = search_known_k(okey(mid), kxa, kxb);
+        const int k = search_known_w(win, mid);
         if (k < 0) break;
         if (k) s.hi = mid; else s.lo = mid;
         ++s.step;
@@ -349,12 +374,12 @@ KVQ_HD inline double search_first_unknown(const SearchState &s) { return half_su
 
 // Path of lane L: writes the unknown midpoints it meets into probe[id].
 KVQ_HD inline void search_path(const SearchState &s, int L, double *probe) {
-    const uint64_t kxa = okey(s.xa), kxb = okey(s.xb);
+    const SearchWindow win = search_window_of(s);
     double a = s.lo, b = s.hi;
     int u = 0, pre = 0;
     for (int dep = s.step; dep < kSearchSteps && u < 5; ++dep) {
         const double mid = half_sum(a, b);
-        int k = search_known_k(okey(mid), kxa, kxb);
+        int k = search_known_w(win, mid);
         if (k < 0) {
             probe[(1 << u) - 1 + pre] = mid;
             k = ((L >> (4 - u)) & 1) ? 0 : 1;   // bit 1: take the infeasible branch
@@ -422,6 +447,7 @@ KVQ_HD inline void search_copy_scalars(SearchState &d, const SearchState &s) {
     d.xa_probe = s.xa_probe; d.xb_probe = s.xb_probe; d.infeasible = s.infeasible;
     d.rounds = s.rounds; d.pilot_stride = s.pilot_stride; d.pilot_blocks = s.pilot_blocks;
     d.have_grid = s.have_grid;
+    d.f32_lambda = s.f32_lambda;
 }
 
 // Single-thread version (host tests).  R: fixed-point rates; B: the budget in

@@ -48,10 +48,11 @@ static double Rfun(double lam, int nbp, const double *bl, const double *br, doub
 }
 // pilot_bias < 0: no pilot; else the pilot sees R * (1 + pilot_bias) on 1/16 of the blocks
 extern "C" int kvqs_run(double hi0, double B, int nbp, const double *bl, const double *br,
-                        double R0, double *out, double pilot_bias) {
+                        double R0, double *out, double pilot_bias, int f32) {
     kvq::SearchState s;
     kvq::search_init(s);
     s.hi0 = hi0;
+    s.f32_lambda = f32 == 1;          // f32 = 2: R at float(lambda), rule off
     const int64_t nb = 4096;
     if (pilot_bias >= 0.0 || pilot_bias <= -1.0) {}
     if (pilot_bias > -1.0) kvq::search_set_pilot(s, nb, 16);
@@ -60,7 +61,9 @@ extern "C" int kvqs_run(double hi0, double B, int nbp, const double *bl, const d
         long long R[kvq::kSearchProbes];
         const bool pilot = s.phase == kvq::kSearchPilot;
         for (int p = 0; p < kvq::kSearchProbes; ++p) {
-            double v = p < s.nprobe || pilot ? Rfun(kvq::search_probe(s, p), nbp, bl, br, R0) : 0.0;
+            double lam = kvq::search_probe(s, p);
+            if (f32) lam = (double)(float)lam;          // R sees lambda only as binary32
+            double v = p < s.nprobe || pilot ? Rfun(lam, nbp, bl, br, R0) : 0.0;
             if (pilot) v = v * (1.0 + pilot_bias) * (double)s.pilot_blocks / (double)nb;
             R[p] = fx(v);
         }
@@ -93,7 +96,7 @@ def lib():
     L.kvqs_budget_fx.argtypes = [C.c_double]
     L.kvqs_run.restype = C.c_int
     L.kvqs_run.argtypes = [C.c_double, C.c_double, C.c_int, C.c_void_p, C.c_void_p, C.c_double,
-                           C.c_void_p, C.c_double]
+                           C.c_void_p, C.c_double, C.c_int]
     return L
 
 
@@ -105,9 +108,13 @@ def R_of(lam, bl, br, R0):
     return r
 
 
-def bisect40(hi0, B, bl, br, R0):
-    """The sequential reading: lambda = 0 if feasible, else doubling, then 40 steps."""
-    R = lambda lam: R_of(lam, bl, br, R0)
+def bisect40(hi0, B, bl, br, R0, f32=False):
+    """The sequential reading: lambda = 0 if feasible, else doubling, then 40 steps
+    (f32: R evaluated at the binary32 rounding of lambda, as on the GPU)."""
+    if f32:
+        R = lambda lam: R_of(float(np.float32(lam)), bl, br, R0)
+    else:
+        R = lambda lam: R_of(lam, bl, br, R0)
     if R(0.0) <= B:
         return 0.0, 0
     hi, n = hi0, 0
@@ -126,11 +133,11 @@ def bisect40(hi0, B, bl, br, R0):
     return hi, 0
 
 
-def run(lib, hi0, B, bl, br, R0, pilot=-2.0):
+def run(lib, hi0, B, bl, br, R0, pilot=-2.0, f32=0):
     out = (C.c_double * 6)()
     a = (C.c_double * len(bl))(*bl)
     b = (C.c_double * len(br))(*br)
-    rc = lib.kvqs_run(hi0, B, len(bl), a, b, R0, out, pilot)
+    rc = lib.kvqs_run(hi0, B, len(bl), a, b, R0, out, pilot, f32)
     assert rc == 0
     return list(out)
 
@@ -167,6 +174,29 @@ def test_same_lambda_as_sequential_bisection(lib):
             assert lam == 0.0 or want - hi0 * 2 ** -39 <= xb <= want
         rounds.append(nr)
     assert sum(rounds) / len(rounds) < 8
+
+
+def test_binary32_lambda_rule_keeps_the_bisection(lib):
+    # when R sees lambda only through float(lambda), midpoints that round to
+    # float(xa) or float(xb) are known without an evaluation: same lambda as
+    # the 40 sequential steps of that R, in no more rounds
+    rng = random.Random(11)
+    saved = 0
+    for _ in range(1500):
+        hi0, bl, br, R0 = random_case(rng)
+        # breakpoints close together near the answer, where binary32 matters
+        B = rng.uniform(0, R0)
+        want, infeasible = bisect40(hi0, B, bl, br, R0, f32=True)
+        lam, xb, Rxb, nr, inf, step = run(lib, hi0, B, bl, br, R0, f32=1)
+        assert lam == want, (hi0, B)
+        assert inf == infeasible
+        plain = run(lib, hi0, B, bl, br, R0, f32=2)
+        assert plain[0] == want
+        if not infeasible:
+            assert Rxb <= B
+        assert nr <= plain[3]
+        saved += plain[3] - nr
+    assert saved > 0
 
 
 @pytest.mark.parametrize("bias", [0.0, 0.05, -0.05, 0.4, -0.4])
