@@ -718,12 +718,14 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
         }
     }
 
-    // ---- emit (sC holds the final state)
+    // ---- emit (sC holds the final state): a thread per block, so every
+    // block's loads are in flight at once
     const int xb_probe = sC.s.xb_probe;
     const int last_round = sC.s.rounds - 1;
-    __shared__ double sD[W];
-    double Dsum = 0.0;                 // this warp's blocks, in order
-    for (int64_t b = (int64_t)blockIdx.x * W + w; b < nb; b += (int64_t)gridDim.x * W) {
+    __shared__ double sD[W * 32];
+    double Dsum = 0.0;                 // this thread's blocks, in order
+    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nb;
+         b += (int64_t)gridDim.x * blockDim.x) {
         const float *tb = tables + b * kRecFloats + kRecTbl;
         uint32_t mask;
         float rate;
@@ -737,39 +739,43 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
         mask &= 0x1ffffu;
         if (mask == 0u) mask = 1u;
         const int k = min(__popc(mask), 16);
-        const bool in = lane < 17 && (mask >> lane & 1u);
-        const int pos = __popc(mask & ((1u << lane) - 1u));
-        float dv = 0.f;
-        if (in) {
-            const uint32_t above = lane < 16 ? (mask >> (lane + 1)) : 0u;
-            if (above) {
-                const int nxt = lane + __ffs(above);
-                dv = dp_at(tb, lane, nxt);
-            }
-            const float q = tb[kTblC + lane];
-            if (pos < 16) codebook[b * 16 + pos] = q;
-            if (pos == k - 1)
-                for (int t = k; t < 16; ++t) codebook[b * 16 + t] = q;
-        }
+        // the chain's levels in slot order, and the sum of its interval
+        // distortions (slot by slot, in order)
+        float dv = 0.f, top = 0.f;
+        int pos = 0, prev = -1;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dv += __shfl_down_sync(0xffffffffu, dv, o);
-        if (lane == 0) {
-            const int d = __float_as_int(tb[kTblHdr + 1]);
-            kout[b] = (uint8_t)k;
-            Dr[b] = dv;
-            Hr[b] = rate / (float)d;
+        for (int t = 0; t < 17; ++t) {
+            if (mask >> t & 1u) {
+                const float q = tb[kTblC + t];
+                if (prev >= 0) dv += dp_at(tb, prev, t);
+                if (pos < 16) codebook[b * 16 + pos] = q;
+                top = q;
+                ++pos;
+                prev = t;
+            }
         }
+        for (int t = k; t < 16; ++t) codebook[b * 16 + t] = top;
+        const int d = __float_as_int(tb[kTblHdr + 1]);
+        kout[b] = (uint8_t)k;
+        Dr[b] = dv;
+        Hr[b] = rate / (float)d;
         Dsum += (double)dv;
     }
-    if (lane == 0) sD[w] = Dsum;
+    sD[threadIdx.x] = Dsum;
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 32) {
+        // fixed tree over the CTA's threads: column of W, then a shuffle tree
         double dd = 0.0;
-        for (int k = 0; k < W; ++k) dd += sD[k];
-        epartial[blockIdx.x] = dd;
-        __threadfence();
-        const unsigned t = atomicAdd(&ctrl->ticket_emit, 1u);
-        is_last = (t == gridDim.x - 1);
+#pragma unroll
+        for (int k = 0; k < W; ++k) dd += sD[k * 32 + threadIdx.x];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dd += __shfl_down_sync(0xffffffffu, dd, o);
+        if (threadIdx.x == 0) {
+            epartial[blockIdx.x] = dd;
+            __threadfence();
+            const unsigned t = atomicAdd(&ctrl->ticket_emit, 1u);
+            is_last = (t == gridDim.x - 1);
+        }
     }
     __syncthreads();
     if (!is_last) return;

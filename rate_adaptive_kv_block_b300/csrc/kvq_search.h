@@ -22,11 +22,10 @@
 // Rates are sums of per-block d_r H_r in fixed point (integers in units of
 // 2^-20 bit) and the budget is compared as floor(B 2^20), so R <= B is an
 // integer comparison with the same outcome as the real one.  The walk's
-// midpoints 0.5 (lo + hi) are binary64 values computed with integer
-// operations that round exactly as the binary64 sum does (half_sum), and
-// lambdas are compared through order-preserving integer keys: the control
-// runs on a GPU whose double-precision unit is slow, and every one of these
-// steps is on the search's critical path.
+// midpoints 0.5 (lo + hi) are one binary64 add of exactly halved operands
+// (half_sum), and lambdas are compared through order-preserving integer keys:
+// the control runs on a GPU whose double-precision unit has a long latency,
+// and every one of these steps is on the search's critical path.
 //
 // Plain C++ usable on the host (tests) and the device (last CTA of a round).
 #pragma once
@@ -96,89 +95,22 @@ KVQ_HD inline uint64_t okey(double x) {
     return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
 }
 
-// 0.5 * (a + b) for finite a, b >= 0, bit for bit as binary64 arithmetic
-// with round-to-nearest-even computes it: the sum rounded once, then halved
-// (exact for normal results).  Integer operations only; inputs outside the
-// fast paths (a subnormal operand, a result that would not stay normal) take
-// the floating-point expression itself.
-KVQ_HD inline double half_sum_general(uint64_t ua, uint64_t ub) {
-    // ua <= ub, both non-negative and normal (or ua == 0)
-    const uint64_t frac = (1ull << 52) - 1;
-    const int eb = (int)(ub >> 52);
-    const int ea = (int)(ua >> 52);
-    uint64_t sig;
-    int e;
-    if (ua == 0) {
-        sig = (ub & frac) | (1ull << 52);
-        e = eb;
-    } else {
-        const int d = eb - ea;
-        if (d >= 54) {                       // a below half an ulp of b
-            sig = (ub & frac) | (1ull << 52);
-            e = eb;
-        } else {
-            const uint64_t ma = ((ua & frac) | (1ull << 52)) << 10;   // bit 62 leading
-            const uint64_t mb = ((ub & frac) | (1ull << 52)) << 10;
-            uint64_t sticky = d ? ((ma & ((1ull << d) - 1)) != 0) : 0;
-            uint64_t m = mb + (ma >> d);                              // < 2^64
-            e = eb;
-            if (m >> 63) {
-                sticky |= m & 1ull;
-                m >>= 1;
-                ++e;
-            }
-            sig = m >> 10;                                            // 53 bits
-            const uint64_t r = m & 0x3ffull;
-            const bool up = r > 0x200ull || (r == 0x200ull && (sticky || (sig & 1ull)));
-            if (up) {
-                ++sig;
-                if (sig >> 53) {
-                    sig >>= 1;
-                    ++e;
-                }
-            }
-        }
-    }
-    if (e - 1 < 1 || e - 1 >= 2047) return 0.5 * (dfrom(ua) + dfrom(ub));
-    return dfrom(((uint64_t)(e - 1) << 52) | (sig & frac));
-}
-
+// 0.5 * (a + b), bit for bit as binary64 arithmetic computes it, for finite
+// a, b >= 0: halving is exact for normal numbers and commutes with rounding,
+// so RN(a + b) / 2 = RN(a/2 + b/2); each half is an exponent decrement
+// (integer) and one binary64 add remains on the critical path instead of an
+// add and a multiply.  Zero, subnormal or near-subnormal operands take the
+// expression itself.
 KVQ_HD inline double half_sum(double a, double b) {
-    uint64_t ua = dbits(a), ub = dbits(b);
-    if (ua > ub) { const uint64_t t = ua; ua = ub; ub = t; }     // a <= b (non-negative)
-    const int eb = (int)(ub >> 52);
-    const int ea = (int)(ua >> 52);
-    if (eb <= 1 || eb >= 2046 || (ub >> 63) || (ea == 0 && ua != 0))
-        return 0.5 * (dfrom(ua) + dfrom(ub));
-    const uint64_t frac = (1ull << 52) - 1;
-    // the bisection's own cases: lo = 0 (halve hi), or lo and hi within a
-    // binade of each other (exponents equal or one apart)
-    if (ua == 0) return dfrom(ub - (1ull << 52));
-    const int d = eb - ea;
-    if (d <= 1) {
-        const uint64_t ma = (ua & frac) | (1ull << 52);
-        const uint64_t mb = (ub & frac) | (1ull << 52);
-        const uint64_t lost = d ? (ma & 1ull) : 0ull;               // bit shifted out of a
-        const uint64_t m = mb + (ma >> d);                          // 53 or 54 bits
-        uint64_t sig;
-        int e;                                                      // exponent of the half sum
-        if (m >> 53) {                                              // sum in [2^53, 2^54)
-            sig = m >> 1;
-            const uint64_t g = m & 1ull;                            // half an ulp
-            if (g && (lost || (sig & 1ull))) ++sig;
-            e = eb;
-        } else {                                                    // d = 1, no carry
-            sig = m;
-            if (lost && (sig & 1ull)) ++sig;                        // exact tie: to even
-            e = eb - 1;
-        }
-        if (sig >> 53) {
-            sig >>= 1;
-            ++e;
-        }
-        return dfrom(((uint64_t)e << 52) | (sig & frac));
+    const uint64_t ua = dbits(a), ub = dbits(b);
+    const uint32_t ea = (uint32_t)(ua >> 52), eb = (uint32_t)(ub >> 52);   // sign bit 0
+    const bool na = ea >= 3 && ea <= 2046, nbb = eb >= 3 && eb <= 2046;
+    if ((na || ua == 0) && (nbb || ub == 0) && (na || nbb)) {
+        const double ah = ua == 0 ? 0.0 : dfrom(ua - (1ull << 52));
+        const double bh = ub == 0 ? 0.0 : dfrom(ub - (1ull << 52));
+        return ah + bh;
     }
-    return half_sum_general(ua, ub);
+    return 0.5 * (a + b);
 }
 
 // x * 2^t for x = 0 or normal x > 0 whose result stays normal (exponent
