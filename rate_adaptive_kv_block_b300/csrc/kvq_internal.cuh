@@ -105,14 +105,18 @@ struct DecodeTables {
     uint32_t trip[kHHFloats];
     uint32_t pair[kDpFloats];
 };
+// trip[idx]: pidx(i, j) | pidx(j, l) << 8 | i << 16 | j << 21 | l << 26 of HH
+// entry idx (l = 17 on row padding); pair[idx]: j | l << 8 of D entry idx.
 constexpr DecodeTables make_decode() {
     DecodeTables t{};
     for (int j = 1; j < 16; ++j)
         for (int i = 0; i < j; ++i)
             for (int k = 0; k < pad4(16 - j); ++k) {
                 const int l = j + 1 + k;
-                t.trip[trip_off(i, j) + k] =
-                    (uint32_t)i | ((uint32_t)j << 8) | ((uint32_t)(l < 17 ? l : 17) << 16);
+                const uint32_t pjl = l < 17 ? (uint32_t)pidx(j, l) : 0u;
+                t.trip[trip_off(i, j) + k] = (uint32_t)pidx(i, j) | (pjl << 8) |
+                                             ((uint32_t)i << 16) | ((uint32_t)j << 21) |
+                                             ((uint32_t)(l < 17 ? l : 17) << 26);
             }
     for (int j = 0; j < 16; ++j)
         for (int k = 0; k < pad4(16 - j); ++k) {

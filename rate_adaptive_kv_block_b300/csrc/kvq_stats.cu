@@ -82,12 +82,14 @@ __device__ __forceinline__ void add_piece(uint32_t b, int j0, int j1, uint32_t n
     const float u = bin_ulp(b);
     const float Y0 = key_value((b << 8) | (uint32_t)j0) - cp;   // >= 0
     const float T1 = cq - key_value((b << 8) | (uint32_t)j1);   // >= 0
-    const long long L = j1 - j0;
-    const long long nn = n;
-    const long long si = (long long)S1 - (long long)j0 * nn;                          // sum i
-    const long long sii = (long long)S2 - 2ll * j0 * (long long)S1 + (long long)j0 * j0 * nn;  // sum i^2
-    const long long sli = L * nn - si;                                                 // sum (L - i)
-    const long long sx = L * si - sii;                                                 // sum i (L - i)
+    // integer sums of i = j - j0 over the piece; every true value lies in
+    // [0, 2^32), so 32-bit modular arithmetic gives it exactly
+    const uint32_t L = (uint32_t)(j1 - j0), u0 = (uint32_t)j0;
+    const uint32_t nn = n;
+    const uint32_t si = S1 - u0 * nn;                               // sum i
+    const uint32_t sii = S2 - 2u * u0 * S1 + u0 * u0 * nn;          // sum i^2
+    const uint32_t sli = L * nn - si;                               // sum (L - i)
+    const uint32_t sx = L * si - sii;                               // sum i (L - i)
     const float fn = (float)nn, fsi = (float)si, fsli = (float)sli, fsx = (float)sx;
     an += fn;
     as1 += fn * Y0 + u * fsi;
@@ -97,16 +99,17 @@ __device__ __forceinline__ void add_piece(uint32_t b, int j0, int j1, uint32_t n
 
 template <int UNITS>
 __global__ void __launch_bounds__(kStatsThreads)
-stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsHeader *__restrict__ hdr,
-             float *__restrict__ recs, int32_t *__restrict__ status) {
+stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr,
+             StatsHeader *__restrict__ hdr, float *__restrict__ recs,
+             int32_t *__restrict__ status) {
     __shared__ __align__(16) StatsSmem sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = L.group, D = L.D;
     const int d = 32 * G;
     const int nG = D / G;
     const int64_t blk = blockIdx.x;
-    const int g = (int)(blk % nG);
-    const int64_t tbk = blk / nG;                       // stream * (T/32) + token block
+    const int g = (int)(blk & (nG - 1));                // nG, G are powers of two
+    const int64_t tbk = blk >> lg_ng;                   // stream * (T/32) + token block
     const int units = d / 8, upr = G / 8;               // 8-entry units, units per row
 
     // ---- load: UNITS 16-byte units per thread
@@ -116,7 +119,7 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsHeader *__restri
         const int u = tid + k * kStatsThreads;
         raw[k] = make_uint4(0, 0, 0, 0);
         if (u < units) {
-            const int row = u / upr, cu = u % upr;
+            const int row = u >> lg_upr, cu = u & (upr - 1);
             const int64_t off = (tbk * 32 + row) * (int64_t)D + (int64_t)g * G + cu * 8;
             raw[k] = __ldg(reinterpret_cast<const uint4 *>(x + off));
         }
@@ -175,10 +178,19 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsHeader *__restri
     // j (d-1) <= 16 (pre + cnt) - 9
     int jlo = 17, jhi = -1;
     if (cnt > 0) {
+        // floor(v / (d-1)) for 0 <= v < 2^20: a single-precision estimate
+        // (off by at most one) corrected with exact integer products
         const int dm1 = d - 1;
+        const float inv = 1.0f / (float)dm1;
+        auto fdiv = [&](int v) {
+            int q = (int)((float)v * inv);
+            if (q * dm1 > v) --q;
+            if ((q + 1) * dm1 <= v) ++q;
+            return q;
+        };
         const int a = 16 * pre - 8, bnd = 16 * (pre + cnt) - 9;
-        jlo = a <= 0 ? 0 : (a + dm1 - 1) / dm1;
-        jhi = bnd < 0 ? -1 : min(bnd / dm1, kCand - 1);
+        jlo = a <= 0 ? 0 : fdiv(a + dm1 - 1);
+        jhi = bnd < 0 ? -1 : min(fdiv(bnd), kCand - 1);
     }
     const bool tgt = jlo <= jhi;
     for (int j = jlo; j <= jhi; ++j) {
@@ -225,37 +237,46 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsHeader *__restri
             if (lane >= o) en += a;
         }
         en -= n;                                                // exclusive
-        uint32_t P1 = 0, P2 = 0;
+        // inclusive prefix count at each of the lane's keys, and the key's
+        // (count, count j, count j^2)
+        uint32_t ci[8], pj[8], pjj[8];
+        {
+            uint32_t run = en;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const uint32_t jj = lane * 8 + q;
-            P1 += c8[q] * jj;
-            P2 += c8[q] * jj * jj;
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t jj = (uint32_t)(lane * 8 + q);
+                run += c8[q];
+                ci[q] = run;
+                pj[q] = c8[q] * jj;
+                pjj[q] = c8[q] * jj * jj;
+            }
         }
         const int j0 = sm.slot_first[sl], nr = sm.slot_nrank[sl];
         for (int j = j0; j < j0 + nr; ++j) {
+            // the rank's key is the first whose inclusive prefix exceeds the
+            // residual: count (and sum over) the keys whose prefix does not
             const uint32_t res = (uint32_t)sm.rank_res[j];
-            const bool mine = res >= en && res < en + n;
-            const int L = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
-            const uint32_t b1 = __reduce_add_sync(0xffffffffu, lane < L ? P1 : 0u);
-            const uint32_t b2 = __reduce_add_sync(0xffffffffu, lane < L ? P2 : 0u);
-            if (lane == L) {
-                uint32_t cum = en, p1 = b1, p2 = b2;
+            uint32_t kb = 0, c0 = 0, p1 = 0, p2 = 0, cle = 0;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint32_t jj = lane * 8 + q;
-                    if (res < cum + c8[q]) {
-                        sm.rank_key[j] = (sm.rank_bin[j] << 8) | (int)jj;
-                        sm.rank_p0[j] = (int)cum;
-                        sm.rank_p1[j] = p1;
-                        sm.rank_p2[j] = p2;
-                        sm.rank_cnt[j] = (int)c8[q];
-                        break;
-                    }
-                    cum += c8[q];
-                    p1 += c8[q] * jj;
-                    p2 += c8[q] * jj * jj;
-                }
+            for (int q = 0; q < 8; ++q) {
+                const bool below = ci[q] <= res;
+                kb += below ? 1u : 0u;
+                c0 += below ? c8[q] : 0u;
+                p1 += below ? pj[q] : 0u;
+                p2 += below ? pjj[q] : 0u;
+                cle += (ci[q] - c8[q] <= res) ? c8[q] : 0u;     // keys at or below
+            }
+            const uint32_t key = __reduce_add_sync(0xffffffffu, kb);
+            const uint32_t P0 = __reduce_add_sync(0xffffffffu, c0);
+            const uint32_t P1 = __reduce_add_sync(0xffffffffu, p1);
+            const uint32_t P2 = __reduce_add_sync(0xffffffffu, p2);
+            const uint32_t CL = __reduce_add_sync(0xffffffffu, cle);
+            if (lane == 0) {
+                sm.rank_key[j] = (sm.rank_bin[j] << 8) | (int)key;
+                sm.rank_p0[j] = (int)P0;
+                sm.rank_p1[j] = P1;
+                sm.rank_p2[j] = P2;
+                sm.rank_cnt[j] = (int)(CL - P0);
             }
         }
     }
@@ -394,12 +415,14 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, StatsHeader *__restri
         const int j = dcd & 255, l = dcd >> 8;
         tb[kTblD + idx] = l < 17 ? sm.pDp[pidx(j, l)] : __int_as_float(0x7f800000);
     }
+    // slots that hold a candidate (0 .. m'-2, and 16 for the maximum)
+    const uint32_t realm = mp > 1 ? (((1u << (mp - 1)) - 1u) | (1u << 16)) : 0u;
     for (int idx = tid; idx < kHHFloats; idx += kStatsThreads) {
         const uint32_t dcd = kDecode.trip[idx];
-        const int i = dcd & 255, j = (dcd >> 8) & 255, l = dcd >> 16;
+        const uint32_t i = (dcd >> 16) & 31u, j = (dcd >> 21) & 31u, l = dcd >> 26;
         float v = 0.f;
-        if (l < 17 && mp > 1 && real(i) && real(j) && real(l))
-            v = hterm(sm.pUp[pidx(i, j)] + sm.pDn[pidx(j, l)]);
+        if (l < 17u && ((realm >> i) & (realm >> j) & (realm >> l) & 1u))
+            v = hterm(sm.pUp[dcd & 255u] + sm.pDn[(dcd >> 8) & 255u]);
         tb[kTblHH + idx] = v;
     }
     if (tid < 20) {
@@ -435,13 +458,16 @@ int launch_stats(const uint16_t *x, const kvq_layout &L, void *stats, int32_t *s
     if (cudaMemsetAsync(stats, 0, sizeof(StatsHeader), st) != cudaSuccess) return KVQ_ERR_CUDA;
     if (nb == 0) return KVQ_OK;
     const int units = 4 * L.group;   // 8-entry units per block
+    int lg_ng = 0, lg_upr = 0;
+    while ((1 << lg_ng) < L.D / L.group) ++lg_ng;
+    while ((1 << lg_upr) < L.group / 8) ++lg_upr;
     StatsHeader *hdr = static_cast<StatsHeader *>(stats);
     float *recs = reinterpret_cast<float *>(static_cast<char *>(stats) + sizeof(StatsHeader));
     const dim3 grid((unsigned)nb);
     if (units <= kStatsThreads)
-        stats_kernel<1><<<grid, kStatsThreads, 0, st>>>(x, L, hdr, recs, status);
+        stats_kernel<1><<<grid, kStatsThreads, 0, st>>>(x, L, lg_ng, lg_upr, hdr, recs, status);
     else
-        stats_kernel<2><<<grid, kStatsThreads, 0, st>>>(x, L, hdr, recs, status);
+        stats_kernel<2><<<grid, kStatsThreads, 0, st>>>(x, L, lg_ng, lg_upr, hdr, recs, status);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
