@@ -8,26 +8,32 @@
 // codepoints; one global lambda.
 //
 // Kernels (all on the caller's stream, no host synchronisation):
-//   ctrl_init      reset the control word in the workspace
+//   ctrl_init      reset the control block in the workspace
 //   (the lambda-independent DP tables of every block -- interval distortion
 //   and entropy terms in "slot" space, see kvq_internal.cuh -- come from
 //   kvq_stats, with max_r (c_max - c_min)^2 in the stats header)
-//   search_round   one warp per block, one lane per probe lambda: each lane
-//                  runs the whole exact DP at its own lambda, so the warp
-//                  evaluates 32 lambdas with no cross-lane traffic and the
-//                  table reads are shared-memory broadcasts.  The rates are
-//                  reduced in a fixed order (per CTA, then by the last CTA
-//                  to finish) and that CTA advances the search:
-//                    bracket round: probes 0 and hi0 * 2^t, t = 0..30;
-//                    bisection round: the 31 nodes of the next 5 levels of
-//                    the bisection tree under [lo, hi] -- every midpoint the
-//                    sequential bisection could visit in its next 5 steps,
-//                    computed with the same fp64 formula 0.5 (lo + hi) --
-//                    then the walk takes the 5 steps.  8 rounds = 40 steps,
-//                    the same lambda as 40 sequential steps.
-//   emit           per block: the chain at the final lambda (recorded by the
-//                  round that evaluated it) -> codebook, k, D_r, H_r; totals;
-//                  the subgradient update in KVQ_SUBGRADIENT mode.
+//   search_kernel  one persistent, cooperative launch for every round of the
+//                  search and the emit.  In a round, one warp per block and
+//                  one lane per probe lambda: each lane runs the whole exact
+//                  DP at its own lambda, so the warp evaluates 32 lambdas
+//                  with no cross-lane traffic and the table reads are
+//                  shared-memory broadcasts.  Per-probe rate sums are exact
+//                  fixed-point integer atomics; the last CTA to finish the
+//                  round advances the search (kvq_search.h) and releases the
+//                  grid for the next round:
+//                    pilot round (large tensors): a sample of the blocks at
+//                    the bracket probes, for an estimate of lambda;
+//                    round 0: probes 0, hi0 * 2^{0,1,2} and a grid (around
+//                    the estimate when there is one);
+//                    bisection rounds: the unknown nodes of the next 5
+//                    levels of the bisection tree under [lo, hi] -- every
+//                    midpoint the sequential bisection could visit next --
+//                    then the walk takes those steps: the same lambda as 40
+//                    sequential steps.
+//                  Emit, after the last round: per block, the chain at the
+//                  final lambda (recorded by the round that evaluated it) ->
+//                  codebook, k, D_r, H_r; totals; the subgradient update in
+//                  KVQ_SUBGRADIENT mode.
 #include <math.h>
 
 #include "kvq_internal.cuh"

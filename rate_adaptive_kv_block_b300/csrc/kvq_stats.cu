@@ -15,14 +15,16 @@
 //   pass 2  entries of those (<= 17) bins count their low byte in a second
 //           histogram (two 16-bit counters per 32-bit word);
 //   select  one warp per selected bin finds the exact key of each rank and
-//           the prefix sums of (1, j, j^2) below it (a count scan, then two
-//           warp reductions).
+//           the prefix sums of (1, j, j^2) below it (a count scan, then
+//           warp reductions over the keys whose prefix stays at or below the
+//           rank).
 // Inside a bin the value is affine in j (one binade quarter: fixed sign and
 // exponent), so the atom moments follow from those exact integer sums without
 // touching the entries again: half a warp per atom sums its bins with a
 // fixed-order tree.  The CTA then builds the block's lambda-independent DP
 // tables (interval distortion and entropy terms, one entropy log2 per level
-// triple) and writes them with the stats row as the block's record.  Every fp32 term added is non-negative, so there is no cancellation.
+// triple) and writes them with the stats row as the block's record.  Every
+// fp32 term added is non-negative, so there is no cancellation.
 // Non-finite entries are the keys of the four lowest and four highest bins.
 #include "kvq_internal.cuh"
 
