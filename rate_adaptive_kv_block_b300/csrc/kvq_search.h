@@ -224,6 +224,48 @@ KVQ_HD inline int search_known(const SearchState &s, double mid) {
     return search_known_w(search_window_of(s), mid);
 }
 
+// Take bisection steps from depth `step` on [lo, hi] while the midpoint is
+// known from the window; returns the depth of the first unknown midpoint
+// (kSearchSteps if none), with lo, hi the interval there.  Fast path (every
+// practical case): lo = 0 with hi far from the subnormal range, or lo normal
+// -- then every midpoint is normal, its half is an exponent decrement, and
+// for positive values order keys compare as raw bits.  Elsewhere the same
+// steps with half_sum and order keys.
+KVQ_HD inline int walk_known(double &lo, double &hi, int step, const SearchWindow &w) {
+    const uint64_t ul = dbits(lo), uh = dbits(hi);
+    const uint32_t el = (uint32_t)(ul >> 52), eh = (uint32_t)(uh >> 52);
+    const bool fast = eh <= 2046 && (ul >> 63) == 0 && ((ul == 0 && eh >= 48) || el >= 3);
+    if (fast) {
+        // raw-bit thresholds for positive midpoints: mid >= xb, mid <= xa
+        const uint64_t rxb = w.kxb ^ (1ull << 63);           // xb >= 0 (or +inf)
+        const uint64_t rxa = (w.kxa >> 63) ? (w.kxa ^ (1ull << 63)) : 0ull;   // xa < 0: none
+        double lh = ul ? dfrom(ul - (1ull << 52)) : 0.0;
+        double hh = dfrom(uh - (1ull << 52));
+        while (step < kSearchSteps) {
+            const double mid = lh + hh;
+            const uint64_t um = dbits(mid);
+            int k;
+            if (um >= rxb) k = 1;
+            else if (um <= rxa) k = 0;
+            else if (w.f32 && (float)mid == w.fxb) k = 1;
+            else if (w.f32 && (float)mid == w.fxa) k = 0;
+            else break;
+            const double mh = dfrom(um - (1ull << 52));
+            if (k) { hi = mid; hh = mh; } else { lo = mid; lh = mh; }
+            ++step;
+        }
+        return step;
+    }
+    while (step < kSearchSteps) {
+        const double mid = half_sum(lo, hi);
+        const int k = search_known_w(w, mid);
+        if (k < 0) break;
+        if (k) hi = mid; else lo = mid;
+        ++step;
+    }
+    return step;
+}
+
 // The update is split so that a warp can run it with one lane per probe:
 //   search_window   fold the round's evaluations into (xa, xb)
 //   search_advance  bracket decisions and the walk (cheap, sequential)
@@ -285,13 +327,7 @@ KVQ_HD inline int search_advance(SearchState &s, const long long *R, long long B
         s.phase = kSearchWalk;
     }
     const SearchWindow win = search_window_of(s);
-    while (s.step < kSearchSteps) {
-        const double mid = half_sum(s.lo, s.hi);
-        const int k = search_known_w(win, mid);
-        if (k < 0) break;
-        if (k) s.hi = mid; else s.lo = mid;
-        ++s.step;
-    }
+    s.step = walk_known(s.lo, s.hi, s.step, win);
     if (s.step >= kSearchSteps) {
         s.lambda = s.hi;
         s.phase = kSearchDone;
@@ -308,17 +344,16 @@ KVQ_HD inline double search_first_unknown(const SearchState &s) { return half_su
 KVQ_HD inline void search_path(const SearchState &s, int L, double *probe) {
     const SearchWindow win = search_window_of(s);
     double a = s.lo, b = s.hi;
-    int u = 0, pre = 0;
-    for (int dep = s.step; dep < kSearchSteps && u < 5; ++dep) {
+    int dep = s.step;
+    for (int u = 0, pre = 0; u < 5; ++u) {
+        dep = walk_known(a, b, dep, win);           // known steps up to the next unknown
+        if (dep >= kSearchSteps) break;
         const double mid = half_sum(a, b);
-        int k = search_known_w(win, mid);
-        if (k < 0) {
-            probe[(1 << u) - 1 + pre] = mid;
-            k = ((L >> (4 - u)) & 1) ? 0 : 1;   // bit 1: take the infeasible branch
-            pre = 2 * pre + (k ? 0 : 1);
-            ++u;
-        }
+        probe[(1 << u) - 1 + pre] = mid;
+        const int k = ((L >> (4 - u)) & 1) ? 0 : 1;  // bit 1: take the infeasible branch
+        pre = 2 * pre + (k ? 0 : 1);
         if (k) b = mid; else a = mid;
+        ++dep;
     }
 }
 
