@@ -730,38 +730,47 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
     const int last_round = sC.s.rounds - 1;
     __shared__ double sD[W * 32];
     double Dsum = 0.0;                 // this thread's blocks, in order
-    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nb;
+    // blocks dealt round-robin over the CTAs (consecutive CTAs, consecutive
+    // blocks), so every SM takes part and no SM's load unit is the bottleneck
+    for (int64_t b = (int64_t)blockIdx.x + (int64_t)gridDim.x * threadIdx.x; b < nb;
          b += (int64_t)gridDim.x * blockDim.x) {
         const float *tb = tables + b * kRecFloats + kRecTbl;
-        uint32_t mask;
-        float rate;
-        if (xb_probe >= 0 && __ldcg(&evr[b]) == last_round) {
-            mask = __ldcg(&masks[b * 32 + xb_probe]);
-            rate = __ldcg(&rates[b * 32 + xb_probe]);
-        } else {
-            mask = __ldcg(&mask_hi[b]);
-            rate = __ldcg(&rate_hi[b]);
-        }
+        // every load that does not depend on the chosen chain, at once
+        const int32_t ev = __ldcg(&evr[b]);
+        const int xp = xb_probe >= 0 ? xb_probe : 0;
+        const uint32_t m_last = __ldcg(&masks[b * 32 + xp]);
+        const float r_last = __ldcg(&rates[b * 32 + xp]);
+        const uint32_t m_hi = __ldcg(&mask_hi[b]);
+        const float r_hi = __ldcg(&rate_hi[b]);
+        float qv[17];
+#pragma unroll
+        for (int t = 0; t < 17; ++t) qv[t] = tb[kTblC + t];
+        const int d = __float_as_int(tb[kTblHdr + 1]);
+        const bool from_last = xb_probe >= 0 && ev == last_round;
+        uint32_t mask = from_last ? m_last : m_hi;
+        const float rate = from_last ? r_last : r_hi;
         mask &= 0x1ffffu;
         if (mask == 0u) mask = 1u;
         const int k = min(__popc(mask), 16);
         // the chain's levels in slot order, and the sum of its interval
-        // distortions (slot by slot, in order)
-        float dv = 0.f, top = 0.f;
-        int pos = 0, prev = -1;
+        // distortions (slot by slot, in order); table addresses come from the
+        // mask alone, so the loads issue together
+        float dv = 0.f, top = qv[0];
+        int prev = 0;
 #pragma unroll
         for (int t = 0; t < 17; ++t) {
-            if (mask >> t & 1u) {
-                const float q = tb[kTblC + t];
-                if (prev >= 0) dv += dp_at(tb, prev, t);
-                if (pos < 16) codebook[b * 16 + pos] = q;
-                top = q;
-                ++pos;
+            const bool in = (mask >> t) & 1u;
+            const bool link = in && t > 0;
+            const float dd = tb[kTblD + (link ? dp_off(prev) + t - prev - 1 : 0)];
+            if (link) dv += dd;
+            const int pos = __popc(mask & ((1u << t) - 1u));
+            if (in && pos < 16) codebook[b * 16 + pos] = qv[t];
+            if (in) {
+                top = qv[t];
                 prev = t;
             }
         }
         for (int t = k; t < 16; ++t) codebook[b * 16 + t] = top;
-        const int d = __float_as_int(tb[kTblHdr + 1]);
         kout[b] = (uint8_t)k;
         Dr[b] = dv;
         Hr[b] = rate / (float)d;
