@@ -34,11 +34,15 @@ constexpr int kStatsThreads = 256;
 constexpr int kStatsWarps = kStatsThreads / 32;
 
 struct StatsSmem {
-    uint32_t h1a[kStatsWarps][256];   // per warp: (count << 22) | sum j
-    uint32_t h1b[kStatsWarps][256];   // per warp: sum j^2
+    union {
+        struct {
+            uint32_t h1a[kStatsWarps][256];   // per warp: (count << 22) | sum j
+            uint32_t h1b[kStatsWarps][256];   // per warp: sum j^2
+        };
+        uint32_t l2[17][128];                 // after the merge: low-byte counts
+    };
     int32_t cnt[256];
     uint32_t s1[256], s2[256];
-    uint32_t l2[17][128];
     uint8_t binslot[256];
     int32_t warp_tot[kStatsWarps];
     int32_t rank_bin[17], rank_res[17], rank_slot[17];
@@ -100,7 +104,7 @@ __device__ __forceinline__ void add_piece(uint32_t b, int j0, int j1, uint32_t n
 }
 
 template <int UNITS>
-__global__ void __launch_bounds__(kStatsThreads)
+__global__ void __launch_bounds__(kStatsThreads, 6)
 stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr,
              StatsHeader *__restrict__ hdr, float *__restrict__ recs,
              int32_t *__restrict__ status) {
@@ -130,8 +134,6 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
     {
         uint4 *z = reinterpret_cast<uint4 *>(&sm.h1a[0][0]);
         for (int i = tid; i < 2 * kStatsWarps * 256 / 4; i += kStatsThreads) z[i] = make_uint4(0, 0, 0, 0);
-        uint4 *z2 = reinterpret_cast<uint4 *>(&sm.l2[0][0]);
-        for (int i = tid; i < 17 * 128 / 4; i += kStatsThreads) z2[i] = make_uint4(0, 0, 0, 0);
         if (tid < kPairs) {
             sm.pDp[tid] = __int_as_float(0x7f800000);   // +inf: no such pair
             sm.pUp[tid] = 0.f;
@@ -175,6 +177,11 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
     sm.s2[tid] = S2;
     int total;
     const int pre = block_excl_scan(cnt, sm.warp_tot, total);
+    // every warp table has been read: its memory becomes the low-byte table
+    {
+        uint4 *z2 = reinterpret_cast<uint4 *>(&sm.l2[0][0]);
+        for (int i = tid; i < 17 * 128 / 4; i += kStatsThreads) z2[i] = make_uint4(0, 0, 0, 0);
+    }
     // ranks r_j = floor((j (d-1) + 8) / 16) inside [pre, pre + cnt):
     // r_j >= pre  <=>  j (d-1) >= 16 pre - 8;  r_j < pre + cnt  <=>
     // j (d-1) <= 16 (pre + cnt) - 9
