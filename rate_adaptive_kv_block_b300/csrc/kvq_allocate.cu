@@ -391,6 +391,11 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 __device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -409,6 +414,33 @@ __device__ __forceinline__ void stage_ctrl(Ctrl &dst, const Ctrl *src) {
     const int4 *s4 = reinterpret_cast<const int4 *>(src);
     int4 *d4 = reinterpret_cast<int4 *>(&dst);
     for (int i = threadIdx.x; i < (int)(sizeof(Ctrl) / 16); i += blockDim.x) d4[i] = __ldcg(s4 + i);
+}
+
+// The search state back to global memory, 16 bytes per lane of one warp.
+__device__ __forceinline__ void publish_search(Ctrl *ctrl, const SearchState &S, int L) {
+    static_assert(sizeof(SearchState) % 16 == 0, "search state in 16-byte pieces");
+    const int4 *src = reinterpret_cast<const int4 *>(&S);
+    int4 *dst = reinterpret_cast<int4 *>(&ctrl->s);
+    for (int i = L; i < (int)(sizeof(SearchState) / 16); i += 32) dst[i] = src[i];
+}
+
+// Thread 0 waits (bounded) until the release generation reaches `target`;
+// false if it gave up.
+__device__ __forceinline__ bool wait_gen(const Ctrl *ctrl, uint32_t target) {
+    uint32_t spins = 0;
+    const unsigned long long t0 = global_ns();
+    while (ld_acquire_u32(&ctrl->gen) < target) {
+        if (++spins > kSpinLimit || global_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
+// Stage only the search state (the probes of a round, its final phase).
+__device__ __forceinline__ void stage_search(SearchState &dst, const SearchState *src) {
+    const int4 *s4 = reinterpret_cast<const int4 *>(src);
+    int4 *d4 = reinterpret_cast<int4 *>(&dst);
+    for (int i = threadIdx.x; i < (int)(sizeof(SearchState) / 16); i += blockDim.x) d4[i] = __ldcg(s4 + i);
 }
 
 // The whole search and the emit in one persistent, cooperative launch.
@@ -450,6 +482,11 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
     __shared__ int32_t sList[W * 32];
     __shared__ float sRb[W * 32];
 
+    // A round's control publishes twice: first the window (which blocks can
+    // still change, so the next round's phase A and table loads can start),
+    // then the round's probes.  `ready`: this CTA holds the current probes.
+    bool ready = true;                   // round 0's come from ctrl_init
+    if (threadIdx.x == 0) timed_out = false;
     for (int iter = 0; iter < kMaxRounds; ++iter) {
         stage_ctrl(sC, ctrl);
         if (threadIdx.x == 0) sAct = 0u;
@@ -465,8 +502,9 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
         int32_t *lout = list + (size_t)((round + 1) & 1) * nb;
         const int64_t nitems = walk ? (int64_t)sC.cnt[round & 1]
                                     : pilot ? (int64_t)sC.s.pilot_blocks : nb;
-        const float lam = (float)(fixed ? sC.lambda_fixed : search_probe(sC.s, lane));
+        float lam = ready ? (float)(fixed ? sC.lambda_fixed : search_probe(sC.s, lane)) : 0.f;
         long long my_sum = 0;
+        bool done = false;
         // Items in chunks of one per thread: item it = blockIdx.x + gridDim.x
         // * (c * blockDim.x + threadIdx.x), so consecutive CTAs take
         // consecutive items.  Phase A (a thread per item) carries the walk's
@@ -521,13 +559,37 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                 lbase = __shfl_sync(0xffffffffu, lbase, 0);
             }
             __syncthreads();
+            const bool prefetched = !ready;
+            if (!ready) {
+                // phase A ran on the published window: load each warp's first
+                // table while the control finishes the round's probes
+                if (w < (int)sN) {
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        tables + (int64_t)sList[w] * kRecFloats + kRecTbl);
+                    float4 *dst = reinterpret_cast<float4 *>(sTbl);
+                    for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
+                }
+                if (threadIdx.x == 0 && !wait_gen(ctrl, 2u * (uint32_t)iter)) timed_out = true;
+                __syncthreads();
+                if (timed_out) break;
+                stage_search(sC.s, &ctrl->s);
+                __syncthreads();
+                ready = true;
+                if (sC.s.phase == kSearchDone) {   // the walk ended: nothing to evaluate
+                    done = true;
+                    break;
+                }
+                lam = (float)(fixed ? sC.lambda_fixed : search_probe(sC.s, lane));
+            }
             const uint32_t n = sN;
             for (uint32_t q = w; q < n; q += W) {
                 const int64_t b = sList[q];
                 const float rb = sRb[q];
-                const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
-                float4 *dst = reinterpret_cast<float4 *>(sTbl);
-                for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
+                if (!(prefetched && q == (uint32_t)w)) {
+                    const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
+                    float4 *dst = reinterpret_cast<float4 *>(sTbl);
+                    for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
+                }
                 __syncwarp();
                 const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
                 float rate;
@@ -555,18 +617,39 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
             if (threadIdx.x == 0) sAct += n;
             __syncthreads();
         }
+        if (!ready && !timed_out) {
+            // no items here: still wait for the probes, so that the previous
+            // control has finished before this CTA can take the ticket
+            if (threadIdx.x == 0 && !wait_gen(ctrl, 2u * (uint32_t)iter)) timed_out = true;
+            __syncthreads();
+            if (!timed_out) {
+                stage_search(sC.s, &ctrl->s);
+                __syncthreads();
+                ready = true;
+                done = sC.s.phase == kSearchDone;
+            }
+        }
+        if (timed_out) {
+            if (threadIdx.x == 0) {
+                atomicExch(&ctrl->err, 1u);
+                *status = KVQ_ERR_TIMEOUT;
+            }
+            return;
+        }
+        if (done) break;
         sSum[w * 32 + lane] = my_sum;
         __syncthreads();
         if (threadIdx.x < 32) {
             long long sum = 0;
             for (int k = 0; k < W; ++k) sum += sSum[k * 32 + threadIdx.x];
-            if (sum) atomicAdd(&ctrl->acc[threadIdx.x], (unsigned long long)sum);
-            __threadfence();
+            if (sum) atomicAdd(&ctrl->acc[threadIdx.x], (unsigned long long)sum);   // no return: a reduction
         }
         __syncthreads();
         if (threadIdx.x == 0) {
             if (sAct) atomicAdd(&ctrl->active[min(round, 15)], sAct);
-            const unsigned t = atomicAdd(&ctrl->ticket, 1u);
+            // acquire-release ticket: orders this CTA's sums (made before the
+            // barrier) before it, and the last CTA sees every CTA's sums
+            const unsigned t = atom_add_acq_rel_u32(&ctrl->ticket, 1u);
             is_last = (t == gridDim.x - 1);
             timed_out = false;
         }
@@ -575,7 +658,6 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
             // ---- last CTA: stage the control block again (the sums are
             // final now), advance the search in shared memory, write back
             // what changed, then release the other CTAs
-            __threadfence();
             stage_ctrl(sC, ctrl);
             __syncthreads();
             if (threadIdx.x < 32) {
@@ -588,6 +670,8 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                 const long long Bfx = sC.budget_fx;
                 if (L == 0) S.hi0 = __longlong_as_double((long long)sC.hi0_bits);
                 __syncwarp();
+                SearchState st;              // every lane keeps the same copy
+                bool walk_on = false;        // a walk follows the first publication
                 if (sC.fixed) {
                     if (L == 0) {
                         S.xb_probe = 0;
@@ -627,8 +711,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                     const double Rb = __shfl_sync(0xffffffffu, r, ib >= 0 ? ib : 0);
                     const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
                     const double Ra = __shfl_sync(0xffffffffu, r, ia >= 0 ? ia : 0);
-                    SearchState st;                       // every lane computes the same estimate
-                    search_copy_scalars(st, S);
+                    search_copy_scalars(st, S);        // every lane computes the same estimate
                     const double est = search_pilot_finish(st, ib, ib >= 0 ? vb : INFINITY, ib >= 0 ? Rb : 0.0,
                                                            ia, ia >= 0 ? va : -1.0, ia >= 0 ? Ra : 0.0, B);
                     __syncwarp();
@@ -664,10 +747,28 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                     const uint32_t ma = __ballot_sync(0xffffffffu, inf && kv == ka);
                     const int ia = ma ? __ffs(ma) - 1 : -1;
                     const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
-                    SearchState st;                       // every lane walks the same path
                     search_copy_scalars(st, S);
                     search_window(st, ib >= 0 ? vb : INFINITY, ib, ib >= 0 ? Rfx[ib] : 0, va, ia);
-                    const int go = search_advance(st, Rfx, Bfx);
+                    walk_on = search_decide(st, Rfx, Bfx);
+                    __syncwarp();
+                    if (L == 0) {
+                        search_copy_scalars(S, st);
+                        if (st.infeasible) ctrl->status = KVQ_ERR_INFEASIBLE;
+                    }
+                }
+                // first publication: the window and the next round's kind
+                __syncwarp();
+                if (L == 0) {
+                    if (!sC.fixed && S.xb_probe >= 0) ctrl->Rxb_fx = Rfx[S.xb_probe];
+                    ctrl->cnt[round & 1] = 0u;     // consumed; the next round appends here
+                    ctrl->ticket = 0u;
+                }
+                publish_search(ctrl, S, L);
+                __syncwarp();            // the warp's writes, then one release store
+                if (L == 0) st_release_u32(&ctrl->gen, 2u * (uint32_t)iter + 1u);
+                // second publication: the walk and the next round's probes
+                if (walk_on) {
+                    const int go = search_walk(st);
                     __syncwarp();
                     if (go) {
                         __shared__ double sProbe[kSearchProbes];
@@ -678,42 +779,20 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                         S.probe[L] = sProbe[L];
                     }
                     __syncwarp();
-                    if (L == 0) {
-                        search_copy_scalars(S, st);
-                        if (st.infeasible) ctrl->status = KVQ_ERR_INFEASIBLE;
-                    }
+                    if (L == 0) search_copy_scalars(S, st);
+                    __syncwarp();
+                    publish_search(ctrl, S, L);
                 }
                 __syncwarp();
-                if (L == 0) {
-                    if (!sC.fixed && S.xb_probe >= 0) ctrl->Rxb_fx = Rfx[S.xb_probe];
-                    ctrl->cnt[round & 1] = 0u;     // consumed; the next round appends here
-                    ctrl->ticket = 0u;
-                }
-                {
-                    // the search state back to global memory, 16 bytes per lane
-                    static_assert(sizeof(SearchState) % 16 == 0, "search state in 16-byte pieces");
-                    const int4 *src = reinterpret_cast<const int4 *>(&S);
-                    int4 *dst = reinterpret_cast<int4 *>(&ctrl->s);
-                    for (int i = L; i < (int)(sizeof(SearchState) / 16); i += 32) dst[i] = src[i];
-                }
-                __threadfence();
-                __syncwarp();
-                if (L == 0) st_release_u32(&ctrl->gen, (uint32_t)(iter + 1));
+                if (L == 0) st_release_u32(&ctrl->gen, 2u * (uint32_t)iter + 2u);
             }
             __syncthreads();
+            ready = true;
         } else {
-            if (threadIdx.x == 0) {
-                uint32_t spins = 0;
-                const unsigned long long t0 = global_ns();
-                while (ld_acquire_u32(&ctrl->gen) < (uint32_t)(iter + 1)) {
-                    if (++spins > kSpinLimit || global_ns() - t0 > kWaitLimitNs) {
-                        timed_out = true;
-                        break;
-                    }
-                    __nanosleep(64);
-                }
-            }
+            // the next round starts on the first publication
+            if (threadIdx.x == 0 && !wait_gen(ctrl, 2u * (uint32_t)iter + 1u)) timed_out = true;
             __syncthreads();
+            ready = false;
             if (timed_out) {
                 if (threadIdx.x == 0) {
                     atomicExch(&ctrl->err, 1u);

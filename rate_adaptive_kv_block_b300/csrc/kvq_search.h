@@ -287,8 +287,9 @@ KVQ_HD inline void search_window(SearchState &s, double vb, int ib, long long Rb
     if (ia >= 0 && okey(va) > okey(s.xa) && okey(va) < okey(s.xb)) { s.xa = va; s.xa_probe = ia; }
 }
 
-// Bracket decisions and the walk.  Returns 1 if probes must be generated.
-KVQ_HD inline int search_advance(SearchState &s, const long long *R, long long Bfx) {
+// The round's bracket decisions (phase changes; lambda = 0; infeasible).
+// Returns 1 if the bisection walk goes on.
+KVQ_HD inline int search_decide(SearchState &s, const long long *R, long long Bfx) {
     s.rounds += 1;
     if (s.phase == kSearchBracket || s.phase == kSearchDouble) {
         if (s.phase == kSearchBracket && R[0] <= Bfx) {          // lambda = 0
@@ -326,6 +327,12 @@ KVQ_HD inline int search_advance(SearchState &s, const long long *R, long long B
         s.step = 0;
         s.phase = kSearchWalk;
     }
+    return 1;
+}
+
+// The walk: the bisection steps the window decides.  Returns 1 if probes
+// must be generated (phase stays Walk), 0 when the 40 steps are done.
+KVQ_HD inline int search_walk(SearchState &s) {
     const SearchWindow win = search_window_of(s);
     s.step = walk_known(s.lo, s.hi, s.step, win);
     if (s.step >= kSearchSteps) {
@@ -335,6 +342,11 @@ KVQ_HD inline int search_advance(SearchState &s, const long long *R, long long B
     }
     s.nprobe = kSearchProbes - 1;
     return 1;
+}
+
+// Bracket decisions and the walk.  Returns 1 if probes must be generated.
+KVQ_HD inline int search_advance(SearchState &s, const long long *R, long long Bfx) {
+    return search_decide(s, R, Bfx) ? search_walk(s) : 0;
 }
 
 // The first unknown midpoint (all paths start there).
