@@ -321,13 +321,19 @@ def main():
         buf.D_r, buf.H_r, buf.totals, buf.status)))
     g_quant = graph_of(lambda: (flush_l2(1), kvq.kvq_quantize(x, L, buf.codebook, buf.k, 0, 0,
                                                               buf.codes, buf.status_quant)))
+    # the same search with emit and quantize fused into its persistent kernel
+    # (kvq_allocate_quantize), reported beside the separate calls
+    g_fused = graph_of(lambda: (flush_l2(1), kvq.kvq_allocate_quantize(
+        buf.stats, x, L, s, B, kvq.KVQ_BISECT40, 0.0, buf.lam, buf.workspace, buf.codebook, buf.k,
+        buf.D_r, buf.H_r, buf.totals, 0, 0, buf.codes, buf.status)))
     nrep = max(args.steps, 10)
-    for g_ in (g_flush, g_stats, g_alloc, g_quant):
+    for g_ in (g_flush, g_stats, g_alloc, g_quant, g_fused):
         device_ms(g_, 2)
     t_flush = device_ms(g_flush, nrep)
     t_scold = device_ms(g_stats, nrep) - t_flush
     t_acold = device_ms(g_alloc, nrep) - t_flush
     t_qcold = device_ms(g_quant, nrep) - t_flush
+    t_fcold = device_ms(g_fused, nrep) - t_flush
 
     # End to end through the C ABI from pinned host memory, pipelined over
     # three streams the way a serving loop would run it: step i's input copy
@@ -406,6 +412,7 @@ def main():
         "eager_stats_ms": mean(t_stats), "eager_allocate_ms": mean(t_alloc),
         "eager_quantize_ms": mean(t_quant),
         "stats_cold_ms": t_scold, "quantize_cold_ms": t_qcold, "allocate_cold_ms": t_acold,
+        "fused_allocate_quantize_cold_ms": t_fcold,
         "cold_method": "graph (L2 flush + kernel) minus graph (L2 flush), device-timed",
         "stats_cold_GBps": s_bytes / (t_scold * 1e-3) / 1e9,
         "quantize_cold_GBps": q_bytes / (t_qcold * 1e-3) / 1e9,

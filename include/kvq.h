@@ -169,6 +169,25 @@ int kvq_allocate_static(const void *stats, kvq_layout L, int s, double budget_bi
                         int32_t *status, void *stream);
 
 /*
+ * kvq_allocate_quantize -- kvq_allocate followed by kvq_quantize in one
+ * launch, with the same results bit for bit (codebook, k, D_r, H_r, totals,
+ * lambda, status; codes as kvq_quantize writes them for this seed and
+ * index_base).  A block whose rate is equal at both ends of the search's
+ * window is constant inside it, so its codebook is already final: such
+ * blocks are emitted and quantized while the last rounds of the lambda
+ * search run, by warps the search leaves idle.  Arguments as for
+ * kvq_allocate and kvq_quantize (x is read again; the workspace is
+ * kvq_workspace_bytes(L, s)); a timed-out copy or wait is reported in
+ * `status` as KVQ_ERR_TIMEOUT.
+ */
+int kvq_allocate_quantize(const void *stats, const uint16_t *x, kvq_layout L, int s,
+                          double budget_bits, int mode, double eta, double *lambda,
+                          void *workspace, float *codebook, uint8_t *k, float *D_r,
+                          float *H_r, double *totals, uint64_t seed,
+                          uint64_t index_base, uint8_t *codes, int32_t *status,
+                          void *stream);
+
+/*
  * kvq_quantize -- unbiased stochastic interpolation and 4-bit packing ("Key
  * formulas": P(q_{i+1} | x) = (x - q_i)/(q_{i+1} - q_i)).  For entry x of
  * block r with levels q_0 < ... < q_{k-1}: i = the largest index with

@@ -37,6 +37,7 @@
 #include <math.h>
 
 #include "kvq_internal.cuh"
+#include "kvq_quant_core.cuh"
 
 namespace kvq {
 
@@ -47,8 +48,7 @@ constexpr int kMaxGrid = 4096;        // CTAs of the persistent search kernel (a
 // CTAs of the persistent search kernel resident at once, per device (set by
 // allocate_init, which the API runs once per device before the first launch)
 constexpr int kMaxDevices = 64;
-static int g_resident[kMaxDevices];
-static int g_resident_gen[kMaxDevices];
+static int g_resident[kMaxDevices][2][2];   // [device][s < 16][fused]
 
 // ---------------------------------------------------------------- workspace
 struct Workspace {
@@ -60,7 +60,9 @@ struct Workspace {
     uint32_t *mask_hi;    // [nblk]       chain at xb
     int32_t *evr;         // [nblk]       round that last evaluated the block
     int32_t *list;        // [2][nblk]    candidate lists (ping-pong)
-    double *epartial;     // [grid]       per-CTA sums of D_r
+    double *epartial;     // [grid]       per-CTA sums of D_r (unused)
+    int32_t *fin;         // [nblk]       fused path: blocks in the order their chain became final
+    uint8_t *fflag;       // [nblk]       fused path: 1 once queued
 };
 
 static size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -74,6 +76,8 @@ size_t workspace_bytes(int64_t nb, int s) {
     b += align_up((size_t)nb * sizeof(int32_t));
     b += align_up((size_t)nb * 2 * sizeof(int32_t));
     b += align_up((size_t)(nb < kMaxGrid ? nb : kMaxGrid) * sizeof(double));
+    b += align_up((size_t)nb * sizeof(int32_t));
+    b += align_up((size_t)nb);
     return b;
 }
 
@@ -97,6 +101,10 @@ static Workspace carve(void *base, int64_t nb) {
     w.list = reinterpret_cast<int32_t *>(p);
     p += align_up((size_t)nb * 2 * sizeof(int32_t));
     w.epartial = reinterpret_cast<double *>(p);
+    p += align_up((size_t)(nb < kMaxGrid ? nb : kMaxGrid) * sizeof(double));
+    w.fin = reinterpret_cast<int32_t *>(p);
+    p += align_up((size_t)nb * sizeof(int32_t));
+    w.fflag = reinterpret_cast<uint8_t *>(p);
     return w;
 }
 
@@ -126,6 +134,9 @@ __global__ void ctrl_init_kernel(Ctrl *c, const StatsHeader *hdr, double budget,
     c->ticket_emit = 0u;
     c->gen = 0u;
     c->err = 0u;
+    c->fin_tail = 0u;
+    c->fin_avail = 0u;
+    c->ticket_f = 0u;
     for (int i = 0; i < 32; ++i) c->acc[i] = 0ull;
     for (int i = 0; i < 16; ++i) c->active[i] = 0u;
     c->Rxb_fx = 0;
@@ -370,6 +381,115 @@ __device__ void dp_path_b(const float *__restrict__ tb, float lam, int s,
     mask = sM[p * 32 + lane];
 }
 
+// ------------------------------------------------- fused emit + quantize
+// The allocate-and-quantize path quantizes each block as soon as its chain is
+// final -- a block whose rate is equal at both ends of the window is constant
+// inside it, so its choice at the final lambda is already known -- using the
+// warps that the late, nearly empty rounds of the search leave idle.
+struct QuantArgs {
+    const uint16_t *x;      // [S, T, D] binary16
+    uint8_t *codes;         // [nblocks][16 group]
+    uint64_t seed, index_base;
+    int D, G;
+    int lg_ng;              // log2(D / G)
+    int lg_upr;             // log2(G / 8)
+};
+
+// Per block, once: from the block's final chain `mask`, the levels, the
+// quantizer's thresholds T[1..15] (returned) and decision table (in
+// `scratch`, 64 floats of the warp's own shared memory); with `emit`, also
+// the block's codebook, k, D_r, H_r -- the same arithmetic, in the same
+// order, as the emit of kvq_allocate.
+__device__ __forceinline__ void fused_prepare(const float *__restrict__ tables, int64_t b,
+                                              uint32_t mask, float rate, bool emit,
+                                              float *__restrict__ codebook,
+                                              uint8_t *__restrict__ kout, float *__restrict__ Dr,
+                                              float *__restrict__ Hr, float *scratch, int lane,
+                                              uint32_t (&T)[16]) {
+    const float *tb = tables + b * kRecFloats + kRecTbl;
+    mask &= 0x1ffffu;
+    if (mask == 0u) mask = 1u;
+    const int k = min(__popc(mask), 16);
+    float *q = scratch;                                             // 16 levels
+    __half2 *thr = reinterpret_cast<__half2 *>(scratch + 16);       // 16 thresholds
+    float2 *qw = reinterpret_cast<float2 *>(scratch + 32);          // 16 decision entries
+    const bool in = lane < 17 && ((mask >> lane) & 1u);
+    const int pos = __popc(mask & ((1u << lane) - 1u));
+    const float qv = lane < 17 ? tb[kTblC + lane] : 0.f;
+    __syncwarp();                                                   // scratch free
+    if (in && pos < 16) q[pos] = qv;
+    __syncwarp();
+    if (lane < 16 && lane >= k) q[lane] = q[k - 1];
+    __syncwarp();
+    if (emit) {
+        if (lane < 16) codebook[b * 16 + lane] = q[lane];
+        if (lane == 0) {
+            float dv = 0.f;
+            int prev = 0;
+#pragma unroll
+            for (int t = 0; t < 17; ++t) {
+                const bool on = (mask >> t) & 1u;
+                const bool link = on && t > 0;
+                const float dd = tb[kTblD + (link ? dp_off(prev) + t - prev - 1 : 0)];
+                if (link) dv += dd;
+                if (on) prev = t;
+            }
+            const int d = __float_as_int(tb[kTblHdr + 1]);
+            kout[b] = (uint8_t)k;
+            Dr[b] = dv;
+            Hr[b] = rate / (float)d;
+        }
+    }
+    if (lane < 16) quant_table_entry(q, k, lane, thr[lane], qw[lane]);
+    __syncwarp();
+    T[0] = 0u;
+#pragma unroll
+    for (int j = 1; j < 16; ++j) {
+        const __half2 h = thr[j];
+        memcpy(&T[j], &h, 4);
+    }
+}
+
+// The binary16 input of rows 4 part .. 4 part + 3 of block b: this lane's
+// (at most two) 8-entry units.
+__device__ __forceinline__ void fused_load(const QuantArgs &qa, int64_t b, int part, int lane,
+                                           uint4 (&raw)[2]) {
+    const int upr = qa.G >> 3, units = 4 << qa.lg_upr;
+    const int64_t tbk = b >> qa.lg_ng;
+    const int g = (int)(b & ((1 << qa.lg_ng) - 1));
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int u = lane + 32 * r;
+        if (u < units) {
+            const int row = 4 * part + (u >> qa.lg_upr), cu = u & (upr - 1);
+            const int64_t flat = (tbk * 32 + row) * (int64_t)qa.D + (int64_t)g * qa.G + cu * 8;
+            raw[r] = __ldg(reinterpret_cast<const uint4 *>(qa.x + flat));
+        }
+    }
+}
+
+// Codes of rows 4 part .. 4 part + 3 of block b from the loaded input.
+__device__ __forceinline__ void fused_codes(const QuantArgs &qa, int64_t b, int part, int lane,
+                                            const uint4 (&raw)[2], const uint32_t (&T)[16],
+                                            const float *scratch) {
+    const float2 *qw = reinterpret_cast<const float2 *>(scratch + 32);
+    const int G = qa.G, upr = G >> 3, units = 4 << qa.lg_upr;
+    const int64_t tbk = b >> qa.lg_ng;
+    const int g = (int)(b & ((1 << qa.lg_ng) - 1));
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int u = lane + 32 * r;
+        if (u < units) {
+            const int row = 4 * part + (u >> qa.lg_upr), cu = u & (upr - 1);
+            const int64_t flat = (tbk * 32 + row) * (int64_t)qa.D + (int64_t)g * G + cu * 8;
+            const uint32_t packed =
+                quant8(raw[r], T, qw, quant_state(qa.seed, qa.index_base, (uint64_t)flat));
+            *reinterpret_cast<uint32_t *>(qa.codes + b * (int64_t)(16 * G) +
+                                          ((row * G + cu * 8) >> 1)) = packed;
+        }
+    }
+}
+
 // ------------------------------------------------------------ search kernel
 template <bool GENERAL>
 struct RoundCfg {
@@ -396,12 +516,18 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t *p, uint32_t v
     asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 constexpr uint32_t kSpinLimit = 1u << 22;     // polls, at most
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // and at most one second
 constexpr int kMaxRounds = 16;
+constexpr uint32_t kGenFinal = 0x10000u;       // fused path: every CTA out of the rounds
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -443,6 +569,108 @@ __device__ __forceinline__ void stage_search(SearchState &dst, const SearchState
     for (int i = threadIdx.x; i < (int)(sizeof(SearchState) / 16); i += blockDim.x) d4[i] = __ldcg(s4 + i);
 }
 
+// Work the fused path's queue (positions below `avail`) for one warp until
+// the release generation reaches `target`: the warp's share is queue
+// positions qj, qj + total_warps, ..., each block in 8 parts of 4 rows (qpart
+// = the next part); per block the levels and tables are prepared once, each
+// part's input is loaded before the previous part is computed, and the
+// release is checked between parts.  Bounded in time like every wait.  Kept
+// out of line so that its registers do not add to the DP's.
+__device__ __noinline__ void run_queue(const Ctrl *ctrl, uint32_t target, uint64_t avail,
+                                       const int32_t *__restrict__ fin,
+                                       const uint32_t *__restrict__ mask_hi,
+                                       const float *__restrict__ rate_hi,
+                                       const float *__restrict__ tables, const QuantArgs &qa,
+                                       float *__restrict__ codebook, uint8_t *__restrict__ kout,
+                                       float *__restrict__ Dr, float *__restrict__ Hr,
+                                       float *scratch, int lane, uint64_t total_warps,
+                                       uint64_t &qj, int &qpart) {
+    const unsigned long long t0 = global_ns();
+    bool prepared = false;
+    int64_t b = 0;
+    uint32_t T[16];
+    uint4 raw[2];
+    // the generation is polled with a relaxed load issued before each part and
+    // read after it, so the poll's latency hides behind the part's work (the
+    // caller's bounded wait then acquires)
+    uint32_t gpoll = lane == 0 ? ld_relaxed_u32(&ctrl->gen) : 0u;
+    for (;;) {
+        const uint32_t gcur = __shfl_sync(0xffffffffu, gpoll, 0);
+        if (gcur >= target) break;
+        if (lane == 0) gpoll = ld_relaxed_u32(&ctrl->gen);
+        if (qj >= avail) {
+            if (global_ns() - t0 > kWaitLimitNs) break;
+            __nanosleep(100);
+            continue;
+        }
+        if (!prepared) {
+            b = __ldcg(&fin[qj]);
+            const uint32_t mk = __ldcg(&mask_hi[b]);
+            const float rt = __ldcg(&rate_hi[b]);
+            fused_load(qa, b, qpart, lane, raw);
+            fused_prepare(tables, b, mk, rt, qpart == 0, codebook, kout, Dr, Hr, scratch, lane, T);
+            prepared = true;
+        }
+        uint4 nxt[2];
+        if (qpart < 7) fused_load(qa, b, qpart + 1, lane, nxt);
+        fused_codes(qa, b, qpart, lane, raw, T, scratch);
+        raw[0] = nxt[0];
+        raw[1] = nxt[1];
+        if (++qpart == 8) {
+            qpart = 0;
+            qj += total_warps;
+            prepared = false;
+        }
+    }
+}
+
+// The rest of one warp's queue share, then the blocks that no round
+// finalized (their chain at the search's end), after every CTA has left the
+// rounds.
+__device__ __noinline__ void finish_blocks(const Ctrl *ctrl, int64_t nb, int xb_probe,
+                                           int last_round, const int32_t *__restrict__ fin,
+                                           const uint8_t *__restrict__ fflag,
+                                           const int32_t *__restrict__ evr,
+                                           const uint32_t *__restrict__ masks,
+                                           const float *__restrict__ rates,
+                                           const uint32_t *__restrict__ mask_hi,
+                                           const float *__restrict__ rate_hi,
+                                           const float *__restrict__ tables, const QuantArgs &qa,
+                                           float *__restrict__ codebook, uint8_t *__restrict__ kout,
+                                           float *__restrict__ Dr, float *__restrict__ Hr,
+                                           float *scratch, int lane, uint64_t gw,
+                                           uint64_t total_warps, uint64_t qj, int qpart) {
+    const uint64_t fin_total = __ldcg(&ctrl->fin_tail);
+    uint32_t T[16];
+    uint4 raw[2], nxt[2];
+    for (; qj < fin_total; qj += total_warps, qpart = 0) {
+        const int64_t b = __ldcg(&fin[qj]);
+        fused_load(qa, b, qpart, lane, raw);
+        fused_prepare(tables, b, __ldcg(&mask_hi[b]), __ldcg(&rate_hi[b]), qpart == 0, codebook,
+                      kout, Dr, Hr, scratch, lane, T);
+        for (int part = qpart; part < 8; ++part) {
+            if (part < 7) fused_load(qa, b, part + 1, lane, nxt);
+            fused_codes(qa, b, part, lane, raw, T, scratch);
+            raw[0] = nxt[0];
+            raw[1] = nxt[1];
+        }
+    }
+    for (int64_t b = (int64_t)gw; b < nb; b += (int64_t)total_warps) {
+        if (__ldcg(&fflag[b])) continue;
+        const bool from_last = xb_probe >= 0 && __ldcg(&evr[b]) == last_round;
+        const uint32_t mk = from_last ? __ldcg(&masks[b * 32 + xb_probe]) : __ldcg(&mask_hi[b]);
+        const float rt = from_last ? __ldcg(&rates[b * 32 + xb_probe]) : __ldcg(&rate_hi[b]);
+        fused_load(qa, b, 0, lane, raw);
+        fused_prepare(tables, b, mk, rt, true, codebook, kout, Dr, Hr, scratch, lane, T);
+        for (int part = 0; part < 8; ++part) {
+            if (part < 7) fused_load(qa, b, part + 1, lane, nxt);
+            fused_codes(qa, b, part, lane, raw, T, scratch);
+            raw[0] = nxt[0];
+            raw[1] = nxt[1];
+        }
+    }
+}
+
 // The whole search and the emit in one persistent, cooperative launch.
 //
 // Each round: the grid's warps take the round's blocks (all blocks in the
@@ -458,7 +686,7 @@ __device__ __forceinline__ void stage_search(SearchState &dst, const SearchState
 // D_r (sum of the chain's interval distortions, reduced in a fixed tree) and
 // H_r.  Sum D_r: per CTA in warp and block order, then the last CTA adds the
 // CTA partials in a fixed pattern and a fixed shuffle tree.
-template <bool GENERAL>
+template <bool GENERAL, bool QUANT>
 __global__ void __launch_bounds__(RoundCfg<GENERAL>::kWarps * 32, 1)
 search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restrict__ ctrl,
               float *__restrict__ rates, uint32_t *__restrict__ masks,
@@ -467,7 +695,8 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
               int32_t *__restrict__ list, double *__restrict__ epartial,
               float *__restrict__ codebook, uint8_t *__restrict__ kout, float *__restrict__ Dr,
               float *__restrict__ Hr, double *__restrict__ totals, double *__restrict__ lambda_out,
-              int32_t *__restrict__ status) {
+              int32_t *__restrict__ status, QuantArgs qa, int32_t *__restrict__ fin,
+              uint8_t *__restrict__ fflag) {
     using Cfg = RoundCfg<GENERAL>;
     constexpr int W = Cfg::kWarps;
     extern __shared__ __align__(16) float smem[];
@@ -487,6 +716,19 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
     // then the round's probes.  `ready`: this CTA holds the current probes.
     bool ready = true;                   // round 0's come from ctrl_init
     if (threadIdx.x == 0) timed_out = false;
+    // fused path: this warp's share of the queue of final blocks (queue
+    // positions qj, qj + total_warps, ...), each in 8 parts of 4 rows; the
+    // warp checks for a release between parts
+    const uint64_t total_warps = (uint64_t)gridDim.x * W;
+    uint64_t qj = (uint64_t)blockIdx.x * W + w;
+    int qpart = 0;
+    float *scratch = sState;             // free whenever the warp is not in a DP
+    if constexpr (QUANT) {
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nb;
+             i += (int64_t)gridDim.x * blockDim.x)
+            fflag[i] = 0;
+    }
+
     for (int iter = 0; iter < kMaxRounds; ++iter) {
         stage_ctrl(sC, ctrl);
         if (threadIdx.x == 0) sAct = 0u;
@@ -548,6 +790,21 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                 }
                 if (act) evr[bsel] = round;
             }
+            if constexpr (QUANT) {
+                // a candidate whose rate is equal at both ends is final:
+                // queue it for the idle warps
+                const bool fin_now = walk && it < nitems && !act;
+                const uint32_t fm = __ballot_sync(0xffffffffu, fin_now);
+                if (fm) {
+                    uint32_t fb = 0;
+                    if (lane == 0) fb = atomicAdd(&ctrl->fin_tail, (uint32_t)__popc(fm));
+                    fb = __shfl_sync(0xffffffffu, fb, 0);
+                    if (fin_now) {
+                        fin[fb + __popc(fm & ((1u << lane) - 1u))] = bsel;
+                        fflag[bsel] = 1;
+                    }
+                }
+            }
             // room in the next round's list: one atomic per warp; the entries
             // are written after the DP, so its latency is hidden
             uint32_t lbase = 0, lrank = 0;
@@ -569,6 +826,10 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                     float4 *dst = reinterpret_cast<float4 *>(sTbl);
                     for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
                 }
+                if constexpr (QUANT)
+                    run_queue(ctrl, 2u * (uint32_t)iter, (uint64_t)sC.fin_avail, fin, mask_hi, rate_hi,
+                              tables, qa, codebook, kout, Dr, Hr, scratch, lane, total_warps, qj,
+                              qpart);
                 if (threadIdx.x == 0 && !wait_gen(ctrl, 2u * (uint32_t)iter)) timed_out = true;
                 __syncthreads();
                 if (timed_out) break;
@@ -620,6 +881,10 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
         if (!ready && !timed_out) {
             // no items here: still wait for the probes, so that the previous
             // control has finished before this CTA can take the ticket
+            if constexpr (QUANT)
+                    run_queue(ctrl, 2u * (uint32_t)iter, (uint64_t)sC.fin_avail, fin, mask_hi, rate_hi,
+                              tables, qa, codebook, kout, Dr, Hr, scratch, lane, total_warps, qj,
+                              qpart);
             if (threadIdx.x == 0 && !wait_gen(ctrl, 2u * (uint32_t)iter)) timed_out = true;
             __syncthreads();
             if (!timed_out) {
@@ -762,6 +1027,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                     if (!sC.fixed && S.xb_probe >= 0) ctrl->Rxb_fx = Rfx[S.xb_probe];
                     ctrl->cnt[round & 1] = 0u;     // consumed; the next round appends here
                     ctrl->ticket = 0u;
+                    ctrl->fin_avail = sC.fin_tail;  // every queue append of this round is in
                 }
                 publish_search(ctrl, S, L);
                 __syncwarp();            // the warp's writes, then one release store
@@ -790,6 +1056,10 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
             ready = true;
         } else {
             // the next round starts on the first publication
+            if constexpr (QUANT)
+                run_queue(ctrl, 2u * (uint32_t)iter + 1u, (uint64_t)sC.fin_avail, fin, mask_hi,
+                          rate_hi, tables, qa, codebook, kout, Dr, Hr, scratch, lane, total_warps,
+                          qj, qpart);
             if (threadIdx.x == 0 && !wait_gen(ctrl, 2u * (uint32_t)iter + 1u)) timed_out = true;
             __syncthreads();
             ready = false;
@@ -803,82 +1073,106 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
         }
     }
 
-    // ---- emit (sC holds the final state): a thread per block, so every
-    // block's loads are in flight at once
+    // ---- after the last round (sC holds the final state)
     const int xb_probe = sC.s.xb_probe;
     const int last_round = sC.s.rounds - 1;
-    __shared__ double sD[W * 32];
-    double Dsum = 0.0;                 // this thread's blocks, in order
-    // blocks dealt round-robin over the CTAs (consecutive CTAs, consecutive
-    // blocks), so every SM takes part and no SM's load unit is the bottleneck
-    for (int64_t b = (int64_t)blockIdx.x + (int64_t)gridDim.x * threadIdx.x; b < nb;
-         b += (int64_t)gridDim.x * blockDim.x) {
-        const float *tb = tables + b * kRecFloats + kRecTbl;
-        // every load that does not depend on the chosen chain, at once
-        const int32_t ev = __ldcg(&evr[b]);
-        const int xp = xb_probe >= 0 ? xb_probe : 0;
-        const uint32_t m_last = __ldcg(&masks[b * 32 + xp]);
-        const float r_last = __ldcg(&rates[b * 32 + xp]);
-        const uint32_t m_hi = __ldcg(&mask_hi[b]);
-        const float r_hi = __ldcg(&rate_hi[b]);
-        float qv[17];
-#pragma unroll
-        for (int t = 0; t < 17; ++t) qv[t] = tb[kTblC + t];
-        const int d = __float_as_int(tb[kTblHdr + 1]);
-        const bool from_last = xb_probe >= 0 && ev == last_round;
-        uint32_t mask = from_last ? m_last : m_hi;
-        const float rate = from_last ? r_last : r_hi;
-        mask &= 0x1ffffu;
-        if (mask == 0u) mask = 1u;
-        const int k = min(__popc(mask), 16);
-        // the chain's levels in slot order, and the sum of its interval
-        // distortions (slot by slot, in order); table addresses come from the
-        // mask alone, so the loads issue together
-        float dv = 0.f, top = qv[0];
-        int prev = 0;
-#pragma unroll
-        for (int t = 0; t < 17; ++t) {
-            const bool in = (mask >> t) & 1u;
-            const bool link = in && t > 0;
-            const float dd = tb[kTblD + (link ? dp_off(prev) + t - prev - 1 : 0)];
-            if (link) dv += dd;
-            const int pos = __popc(mask & ((1u << t) - 1u));
-            if (in && pos < 16) codebook[b * 16 + pos] = qv[t];
-            if (in) {
-                top = qv[t];
-                prev = t;
-            }
-        }
-        for (int t = k; t < 16; ++t) codebook[b * 16 + t] = top;
-        kout[b] = (uint8_t)k;
-        Dr[b] = dv;
-        Hr[b] = rate / (float)d;
-        Dsum += (double)dv;
-    }
-    sD[threadIdx.x] = Dsum;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        // fixed tree over the CTA's threads: column of W, then a shuffle tree
-        double dd = 0.0;
-#pragma unroll
-        for (int k = 0; k < W; ++k) dd += sD[k * 32 + threadIdx.x];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dd += __shfl_down_sync(0xffffffffu, dd, o);
+    if constexpr (QUANT) {
+        // every CTA out of the rounds (the queue is complete), then: the rest
+        // of this warp's queue units, and the blocks the last rounds settled
+        __syncthreads();
         if (threadIdx.x == 0) {
-            epartial[blockIdx.x] = dd;
-            __threadfence();
-            const unsigned t = atomicAdd(&ctrl->ticket_emit, 1u);
-            is_last = (t == gridDim.x - 1);
+            const unsigned t = atom_add_acq_rel_u32(&ctrl->ticket_f, 1u);
+            if (t == gridDim.x - 1) st_release_u32(&ctrl->gen, kGenFinal);
+            else if (!wait_gen(ctrl, kGenFinal)) timed_out = true;
         }
+        __syncthreads();
+        if (timed_out) {
+            if (threadIdx.x == 0) {
+                atomicExch(&ctrl->err, 1u);
+                *status = KVQ_ERR_TIMEOUT;
+            }
+            return;
+        }
+        finish_blocks(ctrl, nb, xb_probe, last_round, fin, fflag, evr, masks, rates, mask_hi, rate_hi,
+                      tables, qa, codebook, kout, Dr, Hr, scratch, lane,
+                      (uint64_t)blockIdx.x * W + w, total_warps, qj, qpart);
+    } else {
+        // emit: a thread per block, so every block's loads are in flight at
+        // once; blocks dealt round-robin over the CTAs (consecutive CTAs,
+        // consecutive blocks), so every SM takes part
+        for (int64_t b = (int64_t)blockIdx.x + (int64_t)gridDim.x * threadIdx.x; b < nb;
+             b += (int64_t)gridDim.x * blockDim.x) {
+            const float *tb = tables + b * kRecFloats + kRecTbl;
+            // every load that does not depend on the chosen chain, at once
+            const int32_t ev = __ldcg(&evr[b]);
+            const int xp = xb_probe >= 0 ? xb_probe : 0;
+            const uint32_t m_last = __ldcg(&masks[b * 32 + xp]);
+            const float r_last = __ldcg(&rates[b * 32 + xp]);
+            const uint32_t m_hi = __ldcg(&mask_hi[b]);
+            const float r_hi = __ldcg(&rate_hi[b]);
+            float qv[17];
+#pragma unroll
+            for (int t = 0; t < 17; ++t) qv[t] = tb[kTblC + t];
+            const int d = __float_as_int(tb[kTblHdr + 1]);
+            const bool from_last = xb_probe >= 0 && ev == last_round;
+            uint32_t mask = from_last ? m_last : m_hi;
+            const float rate = from_last ? r_last : r_hi;
+            mask &= 0x1ffffu;
+            if (mask == 0u) mask = 1u;
+            const int k = min(__popc(mask), 16);
+            // the chain's levels in slot order, and the sum of its interval
+            // distortions (slot by slot, in order); table addresses come from
+            // the mask alone, so the loads issue together
+            float dv = 0.f, top = qv[0];
+            int prev = 0;
+#pragma unroll
+            for (int t = 0; t < 17; ++t) {
+                const bool in = (mask >> t) & 1u;
+                const bool link = in && t > 0;
+                const float dd = tb[kTblD + (link ? dp_off(prev) + t - prev - 1 : 0)];
+                if (link) dv += dd;
+                const int pos = __popc(mask & ((1u << t) - 1u));
+                if (in && pos < 16) codebook[b * 16 + pos] = qv[t];
+                if (in) {
+                    top = qv[t];
+                    prev = t;
+                }
+            }
+            for (int t = k; t < 16; ++t) codebook[b * 16 + t] = top;
+            kout[b] = (uint8_t)k;
+            Dr[b] = dv;
+            Hr[b] = rate / (float)d;
+        }
+    }
+    // ---- totals, by the last CTA to finish: D summed over the blocks in
+    // index order, in a fixed pattern (contiguous chunks of four interleaved
+    // accumulators, then a fixed tree)
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned t = atom_add_acq_rel_u32(&ctrl->ticket_emit, 1u);   // orders this CTA's D_r
+        is_last = (t == gridDim.x - 1);
     }
     __syncthreads();
     if (!is_last) return;
-    __threadfence();
     __shared__ double sPart[W * 32];
     {
-        double acc = 0.0;
-        for (unsigned k = threadIdx.x; k < gridDim.x; k += W * 32) acc += __ldcg(&epartial[k]);
-        sPart[threadIdx.x] = acc;
+        const int64_t chunk = (nb + W * 32 - 1) / (W * 32);
+        const int64_t b0 = (int64_t)threadIdx.x * chunk;
+        const int64_t b1 = b0 + chunk < nb ? b0 + chunk : nb;
+        double acc[4] = {0.0, 0.0, 0.0, 0.0};
+        int64_t i = b0;
+        for (; i + 4 <= b1; i += 4) {
+            const float d0 = __ldcg(&Dr[i]), d1 = __ldcg(&Dr[i + 1]);
+            const float d2 = __ldcg(&Dr[i + 2]), d3 = __ldcg(&Dr[i + 3]);
+            acc[0] += (double)d0;
+            acc[1] += (double)d1;
+            acc[2] += (double)d2;
+            acc[3] += (double)d3;
+        }
+        if (i < b1) acc[0] += (double)__ldcg(&Dr[i]);
+        if (i + 1 < b1) acc[1] += (double)__ldcg(&Dr[i + 1]);
+        if (i + 2 < b1) acc[2] += (double)__ldcg(&Dr[i + 2]);
+        sPart[threadIdx.x] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     }
     __syncthreads();
     if (threadIdx.x >= 32) return;
@@ -906,6 +1200,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
     if (__ldcg(&ctrl->err)) st = KVQ_ERR_TIMEOUT;
     *status = st;
     ctrl->ticket_emit = 0u;
+    ctrl->ticket_f = 0u;
 }
 
 __global__ void empty_alloc_kernel(double *totals, double *lambda_out, int32_t *status, int mode,
@@ -926,7 +1221,8 @@ __global__ void empty_alloc_kernel(double *totals, double *lambda_out, int32_t *
 
 int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget, int mode,
                     double eta, double *lambda, void *workspace, float *codebook, uint8_t *k,
-                    float *Dr, float *Hr, double *totals, int32_t *status, cudaStream_t st) {
+                    float *Dr, float *Hr, double *totals, int32_t *status, cudaStream_t st,
+                    const uint16_t *x, uint64_t seed, uint64_t index_base, uint8_t *codes) {
     const int64_t nb = num_blocks(L);
     if (nb == 0) {
         empty_alloc_kernel<<<1, 32, 0, st>>>(totals, lambda, status, mode, eta, budget);
@@ -939,19 +1235,32 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
     ctrl_init_kernel<<<1, 32, 0, st>>>(ws.ctrl, hdr, budget, eta, mode, lambda, nb);
     if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
     const bool general = s < 16;
+    const bool quant = codes != nullptr;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
-    const int resident = general ? g_resident_gen[dev] : g_resident[dev];
+    const int resident = g_resident[dev][general ? 1 : 0][quant ? 1 : 0];
     const int W = general ? RoundCfg<true>::kWarps : RoundCfg<false>::kWarps;
     const int64_t need = (nb + W - 1) / W;
     int64_t grid = need < resident ? need : resident;
     if (grid > kMaxGrid) grid = kMaxGrid;
     if (grid < 1) return KVQ_ERR_CUDA;
+    QuantArgs qa = {};
+    if (quant) {
+        qa.x = x;
+        qa.codes = codes;
+        qa.seed = seed;
+        qa.index_base = index_base;
+        qa.D = L.D;
+        qa.G = L.group;
+        while ((1 << qa.lg_ng) < L.D / L.group) ++qa.lg_ng;
+        while ((1 << qa.lg_upr) < L.group / 8) ++qa.lg_upr;
+    }
     void *args[] = {(void *)&recs, (void *)&nb, (void *)&s, (void *)&ws.ctrl, (void *)&ws.rates,
                     (void *)&ws.masks, (void *)&ws.rate_lo, (void *)&ws.rate_hi,
                     (void *)&ws.mask_hi, (void *)&ws.evr, (void *)&ws.list, (void *)&ws.epartial,
                     (void *)&codebook, (void *)&k, (void *)&Dr, (void *)&Hr, (void *)&totals,
-                    (void *)&lambda, (void *)&status};
+                    (void *)&lambda, (void *)&status, (void *)&qa, (void *)&ws.fin,
+                    (void *)&ws.fflag};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)(W * 32));
@@ -962,7 +1271,10 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const void *fn = general ? (const void *)search_kernel<true> : (const void *)search_kernel<false>;
+    const void *fn = general ? (quant ? (const void *)search_kernel<true, true>
+                                      : (const void *)search_kernel<true, false>)
+                             : (quant ? (const void *)search_kernel<false, true>
+                                      : (const void *)search_kernel<false, false>);
     if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return KVQ_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
@@ -980,29 +1292,34 @@ int allocate_report(const void *workspace, kvq_report *r) {
     return KVQ_OK;
 }
 
+template <bool GENERAL, bool QUANT>
+static int setup_search_kernel(int sms, int &resident) {
+    const void *fn = (const void *)search_kernel<GENERAL, QUANT>;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)RoundCfg<GENERAL>::kSmem) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, RoundCfg<GENERAL>::kWarps * 32,
+                                                      RoundCfg<GENERAL>::kSmem) != cudaSuccess ||
+        occ < 1)
+        return KVQ_ERR_CUDA;
+    resident = occ * sms;
+    return KVQ_OK;
+}
+
 int allocate_init() {
-    // more than 48 KB of dynamic shared memory for the search kernel, and the
-    // number of its CTAs that fit on the device at once (the cooperative grid)
-    int dev = 0, sms = 0, occ = 0, occg = 0;
+    // more than 48 KB of dynamic shared memory for the search kernels, and the
+    // number of their CTAs that fit on the device at once (the cooperative grid)
+    int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
-    if (cudaFuncSetAttribute(search_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)RoundCfg<false>::kSmem) != cudaSuccess)
-        return KVQ_ERR_CUDA;
-    if (cudaFuncSetAttribute(search_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)RoundCfg<true>::kSmem) != cudaSuccess)
-        return KVQ_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return KVQ_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, search_kernel<false>,
-                                                      RoundCfg<false>::kWarps * 32,
-                                                      RoundCfg<false>::kSmem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occg, search_kernel<true>,
-                                                      RoundCfg<true>::kWarps * 32,
-                                                      RoundCfg<true>::kSmem) != cudaSuccess)
+    int (&r)[2][2] = g_resident[dev];
+    if (setup_search_kernel<false, false>(sms, r[0][0]) != KVQ_OK ||
+        setup_search_kernel<false, true>(sms, r[0][1]) != KVQ_OK ||
+        setup_search_kernel<true, false>(sms, r[1][0]) != KVQ_OK ||
+        setup_search_kernel<true, true>(sms, r[1][1]) != KVQ_OK)
         return KVQ_ERR_CUDA;
-    if (occ < 1 || occg < 1) return KVQ_ERR_CUDA;
-    g_resident[dev] = occ * sms;
-    g_resident_gen[dev] = occg * sms;
     return KVQ_OK;
 }
 

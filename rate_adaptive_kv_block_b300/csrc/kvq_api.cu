@@ -11,7 +11,9 @@ int launch_stats(const uint16_t *x, const kvq_layout &L, void *stats, int32_t *s
                  cudaStream_t st);
 int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget, int mode,
                     double eta, double *lambda, void *workspace, float *codebook, uint8_t *k,
-                    float *Dr, float *Hr, double *totals, int32_t *status, cudaStream_t st);
+                    float *Dr, float *Hr, double *totals, int32_t *status, cudaStream_t st,
+                    const uint16_t *x = nullptr, uint64_t seed = 0, uint64_t index_base = 0,
+                    uint8_t *codes = nullptr);
 int launch_quantize(const uint16_t *x, const kvq_layout &L, const float *codebook,
                     const uint8_t *k, uint64_t seed, uint64_t index_base, uint8_t *codes,
                     int32_t *status, cudaStream_t st);
@@ -120,6 +122,37 @@ int kvq_allocate(const void *stats, kvq_layout L, int s, double budget_bits, int
     if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
     return launch_allocate(stats, L, s, budget_bits, mode, eta, lambda, workspace, codebook, k,
                            D_r, H_r, totals, status, static_cast<cudaStream_t>(stream));
+}
+
+int kvq_allocate_quantize(const void *stats, const uint16_t *x, kvq_layout L, int s,
+                          double budget_bits, int mode, double eta, double *lambda,
+                          void *workspace, float *codebook, uint8_t *k, float *D_r, float *H_r,
+                          double *totals, uint64_t seed, uint64_t index_base, uint8_t *codes,
+                          int32_t *status, void *stream) {
+    if (!layout_ok(L) || s < 2 || s > kMaxLev) return KVQ_ERR_INVALID_ARG;
+    if (!(budget_bits >= 0.0) || !isfinite(budget_bits)) return KVQ_ERR_INVALID_ARG;
+    if (mode != KVQ_BISECT40 && mode != KVQ_SUBGRADIENT) return KVQ_ERR_INVALID_ARG;
+    if (!(eta >= 0.0) || !isfinite(eta)) return KVQ_ERR_INVALID_ARG;
+    if (!lambda || !totals || !status) return KVQ_ERR_INVALID_ARG;
+    if (index_base & 1u) return KVQ_ERR_INVALID_ARG;
+    const uint64_t n = (uint64_t)L.S * (uint64_t)L.T * (uint64_t)L.D;
+    if (index_base > (1ull << 40) || n > (1ull << 40) - index_base) return KVQ_ERR_INVALID_ARG;
+    const int64_t nb = num_blocks(L);
+    if (nb > 0) {
+        if (!stats || !x || !workspace || !codebook || !k || !D_r || !H_r || !codes)
+            return KVQ_ERR_INVALID_ARG;
+        if (!aligned16(stats) || !aligned16(x) || !aligned16(workspace) || !aligned16(codebook) ||
+            !aligned16(codes))
+            return KVQ_ERR_INVALID_ARG;
+        if (nb > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
+    }
+    if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
+    if (nb == 0)
+        return launch_allocate(stats, L, s, budget_bits, mode, eta, lambda, workspace, codebook,
+                               k, D_r, H_r, totals, status, static_cast<cudaStream_t>(stream));
+    return launch_allocate(stats, L, s, budget_bits, mode, eta, lambda, workspace, codebook, k,
+                           D_r, H_r, totals, status, static_cast<cudaStream_t>(stream), x, seed,
+                           index_base, codes);
 }
 
 int kvq_allocate_static(const void *stats, kvq_layout L, int s, double budget_bits, int mode,

@@ -144,6 +144,10 @@ struct alignas(16) Ctrl {
     uint32_t ticket_emit;   // same, emit
     uint32_t gen;           // rounds released to the grid (persistent search kernel)
     uint32_t err;           // a CTA gave up waiting for a release
+    uint32_t fin_tail;      // fused path: blocks whose chain is final, queued so far
+    uint32_t fin_avail;     // fused path: queued blocks published to the idle warps
+    uint32_t ticket_f;      // fused path: CTAs out of the rounds
+    uint32_t pad_f;
     uint32_t active[16];    // blocks evaluated in each round (diagnostics)
     int64_t nb;             // blocks
     // sum over all blocks of d_r H_r at xb, fixed point; the rounds of the

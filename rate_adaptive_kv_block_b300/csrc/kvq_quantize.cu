@@ -16,6 +16,7 @@
 // (explicit round-to-nearest, so no multiply-add contraction can change a
 // code), and one SplitMix64 output gives both uniforms.
 #include "kvq_internal.cuh"
+#include "kvq_quant_core.cuh"
 
 namespace kvq {
 
@@ -24,33 +25,6 @@ constexpr int kQStages = 4;
 constexpr int kQMaxCols = 256;               // features per tile (at most)
 constexpr int kQMaxGroups = kQMaxCols / 8;   // blocks per tile (at most)
 constexpr uint32_t kQWaitLimit = 1u << 22;   // mbarrier polls before giving up
-
-// SplitMix64 output function (Steele, Lea, Flood 2014), written on the two
-// 32-bit halves (hi:lo) of the state so that each step is one funnel shift,
-// one xor or one 32-bit multiply-add: returns the output's high and low words.
-__device__ __forceinline__ void splitmix_mix(uint32_t lo, uint32_t hi, uint32_t &ohi,
-                                             uint32_t &olo) {
-    // z ^= z >> 30; z *= 0xBF58476D1CE4E5B9
-    lo ^= __funnelshift_r(lo, hi, 30);
-    hi ^= hi >> 30;
-    const uint32_t nlo0 = lo * 0x1CE4E5B9u;
-    const uint32_t nhi0 = __umulhi(lo, 0x1CE4E5B9u) + lo * 0xBF58476Du + hi * 0x1CE4E5B9u;
-    // z ^= z >> 27; z *= 0x94D049BB133111EB
-    const uint32_t nlo = nlo0 ^ __funnelshift_r(nlo0, nhi0, 27);
-    const uint32_t nhi = nhi0 ^ (nhi0 >> 27);
-    lo = nlo * 0x133111EBu;
-    hi = __umulhi(nlo, 0x133111EBu) + nlo * 0x94D049BBu + nhi * 0x133111EBu;
-    // z ^= z >> 31
-    olo = lo ^ __funnelshift_r(lo, hi, 31);
-    ohi = hi ^ (hi >> 31);
-}
-constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;
-
-__device__ __forceinline__ __half2 as_h2(uint32_t u) {
-    __half2 h;
-    memcpy(&h, &u, 4);
-    return h;
-}
 
 // ------------------------------------------------------------- mbarriers
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -148,7 +122,6 @@ quantize_kernel(const uint16_t *__restrict__ x, const float *__restrict__ codebo
             if (t < ntiles) issue_tile(g, t, x, codebook, qsm + s * g.stage_bytes, &bars[s]);
         }
     }
-    const float INF = __int_as_float(0x7f800000);
     const int upr = 1 << g.upr_log2;
     const int cu = tid & (upr - 1);
     const int row0 = tid >> g.upr_log2, rstep = kQThreads >> g.upr_log2;
@@ -173,14 +146,7 @@ quantize_kernel(const uint16_t *__restrict__ x, const float *__restrict__ codebo
             int k = 1;
 #pragma unroll
             for (int m = 0; m < 15; ++m) k += q[m] < top ? 1 : 0;
-            const float qj = q[j];
-            const float th = (j >= 1 && j <= k - 2) ? qj : INF;
-            tb.thr[b][j] = __floats2half2_rn(th, th);     // exact: levels are binary16 values
-            const float qn = q[j < 15 ? j + 1 : 15];
-            float ws = 0.f;
-            if (k <= 1) ws = INF;                         // k = 1: never move up
-            else if (j <= k - 2) ws = __fmul_rn(__fsub_rn(qn, qj), 5.9604644775390625e-8f);  // 2^-24
-            tb.qw[b][j] = make_float2(-qj, ws);
+            quant_table_entry(q, k, j, tb.thr[b][j], tb.qw[b][j]);
         }
         __syncthreads();
         // this thread's block: 15 thresholds in registers
@@ -196,45 +162,11 @@ quantize_kernel(const uint16_t *__restrict__ x, const float *__restrict__ codebo
         const int col = chunk * g.Dc + f0;                      // feature of the first entry
         const int64_t blk = (slab << g.bps_log2) + (col >> g.g_log2);
         uint8_t *cbase = codes + blk * hb + ((col & (g.G - 1)) >> 1);
-        uint64_t z = seed + ((index_base + (uint64_t)((slab * 32 + row0) * (int64_t)g.D + col)) / 2 + 1) * kGolden;
+        uint64_t z = quant_state(seed, index_base, (uint64_t)((slab * 32 + row0) * (int64_t)g.D + col));
         const uint64_t zstep = (uint64_t)(rstep * g.D / 2) * kGolden;
         for (int row = row0; row < 32; row += rstep, z += zstep) {
             const uint4 raw = *reinterpret_cast<const uint4 *>(buf + (row * g.Dc + f0) * 2);
-            const uint32_t xw0 = raw.x, xw1 = raw.y, xw2 = raw.z, xw3 = raw.w;
-            uint32_t packed = 0;
-            uint64_t zz = z;
-#pragma unroll
-            for (int pr = 0; pr < 4; ++pr) {
-                const __half2 X = as_h2(pr == 0 ? xw0 : pr == 1 ? xw1 : pr == 2 ? xw2 : xw3);
-                // interval index of both halves: 4-level binary search over
-                // T1..T15 (sorted, +inf padded); m* are 0xffff-per-half masks
-                const uint32_t m1 = __hge2_mask(X, as_h2(T[8]));
-                const uint32_t t2 = (T[12] & m1) | (T[4] & ~m1);
-                const uint32_t m2 = __hge2_mask(X, as_h2(t2));
-                const uint32_t a3 = (T[6] & m2) | (T[2] & ~m2), b3 = (T[14] & m2) | (T[10] & ~m2);
-                const uint32_t t3 = (b3 & m1) | (a3 & ~m1);
-                const uint32_t m3 = __hge2_mask(X, as_h2(t3));
-                const uint32_t a4 = (T[3] & m3) | (T[1] & ~m3), b4 = (T[7] & m3) | (T[5] & ~m3);
-                const uint32_t c4 = (T[11] & m3) | (T[9] & ~m3), d4 = (T[15] & m3) | (T[13] & ~m3);
-                const uint32_t lo4 = (b4 & m2) | (a4 & ~m2), hi4 = (d4 & m2) | (c4 & ~m2);
-                const uint32_t t4 = (hi4 & m1) | (lo4 & ~m1);
-                const uint32_t m4 = __hge2_mask(X, as_h2(t4));
-                const uint32_t idx = (m1 & 0x00080008u) | (m2 & 0x00040004u) | (m3 & 0x00020002u) |
-                                     (m4 & 0x00010001u);
-                const int i0 = (int)(idx & 15u), i1 = (int)(idx >> 16);
-                const float2 e0 = qw[i0], e1 = qw[i1];
-                uint32_t hhi, hlo;
-                splitmix_mix((uint32_t)zz, (uint32_t)(zz >> 32), hhi, hlo);
-                zz += kGolden;
-                const float2 xf = __half22float2(X);
-                const float2 r = __fadd2_rn(xf, make_float2(e0.x, e1.x));          // x - q_i
-                const float2 u = make_float2((float)(hhi >> 8), (float)(hlo >> 8));
-                const float2 tw = __fmul2_rn(u, make_float2(e0.y, e1.y));
-                const uint32_t c0 = (uint32_t)i0 + (tw.x < r.x ? 1u : 0u);
-                const uint32_t c1 = (uint32_t)i1 + (tw.y < r.y ? 1u : 0u);
-                packed |= (c0 | (c1 << 4)) << (8 * pr);
-            }
-            *reinterpret_cast<uint32_t *>(cbase + (int64_t)row * (g.G / 2)) = packed;
+            *reinterpret_cast<uint32_t *>(cbase + (int64_t)row * (g.G / 2)) = quant8(raw, T, qw, z);
         }
         __syncthreads();                         // every thread is done with this stage
         if (tid == 0) {

@@ -90,6 +90,9 @@ def lib():
         L.kvq_allocate.restype = C.c_int
         L.kvq_allocate.argtypes = [vp, _Layout, C.c_int, dbl, C.c_int, dbl, vp, vp, vp, vp,
                                    vp, vp, vp, vp, vp]
+        L.kvq_allocate_quantize.restype = C.c_int
+        L.kvq_allocate_quantize.argtypes = [vp, vp, _Layout, C.c_int, dbl, C.c_int, dbl, vp, vp,
+                                            vp, vp, vp, vp, vp, u64, u64, vp, vp, vp]
         L.kvq_allocate_static.restype = C.c_int
         L.kvq_allocate_static.argtypes = [vp, _Layout, C.c_int, dbl, C.c_int, dbl, vp, vp, vp,
                                           vp, vp, vp, vp, vp]
@@ -147,6 +150,17 @@ def kvq_allocate(stats, L: Layout, s: int, budget_bits: float, mode: int, eta: f
                               float(eta), _ptr(lam), _ptr(workspace), _ptr(codebook), _ptr(k),
                               _ptr(D_r), _ptr(H_r), _ptr(totals), _ptr(status),
                               _stream(stream)), "kvq_allocate")
+
+
+def kvq_allocate_quantize(stats, x, L: Layout, s: int, budget_bits: float, mode: int, eta: float,
+                          lam, workspace, codebook, k, D_r, H_r, totals, seed: int,
+                          index_base: int, codes, status, stream=None):
+    """kvq_allocate and kvq_quantize in one launch (same results)."""
+    _check(lib().kvq_allocate_quantize(_ptr(stats), _ptr(x), L.c(), int(s), float(budget_bits),
+                                       int(mode), float(eta), _ptr(lam), _ptr(workspace),
+                                       _ptr(codebook), _ptr(k), _ptr(D_r), _ptr(H_r),
+                                       _ptr(totals), int(seed), int(index_base), _ptr(codes),
+                                       _ptr(status), _stream(stream)), "kvq_allocate_quantize")
 
 
 def kvq_allocate_static(stats, L: Layout, s: int, budget_bits: float, mode: int, eta: float,
@@ -211,13 +225,19 @@ class Buffers:
 
 
 def quantize(x, L: Layout, budget_bits: float, s: int, seed: int = 0, index_base: int = 0,
-             mode: int = KVQ_BISECT40, eta: float = 0.0, buf: Buffers = None, stream=None):
+             mode: int = KVQ_BISECT40, eta: float = 0.0, buf: Buffers = None, stream=None,
+             fused: bool = False):
     """kvq_stats + kvq_allocate + kvq_quantize on x (a [S,T,D] float16 CUDA
-    tensor).  Returns the Buffers (codes, codebook, k, D_r, H_r, totals,
+    tensor); fused: kvq_allocate_quantize instead of the last two.  Returns the Buffers (codes, codebook, k, D_r, H_r, totals,
     lambda, statuses), all still on the device."""
     if buf is None:
         buf = Buffers(L, s, x.device)
     kvq_stats(x, L, buf.stats, buf.status_stats, stream=stream)
+    if fused:
+        kvq_allocate_quantize(buf.stats, x, L, s, budget_bits, mode, eta, buf.lam, buf.workspace,
+                              buf.codebook, buf.k, buf.D_r, buf.H_r, buf.totals, seed,
+                              index_base, buf.codes, buf.status, stream=stream)
+        return buf
     kvq_allocate(buf.stats, L, s, budget_bits, mode, eta, buf.lam, buf.workspace, buf.codebook,
                  buf.k, buf.D_r, buf.H_r, buf.totals, buf.status, stream=stream)
     kvq_quantize(x, L, buf.codebook, buf.k, seed, index_base, buf.codes, buf.status_quant,

@@ -258,3 +258,55 @@ def test_graph_capture_replays_the_eager_results():
         for key in ("codebook", "k", "D_r", "H_r", "totals", "lam", "status", "codes"):
             a, b = getattr(gbuf, key), getattr(ebuf, key)
             assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), key
+
+
+# ------------------------------------------- fused allocate + quantize
+
+FUSED_CASES = [
+    # name, T, S, s, budget index, mode
+    ("llama3_8b_layer", None, None, 16, 0, kvq.KVQ_BISECT40),    # the benchmark workload
+    ("k_head_small", None, None, 8, 0, kvq.KVQ_BISECT40),        # s < 16: general DP path
+    ("hadamard_groups", 1024, None, 16, 1, kvq.KVQ_BISECT40),    # 32-feature groups
+    ("full_model_cache", 2048, 32, 16, 0, kvq.KVQ_BISECT40),
+    ("decode_admission", None, 1024, 16, 0, kvq.KVQ_SUBGRADIENT),
+]
+
+
+@pytest.mark.parametrize("name,T,S,s,bi,mode", FUSED_CASES)
+def test_fused_allocate_quantize_equals_separate_calls(name, T, S, s, bi, mode):
+    """kvq_allocate_quantize gives exactly kvq_allocate + kvq_quantize."""
+    _need_gpu()
+    w = synth.workload(name, T=T, S=S)
+    xd = synth.make_torch(w, seed=41)
+    L = kvq.Layout(w.S, w.T, w.D, w.G)
+    B = w.budgets[bi] * w.entries
+    lam0 = 0.05 if mode == kvq.KVQ_SUBGRADIENT else 0.0
+    eta = 1e-6 if mode == kvq.KVQ_SUBGRADIENT else 0.0
+    ref, got = kvq.Buffers(L, s), kvq.Buffers(L, s)
+    for b in (ref, got):
+        b.lam.fill_(lam0)
+        b.codes.fill_(0xAB)
+    kvq.quantize(xd, L, B, s, seed=9, index_base=2 * 77, mode=mode, eta=eta, buf=ref)
+    kvq.quantize(xd, L, B, s, seed=9, index_base=2 * 77, mode=mode, eta=eta, buf=got, fused=True)
+    torch.cuda.synchronize()
+    assert int(got.status.item()) == 0
+    for key in ("codebook", "k", "D_r", "H_r", "totals", "lam", "status", "codes"):
+        a, b = getattr(ref, key), getattr(got, key)
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), key
+
+
+def test_fused_edge_layouts():
+    """Empty layout, lambda = 0 (large budget) and a layout of a few blocks."""
+    _need_gpu()
+    for S, T, D, G, bpe in [(0, 64, 128, 128, 2.0), (2, 64, 128, 128, 20.0), (1, 32, 64, 8, 1.0),
+                           (3, 96, 256, 16, 2.5)]:
+        L = kvq.Layout(S, T, D, G)
+        x = torch.randn((S, T, D), device="cuda").to(torch.float16)
+        ref, got = kvq.Buffers(L, 16), kvq.Buffers(L, 16)
+        B = bpe * S * T * D
+        kvq.quantize(x, L, B, 16, seed=3, buf=ref)
+        kvq.quantize(x, L, B, 16, seed=3, buf=got, fused=True)
+        torch.cuda.synchronize()
+        for key in ("codebook", "k", "D_r", "H_r", "totals", "lam", "status", "codes"):
+            a, b = getattr(ref, key), getattr(got, key)
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (S, T, D, G, key)
