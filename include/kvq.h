@@ -152,8 +152,8 @@ int kvq_allocate(const void *stats, kvq_layout L, int s, double budget_bits,
  * The scratch is a fixed array of KVQ_STATIC_WORKSPACE_BYTES (8 MiB) in the
  * library's device memory, present on every GPU that loads the library until
  * the process exits.  It holds layouts whose kvq_workspace_bytes(L, s) is at
- * most that size (about 29 700 blocks: 7.6 million entries with group 8,
- * 121 million with group 128); larger layouts return KVQ_ERR_TOO_LARGE without
+ * most that size (about 29 400 blocks: 7.5 million entries with group 8,
+ * 120 million with group 128); larger layouts return KVQ_ERR_TOO_LARGE without
  * launching anything.
  * Nothing is allocated: the first call on each device looks up the array's
  * address once (cudaGetSymbolAddress) -- make that first call outside any

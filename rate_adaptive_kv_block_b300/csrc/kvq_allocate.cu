@@ -60,7 +60,7 @@ struct Workspace {
     uint32_t *mask_hi;    // [nblk]       chain at xb
     int32_t *evr;         // [nblk]       round that last evaluated the block
     int32_t *list;        // [2][nblk]    candidate lists (ping-pong)
-    double *epartial;     // [grid]       per-CTA sums of D_r (unused)
+    double *epartial;     // [nblk / 32]  D_r summed over each 32 consecutive blocks
     int32_t *fin;         // [nblk]       fused path: blocks in the order their chain became final
     uint8_t *fflag;       // [nblk]       fused path: 1 once queued
 };
@@ -75,7 +75,7 @@ size_t workspace_bytes(int64_t nb, int s) {
     b += 3 * align_up((size_t)nb * sizeof(float));
     b += align_up((size_t)nb * sizeof(int32_t));
     b += align_up((size_t)nb * 2 * sizeof(int32_t));
-    b += align_up((size_t)(nb < kMaxGrid ? nb : kMaxGrid) * sizeof(double));
+    b += align_up((size_t)((nb + 31) / 32) * sizeof(double));
     b += align_up((size_t)nb * sizeof(int32_t));
     b += align_up((size_t)nb);
     return b;
@@ -101,7 +101,7 @@ static Workspace carve(void *base, int64_t nb) {
     w.list = reinterpret_cast<int32_t *>(p);
     p += align_up((size_t)nb * 2 * sizeof(int32_t));
     w.epartial = reinterpret_cast<double *>(p);
-    p += align_up((size_t)(nb < kMaxGrid ? nb : kMaxGrid) * sizeof(double));
+    p += align_up((size_t)((nb + 31) / 32) * sizeof(double));
     w.fin = reinterpret_cast<int32_t *>(p);
     p += align_up((size_t)nb * sizeof(int32_t));
     w.fflag = reinterpret_cast<uint8_t *>(p);
@@ -1034,13 +1034,14 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                 if (L == 0) st_release_u32(&ctrl->gen, 2u * (uint32_t)iter + 1u);
                 // second publication: the walk and the next round's probes
                 if (walk_on) {
-                    const int go = search_walk(st);
+                    const SearchWindow win = search_window_of(st);   // the walk keeps it
+                    const int go = search_walk_w(st, win);
                     __syncwarp();
                     if (go) {
                         __shared__ double sProbe[kSearchProbes];
                         sProbe[L] = search_first_unknown(st);
                         __syncwarp();
-                        search_path(st, L, sProbe);
+                        search_path_w(st, win, L, sProbe);
                         __syncwarp();
                         S.probe[L] = sProbe[L];
                     }
@@ -1098,55 +1099,66 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                       (uint64_t)blockIdx.x * W + w, total_warps, qj, qpart);
     } else {
         // emit: a thread per block, so every block's loads are in flight at
-        // once; blocks dealt round-robin over the CTAs (consecutive CTAs,
-        // consecutive blocks), so every SM takes part
-        for (int64_t b = (int64_t)blockIdx.x + (int64_t)gridDim.x * threadIdx.x; b < nb;
-             b += (int64_t)gridDim.x * blockDim.x) {
-            const float *tb = tables + b * kRecFloats + kRecTbl;
-            // every load that does not depend on the chosen chain, at once
-            const int32_t ev = __ldcg(&evr[b]);
-            const int xp = xb_probe >= 0 ? xb_probe : 0;
-            const uint32_t m_last = __ldcg(&masks[b * 32 + xp]);
-            const float r_last = __ldcg(&rates[b * 32 + xp]);
-            const uint32_t m_hi = __ldcg(&mask_hi[b]);
-            const float r_hi = __ldcg(&rate_hi[b]);
-            float qv[17];
+        // once; a warp takes 32 consecutive blocks (chunk g), the chunks dealt
+        // round-robin over the CTAs so that every SM takes part; the warp then
+        // sums its blocks' D_r in a fixed shuffle tree (the chunk sum)
+        const int64_t nch = (nb + 31) / 32;
+        for (int64_t g = (int64_t)blockIdx.x + (int64_t)gridDim.x * w; g < nch;
+             g += (int64_t)gridDim.x * W) {
+            const int64_t b = g * 32 + lane;
+            float dv = 0.f;
+            if (b < nb) {
+                const float *tb = tables + b * kRecFloats + kRecTbl;
+                // every load that does not depend on the chosen chain, at once
+                const int32_t ev = __ldcg(&evr[b]);
+                const int xp = xb_probe >= 0 ? xb_probe : 0;
+                const uint32_t m_last = __ldcg(&masks[b * 32 + xp]);
+                const float r_last = __ldcg(&rates[b * 32 + xp]);
+                const uint32_t m_hi = __ldcg(&mask_hi[b]);
+                const float r_hi = __ldcg(&rate_hi[b]);
+                float qv[17];
 #pragma unroll
-            for (int t = 0; t < 17; ++t) qv[t] = tb[kTblC + t];
-            const int d = __float_as_int(tb[kTblHdr + 1]);
-            const bool from_last = xb_probe >= 0 && ev == last_round;
-            uint32_t mask = from_last ? m_last : m_hi;
-            const float rate = from_last ? r_last : r_hi;
-            mask &= 0x1ffffu;
-            if (mask == 0u) mask = 1u;
-            const int k = min(__popc(mask), 16);
-            // the chain's levels in slot order, and the sum of its interval
-            // distortions (slot by slot, in order); table addresses come from
-            // the mask alone, so the loads issue together
-            float dv = 0.f, top = qv[0];
-            int prev = 0;
+                for (int t = 0; t < 17; ++t) qv[t] = tb[kTblC + t];
+                const int d = __float_as_int(tb[kTblHdr + 1]);
+                const bool from_last = xb_probe >= 0 && ev == last_round;
+                uint32_t mask = from_last ? m_last : m_hi;
+                const float rate = from_last ? r_last : r_hi;
+                mask &= 0x1ffffu;
+                if (mask == 0u) mask = 1u;
+                const int k = min(__popc(mask), 16);
+                // the chain's levels in slot order, and the sum of its interval
+                // distortions (slot by slot, in order); table addresses come from
+                // the mask alone, so the loads issue together
+                float top = qv[0];
+                int prev = 0;
 #pragma unroll
-            for (int t = 0; t < 17; ++t) {
-                const bool in = (mask >> t) & 1u;
-                const bool link = in && t > 0;
-                const float dd = tb[kTblD + (link ? dp_off(prev) + t - prev - 1 : 0)];
-                if (link) dv += dd;
-                const int pos = __popc(mask & ((1u << t) - 1u));
-                if (in && pos < 16) codebook[b * 16 + pos] = qv[t];
-                if (in) {
-                    top = qv[t];
-                    prev = t;
+                for (int t = 0; t < 17; ++t) {
+                    const bool in = (mask >> t) & 1u;
+                    const bool link = in && t > 0;
+                    const float dd = tb[kTblD + (link ? dp_off(prev) + t - prev - 1 : 0)];
+                    if (link) dv += dd;
+                    const int pos = __popc(mask & ((1u << t) - 1u));
+                    if (in && pos < 16) codebook[b * 16 + pos] = qv[t];
+                    if (in) {
+                        top = qv[t];
+                        prev = t;
+                    }
                 }
+                for (int t = k; t < 16; ++t) codebook[b * 16 + t] = top;
+                kout[b] = (uint8_t)k;
+                Dr[b] = dv;
+                Hr[b] = rate / (float)d;
             }
-            for (int t = k; t < 16; ++t) codebook[b * 16 + t] = top;
-            kout[b] = (uint8_t)k;
-            Dr[b] = dv;
-            Hr[b] = rate / (float)d;
+            double t = (double)dv;          // lanes past the last block add 0
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_down_sync(0xffffffffu, t, o);
+            if (lane == 0) epartial[g] = t;
         }
     }
-    // ---- totals, by the last CTA to finish: D summed over the blocks in
-    // index order, in a fixed pattern (contiguous chunks of four interleaved
-    // accumulators, then a fixed tree)
+    // ---- totals, by the last CTA to finish: D = the chunk sums (32
+    // consecutive blocks each, a fixed shuffle tree) added in index order in a
+    // fixed pattern (contiguous runs of four interleaved accumulators, then a
+    // fixed tree)
     __syncthreads();
     if (threadIdx.x == 0) {
         const unsigned t = atom_add_acq_rel_u32(&ctrl->ticket_emit, 1u);   // orders this CTA's D_r
@@ -1154,24 +1166,46 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
     }
     __syncthreads();
     if (!is_last) return;
+    const int64_t nch = (nb + 31) / 32;
+    if constexpr (QUANT) {
+        // the fused path wrote D_r block by block: the chunk sums from them,
+        // in the same tree (8 chunks per warp at a time, loads first)
+        for (int64_t g0 = (int64_t)w * 8; g0 < nch; g0 += (int64_t)W * 8) {
+            double v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t b = (g0 + u) * 32 + lane;
+                v[u] = (g0 + u < nch && b < nb) ? (double)__ldcg(&Dr[b]) : 0.0;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] += __shfl_down_sync(0xffffffffu, v[u], o);
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (g0 + u < nch) epartial[g0 + u] = v[u];
+            }
+        }
+        __syncthreads();
+    }
     __shared__ double sPart[W * 32];
     {
-        const int64_t chunk = (nb + W * 32 - 1) / (W * 32);
+        const int64_t chunk = (nch + W * 32 - 1) / (W * 32);
         const int64_t b0 = (int64_t)threadIdx.x * chunk;
-        const int64_t b1 = b0 + chunk < nb ? b0 + chunk : nb;
+        const int64_t b1 = b0 + chunk < nch ? b0 + chunk : nch;
+        // chunk sum b0 + 4m + j goes to accumulator j, in order of m; the
+        // loads of 32 of them are issued before their adds
         double acc[4] = {0.0, 0.0, 0.0, 0.0};
-        int64_t i = b0;
-        for (; i + 4 <= b1; i += 4) {
-            const float d0 = __ldcg(&Dr[i]), d1 = __ldcg(&Dr[i + 1]);
-            const float d2 = __ldcg(&Dr[i + 2]), d3 = __ldcg(&Dr[i + 3]);
-            acc[0] += (double)d0;
-            acc[1] += (double)d1;
-            acc[2] += (double)d2;
-            acc[3] += (double)d3;
+        for (int64_t i = b0; i < b1; i += 32) {
+            double v[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) v[u] = i + u < b1 ? __ldcg(&epartial[i + u]) : 0.0;
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                if (i + u < b1) acc[u & 3] += v[u];
         }
-        if (i < b1) acc[0] += (double)__ldcg(&Dr[i]);
-        if (i + 1 < b1) acc[1] += (double)__ldcg(&Dr[i + 1]);
-        if (i + 2 < b1) acc[2] += (double)__ldcg(&Dr[i + 2]);
         sPart[threadIdx.x] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     }
     __syncthreads();

@@ -41,6 +41,17 @@
 #endif
 #endif
 
+// Out of line: a rarely taken branch whose arithmetic (binary64, on a GPU
+// with a slow double-precision unit) must not be evaluated speculatively on
+// the common path.
+#ifndef KVQ_COLD
+#ifdef __CUDA_ARCH__
+#define KVQ_COLD __noinline__
+#else
+#define KVQ_COLD __attribute__((noinline))
+#endif
+#endif
+
 namespace kvq {
 
 constexpr int kSearchProbes = 32;
@@ -96,13 +107,20 @@ KVQ_HD inline uint64_t okey(double x) {
 }
 
 // 0.5 * (a + b), bit for bit as binary64 arithmetic computes it, for finite
-// a, b >= 0: halving is exact for normal numbers and commutes with rounding,
-// so RN(a + b) / 2 = RN(a/2 + b/2); each half is an exponent decrement
-// (integer) and one binary64 add remains on the critical path instead of an
-// add and a multiply.  Zero, subnormal or near-subnormal operands take the
-// expression itself.
+// a, b >= 0.  Same exponent field (the late steps of every bisection): the
+// raw bits are a fixed-point significand, so the midpoint is their integer
+// mean rounded half to even.  Otherwise halving is exact for normal numbers
+// and commutes with rounding, so RN(a + b) / 2 = RN(a/2 + b/2); each half is
+// an exponent decrement (integer) and one binary64 add remains instead of an
+// add and a multiply.  Zero or near-subnormal operands in different binades
+// take the expression itself.
+KVQ_HD inline uint64_t mean_bits_same_exponent(uint64_t ua, uint64_t ub) {
+    const uint64_t t = ua + ub, h = t >> 1;   // no overflow: both below 2^63
+    return h + (t & h & 1u);                  // a tie goes to the even neighbour
+}
 KVQ_HD inline double half_sum(double a, double b) {
     const uint64_t ua = dbits(a), ub = dbits(b);
+    if ((ua >> 52) == (ub >> 52) && (ua >> 52) < 2047) return dfrom(mean_bits_same_exponent(ua, ub));
     const uint32_t ea = (uint32_t)(ua >> 52), eb = (uint32_t)(ub >> 52);   // sign bit 0
     const bool na = ea >= 3 && ea <= 2046, nbb = eb >= 3 && eb <= 2046;
     if ((na || ua == 0) && (nbb || ub == 0) && (na || nbb)) {
@@ -111,6 +129,50 @@ KVQ_HD inline double half_sum(double a, double b) {
         return ah + bh;
     }
     return 0.5 * (a + b);
+}
+
+// Raw bits of the smallest binary64 value that rounds (to nearest, ties to
+// even) to the binary32 value f, for f > 0 (+inf included), and of the
+// largest one, for finite f >= 0: the midpoints between f and its neighbours,
+// exact in binary64, or the next double inward when the tie goes to the
+// neighbour.  For a normal f the binary64 bits of f are its binary32 bits
+// shifted left by 29 with the exponent rebiased, a binary32 half-ulp is 2^28
+// binary64 ulps of the same binade (of the binade below, for the midpoint
+// under a power of two), and +inf continues the pattern (2^128 - 2^103 is the
+// smallest value that overflows); subnormal neighbours take the arithmetic
+// itself.
+KVQ_HD inline uint64_t f32_as_f64_bits(uint32_t fb) {
+    return ((uint64_t)fb << 29) + (896ull << 52);   // exponent bias 1023 - 127
+}
+KVQ_HD inline KVQ_COLD uint64_t f32_low_bits_sub(float f) {
+    uint32_t fb;
+    memcpy(&fb, &f, 4);
+    const uint32_t pb = fb - 1u;
+    float p;
+    memcpy(&p, &pb, 4);
+    const double m = ((double)p + (double)f) * 0.5;
+    return (fb & 1u) ? dbits(m) + 1u : dbits(m);
+}
+KVQ_HD inline KVQ_COLD uint64_t f32_high_bits_sub(float f) {
+    uint32_t fb;
+    memcpy(&fb, &f, 4);
+    const uint32_t nb = fb + 1u;
+    float n;
+    memcpy(&n, &nb, 4);
+    const double m = ((double)f + (double)n) * 0.5;
+    return (fb & 1u) ? dbits(m) - 1u : dbits(m);
+}
+KVQ_HD inline uint64_t f32_low_bits(float f) {
+    uint32_t fb;
+    memcpy(&fb, &f, 4);
+    if (fb > 0x00800000u) return f32_as_f64_bits(fb) - (1ull << 28) + (fb & 1u);
+    return f32_low_bits_sub(f);
+}
+KVQ_HD inline uint64_t f32_high_bits(float f) {
+    uint32_t fb;
+    memcpy(&fb, &f, 4);
+    if (fb >= 0x00800000u) return f32_as_f64_bits(fb) + (1ull << 28) - (fb & 1u);
+    return f32_high_bits_sub(f);
 }
 
 // x * 2^t for x = 0 or normal x > 0 whose result stays normal (exponent
@@ -167,11 +229,17 @@ KVQ_HD inline double search_grid(double hi0, int k) {
     return (k & 1) ? pow2_scale(hi0 * odd, -(3 * k - 1) / 2) : pow2_scale(hi0, -(3 * k) / 2);
 }
 
-// Fine grid of round 0 around an estimate: est * 1.35^((2k - 27) / 27),
-// k = 0..27, the factor in single precision (the grid only places probes).
+// Fine grid of round 0 around an estimate, k = 0..27: 14 probes on each side
+// of est, the j-th out (j = 0..13) at est * 2^(+-c (g^(j+1) - 1) / (g - 1)),
+// c = 0.0215, g = 1.25: cells of 1.5 % next to the estimate, growing by a
+// quarter per probe out to a factor 3.7 either way, so that the grid spans
+// the pilot's whole bracket (a factor 2^1.5) wherever the estimate falls in
+// it, and the window after round 0 is narrow when the estimate is good.  In
+// single precision (the grid only places probes).
 KVQ_HD inline double search_fine(double est, int k) {
-    const float e = (float)(2 * k - 27) * (0.43295940727610627f / 27.0f);   // log2(1.35) / 27
-    return est * (double)exp2f(e);
+    const int j = k < 14 ? 13 - k : k - 14;
+    const float off = 0.0215f * (exp2f((float)(j + 1) * 0.32192809f) - 1.0f) * 4.0f;   // log2(1.25)
+    return est * (double)exp2f(k < 14 ? -off : off);
 }
 
 // lambda evaluated by probe p this round
@@ -193,11 +261,16 @@ KVQ_HD inline double search_probe(const SearchState &s, int p) {
 // keys of both ends, and, when R depends on lambda only through its binary32
 // rounding (the GPU evaluates the DP at float(lambda)), the binary32 values
 // of both ends: a midpoint that rounds to float(xb) is feasible, one that
-// rounds to float(xa) is not.
+// rounds to float(xa) is not.  For positive midpoints the same tests are
+// integer comparisons of raw bits: mid >= xb (rxb), mid <= xa (rxa), and,
+// inside the window, float(mid) == float(xb) iff mid >= the smallest double
+// rounding to float(xb) (lb), float(mid) == float(xa) iff mid <= the largest
+// double rounding to float(xa) (ha).
 struct SearchWindow {
     uint64_t kxa, kxb;
     float fxa, fxb;
     int f32;
+    uint64_t rxa, rxb, lb, ha;
 };
 KVQ_HD inline SearchWindow search_window_of(const SearchState &s) {
     SearchWindow w;
@@ -206,6 +279,15 @@ KVQ_HD inline SearchWindow search_window_of(const SearchState &s) {
     w.fxa = (float)s.xa;
     w.fxb = (float)s.xb;
     w.f32 = s.f32_lambda;
+    w.rxb = w.kxb ^ (1ull << 63);                               // xb >= 0 (or +inf)
+    w.rxa = (w.kxa >> 63) ? (w.kxa ^ (1ull << 63)) : 0ull;      // xa < 0: none
+    w.lb = ~0ull;                                               // never reached
+    w.ha = 0ull;
+    if (w.f32) {
+        if (s.xb >= 0.0) w.lb = w.fxb > 0.f ? f32_low_bits(w.fxb) : 0ull;
+        if (s.xa >= 0.0)                                        // -0 compares equal to +0
+            w.ha = w.fxa < INFINITY ? f32_high_bits(w.fxa == 0.f ? 0.f : w.fxa) : dbits(INFINITY);
+    }
     return w;
 }
 // P(mid) if it follows from the window, else -1
@@ -228,32 +310,57 @@ KVQ_HD inline int search_known(const SearchState &s, double mid) {
 // known from the window; returns the depth of the first unknown midpoint
 // (kSearchSteps if none), with lo, hi the interval there.  Fast path (every
 // practical case): lo = 0 with hi far from the subnormal range, or lo normal
-// -- then every midpoint is normal, its half is an exponent decrement, and
-// for positive values order keys compare as raw bits.  Elsewhere the same
-// steps with half_sum and order keys.
-KVQ_HD inline int walk_known(double &lo, double &hi, int step, const SearchWindow &w) {
-    const uint64_t ul = dbits(lo), uh = dbits(hi);
+// -- then every midpoint is a positive normal number, computed on raw bits
+// (lo = 0: an exponent decrement; same exponent: the rounded integer mean;
+// else one binary64 add of the halves), and the window tests are the raw-bit
+// comparisons above.  Elsewhere the same steps with half_sum and order keys.
+KVQ_HD inline bool walk_fast(uint64_t ul, uint64_t uh) {
     const uint32_t el = (uint32_t)(ul >> 52), eh = (uint32_t)(uh >> 52);
-    const bool fast = eh <= 2046 && (ul >> 63) == 0 && ((ul == 0 && eh >= 48) || el >= 3);
-    if (fast) {
-        // raw-bit thresholds for positive midpoints: mid >= xb, mid <= xa
-        const uint64_t rxb = w.kxb ^ (1ull << 63);           // xb >= 0 (or +inf)
-        const uint64_t rxa = (w.kxa >> 63) ? (w.kxa ^ (1ull << 63)) : 0ull;   // xa < 0: none
-        double lh = ul ? dfrom(ul - (1ull << 52)) : 0.0;
-        double hh = dfrom(uh - (1ull << 52));
-        while (step < kSearchSteps) {
-            const double mid = lh + hh;
-            const uint64_t um = dbits(mid);
-            int k;
-            if (um >= rxb) k = 1;
-            else if (um <= rxa) k = 0;
-            else if (w.f32 && (float)mid == w.fxb) k = 1;
-            else if (w.f32 && (float)mid == w.fxa) k = 0;
-            else break;
-            const double mh = dfrom(um - (1ull << 52));
-            if (k) { hi = mid; hh = mh; } else { lo = mid; lh = mh; }
-            ++step;
+    return eh <= 2046 && (ul >> 63) == 0 && ((ul == 0 && eh >= 48) || el >= 3);
+}
+// The midpoint's raw bits on the fast path.
+KVQ_HD inline KVQ_COLD uint64_t mid_bits_halves(uint64_t ul, uint64_t uh) {
+    return dbits(dfrom(ul - (1ull << 52)) + dfrom(uh - (1ull << 52)));
+}
+KVQ_HD inline uint64_t mid_bits_fast(uint64_t ul, uint64_t uh) {
+    if (ul == 0) return uh - (1ull << 52);
+    if ((ul ^ uh) >> 52 == 0) return mean_bits_same_exponent(ul, uh);
+    return mid_bits_halves(ul, uh);
+}
+KVQ_HD inline bool window_known(uint64_t um, const SearchWindow &w, bool &k) {
+    const bool f1 = um >= w.rxb, f0 = um <= w.rxa, g1 = um >= w.lb, g0 = um <= w.ha;
+    k = f1 || (!f0 && g1);
+    return f1 || f0 || g1 || g0;
+}
+KVQ_HD inline int walk_known(double &lo, double &hi, int step, const SearchWindow &w) {
+    uint64_t ul = dbits(lo), uh = dbits(hi);
+    if (walk_fast(ul, uh)) {
+        // three phases, each a loop without inner branches: lo = 0 (the
+        // midpoint halves hi), lo and hi in different binades (one add of
+        // the halves), the same binade (integer mean; it stays so)
+        bool k = false;
+        for (; step < kSearchSteps && ul == 0; ++step) {
+            const uint64_t um = uh - (1ull << 52);
+            if (!window_known(um, w, k)) goto done;
+            ul = k ? ul : um;
+            uh = k ? um : uh;
         }
+        for (; step < kSearchSteps && ((ul ^ uh) >> 52) != 0; ++step) {
+            const uint64_t um = mid_bits_halves(ul, uh);
+            if (!window_known(um, w, k)) goto done;
+            ul = k ? ul : um;
+            uh = k ? um : uh;
+        }
+#pragma unroll 4
+        for (; step < kSearchSteps; ++step) {
+            const uint64_t um = mean_bits_same_exponent(ul, uh);
+            if (!window_known(um, w, k)) goto done;
+            ul = k ? ul : um;
+            uh = k ? um : uh;
+        }
+    done:
+        lo = dfrom(ul);
+        hi = dfrom(uh);
         return step;
     }
     while (step < kSearchSteps) {
@@ -331,9 +438,10 @@ KVQ_HD inline int search_decide(SearchState &s, const long long *R, long long Bf
 }
 
 // The walk: the bisection steps the window decides.  Returns 1 if probes
-// must be generated (phase stays Walk), 0 when the 40 steps are done.
-KVQ_HD inline int search_walk(SearchState &s) {
-    const SearchWindow win = search_window_of(s);
+// must be generated (phase stays Walk), 0 when the 40 steps are done.  The
+// window is the one search_window_of gives for s (the walk does not change
+// it).
+KVQ_HD inline int search_walk_w(SearchState &s, const SearchWindow &win) {
     s.step = walk_known(s.lo, s.hi, s.step, win);
     if (s.step >= kSearchSteps) {
         s.lambda = s.hi;
@@ -343,6 +451,7 @@ KVQ_HD inline int search_walk(SearchState &s) {
     s.nprobe = kSearchProbes - 1;
     return 1;
 }
+KVQ_HD inline int search_walk(SearchState &s) { return search_walk_w(s, search_window_of(s)); }
 
 // Bracket decisions and the walk.  Returns 1 if probes must be generated.
 KVQ_HD inline int search_advance(SearchState &s, const long long *R, long long Bfx) {
@@ -353,7 +462,8 @@ KVQ_HD inline int search_advance(SearchState &s, const long long *R, long long B
 KVQ_HD inline double search_first_unknown(const SearchState &s) { return half_sum(s.lo, s.hi); }
 
 // Path of lane L: writes the unknown midpoints it meets into probe[id].
-KVQ_HD inline void search_path(const SearchState &s, int L, double *probe) {
+// Generic form (half_sum and order keys), for any bracket.
+KVQ_HD inline void search_path_generic(const SearchState &s, int L, double *probe) {
     const SearchWindow win = search_window_of(s);
     double a = s.lo, b = s.hi;
     int dep = s.step;
@@ -367,6 +477,41 @@ KVQ_HD inline void search_path(const SearchState &s, int L, double *probe) {
         if (k) b = mid; else a = mid;
         ++dep;
     }
+}
+
+// Path of lane L (see search_path_generic), on the walk's fast path; `win`
+// is search_window_of(s).
+KVQ_HD inline void search_path_w(const SearchState &s, const SearchWindow &win, int L,
+                                 double *probe) {
+    uint64_t ul = dbits(s.lo), uh = dbits(s.hi);
+    if (walk_fast(ul, uh)) {
+        // the same steps on raw bits (see walk_known), the loop bodies
+        // without branches so that the lanes of a warp stay converged: while
+        // lo = 0 or lo and hi lie in different binades, then (the usual
+        // case, and it stays so) in one binade
+        int u = 0, pre = 0, dep = s.step;
+        auto take = [&](uint64_t um) {
+            bool k;
+            const bool rec = !window_known(um, win, k);
+            const int bit = (L >> (4 - u)) & 1;             // 1: take the infeasible branch
+            const int id = (1 << u) - 1 + pre;
+            if (rec) probe[id] = dfrom(um);
+            k = rec ? bit == 0 : k;
+            pre = rec ? 2 * pre + bit : pre;
+            u += rec ? 1 : 0;
+            ul = k ? ul : um;
+            uh = k ? um : uh;
+        };
+        for (; dep < kSearchSteps && u < 5 && (ul == 0 || ((ul ^ uh) >> 52) != 0); ++dep)
+            take(mid_bits_fast(ul, uh));
+#pragma unroll 4
+        for (; dep < kSearchSteps && u < 5; ++dep) take(mean_bits_same_exponent(ul, uh));
+        return;
+    }
+    search_path_generic(s, L, probe);
+}
+KVQ_HD inline void search_path(const SearchState &s, int L, double *probe) {
+    search_path_w(s, search_window_of(s), L, probe);
 }
 
 // Pilot round: estimate where R crosses B from the sample's rates (scaled to

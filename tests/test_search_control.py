@@ -4,6 +4,7 @@ returns the same lambda as the sequential bisection, bit for bit, whatever the
 breakpoints; and it needs far fewer rounds of evaluations than 40.  Its
 integer helpers round and compare exactly as binary64 arithmetic does."""
 import ctypes as C
+import math
 import os
 import random
 import struct
@@ -40,6 +41,70 @@ extern "C" long kvqs_okey_check(const double *a, const double *b, long n) {
     return bad;
 }
 extern "C" double kvqs_pow2_scale(double x, int t) { return kvq::pow2_scale(x, t); }
+// the walk and the probe paths against the definition: 0.5 (lo + hi) and
+// comparisons of doubles (and of their binary32 roundings); returns the
+// number of mismatching states
+static int ref_known(const kvq::SearchState &s, double m) {
+    if (m >= s.xb) return 1;
+    if (m <= s.xa) return 0;
+    if (s.f32_lambda) {
+        if ((float)m == (float)s.xb) return 1;
+        if ((float)m == (float)s.xa) return 0;
+    }
+    return -1;
+}
+extern "C" long kvqs_path_check(const double *st, long n) {
+    long bad = 0;
+    for (long i = 0; i < n; ++i) {
+        kvq::SearchState s;
+        kvq::search_init(s);
+        s.lo = st[5 * i]; s.hi = st[5 * i + 1]; s.xa = st[5 * i + 2]; s.xb = st[5 * i + 3];
+        s.step = 0;
+        s.f32_lambda = st[5 * i + 4] != 0.0;
+        // the walk
+        double lo = s.lo, hi = s.hi;
+        int dep = 0;
+        while (dep < kvq::kSearchSteps) {
+            const double m = 0.5 * (lo + hi);
+            const int k = ref_known(s, m);
+            if (k < 0) break;
+            if (k) hi = m; else lo = m;
+            ++dep;
+        }
+        kvq::SearchState w = s;
+        const int go = kvq::search_walk(w);
+        if (w.step != dep || w.lo != lo || w.hi != hi || go != (dep < kvq::kSearchSteps)) { ++bad; continue; }
+        if (!go) continue;
+        // every lane's path
+        double want[32], got[32];
+        for (int p = 0; p < 32; ++p) want[p] = got[p] = -7.0;
+        for (int L = 0; L < 32; ++L) {
+            double a = lo, b = hi;
+            int u = 0, pre = 0;
+            for (int d = dep; d < kvq::kSearchSteps && u < 5; ++d) {
+                const double m = 0.5 * (a + b);
+                int k = ref_known(s, m);
+                if (k < 0) {
+                    want[(1 << u) - 1 + pre] = m;
+                    k = ((L >> (4 - u)) & 1) == 0;
+                    pre = 2 * pre + (k ? 0 : 1);
+                    ++u;
+                }
+                if (k) b = m; else a = m;
+            }
+            kvq::search_path(w, L, got);
+        }
+        for (int p = 0; p < 32; ++p) if (kvq::dbits(want[p]) != kvq::dbits(got[p])) { ++bad; break; }
+    }
+    return bad;
+}
+extern "C" void kvqs_f32_bounds(const float *f, long n, unsigned long long *lo,
+                                unsigned long long *hi) {
+    for (long i = 0; i < n; ++i) {
+        lo[i] = f[i] > 0.f ? kvq::f32_low_bits(f[i]) : 0ull;
+        hi[i] = f[i] < INFINITY ? kvq::f32_high_bits(f[i]) : 0ull;
+    }
+}
 extern "C" long long kvqs_budget_fx(double B) { return kvq::budget_fx(B); }
 static double Rfun(double lam, int nbp, const double *bl, const double *br, double R0) {
     double r = R0;
@@ -92,6 +157,10 @@ def lib():
     L.kvqs_okey_check.argtypes = [C.c_void_p, C.c_void_p, C.c_long]
     L.kvqs_pow2_scale.restype = C.c_double
     L.kvqs_pow2_scale.argtypes = [C.c_double, C.c_int]
+    L.kvqs_path_check.restype = C.c_long
+    L.kvqs_path_check.argtypes = [C.c_void_p, C.c_long]
+    L.kvqs_f32_bounds.restype = None
+    L.kvqs_f32_bounds.argtypes = [C.c_void_p, C.c_long, C.c_void_p, C.c_void_p]
     L.kvqs_budget_fx.restype = C.c_longlong
     L.kvqs_budget_fx.argtypes = [C.c_double]
     L.kvqs_run.restype = C.c_int
@@ -307,3 +376,63 @@ def test_pow2_scale_and_budget_fixed_point(lib):
         # R <= B  iff  R_fx <= floor(B 2^20), for integer R_fx
         for R in (fxB - 1, fxB, fxB + 1):
             assert (R / 2 ** 20 <= B) == (R <= fxB)
+
+
+def test_binary32_rounding_bounds(lib):
+    """The raw-bit bounds of the walk's binary32 rule: the smallest double that
+    rounds to f rounds to f and its predecessor does not; the largest one
+    rounds to f and its successor does not (ties to even on both sides,
+    subnormals, zero, the largest finite value and +inf included)."""
+    rng = np.random.default_rng(6)
+    bits = rng.integers(0, 0x7F800000, 200000, dtype=np.uint32)
+    bits[:8] = [0, 1, 2, 3, 0x007FFFFF, 0x00800000, 0x7F7FFFFF, 0x3F800000]
+    bits[8:4096] = (bits[8:4096] & 0x7F800000) | rng.integers(0, 2, 4088).astype(np.uint32)
+    f = np.concatenate([bits.view(np.float32), np.array([np.inf], dtype=np.float32)])
+    lo = np.zeros(len(f), dtype=np.uint64)
+    hi = np.zeros(len(f), dtype=np.uint64)
+    lib.kvqs_f32_bounds(f.ctypes.data, len(f), lo.ctypes.data, hi.ctypes.data)
+    to32 = lambda u: u.view(np.float64).astype(np.float32)
+    with np.errstate(over="ignore"):
+        pos = f > 0
+        assert np.array_equal(to32(lo[pos]), f[pos])
+        assert np.all(to32(lo[pos] - np.uint64(1)) < f[pos])
+        fin = np.isfinite(f)
+        assert np.array_equal(to32(hi[fin]), f[fin])
+        assert np.all(to32(hi[fin] + np.uint64(1)) > f[fin])
+
+
+def test_walk_and_probe_paths_follow_the_definition(lib):
+    """search_walk and search_path (integer midpoints, raw-bit window tests)
+    against 0.5 (lo + hi) and double / binary32 comparisons, on brackets from
+    real bisections: lo = 0 or a midpoint, windows from far wider than the
+    bracket to a few binary32 ulps (where the binary32 rule decides), answers
+    near powers of two (brackets across binades) and tiny or huge scales."""
+    rng = random.Random(7)
+    rows = []
+    for i in range(6000):
+        scale = 10 ** rng.uniform(-12, 12)
+        lam = scale * rng.uniform(0.5, 2.0)
+        if i % 5 == 0:
+            lam = 2.0 ** rng.randint(-30, 30) * (1 + rng.choice([-1, 1]) * 10 ** rng.uniform(-9, -2))
+        hi = 2.0 ** math.ceil(math.log2(lam) + rng.randint(0, 3))
+        lo = 0.0
+        for _ in range(rng.randint(0, 30)):      # some steps of the true bisection
+            mid = 0.5 * (lo + hi)
+            if mid >= lam:
+                hi = mid
+            else:
+                lo = mid
+        width = lam * 10 ** rng.uniform(-9.5, -0.5)
+        if rng.random() < 0.2:
+            ulp = float(np.spacing(np.float32(lam)))
+            width = ulp * rng.uniform(0.5, 6.0)
+        xa = lam - width * rng.uniform(0.05, 1.0)
+        xb = lam + width * rng.uniform(0.05, 1.0)
+        xa = max(xa, lo) if rng.random() < 0.5 else xa
+        if rng.random() < 0.1:
+            xa = -1.0                            # nothing infeasible known yet
+        if not (xa < xb):
+            continue
+        rows.append((lo, hi, xa, xb, float(rng.random() < 0.6)))
+    a = np.ascontiguousarray(np.array(rows, dtype=np.float64).ravel())
+    assert lib.kvqs_path_check(a.ctypes.data, len(rows)) == 0
