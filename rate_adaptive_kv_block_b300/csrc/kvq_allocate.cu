@@ -151,6 +151,12 @@ __global__ void ctrl_init_kernel(Ctrl *c, const StatsHeader *hdr, double budget,
 // State value G(j,l): distortion of the intervals up to (j,l) plus lambda
 // times the entropy terms of the levels before l.  Lane-private state in
 // shared memory, [pair][lane].  Returns the chain's d_r H_r and its mask.
+// min(a, b, c) in one instruction
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 __device__ __forceinline__ float hh_at(const float *tb, int i, int j, int l) {
     return tb[kTblHH + trip_off(i, j) + l - j - 1];
 }
@@ -188,22 +194,41 @@ __device__ __forceinline__ void dp_a_stage(const float *__restrict__ tb, float l
         }
         acc[0] = INF;
     }
+    // predecessors i in pairs: two targets per packed fused multiply-add
+    // (same rounding as fmaf), one three-input minimum per target and pair
+    // (a minimum is exact, so the result is that of the pairwise chain)
+    const float2 l2 = make_float2(lam, lam);
 #pragma unroll
-    for (int i = 0; i < J; ++i) {
-        const float g = sG1[pidx(i, J) * 32 + lane];
-        const float2 g2 = make_float2(g, g), l2 = make_float2(lam, lam);
-        const float4 *h4 = reinterpret_cast<const float4 *>(tb + kTblHH + trip_off(i, J));
+    for (int i = 0; i < J; i += 2) {
+        const bool two = i + 1 < J;
+        const float ga = sG1[pidx(i, J) * 32 + lane];
+        const float gb = two ? sG1[pidx(i + 1 < J ? i + 1 : i, J) * 32 + lane] : 0.f;
+        const float2 ga2 = make_float2(ga, ga), gb2 = make_float2(gb, gb);
+        const float4 *ha4 = reinterpret_cast<const float4 *>(tb + kTblHH + trip_off(i, J));
+        const float4 *hb4 = reinterpret_cast<const float4 *>(
+            tb + kTblHH + trip_off(i + 1 < J ? i + 1 : i, J));
 #pragma unroll
         for (int q = 0; q < nq; ++q) {
-            const float4 h = h4[q];
-            // two targets per packed fused multiply-add (same rounding as fmaf)
-            const float2 c01 = __ffma2_rn(l2, make_float2(h.x, h.y), g2);
-            const float2 c23 = __ffma2_rn(l2, make_float2(h.z, h.w), g2);
-            const float cs[4] = {c01.x, c01.y, c23.x, c23.y};
+            const float4 ha = ha4[q];
+            const float2 a01 = __ffma2_rn(l2, make_float2(ha.x, ha.y), ga2);
+            const float2 a23 = __ffma2_rn(l2, make_float2(ha.z, ha.w), ga2);
+            const float as[4] = {a01.x, a01.y, a23.x, a23.y};
+            if (two) {
+                const float4 hb = hb4[q];
+                const float2 b01 = __ffma2_rn(l2, make_float2(hb.x, hb.y), gb2);
+                const float2 b23 = __ffma2_rn(l2, make_float2(hb.z, hb.w), gb2);
+                const float bs[4] = {b01.x, b01.y, b23.x, b23.y};
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int t = 4 * q + r;
-                if (t < n) acc[t] = fminf(acc[t], cs[r]);
+                for (int r = 0; r < 4; ++r) {
+                    const int t = 4 * q + r;
+                    if (t < n) acc[t] = fmin3(acc[t], as[r], bs[r]);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int t = 4 * q + r;
+                    if (t < n) acc[t] = fminf(acc[t], as[r]);
+                }
             }
         }
     }
