@@ -310,3 +310,39 @@ def test_fused_edge_layouts():
         for key in ("codebook", "k", "D_r", "H_r", "totals", "lam", "status", "codes"):
             a, b = getattr(ref, key), getattr(got, key)
             assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (S, T, D, G, key)
+
+
+# ---------------------------------------------------------- search rounds
+
+ROUND_CASES = [
+    # (workload, T, S, bits/entry): budgets whose pilot estimate is off by
+    # 30-45 %, where a fine grid of fixed width around it missed lambda
+    ("llama3_8b_layer", 2048, 16, 2.0),
+    ("full_model_cache", 2048, 16, 2.0),
+    ("decode_admission", 32, 2048, 1.5),
+    ("hadamard_groups", 4096, 8, 2.0),
+]
+
+
+@pytest.mark.parametrize("name,T,S,bpe", ROUND_CASES)
+def test_search_needs_one_round_over_every_block(name, T, S, bpe):
+    """Round 0's grid spans the pilot's whole bracket, so after it only the
+    blocks whose rate can still change are evaluated again; lambda is still
+    the sequential bisection's (the oracle's within the parity tolerance)."""
+    _need_gpu()
+    w = synth.workload(name, T=T, S=S)
+    x = synth.make_numpy(w, seed=0)
+    xd = torch.from_numpy(x.view(np.int16)).view(torch.float16).cuda()
+    L = kvq.Layout(w.S, w.T, w.D, w.G)
+    nb = L.nblocks
+    assert nb >= 1024                      # large enough for a pilot round
+    buf = kvq.Buffers(L, 16)
+    kvq.quantize(xd, L, bpe * w.entries, 16, buf=buf)
+    torch.cuda.synchronize()
+    rep = kvq.kvq_allocate_report(buf.workspace)
+    active = rep["active"]
+    assert active[0] < nb                  # the pilot: a sample
+    assert active[1] == nb                 # round 0: every block
+    assert all(a < nb // 2 for a in active[2:]), active
+    want = oracle.allocate_bisect(x.view(np.float16), w.G, 16, bpe * w.entries)["lambda"]
+    assert abs(float(buf.lam.item()) - want) <= 1e-4 * want
