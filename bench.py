@@ -175,6 +175,62 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def attention_bench(w, L, buf, flush_l2, graph_of, device_ms, t_flush, nrep, hbm, src, dev):
+    """kvq_decode_attention on the quantized layer, L2 flushed before every
+    launch: its time, the bytes it must read (codes, codebooks, queries) and
+    the fraction of the HBM roofline; PyTorch's attention on the binary16
+    decode of the same cache for comparison."""
+    import math
+    import torch
+    import torch.nn.functional as F
+    from rate_adaptive_kv_block_b300 import kvq
+    S_kv, D, n_rep = w.S // 2, w.D, 4
+    half = S_kv * (w.T // 32) * (w.D // w.G)          # blocks of the K streams
+    L_kv = kvq.Layout(S_kv, w.T, w.D, w.G)
+    g = torch.Generator(device="cpu").manual_seed(1)
+    qa = torch.randn((S_kv * n_rep, D), generator=g).to(dev)
+    out = torch.empty_like(qa)
+    ws = torch.empty(kvq.kvq_attention_workspace_bytes(L_kv, n_rep), dtype=torch.uint8, device=dev)
+    kc, vc = buf.codes[:half], buf.codes[half:]
+    kcb, vcb = buf.codebook[:half], buf.codebook[half:]
+    scale = 1.0 / math.sqrt(D)
+
+    def run():
+        kvq.kvq_decode_attention(qa, n_rep, L_kv, kc, kcb, vc, vcb, w.T, scale, ws, out)
+    g_att = graph_of(lambda: (flush_l2(1), run()))
+    device_ms(g_att, 2)
+    t_att = device_ms(g_att, nrep) - t_flush
+    nbytes = 2 * half * 16 * w.G + 2 * half * 64 + 2 * qa.numel() * 4
+    res = {"what": "one decoding step: %d query heads, %d KV heads x %d tokens x %d, read from "
+                   "the 4-bit codes" % (S_kv * n_rep, S_kv, w.T, D),
+           "ms": t_att, "bytes": nbytes, "GBps": nbytes / (t_att * 1e-3) / 1e9,
+           "roofline": {"bound": "hbm", "achieved": nbytes / (t_att * 1e-3) / 1e9, "peak": hbm,
+                        "unit": "GB/s", "frac": nbytes / (t_att * 1e-3) / 1e9 / hbm,
+                        "peak_source": src},
+           "kernels_per_call": 2}
+    try:
+        y16 = torch.empty((w.S, w.T, D), dtype=torch.float16, device=dev)
+        kvq.kvq_dequantize(buf.codes, buf.codebook, L, y16)
+        Kf, Vf = y16[:S_kv].unsqueeze(0), y16[S_kv:].unsqueeze(0)
+        qh = qa.half().view(1, S_kv * n_rep, 1, D)
+        ref = {}
+
+        def sdpa():
+            ref["o"] = F.scaled_dot_product_attention(qh, Kf, Vf, scale=scale, enable_gqa=True)
+        sdpa()
+        g_sdpa = graph_of(lambda: (flush_l2(1), sdpa()))
+        device_ms(g_sdpa, 2)
+        t_sdpa = device_ms(g_sdpa, nrep) - t_flush
+        run()
+        torch.cuda.synchronize()
+        diff = (ref["o"].view(-1, D).float() - out).abs().max().item()
+        res["torch_sdpa_fp16"] = {"ms": t_sdpa, "bytes": 2 * S_kv * w.T * D * 2,
+                                  "max_abs_diff_vs_ours": diff}
+    except Exception as e:                          # the comparison is context only
+        res["torch_sdpa_fp16"] = {"unavailable": str(e)[:200]}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -335,6 +391,12 @@ def main():
     t_qcold = device_ms(g_quant, nrep) - t_flush
     t_fcold = device_ms(g_fused, nrep) - t_flush
 
+    # decode attention over this layer's stored cache (kvq_decode_attention):
+    # 32 query heads (4 per KV head) on the 8 K and 8 V streams, every token;
+    # beside it PyTorch's scaled_dot_product_attention on the binary16 decode
+    # of the same cache (a library kernel, for context)
+    att = attention_bench(w, L, buf, flush_l2, graph_of, device_ms, t_flush, nrep, *peaks(), dev)
+
     # End to end through the C ABI from pinned host memory, pipelined over
     # three streams the way a serving loop would run it: step i's input copy
     # overlaps step i-1's kernels and step i-2's result copy.  Every step
@@ -413,6 +475,7 @@ def main():
         "eager_quantize_ms": mean(t_quant),
         "stats_cold_ms": t_scold, "quantize_cold_ms": t_qcold, "allocate_cold_ms": t_acold,
         "fused_allocate_quantize_cold_ms": t_fcold,
+        "decode_attention": att,
         "cold_method": "graph (L2 flush + kernel) minus graph (L2 flush), device-timed",
         "stats_cold_GBps": s_bytes / (t_scold * 1e-3) / 1e9,
         "quantize_cold_GBps": q_bytes / (t_qcold * 1e-3) / 1e9,

@@ -18,6 +18,7 @@
  *     kvq_allocate   -> lambda, per-block codebook / k / D_r / H_r
  *     kvq_quantize   -> packed codes
  *     kvq_dequantize -> binary16 reconstruction ("decode before attention")
+ *     kvq_decode_attention -> attention of a decoding step read from the codes
  *
  * Conventions for every entry point:
  *   - Pointers named "device" are CUDA device memory owned by the caller; the
@@ -220,6 +221,45 @@ int kvq_quantize(const uint16_t *x, kvq_layout L, const float *codebook,
  */
 int kvq_dequantize(const uint8_t *codes, const float *codebook, kvq_layout L,
                    uint16_t *y, void *stream);
+
+/*
+ * kvq_decode_attention -- one decoding step of attention over the quantized
+ * cache, with the codes decoded in registers ("Implementation notes": decode
+ * before attention; the page records attention latency).  For query head hq
+ * and its KV head h = hq / n_rep:
+ *     s_t = scale * sum_f q[hq][f] K[h][t][f]      for t < T_valid
+ *     out[hq][f] = sum_t softmax(s)_t V[h][t][f]
+ * where K[h][t][f] = k_codebook[block][code] is the level the entry's 4-bit
+ * code selects (the stored value; no binary16 copy is made), V likewise.
+ * Arithmetic in fp32 (products, sums, base-2 exponentials of
+ * scale*log2(e)-scaled scores); the token range is split over CTAs and the
+ * splits are combined by rescaling to a common maximum.
+ *   q             device fp32 [S * n_rep][128]: the query heads, grouped by
+ *                 KV head (hq = h * n_rep + r); read.
+ *   n_rep         query heads per KV head: 1, 2 or 4.
+ *   L             layout of the K (and the V) tensor: S = KV heads, T tokens,
+ *                 D = 128, any valid group.
+ *   k_codes, k_codebook, v_codes, v_codebook
+ *                 device outputs of kvq_quantize / kvq_allocate for the K and
+ *                 the V tensor of layout L (for a tensor that stacks K and V
+ *                 as streams, pointers to their first blocks); read.
+ *   T_valid       tokens attended, 0 <= T_valid <= T (0: out = 0).
+ *   scale         finite softmax scale (1/sqrt(128) for plain attention).
+ *   workspace     device, kvq_attention_workspace_bytes(L, n_rep) bytes of
+ *                 scratch (per-split partial results); overwritten.
+ *   out           device fp32 [S * n_rep][128], written.
+ *   status        device int32 or NULL: set to KVQ_ERR_TIMEOUT if a bulk copy
+ *                 of codes into shared memory never completed (that token
+ *                 range is then left out of out); untouched otherwise.
+ * Errors: KVQ_ERR_INVALID_ARG for D != 128, n_rep not in {1, 2, 4}, more
+ * than 65535 KV heads, T_valid out of range, a non-finite scale, a missing or
+ * unaligned pointer.
+ */
+size_t kvq_attention_workspace_bytes(kvq_layout L, int n_rep);
+int kvq_decode_attention(const float *q, int n_rep, kvq_layout L, const uint8_t *k_codes,
+                         const float *k_codebook, const uint8_t *v_codes,
+                         const float *v_codebook, int64_t T_valid, float scale, void *workspace,
+                         float *out, int32_t *status, void *stream);
 
 /*
  * kvq_allocate_report -- what the last kvq_allocate on this workspace did

@@ -245,5 +245,32 @@ def dequantize(codes, codebook, shape, G, b0=0, nb=None, y=None):
     return y
 
 
+def decode_attention(q, k_codes, k_codebook, v_codes, v_codebook, S, T, D, G, n_rep, T_valid,
+                     scale):
+    """One decoding step of attention over the stored cache, in fp64 ("Rate-
+    adaptive KV-cache quantizer", "Implementation notes": decode before
+    attention).  The K and V tensors [S, T, D] are decoded with dequantize;
+    for query head hq = h * n_rep + r (q: [S * n_rep, D]):
+        s_t = scale * sum_f q[hq, f] K[h, t, f]           (t < T_valid)
+        out[hq] = sum_t exp(s_t - max s) V[h, t] / sum_t exp(s_t - max s)
+    Returns float64 [S * n_rep, D]; zeros when T_valid = 0."""
+    K = _f16(dequantize(k_codes, k_codebook, (S, T, D), G))[:, :T_valid]
+    V = _f16(dequantize(v_codes, v_codebook, (S, T, D), G))[:, :T_valid]
+    q = np.asarray(q, dtype=np.float64).reshape(S, n_rep, D)
+    out = np.zeros((S, n_rep, D))
+    if T_valid == 0:
+        return out.reshape(S * n_rep, D)
+    for h in range(S):
+        s = scale * (q[h] @ K[h].T)                    # [n_rep, T_valid]
+        w = np.exp(s - s.max(axis=1, keepdims=True))
+        out[h] = (w @ V[h]) / w.sum(axis=1, keepdims=True)
+    return out.reshape(S * n_rep, D)
+
+
+def _f16(y):
+    """uint16 binary16 bit patterns -> float64 values."""
+    return np.asarray(y, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
 if os.environ.get("KVQ_ORACLE_THREADS"):
     set_threads(int(os.environ["KVQ_ORACLE_THREADS"]))

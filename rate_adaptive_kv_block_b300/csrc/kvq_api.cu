@@ -21,6 +21,12 @@ int quantize_init();
 int launch_dequantize(const uint8_t *codes, const float *codebook, const kvq_layout &L,
                       uint16_t *y, cudaStream_t st);
 size_t workspace_bytes(int64_t nb, int s);
+size_t attention_workspace_bytes(const kvq_layout &L, int n_rep);
+int launch_decode_attention(const float *q, int n_rep, const kvq_layout &L, const uint8_t *kc,
+                            const float *kcb, const uint8_t *vc, const float *vcb,
+                            int64_t T_valid, float scale, void *workspace, float *out,
+                            int32_t *status, cudaStream_t st);
+int attention_init();
 int allocate_init();
 int allocate_report(const void *workspace, kvq_report *r);
 
@@ -47,6 +53,7 @@ static int init_once() {
     if (!done[dev]) {
         state[dev] = allocate_init();
         if (state[dev] == KVQ_OK) state[dev] = quantize_init();
+        if (state[dev] == KVQ_OK) state[dev] = attention_init();
         done[dev] = true;
     }
     return state[dev];
@@ -196,6 +203,37 @@ int kvq_dequantize(const uint8_t *codes, const float *codebook, kvq_layout L, ui
         if (L.S * (L.T / 32) > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
     }
     return launch_dequantize(codes, codebook, L, y, static_cast<cudaStream_t>(stream));
+}
+
+static bool attention_layout_ok(const kvq_layout &L, int n_rep) {
+    return layout_ok(L) && L.D == 128 && (n_rep == 1 || n_rep == 2 || n_rep == 4) &&
+           L.S <= 65535 && L.S * n_rep <= 0x7fffffffll;
+}
+
+size_t kvq_attention_workspace_bytes(kvq_layout L, int n_rep) {
+    if (!attention_layout_ok(L, n_rep)) return 0;
+    return attention_workspace_bytes(L, n_rep);
+}
+
+int kvq_decode_attention(const float *q, int n_rep, kvq_layout L, const uint8_t *k_codes,
+                         const float *k_codebook, const uint8_t *v_codes,
+                         const float *v_codebook, int64_t T_valid, float scale, void *workspace,
+                         float *out, int32_t *status, void *stream) {
+    if (!attention_layout_ok(L, n_rep)) return KVQ_ERR_INVALID_ARG;
+    if (T_valid < 0 || T_valid > L.T || !(scale == scale) || isinf(scale)) return KVQ_ERR_INVALID_ARG;
+    if (L.S == 0) return KVQ_OK;
+    if (!q || !out || !workspace) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
+    if (T_valid > 0) {
+        if (!k_codes || !k_codebook || !v_codes || !v_codebook) return KVQ_ERR_INVALID_ARG;
+        if (!aligned16(k_codes) || !aligned16(k_codebook) || !aligned16(v_codes) ||
+            !aligned16(v_codebook))
+            return KVQ_ERR_INVALID_ARG;
+    }
+    if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
+    return launch_decode_attention(q, n_rep, L, k_codes, k_codebook, v_codes, v_codebook, T_valid,
+                                   scale, workspace, out, status,
+                                   static_cast<cudaStream_t>(stream));
 }
 
 int kvq_allocate_report(const void *workspace, kvq_report *report) {

@@ -16,6 +16,7 @@
 // (explicit round-to-nearest, so no multiply-add contraction can change a
 // code), and one SplitMix64 output gives both uniforms.
 #include "kvq_internal.cuh"
+#include "kvq_bulk.cuh"
 #include "kvq_quant_core.cuh"
 
 namespace kvq {
@@ -26,43 +27,6 @@ constexpr int kQMaxCols = 256;               // features per tile (at most)
 constexpr int kQMaxGroups = kQMaxCols / 8;   // blocks per tile (at most)
 constexpr uint32_t kQWaitLimit = 1u << 22;   // mbarrier polls before giving up
 
-// ------------------------------------------------------------- mbarriers
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-// true once the phase with this parity has completed; false after the limit
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kQWaitLimit; ++it) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n"
-            " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(smem_addr(bar)), "r"(parity)
-            : "memory");
-        if (done) return true;
-    }
-    return false;
-}
-// bulk copy global -> shared, completing on `bar` (16-byte aligned, size % 16 == 0)
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
-                                         uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
 
 // --------------------------------------------------------------- tiles
 struct QGeom {
@@ -132,7 +96,7 @@ quantize_kernel(const uint16_t *__restrict__ x, const float *__restrict__ codebo
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++n) {
         const uint32_t s = n % kQStages;
         char *buf = qsm + s * g.stage_bytes;
-        if (!mbar_wait(&bars[s], (n / kQStages) & 1u)) {
+        if (!mbar_wait(&bars[s], (n / kQStages) & 1u, kQWaitLimit)) {
             if (tid == 0) failed = true;
         }
         __syncthreads();
@@ -185,7 +149,7 @@ quantize_kernel(const uint16_t *__restrict__ x, const float *__restrict__ codebo
             for (uint32_t k = 0; k < kQStages; ++k) {
                 const uint32_t nk = n + k;
                 const int64_t tk = (int64_t)blockIdx.x + (int64_t)nk * gridDim.x;
-                if (tk < ntiles) mbar_wait(&bars[nk % kQStages], (nk / kQStages) & 1u);
+                if (tk < ntiles) mbar_wait(&bars[nk % kQStages], (nk / kQStages) & 1u, kQWaitLimit);
             }
         }
         __syncthreads();

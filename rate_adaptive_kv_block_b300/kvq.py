@@ -100,6 +100,11 @@ def lib():
         L.kvq_quantize.argtypes = [vp, _Layout, vp, vp, u64, u64, vp, vp, vp]
         L.kvq_dequantize.restype = C.c_int
         L.kvq_dequantize.argtypes = [vp, vp, _Layout, vp, vp]
+        L.kvq_attention_workspace_bytes.restype = C.c_size_t
+        L.kvq_attention_workspace_bytes.argtypes = [_Layout, C.c_int]
+        L.kvq_decode_attention.restype = C.c_int
+        L.kvq_decode_attention.argtypes = [vp, C.c_int, _Layout, vp, vp, vp, vp, i64, C.c_float,
+                                           vp, vp, vp, vp]
         L.kvq_allocate_report.restype = C.c_int
         L.kvq_allocate_report.argtypes = [vp, C.POINTER(_Report)]
         L.kvq_status_string.restype = C.c_char_p
@@ -186,6 +191,21 @@ def kvq_quantize(x, L: Layout, codebook, k, seed: int, index_base: int, codes, s
 def kvq_dequantize(codes, codebook, L: Layout, y, stream=None):
     _check(lib().kvq_dequantize(_ptr(codes), _ptr(codebook), L.c(), _ptr(y), _stream(stream)),
            "kvq_dequantize")
+
+
+def kvq_attention_workspace_bytes(L: Layout, n_rep: int) -> int:
+    return int(lib().kvq_attention_workspace_bytes(L.c(), n_rep))
+
+
+def kvq_decode_attention(q, n_rep: int, L: Layout, k_codes, k_codebook, v_codes, v_codebook,
+                         T_valid: int, scale: float, workspace, out, status=None, stream=None):
+    """Attention of one decoding step read from the codes (see include/kvq.h);
+    q and out are fp32 [L.S * n_rep, 128] device tensors."""
+    _check(lib().kvq_decode_attention(_ptr(q), n_rep, L.c(), _ptr(k_codes), _ptr(k_codebook),
+                                      _ptr(v_codes), _ptr(v_codebook), int(T_valid),
+                                      float(scale), _ptr(workspace), _ptr(out),
+                                      _ptr(status) if status is not None else None,
+                                      _stream(stream)), "kvq_decode_attention")
 
 
 def stats_rows(stats):

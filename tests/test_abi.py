@@ -76,3 +76,31 @@ def test_host_validation_rejects_bad_arguments():
     assert lib.kvq_dequantize(None, C.c_void_p(p.p), L.c(), C.c_void_p(p.p), st(s)) == bad
     with pytest.raises(kvq.KvqError):
         kvq.kvq_stats(p, L, p, p, m=16, stream=s)
+
+
+def test_decode_attention_host_validation():
+    """kvq_decode_attention rejects unsupported shapes and bad arguments on
+    the host; its workspace size is one partial result per KV head, split
+    and query head."""
+    L = kvq.Layout(8, 8192, 128, 128)
+    assert kvq.kvq_attention_workspace_bytes(L, 4) == 8 * 64 * 4 * 130 * 4
+    assert kvq.kvq_attention_workspace_bytes(kvq.Layout(8, 8192, 64, 64), 4) == 0   # D != 128
+    assert kvq.kvq_attention_workspace_bytes(L, 3) == 0                             # n_rep
+    p, odd = _Fake(1 << 20), _Fake((1 << 20) + 8)
+    s = _Stream()
+    bad = kvq.KVQ_ERR_INVALID_ARG
+    lib = kvq.lib()
+    st = kvq._stream
+    v = C.c_void_p(p.p)
+
+    def call(q=v, n_rep=4, lay=L, T_valid=8192, scale=0.088, ws=v, out=v, kc=v):
+        return lib.kvq_decode_attention(q, n_rep, lay.c(), kc, v, v, v, T_valid, scale, ws, out,
+                                        None, st(s))
+    assert call(n_rep=3) == bad
+    assert call(lay=kvq.Layout(8, 8192, 256, 128)) == bad
+    assert call(T_valid=8193) == bad and call(T_valid=-1) == bad
+    assert call(scale=float("nan")) == bad and call(scale=float("inf")) == bad
+    assert call(q=None) == bad and call(ws=None) == bad and call(out=C.c_void_p(odd.p)) == bad
+    assert call(kc=None) == bad and call(kc=C.c_void_p(odd.p)) == bad
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_decode_attention(p, 3, L, p, p, p, p, 8192, 0.088, p, p, stream=s)
