@@ -134,11 +134,11 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
     }
     // value lanes: features 8 fg .. 8 fg + 7, tokens 4 tg .. 4 tg + 3
     const int fg = tid & 15, tg = tid >> 4;
-    float acc[R][8];
+    float2 acc[R][4];                               // features 8 fg + 2b, + 2b + 1
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[r][j] = 0.f;
+        for (int b = 0; b < 4; ++b) acc[r][b] = make_float2(0.f, 0.f);
     __syncthreads();
 
     int cfail = nchunks;
@@ -163,24 +163,26 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass) {
                 const int t = 16 * pass + tok;
-                float dot[R];
+                float2 dot[R];                       // even and odd features apart
 #pragma unroll
-                for (int r = 0; r < R; ++r) dot[r] = 0.f;
+                for (int r = 0; r < R; ++r) dot[r] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int f = 16 * k8 + 8 * u;
                     const uint32_t w = *reinterpret_cast<const uint32_t *>(kcode + code_offset(t, f, G));
                     const float *lv = klv + (f / G) * 16;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float kv = lv[(w >> (4 * i)) & 15u];
+                    for (int b = 0; b < 4; ++b) {
+                        const float2 kk = make_float2(lv[(w >> (8 * b)) & 15u], lv[(w >> (8 * b + 4)) & 15u]);
 #pragma unroll
-                        for (int r = 0; r < R; ++r) dot[r] = fmaf(qr[r][8 * u + i], kv, dot[r]);
+                        for (int r = 0; r < R; ++r)
+                            dot[r] = __ffma2_rn(make_float2(qr[r][8 * u + 2 * b], qr[r][8 * u + 2 * b + 1]),
+                                                kk, dot[r]);
                     }
                 }
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    float v = dot[r];
+                    float v = dot[r].x + dot[r].y;
                     v += __shfl_xor_sync(0xffffffffu, v, 1);
                     v += __shfl_xor_sync(0xffffffffu, v, 2);
                     v += __shfl_xor_sync(0xffffffffu, v, 4);
@@ -221,9 +223,9 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
         // values: rescale, then add the chunk's tokens
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const float a = salpha[r];
+            const float2 a = make_float2(salpha[r], salpha[r]);
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) acc[r][jj] *= a;
+            for (int b = 0; b < 4; ++b) acc[r][b] = __fmul2_rn(acc[r][b], a);
         }
         for (int j = 0; j < nblk; ++j) {
             const unsigned char *vcode = vcode0 + j * kAttnCodeBytes;
@@ -233,14 +235,14 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
             for (int k = 0; k < 4; ++k) {
                 const int t = 4 * tg + k;
                 const uint32_t w = *reinterpret_cast<const uint32_t *>(vcode + code_offset(t, f, G));
-                float pr[R];
+                float2 pr[R];
 #pragma unroll
-                for (int r = 0; r < R; ++r) pr[r] = sp[r][32 * j + t];
+                for (int r = 0; r < R; ++r) pr[r] = make_float2(sp[r][32 * j + t], sp[r][32 * j + t]);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float vv = lv[(w >> (4 * i)) & 15u];
+                for (int b = 0; b < 4; ++b) {
+                    const float2 vv = make_float2(lv[(w >> (8 * b)) & 15u], lv[(w >> (8 * b + 4)) & 15u]);
 #pragma unroll
-                    for (int r = 0; r < R; ++r) acc[r][i] = fmaf(pr[r], vv, acc[r][i]);
+                    for (int r = 0; r < R; ++r) acc[r][b] = __ffma2_rn(pr[r], vv, acc[r][b]);
                 }
             }
         }
@@ -272,7 +274,10 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) sacc[tg][r][8 * fg + jj] = acc[r][jj];
+        for (int b = 0; b < 4; ++b) {
+            sacc[tg][r][8 * fg + 2 * b] = acc[r][b].x;
+            sacc[tg][r][8 * fg + 2 * b + 1] = acc[r][b].y;
+        }
     __syncthreads();
     for (int i = tid; i < R * D; i += kAttnThreads) {
         const int r = i / D, f = i % D;
