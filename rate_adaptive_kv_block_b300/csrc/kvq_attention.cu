@@ -38,13 +38,13 @@ namespace kvq {
 constexpr int kAttnD = 128;         // head dimension
 constexpr int kAttnThreads = 128;
 constexpr int kAttnMaxSplits = 64;  // splits per KV head (workspace size)
-constexpr int kAttnChunk = 4;       // token blocks per bulk-copy stage
+constexpr int kAttnChunkMax = 8;    // token blocks per bulk-copy stage (at most)
 constexpr uint32_t kAttnWaitLimit = 1u << 22;   // mbarrier polls before giving up
 // one token block of one tensor: 32 tokens x 128 features at 4 bits (every
 // feature group), and its codebooks (16 fp32 per feature group)
 constexpr uint32_t kAttnCodeBytes = 16 * kAttnD;
-__host__ __device__ constexpr uint32_t attn_stage_bytes(int nG) {
-    return kAttnChunk * (2 * kAttnCodeBytes + 2 * 64u * (uint32_t)nG);
+__host__ __device__ constexpr uint32_t attn_stage_bytes(int chunk, int nG) {
+    return (uint32_t)chunk * (2 * kAttnCodeBytes + 2 * 64u * (uint32_t)nG);
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -70,7 +70,8 @@ __global__ void __launch_bounds__(kAttnThreads)
 attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
                     const float *__restrict__ kcb, const uint8_t *__restrict__ vc,
                     const float *__restrict__ vcb, int64_t ntb, int G, int64_t T_valid,
-                    float scale2, int bps, float *__restrict__ part, int32_t *__restrict__ status) {
+                    float scale2, int bps, int chunk, float *__restrict__ part,
+                    int32_t *__restrict__ status) {
     constexpr int D = kAttnD;
     const float NEG = __int_as_float(0xff800000);   // -inf
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -80,29 +81,29 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
     const int64_t ntb_valid = (T_valid + 31) / 32;
     const int64_t tb0 = (int64_t)split * bps;
     const int64_t tb1 = min(tb0 + bps, ntb_valid);
-    const int nchunks = tb1 > tb0 ? (int)((tb1 - tb0 + kAttnChunk - 1) / kAttnChunk) : 0;
+    const int nchunks = tb1 > tb0 ? (int)((tb1 - tb0 + chunk - 1) / chunk) : 0;
 
     extern __shared__ __align__(128) unsigned char asm_[];   // two stages
-    const uint32_t stage = attn_stage_bytes(nG);
+    const uint32_t stage = attn_stage_bytes(chunk, nG);
     __shared__ __align__(8) uint64_t bars[2];
-    __shared__ float ss[R][32 * kAttnChunk], sp[R][32 * kAttnChunk];   // scores, weights of a chunk
+    __shared__ float ss[R][32 * kAttnChunkMax], sp[R][32 * kAttnChunkMax];   // scores, weights of a chunk
     __shared__ float sm[R], sl[R], salpha[R];       // running max, sum; rescale factor
     __shared__ float sacc[8][R][D];                 // token groups' outputs, added at the end
     __shared__ bool failed;
 
-    // stage layout: K codes, V codes (kAttnChunk x 2048 bytes each), K
-    // codebooks, V codebooks (kAttnChunk x nG x 16 floats each)
+    // stage layout: K codes, V codes (chunk x 2048 bytes each), K codebooks,
+    // V codebooks (chunk x nG x 16 floats each)
     auto issue = [&](int c) {
         unsigned char *buf = asm_ + (c & 1) * stage;
-        const int64_t tbs = tb0 + (int64_t)c * kAttnChunk;
-        const uint32_t nblk = (uint32_t)min((int64_t)kAttnChunk, tb1 - tbs);
+        const int64_t tbs = tb0 + (int64_t)c * chunk;
+        const uint32_t nblk = (uint32_t)min((int64_t)chunk, tb1 - tbs);
         const int64_t blk0 = (h * ntb + tbs) * nG;                 // first block of the chunk
         const uint32_t cbytes = nblk * kAttnCodeBytes, bbytes = nblk * 64u * (uint32_t)nG;
         mbar_expect_tx(&bars[c & 1], 2 * cbytes + 2 * bbytes);
         bulk_g2s(buf, kc + blk0 * 16 * G, cbytes, &bars[c & 1]);
-        bulk_g2s(buf + kAttnChunk * kAttnCodeBytes, vc + blk0 * 16 * G, cbytes, &bars[c & 1]);
-        bulk_g2s(buf + 2 * kAttnChunk * kAttnCodeBytes, kcb + blk0 * 16, bbytes, &bars[c & 1]);
-        bulk_g2s(buf + 2 * kAttnChunk * kAttnCodeBytes + kAttnChunk * 64u * nG, vcb + blk0 * 16,
+        bulk_g2s(buf + chunk * kAttnCodeBytes, vc + blk0 * 16 * G, cbytes, &bars[c & 1]);
+        bulk_g2s(buf + 2 * chunk * kAttnCodeBytes, kcb + blk0 * 16, bbytes, &bars[c & 1]);
+        bulk_g2s(buf + 2 * chunk * kAttnCodeBytes + chunk * 64u * nG, vcb + blk0 * 16,
                  bbytes, &bars[c & 1]);
     };
     if (tid == 0) {
@@ -151,11 +152,11 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
             break;
         }
         const unsigned char *buf = asm_ + (c & 1) * stage;
-        const int64_t tbs = tb0 + (int64_t)c * kAttnChunk;
-        const int nblk = (int)min((int64_t)kAttnChunk, tb1 - tbs);
-        const unsigned char *kcode0 = buf, *vcode0 = buf + kAttnChunk * kAttnCodeBytes;
-        const float *klv0 = reinterpret_cast<const float *>(buf + 2 * kAttnChunk * kAttnCodeBytes);
-        const float *vlv0 = klv0 + kAttnChunk * nG * 16;
+        const int64_t tbs = tb0 + (int64_t)c * chunk;
+        const int nblk = (int)min((int64_t)chunk, tb1 - tbs);
+        const unsigned char *kcode0 = buf, *vcode0 = buf + chunk * kAttnCodeBytes;
+        const float *klv0 = reinterpret_cast<const float *>(buf + 2 * chunk * kAttnCodeBytes);
+        const float *vlv0 = klv0 + chunk * nG * 16;
         // scores of the chunk's tokens: 16 tokens per pass, 8 lanes per token
         for (int j = 0; j < nblk; ++j) {
             const unsigned char *kcode = kcode0 + j * kAttnCodeBytes;
@@ -195,10 +196,10 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
         // lane, lane + 32, ..)
         if (warp < R) {
             const int r = warp;
-            float sc[kAttnChunk];
+            float sc[kAttnChunkMax];
             float bm = NEG;
 #pragma unroll
-            for (int k = 0; k < kAttnChunk; ++k) {
+            for (int k = 0; k < kAttnChunkMax; ++k) {
                 sc[k] = k < nblk ? ss[r][32 * k + lane] : NEG;
                 bm = fmaxf(bm, sc[k]);
             }
@@ -207,7 +208,7 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
             float alpha = 1.f, psum = 0.f;
             if (m_new != NEG) alpha = exp2f(m_old - m_new);          // 0 while nothing was seen
 #pragma unroll
-            for (int k = 0; k < kAttnChunk; ++k) {
+            for (int k = 0; k < kAttnChunkMax; ++k) {
                 const float p = (m_new == NEG || sc[k] == NEG) ? 0.f : exp2f(sc[k] - m_new);
                 if (k < nblk) sp[r][32 * k + lane] = p;
                 psum += p;
@@ -343,7 +344,7 @@ size_t attention_workspace_bytes(const kvq_layout &L, int n_rep) {
 }
 
 int attention_init() {
-    const int smem = 2 * (int)attn_stage_bytes(kAttnD / 8);    // the largest stage (group 8)
+    const int smem = 2 * (int)attn_stage_bytes(kAttnChunkMax, kAttnD / 8);   // the largest ring
     if (cudaFuncSetAttribute(attn_partial_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess ||
         cudaFuncSetAttribute(attn_partial_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -379,19 +380,22 @@ int launch_decode_attention(const float *q, int n_rep, const kvq_layout &L, cons
         nsplit = (int)((ntb_valid + bps - 1) / bps);
         const dim3 grid((unsigned)nsplit, (unsigned)H);
         const float scale2 = scale * 1.4426950408889634f;   // log2(e)
-        const size_t smem = 2 * (size_t)attn_stage_bytes(L.D / L.group);
+        // a CTA's range in one chunk when it has at most 8 blocks, else a
+        // ring of two stages of 8
+        const int chunk = (int)(bps < kAttnChunkMax ? bps : kAttnChunkMax);
+        const size_t smem = (bps > chunk ? 2 : 1) * (size_t)attn_stage_bytes(chunk, L.D / L.group);
         switch (n_rep) {
         case 1:
             attn_partial_kernel<1><<<grid, kAttnThreads, smem, st>>>(
-                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, part, status);
+                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, status);
             break;
         case 2:
             attn_partial_kernel<2><<<grid, kAttnThreads, smem, st>>>(
-                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, part, status);
+                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, status);
             break;
         default:
             attn_partial_kernel<4><<<grid, kAttnThreads, smem, st>>>(
-                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, part, status);
+                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, status);
             break;
         }
         if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
