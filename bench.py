@@ -175,6 +175,66 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def comparator_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev):
+    """The page's comparators on the same layer: uniform INT4 (16 equally
+    spaced levels from the block's minimum to its maximum, nearest level) and
+    uniform stochastic quantization (same levels, unbiased interpolation),
+    against the rate-adaptive quantizer at its budget and at the rate the
+    INT4 codes would take entropy-coded per block.  Distortion = mean squared
+    error of the binary16 decode; rates in bits per entry (entropies of the
+    codes' empirical frequencies per block for the uniform ones, sum d_r H_r
+    for the rate-adaptive one).  Kernel times with L2 flushed."""
+    import torch
+    from rate_adaptive_kv_block_b300 import kvq
+    nb, d = L.nblocks, 32 * w.G
+    xf = x.float()
+    y = torch.empty_like(x)
+
+    def mse(codes, cb):
+        kvq.kvq_dequantize(codes, cb, L, y)
+        return float(((y.float() - xf) ** 2).mean())
+
+    def code_entropy(codes):
+        c = torch.stack([codes & 15, codes >> 4], dim=-1).reshape(nb, d).long()
+        idx = c + 16 * torch.arange(nb, device=dev).unsqueeze(1)
+        n = torch.bincount(idx.reshape(-1), minlength=16 * nb).reshape(nb, 16).double()
+        p = n / d
+        h = -(torch.where(n > 0, p * torch.log2(p), torch.zeros_like(p))).sum(dim=1)
+        return float(h.mean())
+
+    ucb = torch.empty((nb, 16), dtype=torch.float32, device=dev)
+    uk = torch.empty(nb, dtype=torch.uint8, device=dev)
+    ust = torch.zeros(1, dtype=torch.int32, device=dev)
+    ucodes = torch.empty_like(buf.codes)
+    g_u = graph_of(lambda: (flush_l2(1), kvq.kvq_uniform_codebook(x, L, ucb, uk, ust),
+                            kvq.kvq_quantize_nearest(x, L, ucb, uk, ucodes)))
+    device_ms(g_u, 2)
+    t_u = device_ms(g_u, nrep) - t_flush
+    mse_near = mse(ucodes, ucb)
+    h_near = code_entropy(ucodes)
+    kvq.kvq_quantize(x, L, ucb, uk, 0, 0, ucodes)
+    mse_sto = mse(ucodes, ucb)
+    h_sto = code_entropy(ucodes)
+    mse_ecasq = mse(buf.codes, buf.codebook)
+    rate_ecasq = float(buf.totals[0].item()) / x.numel()
+    # the rate-adaptive quantizer at the entropy-coded rate of the INT4 codes
+    b2 = kvq.Buffers(L, w.s, dev)
+    kvq.quantize(x, L, h_near * x.numel(), w.s, buf=b2)
+    torch.cuda.synchronize()
+    mse_eq = mse(b2.codes, b2.codebook)
+    return {"what": "mean squared error of the binary16 decode and rate in bits/entry on this "
+                    "layer; uniform = 16 equally spaced levels per block from its minimum to its "
+                    "maximum; uniform rates are the per-block entropies of the codes",
+            "uniform_int4_nearest": {"mse": mse_near, "rate_bits": h_near, "stored_bits": 4.0},
+            "uniform_stochastic": {"mse": mse_sto, "rate_bits": h_sto, "stored_bits": 4.0},
+            "rate_adaptive_at_budget": {"mse": mse_ecasq, "rate_bits": rate_ecasq, "stored_bits": 4.0},
+            "rate_adaptive_at_int4_rate": {"mse": mse_eq,
+                                           "rate_bits": float(b2.totals[0].item()) / x.numel(),
+                                           "stored_bits": 4.0},
+            "uniform_int4_ms": t_u,
+            "uniform_int4_GBps": (x.numel() * 2 + x.numel() // 2 + nb * 65) / (t_u * 1e-3) / 1e9}
+
+
 def attention_bench(w, L, buf, flush_l2, graph_of, device_ms, t_flush, nrep, hbm, src, dev):
     """kvq_decode_attention on the quantized layer, L2 flushed before every
     launch: its time, the bytes it must read (codes, codebooks, queries) and
@@ -396,6 +456,7 @@ def main():
     # beside it PyTorch's scaled_dot_product_attention on the binary16 decode
     # of the same cache (a library kernel, for context)
     att = attention_bench(w, L, buf, flush_l2, graph_of, device_ms, t_flush, nrep, *peaks(), dev)
+    comp = comparator_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev)
 
     # End to end through the C ABI from pinned host memory, pipelined over
     # three streams the way a serving loop would run it: step i's input copy
@@ -476,6 +537,7 @@ def main():
         "stats_cold_ms": t_scold, "quantize_cold_ms": t_qcold, "allocate_cold_ms": t_acold,
         "fused_allocate_quantize_cold_ms": t_fcold,
         "decode_attention": att,
+        "comparators": comp,
         "cold_method": "graph (L2 flush + kernel) minus graph (L2 flush), device-timed",
         "stats_cold_GBps": s_bytes / (t_scold * 1e-3) / 1e9,
         "quantize_cold_GBps": q_bytes / (t_qcold * 1e-3) / 1e9,

@@ -223,6 +223,35 @@ int kvq_dequantize(const uint8_t *codes, const float *codebook, kvq_layout L,
                    uint16_t *y, void *stream);
 
 /*
+ * kvq_uniform_codebook -- codebooks of the uniform comparator ("Implementation
+ * notes": compare uniform INT4 and uniform stochastic quantization at equal
+ * cache bytes): per block, from its minimum m and maximum M,
+ *     delta = fl32(fl32(M - m) / 15),  level_j = binary16(fl32(m + fl32(j delta)))
+ * for j = 0..14 and level_15 = M (fp32 round-to-nearest, no contraction),
+ * repeats removed: k distinct levels in codebook slots 0..k-1, slots k..15
+ * repeat the top.  kvq_quantize with these codebooks is uniform stochastic
+ * quantization; kvq_quantize_nearest with them is uniform INT4.
+ *   x         device [S,T,D] binary16, read.
+ *   codebook  device fp32 [nblocks][16], written.
+ *   k         device u8 [nblocks], written.
+ *   status    device int32, written: KVQ_OK, or KVQ_ERR_NONFINITE if a block
+ *             holds NaN or +-Inf (its codebook is then unspecified).
+ */
+int kvq_uniform_codebook(const uint16_t *x, kvq_layout L, float *codebook, uint8_t *k,
+                         int32_t *status, void *stream);
+
+/*
+ * kvq_quantize_nearest -- deterministic rounding to the nearest level of any
+ * codebook in the format above (the INT4 comparator with kvq_uniform_codebook):
+ * i = the largest index with q_i <= x (capped at k-2), code = i + [w < 2 r]
+ * with w = fl32(q_{i+1} - q_i), r = fl32(x - q_i) (a tie keeps the lower level);
+ * k = 1: code 0.  Codes packed as kvq_quantize's.  Arguments as kvq_quantize's
+ * without seed and index_base.
+ */
+int kvq_quantize_nearest(const uint16_t *x, kvq_layout L, const float *codebook, const uint8_t *k,
+                         uint8_t *codes, int32_t *status, void *stream);
+
+/*
  * kvq_decode_attention -- one decoding step of attention over the quantized
  * cache, with the codes decoded in registers ("Implementation notes": decode
  * before attention; the page records attention latency).  For query head hq

@@ -245,6 +245,58 @@ def dequantize(codes, codebook, shape, G, b0=0, nb=None, y=None):
     return y
 
 
+def uniform_codebook(x, G):
+    """Codebooks of the uniform comparator ("Rate-adaptive KV-cache quantizer",
+    "Implementation notes": uniform INT4 and uniform stochastic quantization at
+    equal bytes): per block from its minimum m and maximum M (a zero of either
+    sign taken as +0), delta =
+    fl32(fl32(M - m) / 15), level_j = binary16(fl32(m + fl32(j delta))) for
+    j < 15, level_15 = M, repeats removed, slots k..15 repeat the top.
+    Returns (codebook float32 [nb, 16], k uint8 [nb])."""
+    xv = _f16(_x(x)).astype(np.float32)
+    S, T, D = xv.shape
+    blocks = xv.reshape(S, T // 32, 32, D // G, G).transpose(0, 1, 3, 2, 4).reshape(-1, 32 * G)
+    nb = blocks.shape[0]
+    cb = np.zeros((nb, 16), dtype=np.float32)
+    k = np.zeros(nb, dtype=np.uint8)
+    for b in range(nb):
+        zero = np.float32(0)
+        m = np.float32(np.float32(blocks[b].min()) + zero)      # -0 -> +0
+        M = np.float32(np.float32(blocks[b].max()) + zero)
+        delta = np.float32(np.float32(M - m) / np.float32(15))
+        lv = [np.float32(np.float16(np.float32(m + np.float32(np.float32(j) * delta)))) for j in range(15)]
+        lv.append(M)
+        distinct = [lv[0]] + [v for a, v in zip(lv, lv[1:]) if v != a]
+        k[b] = len(distinct)
+        cb[b, :len(distinct)] = distinct
+        cb[b, len(distinct):] = distinct[-1]
+    return cb, k
+
+
+def quantize_nearest(x, G, codebook, k):
+    """Codes [nb, 16 G] of rounding every entry to the nearest level: i = the
+    largest index with q_i <= x (at most k-2), code = i + [w < 2 r] with
+    w = fl32(q_{i+1} - q_i), r = fl32(x - q_i); k = 1: code 0.  Packed as the
+    quantizer's (low nibble = even entry)."""
+    xv = _f16(_x(x)).astype(np.float32)
+    S, T, D = xv.shape
+    blocks = xv.reshape(S, T // 32, 32, D // G, G).transpose(0, 1, 3, 2, 4).reshape(-1, 32 * G)
+    nb = blocks.shape[0]
+    codes = np.zeros((nb, 32 * G), dtype=np.uint8)
+    cb = np.asarray(codebook, dtype=np.float32)
+    for b in range(nb):
+        kb = int(k[b])
+        if kb <= 1:
+            continue
+        q = cb[b, :kb]
+        v = blocks[b]
+        i = np.clip(np.searchsorted(q, v, side="right") - 1, 0, kb - 2)
+        w = (q[i + 1] - q[i]).astype(np.float32)
+        r = (v - q[i]).astype(np.float32)
+        codes[b] = (i + (w < np.float32(2) * r)).astype(np.uint8)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+
+
 def decode_attention(q, k_codes, k_codebook, v_codes, v_codebook, S, T, D, G, n_rep, T_valid,
                      scale):
     """One decoding step of attention over the stored cache, in fp64 ("Rate-

@@ -16,7 +16,9 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
                     uint8_t *codes = nullptr);
 int launch_quantize(const uint16_t *x, const kvq_layout &L, const float *codebook,
                     const uint8_t *k, uint64_t seed, uint64_t index_base, uint8_t *codes,
-                    int32_t *status, cudaStream_t st);
+                    int32_t *status, cudaStream_t st, bool nearest = false);
+int launch_uniform_codebook(const uint16_t *x, const kvq_layout &L, float *codebook, uint8_t *k,
+                            int32_t *status, cudaStream_t st);
 int quantize_init();
 int launch_dequantize(const uint8_t *codes, const float *codebook, const kvq_layout &L,
                       uint16_t *y, cudaStream_t st);
@@ -191,6 +193,31 @@ int kvq_quantize(const uint16_t *x, kvq_layout L, const float *codebook, const u
     if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
     return launch_quantize(x, L, codebook, k, seed, index_base, codes, status,
                            static_cast<cudaStream_t>(stream));
+}
+
+int kvq_uniform_codebook(const uint16_t *x, kvq_layout L, float *codebook, uint8_t *k,
+                         int32_t *status, void *stream) {
+    if (!layout_ok(L)) return KVQ_ERR_INVALID_ARG;
+    const int64_t nb = num_blocks(L);
+    if (nb > 0) {
+        if (!x || !codebook || !k || !status) return KVQ_ERR_INVALID_ARG;
+        if (!aligned16(x) || !aligned16(codebook)) return KVQ_ERR_INVALID_ARG;
+    }
+    return launch_uniform_codebook(x, L, codebook, k, status, static_cast<cudaStream_t>(stream));
+}
+
+int kvq_quantize_nearest(const uint16_t *x, kvq_layout L, const float *codebook, const uint8_t *k,
+                         uint8_t *codes, int32_t *status, void *stream) {
+    if (!layout_ok(L)) return KVQ_ERR_INVALID_ARG;
+    const int64_t nb = num_blocks(L);
+    if (nb > 0) {
+        if (!x || !codebook || !k || !codes) return KVQ_ERR_INVALID_ARG;
+        if (!aligned16(x) || !aligned16(codebook) || !aligned16(codes)) return KVQ_ERR_INVALID_ARG;
+        if (L.S * (L.T / 32) > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
+    }
+    if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
+    return launch_quantize(x, L, codebook, k, 0, 0, codes, status,
+                           static_cast<cudaStream_t>(stream), true);
 }
 
 int kvq_dequantize(const uint8_t *codes, const float *codebook, kvq_layout L, uint16_t *y,

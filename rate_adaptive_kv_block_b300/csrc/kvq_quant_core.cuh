@@ -45,7 +45,9 @@ __device__ __forceinline__ void splitmix_mix(uint32_t lo, uint32_t hi, uint32_t 
 }
 
 // Threshold j (0..15) and decision entry j of a block from its 16 codebook
-// slots; `k` = number of distinct levels.
+// slots; `k` = number of distinct levels.  NEAREST (the deterministic
+// comparator): w_i = q_{i+1} - q_i unscaled.
+template <bool NEAREST = false>
 __device__ __forceinline__ void quant_table_entry(const float *q, int k, int j, __half2 &thr,
                                                   float2 &qw) {
     const float INF = __int_as_float(0x7f800000);
@@ -55,7 +57,8 @@ __device__ __forceinline__ void quant_table_entry(const float *q, int k, int j, 
     const float qn = q[j < 15 ? j + 1 : 15];
     float ws = 0.f;
     if (k <= 1) ws = INF;                             // k = 1: never move up
-    else if (j <= k - 2) ws = __fmul_rn(__fsub_rn(qn, qj), 5.9604644775390625e-8f);  // 2^-24
+    else if (j <= k - 2)
+        ws = NEAREST ? __fsub_rn(qn, qj) : __fmul_rn(__fsub_rn(qn, qj), 5.9604644775390625e-8f);  // 2^-24
     qw = make_float2(-qj, ws);
 }
 
@@ -96,6 +99,43 @@ __device__ __forceinline__ uint32_t quant8(const uint4 raw, const uint32_t (&T)[
         const float2 tw = __fmul2_rn(u, make_float2(e0.y, e1.y));
         const uint32_t c0 = (uint32_t)i0 + (tw.x < r.x ? 1u : 0u);
         const uint32_t c1 = (uint32_t)i1 + (tw.y < r.y ? 1u : 0u);
+        packed |= (c0 | (c1 << 4)) << (8 * pr);
+    }
+    return packed;
+}
+
+// Codes of 8 consecutive entries rounded to the nearest level (the
+// deterministic comparator of "Rate-adaptive KV-cache quantizer",
+// "Implementation notes": uniform INT4 at equal bytes): the same interval
+// search, then code i + [w_i < 2 (x - q_i)] in fp32 round-to-nearest (a tie
+// keeps the lower level).  qw holds (-q_i, w_i).
+__device__ __forceinline__ uint32_t quant8_nearest(const uint4 raw, const uint32_t (&T)[16],
+                                                   const float2 *qw) {
+    const uint32_t xw0 = raw.x, xw1 = raw.y, xw2 = raw.z, xw3 = raw.w;
+    uint32_t packed = 0;
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+        const __half2 X = as_h2(pr == 0 ? xw0 : pr == 1 ? xw1 : pr == 2 ? xw2 : xw3);
+        const uint32_t m1 = __hge2_mask(X, as_h2(T[8]));
+        const uint32_t t2 = (T[12] & m1) | (T[4] & ~m1);
+        const uint32_t m2 = __hge2_mask(X, as_h2(t2));
+        const uint32_t a3 = (T[6] & m2) | (T[2] & ~m2), b3 = (T[14] & m2) | (T[10] & ~m2);
+        const uint32_t t3 = (b3 & m1) | (a3 & ~m1);
+        const uint32_t m3 = __hge2_mask(X, as_h2(t3));
+        const uint32_t a4 = (T[3] & m3) | (T[1] & ~m3), b4 = (T[7] & m3) | (T[5] & ~m3);
+        const uint32_t c4 = (T[11] & m3) | (T[9] & ~m3), d4 = (T[15] & m3) | (T[13] & ~m3);
+        const uint32_t lo4 = (b4 & m2) | (a4 & ~m2), hi4 = (d4 & m2) | (c4 & ~m2);
+        const uint32_t t4 = (hi4 & m1) | (lo4 & ~m1);
+        const uint32_t m4 = __hge2_mask(X, as_h2(t4));
+        const uint32_t idx = (m1 & 0x00080008u) | (m2 & 0x00040004u) | (m3 & 0x00020002u) |
+                             (m4 & 0x00010001u);
+        const int i0 = (int)(idx & 15u), i1 = (int)(idx >> 16);
+        const float2 e0 = qw[i0], e1 = qw[i1];
+        const float2 xf = __half22float2(X);
+        const float2 r = __fadd2_rn(xf, make_float2(e0.x, e1.x));          // x - q_i
+        const float2 r2 = __fadd2_rn(r, r);                                 // exact
+        const uint32_t c0 = (uint32_t)i0 + (e0.y < r2.x ? 1u : 0u);
+        const uint32_t c1 = (uint32_t)i1 + (e1.y < r2.y ? 1u : 0u);
         packed |= (c0 | (c1 << 4)) << (8 * pr);
     }
     return packed;

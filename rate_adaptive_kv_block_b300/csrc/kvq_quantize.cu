@@ -64,6 +64,7 @@ struct QTables {
     float2 qw[kQMaxGroups][16];     // (-q_i, (q_{i+1} - q_i) * 2^-24); k = 1: (-q_0, +inf)
 };
 
+template <bool NEAREST>
 __global__ void __launch_bounds__(kQThreads, 6)
 quantize_kernel(const uint16_t *__restrict__ x, const float *__restrict__ codebook, QGeom g,
                 int64_t ntiles, uint64_t seed, uint64_t index_base, uint8_t *__restrict__ codes,
@@ -110,7 +111,7 @@ quantize_kernel(const uint16_t *__restrict__ x, const float *__restrict__ codebo
             int k = 1;
 #pragma unroll
             for (int m = 0; m < 15; ++m) k += q[m] < top ? 1 : 0;
-            quant_table_entry(q, k, j, tb.thr[b][j], tb.qw[b][j]);
+            quant_table_entry<NEAREST>(q, k, j, tb.thr[b][j], tb.qw[b][j]);
         }
         __syncthreads();
         // this thread's block: 15 thresholds in registers
@@ -130,7 +131,10 @@ quantize_kernel(const uint16_t *__restrict__ x, const float *__restrict__ codebo
         const uint64_t zstep = (uint64_t)(rstep * g.D / 2) * kGolden;
         for (int row = row0; row < 32; row += rstep, z += zstep) {
             const uint4 raw = *reinterpret_cast<const uint4 *>(buf + (row * g.Dc + f0) * 2);
-            *reinterpret_cast<uint32_t *>(cbase + (int64_t)row * (g.G / 2)) = quant8(raw, T, qw, z);
+            uint32_t cw;
+            if constexpr (NEAREST) cw = quant8_nearest(raw, T, qw);
+            else cw = quant8(raw, T, qw, z);
+            *reinterpret_cast<uint32_t *>(cbase + (int64_t)row * (g.G / 2)) = cw;
         }
         __syncthreads();                         // every thread is done with this stage
         if (tid == 0) {
@@ -207,14 +211,16 @@ int quantize_init() {
     int dev = 0, sms = 0, occ = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
     const int smem = kQStages * ((64 * kQMaxCols + 64 * kQMaxGroups + 127) & ~127);
-    if (cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(quantize_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess ||
+        cudaFuncSetAttribute(quantize_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
         return KVQ_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return KVQ_ERR_CUDA;
     // the grid for the llama-shaped tile size (8 KB + codebook per stage)
     const int smem128 = kQStages * ((64 * 128 + 64 + 127) & ~127);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quantize_kernel, kQThreads, smem128) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quantize_kernel<false>, kQThreads, smem128) !=
         cudaSuccess)
         return KVQ_ERR_CUDA;
     g_quant_grid[dev] = (occ < 1 ? 1 : occ) * sms;
@@ -223,7 +229,7 @@ int quantize_init() {
 
 int launch_quantize(const uint16_t *x, const kvq_layout &L, const float *codebook,
                     const uint8_t *k, uint64_t seed, uint64_t index_base, uint8_t *codes,
-                    int32_t *status, cudaStream_t st) {
+                    int32_t *status, cudaStream_t st, bool nearest) {
     (void)k;   // the kernel reads k from the codebook (slots k..15 repeat the top level)
     const QGeom g = geometry(L);
     const int64_t ntiles = L.S * (L.T / 32) * g.nchunk;
@@ -233,8 +239,12 @@ int launch_quantize(const uint16_t *x, const kvq_layout &L, const float *codeboo
     int64_t grid = g_quant_grid[dev] > 0 ? g_quant_grid[dev] : 148;
     if (grid > ntiles) grid = ntiles;
     const size_t smem = (size_t)kQStages * g.stage_bytes;
-    quantize_kernel<<<(unsigned)grid, kQThreads, smem, st>>>(x, codebook, g, ntiles, seed,
-                                                             index_base, codes, status);
+    if (nearest)
+        quantize_kernel<true><<<(unsigned)grid, kQThreads, smem, st>>>(x, codebook, g, ntiles, seed,
+                                                                       index_base, codes, status);
+    else
+        quantize_kernel<false><<<(unsigned)grid, kQThreads, smem, st>>>(x, codebook, g, ntiles, seed,
+                                                                        index_base, codes, status);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

@@ -100,6 +100,10 @@ def lib():
         L.kvq_quantize.argtypes = [vp, _Layout, vp, vp, u64, u64, vp, vp, vp]
         L.kvq_dequantize.restype = C.c_int
         L.kvq_dequantize.argtypes = [vp, vp, _Layout, vp, vp]
+        L.kvq_uniform_codebook.restype = C.c_int
+        L.kvq_uniform_codebook.argtypes = [vp, _Layout, vp, vp, vp, vp]
+        L.kvq_quantize_nearest.restype = C.c_int
+        L.kvq_quantize_nearest.argtypes = [vp, _Layout, vp, vp, vp, vp, vp]
         L.kvq_attention_workspace_bytes.restype = C.c_size_t
         L.kvq_attention_workspace_bytes.argtypes = [_Layout, C.c_int]
         L.kvq_decode_attention.restype = C.c_int
@@ -191,6 +195,19 @@ def kvq_quantize(x, L: Layout, codebook, k, seed: int, index_base: int, codes, s
 def kvq_dequantize(codes, codebook, L: Layout, y, stream=None):
     _check(lib().kvq_dequantize(_ptr(codes), _ptr(codebook), L.c(), _ptr(y), _stream(stream)),
            "kvq_dequantize")
+
+
+def kvq_uniform_codebook(x, L: Layout, codebook, k, status, stream=None):
+    """Uniform comparator codebooks (see include/kvq.h)."""
+    _check(lib().kvq_uniform_codebook(_ptr(x), L.c(), _ptr(codebook), _ptr(k), _ptr(status),
+                                      _stream(stream)), "kvq_uniform_codebook")
+
+
+def kvq_quantize_nearest(x, L: Layout, codebook, k, codes, status=None, stream=None):
+    """Round every entry to the nearest level of its block's codebook."""
+    _check(lib().kvq_quantize_nearest(_ptr(x), L.c(), _ptr(codebook), _ptr(k), _ptr(codes),
+                                      _ptr(status) if status is not None else None,
+                                      _stream(stream)), "kvq_quantize_nearest")
 
 
 def kvq_attention_workspace_bytes(L: Layout, n_rep: int) -> int:
