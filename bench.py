@@ -235,6 +235,38 @@ def comparator_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep,
             "uniform_int4_GBps": (x.numel() * 2 + x.numel() // 2 + nb * 65) / (t_u * 1e-3) / 1e9}
 
 
+def entropy_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev):
+    """The layer's codes entropy-coded (kvq_entropy_encode): stored bits per
+    entry against the rate the allocation targets, and the coder's times
+    (L2 flushed before each launch)."""
+    import torch
+    from rate_adaptive_kv_block_b300 import kvq
+    nb = L.nblocks
+    cap = kvq.kvq_entropy_slot_bytes(L)
+    out = torch.zeros((nb, cap), dtype=torch.uint8, device=dev)
+    nbytes = torch.zeros(nb, dtype=torch.int32, device=dev)
+    back = torch.empty_like(buf.codes)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    g_e = graph_of(lambda: (flush_l2(1), kvq.kvq_entropy_encode(buf.codes, L, out, nbytes)))
+    g_d = graph_of(lambda: (flush_l2(1), kvq.kvq_entropy_decode(out, L, back, st)))
+    device_ms(g_e, 2)
+    device_ms(g_d, 2)
+    t_e = device_ms(g_e, nrep) - t_flush
+    t_d = device_ms(g_d, nrep) - t_flush
+    torch.cuda.synchronize()
+    assert torch.equal(back, buf.codes) and int(st.item()) == 0
+    stored = float(nbytes.double().sum())
+    n = x.numel()
+    return {"what": "the layer's 4-bit codes entropy-coded per block (rANS, exact counts, 32 "
+                    "streams per block); bits per entry include the 96-byte block headers, not "
+                    "the 64-byte codebooks",
+            "stored_bits_per_entry": stored * 8 / n, "rate_target_bits": float(buf.totals[0]) / n,
+            "packed_bits_per_entry": 4.0,
+            "encode_ms": t_e, "decode_ms": t_d,
+            "encode_GBps_of_codes": (n / 2) / (t_e * 1e-3) / 1e9,
+            "decode_GBps_of_codes": (n / 2) / (t_d * 1e-3) / 1e9}
+
+
 def attention_bench(w, L, buf, flush_l2, graph_of, device_ms, t_flush, nrep, hbm, src, dev):
     """kvq_decode_attention on the quantized layer, L2 flushed before every
     launch: its time, the bytes it must read (codes, codebooks, queries) and
@@ -457,6 +489,7 @@ def main():
     # of the same cache (a library kernel, for context)
     att = attention_bench(w, L, buf, flush_l2, graph_of, device_ms, t_flush, nrep, *peaks(), dev)
     comp = comparator_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev)
+    ent = entropy_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev)
 
     # End to end through the C ABI from pinned host memory, pipelined over
     # three streams the way a serving loop would run it: step i's input copy
@@ -538,6 +571,7 @@ def main():
         "fused_allocate_quantize_cold_ms": t_fcold,
         "decode_attention": att,
         "comparators": comp,
+        "entropy_coding": ent,
         "cold_method": "graph (L2 flush + kernel) minus graph (L2 flush), device-timed",
         "stats_cold_GBps": s_bytes / (t_scold * 1e-3) / 1e9,
         "quantize_cold_GBps": q_bytes / (t_qcold * 1e-3) / 1e9,

@@ -49,6 +49,7 @@ extern "C" {
 #define KVQ_ERR_INFEASIBLE 4  /* device status: budget unreachable         */
 #define KVQ_ERR_TOO_LARGE 5   /* kvq_allocate_static: layout over its limit  */
 #define KVQ_ERR_TIMEOUT 6     /* device status: a grid-wide wait gave up     */
+#define KVQ_ERR_CORRUPT 7     /* device status: an entropy-coded slot is malformed */
 
 /* lambda modes of kvq_allocate */
 #define KVQ_BISECT40 0        /* global lambda by the 40-step bisection      */
@@ -250,6 +251,38 @@ int kvq_uniform_codebook(const uint16_t *x, kvq_layout L, float *codebook, uint8
  */
 int kvq_quantize_nearest(const uint16_t *x, kvq_layout L, const float *codebook, const uint8_t *k,
                          uint8_t *codes, int32_t *status, void *stream);
+
+/*
+ * Entropy coding of the symbol stream ("Implementation notes": store the
+ * codebook, symbol stream and block lengths, arithmetic coding of the
+ * symbols): every block's 4-bit codes as 32 interleaved rANS streams (32-bit
+ * state, byte renormalisation, L = 2^23) modelled by the block's exact symbol
+ * counts (total d = 32 * group, a power of two), in a slot of fixed capacity
+ * kvq_entropy_slot_bytes(L) = d/2 + 288 bytes:
+ *   [0, 32)   16 x u16 little-endian: count of each symbol
+ *   [32, 96)  32 x u16: bytes of stream l (entries l, l+32, .. of the block)
+ *   [96, ..)  the streams in order; each = the encoder's final state (4
+ *             bytes, little-endian), then its renormalisation bytes in the
+ *             order the decoder reads them.
+ * kvq_entropy_encode
+ *   codes   device [nblocks][d/2] packed codes (kvq_quantize's), read.
+ *   out     device [nblocks][slot bytes], written (bytes past a block's size
+ *           are left as they were).
+ *   nbytes  device u32 [nblocks]: the block's stored size 96 + sum of its
+ *           stream lengths, written.
+ * kvq_entropy_decode
+ *   in      device slots as written by kvq_entropy_encode, read.
+ *   codes   device [nblocks][d/2], written: the codes that were encoded.
+ *   status  device int32, written: KVQ_OK, or KVQ_ERR_CORRUPT if a slot's
+ *           counts do not add up to d, its streams overrun the slot, or a
+ *           stream ends before or after its symbols (that block's codes are
+ *           then unspecified; no byte outside the slot is read).
+ */
+size_t kvq_entropy_slot_bytes(kvq_layout L);
+int kvq_entropy_encode(const uint8_t *codes, kvq_layout L, uint8_t *out, uint32_t *nbytes,
+                       void *stream);
+int kvq_entropy_decode(const uint8_t *in, kvq_layout L, uint8_t *codes, int32_t *status,
+                       void *stream);
 
 /*
  * kvq_decode_attention -- one decoding step of attention over the quantized

@@ -297,6 +297,76 @@ def quantize_nearest(x, G, codebook, k):
     return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
 
 
+RANS_L = 1 << 23
+
+
+def _unpack(codes_row):
+    c = np.asarray(codes_row, dtype=np.uint8)
+    out = np.empty(2 * len(c), dtype=np.int64)
+    out[0::2], out[1::2] = c & 15, c >> 4
+    return out
+
+
+def entropy_encode(codes, d):
+    """Entropy coding of every block's symbols ("Rate-adaptive KV-cache
+    quantizer", "Implementation notes": arithmetic coding of the symbol
+    stream): rANS (Duda 2013) with 32-bit state in [L, 256 L), L = 2^23, byte
+    renormalisation, the block's exact symbol counts as the model (total d);
+    32 streams, stream l = entries l, l+32, ..; each stream stored as the
+    encoder's final state (4 bytes little-endian) then its renormalisation
+    bytes in reverse order of emission.  Slot = 16 u16 counts, 32 u16 stream
+    lengths, the streams.  Returns a list of bytes objects (one per block)."""
+    lg = int(d).bit_length() - 1
+    n = d // 32
+    slots = []
+    for row in np.asarray(codes, dtype=np.uint8):
+        sym = _unpack(row)
+        cnt = np.bincount(sym, minlength=16)
+        cum = np.concatenate([[0], np.cumsum(cnt)])
+        streams = []
+        for lane in range(32):
+            x, emitted = RANS_L, []
+            for j in range(n - 1, -1, -1):
+                c = int(sym[lane + 32 * j])
+                f, bc = int(cnt[c]), int(cum[c])
+                xmax = ((RANS_L >> lg) << 8) * f
+                while x >= xmax:
+                    emitted.append(x & 255)
+                    x >>= 8
+                x = ((x // f) << lg) + (x % f) + bc
+            streams.append(bytes([x & 255, (x >> 8) & 255, (x >> 16) & 255, (x >> 24) & 255]
+                                 + emitted[::-1]))
+        head = b"".join(int(v).to_bytes(2, "little") for v in cnt)
+        head += b"".join(len(st).to_bytes(2, "little") for st in streams)
+        slots.append(head + b"".join(streams))
+    return slots
+
+
+def entropy_decode(slot, d):
+    """The packed codes [d/2] of one slot written by entropy_encode."""
+    lg = int(d).bit_length() - 1
+    n = d // 32
+    cnt = [int.from_bytes(slot[2 * t:2 * t + 2], "little") for t in range(16)]
+    cum = np.concatenate([[0], np.cumsum(cnt)])
+    lens = [int.from_bytes(slot[32 + 2 * l:34 + 2 * l], "little") for l in range(32)]
+    sym = np.zeros(d, dtype=np.int64)
+    p = 96
+    for lane in range(32):
+        st = slot[p:p + lens[lane]]
+        p += lens[lane]
+        x = int.from_bytes(st[:4], "little")
+        q = 4
+        for j in range(n):
+            s = x & (d - 1)
+            c = int(np.searchsorted(cum, s, side="right") - 1)
+            x = cnt[c] * (x >> lg) + s - int(cum[c])
+            while x < RANS_L:
+                x = (x << 8) | st[q]
+                q += 1
+            sym[lane + 32 * j] = c
+    return (sym[0::2] | (sym[1::2] << 4)).astype(np.uint8)
+
+
 def decode_attention(q, k_codes, k_codebook, v_codes, v_codebook, S, T, D, G, n_rep, T_valid,
                      scale):
     """One decoding step of attention over the stored cache, in fp64 ("Rate-

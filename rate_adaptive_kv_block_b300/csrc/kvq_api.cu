@@ -29,6 +29,11 @@ int launch_decode_attention(const float *q, int n_rep, const kvq_layout &L, cons
                             int64_t T_valid, float scale, void *workspace, float *out,
                             int32_t *status, cudaStream_t st);
 int attention_init();
+int launch_entropy_encode(const uint8_t *codes, const kvq_layout &L, uint8_t *out,
+                          uint32_t *nbytes, cudaStream_t st);
+int launch_entropy_decode(const uint8_t *in, const kvq_layout &L, uint8_t *codes, int32_t *status,
+                          cudaStream_t st);
+size_t entropy_slot(const kvq_layout &L);
 int allocate_init();
 int allocate_report(const void *workspace, kvq_report *r);
 
@@ -232,6 +237,25 @@ int kvq_dequantize(const uint8_t *codes, const float *codebook, kvq_layout L, ui
     return launch_dequantize(codes, codebook, L, y, static_cast<cudaStream_t>(stream));
 }
 
+size_t kvq_entropy_slot_bytes(kvq_layout L) {
+    if (!layout_ok(L)) return 0;
+    return entropy_slot(L);
+}
+
+int kvq_entropy_encode(const uint8_t *codes, kvq_layout L, uint8_t *out, uint32_t *nbytes,
+                       void *stream) {
+    if (!layout_ok(L)) return KVQ_ERR_INVALID_ARG;
+    if (num_blocks(L) > 0 && (!codes || !out || !nbytes)) return KVQ_ERR_INVALID_ARG;
+    return launch_entropy_encode(codes, L, out, nbytes, static_cast<cudaStream_t>(stream));
+}
+
+int kvq_entropy_decode(const uint8_t *in, kvq_layout L, uint8_t *codes, int32_t *status,
+                       void *stream) {
+    if (!layout_ok(L)) return KVQ_ERR_INVALID_ARG;
+    if (!status || (num_blocks(L) > 0 && (!in || !codes))) return KVQ_ERR_INVALID_ARG;
+    return launch_entropy_decode(in, L, codes, status, static_cast<cudaStream_t>(stream));
+}
+
 static bool attention_layout_ok(const kvq_layout &L, int n_rep) {
     return layout_ok(L) && L.D == 128 && (n_rep == 1 || n_rep == 2 || n_rep == 4) &&
            L.S <= 65535 && L.S * n_rep <= 0x7fffffffll;
@@ -277,6 +301,7 @@ const char *kvq_status_string(int status) {
     case KVQ_ERR_INFEASIBLE: return "budget infeasible";
     case KVQ_ERR_TIMEOUT: return "device wait timed out";
     case KVQ_ERR_TOO_LARGE: return "layout needs more scratch than the static workspace holds";
+    case KVQ_ERR_CORRUPT: return "malformed entropy-coded slot";
     default: return "unknown status";
     }
 }

@@ -22,6 +22,7 @@ KVQ_ERR_NONFINITE = 3
 KVQ_ERR_INFEASIBLE = 4
 KVQ_ERR_TOO_LARGE = 5
 KVQ_ERR_TIMEOUT = 6
+KVQ_ERR_CORRUPT = 7
 KVQ_STATIC_WORKSPACE_BYTES = 8 << 20
 KVQ_BISECT40 = 0
 KVQ_SUBGRADIENT = 1
@@ -104,6 +105,12 @@ def lib():
         L.kvq_uniform_codebook.argtypes = [vp, _Layout, vp, vp, vp, vp]
         L.kvq_quantize_nearest.restype = C.c_int
         L.kvq_quantize_nearest.argtypes = [vp, _Layout, vp, vp, vp, vp, vp]
+        L.kvq_entropy_slot_bytes.restype = C.c_size_t
+        L.kvq_entropy_slot_bytes.argtypes = [_Layout]
+        L.kvq_entropy_encode.restype = C.c_int
+        L.kvq_entropy_encode.argtypes = [vp, _Layout, vp, vp, vp]
+        L.kvq_entropy_decode.restype = C.c_int
+        L.kvq_entropy_decode.argtypes = [vp, _Layout, vp, vp, vp]
         L.kvq_attention_workspace_bytes.restype = C.c_size_t
         L.kvq_attention_workspace_bytes.argtypes = [_Layout, C.c_int]
         L.kvq_decode_attention.restype = C.c_int
@@ -208,6 +215,22 @@ def kvq_quantize_nearest(x, L: Layout, codebook, k, codes, status=None, stream=N
     _check(lib().kvq_quantize_nearest(_ptr(x), L.c(), _ptr(codebook), _ptr(k), _ptr(codes),
                                       _ptr(status) if status is not None else None,
                                       _stream(stream)), "kvq_quantize_nearest")
+
+
+def kvq_entropy_slot_bytes(L: Layout) -> int:
+    return int(lib().kvq_entropy_slot_bytes(L.c()))
+
+
+def kvq_entropy_encode(codes, L: Layout, out, nbytes, stream=None):
+    """Entropy-code every block's codes into its fixed-capacity slot."""
+    _check(lib().kvq_entropy_encode(_ptr(codes), L.c(), _ptr(out), _ptr(nbytes), _stream(stream)),
+           "kvq_entropy_encode")
+
+
+def kvq_entropy_decode(inp, L: Layout, codes, status, stream=None):
+    """Decode the slots of kvq_entropy_encode back into packed codes."""
+    _check(lib().kvq_entropy_decode(_ptr(inp), L.c(), _ptr(codes), _ptr(status), _stream(stream)),
+           "kvq_entropy_decode")
 
 
 def kvq_attention_workspace_bytes(L: Layout, n_rep: int) -> int:

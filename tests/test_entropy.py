@@ -1,0 +1,114 @@
+"""Entropy coding of the symbol stream (kvq_entropy_encode / kvq_entropy_decode)
+and its oracle (oracle.entropy_encode / entropy_decode): rANS with the block's
+exact symbol counts.
+
+Oracle pins: decoding gives back the symbols (skewed, uniform, one-symbol and
+gap-ridden distributions); the stored bytes are within the rANS bounds of the
+block's empirical entropy: d H / 8 <= payload <= d H / 8 + 6 bytes per
+stream (state and renormalisation slack).  GPU: the slots (their stored
+bytes) and sizes equal the oracle's byte for byte, decode inverts encode, and
+a damaged slot is reported without reading outside it.
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def _pack(sym):
+    sym = np.asarray(sym, dtype=np.uint8)
+    return (sym[..., 0::2] | (sym[..., 1::2] << 4)).astype(np.uint8)
+
+
+def _entropy_bits(sym):
+    n = np.bincount(sym, minlength=16)
+    p = n[n > 0] / len(sym)
+    return float(-(n[n > 0] * np.log2(p)).sum())
+
+
+CASES = {
+    "skewed": lambda r, d: np.minimum(r.geometric(0.45, d) - 1, 15),
+    "uniform16": lambda r, d: r.permutation(np.repeat(np.arange(16), d // 16)),
+    "one_symbol": lambda r, d: np.full(d, 7),
+    "gaps": lambda r, d: r.choice([0, 3, 15], size=d, p=[0.7, 0.2, 0.1]),
+    "rare": lambda r, d: np.where(r.random(d) < 0.002, 13, 2),
+}
+
+
+@pytest.mark.parametrize("d", [4096, 1024, 256])
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_oracle_round_trip_and_size_bounds(case, d):
+    r = np.random.default_rng(zlib.crc32(("%s/%d" % (case, d)).encode()))
+    sym = CASES[case](r, d).astype(np.int64)
+    codes = _pack(sym)[None, :]
+    slot = oracle.entropy_encode(codes, d)[0]
+    assert np.array_equal(oracle.entropy_decode(slot, d), codes[0])
+    payload = len(slot) - 96
+    h = _entropy_bits(sym)
+    assert h / 8 <= payload + 1e-9
+    assert payload <= h / 8 + 32 * 6
+    if case == "uniform16":
+        assert abs(payload - d / 2) <= 32 * 6          # exactly 4 bits a symbol, plus the states
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,T,S,G", [("llama3_8b_layer", 256, 16, 128),
+                                        ("hadamard_groups", 256, 8, 32),
+                                        ("k_head_small", 128, 4, 8)])
+def test_entropy_coder_matches_oracle_and_round_trips(name, T, S, G):
+    import torch
+    from rate_adaptive_kv_block_b300 import kvq, synth
+    w = synth.workload(name, T=T, S=S)
+    x = synth.make_torch(w, seed=2, device="cuda")
+    L = kvq.Layout(w.S, w.T, w.D, G)
+    buf = kvq.Buffers(L, 16)
+    kvq.quantize(x, L, 2.5 * w.entries, 16, buf=buf)
+    nb, d = L.nblocks, 32 * G
+    cap = kvq.kvq_entropy_slot_bytes(L)
+    assert cap == d // 2 + 288
+    out = torch.zeros((nb, cap), dtype=torch.uint8, device="cuda")
+    nbytes = torch.zeros(nb, dtype=torch.int32, device="cuda")
+    kvq.kvq_entropy_encode(buf.codes, L, out, nbytes)
+    back = torch.empty_like(buf.codes)
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    kvq.kvq_entropy_decode(out, L, back, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvq.KVQ_OK
+    assert torch.equal(back, buf.codes)
+    want = oracle.entropy_encode(buf.codes.cpu().numpy(), d)
+    got, sizes = out.cpu().numpy(), nbytes.cpu().numpy()
+    for b in range(nb):
+        assert sizes[b] == len(want[b])
+        assert bytes(got[b, :sizes[b]]) == want[b]
+
+
+@pytest.mark.gpu
+def test_entropy_decode_reports_a_damaged_slot():
+    import torch
+    from rate_adaptive_kv_block_b300 import kvq, synth
+    w = synth.workload("llama3_8b_layer", T=64, S=4)
+    x = synth.make_torch(w, seed=3, device="cuda")
+    L = kvq.Layout(w.S, w.T, w.D, w.G)
+    buf = kvq.Buffers(L, 16)
+    kvq.quantize(x, L, 2.5 * w.entries, 16, buf=buf)
+    cap = kvq.kvq_entropy_slot_bytes(L)
+    out = torch.zeros((L.nblocks, cap), dtype=torch.uint8, device="cuda")
+    nbytes = torch.zeros(L.nblocks, dtype=torch.int32, device="cuda")
+    kvq.kvq_entropy_encode(buf.codes, L, out, nbytes)
+    torch.cuda.synchronize()
+    back = torch.empty_like(buf.codes)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for damage in ("counts", "lengths", "stream"):
+        bad = out.clone()
+        if damage == "counts":
+            bad[1, 0] ^= 1                      # counts no longer add up to d
+        elif damage == "lengths":
+            bad[2, 33] = 0xFF                   # a stream longer than the slot
+        else:
+            bad[3, 32] = 3                      # stream 0 shorter than its state
+            bad[3, 33] = 0
+        kvq.kvq_entropy_decode(bad, L, back, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == kvq.KVQ_ERR_CORRUPT, damage
