@@ -245,14 +245,16 @@ size_t kvq_entropy_slot_bytes(kvq_layout L) {
 int kvq_entropy_encode(const uint8_t *codes, kvq_layout L, uint8_t *out, uint32_t *nbytes,
                        void *stream) {
     if (!layout_ok(L)) return KVQ_ERR_INVALID_ARG;
-    if (num_blocks(L) > 0 && (!codes || !out || !nbytes)) return KVQ_ERR_INVALID_ARG;
+    if (num_blocks(L) > 0 && (!codes || !out || !nbytes || !aligned16(codes) || !aligned16(out)))
+        return KVQ_ERR_INVALID_ARG;
     return launch_entropy_encode(codes, L, out, nbytes, static_cast<cudaStream_t>(stream));
 }
 
 int kvq_entropy_decode(const uint8_t *in, kvq_layout L, uint8_t *codes, int32_t *status,
                        void *stream) {
     if (!layout_ok(L)) return KVQ_ERR_INVALID_ARG;
-    if (!status || (num_blocks(L) > 0 && (!in || !codes))) return KVQ_ERR_INVALID_ARG;
+    if (!status || (num_blocks(L) > 0 && (!in || !codes || !aligned16(in) || !aligned16(codes))))
+        return KVQ_ERR_INVALID_ARG;
     return launch_entropy_decode(in, L, codes, status, static_cast<cudaStream_t>(stream));
 }
 

@@ -46,7 +46,7 @@ __device__ __forceinline__ int ilog2(int v) { return 31 - __clz(v); }
 
 // symbol of slot s: the c with b_c <= s < b_{c+1} (cum[0] = 0, cum[16] = d;
 // symbols with count 0 have b_c = b_{c+1} and are never found)
-__device__ __forceinline__ int rans_symbol(const uint32_t (&cum)[17], uint32_t s) {
+__device__ __forceinline__ int rans_symbol(const uint32_t *cum, uint32_t s) {
     int c = 0;
 #pragma unroll
     for (int step = 8; step > 0; step >>= 1)
@@ -54,15 +54,38 @@ __device__ __forceinline__ int rans_symbol(const uint32_t (&cum)[17], uint32_t s
     return c;
 }
 
+// x / f for x < 2^31 and 1 <= f <= 4096 by one 64-bit product: with
+// l = ceil(log2 f) and m = floor(2^(31+l) / f) + 1 (at most 32 bits),
+// floor(x m / 2^(31+l)) = floor(x / f) for every 31-bit x (Granlund and
+// Montgomery 1994, Theorem 4.2)
+struct Recip {
+    uint32_t m;
+    uint32_t sh;
+};
+__device__ __forceinline__ Recip recip_of(uint32_t f) {
+    const uint32_t l = f > 1 ? 32u - __clz(f - 1u) : 0u;
+    const uint64_t m = ((1ull << (31 + l)) / f) + 1ull;
+    return Recip{(uint32_t)m, 31u + l};
+}
+__device__ __forceinline__ uint32_t div_by(uint32_t x, Recip r) {
+    return (uint32_t)(((uint64_t)x * r.m) >> r.sh);
+}
+
 __global__ void __launch_bounds__(kEntWarps * 32)
 entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
                       uint8_t *__restrict__ out, uint32_t *__restrict__ nbytes) {
     __shared__ uint8_t scratch[kEntWarps][32][kEntLaneCap];
+    __shared__ __align__(16) uint8_t sslot[kEntWarps][entropy_slot_bytes(4096)];
+    __shared__ uint4 smodel[kEntWarps][16];        // per symbol: count, cumulative, reciprocal
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t b = (int64_t)blockIdx.x * kEntWarps + w;
     if (b >= nb) return;
     const int n = d / 32, lg = ilog2(d);
-    const uint8_t *cb = codes + b * (d / 2);
+    // the block's codes in shared memory (coalesced 16-byte loads)
+    uint8_t *cb = sslot[w];
+    for (int i = lane; i < d / 32; i += 32)
+        reinterpret_cast<uint4 *>(cb)[i] = reinterpret_cast<const uint4 *>(codes + b * (d / 2))[i];
+    __syncwarp();
     // the block's counts (lane-private, then a warp sum)
     uint32_t cnt[16];
 #pragma unroll
@@ -81,23 +104,40 @@ entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     cum[0] = 0;
 #pragma unroll
     for (int t = 0; t < 16; ++t) cum[t + 1] = cum[t] + cnt[t];
+    // the model, one entry per symbol in shared memory (lane t < 16: its
+    // count, cumulative count and the count's reciprocal, a 64-bit division
+    // once per block)
+    if (lane < 16) {
+        uint32_t f = 0, bc = 0;
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            if (t == lane) { f = cnt[t]; bc = cum[t]; }
+        const Recip r = recip_of(f > 0 ? f : 1u);
+        smodel[w][lane] = make_uint4(f, bc, r.m, r.sh);
+    }
+    // the symbols of this lane's stream (the codes' buffer is reused for the
+    // slot below)
+    uint8_t mysym[4096 / 32];
+    for (int j = 0; j < n; ++j) {
+        const int e = lane + 32 * j;
+        mysym[j] = (cb[e >> 1] >> ((e & 1) * 4)) & 15;
+    }
+    __syncwarp();
     // this lane's stream, last entry first, bytes written downwards
     uint8_t *buf = scratch[w][lane];
     int pos = kEntLaneCap;
     uint32_t x = kRansL;
     for (int j = n - 1; j >= 0; --j) {
-        const int e = lane + 32 * j;
-        const int c = (cb[e >> 1] >> ((e & 1) * 4)) & 15;
-        uint32_t f = 0, bc = 0;
-#pragma unroll
-        for (int t = 0; t < 16; ++t)
-            if (t == c) { f = cnt[t]; bc = cum[t]; }
+        const uint4 md = smodel[w][mysym[j]];
+        const uint32_t f = md.x, bc = md.y;
+        const Recip r{md.z, md.w};
         const uint32_t xmax = ((kRansL >> lg) << 8) * f;
         while (x >= xmax) {
             buf[--pos] = (uint8_t)(x & 255u);
             x >>= 8;
         }
-        x = ((x / f) << lg) + (x % f) + bc;
+        const uint32_t qd = div_by(x, r);
+        x = (qd << lg) + (x - qd * f) + bc;
     }
     pos -= 4;
     buf[pos] = (uint8_t)x;
@@ -114,34 +154,62 @@ entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     }
     const uint32_t total = __shfl_sync(0xffffffffu, off, 31);
     off -= len;
-    uint8_t *slot = out + b * (int64_t)entropy_slot_bytes(d);
+    // the slot assembled in shared memory, then stored with 16-byte writes
+    uint8_t *ss = sslot[w];
     if (lane < 16) {
-        slot[2 * lane] = (uint8_t)cnt[lane];
-        slot[2 * lane + 1] = (uint8_t)(cnt[lane] >> 8);
+        ss[2 * lane] = (uint8_t)cnt[lane];
+        ss[2 * lane + 1] = (uint8_t)(cnt[lane] >> 8);
     }
-    slot[32 + 2 * lane] = (uint8_t)len;
-    slot[32 + 2 * lane + 1] = (uint8_t)(len >> 8);
-    for (uint32_t i = 0; i < len; ++i) slot[kEntHeader + off + i] = buf[pos + i];
-    if (lane == 0) nbytes[b] = kEntHeader + total;
+    ss[32 + 2 * lane] = (uint8_t)len;
+    ss[32 + 2 * lane + 1] = (uint8_t)(len >> 8);
+    for (uint32_t i = 0; i < len; ++i) ss[kEntHeader + off + i] = buf[pos + i];
+    __syncwarp();
+    const uint32_t size = kEntHeader + total;
+    uint8_t *slot = out + b * (int64_t)entropy_slot_bytes(d);
+    for (uint32_t i = 16 * lane; i < size; i += 16 * 32) {
+        if (i + 16 <= size) {
+            *reinterpret_cast<uint4 *>(slot + i) = *reinterpret_cast<const uint4 *>(ss + i);
+        } else {
+            for (uint32_t k = i; k < size; ++k) slot[k] = ss[k];
+        }
+    }
+    if (lane == 0) nbytes[b] = size;
 }
 
 __global__ void __launch_bounds__(kEntWarps * 32)
 entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
                       uint8_t *__restrict__ codes, int32_t *__restrict__ status) {
     __shared__ uint8_t sym[kEntWarps][4096];
+    __shared__ __align__(16) uint8_t sslot[kEntWarps][entropy_slot_bytes(4096)];
+    __shared__ uint32_t scum[kEntWarps][17], scnt[kEntWarps][16];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t b = (int64_t)blockIdx.x * kEntWarps + w;
     if (b >= nb) return;
     const int n = d / 32, lg = ilog2(d);
     const uint32_t cap = entropy_slot_bytes(d);
-    const uint8_t *slot = in + b * (int64_t)cap;
-    uint32_t cnt[16], cum[17];
-    cum[0] = 0;
+    // the whole slot in shared memory (16-byte loads; the capacity is a
+    // multiple of 16)
+    for (uint32_t i = lane; i < cap / 16; i += 32)
+        reinterpret_cast<uint4 *>(sslot[w])[i] =
+            reinterpret_cast<const uint4 *>(in + b * (int64_t)cap)[i];
+    __syncwarp();
+    const uint8_t *slot = sslot[w];
+    // counts and cumulative counts in shared memory (lane t < 16 reads
+    // count t; a warp scan gives the cumulative counts)
+    uint32_t mycnt = lane < 16 ? ((uint32_t)slot[2 * lane] | ((uint32_t)slot[2 * lane + 1] << 8)) : 0u;
+    uint32_t incl = mycnt;
 #pragma unroll
-    for (int t = 0; t < 16; ++t) {
-        cnt[t] = (uint32_t)slot[2 * t] | ((uint32_t)slot[2 * t + 1] << 8);
-        cum[t + 1] = cum[t] + cnt[t];
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
     }
+    if (lane < 16) {
+        scnt[w][lane] = mycnt;
+        scum[w][lane] = incl - mycnt;
+    }
+    if (lane == 16) scum[w][16] = incl;            // lanes >= 16 add nothing: the total
+    __syncwarp();
+    const uint32_t *cum = scum[w];
     const uint32_t len = (uint32_t)slot[32 + 2 * lane] | ((uint32_t)slot[32 + 2 * lane + 1] << 8);
     uint32_t off = len;
 #pragma unroll
@@ -167,10 +235,7 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
         if (!bad) {
             const uint32_t s = x & ((1u << lg) - 1u);
             c = rans_symbol(cum, s);
-            uint32_t f = 0, bc = 0;
-#pragma unroll
-            for (int t = 0; t < 16; ++t)
-                if (t == c) { f = cnt[t]; bc = cum[t]; }
+            const uint32_t f = scnt[w][c], bc = cum[c];
             x = f * (x >> lg) + s - bc;
             while (x < kRansL) {
                 if (p >= end) { overrun = true; break; }   // never reads past its stream
