@@ -40,24 +40,24 @@ def lib():
         L.kvqo_flat_index.restype = i64
         L.kvqo_flat_index.argtypes = [i64, C.c_int, C.c_int, i64, C.c_int]
         L.kvqo_stats.restype = None
-        L.kvqo_stats.argtypes = [vp, i64, i64, C.c_int, C.c_int, i64, i64,
+        L.kvqo_stats.argtypes = [vp, vp, i64, i64, C.c_int, C.c_int, i64, i64,
                                  vp, vp, vp, vp]
         L.kvqo_allocate_bisect.restype = C.c_int
-        L.kvqo_allocate_bisect.argtypes = [vp, i64, i64, C.c_int, C.c_int, vp,
+        L.kvqo_allocate_bisect.argtypes = [vp, vp, i64, i64, C.c_int, C.c_int, vp,
                                            i64, C.c_int, dbl, vp, vp, vp, vp,
                                            vp, vp, vp, vp, vp]
         L.kvqo_allocate_at.restype = C.c_int
-        L.kvqo_allocate_at.argtypes = [vp, i64, i64, C.c_int, C.c_int, vp, i64,
+        L.kvqo_allocate_at.argtypes = [vp, vp, i64, i64, C.c_int, C.c_int, vp, i64,
                                        C.c_int, dbl, dbl, dbl, vp, vp, vp, vp,
                                        vp, vp, vp, vp]
         L.kvqo_rate_at.restype = dbl
-        L.kvqo_rate_at.argtypes = [vp, i64, i64, C.c_int, C.c_int, vp, i64,
+        L.kvqo_rate_at.argtypes = [vp, vp, i64, i64, C.c_int, C.c_int, vp, i64,
                                    C.c_int, dbl]
         L.kvqo_block_tables.restype = C.c_int
-        L.kvqo_block_tables.argtypes = [vp, i64, C.c_int, C.c_int, i64, vp, vp,
+        L.kvqo_block_tables.argtypes = [vp, vp, i64, C.c_int, C.c_int, i64, vp, vp,
                                         vp, vp]
         L.kvqo_chain_cost.restype = None
-        L.kvqo_chain_cost.argtypes = [vp, i64, C.c_int, C.c_int, i64,
+        L.kvqo_chain_cost.argtypes = [vp, vp, i64, C.c_int, C.c_int, i64,
                                       C.c_uint32, vp, vp]
         L.kvqo_quantize.restype = None
         L.kvqo_quantize.argtypes = [vp, i64, i64, C.c_int, C.c_int, vp, vp, u64,
@@ -79,6 +79,15 @@ def _x(x):
         x = x.view(np.uint16)
     assert x.dtype == np.uint16 and x.ndim == 3, "x must be [S,T,D] binary16"
     return x
+
+
+def _w(w, x):
+    """Per-entry weights (float32, the shape of x) or None (unweighted)."""
+    if w is None:
+        return None
+    w = np.ascontiguousarray(np.asarray(w, dtype=np.float32))
+    assert w.shape == x.shape, "weights must have the shape of x"
+    return w
 
 
 def _ids(ids):
@@ -119,9 +128,12 @@ def flat_index(T, D, G, b, e) -> int:
     return lib().kvqo_flat_index(T, D, G, b, e)
 
 
-def stats(x, G, b0=0, nb=None):
-    """Candidates, m', atom moments (n, s1, t1, e) and the non-finite flag."""
+def stats(x, G, b0=0, nb=None, w=None):
+    """Candidates, m', atom moments (n, s1, t1, e) and the flags (bit 0: a
+    non-finite value, bit 1: an invalid weight).  With per-entry weights w the
+    moments are weighted (n = sum w, s1 = sum w (x - c_p), ...)."""
     x = _x(x)
+    w = _w(w, x)
     S, T, D = x.shape
     if nb is None:
         nb = num_blocks(S, T, D, G) - b0
@@ -129,8 +141,8 @@ def stats(x, G, b0=0, nb=None):
     mp = np.zeros(nb, dtype=np.int32)
     atoms = np.zeros((nb, 16, 4))
     bad = np.zeros(nb, dtype=np.int32)
-    lib().kvqo_stats(_p(x), S, T, D, G, b0, nb, _p(cand), _p(mp), _p(atoms),
-                     _p(bad))
+    lib().kvqo_stats(_p(x), _p(w), S, T, D, G, b0, nb, _p(cand), _p(mp),
+                     _p(atoms), _p(bad))
     return {"cand": cand, "mprime": mp, "atoms": atoms, "nonfinite": bad}
 
 
@@ -146,11 +158,12 @@ def _alloc_out(nb):
     }
 
 
-def allocate_bisect(x, G, s, budget_bits, ids=None):
+def allocate_bisect(x, G, s, budget_bits, ids=None, w=None):
     """Global lambda by the 40-step bisection, and the per-block choice there.
     Returns a dict with lambda, bracket (lo, hi), status and per-block arrays
-    (ids order)."""
+    (ids order).  w: per-entry distortion weights (None: unweighted)."""
     x = _x(x)
+    w = _w(w, x)
     S, T, D = x.shape
     ids = _ids(ids)
     nb = num_blocks(S, T, D, G) if ids is None else len(ids)
@@ -158,7 +171,7 @@ def allocate_bisect(x, G, s, budget_bits, ids=None):
     lam = np.zeros(1)
     bracket = np.zeros(2)
     st = lib().kvqo_allocate_bisect(
-        _p(x), S, T, D, G, _p(ids), nb, s, float(budget_bits), _p(lam),
+        _p(x), _p(w), S, T, D, G, _p(ids), nb, s, float(budget_bits), _p(lam),
         _p(bracket), _p(out["codebook"]), _p(out["k"]), _p(out["D_r"]),
         _p(out["H_r"]), _p(out["gap"]), _p(out["mask"]), _p(out["totals"]))
     out.update(status=st, **{"lambda": float(lam[0])},
@@ -166,17 +179,18 @@ def allocate_bisect(x, G, s, budget_bits, ids=None):
     return out
 
 
-def allocate_at(x, G, s, lam, eta=0.0, budget_bits=0.0, ids=None):
+def allocate_at(x, G, s, lam, eta=0.0, budget_bits=0.0, ids=None, w=None):
     """Per-block choice at a fixed lambda; lambda_next is the subgradient
     update max(0, lambda + eta (R - budget_bits))."""
     x = _x(x)
+    w = _w(w, x)
     S, T, D = x.shape
     ids = _ids(ids)
     nb = num_blocks(S, T, D, G) if ids is None else len(ids)
     out = _alloc_out(nb)
     nxt = np.zeros(1)
     st = lib().kvqo_allocate_at(
-        _p(x), S, T, D, G, _p(ids), nb, s, float(lam), float(eta),
+        _p(x), _p(w), S, T, D, G, _p(ids), nb, s, float(lam), float(eta),
         float(budget_bits), _p(nxt), _p(out["codebook"]), _p(out["k"]),
         _p(out["D_r"]), _p(out["H_r"]), _p(out["gap"]), _p(out["mask"]),
         _p(out["totals"]))
@@ -184,32 +198,36 @@ def allocate_at(x, G, s, lam, eta=0.0, budget_bits=0.0, ids=None):
     return out
 
 
-def rate_at(x, G, s, lam, ids=None) -> float:
+def rate_at(x, G, s, lam, ids=None, w=None) -> float:
     x = _x(x)
+    w = _w(w, x)
     S, T, D = x.shape
     ids = _ids(ids)
     nb = num_blocks(S, T, D, G) if ids is None else len(ids)
-    return lib().kvqo_rate_at(_p(x), S, T, D, G, _p(ids), nb, s, float(lam))
+    return lib().kvqo_rate_at(_p(x), _p(w), S, T, D, G, _p(ids), nb, s, float(lam))
 
 
-def block_tables(x, G, b):
-    """(m', cand[17], Dpq, Mup, Mdn) of block b, each table 17x17."""
+def block_tables(x, G, b, w=None):
+    """(m', cand[17], Dpq, Mup, Mdn) of block b, each table 17x17 (Dpq
+    weighted when w is given)."""
     x = _x(x)
+    w = _w(w, x)
     S, T, D = x.shape
     cand = np.zeros(17)
     Dpq, Mup, Mdn = (np.zeros((17, 17)) for _ in range(3))
-    mp = lib().kvqo_block_tables(_p(x), T, D, G, b, _p(cand), _p(Dpq),
+    mp = lib().kvqo_block_tables(_p(x), _p(w), T, D, G, b, _p(cand), _p(Dpq),
                                  _p(Mup), _p(Mdn))
     return mp, cand, Dpq, Mup, Mdn
 
 
-def chain_cost(x, G, b, mask):
+def chain_cost(x, G, b, mask, w=None):
     """(D_r, d_r H_r) of the chain `mask` (bit j = candidate j) of block b."""
     x = _x(x)
+    w = _w(w, x)
     S, T, D = x.shape
     Dr = np.zeros(1)
     Rr = np.zeros(1)
-    lib().kvqo_chain_cost(_p(x), T, D, G, b, int(mask), _p(Dr), _p(Rr))
+    lib().kvqo_chain_cost(_p(x), _p(w), T, D, G, b, int(mask), _p(Dr), _p(Rr))
     return float(Dr[0]), float(Rr[0])
 
 

@@ -121,22 +121,47 @@ int64_t kvqo_flat_index(int64_t T, int D, int G, int64_t b, int e)
 /* merged, giving m' <= 17 strictly increasing levels.                       */
 /* ------------------------------------------------------------------------ */
 
-static int cmp_double(const void *a, const void *b)
+/* ------------------------------------------------------------------------ */
+/* Weights ("Implementation notes": D_r may be weighted by the attention     */
+/* sensitivity measured on a calibration batch).                             */
+/* Reading: the caller gives one weight w_e >= 0 per entry (fp32, the same   */
+/* [S,T,D] layout as x; NULL = every weight 1) and the block's distortion    */
+/* becomes D_r = sum_e w_e E[(hat x_e - x_e)^2]; the rate H_r stays the      */
+/* entropy of the unweighted expected codepoint frequencies, because it      */
+/* counts the stored symbols.  A weight that is negative, NaN or infinite is */
+/* reported (flag bit 1) and counted as 0.                                   */
+/* ------------------------------------------------------------------------ */
+
+typedef struct { double v, w; } kvqo_entry_t;
+
+static int cmp_entry(const void *a, const void *b)
 {
-    double x = *(const double *)a, y = *(const double *)b;
+    double x = ((const kvqo_entry_t *)a)->v, y = ((const kvqo_entry_t *)b)->v;
     return (x > y) - (x < y);
 }
 
-/* sorted values of block b; returns 1 if any value is NaN or infinite */
-static int block_sorted(const uint16_t *x, int64_t T, int D, int G, int64_t b,
-                        double *v)
+/* values (sorted) of block b with their weights carried along; returns bit 0
+ * if any value is NaN or infinite, bit 1 if any weight is invalid */
+static int block_sorted(const uint16_t *x, const float *wt, int64_t T, int D,
+                        int G, int64_t b, double *v, double *wv)
 {
     int d = 32 * G, bad = 0;
+    kvqo_entry_t *ent = (kvqo_entry_t *)malloc(sizeof(kvqo_entry_t) * d);
     for (int e = 0; e < d; e++) {
-        v[e] = kvqo_f16_to_double(x[kvqo_flat_index(T, D, G, b, e)]);
-        if (!isfinite(v[e])) { bad = 1; v[e] = 0.0; }
+        int64_t f = kvqo_flat_index(T, D, G, b, e);
+        double xv = kvqo_f16_to_double(x[f]);
+        double w = wt ? (double)wt[f] : 1.0;
+        if (!isfinite(xv)) { bad |= 1; xv = 0.0; }
+        if (!(w >= 0.0) || !isfinite(w)) { bad |= 2; w = 0.0; }
+        ent[e].v = xv;
+        ent[e].w = w;
     }
-    qsort(v, (size_t)d, sizeof(double), cmp_double);
+    qsort(ent, (size_t)d, sizeof(kvqo_entry_t), cmp_entry);
+    for (int e = 0; e < d; e++) {
+        v[e] = ent[e].v;
+        if (wv) wv[e] = ent[e].w;
+    }
+    free(ent);
     return bad;
 }
 
@@ -155,23 +180,26 @@ static int candidates_from_sorted(const double *v, int d, double *c)
 /* Atom statistics (the GPU summarises a block by these): atom p, p = 0..m'-2,
  * holds the elements with c_p <= x < c_{p+1}; the last atom also holds the
  * elements equal to the maximum.  Per atom: n, s1 = sum(x - c_p),
- * t1 = sum(c_{p+1} - x), e = sum((x - c_p)(c_{p+1} - x)).
+ * t1 = sum(c_{p+1} - x), e = sum((x - c_p)(c_{p+1} - x)); with weights wt
+ * (non-NULL) every sum is weighted: n = sum w, s1 = sum w (x - c_p), ...
  * Outputs for blocks [b0, b0+nb): cand[nb][17] (padded with the maximum),
- * mprime[nb], atoms[nb][16][4], nonfinite[nb]. */
-void kvqo_stats(const uint16_t *x, int64_t S, int64_t T, int D, int G,
-                int64_t b0, int64_t nb, double *cand, int32_t *mprime,
-                double *atoms, int32_t *nonfinite)
+ * mprime[nb], atoms[nb][16][4], flags[nb] (bit 0 non-finite value, bit 1
+ * invalid weight). */
+void kvqo_stats(const uint16_t *x, const float *wt, int64_t S, int64_t T,
+                int D, int G, int64_t b0, int64_t nb, double *cand,
+                int32_t *mprime, double *atoms, int32_t *nonfinite)
 {
     (void)S;
     int d = 32 * G;
 #pragma omp parallel
     {
         double *v = (double *)malloc(sizeof(double) * d);
+        double *wv = (double *)malloc(sizeof(double) * d);
 #pragma omp for schedule(dynamic, 16)
         for (int64_t i = 0; i < nb; i++) {
             int64_t b = b0 + i;
             double c[KVQO_M];
-            nonfinite[i] = block_sorted(x, T, D, G, b, v);
+            nonfinite[i] = block_sorted(x, wt, T, D, G, b, v, wv);
             int mp = candidates_from_sorted(v, d, c);
             mprime[i] = mp;
             for (int j = 0; j < KVQO_M; j++)
@@ -182,14 +210,15 @@ void kvqo_stats(const uint16_t *x, int64_t S, int64_t T, int D, int G,
             for (int e = 0; e < d; e++) {
                 int p = 0;
                 while (p + 1 <= mp - 2 && v[e] >= c[p + 1]) p++;
-                double y = v[e] - c[p], t = c[p + 1] - v[e];
-                a[p * 4 + 0] += 1.0;
-                a[p * 4 + 1] += y;
-                a[p * 4 + 2] += t;
-                a[p * 4 + 3] += y * t;
+                double y = v[e] - c[p], t = c[p + 1] - v[e], w = wv[e];
+                a[p * 4 + 0] += w;
+                a[p * 4 + 1] += w * y;
+                a[p * 4 + 2] += w * t;
+                a[p * 4 + 3] += w * y * t;
             }
         }
         free(v);
+        free(wv);
     }
 }
 
@@ -199,23 +228,28 @@ void kvqo_stats(const uint16_t *x, int64_t S, int64_t T, int D, int G,
 /* (x - q_i)/(q_{i+1} - q_i), conditional MSE (q_{i+1} - x)(x - q_i)).       */
 /* For levels a = c_P < b = c_Q and the elements x of the block in [a, b)    */
 /* (plus x == b when b is the maximum):                                      */
-/*   Dpq[P][Q] = sum (b - x)(x - a)          conditional MSE                 */
+/*   Dpq[P][Q] = sum w (b - x)(x - a)        conditional MSE, weighted       */
 /*   Mup[P][Q] = sum (x - a)/(b - a)         expected count sent to b        */
 /*   Mdn[P][Q] = sum (b - x)/(b - a)         expected count sent to a        */
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
     int d, mp;
+    double wmax;                 /* largest weight of the block */
     double c[KVQO_M];
     double Dpq[KVQO_M][KVQO_M];
     double Mup[KVQO_M][KVQO_M];
     double Mdn[KVQO_M][KVQO_M];
 } kvqo_block_t;
 
-static void block_tables(const double *v, int d, kvqo_block_t *B)
+static void block_tables(const double *v, const double *wv, int d,
+                         kvqo_block_t *B)
 {
     B->d = d;
     B->mp = candidates_from_sorted(v, d, B->c);
+    B->wmax = 0.0;
+    for (int e = 0; e < d; e++)
+        if (wv[e] > B->wmax) B->wmax = wv[e];
     memset(B->Dpq, 0, sizeof B->Dpq);
     memset(B->Mup, 0, sizeof B->Mup);
     memset(B->Mdn, 0, sizeof B->Mdn);
@@ -228,7 +262,7 @@ static void block_tables(const double *v, int d, kvqo_block_t *B)
                 double xv = v[e];
                 int in = (xv >= a && xv < b) || (Q == mp - 1 && xv == b);
                 if (!in) continue;
-                Ds += (b - xv) * (xv - a);
+                Ds += wv[e] * ((b - xv) * (xv - a));
                 Us += (xv - a) / W;
                 Ls += (b - xv) / W;
             }
@@ -378,7 +412,8 @@ static void block_choose(const kvqo_block_t *B, int s, double lambda,
 /* bisection is the task's): R(lambda) = sum_r d_r H_r summed in block order */
 /* in fp64, feasible iff R <= B.                                             */
 /*   1. if R(0) <= B: lambda = 0.                                            */
-/*   2. lo = 0, hi = max_r (c_max - c_min)^2; while R(hi) > B, hi *= 2, at   */
+/*   2. lo = 0, hi = max_r (c_max - c_min)^2 (times the block's largest      */
+/*      weight when D_r is weighted); while R(hi) > B, hi *= 2, at           */
 /*      most 30 times; still infeasible -> status 4 (infeasible), lambda =   */
 /*      hi, and the allocation at hi is returned.                            */
 /*   3. 40 steps: mid = 0.5 (lo + hi); R(mid) <= B ? hi = mid : lo = mid.    */
@@ -395,8 +430,8 @@ typedef struct {
     int32_t *bad;
 } kvqo_set_t;
 
-static void set_build(const uint16_t *x, int64_t T, int D, int G,
-                      const int64_t *ids, int64_t nb, kvqo_set_t *st)
+static void set_build(const uint16_t *x, const float *wt, int64_t T, int D,
+                      int G, const int64_t *ids, int64_t nb, kvqo_set_t *st)
 {
     int d = 32 * G;
     st->nb = nb;
@@ -406,12 +441,14 @@ static void set_build(const uint16_t *x, int64_t T, int D, int G,
 #pragma omp parallel
     {
         double *v = (double *)malloc(sizeof(double) * d);
+        double *wv = (double *)malloc(sizeof(double) * d);
 #pragma omp for schedule(dynamic, 8)
         for (int64_t i = 0; i < nb; i++) {
-            st->bad[i] = block_sorted(x, T, D, G, ids ? ids[i] : i, v);
-            block_tables(v, d, &st->blk[i]);
+            st->bad[i] = block_sorted(x, wt, T, D, G, ids ? ids[i] : i, v, wv);
+            block_tables(v, wv, d, &st->blk[i]);
         }
         free(v);
+        free(wv);
     }
 }
 
@@ -484,11 +521,23 @@ static void set_emit(const kvqo_set_t *st, int s, double lambda,
 #define KVQO_OK 0
 #define KVQO_INFEASIBLE 4
 #define KVQO_NONFINITE 3
+#define KVQO_BAD_WEIGHT 8
+
+/* status of a block set: an invalid weight outranks a non-finite value */
+static int set_status(const kvqo_set_t *st)
+{
+    int status = KVQO_OK;
+    for (int64_t i = 0; i < st->nb; i++) {
+        if (st->bad[i] & 2) return KVQO_BAD_WEIGHT;
+        if (st->bad[i] & 1) status = KVQO_NONFINITE;
+    }
+    return status;
+}
 
 /* Bisection over blocks ids[0..nb) (ids == NULL: blocks 0..nb-1).
  * bracket[0..1] receives the final (lo, hi).  Returns the status. */
-int kvqo_allocate_bisect(const uint16_t *x, int64_t S, int64_t T, int D, int G,
-                         const int64_t *ids, int64_t nb, int s,
+int kvqo_allocate_bisect(const uint16_t *x, const float *wt, int64_t S,
+                         int64_t T, int D, int G, const int64_t *ids, int64_t nb, int s,
                          double budget_bits, double *lambda_out,
                          double *bracket, float *codebook, uint8_t *kout,
                          double *Dr, double *Hr, double *gap, uint32_t *masks,
@@ -496,10 +545,8 @@ int kvqo_allocate_bisect(const uint16_t *x, int64_t S, int64_t T, int D, int G,
 {
     (void)S;
     kvqo_set_t st;
-    set_build(x, T, D, G, ids, nb, &st);
-    int status = KVQO_OK;
-    for (int64_t i = 0; i < nb; i++)
-        if (st.bad[i]) status = KVQO_NONFINITE;
+    set_build(x, wt, T, D, G, ids, nb, &st);
+    int status = set_status(&st);
     double *rates = (double *)malloc(sizeof(double) * (size_t)(nb ? nb : 1));
     double lo = 0.0, hi = 0.0, lambda;
     if (set_rate(&st, s, 0.0, rates) <= budget_bits) {
@@ -508,7 +555,8 @@ int kvqo_allocate_bisect(const uint16_t *x, int64_t S, int64_t T, int D, int G,
         for (int64_t i = 0; i < nb; i++) {
             const kvqo_block_t *B = &st.blk[i];
             double w = B->c[B->mp - 1] - B->c[0];
-            if (w * w > hi) hi = w * w;
+            double h = (w * w) * B->wmax;   /* wmax = 1 without weights */
+            if (h > hi) hi = h;
         }
         int n = 0;
         int feas = set_rate(&st, s, hi, rates) <= budget_bits;
@@ -539,18 +587,16 @@ int kvqo_allocate_bisect(const uint16_t *x, int64_t S, int64_t T, int D, int G,
 /* Choice at a fixed lambda (used for the one-step subgradient map, and to
  * check the codebooks at a given lambda).  *lambda_next receives
  * max(0, lambda + eta (R - budget_bits)). */
-int kvqo_allocate_at(const uint16_t *x, int64_t S, int64_t T, int D, int G,
-                     const int64_t *ids, int64_t nb, int s, double lambda,
+int kvqo_allocate_at(const uint16_t *x, const float *wt, int64_t S, int64_t T,
+                     int D, int G, const int64_t *ids, int64_t nb, int s, double lambda,
                      double eta, double budget_bits, double *lambda_next,
                      float *codebook, uint8_t *kout, double *Dr, double *Hr,
                      double *gap, uint32_t *masks, double *totals)
 {
     (void)S;
     kvqo_set_t st;
-    set_build(x, T, D, G, ids, nb, &st);
-    int status = KVQO_OK;
-    for (int64_t i = 0; i < nb; i++)
-        if (st.bad[i]) status = KVQO_NONFINITE;
+    set_build(x, wt, T, D, G, ids, nb, &st);
+    int status = set_status(&st);
     double tot[3];
     set_emit(&st, s, lambda, codebook, kout, Dr, Hr, gap, masks, tot);
     if (totals) memcpy(totals, tot, sizeof tot);
@@ -563,12 +609,13 @@ int kvqo_allocate_at(const uint16_t *x, int64_t S, int64_t T, int D, int G,
 }
 
 /* Rate R(lambda) = sum_r d_r H_r over the given blocks (fp64, block order). */
-double kvqo_rate_at(const uint16_t *x, int64_t S, int64_t T, int D, int G,
-                    const int64_t *ids, int64_t nb, int s, double lambda)
+double kvqo_rate_at(const uint16_t *x, const float *wt, int64_t S, int64_t T,
+                    int D, int G, const int64_t *ids, int64_t nb, int s,
+                    double lambda)
 {
     (void)S;
     kvqo_set_t st;
-    set_build(x, T, D, G, ids, nb, &st);
+    set_build(x, wt, T, D, G, ids, nb, &st);
     double *rates = (double *)malloc(sizeof(double) * (size_t)(nb ? nb : 1));
     double R = set_rate(&st, s, lambda, rates);
     free(rates);
@@ -577,15 +624,18 @@ double kvqo_rate_at(const uint16_t *x, int64_t S, int64_t T, int D, int G,
 }
 
 /* Interval tables of one block (for the tests' independent checks). */
-int kvqo_block_tables(const uint16_t *x, int64_t T, int D, int G, int64_t b,
-                      double *cand, double *Dpq, double *Mup, double *Mdn)
+int kvqo_block_tables(const uint16_t *x, const float *wt, int64_t T, int D,
+                      int G, int64_t b, double *cand, double *Dpq, double *Mup,
+                      double *Mdn)
 {
     int d = 32 * G;
     double *v = (double *)malloc(sizeof(double) * d);
+    double *wv = (double *)malloc(sizeof(double) * d);
     kvqo_block_t B;
-    block_sorted(x, T, D, G, b, v);
-    block_tables(v, d, &B);
+    block_sorted(x, wt, T, D, G, b, v, wv);
+    block_tables(v, wv, d, &B);
     free(v);
+    free(wv);
     for (int j = 0; j < KVQO_M; j++) cand[j] = j < B.mp ? B.c[j] : B.c[B.mp - 1];
     memcpy(Dpq, B.Dpq, sizeof B.Dpq);
     memcpy(Mup, B.Mup, sizeof B.Mup);
@@ -595,15 +645,17 @@ int kvqo_block_tables(const uint16_t *x, int64_t T, int D, int G, int64_t b,
 
 /* Objective pieces of an arbitrary chain (mask over candidate indices) of
  * block b: Dr, d_r H_r. */
-void kvqo_chain_cost(const uint16_t *x, int64_t T, int D, int G, int64_t b,
-                     uint32_t mask, double *Dr, double *Rr)
+void kvqo_chain_cost(const uint16_t *x, const float *wt, int64_t T, int D,
+                     int G, int64_t b, uint32_t mask, double *Dr, double *Rr)
 {
     int d = 32 * G;
     double *v = (double *)malloc(sizeof(double) * d);
+    double *wv = (double *)malloc(sizeof(double) * d);
     kvqo_block_t B;
-    block_sorted(x, T, D, G, b, v);
-    block_tables(v, d, &B);
+    block_sorted(x, wt, T, D, G, b, v, wv);
+    block_tables(v, wv, d, &B);
     free(v);
+    free(wv);
     chain_cost(&B, mask, Dr, Rr);
 }
 

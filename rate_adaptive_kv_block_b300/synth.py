@@ -156,3 +156,52 @@ def make_torch(w: Workload, seed: int = 0, device: str = "cuda"):
             x[row:row + m] = v.to(torch.float16)
             row += m
     return x
+
+
+# ------------------------------------------------ distortion weights
+# Seeded per-entry weights with the structure of attention sensitivity
+# measured on a calibration batch: the first ceil(S/2) streams are keys, whose
+# error reaches the logits through q . dk, so their weight depends on the
+# feature only (the mean squared query component: log-normal with log-std 1,
+# and 4 outlier channels x25); the other streams are values, whose error
+# reaches the output through sum_t p_t dv_t, so their weight depends on the
+# token only (the mean squared attention probability: log-normal with log-std
+# 1.5, and the first 4 tokens, attention sinks, x50).  Each stream's weights
+# are scaled to mean 1.  Random draws only; float32 [S, T, D].
+
+def _key_weights_np(n, D, rng):
+    w = np.exp(rng.standard_normal((n, 1, D), dtype=np.float32))
+    w[:, :, rng.permutation(D)[:4]] *= 25.0
+    return w / w.mean(axis=2, keepdims=True)
+
+
+def _value_weights_np(n, T, rng):
+    w = np.exp(1.5 * rng.standard_normal((n, T, 1), dtype=np.float32))
+    w[:, :4, :] *= 50.0
+    return w / w.mean(axis=1, keepdims=True)
+
+
+def weights_numpy(w: Workload, seed: int = 0) -> np.ndarray:
+    """[S, T, D] float32 distortion weights (CPU backend)."""
+    rng = np.random.default_rng(seed)
+    nk = (w.S + 1) // 2
+    out = np.empty((w.S, w.T, w.D), dtype=np.float32)
+    out[:nk] = _key_weights_np(nk, w.D, rng)
+    out[nk:] = _value_weights_np(w.S - nk, w.T, rng)
+    return out
+
+
+def weights_torch(w: Workload, seed: int = 0, device: str = "cuda"):
+    """[S, T, D] float32 distortion weights on `device` (torch backend)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    nk = (w.S + 1) // 2
+    out = torch.empty((w.S, w.T, w.D), dtype=torch.float32, device=device)
+    kw = torch.exp(torch.randn((nk, 1, w.D), generator=g, device=device))
+    kw[:, :, torch.randperm(w.D, generator=g, device=device)[:4]] *= 25.0
+    out[:nk] = kw / kw.mean(dim=2, keepdim=True)
+    vw = torch.exp(1.5 * torch.randn((w.S - nk, w.T, 1), generator=g, device=device))
+    vw[:, :4, :] *= 50.0
+    out[nk:] = vw / vw.mean(dim=1, keepdim=True)
+    return out

@@ -24,10 +24,13 @@ def candidates(v):
     return np.array(out)
 
 
-def chain_cost_elementwise(v, q):
-    """(D, d*H, expected counts) of levels q for values v, per element."""
+def chain_cost_elementwise(v, q, wt=None):
+    """(D, d*H, expected counts) of levels q for values v, per element; with
+    per-element weights wt the distortion is sum wt (q_hi - x)(x - q_lo) and
+    the counts stay unweighted."""
     v = np.asarray(v, dtype=np.float64)
     q = np.asarray(q, dtype=np.float64)
+    wt = np.ones_like(v) if wt is None else np.asarray(wt, dtype=np.float64)
     d = len(v)
     k = len(q)
     if k == 1:
@@ -37,7 +40,7 @@ def chain_cost_elementwise(v, q):
     lo, hi = q[i], q[i + 1]
     w = hi - lo
     pup = (v - lo) / w
-    D = float(np.sum((hi - v) * (v - lo)))
+    D = float(np.sum(wt * (hi - v) * (v - lo)))
     M = np.zeros(k)
     np.add.at(M, i, 1.0 - pup)
     np.add.at(M, i + 1, pup)
@@ -68,14 +71,14 @@ def better(a, b):
     return a[1] < b[1]
 
 
-def best_chain(v, s, lam):
+def best_chain(v, s, lam, wt=None):
     """Minimum of D + lam*d*H over all admissible chains, per element.
     Returns (obj, chain, D, R, second_obj)."""
     c = candidates(v)
     best = None
     second = None
     for ch in all_chains(len(c), s):
-        D, R, _ = chain_cost_elementwise(v, c[list(ch)])
+        D, R, _ = chain_cost_elementwise(v, c[list(ch)], wt)
         cand = (D + lam * R, ch, D, R)
         if best is None or better(cand, best):
             second = best

@@ -29,14 +29,17 @@ def to_np(x_t):
     return x_t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def run(x, G, s, budget, seed=0, index_base=0, mode=kvq.KVQ_BISECT40, eta=0.0, lam0=0.0):
-    """Whole path on the GPU; returns numpy copies of every output."""
+def run(x, G, s, budget, seed=0, index_base=0, mode=kvq.KVQ_BISECT40, eta=0.0, lam0=0.0, w=None):
+    """Whole path on the GPU (kvq_stats_weighted when per-entry weights w are
+    given); returns numpy copies of every output."""
     S, T, D = x.shape
     L = kvq.Layout(S, T, D, G)
     xd = x if isinstance(x, torch.Tensor) else to_dev(x)
+    wd = None if w is None else torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32)).to(xd.device)
     buf = kvq.Buffers(L, s, xd.device)
     buf.lam.fill_(lam0)
-    kvq.quantize(xd, L, budget, s, seed=seed, index_base=index_base, mode=mode, eta=eta, buf=buf)
+    kvq.quantize(xd, L, budget, s, seed=seed, index_base=index_base, mode=mode, eta=eta, buf=buf,
+                 weights=wd)
     y = torch.empty_like(xd)
     kvq.kvq_dequantize(buf.codes, buf.codebook, L, y)
     torch.cuda.synchronize()
@@ -62,17 +65,19 @@ def run(x, G, s, budget, seed=0, index_base=0, mode=kvq.KVQ_BISECT40, eta=0.0, l
     }
 
 
-def check_stats(g, ora, ids=None):
-    """GPU stats rows (ids: which GPU blocks the oracle rows are) vs oracle."""
+def check_stats(g, ora, ids=None, weighted=False):
+    """GPU stats rows (ids: which GPU blocks the oracle rows are) vs oracle;
+    weighted: the moments are weighted sums, the first one too."""
     ids = np.arange(len(ora["mprime"])) if ids is None else np.asarray(ids)
     mp = ora["mprime"]
     assert np.array_equal(g["mprime"][ids], mp)
     c_g = g["cand"][ids]
     assert np.array_equal(c_g, ora["cand"]), "candidates differ"
-    assert np.array_equal(g["flags"][ids] & 1, ora["nonfinite"])
+    assert np.array_equal(g["flags"][ids] & 3, ora["nonfinite"])
     a_g, a_o = g["atoms"][ids], ora["atoms"]
-    assert np.array_equal(a_g[..., 0], a_o[..., 0]), "atom counts differ"
-    for q in (1, 2, 3):
+    if not weighted:
+        assert np.array_equal(a_g[..., 0], a_o[..., 0]), "atom counts differ"
+    for q in ((0, 1, 2, 3) if weighted else (1, 2, 3)):
         err = np.abs(a_g[..., q] - a_o[..., q])
         tol = MOM_REL * np.abs(a_o[..., q]) + 1e-7 * np.abs(a_o[..., q]).max(axis=1, keepdims=True)
         bad = err > tol + 1e-30
@@ -90,11 +95,12 @@ def chain_mask_from_codebook(cand, mp, q, k):
     return m
 
 
-def check_choice(g, x_np, G, s, lam, ids=None, slab_ids=None):
+def check_choice(g, x_np, G, s, lam, ids=None, slab_ids=None, w=None):
     """Codebooks / k / D_r / H_r of the GPU against the oracle's choice at the
     same lambda.  ids: oracle block ids (in x_np); slab_ids: the GPU block ids
-    they correspond to.  Returns the oracle result and the non-tie mask."""
-    at = oracle.allocate_at(x_np, G, s, lam, ids=ids)
+    they correspond to; w: distortion weights.  Returns the oracle result and
+    the non-tie mask."""
+    at = oracle.allocate_at(x_np, G, s, lam, ids=ids, w=w)
     gi = np.arange(len(at["k"])) if slab_ids is None else np.asarray(slab_ids)
     nontie = at["gap"] > GAP
     cb_g, k_g = g["codebook"][gi], g["k"][gi]
@@ -112,9 +118,9 @@ def check_choice(g, x_np, G, s, lam, ids=None, slab_ids=None):
     # tie blocks: the GPU's choice is (near-)optimal too
     for i in np.nonzero(~nontie & ~same)[0]:
         b = int(i) if ids is None else int(ids[i])
-        mp, cand, _, _, _ = oracle.block_tables(x_np, G, b)
+        mp, cand, _, _, _ = oracle.block_tables(x_np, G, b, w=w)
         m = chain_mask_from_codebook(cand, mp, cb_g[i], int(k_g[i]))
-        Dc, Rc = oracle.chain_cost(x_np, G, b, m)
+        Dc, Rc = oracle.chain_cost(x_np, G, b, m, w=w)
         obj_g = Dc + lam * Rc
         obj_o = at["D_r"][i] + lam * at["H_r"][i] * d
         assert obj_g <= obj_o * (1 + 2 * GAP) + 1e-9

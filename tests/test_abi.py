@@ -40,6 +40,7 @@ def test_sizes_and_layout_validation():
     assert kvq.kvq_num_blocks(kvq.Layout(1, 32, 8 * 33, 8)) == -1        # > 32 groups
     assert kvq.kvq_num_blocks(kvq.Layout(0, 32, 128, 32)) == 0
     assert kvq.kvq_status_string(3) == "non-finite input entry"
+    assert kvq.kvq_status_string(kvq.KVQ_ERR_BAD_WEIGHT) == "negative or non-finite distortion weight"
 
 
 class _Fake:
@@ -65,6 +66,11 @@ def test_host_validation_rejects_bad_arguments():
     assert lib.kvq_stats(C.c_void_p(p.p), L.c(), 16, C.c_void_p(p.p), C.c_void_p(p.p), st(s)) == bad
     assert lib.kvq_stats(C.c_void_p(odd.p), L.c(), 17, C.c_void_p(p.p), C.c_void_p(p.p), st(s)) == bad
     assert lib.kvq_stats(C.c_void_p(p.p), L.c(), 17, C.c_void_p(p.p), None, st(s)) == bad
+    v = C.c_void_p(p.p)
+    assert lib.kvq_stats_weighted(v, None, L.c(), 17, v, v, st(s)) == bad            # no weights
+    assert lib.kvq_stats_weighted(v, C.c_void_p(odd.p), L.c(), 17, v, v, st(s)) == bad
+    assert lib.kvq_stats_weighted(v, v, L.c(), 16, v, v, st(s)) == bad
+    assert lib.kvq_stats_weighted(v, v, kvq.Layout(2, 65, 128, 128).c(), 17, v, v, st(s)) == bad
     args = [C.c_void_p(p.p)] * 9
     for s_, B, mode, eta in [(1, 1.0, 0, 0.0), (17, 1.0, 0, 0.0), (8, -1.0, 0, 0.0),
                              (8, float("nan"), 0, 0.0), (8, 1.0, 2, 0.0), (8, 1.0, 1, -1.0)]:
