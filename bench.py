@@ -235,6 +235,63 @@ def comparator_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep,
             "uniform_int4_GBps": (x.numel() * 2 + x.numel() // 2 + nb * 65) / (t_u * 1e-3) / 1e9}
 
 
+def weighted_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev):
+    """D_r weighted by attention sensitivity (kvq_stats_weighted) on the same
+    layer at the same budget: seeded synthetic sensitivities (keys per
+    feature, values per token, each stream's mean 1), the weighted stats
+    kernel and the whole weighted step with L2 flushed, and the weighted and
+    plain squared error of the binary16 decode for the weighted allocation and
+    for the unweighted one (buf)."""
+    import torch
+    from rate_adaptive_kv_block_b300 import kvq, synth
+    s, B = w.s, w.budgets[0] * x.numel()
+    Wt = synth.weights_torch(w, seed=7, device=dev)
+    bw = kvq.Buffers(L, s, dev)
+
+    def stats_w():
+        kvq.kvq_stats_weighted(x, Wt, L, bw.stats, bw.status_stats)
+
+    def step_w():
+        stats_w()
+        kvq.kvq_allocate(bw.stats, L, s, B, kvq.KVQ_BISECT40, 0.0, bw.lam, bw.workspace,
+                         bw.codebook, bw.k, bw.D_r, bw.H_r, bw.totals, bw.status)
+        kvq.kvq_quantize(x, L, bw.codebook, bw.k, 0, 0, bw.codes, bw.status_quant)
+
+    step_w()
+    torch.cuda.synchronize()
+    if int(bw.status_stats.item()) != 0 or int(bw.status.item()) != 0:
+        raise SystemExit("weighted path status %d / %d" % (int(bw.status_stats.item()),
+                                                          int(bw.status.item())))
+    g_sw = graph_of(lambda: (flush_l2(1), stats_w()))
+    g_stw = graph_of(lambda: (flush_l2(1), step_w()))
+    device_ms(g_sw, 2)
+    device_ms(g_stw, 2)
+    t_sw = device_ms(g_sw, nrep) - t_flush
+    t_stw = device_ms(g_stw, nrep) - t_flush
+    xf = x.float()
+    y = torch.empty_like(x)
+
+    def errs(b):
+        kvq.kvq_dequantize(b.codes, b.codebook, L, y)
+        e2 = (y.float() - xf) ** 2
+        return float((Wt * e2).sum() / Wt.sum()), float(e2.mean())
+
+    we_w, mse_w = errs(bw)
+    we_u, mse_u = errs(buf)
+    n = x.numel()
+    return {"what": "distortion weighted per entry by synthetic attention sensitivities "
+                    "(keys: per feature, values: per token); errors of one stochastic "
+                    "decode, weighted error = sum w e^2 / sum w",
+            "stats_weighted_ms": t_sw,
+            "stats_weighted_GBps": (n * 6 + L.nblocks * 4800) / (t_sw * 1e-3) / 1e9,
+            "step_weighted_ms": t_stw,
+            "lambda": float(bw.lam.item()),
+            "weighted_allocation": {"weighted_err": we_w, "mse": mse_w,
+                                    "rate_bits": float(bw.totals[0].item()) / n},
+            "unweighted_allocation": {"weighted_err": we_u, "mse": mse_u,
+                                      "rate_bits": float(buf.totals[0].item()) / n}}
+
+
 def entropy_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev):
     """The layer's codes entropy-coded (kvq_entropy_encode): stored bits per
     entry against the rate the allocation targets, and the coder's times
@@ -490,6 +547,7 @@ def main():
     att = attention_bench(w, L, buf, flush_l2, graph_of, device_ms, t_flush, nrep, *peaks(), dev)
     comp = comparator_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev)
     ent = entropy_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev)
+    wtd = weighted_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev)
 
     # End to end through the C ABI from pinned host memory, pipelined over
     # three streams the way a serving loop would run it: step i's input copy
@@ -572,6 +630,7 @@ def main():
         "decode_attention": att,
         "comparators": comp,
         "entropy_coding": ent,
+        "weighted_distortion": wtd,
         "cold_method": "graph (L2 flush + kernel) minus graph (L2 flush), device-timed",
         "stats_cold_GBps": s_bytes / (t_scold * 1e-3) / 1e9,
         "quantize_cold_GBps": q_bytes / (t_qcold * 1e-3) / 1e9,

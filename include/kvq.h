@@ -50,6 +50,7 @@ extern "C" {
 #define KVQ_ERR_TOO_LARGE 5   /* kvq_allocate_static: layout over its limit  */
 #define KVQ_ERR_TIMEOUT 6     /* device status: a grid-wide wait gave up     */
 #define KVQ_ERR_CORRUPT 7     /* device status: an entropy-coded slot is malformed */
+#define KVQ_ERR_BAD_WEIGHT 8  /* device status: a distortion weight is < 0, NaN or +-Inf */
 
 /* lambda modes of kvq_allocate */
 #define KVQ_BISECT40 0        /* global lambda by the 40-step bisection      */
@@ -107,6 +108,31 @@ int kvq_stats(const uint16_t *x, kvq_layout L, int m, void *stats,
               int32_t *status, void *stream);
 
 /*
+ * kvq_stats_weighted -- kvq_stats with the distortion weighted per entry
+ * ("Implementation notes": optionally weight D_r by the attention
+ * sensitivity measured on a calibration batch).  The block distortion
+ * becomes D_r = sum_e w_e E[(hat x_e - x_e)^2] = sum_e w_e (q_hi - x_e)(x_e -
+ * q_lo); the candidates and the entropy H_r (expected frequencies of the
+ * stored symbols) are those of kvq_stats.  kvq_allocate then minimises
+ * sum_r D_r subject to sum_r d_r H_r <= B with the weighted D_r, and reports
+ * the weighted D_r and sum_r D_r; its bisection starts from
+ * hi = max_r (c_max - c_min)^2 w_max,r (w_max,r the block's largest weight).
+ *   x       device, [S,T,D] binary16, as kvq_stats.
+ *   w       device, [S,T,D] float32 in the layout of x (read once): w_e >= 0.
+ *           Sensitivities that depend only on the feature (keys: the mean
+ *           squared query component) or only on the token (values: the
+ *           mean squared attention probability) are passed broadcast.
+ *   m, stats as kvq_stats (the stats rows hold the weighted atom moments).
+ *   status  device int32: KVQ_OK; KVQ_ERR_BAD_WEIGHT if a weight is negative,
+ *           NaN or infinite (it is counted as 0; such blocks' results are
+ *           unspecified), else KVQ_ERR_NONFINITE if an entry of x is.
+ * The per-atom weighted sums are formed in a fixed order: repeated calls give
+ * identical bits.
+ */
+int kvq_stats_weighted(const uint16_t *x, const float *w, kvq_layout L, int m,
+                       void *stats, int32_t *status, void *stream);
+
+/*
  * kvq_allocate -- per-block codebooks and the global lambda ("Mathematical
  * statement": minimise sum_r D_r subject to sum_r d_r H_r <= B, |Q_r| <= s;
  * with lambda the blocks decouple into argmin_Q D_r + lambda d_r H_r).
@@ -136,7 +162,9 @@ int kvq_stats(const uint16_t *x, kvq_layout L, int m, void *stats,
  *                expected codepoint frequencies.
  *   totals       device double [3]: sum_r d_r H_r, sum_r D_r, and the lambda
  *                the codebooks were chosen at.
- *   status       device int32: KVQ_OK, KVQ_ERR_NONFINITE, KVQ_ERR_INFEASIBLE.
+ *   status       device int32: KVQ_OK, KVQ_ERR_INFEASIBLE, KVQ_ERR_NONFINITE,
+ *                or KVQ_ERR_BAD_WEIGHT (stats from kvq_stats_weighted), the
+ *                last outranking the others.
  */
 int kvq_allocate(const void *stats, kvq_layout L, int s, double budget_bits,
                  int mode, double eta, double *lambda, void *workspace,

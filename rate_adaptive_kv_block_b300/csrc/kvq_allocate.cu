@@ -1256,6 +1256,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
     }
     int st = n->status;
     if (n->flags & kFlagNonfinite) st = KVQ_ERR_NONFINITE;
+    if (n->flags & kFlagBadWeight) st = KVQ_ERR_BAD_WEIGHT;
     if (__ldcg(&ctrl->err)) st = KVQ_ERR_TIMEOUT;
     *status = st;
     ctrl->ticket_emit = 0u;

@@ -7,8 +7,8 @@
 #include "kvq_internal.cuh"
 
 namespace kvq {
-int launch_stats(const uint16_t *x, const kvq_layout &L, void *stats, int32_t *status,
-                 cudaStream_t st);
+int launch_stats(const uint16_t *x, const float *wt, const kvq_layout &L, void *stats,
+                 int32_t *status, cudaStream_t st);
 int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget, int mode,
                     double eta, double *lambda, void *workspace, float *codebook, uint8_t *k,
                     float *Dr, float *Hr, double *totals, int32_t *status, cudaStream_t st,
@@ -115,7 +115,17 @@ int kvq_stats(const uint16_t *x, kvq_layout L, int m, void *stats, int32_t *stat
     const int64_t nb = num_blocks(L);
     if (nb > 0 && (!x || !stats || !aligned16(x) || !aligned16(stats))) return KVQ_ERR_INVALID_ARG;
     if (nb > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
-    return launch_stats(x, L, stats, status, static_cast<cudaStream_t>(stream));
+    return launch_stats(x, nullptr, L, stats, status, static_cast<cudaStream_t>(stream));
+}
+
+int kvq_stats_weighted(const uint16_t *x, const float *w, kvq_layout L, int m, void *stats,
+                       int32_t *status, void *stream) {
+    if (!layout_ok(L) || m != kCand || !status) return KVQ_ERR_INVALID_ARG;
+    const int64_t nb = num_blocks(L);
+    if (nb > 0 && (!x || !w || !stats || !aligned16(x) || !aligned16(w) || !aligned16(stats)))
+        return KVQ_ERR_INVALID_ARG;
+    if (nb > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
+    return launch_stats(x, w, L, stats, status, static_cast<cudaStream_t>(stream));
 }
 
 int kvq_allocate(const void *stats, kvq_layout L, int s, double budget_bits, int mode,
@@ -304,6 +314,7 @@ const char *kvq_status_string(int status) {
     case KVQ_ERR_TIMEOUT: return "device wait timed out";
     case KVQ_ERR_TOO_LARGE: return "layout needs more scratch than the static workspace holds";
     case KVQ_ERR_CORRUPT: return "malformed entropy-coded slot";
+    case KVQ_ERR_BAD_WEIGHT: return "negative or non-finite distortion weight";
     default: return "unknown status";
     }
 }

@@ -18,11 +18,12 @@ constexpr int kTriples = 680;   // slot triples i < j < l
 // One row per block, written by kvq_stats, read by kvq_allocate.  Atom p
 // (p = 0 .. m'-2) holds the entries c_p <= x < c_{p+1} (the last atom also
 // the entries equal to the maximum): n, s1 = sum(x - c_p),
-// t1 = sum(c_{p+1} - x), e = sum((x - c_p)(c_{p+1} - x)).
+// t1 = sum(c_{p+1} - x), e = sum((x - c_p)(c_{p+1} - x)); kvq_stats_weighted
+// stores the weighted sums (n = sum w, s1 = sum w (x - c_p), ...) instead.
 struct StatsRow {
     float c[kCand];      // merged candidates, padded with the maximum
     int32_t mprime;      // number of distinct candidates (1..17)
-    int32_t flags;       // bit 0: a non-finite entry
+    int32_t flags;       // kFlag* bits
     int32_t d;           // entries in the block
     float n[16];
     float s1[16];
@@ -31,7 +32,9 @@ struct StatsRow {
     float pad[12];
 };
 static_assert(sizeof(StatsRow) == 384, "stats row is 384 bytes");
-constexpr int kFlagNonfinite = 1;
+constexpr int kFlagNonfinite = 1;   // a non-finite entry
+constexpr int kFlagBadWeight = 2;   // a negative or non-finite weight
+constexpr int kFlagWeighted = 4;    // the moments and Dp are weighted
 
 // ------------------------------------------------------------- table layout
 // Per-block, lambda-independent DP tables, in "slot" space: the m'
@@ -82,7 +85,8 @@ static_assert(pidx(15, 16) == kPairs - 1, "pair count");
 // Output of kvq_stats: a 256-byte header, then one 4800-byte record per
 // block: the stats row (96 floats) and the DP tables (1104 floats).
 struct StatsHeader {
-    unsigned long long hi0_bits;   // max_r (c_max - c_min)^2 (double bits, atomic max)
+    unsigned long long hi0_bits;   // max_r (c_max - c_min)^2 w_max,r (double bits, atomic max;
+                                   // w_max,r = 1 without weights)
     uint32_t flags;                // OR of the block flags
     uint32_t pad[61];
 };

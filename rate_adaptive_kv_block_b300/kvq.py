@@ -23,6 +23,7 @@ KVQ_ERR_INFEASIBLE = 4
 KVQ_ERR_TOO_LARGE = 5
 KVQ_ERR_TIMEOUT = 6
 KVQ_ERR_CORRUPT = 7
+KVQ_ERR_BAD_WEIGHT = 8
 KVQ_STATIC_WORKSPACE_BYTES = 8 << 20
 KVQ_BISECT40 = 0
 KVQ_SUBGRADIENT = 1
@@ -88,6 +89,8 @@ def lib():
         L.kvq_workspace_bytes.argtypes = [_Layout, C.c_int]
         L.kvq_stats.restype = C.c_int
         L.kvq_stats.argtypes = [vp, _Layout, C.c_int, vp, vp, vp]
+        L.kvq_stats_weighted.restype = C.c_int
+        L.kvq_stats_weighted.argtypes = [vp, vp, _Layout, C.c_int, vp, vp, vp]
         L.kvq_allocate.restype = C.c_int
         L.kvq_allocate.argtypes = [vp, _Layout, C.c_int, dbl, C.c_int, dbl, vp, vp, vp, vp,
                                    vp, vp, vp, vp, vp]
@@ -158,6 +161,13 @@ def kvq_workspace_bytes(L: Layout, s: int) -> int:
 def kvq_stats(x, L: Layout, stats, status, m: int = 17, stream=None):
     _check(lib().kvq_stats(_ptr(x), L.c(), int(m), _ptr(stats), _ptr(status), _stream(stream)),
            "kvq_stats")
+
+
+def kvq_stats_weighted(x, w, L: Layout, stats, status, m: int = 17, stream=None):
+    """kvq_stats with per-entry distortion weights w (float32 CUDA tensor of
+    x's shape)."""
+    _check(lib().kvq_stats_weighted(_ptr(x), _ptr(w), L.c(), int(m), _ptr(stats), _ptr(status),
+                                    _stream(stream)), "kvq_stats_weighted")
 
 
 def kvq_allocate(stats, L: Layout, s: int, budget_bits: float, mode: int, eta: float, lam,
@@ -286,13 +296,18 @@ class Buffers:
 
 def quantize(x, L: Layout, budget_bits: float, s: int, seed: int = 0, index_base: int = 0,
              mode: int = KVQ_BISECT40, eta: float = 0.0, buf: Buffers = None, stream=None,
-             fused: bool = False):
-    """kvq_stats + kvq_allocate + kvq_quantize on x (a [S,T,D] float16 CUDA
-    tensor); fused: kvq_allocate_quantize instead of the last two.  Returns the Buffers (codes, codebook, k, D_r, H_r, totals,
-    lambda, statuses), all still on the device."""
+             fused: bool = False, weights=None):
+    """kvq_stats (kvq_stats_weighted when per-entry distortion weights are
+    given) + kvq_allocate + kvq_quantize on x (a [S,T,D] float16 CUDA tensor);
+    fused: kvq_allocate_quantize instead of the last two.  Returns the Buffers
+    (codes, codebook, k, D_r, H_r, totals, lambda, statuses), all still on the
+    device."""
     if buf is None:
         buf = Buffers(L, s, x.device)
-    kvq_stats(x, L, buf.stats, buf.status_stats, stream=stream)
+    if weights is None:
+        kvq_stats(x, L, buf.stats, buf.status_stats, stream=stream)
+    else:
+        kvq_stats_weighted(x, weights, L, buf.stats, buf.status_stats, stream=stream)
     if fused:
         kvq_allocate_quantize(buf.stats, x, L, s, budget_bits, mode, eta, buf.lam, buf.workspace,
                               buf.codebook, buf.k, buf.D_r, buf.H_r, buf.totals, seed,
