@@ -610,6 +610,18 @@ stats_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt, kvq_l
     }
 }
 
+// the weighted variant's static plus dynamic shared memory exceeds the
+// default 48 KB per block: opt in once per device
+int stats_init() {
+    if (cudaFuncSetAttribute(stats_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kWAccDynBytes) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    if (cudaFuncSetAttribute(stats_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kWAccDynBytes) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
 int launch_stats(const uint16_t *x, const float *wt, const kvq_layout &L, void *stats,
                  int32_t *status, cudaStream_t st) {
     const int64_t nb = num_blocks(L);

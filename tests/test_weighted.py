@@ -11,7 +11,7 @@ exactly; a power-of-two weight c scales D_r by c and lambda by c exactly; a
 constant weight per block is the unweighted choice at lambda / w; the weighted
 D_r is the expectation of sum w (hat x - x)^2 over the interpolation's
 randomness (Monte Carlo over seeds); zero weights leave only the rate, so the
-fewest levels win; invalid weights are flagged.
+chain of least rate wins (brute force); invalid weights are flagged.
 GPU: weighted stats rows against the oracle, the allocation, codes, repeated
 calls bit-identical, edge weights and the status words.
 """
@@ -153,15 +153,25 @@ def test_weighted_distortion_is_the_expected_weighted_error():
 
 
 def test_zero_weights_leave_the_rate_alone():
+    # D_r = 0 for every chain: at lambda > 0 the chain of least rate wins
+    # (brute force over every admissible chain), at lambda = 0 every chain
+    # ties and the fewest levels win; the other blocks are unaffected.
     rng = np.random.default_rng(26)
     blocks = tiny_blocks(rng)
     x = tiny_x(blocks)
     W = np.ones((len(blocks), 32, 1), dtype=np.float32)
     W[1] = 0.0
+    v = f16(blocks[1])
+    c = bf.candidates(v)
+    rmin = min(bf.chain_cost_elementwise(v, c[list(ch)])[1] for ch in bf.all_chains(len(c), 8))
     for lam in (0.0, 0.3):
         got = oracle.allocate_at(x, 1, 8, lam, w=W)
         ref = oracle.allocate_at(x, 1, 8, lam)
-        assert got["k"][1] == 2 and got["D_r"][1] == 0.0       # fewest levels, no distortion
+        assert got["D_r"][1] == 0.0
+        if lam == 0.0:
+            assert got["k"][1] == 2
+        else:
+            assert got["H_r"][1] * 32 == pytest.approx(rmin, rel=1e-12)
         keep = [0, 2, 3]
         assert np.array_equal(got["mask"][keep], ref["mask"][keep])
 
@@ -275,7 +285,7 @@ def test_weighted_edge_weights_and_status():
     ora = oracle.allocate_bisect(x, 128, 16, B, w=W)
     assert g["lambda"] == pytest.approx(ora["lambda"], rel=gc.LAM_REL)
     gc.check_choice(g, x, 128, 16, g["lambda"], w=W)
-    assert g["k"][0] == 2
+    assert g["D_r"][0] == 0.0                       # no weight, no distortion
     # all weights zero: lambda 0, the fewest levels everywhere
     g0 = gc.run(x, 128, 16, B, w=np.zeros(x.shape, dtype=np.float32))
     assert g0["status"] == 0 and g0["lambda"] == 0.0 and np.all(g0["k"] == 2)
