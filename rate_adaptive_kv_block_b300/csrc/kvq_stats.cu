@@ -26,28 +26,12 @@
 // triple) and writes them with the stats row as the block's record.  Every
 // fp32 term added is non-negative, so there is no cancellation.
 // Non-finite entries are the keys of the four lowest and four highest bins.
-//
-// Weighted variant (kvq_stats_weighted; "Implementation notes": D_r may be
-// weighted by attention sensitivity measured on a calibration batch): the
-// caller gives a weight w >= 0 per entry and the distortion tables become
-// sum w (b - x)(x - a); the entropy terms keep the unweighted moments (they
-// count stored symbols).  Weights do not fit the per-bin integer sums, so
-// after the candidates are known every thread sends each of its entries to
-// its atom (a 4-step binary search over the candidate keys) and adds
-// (w, w y, w t, w y t) to a private float4 column of that atom in shared
-// memory; a fixed-order tree over the 256 columns then gives the weighted
-// atom moments, so the result does not depend on scheduling.
 #include "kvq_internal.cuh"
 
 namespace kvq {
 
 constexpr int kStatsThreads = 256;
 constexpr int kStatsWarps = kStatsThreads / 32;
-// weighted variant: one float4 column per (atom, thread); atoms 0..3 live in
-// the histogram union (dead by then), atoms 4..15 in dynamic shared memory
-constexpr int kWAccUnionRows = 4;
-constexpr size_t kWAccDynBytes = (size_t)(16 - kWAccUnionRows) * kStatsThreads * sizeof(float4);
-static_assert(kWAccDynBytes <= 48 * 1024, "weighted columns fit the default dynamic limit");
 
 struct StatsSmem {
     union {
@@ -70,14 +54,8 @@ struct StatsSmem {
     float dc[17];
     int32_t mprime, nslots;
     float an[16], as1[16], at1[16], ae[16];
-    float wn[16], ws1[16], wt1[16], we[16];   // weighted moments (weighted variant)
-    int32_t bk[16];                           // atom boundary keys, padded with 0x10000
-    uint32_t wmax_bits, wbad;
     float pDp[kPairs], pUp[kPairs], pDn[kPairs];   // pair tables, slot space
 };
-
-static_assert(sizeof(uint32_t) * 2 * kStatsWarps * 256 >= kWAccUnionRows * kStatsThreads * sizeof(float4),
-              "the histogram union holds the first weighted rows");
 
 __device__ __forceinline__ int block_excl_scan(int v, int32_t *warp_tot, int &total) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -125,13 +103,12 @@ __device__ __forceinline__ void add_piece(uint32_t b, int j0, int j1, uint32_t n
     ae += fn * Y0 * T1 + Y0 * u * fsli + T1 * u * fsi + u * u * fsx;
 }
 
-template <int UNITS, bool WEIGHTED>
-__global__ void __launch_bounds__(kStatsThreads, WEIGHTED ? 3 : 6)
-stats_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt, kvq_layout L,
-             int lg_ng, int lg_upr, StatsHeader *__restrict__ hdr, float *__restrict__ recs,
+template <int UNITS>
+__global__ void __launch_bounds__(kStatsThreads, 6)
+stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr,
+             StatsHeader *__restrict__ hdr, float *__restrict__ recs,
              int32_t *__restrict__ status) {
     __shared__ __align__(16) StatsSmem sm;
-    extern __shared__ __align__(16) float4 wacc_dyn[];   // weighted variant only
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = L.group, D = L.D;
     const int d = 32 * G;
@@ -151,19 +128,12 @@ stats_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt, kvq_l
             const int row = u >> lg_upr, cu = u & (upr - 1);
             const int64_t off = (tbk * 32 + row) * (int64_t)D + (int64_t)g * G + cu * 8;
             raw[k] = __ldg(reinterpret_cast<const uint4 *>(x + off));
-            if constexpr (WEIGHTED) {   // the weights are read after the select: warm L2
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(wt + off));
-            }
         }
     }
     // zero the tables while the loads are in flight
     {
         uint4 *z = reinterpret_cast<uint4 *>(&sm.h1a[0][0]);
         for (int i = tid; i < 2 * kStatsWarps * 256 / 4; i += kStatsThreads) z[i] = make_uint4(0, 0, 0, 0);
-        if (tid == 0) {
-            sm.wmax_bits = 0u;
-            sm.wbad = 0u;
-        }
         if (tid < kPairs) {
             sm.pDp[tid] = __int_as_float(0x7f800000);   // +inf: no such pair
             sm.pUp[tid] = 0.f;
@@ -337,78 +307,8 @@ stats_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt, kvq_l
             sm.dc[p] = key_value((uint32_t)key);
         }
         if (lane == 0) sm.mprime = __popc(bal);
-        if constexpr (WEIGHTED) {
-            // boundaries of atoms 1 .. m'-2 (the maximum closes the last atom)
-            __syncwarp();
-            const int mpw = __popc(bal);
-            if (lane < 16) sm.bk[lane] = (lane + 1 <= mpw - 2) ? sm.dkey[lane + 1] : 0x10000;
-        }
     }
     __syncthreads();
-
-    // ---- weighted variant: every entry adds (w, w y, w t, w y t) to its own
-    //      column of its atom (y = x - c_p, t = c_{p+1} - x)
-    auto wrow = [&](int p) -> float4 * {
-        return p < kWAccUnionRows ? reinterpret_cast<float4 *>(&sm.h1a[0][0]) + p * kStatsThreads
-                                  : wacc_dyn + (p - kWAccUnionRows) * kStatsThreads;
-    };
-    if constexpr (WEIGHTED) {
-#pragma unroll
-        for (int p = 0; p < 16; ++p) wrow(p)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 wv[UNITS][2];
-#pragma unroll
-        for (int k = 0; k < UNITS; ++k) {
-            const int u = tid + k * kStatsThreads;
-            wv[k][0] = wv[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (u < units) {
-                const int row = u >> lg_upr, cu = u & (upr - 1);
-                const int64_t off = (tbk * 32 + row) * (int64_t)D + (int64_t)g * G + cu * 8;
-                wv[k][0] = __ldg(reinterpret_cast<const float4 *>(wt + off));
-                wv[k][1] = __ldg(reinterpret_cast<const float4 *>(wt + off + 4));
-            }
-        }
-        const int mpw = sm.mprime;
-        bool wb = false;
-        uint32_t wmx = 0u;
-#pragma unroll
-        for (int k = 0; k < UNITS; ++k) {
-            const int u = tid + k * kStatsThreads;
-            if (u >= units) continue;
-            const float w8[8] = {wv[k][0].x, wv[k][0].y, wv[k][0].z, wv[k][0].w,
-                                 wv[k][1].x, wv[k][1].y, wv[k][1].z, wv[k][1].w};
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float w = w8[q];
-                const bool ok = w >= 0.f && w <= 3.4028234663852886e38f;   // rejects NaN, inf, < 0
-                wb |= !ok;
-                w = ok ? w + 0.f : 0.f;                                     // -0 -> +0
-                wmx = max(wmx, __float_as_uint(w));                        // w >= 0: bits order
-                if (mpw < 2) continue;
-                const uint32_t key = (keys[k][q >> 1] >> ((q & 1) * 16)) & 0xffffu;
-                int p = 0;
-                p += key >= (uint32_t)sm.bk[7] ? 8 : 0;
-                p += key >= (uint32_t)sm.bk[p + 3] ? 4 : 0;
-                p += key >= (uint32_t)sm.bk[p + 1] ? 2 : 0;
-                p += key >= (uint32_t)sm.bk[p] ? 1 : 0;
-                const float xv = key_value(key);
-                const float y = xv - sm.dc[p], t = sm.dc[p + 1] - xv;
-                const float wy = w * y;
-                float4 *cell = wrow(p) + tid;
-                float4 a = *cell;
-                a.x += w;
-                a.y += wy;
-                a.z += w * t;
-                a.w += wy * t;
-                *cell = a;
-            }
-        }
-        wmx = __reduce_max_sync(0xffffffffu, wmx);
-        const bool anyb = __any_sync(0xffffffffu, wb);
-        if (lane == 0) {
-            atomicMax(&sm.wmax_bits, wmx);
-            if (anyb) atomicOr(&sm.wbad, 1u);
-        }
-    }
 
     // ---- atom moments: half a warp per atom (16 atoms in one pass over the 8
     //      warps).  Sub-lane 0 takes the piece above the atom's lower
@@ -468,40 +368,6 @@ stats_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt, kvq_l
     }
     __syncthreads();
 
-    // ---- weighted variant: sum the 256 columns of each atom in a fixed order
-    //      (warp w takes atoms 2w and 2w+1: lane l adds columns l, l+32, ...,
-    //      then a 32-lane tree)
-    if constexpr (WEIGHTED) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int p = 2 * warp + h;
-            const float4 *r = wrow(p);
-            float4 a = r[lane];
-#pragma unroll
-            for (int c = 1; c < kStatsThreads / 32; ++c) {
-                const float4 b = r[lane + 32 * c];
-                a.x += b.x;
-                a.y += b.y;
-                a.z += b.z;
-                a.w += b.w;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                a.x += __shfl_down_sync(0xffffffffu, a.x, o);
-                a.y += __shfl_down_sync(0xffffffffu, a.y, o);
-                a.z += __shfl_down_sync(0xffffffffu, a.z, o);
-                a.w += __shfl_down_sync(0xffffffffu, a.w, o);
-            }
-            if (lane == 0) {
-                sm.wn[p] = a.x;
-                sm.ws1[p] = a.y;
-                sm.wt1[p] = a.z;
-                sm.we[p] = a.w;
-            }
-        }
-        __syncthreads();
-    }
-
     // ---- pair tables in slot space (candidates 0 .. m'-2 in slots 0 .., the
     //      maximum in slot 16): for a = c_P < b = c_Q, over the atoms p of
     //      [a, b) with A = c_p - a, B = b - c_{p+1}:
@@ -517,13 +383,9 @@ stats_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt, kvq_l
         const float a = sm.dc[P], bq = sm.dc[Q];
         float Dv = 0.f, Us = 0.f, Ls = 0.f;
         for (int p = P; p < Q; ++p) {
-            const float n = sm.an[p], s1 = sm.as1[p], t1 = sm.at1[p];
+            const float n = sm.an[p], s1 = sm.as1[p], t1 = sm.at1[p], e = sm.ae[p];
             const float A = sm.dc[p] - a, Bq = bq - sm.dc[p + 1];
-            if constexpr (WEIGHTED) {
-                Dv += sm.wn[p] * A * Bq + A * sm.wt1[p] + Bq * sm.ws1[p] + sm.we[p];
-            } else {
-                Dv += n * A * Bq + A * t1 + Bq * s1 + sm.ae[p];
-            }
+            Dv += n * A * Bq + A * t1 + Bq * s1 + e;
             Us += s1 + n * A;
             Ls += t1 + n * Bq;
         }
@@ -540,20 +402,17 @@ stats_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt, kvq_l
     //      (non-finite keys live in bins 0..3 and 252..255)
     const bool bad = (sm.cnt[0] | sm.cnt[1] | sm.cnt[2] | sm.cnt[3] | sm.cnt[252] | sm.cnt[253] |
                       sm.cnt[254] | sm.cnt[255]) != 0;
-    const bool wbad = WEIGHTED && sm.wbad != 0u;
-    const int bflags = (bad ? kFlagNonfinite : 0) | (wbad ? kFlagBadWeight : 0) |
-                       (WEIGHTED ? kFlagWeighted : 0);
     float *rec = recs + blk * kRecFloats;
     if (tid < 96) {
         float v = 0.f;
         if (tid < 17) v = sm.dc[tid < mp ? tid : mp - 1];
         else if (tid == 17) v = __int_as_float(mp);
-        else if (tid == 18) v = __int_as_float(bflags);
+        else if (tid == 18) v = __int_as_float(bad ? kFlagNonfinite : 0);
         else if (tid == 19) v = __int_as_float(d);
-        else if (tid < 36) v = WEIGHTED ? sm.wn[tid - 20] : sm.an[tid - 20];
-        else if (tid < 52) v = WEIGHTED ? sm.ws1[tid - 36] : sm.as1[tid - 36];
-        else if (tid < 68) v = WEIGHTED ? sm.wt1[tid - 52] : sm.at1[tid - 52];
-        else if (tid < 84) v = WEIGHTED ? sm.we[tid - 68] : sm.ae[tid - 68];
+        else if (tid < 36) v = sm.an[tid - 20];
+        else if (tid < 52) v = sm.as1[tid - 36];
+        else if (tid < 68) v = sm.at1[tid - 52];
+        else if (tid < 84) v = sm.ae[tid - 68];
         rec[tid] = v;
     }
     float *tb = rec + kRecTbl;
@@ -593,35 +452,23 @@ stats_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt, kvq_l
         tb[kTblC + t] = cv;
     } else if (tid < 24) {
         const int t = tid - 20;
-        tb[kTblHdr + t] = __int_as_float(t == 0 ? mp : t == 1 ? d : t == 2 ? bflags : 0);
+        tb[kTblHdr + t] = __int_as_float(t == 0 ? mp : t == 1 ? d : t == 2 ? (bad ? kFlagNonfinite : 0) : 0);
     } else if (tid == 32) {
         const double wd = (double)sm.dc[mp - 1] - (double)sm.dc[0];
-        double w2 = wd * wd;
-        if constexpr (WEIGHTED) w2 = w2 * (double)__uint_as_float(sm.wmax_bits);
+        const double w2 = wd * wd;
         if (w2 == w2) atomicMax(&hdr->hi0_bits, (unsigned long long)__double_as_longlong(w2));
         if (bad) {
             atomicOr(&hdr->flags, (uint32_t)kFlagNonfinite);
             atomicMax(status, (int32_t)KVQ_ERR_NONFINITE);
         }
-        if (wbad) {
-            atomicOr(&hdr->flags, (uint32_t)kFlagBadWeight);
-            atomicMax(status, (int32_t)KVQ_ERR_BAD_WEIGHT);
-        }
     }
 }
 
-// the weighted variant's static plus dynamic shared memory exceeds the
-// default 48 KB per block: opt in once per device
-int stats_init() {
-    if (cudaFuncSetAttribute(stats_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kWAccDynBytes) != cudaSuccess)
-        return KVQ_ERR_CUDA;
-    if (cudaFuncSetAttribute(stats_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kWAccDynBytes) != cudaSuccess)
-        return KVQ_ERR_CUDA;
-    return KVQ_OK;
-}
+int launch_stats_weights(const uint16_t *x, const float *wt, const kvq_layout &L, int lg_ng,
+                         int lg_upr, void *stats, int32_t *status, cudaStream_t st);
 
+// wt == nullptr: kvq_stats; otherwise kvq_stats_weighted, which runs the
+// weighting pass (kvq_weight.cu) over the records this kernel wrote
 int launch_stats(const uint16_t *x, const float *wt, const kvq_layout &L, void *stats,
                  int32_t *status, cudaStream_t st) {
     const int64_t nb = num_blocks(L);
@@ -635,20 +482,13 @@ int launch_stats(const uint16_t *x, const float *wt, const kvq_layout &L, void *
     StatsHeader *hdr = static_cast<StatsHeader *>(stats);
     float *recs = reinterpret_cast<float *>(static_cast<char *>(stats) + sizeof(StatsHeader));
     const dim3 grid((unsigned)nb);
-    if (wt == nullptr) {
-        if (units <= kStatsThreads)
-            stats_kernel<1, false><<<grid, kStatsThreads, 0, st>>>(x, wt, L, lg_ng, lg_upr, hdr, recs, status);
-        else
-            stats_kernel<2, false><<<grid, kStatsThreads, 0, st>>>(x, wt, L, lg_ng, lg_upr, hdr, recs, status);
-    } else {
-        if (units <= kStatsThreads)
-            stats_kernel<1, true><<<grid, kStatsThreads, kWAccDynBytes, st>>>(x, wt, L, lg_ng, lg_upr, hdr,
-                                                                              recs, status);
-        else
-            stats_kernel<2, true><<<grid, kStatsThreads, kWAccDynBytes, st>>>(x, wt, L, lg_ng, lg_upr, hdr,
-                                                                              recs, status);
-    }
-    return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+    if (units <= kStatsThreads)
+        stats_kernel<1><<<grid, kStatsThreads, 0, st>>>(x, L, lg_ng, lg_upr, hdr, recs, status);
+    else
+        stats_kernel<2><<<grid, kStatsThreads, 0, st>>>(x, L, lg_ng, lg_upr, hdr, recs, status);
+    if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+    if (wt == nullptr) return KVQ_OK;
+    return launch_stats_weights(x, wt, L, lg_ng, lg_upr, stats, status, st);
 }
 
 }  // namespace kvq

@@ -1,0 +1,235 @@
+// Weighting pass of kvq_stats_weighted ("Rate-adaptive KV-cache quantizer",
+// "Implementation notes": optionally weight D_r by the attention sensitivity
+// measured on a calibration batch).
+//
+// Runs after the stats kernel on the records it wrote.  The candidates and
+// the entropy terms do not change (H_r counts the stored symbols, whatever
+// their weight); only the distortion does: D(a, b) = sum w (b - x)(x - a).
+// One CTA of 256 threads per block; every global load is issued first:
+//   1. the block's entries (16-byte loads of x, 32-byte loads of w) go to
+//      their atoms [c_p, c_{p+1}) (the maximum closes the last atom) by a
+//      4-step binary search over the candidates, which sit in lanes and are
+//      read by shuffles;
+//   2. each entry adds (w, w y, w t, w y t), y = x - c_p, t = c_{p+1} - x, to
+//      its thread's float4 column of that atom; threads 0..127 and then
+//      128..255 take turns on the same 128 columns (32 KB of shared memory);
+//   3. a fixed-order tree over the columns gives the weighted atom moments
+//      (repeated calls give identical bits);
+//   4. the pair table D(c_P, c_Q) = sum over the atoms p of [P, Q) of
+//      n A B + A t1 + B s1 + e (A = c_p - c_P, B = c_Q - c_{p+1}) replaces the
+//      record's distortion table; the row's moments become the weighted ones.
+// The bisection's starting point becomes max_r (c_max - c_min)^2 w_max,r.  A
+// negative or non-finite weight counts as 0 and sets KVQ_ERR_BAD_WEIGHT; an
+// entry the stats kernel flagged non-finite counts with weight 0.
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+constexpr int kWThreads = 256;
+constexpr int kWCols = kWThreads / 2;
+constexpr size_t kWColBytes = (size_t)16 * kWCols * sizeof(float4);   // 32 KB
+
+template <int UNITS>
+__global__ void __launch_bounds__(kWThreads, 5)
+stats_weight_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt, kvq_layout L,
+                    int lg_ng, int lg_upr, StatsHeader *__restrict__ hdr,
+                    float *__restrict__ recs, int32_t *__restrict__ status) {
+    extern __shared__ __align__(16) float4 cols[];    // [16 atoms][128 columns]
+    __shared__ float sc[kCand];
+    __shared__ int32_t s_mp, s_rflags, s_tflags;
+    __shared__ float wn[16], ws1[16], wt1[16], we[16];
+    __shared__ float pD[kPairs];
+    __shared__ uint32_t s_wmax, s_wbad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = L.group, D = L.D, d = 32 * G, nG = D / G;
+    const int64_t blk = blockIdx.x;
+    const int g = (int)(blk & (nG - 1));
+    const int64_t tbk = blk >> lg_ng;
+    const int units = d / 8, upr = G / 8;
+    float *rec = recs + blk * kRecFloats;
+    float *tb = rec + kRecTbl;
+    const int col = tid & (kWCols - 1);
+
+    // every global load of the block first: the record's candidates, m' and
+    // flags, and this thread's entries and weights (the second half of the
+    // block waits for its turn with its data already in registers)
+    uint4 xr[UNITS];
+    float4 wa[UNITS], wc[UNITS];
+#pragma unroll
+    for (int k = 0; k < UNITS; ++k) {
+        const int u = tid + k * kWThreads;
+        xr[k] = make_uint4(0u, 0u, 0u, 0u);
+        wa[k] = wc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (u < units) {
+            const int row = u >> lg_upr, cu = u & (upr - 1);
+            const int64_t off = (tbk * 32 + row) * (int64_t)D + (int64_t)g * G + cu * 8;
+            xr[k] = __ldg(reinterpret_cast<const uint4 *>(x + off));
+            wa[k] = __ldg(reinterpret_cast<const float4 *>(wt + off));
+            wc[k] = __ldg(reinterpret_cast<const float4 *>(wt + off + 4));
+        }
+    }
+    if (tid < kCand) sc[tid] = rec[tid];
+    else if (tid == 32) s_mp = __float_as_int(rec[17]);
+    else if (tid == 33) s_rflags = __float_as_int(rec[18]);
+    else if (tid == 34) s_tflags = __float_as_int(tb[kTblHdr + 2]);
+    if (tid < kPairs) pD[tid] = __int_as_float(0x7f800000);   // +inf: no such pair
+    if (tid == 0) {
+        s_wmax = 0u;
+        s_wbad = 0u;
+    }
+    if (tid < kWCols) {
+#pragma unroll
+        for (int p = 0; p < 16; ++p) cols[p * kWCols + col] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+    const int mp = min(max(s_mp, 1), kCand);
+
+    // lane j holds the boundary c_{j+1} (j < m'-2, else +inf) and the level c_j
+    const float inf = __int_as_float(0x7f800000);
+    const float bl = (lane < 16 && lane + 1 <= mp - 2) ? sc[lane + 1] : inf;
+    const float cl = sc[lane < kCand ? lane : kCand - 1];
+    const float b7 = __shfl_sync(0xffffffffu, bl, 7);
+
+    auto scatter = [&]() {
+        bool wb = false;
+        uint32_t wmx = 0u;
+#pragma unroll
+        for (int k = 0; k < UNITS; ++k) {
+            const int u = tid + k * kWThreads;
+            if (u >= units) continue;                         // units is a multiple of 32
+            const uint32_t x4[4] = {xr[k].x, xr[k].y, xr[k].z, xr[k].w};
+            const float w8[8] = {wa[k].x, wa[k].y, wa[k].z, wa[k].w, wc[k].x, wc[k].y, wc[k].z, wc[k].w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {                     // warp-uniform control only
+                float w = w8[q];
+                const bool ok = w >= 0.f && w <= 3.4028234663852886e38f;   // rejects NaN, inf, < 0
+                wb |= !ok;
+                w = ok ? w + 0.f : 0.f;                                     // -0 -> +0
+                wmx = max(wmx, __float_as_uint(w));                        // w >= 0: bits order
+                const uint32_t h = (x4[q >> 1] >> ((q & 1) * 16)) & 0xffffu;
+                // a non-finite entry (flagged by the stats kernel) adds nothing
+                const bool live = (h & 0x7c00u) != 0x7c00u;
+                const float xv = live ? __half2float(__ushort_as_half((unsigned short)h)) : 0.f;
+                if (mp < 2) continue;
+                int p = xv >= b7 ? 8 : 0;
+                p += xv >= __shfl_sync(0xffffffffu, bl, p + 3) ? 4 : 0;
+                p += xv >= __shfl_sync(0xffffffffu, bl, p + 1) ? 2 : 0;
+                p += xv >= __shfl_sync(0xffffffffu, bl, p) ? 1 : 0;
+                const float y = xv - __shfl_sync(0xffffffffu, cl, p);
+                const float t = __shfl_sync(0xffffffffu, cl, p + 1) - xv;
+                const float wy = w * y;
+                float4 *cell = cols + p * kWCols + col;
+                float4 a = *cell;
+                a.x += live ? w : 0.f;
+                a.y += live ? wy : 0.f;
+                a.z += live ? w * t : 0.f;
+                a.w += live ? wy * t : 0.f;
+                *cell = a;
+            }
+        }
+        wmx = __reduce_max_sync(0xffffffffu, wmx);
+        const bool anyb = __any_sync(0xffffffffu, wb);
+        if (lane == 0) {
+            atomicMax(&s_wmax, wmx);
+            if (anyb) atomicOr(&s_wbad, 1u);
+        }
+    };
+    if (tid < kWCols) scatter();
+    __syncthreads();
+    if (tid >= kWCols) scatter();
+    __syncthreads();
+
+    // fixed-order sums: warp w takes atoms 2w and 2w+1; lane l adds columns
+    // l, l+32, l+64, l+96, then a 32-lane tree
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int p = 2 * warp + hh;
+        const float4 *r = cols + p * kWCols;
+        float4 a = r[lane];
+#pragma unroll
+        for (int c = 1; c < kWCols / 32; ++c) {
+            const float4 b = r[lane + 32 * c];
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            a.x += __shfl_down_sync(0xffffffffu, a.x, o);
+            a.y += __shfl_down_sync(0xffffffffu, a.y, o);
+            a.z += __shfl_down_sync(0xffffffffu, a.z, o);
+            a.w += __shfl_down_sync(0xffffffffu, a.w, o);
+        }
+        if (lane == 0) {
+            wn[p] = a.x;
+            ws1[p] = a.y;
+            wt1[p] = a.z;
+            we[p] = a.w;
+        }
+    }
+    __syncthreads();
+
+    // weighted distortion of every candidate pair, in slot space (the maximum
+    // in slot 16), every term non-negative
+    const int npr = mp * (mp - 1) / 2;
+    if (tid < npr) {
+        int P = 0, rem = tid;
+        while (rem >= mp - 1 - P) { rem -= mp - 1 - P; ++P; }
+        const int Q = P + 1 + rem;
+        const float a = sc[P], bq = sc[Q];
+        float Dv = 0.f;
+        for (int p = P; p < Q; ++p) {
+            const float A = sc[p] - a, Bq = bq - sc[p + 1];
+            Dv += wn[p] * A * Bq + A * wt1[p] + Bq * ws1[p] + we[p];
+        }
+        const int sj = P == mp - 1 ? 16 : P, sl = Q == mp - 1 ? 16 : Q;
+        pD[pidx(sj, sl)] = Dv;
+    }
+    __syncthreads();
+
+    const bool wbad = s_wbad != 0u;
+    const int addf = kFlagWeighted | (wbad ? kFlagBadWeight : 0);
+    for (int idx = tid; idx < kDpFloats; idx += kWThreads) {
+        const uint32_t dcd = kDecode.pair[idx];
+        const int j = dcd & 255, l = dcd >> 8;
+        tb[kTblD + idx] = l < 17 ? pD[pidx(j, l)] : inf;
+    }
+    if (tid >= 20 && tid < 84) {
+        const int q = (tid - 20) >> 4, p = (tid - 20) & 15;
+        rec[tid] = q == 0 ? wn[p] : q == 1 ? ws1[p] : q == 2 ? wt1[p] : we[p];
+    } else if (tid == 18) {
+        rec[18] = __int_as_float(s_rflags | addf);
+    } else if (tid == 19) {
+        tb[kTblHdr + 2] = __int_as_float(s_tflags | addf);
+    } else if (tid == 0) {
+        const double wd = (double)sc[mp - 1] - (double)sc[0];
+        const double w2 = (wd * wd) * (double)__uint_as_float(s_wmax);
+        if (w2 == w2) atomicMax(&hdr->hi0_bits, (unsigned long long)__double_as_longlong(w2));
+        if (wbad) {
+            atomicOr(&hdr->flags, (uint32_t)kFlagBadWeight);
+            atomicMax(status, (int32_t)KVQ_ERR_BAD_WEIGHT);
+        }
+    }
+}
+
+int launch_stats_weights(const uint16_t *x, const float *wt, const kvq_layout &L, int lg_ng,
+                         int lg_upr, void *stats, int32_t *status, cudaStream_t st) {
+    const int64_t nb = num_blocks(L);
+    StatsHeader *hdr = static_cast<StatsHeader *>(stats);
+    // the stats kernel left max_r (c_max - c_min)^2 here: start the weighted
+    // maximum afresh
+    if (cudaMemsetAsync(&hdr->hi0_bits, 0, sizeof(hdr->hi0_bits), st) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    float *recs = reinterpret_cast<float *>(static_cast<char *>(stats) + sizeof(StatsHeader));
+    const dim3 grid((unsigned)nb);
+    if (4 * L.group <= kWThreads)
+        stats_weight_kernel<1><<<grid, kWThreads, kWColBytes, st>>>(x, wt, L, lg_ng, lg_upr, hdr,
+                                                                    recs, status);
+    else
+        stats_weight_kernel<2><<<grid, kWThreads, kWColBytes, st>>>(x, wt, L, lg_ng, lg_upr, hdr,
+                                                                    recs, status);
+    return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace kvq
