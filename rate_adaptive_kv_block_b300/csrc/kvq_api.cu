@@ -35,6 +35,7 @@ int launch_entropy_decode(const uint8_t *in, const kvq_layout &L, uint8_t *codes
                           cudaStream_t st);
 size_t entropy_slot(const kvq_layout &L);
 int allocate_init();
+int weights_init();
 int allocate_report(const void *workspace, kvq_report *r);
 
 static bool layout_ok(const kvq_layout &L) {
@@ -61,6 +62,7 @@ static int init_once() {
         state[dev] = allocate_init();
         if (state[dev] == KVQ_OK) state[dev] = quantize_init();
         if (state[dev] == KVQ_OK) state[dev] = attention_init();
+        if (state[dev] == KVQ_OK) state[dev] = weights_init();
         done[dev] = true;
     }
     return state[dev];
@@ -125,6 +127,7 @@ int kvq_stats_weighted(const uint16_t *x, const float *w, kvq_layout L, int m, v
     if (nb > 0 && (!x || !w || !stats || !aligned16(x) || !aligned16(w) || !aligned16(stats)))
         return KVQ_ERR_INVALID_ARG;
     if (nb > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
+    if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
     return launch_stats(x, w, L, stats, status, static_cast<cudaStream_t>(stream));
 }
 

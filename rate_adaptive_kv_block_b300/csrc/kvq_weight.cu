@@ -10,9 +10,10 @@
 //      their atoms [c_p, c_{p+1}) (the maximum closes the last atom) by a
 //      4-step binary search over the candidates, which sit in lanes and are
 //      read by shuffles;
-//   2. each entry adds (w, w y, w t, w y t), y = x - c_p, t = c_{p+1} - x, to
-//      its thread's float4 column of that atom; threads 0..127 and then
-//      128..255 take turns on the same 128 columns (32 KB of shared memory);
+//   2. each entry adds (w y, w t, w y t), y = x - c_p, t = c_{p+1} - x, to
+//      its thread's column of that atom (48 KB of shared memory); the weight
+//      sum of the atom is (sum w y + sum w t) / (c_{p+1} - c_p), since
+//      y + t = c_{p+1} - c_p for every entry (a sum of non-negative terms);
 //   3. a fixed-order tree over the columns gives the weighted atom moments
 //      (repeated calls give identical bits);
 //   4. the pair table D(c_P, c_Q) = sum over the atoms p of [P, Q) of
@@ -26,15 +27,17 @@
 namespace kvq {
 
 constexpr int kWThreads = 256;
-constexpr int kWCols = kWThreads / 2;
-constexpr size_t kWColBytes = (size_t)16 * kWCols * sizeof(float4);   // 32 KB
+// per (atom, thread): (s1, t1) in one float2 array and e in a float array;
+// the weight sum follows from n W = s1 + t1 (y + t = W for every entry)
+constexpr size_t kWColBytes = (size_t)16 * kWThreads * (sizeof(float2) + sizeof(float));   // 48 KB
 
 template <int UNITS>
-__global__ void __launch_bounds__(kWThreads, 5)
+__global__ void __launch_bounds__(kWThreads, 4)
 stats_weight_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt, kvq_layout L,
                     int lg_ng, int lg_upr, StatsHeader *__restrict__ hdr,
                     float *__restrict__ recs, int32_t *__restrict__ status) {
-    extern __shared__ __align__(16) float4 cols[];    // [16 atoms][128 columns]
+    extern __shared__ __align__(16) float2 cst[];     // [16 atoms][256]: (s1, t1)
+    float *ce = reinterpret_cast<float *>(cst + 16 * kWThreads);   // [16 atoms][256]: e
     __shared__ float sc[kCand];
     __shared__ int32_t s_mp, s_rflags, s_tflags;
     __shared__ float wn[16], ws1[16], wt1[16], we[16];
@@ -48,11 +51,9 @@ stats_weight_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt
     const int units = d / 8, upr = G / 8;
     float *rec = recs + blk * kRecFloats;
     float *tb = rec + kRecTbl;
-    const int col = tid & (kWCols - 1);
 
-    // every global load of the block first: the record's candidates, m' and
-    // flags, and this thread's entries and weights (the second half of the
-    // block waits for its turn with its data already in registers)
+    // every global load of the block first: this thread's entries and
+    // weights, and the record's candidates, m' and flags
     uint4 xr[UNITS];
     float4 wa[UNITS], wc[UNITS];
 #pragma unroll
@@ -77,9 +78,10 @@ stats_weight_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt
         s_wmax = 0u;
         s_wbad = 0u;
     }
-    if (tid < kWCols) {
 #pragma unroll
-        for (int p = 0; p < 16; ++p) cols[p * kWCols + col] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < 16; ++p) {
+        cst[p * kWThreads + tid] = make_float2(0.f, 0.f);
+        ce[p * kWThreads + tid] = 0.f;
     }
     __syncthreads();
     const int mp = min(max(s_mp, 1), kCand);
@@ -90,82 +92,77 @@ stats_weight_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt
     const float cl = sc[lane < kCand ? lane : kCand - 1];
     const float b7 = __shfl_sync(0xffffffffu, bl, 7);
 
-    auto scatter = [&]() {
-        bool wb = false;
-        uint32_t wmx = 0u;
+    bool wb = false;
+    uint32_t wmx = 0u;
 #pragma unroll
-        for (int k = 0; k < UNITS; ++k) {
-            const int u = tid + k * kWThreads;
-            if (u >= units) continue;                         // units is a multiple of 32
-            const uint32_t x4[4] = {xr[k].x, xr[k].y, xr[k].z, xr[k].w};
-            const float w8[8] = {wa[k].x, wa[k].y, wa[k].z, wa[k].w, wc[k].x, wc[k].y, wc[k].z, wc[k].w};
+    for (int k = 0; k < UNITS; ++k) {
+        const int u = tid + k * kWThreads;
+        if (u >= units) continue;                             // units is a multiple of 32
+        const uint32_t x4[4] = {xr[k].x, xr[k].y, xr[k].z, xr[k].w};
+        const float w8[8] = {wa[k].x, wa[k].y, wa[k].z, wa[k].w, wc[k].x, wc[k].y, wc[k].z, wc[k].w};
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {                     // warp-uniform control only
-                float w = w8[q];
-                const bool ok = w >= 0.f && w <= 3.4028234663852886e38f;   // rejects NaN, inf, < 0
-                wb |= !ok;
-                w = ok ? w + 0.f : 0.f;                                     // -0 -> +0
-                wmx = max(wmx, __float_as_uint(w));                        // w >= 0: bits order
-                const uint32_t h = (x4[q >> 1] >> ((q & 1) * 16)) & 0xffffu;
-                // a non-finite entry (flagged by the stats kernel) adds nothing
-                const bool live = (h & 0x7c00u) != 0x7c00u;
-                const float xv = live ? __half2float(__ushort_as_half((unsigned short)h)) : 0.f;
-                if (mp < 2) continue;
-                int p = xv >= b7 ? 8 : 0;
-                p += xv >= __shfl_sync(0xffffffffu, bl, p + 3) ? 4 : 0;
-                p += xv >= __shfl_sync(0xffffffffu, bl, p + 1) ? 2 : 0;
-                p += xv >= __shfl_sync(0xffffffffu, bl, p) ? 1 : 0;
-                const float y = xv - __shfl_sync(0xffffffffu, cl, p);
-                const float t = __shfl_sync(0xffffffffu, cl, p + 1) - xv;
-                const float wy = w * y;
-                float4 *cell = cols + p * kWCols + col;
-                float4 a = *cell;
-                a.x += live ? w : 0.f;
-                a.y += live ? wy : 0.f;
-                a.z += live ? w * t : 0.f;
-                a.w += live ? wy * t : 0.f;
-                *cell = a;
-            }
+        for (int q = 0; q < 8; ++q) {                         // warp-uniform control only
+            // a weight is valid when finite and >= 0 (bits below +inf, or -0)
+            const uint32_t wbits = __float_as_uint(w8[q]);
+            const bool ok = wbits < 0x7f800000u || wbits == 0x80000000u;
+            wb |= !ok;
+            const uint32_t h = (x4[q >> 1] >> ((q & 1) * 16)) & 0xffffu;
+            // a non-finite entry (flagged by the stats kernel) adds nothing
+            const bool live = (h & 0x7c00u) != 0x7c00u;
+            const uint32_t wv = ok ? (wbits & 0x7fffffffu) : 0u;
+            wmx = max(wmx, wv);                               // w >= 0: bits order
+            const float w = live ? __uint_as_float(wv) : 0.f;
+            const float xv = live ? __half2float(__ushort_as_half((unsigned short)h)) : 0.f;
+            if (mp < 2) continue;
+            int p = xv >= b7 ? 8 : 0;
+            p += xv >= __shfl_sync(0xffffffffu, bl, p + 3) ? 4 : 0;
+            p += xv >= __shfl_sync(0xffffffffu, bl, p + 1) ? 2 : 0;
+            p += xv >= __shfl_sync(0xffffffffu, bl, p) ? 1 : 0;
+            const float y = xv - __shfl_sync(0xffffffffu, cl, p);
+            const float t = __shfl_sync(0xffffffffu, cl, p + 1) - xv;
+            const float wy = w * y;
+            const int c = p * kWThreads + tid;
+            float2 a = cst[c];
+            a.x += wy;
+            a.y += w * t;
+            cst[c] = a;
+            ce[c] += wy * t;
         }
-        wmx = __reduce_max_sync(0xffffffffu, wmx);
-        const bool anyb = __any_sync(0xffffffffu, wb);
-        if (lane == 0) {
-            atomicMax(&s_wmax, wmx);
-            if (anyb) atomicOr(&s_wbad, 1u);
-        }
-    };
-    if (tid < kWCols) scatter();
-    __syncthreads();
-    if (tid >= kWCols) scatter();
+    }
+    wmx = __reduce_max_sync(0xffffffffu, wmx);
+    const bool anyb = __any_sync(0xffffffffu, wb);
+    if (lane == 0) {
+        atomicMax(&s_wmax, wmx);
+        if (anyb) atomicOr(&s_wbad, 1u);
+    }
     __syncthreads();
 
     // fixed-order sums: warp w takes atoms 2w and 2w+1; lane l adds columns
-    // l, l+32, l+64, l+96, then a 32-lane tree
+    // l, l+32, ..., l+224, then a 32-lane tree
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         const int p = 2 * warp + hh;
-        const float4 *r = cols + p * kWCols;
-        float4 a = r[lane];
+        float2 a = cst[p * kWThreads + lane];
+        float e = ce[p * kWThreads + lane];
 #pragma unroll
-        for (int c = 1; c < kWCols / 32; ++c) {
-            const float4 b = r[lane + 32 * c];
+        for (int c = 1; c < kWThreads / 32; ++c) {
+            const float2 b = cst[p * kWThreads + lane + 32 * c];
             a.x += b.x;
             a.y += b.y;
-            a.z += b.z;
-            a.w += b.w;
+            e += ce[p * kWThreads + lane + 32 * c];
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             a.x += __shfl_down_sync(0xffffffffu, a.x, o);
             a.y += __shfl_down_sync(0xffffffffu, a.y, o);
-            a.z += __shfl_down_sync(0xffffffffu, a.z, o);
-            a.w += __shfl_down_sync(0xffffffffu, a.w, o);
+            e += __shfl_down_sync(0xffffffffu, e, o);
         }
         if (lane == 0) {
-            wn[p] = a.x;
-            ws1[p] = a.y;
-            wt1[p] = a.z;
-            we[p] = a.w;
+            const float W = p + 1 < mp ? sc[p + 1] - sc[p] : 0.f;
+            wn[p] = W > 0.f ? (a.x + a.y) / W : 0.f;     // sum w = (s1 + t1) / W
+            ws1[p] = a.x;
+            wt1[p] = a.y;
+            we[p] = e;
         }
     }
     __syncthreads();
@@ -211,6 +208,18 @@ stats_weight_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt
             atomicMax(status, (int32_t)KVQ_ERR_BAD_WEIGHT);
         }
     }
+}
+
+// the pass's 48 KB of columns plus its static shared memory exceed the
+// default per-block limit: opt in once per device
+int weights_init() {
+    if (cudaFuncSetAttribute(stats_weight_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kWColBytes) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    if (cudaFuncSetAttribute(stats_weight_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kWColBytes) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    return KVQ_OK;
 }
 
 int launch_stats_weights(const uint16_t *x, const float *wt, const kvq_layout &L, int lg_ng,
