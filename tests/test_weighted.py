@@ -297,3 +297,23 @@ def test_weighted_edge_weights_and_status():
         assert gb["status_stats"] == kvq.KVQ_ERR_BAD_WEIGHT
         assert gb["status"] == kvq.KVQ_ERR_BAD_WEIGHT
         assert gb["flags"][5] & 2 and not (gb["flags"][:5] & 2).any()
+
+
+@pytest.mark.gpu
+def test_weighted_bench_layer_full_size():
+    """The bench's weighted leg exactly: the full layer (4096 blocks), its
+    input and its sensitivities, every block against the oracle."""
+    _gpu()
+    import gpu_common as gc
+    wl = synth.workload("llama3_8b_layer")
+    x = synth.make_numpy(wl, seed=0)
+    W = synth.weights_torch(wl, seed=7).cpu().numpy()
+    B = wl.budgets[0] * x.size
+    g = gc.run(x, wl.G, wl.s, B, seed=0, w=W)
+    assert g["status_stats"] == 0 and g["status"] == 0
+    assert g["totals"][0] <= B
+    gc.check_stats(g, oracle.stats(x, wl.G, w=W), weighted=True)
+    ora = oracle.allocate_bisect(x, wl.G, wl.s, B, w=W)
+    assert g["lambda"] == pytest.approx(ora["lambda"], rel=gc.LAM_REL)
+    gc.check_choice(g, x, wl.G, wl.s, g["lambda"], w=W)
+    gc.check_codes(g, x, wl.G, 0, 0)
