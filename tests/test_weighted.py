@@ -317,3 +317,35 @@ def test_weighted_bench_layer_full_size():
     assert g["lambda"] == pytest.approx(ora["lambda"], rel=gc.LAM_REL)
     gc.check_choice(g, x, wl.G, wl.s, g["lambda"], w=W)
     gc.check_codes(g, x, wl.G, 0, 0)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mode", [0, 1])
+def test_weighted_fused_and_subgradient(mode):
+    """With weighted stats, kvq_allocate_quantize gives exactly kvq_allocate +
+    kvq_quantize (bisection and one subgradient step), and the subgradient
+    step is the oracle's weighted one-step map."""
+    _gpu()
+    import torch
+    from rate_adaptive_kv_block_b300 import kvq
+    wl = synth.workload("llama3_8b_layer", T=1024)
+    x = synth.make_numpy(wl, seed=43)
+    W = synth.weights_numpy(wl, seed=43)
+    xd = torch.from_numpy(x.view(np.int16)).view(torch.float16).cuda()
+    wd = torch.from_numpy(W).cuda()
+    L = kvq.Layout(*x.shape, wl.G)
+    B = 2.5 * x.size
+    lam0, eta = (0.0, 0.0) if mode == kvq.KVQ_BISECT40 else (0.12, 1e-7)
+    ref, got = kvq.Buffers(L, 16), kvq.Buffers(L, 16)
+    for b in (ref, got):
+        b.lam.fill_(lam0)
+    kvq.quantize(xd, L, B, 16, seed=3, mode=mode, eta=eta, buf=ref, weights=wd)
+    kvq.quantize(xd, L, B, 16, seed=3, mode=mode, eta=eta, buf=got, weights=wd, fused=True)
+    torch.cuda.synchronize()
+    assert int(ref.status.item()) == 0 and int(got.status.item()) == 0
+    for key in ("codebook", "k", "D_r", "H_r", "totals", "lam", "codes"):
+        a, b = getattr(ref, key), getattr(got, key)
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), key
+    if mode == kvq.KVQ_SUBGRADIENT:
+        o = oracle.allocate_at(x, wl.G, 16, lam0, eta, B, w=W)
+        assert float(ref.lam.item()) == pytest.approx(o["lambda_next"], rel=1e-4, abs=eta * 1e-4 * B)
