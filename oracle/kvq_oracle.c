@@ -408,8 +408,8 @@ static void block_choose(const kvqo_block_t *B, int s, double lambda,
 /* Whole-tensor allocation with one global lambda ("Mathematical statement": */
 /* minimise sum_r D_r s.t. sum_r d_r H_r <= B; the Lagrangian separates the  */
 /* blocks, coupled only through lambda).                                     */
-/* Reading of the lambda search (the page names none; the fixed 40-step      */
-/* bisection is the task's): R(lambda) = sum_r d_r H_r summed in block order */
+/* Reading of the lambda search (the page names none; taken here as a fixed  */
+/* 40-step bisection): R(lambda) = sum_r d_r H_r summed in block order       */
 /* in fp64, feasible iff R <= B.                                             */
 /*   1. if R(0) <= B: lambda = 0.                                            */
 /*   2. lo = 0, hi = max_r (c_max - c_min)^2 (times the block's largest      */
@@ -661,8 +661,8 @@ void kvqo_chain_cost(const uint16_t *x, const float *wt, int64_t T, int D,
 
 /* ------------------------------------------------------------------------ */
 /* Counter-based uniform for the stochastic interpolation.                   */
-/* Reading (the page only asks for an unbiased random choice; the hash is    */
-/* the task's "counter-based hash, u = hash(seed, index) >> 8"): SplitMix64  */
+/* Reading (the page only asks for an unbiased random choice; taken here as  */
+/* a counter-based hash with u = hash(seed, index) >> 8): SplitMix64         */
 /* (Steele, Lea and Flood, OOPSLA 2014) seeded with `seed`; pair p = i >> 1  */
 /* uses the generator's p-th output z_p = mix(seed + (p + 1) * gamma), and   */
 /* hash(seed, i) is its high 32 bits for even i, its low 32 bits for odd i.  */
