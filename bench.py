@@ -118,6 +118,18 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (from /proc/cpuinfo), or "unknown"."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(w, x_np, budget_per_entry, nblocks=CPU_SAMPLE_BLOCKS, seed=0):
     """The oracle, as it stands, on a bounded sample: `nblocks` whole blocks
     (half from K streams, half from V streams), full path (stats, 40-step
@@ -169,7 +181,7 @@ def run_reference(args, rank, world):
         "data": "synthetic", "impl": "reference",
         "config": {"workload": WORKLOAD_DESC, "sample": desc},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": thr, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -674,7 +686,7 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         gbs, dt, thr, desc = cpu_baseline(w, x_np, w.budgets[0])
         cpu = {"value": gbs, "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc,
-               "seconds": dt}
+               "seconds": dt, "cpu_model": cpu_model()}
 
     if rank == 0:
         line = {
