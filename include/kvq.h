@@ -15,6 +15,8 @@
  *
  * Call sequence (all on one CUDA stream, asynchronous, no host sync inside):
  *     kvq_stats      -> per-block candidate levels and interval statistics
+ *                       (kvq_stats_weighted: the same, distortion weighted
+ *                       per entry by the caller's sensitivities)
  *     kvq_allocate   -> lambda, per-block codebook / k / D_r / H_r
  *     kvq_quantize   -> packed codes
  *     kvq_dequantize -> binary16 reconstruction ("decode before attention")
