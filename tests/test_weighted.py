@@ -349,3 +349,18 @@ def test_weighted_fused_and_subgradient(mode):
     if mode == kvq.KVQ_SUBGRADIENT:
         o = oracle.allocate_at(x, wl.G, 16, lam0, eta, B, w=W)
         assert float(ref.lam.item()) == pytest.approx(o["lambda_next"], rel=1e-4, abs=eta * 1e-4 * B)
+
+
+def test_synthetic_sensitivities_have_the_attention_structure():
+    # keys: one weight per (stream, feature), the same for every token;
+    # values: one weight per (stream, token), the same for every feature;
+    # every stream's mean is 1, every weight positive and finite
+    wl = synth.workload("llama3_8b_layer", T=128, S=6)
+    W = synth.weights_numpy(wl, seed=3)
+    assert W.shape == (6, 128, 128) and W.dtype == np.float32
+    assert np.all(np.isfinite(W)) and np.all(W > 0)
+    nk = 3
+    assert np.all(W[:nk] == W[:nk, :1, :])                  # per feature
+    assert np.all(W[nk:] == W[nk:, :, :1])                  # per token
+    assert np.allclose(W.reshape(6, -1).mean(axis=1), 1.0, rtol=1e-5)
+    assert np.all(W[nk:, :4, 0] > W[nk:, 4:, 0].mean(axis=1, keepdims=True))   # sink tokens
