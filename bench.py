@@ -368,7 +368,7 @@ def attention_bench(w, L, buf, flush_l2, graph_of, device_ms, t_flush, nrep, hbm
            "roofline": {"bound": "hbm", "achieved": nbytes / (t_att * 1e-3) / 1e9, "peak": hbm,
                         "unit": "GB/s", "frac": nbytes / (t_att * 1e-3) / 1e9 / hbm,
                         "peak_source": src},
-           "kernels_per_call": 1, "memsets_per_call": 1}
+           "kernels_per_call": 2}
     try:
         y16 = torch.empty((w.S, w.T, D), dtype=torch.float16, device=dev)
         kvq.kvq_dequantize(buf.codes, buf.codebook, L, y16)

@@ -338,8 +338,7 @@ int kvq_entropy_decode(const uint8_t *in, kvq_layout L, uint8_t *codes, int32_t 
  *   T_valid       tokens attended, 0 <= T_valid <= T (0: out = 0).
  *   scale         finite softmax scale (1/sqrt(128) for plain attention).
  *   workspace     device, kvq_attention_workspace_bytes(L, n_rep) bytes of
- *                 scratch (per-split partial results and one finished-split
- *                 counter per KV head, zeroed by the call); overwritten.
+ *                 scratch (per-split partial results); overwritten.
  *   out           device fp32 [S * n_rep][128], written.
  *   status        device int32 or NULL: set to KVQ_ERR_TIMEOUT if a bulk copy
  *                 of codes into shared memory never completed (that token

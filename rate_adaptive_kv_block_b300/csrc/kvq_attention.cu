@@ -12,7 +12,7 @@
 // per block and feature group; nothing is written back as binary16, so the
 // cache is read at 0.5 byte per entry plus 64 bytes of codebook per block.
 //
-// One kernel on the caller's stream (after zeroing one ticket per KV head):
+// Two kernels on the caller's stream:
 //   attn_partial_kernel  grid (splits, KV heads), 128 threads: a range of
 //                        32-token blocks of one KV head with an online
 //                        softmax (running maximum and sum per query head,
@@ -22,10 +22,8 @@
 //                        contiguous in HBM; they arrive in chunks of 4 token
 //                        blocks by bulk (TMA) copies into a two-stage shared
 //                        ring, the next chunk in flight while one is used
-//                        The last split of a KV head to finish (a ticket
-//                        counts them) combines its query heads: rescales the
-//                        splits to a common maximum and divides by the total
-//                        weight.
+//   attn_combine_kernel  one CTA per query head: rescales the splits to a
+//                        common maximum and divides by the total weight
 // Inside a CTA: scores with 8 lanes per token (16 features each, partial dot
 // products combined by a fixed shuffle tree), values with a lane per 8
 // features and 4 tokens (accumulators in registers), the 8 token groups
@@ -67,61 +65,12 @@ __device__ __forceinline__ uint32_t code_offset(int t, int f, int G) {
     return (uint32_t)((f / G) * 16 * G + ((t * G + (f & (G - 1))) >> 1));
 }
 
-// The combine of query head hq (all 128 threads of the CTA): its splits are
-// contiguous in the workspace ([hq][split][max, sum, D outputs]); lane f
-// loads its output of every split at once (the loads in flight together),
-// lanes 0 .. nsplit-1 one (max, sum) pair each; the splits are rescaled to a
-// common maximum and divided by the total weight.  The partials come from
-// other CTAs: read through L2.
-__device__ __forceinline__ void combine_head(const float *part, int nsplit, int64_t hq,
-                                             float *__restrict__ out, float *sw, float *sls,
-                                             float *sM) {
-    constexpr int D = kAttnD;
-    const int f = threadIdx.x;
-    const float NEG = __int_as_float(0xff800000);
-    const float *base = part + hq * nsplit * (D + 2);
-    float o[kAttnMaxSplits];
-#pragma unroll
-    for (int s = 0; s < kAttnMaxSplits; ++s) o[s] = s < nsplit ? __ldcg(base + s * (D + 2) + 2 + f) : 0.f;
-    float m = NEG, l = 0.f;
-    if (f < nsplit) {
-        m = __ldcg(base + f * (D + 2));
-        l = __ldcg(base + f * (D + 2) + 1);
-    }
-    // the maximum over the splits (warps 0 and 1 hold the 64 candidates)
-    float wm = m;
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, k));
-    if (f == 32) sw[0] = wm;
-    __syncthreads();
-    if (f == 0) *sM = fmaxf(wm, sw[0]);
-    __syncthreads();
-    const float M = *sM;
-    if (f < kAttnMaxSplits) {
-        const float w = (M == NEG || m == NEG) ? 0.f : exp2f(m - M);
-        sw[f] = w;
-        sls[f] = w * l;
-    }
-    __syncthreads();
-    float Lw = 0.f, O = 0.f;
-#pragma unroll
-    for (int s = 0; s < kAttnMaxSplits; ++s) {
-        if (s < nsplit) {
-            Lw += sls[s];
-            O = fmaf(sw[s], o[s], O);
-        }
-    }
-    out[hq * D + f] = Lw > 0.f ? O / Lw : 0.f;
-    __syncthreads();   // sw / sls are reused by the next query head
-}
-
 template <int R>
 __global__ void __launch_bounds__(kAttnThreads)
 attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
                     const float *__restrict__ kcb, const uint8_t *__restrict__ vc,
                     const float *__restrict__ vcb, int64_t ntb, int G, int64_t T_valid,
                     float scale2, int bps, int chunk, float *__restrict__ part,
-                    uint32_t *__restrict__ tickets, float *__restrict__ out,
                     int32_t *__restrict__ status) {
     constexpr int D = kAttnD;
     const float NEG = __int_as_float(0xff800000);   // -inf
@@ -308,72 +257,90 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
     if (failed) {
         // a copy never completed: report it, give the copies in flight (this
         // chunk and the next) a bounded chance to land before the shared
-        // memory is released, and leave this split out of the combine (zero
-        // weight and zero outputs)
+        // memory is released, and leave this split out of the combine
         if (tid == 0) {
             if (status) atomicExch(status, KVQ_ERR_TIMEOUT);
             for (int c = cfail; c < cfail + 2 && c < nchunks; ++c)
                 mbar_wait(&bars[c & 1], (uint32_t)(c >> 1) & 1u, kAttnWaitLimit);
         }
-        for (int i = tid; i < R * D; i += kAttnThreads)
-            part[((h * R + i / D) * nsplit + split) * (D + 2) + 2 + i % D] = 0.f;
         if (tid < R) {
             float *pm = part + ((h * R + tid) * nsplit + split) * (D + 2);
             pm[0] = NEG;
             pm[1] = 0.f;
         }
-    } else {
-        // the token groups' outputs, added in a fixed order
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                sacc[tg][r][8 * fg + 2 * b] = acc[r][b].x;
-                sacc[tg][r][8 * fg + 2 * b + 1] = acc[r][b].y;
-            }
         __syncthreads();
-        for (int i = tid; i < R * D; i += kAttnThreads) {
-            const int r = i / D, f = i % D;
-            float o = 0.f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) o += sacc[k][r][f];
-            part[((h * R + r) * nsplit + split) * (D + 2) + 2 + f] = o;
-        }
-        if (tid < R) {
-            float *pm = part + ((h * R + tid) * nsplit + split) * (D + 2);
-            pm[0] = sm[tid];
-            pm[1] = sl[tid];
-        }
+        return;
     }
-    // the last split of this KV head to finish combines its query heads
-    // (the ticket counts finished splits; the launch zeroes it)
-    __shared__ bool last;
-    __shared__ float csw[kAttnMaxSplits], csl[kAttnMaxSplits], cM;
-    __threadfence();
+    // the token groups' outputs, added in a fixed order
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            sacc[tg][r][8 * fg + 2 * b] = acc[r][b].x;
+            sacc[tg][r][8 * fg + 2 * b + 1] = acc[r][b].y;
+        }
     __syncthreads();
-    if (tid == 0) last = atomicAdd(&tickets[h], 1u) == (uint32_t)nsplit - 1u;
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    for (int r = 0; r < R; ++r) combine_head(part, nsplit, h * R + r, out, csw, csl, &cM);
+    for (int i = tid; i < R * D; i += kAttnThreads) {
+        const int r = i / D, f = i % D;
+        float o = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o += sacc[k][r][f];
+        part[((h * R + r) * nsplit + split) * (D + 2) + 2 + f] = o;
+    }
+    if (tid < R) {
+        float *pm = part + ((h * R + tid) * nsplit + split) * (D + 2);
+        pm[0] = sm[tid];
+        pm[1] = sl[tid];
+    }
 }
 
-// Nothing attended (T_valid = 0): no partial CTA runs, so a CTA per query
-// head writes its zero output.
+// Query head hq's splits are contiguous in the workspace ([hq][split][max,
+// sum, D outputs]): lane f loads its output of every split at once (the
+// loads in flight together), lanes 0 .. nsplit-1 one (max, sum) pair each.
 __global__ void __launch_bounds__(kAttnD)
 attn_combine_kernel(const float *__restrict__ part, int nsplit, float *__restrict__ out) {
+    constexpr int D = kAttnD;
     __shared__ float sw[kAttnMaxSplits], sls[kAttnMaxSplits];
     __shared__ float sM;
-    combine_head(part, nsplit, blockIdx.x, out, sw, sls, &sM);
+    const int hq = blockIdx.x, f = threadIdx.x;
+    const float NEG = __int_as_float(0xff800000);
+    const float *base = part + (int64_t)hq * nsplit * (D + 2);
+    float o[kAttnMaxSplits];
+#pragma unroll
+    for (int s = 0; s < kAttnMaxSplits; ++s) o[s] = s < nsplit ? base[s * (D + 2) + 2 + f] : 0.f;
+    float m = NEG, l = 0.f;
+    if (f < nsplit) {
+        m = base[f * (D + 2)];
+        l = base[f * (D + 2) + 1];
+    }
+    // the maximum over the splits (warps 0 and 1 hold the 64 candidates)
+    float wm = m;
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, k));
+    if (f == 32) sw[0] = wm;
+    __syncthreads();
+    if (f == 0) sM = fmaxf(wm, sw[0]);
+    __syncthreads();
+    const float M = sM;
+    if (f < kAttnMaxSplits) {
+        const float w = (M == NEG || m == NEG) ? 0.f : exp2f(m - M);
+        sw[f] = w;
+        sls[f] = w * l;
+    }
+    __syncthreads();
+    float Lw = 0.f, O = 0.f;
+#pragma unroll
+    for (int s = 0; s < kAttnMaxSplits; ++s) {
+        if (s < nsplit) {
+            Lw += sls[s];
+            O = fmaf(sw[s], o[s], O);
+        }
+    }
+    out[(int64_t)hq * D + f] = Lw > 0.f ? O / Lw : 0.f;
 }
 
-// partial results [S * n_rep][splits][max, sum, D outputs], then one ticket per
-// KV head (16-byte aligned)
-__host__ __device__ constexpr size_t attn_part_bytes(int64_t S, int n_rep) {
-    return (size_t)S * kAttnMaxSplits * n_rep * (kAttnD + 2) * sizeof(float);
-}
 size_t attention_workspace_bytes(const kvq_layout &L, int n_rep) {
-    return attn_part_bytes(L.S, n_rep) + (((size_t)L.S * sizeof(uint32_t) + 15) & ~(size_t)15);
+    return (size_t)L.S * kAttnMaxSplits * n_rep * (kAttnD + 2) * sizeof(float);
 }
 
 int attention_init() {
@@ -401,8 +368,6 @@ int launch_decode_attention(const float *q, int n_rep, const kvq_layout &L, cons
     const int64_t ntb = L.T / 32;
     const int64_t ntb_valid = (T_valid + 31) / 32;
     float *part = static_cast<float *>(workspace);
-    uint32_t *tickets = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) +
-                                                     attn_part_bytes(L.S, n_rep));
     int nsplit = 0;
     if (ntb_valid > 0) {
         // one wave (three CTAs per SM at 168 registers) over all KV heads, at
@@ -414,8 +379,6 @@ int launch_decode_attention(const float *q, int n_rep, const kvq_layout &L, cons
         const int64_t bps = (ntb_valid + want - 1) / want;
         nsplit = (int)((ntb_valid + bps - 1) / bps);
         const dim3 grid((unsigned)nsplit, (unsigned)H);
-        if (cudaMemsetAsync(tickets, 0, (size_t)H * sizeof(uint32_t), st) != cudaSuccess)
-            return KVQ_ERR_CUDA;
         const float scale2 = scale * 1.4426950408889634f;   // log2(e)
         // a CTA's range in one chunk when it has at most 8 blocks, else a
         // ring of two stages of 8
@@ -424,23 +387,20 @@ int launch_decode_attention(const float *q, int n_rep, const kvq_layout &L, cons
         switch (n_rep) {
         case 1:
             attn_partial_kernel<1><<<grid, kAttnThreads, smem, st>>>(
-                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, tickets,
-                out, status);
+                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, status);
             break;
         case 2:
             attn_partial_kernel<2><<<grid, kAttnThreads, smem, st>>>(
-                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, tickets,
-                out, status);
+                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, status);
             break;
         default:
             attn_partial_kernel<4><<<grid, kAttnThreads, smem, st>>>(
-                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, tickets,
-                out, status);
+                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, status);
             break;
         }
-        return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+        if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
     }
-    attn_combine_kernel<<<(unsigned)(H * n_rep), kAttnD, 0, st>>>(part, 0, out);
+    attn_combine_kernel<<<(unsigned)(H * n_rep), kAttnD, 0, st>>>(part, nsplit, out);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

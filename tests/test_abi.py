@@ -89,7 +89,7 @@ def test_decode_attention_host_validation():
     the host; its workspace size is one partial result per KV head, split
     and query head."""
     L = kvq.Layout(8, 8192, 128, 128)
-    assert kvq.kvq_attention_workspace_bytes(L, 4) == 8 * 64 * 4 * 130 * 4 + 32   # + a ticket per KV head
+    assert kvq.kvq_attention_workspace_bytes(L, 4) == 8 * 64 * 4 * 130 * 4
     assert kvq.kvq_attention_workspace_bytes(kvq.Layout(8, 8192, 64, 64), 4) == 0   # D != 128
     assert kvq.kvq_attention_workspace_bytes(L, 3) == 0                             # n_rep
     p, odd = _Fake(1 << 20), _Fake((1 << 20) + 8)
