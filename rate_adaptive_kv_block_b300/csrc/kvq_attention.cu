@@ -257,12 +257,15 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
     if (failed) {
         // a copy never completed: report it, give the copies in flight (this
         // chunk and the next) a bounded chance to land before the shared
-        // memory is released, and leave this split out of the combine
+        // memory is released, and leave this split out of the combine (zero
+        // weight and zero outputs, so that it adds nothing)
         if (tid == 0) {
             if (status) atomicExch(status, KVQ_ERR_TIMEOUT);
             for (int c = cfail; c < cfail + 2 && c < nchunks; ++c)
                 mbar_wait(&bars[c & 1], (uint32_t)(c >> 1) & 1u, kAttnWaitLimit);
         }
+        for (int i = tid; i < R * D; i += kAttnThreads)
+            part[((h * R + i / D) * nsplit + split) * (D + 2) + 2 + i % D] = 0.f;
         if (tid < R) {
             float *pm = part + ((h * R + tid) * nsplit + split) * (D + 2);
             pm[0] = NEG;
