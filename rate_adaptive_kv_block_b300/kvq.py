@@ -166,6 +166,10 @@ def kvq_stats(x, L: Layout, stats, status, m: int = 17, stream=None):
 def kvq_stats_weighted(x, w, L: Layout, stats, status, m: int = 17, stream=None):
     """kvq_stats with per-entry distortion weights w (float32 CUDA tensor of
     x's shape)."""
+    if isinstance(w, torch.Tensor) and (w.dtype != torch.float32 or not w.is_contiguous()
+                                        or w.numel() != L.S * L.T * L.D):
+        raise KvqError("kvq_stats_weighted: the weights must be a contiguous float32 tensor "
+                       "with one entry per element of x")
     _check(lib().kvq_stats_weighted(_ptr(x), _ptr(w), L.c(), int(m), _ptr(stats), _ptr(status),
                                     _stream(stream)), "kvq_stats_weighted")
 

@@ -82,6 +82,13 @@ def test_host_validation_rejects_bad_arguments():
     assert lib.kvq_dequantize(None, C.c_void_p(p.p), L.c(), C.c_void_p(p.p), st(s)) == bad
     with pytest.raises(kvq.KvqError):
         kvq.kvq_stats(p, L, p, p, m=16, stream=s)
+    # the binding checks the weights' type and size before any call
+    import torch
+    for wbad in (torch.zeros((2, 64, 128), dtype=torch.float16),
+                 torch.zeros((2, 64, 64), dtype=torch.float32),
+                 torch.zeros((2, 128, 64), dtype=torch.float32).transpose(1, 2)):
+        with pytest.raises(kvq.KvqError, match="weights"):
+            kvq.kvq_stats_weighted(p, wbad, L, p, p, stream=s)
 
 
 def test_decode_attention_host_validation():
