@@ -682,13 +682,14 @@ def main():
     # exact DP of one block at one lambda: 680 (i < j < l) level triples, one
     # fp32 multiply-add and one min each
     dp_ops = sum(rep["active"]) * 32 * 680 * 2
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     if dominant == "allocate":
-        peak = 148 * 128 * sm_mhz * 1e6 / 1e12          # fp32 lane ops, T/s
+        peak = n_sm * 128 * sm_mhz * 1e6 / 1e12         # fp32 lane ops, T/s
         a = dp_ops / (t_acold * 1e-3) / 1e12
         roof = {"kernel": "kvq_allocate (search rounds)", "bound": "alu", "achieved": a,
                 "peak": peak, "unit": "T fp32 lane-op/s", "frac": a / peak, "traffic": None,
                 "work": "%d DP block-lambda evaluations x 680 triples x 2 ops" % (sum(rep["active"]) * 32),
-                "peak_source": "148 SMs x 128 fp32 lanes x median SM clock"}
+                "peak_source": "%d SMs x 128 fp32 lanes x median SM clock" % n_sm}
     elif dominant == "stats":
         a = kern["stats_cold_GBps"]
         roof = {"kernel": "kvq_stats", "bound": "hbm", "achieved": a, "peak": hbm, "unit": "GB/s",

@@ -182,17 +182,24 @@ int kvq_allocate(const void *stats, kvq_layout L, int s, double budget_bits,
  * all.  Arguments, results and statuses are those of kvq_allocate.
  *
  * The scratch is a fixed array of KVQ_STATIC_WORKSPACE_BYTES (8 MiB) in the
- * library's device memory, present on every GPU that loads the library until
- * the process exits.  It holds layouts whose kvq_workspace_bytes(L, s) is at
- * most that size (about 29 400 blocks: 7.5 million entries with group 8,
- * 120 million with group 128); larger layouts return KVQ_ERR_TOO_LARGE without
- * launching anything.
- * Nothing is allocated: the first call on each device looks up the array's
- * address once (cudaGetSymbolAddress) -- make that first call outside any
- * stream capture.  Every call on a device shares the one array, so calls that
- * can overlap in time (different streams, different host threads without a
- * dependency between them) race on it and corrupt each other's results;
- * serialise them.
+ * library's device memory, in the same module as the search kernel.  It holds
+ * layouts whose kvq_workspace_bytes(L, s) is at most that size (about 29 400
+ * blocks: 7.5 million entries with group 8, 120 million with group 128);
+ * larger layouts return KVQ_ERR_TOO_LARGE without launching anything.
+ * The call itself allocates nothing, but the array exists on a device only
+ * once the CUDA runtime has loaded that module there (with the default lazy
+ * module loading: at the library's per-device set-up, run by the first call
+ * on the device of kvq_allocate, kvq_allocate_static, kvq_allocate_quantize,
+ * kvq_quantize, kvq_quantize_nearest, kvq_stats_weighted or
+ * kvq_decode_attention).  That set-up also looks up the array's device
+ * address (cudaGetSymbolAddress) and sets kernel attributes, so make the
+ * first such call on each device at start-up, while device memory is still
+ * free, and outside any stream capture; from then on the array stays until
+ * the process exits.  A set-up that fails returns KVQ_ERR_CUDA, clears the
+ * runtime error, and is tried again by the next call.
+ * Every call on a device shares the one array, so calls that can overlap in
+ * time (different streams, different host threads without a dependency
+ * between them) race on it and corrupt each other's results; serialise them.
  */
 #define KVQ_STATIC_WORKSPACE_BYTES (8u << 20)
 int kvq_allocate_static(const void *stats, kvq_layout L, int s, double budget_bits,

@@ -50,6 +50,15 @@ constexpr int kMaxGrid = 4096;        // CTAs of the persistent search kernel (a
 constexpr int kMaxDevices = 64;
 static int g_resident[kMaxDevices][2][2];   // [device][s < 16][fused]
 
+// Scratch of kvq_allocate_static: a fixed array in this module's global
+// memory, which also holds the search kernel.  The CUDA runtime creates it on
+// a device when it loads this module there, which allocate_init forces (it
+// sets the search kernel's attributes), and frees it when the process exits.
+// Host code cannot use the name as a device address; allocate_init looks the
+// address up once per device (cudaGetSymbolAddress) and keeps it here.
+static __device__ __align__(256) unsigned char g_static_workspace[KVQ_STATIC_WORKSPACE_BYTES];
+static void *g_static_addr[kMaxDevices];
+
 // ---------------------------------------------------------------- workspace
 struct Workspace {
     Ctrl *ctrl;
@@ -1380,7 +1389,17 @@ int allocate_init() {
         setup_search_kernel<true, false>(sms, r[1][0]) != KVQ_OK ||
         setup_search_kernel<true, true>(sms, r[1][1]) != KVQ_OK)
         return KVQ_ERR_CUDA;
+    // the module is loaded on this device now (the attributes above needed
+    // it), so the static scratch exists: take its device address
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr)
+        return KVQ_ERR_CUDA;
+    g_static_addr[dev] = p;
     return KVQ_OK;
+}
+
+void *static_workspace_address(int dev) {
+    return dev >= 0 && dev < kMaxDevices ? g_static_addr[dev] : nullptr;
 }
 
 }  // namespace kvq

@@ -37,6 +37,7 @@ size_t entropy_slot(const kvq_layout &L);
 int allocate_init();
 int weights_init();
 int allocate_report(const void *workspace, kvq_report *r);
+void *static_workspace_address(int dev);
 
 static bool layout_ok(const kvq_layout &L) {
     if (L.S < 0 || L.T < 0 || L.T % 32 != 0) return false;
@@ -51,47 +52,28 @@ static bool layout_ok(const kvq_layout &L) {
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Per-device one-time set-up (function attributes are per device).
+// Per-device one-time set-up (function attributes are per device), under a
+// lock so that host threads making their first call at the same time do it
+// once.  A failed set-up is not remembered: its error is cleared from the
+// runtime's last-error slot, and the next call tries again.
 static int init_once() {
-    static int state[64];
+    static std::mutex mu;
     static bool done[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return KVQ_ERR_CUDA;
     if (dev >= 64) return KVQ_ERR_CUDA;
-    if (!done[dev]) {
-        state[dev] = allocate_init();
-        if (state[dev] == KVQ_OK) state[dev] = quantize_init();
-        if (state[dev] == KVQ_OK) state[dev] = attention_init();
-        if (state[dev] == KVQ_OK) state[dev] = weights_init();
-        done[dev] = true;
-    }
-    return state[dev];
-}
-
-// Scratch of kvq_allocate_static: a fixed array in the module's global
-// memory, created when a device loads the library and held until the process
-// exits.  One copy per device; every call on that device shares it.
-static __device__ __align__(256) unsigned char g_static_workspace[KVQ_STATIC_WORKSPACE_BYTES];
-
-// Device address of g_static_workspace on the current device, looked up once
-// per device (cudaGetSymbolAddress; no allocation).
-static int static_workspace(void **out) {
-    static std::mutex mu;
-    static void *addr[64];
-    static int state[64];
-    static bool done[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
     std::lock_guard<std::mutex> g(mu);
-    if (!done[dev]) {
-        void *p = nullptr;
-        state[dev] = cudaGetSymbolAddress(&p, g_static_workspace) == cudaSuccess ? KVQ_OK
-                                                                                 : KVQ_ERR_CUDA;
-        addr[dev] = p;
-        done[dev] = true;
+    if (done[dev]) return KVQ_OK;
+    int st = allocate_init();
+    if (st == KVQ_OK) st = quantize_init();
+    if (st == KVQ_OK) st = attention_init();
+    if (st == KVQ_OK) st = weights_init();
+    if (st != KVQ_OK) {
+        (void)cudaGetLastError();
+        return st;
     }
-    *out = addr[dev];
-    return state[dev];
+    done[dev] = true;
+    return KVQ_OK;
 }
 }  // namespace kvq
 
@@ -188,8 +170,13 @@ int kvq_allocate_static(const void *stats, kvq_layout L, int s, double budget_bi
     if (!layout_ok(L) || s < 2 || s > kMaxLev) return KVQ_ERR_INVALID_ARG;
     if (workspace_bytes(num_blocks(L), s) > (size_t)KVQ_STATIC_WORKSPACE_BYTES)
         return KVQ_ERR_TOO_LARGE;
-    void *ws = nullptr;
-    if (static_workspace(&ws) != KVQ_OK || !ws) return KVQ_ERR_CUDA;
+    // the per-device set-up (run by the first call of any entry point on the
+    // device) loaded the module that holds the scratch and took its address
+    if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+    void *ws = static_workspace_address(dev);
+    if (!ws) return KVQ_ERR_CUDA;
     // the control block at the start of the scratch is reset by the first
     // kernel of kvq_allocate; nothing else in it is read before it is written
     return kvq_allocate(stats, L, s, budget_bits, mode, eta, lambda, ws, codebook, k, D_r, H_r,

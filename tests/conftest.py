@@ -14,3 +14,5 @@ if TESTS not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line(
         "markers", "gpu: needs a CUDA device (B300); parity of the CUDA path")
+    config.addinivalue_line(
+        "markers", "full: full-size parity against the oracle (minutes of oracle CPU time)")

@@ -1,10 +1,20 @@
-"""kvq_allocate_static: kvq_allocate with the library's fixed device scratch.
+"""kvq_allocate_static: kvq_allocate with the library's fixed device scratch,
+for callers that cannot allocate device memory at the point of the call (a
+caching allocator's own hooks, a serving process whose memory pool is fully
+reserved, a C caller without an allocator).
 
 Called through the C ABI, it must give exactly what kvq_allocate gives with a
 caller-provided workspace, on two calls in a row (the second one reuses the
-scratch the first one left behind), in a fresh process and after the rest of
-the suite.  The layout-size limit is checked on the host.
+scratch the first one left behind).  The file is collected last, so these
+tests run after the rest of the suite in the same process; one more test runs
+the comparison in a fresh child process where kvq_allocate_static is the first
+call that runs the library's per-device set-up.  The layout-size limit is
+checked on the host.
 """
+import os
+import subprocess
+import sys
+
 import pytest
 import torch
 
@@ -98,6 +108,56 @@ def test_static_scratch_back_to_back_on_one_stream():
     torch.cuda.synchronize()
     for r, g in zip(refs, gots):
         _same(r, g)
+
+
+_FRESH = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1])
+from rate_adaptive_kv_block_b300 import kvq, synth
+torch.cuda.set_device(0)
+w = synth.workload("llama3_8b_layer", T=1024, S=16)
+x = synth.make_torch(w, seed=5, device="cuda")
+L = kvq.Layout(w.S, w.T, w.D, w.G)
+st = torch.zeros(1, dtype=torch.int32, device="cuda")
+stats = torch.empty(kvq.kvq_stats_bytes(L), dtype=torch.uint8, device="cuda")
+kvq.kvq_stats(x, L, stats, st)          # runs no per-device set-up
+B = 2.5 * w.entries
+def outs():
+    nb = L.nblocks
+    return [torch.full((nb, 16), float("nan"), device="cuda"),
+            torch.full((nb,), 255, dtype=torch.uint8, device="cuda"),
+            torch.full((nb,), float("nan"), device="cuda"),
+            torch.full((nb,), float("nan"), device="cuda"),
+            torch.full((3,), float("nan"), dtype=torch.float64, device="cuda"),
+            torch.zeros(1, dtype=torch.float64, device="cuda"),
+            torch.full((1,), -1, dtype=torch.int32, device="cuda")]
+runs = []
+for _ in range(2):                      # the set-up call, then a call on the set-up device
+    cb, k, D, H, tot, lam, sts = outs()
+    kvq.kvq_allocate_static(stats, L, w.s, B, kvq.KVQ_BISECT40, 0.0, lam, cb, k, D, H, tot, sts)
+    runs.append([cb, k, D, H, tot, lam, sts])
+cb, k, D, H, tot, lam, sts = outs()
+ws = torch.empty(kvq.kvq_workspace_bytes(L, w.s), dtype=torch.uint8, device="cuda")
+kvq.kvq_allocate(stats, L, w.s, B, kvq.KVQ_BISECT40, 0.0, lam, ws, cb, k, D, H, tot, sts)
+torch.cuda.synchronize()
+ref = [cb, k, D, H, tot, lam, sts]
+assert int(sts.item()) == 0
+for got in runs:
+    for a, b in zip(ref, got):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+print("FRESH_OK")
+"""
+
+
+@pytest.mark.gpu
+def test_static_scratch_in_a_fresh_process():
+    """In a new process the first kvq_allocate_static call runs the library's
+    per-device set-up (module load, address look-up); it and the next call
+    match kvq_allocate."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FRESH, root], capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "FRESH_OK" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
 
 
 def test_static_scratch_limit_rejected_on_host():
