@@ -27,6 +27,8 @@ def lib():
         vp = C.c_void_p
         L.kvqo_hash32.restype = C.c_uint32
         L.kvqo_hash32.argtypes = [u64, u64]
+        L.kvqo_philox4x32.restype = None
+        L.kvqo_philox4x32.argtypes = [vp, vp, C.c_int, vp]
         L.kvqo_hash_many.restype = None
         L.kvqo_hash_many.argtypes = [u64, u64, i64, vp]
         L.kvqo_set_threads.restype = C.c_int
@@ -102,6 +104,15 @@ def set_threads(n: int) -> int:
 
 def hash32(seed: int, i: int) -> int:
     return lib().kvqo_hash32(seed, i)
+
+
+def philox4x32(ctr, key, rounds: int):
+    """The Philox4x32 block function: 4 counter words, 2 key words -> 4 words."""
+    c = np.ascontiguousarray(np.asarray(ctr, dtype=np.uint32))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+    out = np.zeros(4, dtype=np.uint32)
+    lib().kvqo_philox4x32(_p(c), _p(k), int(rounds), _p(out))
+    return [int(v) for v in out]
 
 
 def hash_many(seed: int, i0: int, n: int) -> np.ndarray:

@@ -662,20 +662,52 @@ void kvqo_chain_cost(const uint16_t *x, const float *wt, int64_t T, int D,
 /* ------------------------------------------------------------------------ */
 /* Counter-based uniform for the stochastic interpolation.                   */
 /* Reading (the page only asks for an unbiased random choice; taken here as  */
-/* a counter-based hash with u = hash(seed, index) >> 8): SplitMix64         */
-/* (Steele, Lea and Flood, OOPSLA 2014) seeded with `seed`; pair p = i >> 1  */
-/* uses the generator's p-th output z_p = mix(seed + (p + 1) * gamma), and   */
-/* hash(seed, i) is its high 32 bits for even i, its low 32 bits for odd i.  */
+/* a counter-based hash with u = hash(seed, index) >> 8): the Philox4x32     */
+/* block function (Salmon, Moraes, Dror and Shaw, "Parallel random numbers:  */
+/* as easy as 1, 2, 3", SC 2011) with 7 rounds, the fewest rounds that paper  */
+/* found to pass TestU01's BigCrush.  Index i uses counter block c = i >> 2  */
+/* as the counter (c mod 2^32, c >> 32, 0, 0) and the key (seed mod 2^32,    */
+/* seed >> 32); hash(seed, i) is output word i mod 4.                        */
+/* One round: the products M0 * x0 and M1 * x2 (32 x 32 -> 64 bits) give     */
+/* hi/lo words, the new block is (hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0),   */
+/* and the key is bumped by the Weyl constants (W0, W1) after each round.    */
 /* ------------------------------------------------------------------------ */
+
+#define KVQO_PHILOX_ROUNDS 7
+
+void kvqo_philox4x32(const uint32_t ctr[4], const uint32_t key[2], int rounds,
+                     uint32_t out[4])
+{
+    const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < rounds; r++) {
+        uint64_t p0 = (uint64_t)M0 * x0;
+        uint64_t p1 = (uint64_t)M1 * x2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        x0 = hi1 ^ x1 ^ k0;
+        x1 = lo1;
+        x2 = hi0 ^ x3 ^ k1;
+        x3 = lo0;
+        k0 += W0;
+        k1 += W1;
+    }
+    out[0] = x0;
+    out[1] = x1;
+    out[2] = x2;
+    out[3] = x3;
+}
 
 uint32_t kvqo_hash32(uint64_t seed, uint64_t i)
 {
-    uint64_t p = i >> 1;
-    uint64_t z = seed + (p + 1u) * 0x9E3779B97F4A7C15ull;
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    z = z ^ (z >> 31);
-    return (i & 1u) ? (uint32_t)(z & 0xffffffffu) : (uint32_t)(z >> 32);
+    uint64_t c = i >> 2;
+    uint32_t ctr[4] = {(uint32_t)c, (uint32_t)(c >> 32), 0u, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    kvqo_philox4x32(ctr, key, KVQO_PHILOX_ROUNDS, out);
+    return out[i & 3u];
 }
 
 /* many hashes at once: out[n] = hash(seed, i0 + n) */

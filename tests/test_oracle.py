@@ -41,16 +41,77 @@ def f16(v):
 
 # --------------------------------------------------------------------- hash
 
-def test_splitmix64_published_outputs():
-    # First outputs of the SplitMix64 generator started from state 0
-    # (Steele, Lea, Flood, "Fast splittable pseudorandom number generators",
-    # OOPSLA 2014; the public-domain reference splitmix64.c).  hash(0, i) is
-    # the high half of output i//2 for even i, the low half for odd i.
-    published = [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F,
-                 0xF88BB8A8724C81EC, 0x1B39896A51A8749B]
-    for p, z in enumerate(published):
-        assert oracle.hash32(0, 2 * p) == z >> 32
-        assert oracle.hash32(0, 2 * p + 1) == z & 0xFFFFFFFF
+# Known-answer vectors of the Philox4x32 block function published with the
+# Random123 library (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+# easy as 1, 2, 3", SC 2011): rounds, counter (4 words), key (2 words) ->
+# output (4 words).
+PHILOX_KAT = [
+    (7, [0, 0, 0, 0], [0, 0], [0x5F6FB709, 0x0D893F64, 0x4F121F81, 0x4F730A48]),
+    (10, [0, 0, 0, 0], [0, 0], [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]),
+    (10, [0xFFFFFFFF] * 4, [0xFFFFFFFF] * 2, [0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD]),
+    (10, [0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344], [0xA4093822, 0x299F31D0],
+     [0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1]),
+]
+
+
+@pytest.mark.parametrize("rounds,ctr,key,want", PHILOX_KAT)
+def test_philox_published_vectors(rounds, ctr, key, want):
+    assert oracle.philox4x32(ctr, key, rounds) == want
+
+
+def test_hash_is_philox7_word_of_the_counter_block():
+    # hash(seed, i) = word i mod 4 of Philox4x32-7 at counter (i >> 2 as two
+    # 32-bit words, 0, 0) and key (seed as two 32-bit words)
+    assert [oracle.hash32(0, i) for i in range(4)] == PHILOX_KAT[0][3]
+    for seed, c in [(1, 0), (0x123456789ABCDEF0, 5), (7, (1 << 38) + 3), (2 ** 64 - 1, 2 ** 40 // 4)]:
+        want = oracle.philox4x32([c & 0xFFFFFFFF, c >> 32, 0, 0],
+                                 [seed & 0xFFFFFFFF, seed >> 32], 7)
+        assert [oracle.hash32(seed, 4 * c + j) for j in range(4)] == want
+    assert list(oracle.hash_many(9, 4 * 77, 8)) == [oracle.hash32(9, 4 * 77 + j) for j in range(8)]
+
+
+def _find_index(seed, pred, start=0, n=1 << 18):
+    h = oracle.hash_many(seed, start, n)
+    hits = np.nonzero(pred(h >> 8))[0]
+    assert len(hits), "no index found"
+    return start + int(hits[0]), int(h[hits[0]] >> 8)
+
+
+def test_rounding_rule_is_strict_at_a_tie():
+    # Levels 0 and 1: w = 1, so fl(u 2^-24 * w) = u 2^-24 exactly.  For an
+    # index whose u has at most 11 significant bits, x = u 2^-24 is a binary16
+    # value and the rule's two sides are equal: the entry must stay at the
+    # lower level (choose q_{i+1} only when fl(t w) < fl(x - q_i)); one
+    # binary16 step above x it must move up, one step below it must not.
+    seed = 4242
+    idx, u = _find_index(seed, lambda u: ((u & 0x1FFF) == 0) & (u >= (1 << 13)))
+    x_tie = u * 2.0 ** -24
+    assert float(np.float16(x_tie)) == x_tie
+    up = float(np.nextafter(np.float16(x_tie), np.float16(1)))
+    dn = float(np.nextafter(np.float16(x_tie), np.float16(0)))
+    q = np.zeros((1, 16), dtype=np.float32)
+    q[0, 1:] = 1.0
+    k = np.array([2], dtype=np.uint8)
+    for xv, want in [(x_tie, 0), (up, 1), (dn, 0)]:
+        # block of 32 x 1 entries (G = 1): put the value at the entry whose
+        # global index is idx (index_base = idx - e for entry e = 0)
+        x = np.zeros((1, 32, 1), dtype=np.float16)
+        x[0, 0, 0] = xv
+        x[0, 1:, 0] = 0.5
+        codes = oracle.quantize(x.view(np.uint16), 1, q, k, seed, idx)
+        assert codes[0, 0] & 15 == want, (xv, want)
+
+
+def test_rounding_rule_uses_the_interval_below_a_level():
+    # x equal to a level: interval i is the largest with q_i <= x (capped at
+    # k-2), and under the rule the code is exactly that level whatever u is
+    q = np.array([[-1.0, 0.25, 0.5, 3.0] + [3.0] * 12], dtype=np.float32)
+    k = np.array([4], dtype=np.uint8)
+    x = np.tile(np.array([-1.0, 0.25, 0.5, 3.0], dtype=np.float16), 8).reshape(1, 32, 1)
+    for seed in range(20):
+        codes = oracle.quantize(x.view(np.uint16), 1, q, k, seed, 4 * seed)
+        c = np.stack([codes[0] & 15, codes[0] >> 4], axis=-1).reshape(-1)
+        assert np.array_equal(c, np.tile([0, 1, 2, 3], 8))
 
 
 def test_hash_uniform_chi2():
