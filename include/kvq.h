@@ -233,14 +233,16 @@ int kvq_allocate_quantize(const void *stats, const uint16_t *x, kvq_layout L, in
  * q_i <= x, capped at k-2; u = hash(seed, index_base + flat index) >> 8; the
  * code is i+1 iff fl(u 2^-24 * (q_{i+1} - q_i)) < fl(x - q_i) in fp32
  * round-to-nearest (no fused multiply-add), else i; k = 1 gives code 0.
- * hash(seed, n) is the SplitMix64 generator seeded with `seed`: output
- * number n>>1, its high 32 bits for even n, low 32 bits for odd n.
+ * hash(seed, n) is word n mod 4 of the Philox4x32 block function with 7
+ * rounds (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+ * 1, 2, 3", SC 2011) at counter (n >> 2 as two 32-bit words, 0, 0) and key
+ * (seed as two 32-bit words).
  *   x           device [S,T,D] binary16.
  *   codebook, k as written by kvq_allocate (k must be the number of distinct
  *               levels, with slots k..15 repeating the largest: the kernel
  *               takes k from the codebook itself).
  *   seed        any 64-bit value.
- *   index_base  even, and index_base + S*T*D <= 2^40.
+ *   index_base  a multiple of 4, and index_base + S*T*D <= 2^40.
  *   codes       device uint8 [nblocks][16*group]: byte e/2 of block r holds
  *               entry e in its low nibble (e even) or high nibble (e odd).
  *   status      device int32 or NULL: set to KVQ_ERR_TIMEOUT if a copy into

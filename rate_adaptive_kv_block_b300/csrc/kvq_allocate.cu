@@ -423,7 +423,8 @@ __device__ void dp_path_b(const float *__restrict__ tb, float lam, int s,
 struct QuantArgs {
     const uint16_t *x;      // [S, T, D] binary16
     uint8_t *codes;         // [nblocks][16 group]
-    uint64_t seed, index_base;
+    uint64_t index_base;
+    PhiloxKey key;          // round keys of the seed
     int D, G;
     int lg_ng;              // log2(D / G)
     int lg_upr;             // log2(G / 8)
@@ -517,7 +518,7 @@ __device__ __forceinline__ void fused_codes(const QuantArgs &qa, int64_t b, int 
             const int row = 4 * part + (u >> qa.lg_upr), cu = u & (upr - 1);
             const int64_t flat = (tbk * 32 + row) * (int64_t)qa.D + (int64_t)g * G + cu * 8;
             const uint32_t packed =
-                quant8(raw[r], T, qw, quant_state(qa.seed, qa.index_base, (uint64_t)flat));
+                quant8(raw[r], T, qw, quant_counter(qa.index_base, (uint64_t)flat), qa.key);
             *reinterpret_cast<uint32_t *>(qa.codes + b * (int64_t)(16 * G) +
                                           ((row * G + cu * 8) >> 1)) = packed;
         }
@@ -1317,7 +1318,7 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
     if (quant) {
         qa.x = x;
         qa.codes = codes;
-        qa.seed = seed;
+        qa.key = philox_key(seed);
         qa.index_base = index_base;
         qa.D = L.D;
         qa.G = L.group;

@@ -143,7 +143,7 @@ int kvq_allocate_quantize(const void *stats, const uint16_t *x, kvq_layout L, in
     if (mode != KVQ_BISECT40 && mode != KVQ_SUBGRADIENT) return KVQ_ERR_INVALID_ARG;
     if (!(eta >= 0.0) || !isfinite(eta)) return KVQ_ERR_INVALID_ARG;
     if (!lambda || !totals || !status) return KVQ_ERR_INVALID_ARG;
-    if (index_base & 1u) return KVQ_ERR_INVALID_ARG;
+    if (index_base & 3u) return KVQ_ERR_INVALID_ARG;
     const uint64_t n = (uint64_t)L.S * (uint64_t)L.T * (uint64_t)L.D;
     if (index_base > (1ull << 40) || n > (1ull << 40) - index_base) return KVQ_ERR_INVALID_ARG;
     const int64_t nb = num_blocks(L);
@@ -187,7 +187,7 @@ int kvq_quantize(const uint16_t *x, kvq_layout L, const float *codebook, const u
                  uint64_t seed, uint64_t index_base, uint8_t *codes, int32_t *status,
                  void *stream) {
     if (!layout_ok(L)) return KVQ_ERR_INVALID_ARG;
-    if (index_base & 1u) return KVQ_ERR_INVALID_ARG;
+    if (index_base & 3u) return KVQ_ERR_INVALID_ARG;
     const uint64_t n = (uint64_t)L.S * (uint64_t)L.T * (uint64_t)L.D;
     if (index_base > (1ull << 40) || n > (1ull << 40) - index_base) return KVQ_ERR_INVALID_ARG;
     if (n > 0) {

@@ -5,10 +5,10 @@
 // For one block with levels q_0 < ... < q_{k-1} (slots k..15 repeat q_{k-1}):
 //   thresholds  T_j = q_j for 1 <= j <= k-2, +inf beyond (binary16 pairs);
 //   decision    (-q_i, w_i) with w_i = (q_{i+1} - q_i) 2^-24 (k = 1: w = +inf).
-// An entry x gets i = #{j : T_j <= x} (a 4-level binary search over the 15
-// sorted thresholds) and code i + [fl(u w_i) < fl(x - q_i)], fp32
-// round-to-nearest, u = hash >> 8; hash(seed, n) = SplitMix64 output n>>1,
-// high word for even n, low word for odd n.
+// An entry x gets i = #{j : T_j <= x} and code i + [fl(u w_i) < fl(x - q_i)],
+// fp32 round-to-nearest, u = hash >> 8.  hash(seed, n) is word n mod 4 of the
+// Philox4x32 block function with 7 rounds (Salmon, Moraes, Dror, Shaw, SC
+// 2011) at counter (n >> 2 as two words, 0, 0) and key (seed as two words).
 #pragma once
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -16,32 +16,58 @@
 
 namespace kvq {
 
-constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;
+constexpr int kPhiloxRounds = 7;
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u, kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u, kPhiloxW1 = 0xBB67AE85u;
+
+// The round keys of one seed: round r uses (seed_lo + r W0, seed_hi + r W1).
+// Passed by value in kernel parameters, so the xors read them from the
+// constant bank.
+struct PhiloxKey {
+    uint32_t k0[kPhiloxRounds], k1[kPhiloxRounds];
+};
+
+__host__ __device__ inline PhiloxKey philox_key(uint64_t seed) {
+    PhiloxKey K;
+    uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+    for (int r = 0; r < kPhiloxRounds; ++r) {
+        K.k0[r] = a;
+        K.k1[r] = b;
+        a += kPhiloxW0;
+        b += kPhiloxW1;
+    }
+    return K;
+}
+
+// Philox4x32-7 of the counter (c0, c1, 0, 0): round 0 multiplies a zero
+// word, so it is one 32 x 32 -> 64-bit product; each later round is two.
+__device__ __forceinline__ uint4 philox7(uint32_t c0, uint32_t c1, const PhiloxKey &K) {
+    uint64_t p0 = (uint64_t)kPhiloxM0 * c0;
+    uint32_t x0 = c1 ^ K.k0[0];
+    uint32_t x1 = 0u;
+    uint32_t x2 = (uint32_t)(p0 >> 32) ^ K.k1[0];
+    uint32_t x3 = (uint32_t)p0;
+#pragma unroll
+    for (int r = 1; r < kPhiloxRounds; ++r) {
+        const uint64_t a = (uint64_t)kPhiloxM0 * x0;
+        const uint64_t b = (uint64_t)kPhiloxM1 * x2;
+        x0 = (uint32_t)(b >> 32) ^ x1 ^ K.k0[r];
+        x1 = (uint32_t)b;
+        x2 = (uint32_t)(a >> 32) ^ x3 ^ K.k1[r];
+        x3 = (uint32_t)a;
+    }
+    return make_uint4(x0, x1, x2, x3);
+}
+
+// Counter block of global entry n (n a multiple of 4): n >> 2.
+__device__ __forceinline__ uint64_t quant_counter(uint64_t index_base, uint64_t flat) {
+    return (index_base + flat) >> 2;
+}
 
 __device__ __forceinline__ __half2 as_h2(uint32_t u) {
     __half2 h;
     memcpy(&h, &u, 4);
     return h;
-}
-
-// SplitMix64 output function (Steele, Lea, Flood 2014), written on the two
-// 32-bit halves (hi:lo) of the state so that each step is one funnel shift,
-// one xor or one 32-bit multiply-add: returns the output's high and low words.
-__device__ __forceinline__ void splitmix_mix(uint32_t lo, uint32_t hi, uint32_t &ohi,
-                                             uint32_t &olo) {
-    // z ^= z >> 30; z *= 0xBF58476D1CE4E5B9
-    lo ^= __funnelshift_r(lo, hi, 30);
-    hi ^= hi >> 30;
-    const uint32_t nlo0 = lo * 0x1CE4E5B9u;
-    const uint32_t nhi0 = __umulhi(lo, 0x1CE4E5B9u) + lo * 0xBF58476Du + hi * 0x1CE4E5B9u;
-    // z ^= z >> 27; z *= 0x94D049BB133111EB
-    const uint32_t nlo = nlo0 ^ __funnelshift_r(nlo0, nhi0, 27);
-    const uint32_t nhi = nhi0 ^ (nhi0 >> 27);
-    lo = nlo * 0x133111EBu;
-    hi = __umulhi(nlo, 0x133111EBu) + nlo * 0x94D049BBu + nhi * 0x133111EBu;
-    // z ^= z >> 31
-    olo = lo ^ __funnelshift_r(lo, hi, 31);
-    ohi = hi ^ (hi >> 31);
 }
 
 // Threshold j (0..15) and decision entry j of a block from its 16 codebook
@@ -63,12 +89,15 @@ __device__ __forceinline__ void quant_table_entry(const float *q, int k, int j, 
 }
 
 // Codes of 8 consecutive entries (one 16-byte load `raw`) of one block:
-// T[1..15] the thresholds as binary16 pairs, qw the decision table, z the
-// SplitMix64 state of the first pair.  Returns 8 nibbles, entry e in bits
-// 4e..4e+3.
+// T[1..15] the thresholds as binary16 pairs, qw the decision table, c the
+// Philox counter of the first 4 entries (the next 4 use c + 1).  Returns 8
+// nibbles, entry e in bits 4e..4e+3.
 __device__ __forceinline__ uint32_t quant8(const uint4 raw, const uint32_t (&T)[16],
-                                           const float2 *qw, uint64_t z) {
+                                           const float2 *qw, uint64_t c, const PhiloxKey &K) {
     const uint32_t xw0 = raw.x, xw1 = raw.y, xw2 = raw.z, xw3 = raw.w;
+    const uint4 ha = philox7((uint32_t)c, (uint32_t)(c >> 32), K);
+    const uint64_t c1 = c + 1u;
+    const uint4 hb = philox7((uint32_t)c1, (uint32_t)(c1 >> 32), K);
     uint32_t packed = 0;
 #pragma unroll
     for (int pr = 0; pr < 4; ++pr) {
@@ -90,16 +119,15 @@ __device__ __forceinline__ uint32_t quant8(const uint4 raw, const uint32_t (&T)[
                              (m4 & 0x00010001u);
         const int i0 = (int)(idx & 15u), i1 = (int)(idx >> 16);
         const float2 e0 = qw[i0], e1 = qw[i1];
-        uint32_t hhi, hlo;
-        splitmix_mix((uint32_t)z, (uint32_t)(z >> 32), hhi, hlo);
-        z += kGolden;
+        const uint32_t h0 = pr == 0 ? ha.x : pr == 1 ? ha.z : pr == 2 ? hb.x : hb.z;
+        const uint32_t h1 = pr == 0 ? ha.y : pr == 1 ? ha.w : pr == 2 ? hb.y : hb.w;
         const float2 xf = __half22float2(X);
         const float2 r = __fadd2_rn(xf, make_float2(e0.x, e1.x));          // x - q_i
-        const float2 u = make_float2((float)(hhi >> 8), (float)(hlo >> 8));
+        const float2 u = make_float2((float)(h0 >> 8), (float)(h1 >> 8));
         const float2 tw = __fmul2_rn(u, make_float2(e0.y, e1.y));
         const uint32_t c0 = (uint32_t)i0 + (tw.x < r.x ? 1u : 0u);
-        const uint32_t c1 = (uint32_t)i1 + (tw.y < r.y ? 1u : 0u);
-        packed |= (c0 | (c1 << 4)) << (8 * pr);
+        const uint32_t cc1 = (uint32_t)i1 + (tw.y < r.y ? 1u : 0u);
+        packed |= (c0 | (cc1 << 4)) << (8 * pr);
     }
     return packed;
 }
@@ -139,11 +167,6 @@ __device__ __forceinline__ uint32_t quant8_nearest(const uint4 raw, const uint32
         packed |= (c0 | (c1 << 4)) << (8 * pr);
     }
     return packed;
-}
-
-// SplitMix64 state of the pair holding global entry `flat` (even) for `seed`.
-__device__ __forceinline__ uint64_t quant_state(uint64_t seed, uint64_t index_base, uint64_t flat) {
-    return seed + ((index_base + flat) / 2 + 1) * kGolden;
 }
 
 }  // namespace kvq

@@ -75,8 +75,9 @@ def test_host_validation_rejects_bad_arguments():
     for s_, B, mode, eta in [(1, 1.0, 0, 0.0), (17, 1.0, 0, 0.0), (8, -1.0, 0, 0.0),
                              (8, float("nan"), 0, 0.0), (8, 1.0, 2, 0.0), (8, 1.0, 1, -1.0)]:
         assert lib.kvq_allocate(C.c_void_p(p.p), L.c(), s_, B, mode, eta, *args, st(s)) == bad
-    assert lib.kvq_quantize(C.c_void_p(p.p), L.c(), C.c_void_p(p.p), C.c_void_p(p.p), 0, 1,
-                            C.c_void_p(p.p), None, st(s)) == bad               # odd base
+    for base in (1, 2, 6):                                                     # base % 4 != 0
+        assert lib.kvq_quantize(C.c_void_p(p.p), L.c(), C.c_void_p(p.p), C.c_void_p(p.p), 0,
+                                base, C.c_void_p(p.p), None, st(s)) == bad
     assert lib.kvq_quantize(C.c_void_p(p.p), L.c(), C.c_void_p(p.p), C.c_void_p(p.p), 0,
                             (1 << 40) - 1000, C.c_void_p(p.p), None, st(s)) == bad   # 2^40 cap
     assert lib.kvq_dequantize(None, C.c_void_p(p.p), L.c(), C.c_void_p(p.p), st(s)) == bad

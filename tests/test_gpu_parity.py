@@ -77,7 +77,7 @@ def test_quantize_bit_exact_with_given_codebooks(name, T, G):
     cb = torch.from_numpy(at["codebook"]).cuda()
     kk = torch.from_numpy(at["k"]).cuda()
     codes = torch.empty((L.nblocks, 16 * G), dtype=torch.uint8, device="cuda")
-    for seed, base in [(0, 0), (12345, 2), (2**63 + 7, 2**39)]:
+    for seed, base in [(0, 0), (12345, 4), (2**63 + 7, 2**39), (99, 2**40 - 2**22)]:
         kvq.kvq_quantize(xd, L, cb, kk, seed, base, codes)
         ref = oracle.quantize(x, G, at["codebook"], at["k"], seed, base)
         assert np.array_equal(codes.cpu().numpy(), ref)
@@ -85,6 +85,64 @@ def test_quantize_bit_exact_with_given_codebooks(name, T, G):
     kvq.kvq_dequantize(codes, cb, L, y)
     ref_y = oracle.dequantize(codes.cpu().numpy(), at["codebook"], x.shape, G)
     assert np.array_equal(gc.to_np(y), ref_y)
+
+
+def _crowded_codebooks(nb, G, rng):
+    """Codebooks (and data) where every other block has several levels in
+    one quarter of a binade (two or more interval thresholds sharing the
+    high byte of the binary16 key), the others ordinary levels."""
+    x = rng.standard_normal((nb, 32, G)).astype(np.float16)
+    cb = np.zeros((nb, 16), dtype=np.float32)
+    k = np.zeros(nb, dtype=np.uint8)
+    for b in range(nb):
+        v = np.sort(x[b].astype(np.float32).ravel())
+        if b % 2 == 0:
+            # levels: min, four values in [1, 1.25), max
+            lv = [v[0], 1.0, 1.0625, 1.125, 1.1875, v[-1]]
+            x[b, 0, :6] = np.array(lv, dtype=np.float16)
+            v = np.sort(x[b].astype(np.float32).ravel())
+            lv = [v[0], 1.0, 1.0625, 1.125, 1.1875, v[-1]]
+        else:
+            lv = list(np.unique(v[np.linspace(0, len(v) - 1, 9).round().astype(int)]))
+        lv = np.array(sorted(set(np.float16(lv).astype(np.float32))), dtype=np.float32)
+        k[b] = len(lv)
+        cb[b, :len(lv)] = lv
+        cb[b, len(lv):] = lv[-1]
+    return x.view(np.uint16), cb, k
+
+
+@pytest.mark.parametrize("G", [128, 32])
+def test_quantize_blocks_with_crowded_levels(G):
+    """Blocks whose thresholds share a bin of the interval table take the
+    binary-search path inside the same launch; codes bit-exact."""
+    _need_gpu()
+    rng = np.random.default_rng(17)
+    D = 128
+    nb_s = 64 if G == 128 else 16                  # 32-token slabs
+    xb, cb, k = _crowded_codebooks(nb_s * (D // G), G, rng)
+    # blocks [nb, 32, G] -> [S=1, T=32*nb_s, D]
+    x = xb.view(np.float16).reshape(nb_s, D // G, 32, G).transpose(0, 2, 1, 3).reshape(1, 32 * nb_s, D)
+    x = np.ascontiguousarray(x).view(np.uint16)
+    L = kvq.Layout(1, 32 * nb_s, D, G)
+    xd = gc.to_dev(x)
+    codes = torch.empty((L.nblocks, 16 * G), dtype=torch.uint8, device="cuda")
+    cbd, kd = torch.from_numpy(cb).cuda(), torch.from_numpy(k).cuda()
+    for seed in (1, 2):
+        kvq.kvq_quantize(xd, L, cbd, kd, seed, 8, codes)
+        want = oracle.quantize(x, G, cb, k, seed, 8)
+        assert np.array_equal(codes.cpu().numpy(), want)
+
+
+def test_quantize_edge_blocks_with_oracle_codebooks():
+    _need_gpu()
+    x = _edge_tensor()                       # [8 blocks, 32, 128], one block per stream
+    at = oracle.allocate_at(x, 128, 16, 0.05)
+    L = kvq.Layout(x.shape[0], 32, 128, 128)
+    xd = gc.to_dev(x)
+    codes = torch.empty((L.nblocks, 16 * 128), dtype=torch.uint8, device="cuda")
+    kvq.kvq_quantize(xd, L, torch.from_numpy(at["codebook"]).cuda(),
+                     torch.from_numpy(at["k"]).cuda(), 5, 0, codes)
+    assert np.array_equal(codes.cpu().numpy(), oracle.quantize(x, 128, at["codebook"], at["k"], 5, 0))
 
 
 # ------------------------------------------------------------ allocation
@@ -286,8 +344,8 @@ def test_fused_allocate_quantize_equals_separate_calls(name, T, S, s, bi, mode):
     for b in (ref, got):
         b.lam.fill_(lam0)
         b.codes.fill_(0xAB)
-    kvq.quantize(xd, L, B, s, seed=9, index_base=2 * 77, mode=mode, eta=eta, buf=ref)
-    kvq.quantize(xd, L, B, s, seed=9, index_base=2 * 77, mode=mode, eta=eta, buf=got, fused=True)
+    kvq.quantize(xd, L, B, s, seed=9, index_base=4 * 77, mode=mode, eta=eta, buf=ref)
+    kvq.quantize(xd, L, B, s, seed=9, index_base=4 * 77, mode=mode, eta=eta, buf=got, fused=True)
     torch.cuda.synchronize()
     assert int(got.status.item()) == 0
     for key in ("codebook", "k", "D_r", "H_r", "totals", "lam", "status", "codes"):
