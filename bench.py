@@ -567,6 +567,7 @@ def main():
     t_flush = device_ms(g_flush, nrep)
     t_scold = device_ms(g_stats, nrep) - t_flush
     t_acold = device_ms(g_alloc, nrep) - t_flush
+    rep_cold = kvq.kvq_allocate_report(buf.workspace)     # the last replay: cold L2
     t_qcold = device_ms(g_quant, nrep) - t_flush
     t_fcold = device_ms(g_fused, nrep) - t_flush
 
@@ -679,6 +680,12 @@ def main():
     rep = kvq.kvq_allocate_report(buf.workspace)
     kern["search_rounds"] = rep["rounds"]
     kern["search_active_blocks"] = rep["active"]
+    kern["search_timeline_us"] = {"what": "device clock from the search kernel's start, after "
+                                          "a cold-L2 replay: each round's evaluations all in, "
+                                          "its control published; end = emit and totals done",
+                                  "dp_done": rep_cold["dp_done_us"],
+                                  "control_done": rep_cold["control_done_us"],
+                                  "end": rep_cold["end_us"]}
     # exact DP of one block at one lambda: 680 (i < j < l) level triples, one
     # fp32 multiply-add and one min each
     dp_ops = sum(rep["active"]) * 32 * 680 * 2

@@ -373,12 +373,18 @@ int kvq_decode_attention(const float *q, int n_rep, kvq_layout L, const uint8_t 
  *   lambda, xa, xb  the answer, and the largest infeasible / smallest
  *              feasible lambda evaluated (the codebooks are the choice at xb)
  *   steps      bisection steps taken (40 unless lambda = 0 or infeasible)
+ *   t_start, t_end  device clock (%globaltimer, ns) at the search kernel's
+ *              start and at the end of its emit
+ *   t_dp[i], t_ctl[i]  device clock when round i's evaluations were all in,
+ *              and when its control had published the next round
  */
 typedef struct kvq_report {
     int32_t rounds;
     int32_t steps;
     uint32_t active[16];
     double lambda, xa, xb;
+    uint64_t t_start, t_end;
+    uint64_t t_dp[16], t_ctl[16];
 } kvq_report;
 int kvq_allocate_report(const void *workspace, kvq_report *report);
 

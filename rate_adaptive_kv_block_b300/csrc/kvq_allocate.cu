@@ -150,6 +150,8 @@ __global__ void ctrl_init_kernel(Ctrl *c, const StatsHeader *hdr, double budget,
     for (int i = 0; i < 16; ++i) c->active[i] = 0u;
     c->Rxb_fx = 0;
     c->cnt[0] = c->cnt[1] = 0u;
+    c->t_start = c->t_end = 0ull;
+    for (int i = 0; i < 16; ++i) c->t_dp[i] = c->t_ctl[i] = 0ull;
 }
 
 // ---------------------------------------------------------------- DP path A
@@ -764,6 +766,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
             fflag[i] = 0;
     }
 
+    if (blockIdx.x == 0 && threadIdx.x == 0) ctrl->t_start = global_ns();
     for (int iter = 0; iter < kMaxRounds; ++iter) {
         stage_ctrl(sC, ctrl);
         if (threadIdx.x == 0) sAct = 0u;
@@ -958,6 +961,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
             // ---- last CTA: stage the control block again (the sums are
             // final now), advance the search in shared memory, write back
             // what changed, then release the other CTAs
+            if (threadIdx.x == 0) ctrl->t_dp[min(round, 15)] = global_ns();
             stage_ctrl(sC, ctrl);
             __syncthreads();
             if (threadIdx.x < 32) {
@@ -1067,17 +1071,20 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                 publish_search(ctrl, S, L);
                 __syncwarp();            // the warp's writes, then one release store
                 if (L == 0) st_release_u32(&ctrl->gen, 2u * (uint32_t)iter + 1u);
+                
                 // second publication: the walk and the next round's probes
                 if (walk_on) {
                     const SearchWindow win = search_window_of(st);   // the walk keeps it
                     const int go = search_walk_w(st, win);
                     __syncwarp();
+                    
                     if (go) {
                         __shared__ double sProbe[kSearchProbes];
                         sProbe[L] = search_first_unknown(st);
                         __syncwarp();
                         search_path_w(st, win, L, sProbe);
                         __syncwarp();
+                        
                         S.probe[L] = sProbe[L];
                     }
                     __syncwarp();
@@ -1086,7 +1093,10 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                     publish_search(ctrl, S, L);
                 }
                 __syncwarp();
-                if (L == 0) st_release_u32(&ctrl->gen, 2u * (uint32_t)iter + 2u);
+                if (L == 0) {
+                    ctrl->t_ctl[min(round, 15)] = global_ns();
+                    st_release_u32(&ctrl->gen, 2u * (uint32_t)iter + 2u);
+                }
             }
             __syncthreads();
             ready = true;
@@ -1271,6 +1281,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
     *status = st;
     ctrl->ticket_emit = 0u;
     ctrl->ticket_f = 0u;
+    ctrl->t_end = global_ns();
 }
 
 __global__ void empty_alloc_kernel(double *totals, double *lambda_out, int32_t *status, int mode,
@@ -1359,6 +1370,12 @@ int allocate_report(const void *workspace, kvq_report *r) {
     r->xa = c.s.xa;
     r->xb = c.s.xb;
     r->steps = c.s.step;
+    r->t_start = c.t_start;
+    r->t_end = c.t_end;
+    for (int i = 0; i < 16; ++i) {
+        r->t_dp[i] = c.t_dp[i];
+        r->t_ctl[i] = c.t_ctl[i];
+    }
     return KVQ_OK;
 }
 

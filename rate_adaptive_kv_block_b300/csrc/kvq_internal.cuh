@@ -161,6 +161,10 @@ struct alignas(16) Ctrl {
     // per-probe sum of d_r H_r over blocks, fixed point (2^-20 bit units):
     // integer adds are exact, so the sum does not depend on arrival order
     unsigned long long acc[32];
+    // %globaltimer stamps (ns; diagnostics): kernel start, the end of each
+    // round's DP (the last CTA's ticket), its control's second publication,
+    // and the end of the emit
+    unsigned long long t_start, t_end, t_dp[16], t_ctl[16];
 };
 static_assert(sizeof(Ctrl) % 16 == 0, "control block in 16-byte pieces");
 constexpr double kRateScale = 1048576.0;   // 2^20

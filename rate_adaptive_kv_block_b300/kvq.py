@@ -61,7 +61,9 @@ class Layout:
 
 class _Report(C.Structure):
     _fields_ = [("rounds", C.c_int32), ("steps", C.c_int32), ("active", C.c_uint32 * 16),
-                ("lambda_", C.c_double), ("xa", C.c_double), ("xb", C.c_double)]
+                ("lambda_", C.c_double), ("xa", C.c_double), ("xb", C.c_double),
+                ("t_start", C.c_uint64), ("t_end", C.c_uint64), ("t_dp", C.c_uint64 * 16),
+                ("t_ctl", C.c_uint64 * 16)]
 
 
 class KvqError(RuntimeError):
@@ -272,8 +274,14 @@ def stats_rows(stats):
 def kvq_allocate_report(workspace) -> dict:
     r = _Report()
     _check(lib().kvq_allocate_report(_ptr(workspace), C.byref(r)), "kvq_allocate_report")
-    return {"rounds": r.rounds, "steps": r.steps, "active": list(r.active)[:max(r.rounds, 0)],
-            "lambda": r.lambda_, "xa": r.xa, "xb": r.xb}
+    n = max(r.rounds, 0)
+    t0 = r.t_start
+    us = lambda t: (t - t0) / 1e3 if t and t0 else None
+    return {"rounds": r.rounds, "steps": r.steps, "active": list(r.active)[:n],
+            "lambda": r.lambda_, "xa": r.xa, "xb": r.xb,
+            "dp_done_us": [us(t) for t in list(r.t_dp)[:n]],
+            "control_done_us": [us(t) for t in list(r.t_ctl)[:n]],
+            "end_us": us(r.t_end)}
 
 
 class Buffers:
