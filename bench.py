@@ -234,6 +234,24 @@ def comparator_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep,
     kvq.quantize(x, L, h_near * x.numel(), w.s, buf=b2)
     torch.cuda.synchronize()
     mse_eq = mse(b2.codes, b2.codebook)
+    # fixed-rate: every block at the same bits per entry (its own lambda_r),
+    # the same total budget; its kernel time (L2 flushed)
+    bpe = w.budgets[0]
+    bf_ = kvq.Buffers(L, w.s, dev)
+    lam_r = torch.empty(nb, dtype=torch.float64, device=dev)
+    bf_.stats.copy_(buf.stats)
+
+    def fixed():
+        kvq.kvq_allocate_fixed_rate(bf_.stats, L, w.s, bpe, bf_.codebook, bf_.k, bf_.D_r, bf_.H_r,
+                                    lam_r, bf_.totals, bf_.status)
+    fixed()
+    kvq.kvq_quantize(x, L, bf_.codebook, bf_.k, 0, 0, bf_.codes)
+    torch.cuda.synchronize()
+    g_f = graph_of(lambda: (flush_l2(1), fixed()))
+    device_ms(g_f, 2)
+    t_f = device_ms(g_f, max(3, nrep // 4)) - t_flush
+    mse_fixed = mse(bf_.codes, bf_.codebook)
+    n = x.numel()
     return {"what": "mean squared error of the binary16 decode and rate in bits/entry on this "
                     "layer; uniform = 16 equally spaced levels per block from its minimum to its "
                     "maximum; uniform rates are the per-block entropies of the codes",
@@ -243,6 +261,16 @@ def comparator_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep,
             "rate_adaptive_at_int4_rate": {"mse": mse_eq,
                                            "rate_bits": float(b2.totals[0].item()) / x.numel(),
                                            "stored_bits": 4.0},
+            "fixed_rate_at_budget": {"what": "every block at <= %.2f bits/entry on its own lambda "
+                                             "(kvq_allocate_fixed_rate): the same total budget as "
+                                             "the rate-adaptive allocation" % bpe,
+                                     "mse": mse_fixed,
+                                     "rate_bits": float(bf_.totals[0].item()) / n,
+                                     "expected_distortion_per_entry": float(bf_.totals[1].item()) / n,
+                                     "rate_adaptive_expected_distortion_per_entry":
+                                         float(buf.totals[1].item()) / n,
+                                     "status": int(bf_.status.item()),
+                                     "allocate_ms": t_f},
             "uniform_int4_ms": t_u,
             "uniform_int4_GBps": (x.numel() * 2 + x.numel() // 2 + nb * 65) / (t_u * 1e-3) / 1e9}
 
@@ -410,6 +438,164 @@ def attention_bench(w, L, buf, flush_l2, graph_of, device_ms, t_flush, nrep, hbm
     return res
 
 
+def other_configs_bench(dev, hbm, src):
+    """The other synthetic workloads, each resident in HBM and larger than
+    L2 (no flush needed between steps), timed with CUDA events:
+      * full_model_cache: 32 layers x {K, V} x 8 heads x 32768 tokens x 128
+        (4.3 GB), one global lambda at B = 2.0: the whole path
+        (stats + allocate + quantize) per step;
+      * decode_admission: per step 64 sequences x 32 layers x {K, V} x 8
+        heads append one 32-token block (268 MB); lambda from the bisection
+        at step 0, then one subgradient step per call (eta = 1e-6, B = 2.5);
+        64 timed steps cycling 8 pre-drawn step tensors: per-step latency
+        (median, p99) and the lambda trace;
+      * hadamard_groups: 8 heads x 131072 tokens x 128 after the 128-point
+        Hadamard rotation, 32-feature groups: stats once, then allocate +
+        quantize for each budget 1.5 / 2 / 3 / 4 bits per entry."""
+    import torch
+    from rate_adaptive_kv_block_b300 import kvq, synth
+    stream = torch.cuda.current_stream()
+    out = {}
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    # ---- full model cache
+    w = synth.workload("full_model_cache")
+    x = synth.make_torch(w, seed=0, device=dev)
+    L = kvq.Layout(w.S, w.T, w.D, w.G)
+    B = w.budgets[0] * w.entries
+    buf = kvq.Buffers(L, w.s, dev)
+
+    def step3():
+        kvq.kvq_stats(x, L, buf.stats, buf.status_stats)
+        kvq.kvq_allocate(buf.stats, L, w.s, B, kvq.KVQ_BISECT40, 0.0, buf.lam, buf.workspace,
+                         buf.codebook, buf.k, buf.D_r, buf.H_r, buf.totals, buf.status)
+        kvq.kvq_quantize(x, L, buf.codebook, buf.k, 0, 0, buf.codes, buf.status_quant)
+    for _ in range(2):
+        step3()
+    torch.cuda.synchronize()
+    assert int(buf.status.item()) == 0
+    ts = []
+    for _ in range(5):
+        a, b = ev(), ev()
+        a.record(stream)
+        step3()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = statistics.median(ts)
+    rep = kvq.kvq_allocate_report(buf.workspace)
+    out["full_model_cache"] = {
+        "workload": "32 layers x {K,V} x 8 heads x 32768 tokens x 128 fp16 (4.3 GB), 524288 "
+                    "blocks of 4096, s=16, B=2.0 bits/entry",
+        "ms_per_step_median": ms, "GBps": x.numel() * 2 / (ms * 1e-3) / 1e9,
+        "tokens_per_s": w.T / (ms * 1e-3), "lambda": float(buf.lam.item()),
+        "rate_bits_per_entry": float(buf.totals[0].item()) / w.entries,
+        "search_rounds": rep["rounds"], "search_active_blocks": rep["active"],
+        "l2": "input 34x larger than L2: no flush"}
+    del x, buf
+    torch.cuda.empty_cache()
+
+    # ---- decode admission: subgradient steps
+    w = synth.workload("decode_admission")
+    L = kvq.Layout(w.S, w.T, w.D, w.G)
+    B = w.budgets[0] * w.entries
+    xs = [synth.make_torch(w, seed=1000 + i, device=dev) for i in range(8)]
+    buf = kvq.Buffers(L, w.s, dev)
+
+    def step4(xt, t, mode):
+        kvq.kvq_stats(xt, L, buf.stats, buf.status_stats)
+        kvq.kvq_allocate(buf.stats, L, w.s, B, mode, w.eta if mode == kvq.KVQ_SUBGRADIENT else 0.0,
+                         buf.lam, buf.workspace, buf.codebook, buf.k, buf.D_r, buf.H_r, buf.totals,
+                         buf.status)
+        kvq.kvq_quantize(xt, L, buf.codebook, buf.k, t, 0, buf.codes, buf.status_quant)
+    step4(xs[0], 0, kvq.KVQ_BISECT40)                  # step 0: the bisection warm start
+    torch.cuda.synchronize()
+    lam0 = float(buf.lam.item())
+    for t in range(1, 4):                               # warm-up subgradient steps
+        step4(xs[t % 8], t, kvq.KVQ_SUBGRADIENT)
+    torch.cuda.synchronize()
+    n = 64
+    evs = [(ev(), ev()) for _ in range(n)]
+    trace = []
+    lam_dev = torch.empty(n, dtype=torch.float64, device=dev)
+    for i in range(n):
+        evs[i][0].record(stream)
+        step4(xs[(4 + i) % 8], 4 + i, kvq.KVQ_SUBGRADIENT)
+        evs[i][1].record(stream)
+        lam_dev[i:i + 1].copy_(buf.lam)
+    torch.cuda.synchronize()
+    lat = sorted(a.elapsed_time(b) for a, b in evs)
+    trace = [lam0] + lam_dev.cpu().tolist()
+    med = statistics.median(lat)
+    out["decode_admission"] = {
+        "workload": "per step 64 sequences x 32 layers x {K,V} x 8 heads x 32 tokens x 128 fp16 "
+                    "(268 MB, 32768 blocks of 4096), s=16, B=2.5 bits/entry, subgradient eta=1e-6 "
+                    "after a bisection warm start; 8 pre-drawn step tensors cycled",
+        "steps": n, "ms_per_step_median": med, "ms_per_step_p99": lat[min(n - 1, int(0.99 * n))],
+        "ms_per_step_min": lat[0], "GBps_median": xs[0].numel() * 2 / (med * 1e-3) / 1e9,
+        "tokens_per_s_median": 64 / (med * 1e-3),
+        "lambda_trace": trace[:17], "lambda_trace_every": "step 0 (bisection), then steps 4..",
+        "l2": "each step's input (268 MB) is larger than L2: no flush"}
+    del xs, buf
+    torch.cuda.empty_cache()
+
+    # ---- Hadamard-rotated groups: budget sweep on one stats result
+    w = synth.workload("hadamard_groups")
+    L = kvq.Layout(w.S, w.T, w.D, w.G)
+    x = synth.make_torch(w, seed=0, device=dev)
+    buf = kvq.Buffers(L, w.s, dev)
+    a, b = ev(), ev()
+    kvq.kvq_stats(x, L, buf.stats, buf.status_stats)   # warm
+    torch.cuda.synchronize()
+    a.record(stream)
+    kvq.kvq_stats(x, L, buf.stats, buf.status_stats)
+    b.record(stream)
+    torch.cuda.synchronize()
+    t_stats = a.elapsed_time(b)
+    sweep = []
+    for bpe in w.budgets:
+        Bb = bpe * w.entries
+
+        def aq():
+            kvq.kvq_allocate(buf.stats, L, w.s, Bb, kvq.KVQ_BISECT40, 0.0, buf.lam, buf.workspace,
+                             buf.codebook, buf.k, buf.D_r, buf.H_r, buf.totals, buf.status)
+            kvq.kvq_quantize(x, L, buf.codebook, buf.k, 0, 0, buf.codes, buf.status_quant)
+        aq()
+        torch.cuda.synchronize()
+        ta, tq = [], []
+        for _ in range(5):
+            e0, e1, e2 = ev(), ev(), ev()
+            e0.record(stream)
+            kvq.kvq_allocate(buf.stats, L, w.s, Bb, kvq.KVQ_BISECT40, 0.0, buf.lam, buf.workspace,
+                             buf.codebook, buf.k, buf.D_r, buf.H_r, buf.totals, buf.status)
+            e1.record(stream)
+            kvq.kvq_quantize(x, L, buf.codebook, buf.k, 0, 0, buf.codes, buf.status_quant)
+            e2.record(stream)
+            torch.cuda.synchronize()
+            ta.append(e0.elapsed_time(e1))
+            tq.append(e1.elapsed_time(e2))
+        assert int(buf.status.item()) == 0
+        rep = kvq.kvq_allocate_report(buf.workspace)
+        ma, mq = statistics.median(ta), statistics.median(tq)
+        qb = x.numel() * 2.5 + L.nblocks * 65
+        sweep.append({"bits_per_entry": bpe, "allocate_ms": ma, "quantize_ms": mq,
+                      "quantize_frac_hbm": qb / (mq * 1e-3) / 1e9 / hbm,
+                      "GBps_allocate_quantize": x.numel() * 2 / ((ma + mq) * 1e-3) / 1e9,
+                      "lambda": float(buf.lam.item()),
+                      "rate_bits_per_entry": float(buf.totals[0].item()) / w.entries,
+                      "search_rounds": rep["rounds"]})
+    out["hadamard_groups"] = {
+        "workload": "8 heads x 131072 tokens x 128 fp16 after a 128-point Hadamard rotation "
+                    "(268 MB), 32-feature groups: 131072 blocks of 1024, s=16",
+        "stats_ms": t_stats, "stats_GBps": x.numel() * 2 / (t_stats * 1e-3) / 1e9,
+        "sweep": sweep, "peak_source": src, "l2": "input (268 MB) larger than L2: no flush"}
+    del x, buf
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -417,7 +603,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-blocks", type=int, default=1024)
+    ap.add_argument("--ref-blocks", type=int, default=CPU_SAMPLE_BLOCKS)
+    ap.add_argument("--no-other-configs", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -579,6 +766,7 @@ def main():
     comp = comparator_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev)
     ent = entropy_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev)
     wtd = weighted_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev)
+    others = None if args.no_other_configs else other_configs_bench(dev, *peaks())
 
     # End to end through the C ABI from pinned host memory, pipelined over
     # three streams the way a serving loop would run it: step i's input copy
@@ -662,6 +850,7 @@ def main():
         "comparators": comp,
         "entropy_coding": ent,
         "weighted_distortion": wtd,
+        "other_configs": others,
         "cold_method": "graph (L2 flush + kernel) minus graph (L2 flush), device-timed",
         "stats_cold_GBps": s_bytes / (t_scold * 1e-3) / 1e9,
         "quantize_cold_GBps": q_bytes / (t_qcold * 1e-3) / 1e9,

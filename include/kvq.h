@@ -227,6 +227,31 @@ int kvq_allocate_quantize(const void *stats, const uint16_t *x, kvq_layout L, in
                           void *stream);
 
 /*
+ * kvq_allocate_fixed_rate -- the fixed-rate comparator ("Implementation
+ * notes": compare against fixed-rate entropy coding at equal total cache
+ * bytes).  The same per-block quantizer as kvq_allocate, but every block r
+ * meets the rate on its own: lambda_r comes from the 40-step bisection of
+ * kvq_allocate applied to block r alone with the budget bits_per_entry * d_r
+ * (R_r(0) <= budget -> 0; bracket from (c_max - c_min)^2 doubled at most 30
+ * times; lambda_r = the bracket's feasible end), and the block gets its
+ * choice at the smallest feasible lambda evaluated.  The total rate is then
+ * at most bits_per_entry * S*T*D, the budget kvq_allocate spreads across
+ * blocks with one lambda.
+ *   stats        kvq_stats output (unweighted: weighted stats set status to
+ *                KVQ_ERR_INVALID_ARG).
+ *   codebook, k, D_r, H_r  as for kvq_allocate; lambda_r  device double
+ *                [nblocks], each block's lambda.
+ *   totals       device double[3]: sum d_r H_r, sum D_r, 0 (fixed order).
+ *   status       device int32: KVQ_OK, KVQ_ERR_INFEASIBLE (some block cannot
+ *                reach its budget; it keeps the choice at the largest bracket),
+ *                KVQ_ERR_NONFINITE, KVQ_ERR_INVALID_ARG (weighted stats).
+ */
+int kvq_allocate_fixed_rate(const void *stats, kvq_layout L, int s,
+                            double bits_per_entry, float *codebook, uint8_t *k,
+                            float *D_r, float *H_r, double *lambda_r,
+                            double *totals, int32_t *status, void *stream);
+
+/*
  * kvq_quantize -- unbiased stochastic interpolation and 4-bit packing ("Key
  * formulas": P(q_{i+1} | x) = (x - q_i)/(q_{i+1} - q_i)).  For entry x of
  * block r with levels q_0 < ... < q_{k-1}: i = the largest index with

@@ -52,6 +52,9 @@ def lib():
         L.kvqo_allocate_at.argtypes = [vp, vp, i64, i64, C.c_int, C.c_int, vp, i64,
                                        C.c_int, dbl, dbl, dbl, vp, vp, vp, vp,
                                        vp, vp, vp, vp]
+        L.kvqo_allocate_fixed_rate.restype = C.c_int
+        L.kvqo_allocate_fixed_rate.argtypes = [vp, vp, i64, i64, C.c_int, C.c_int, vp, i64,
+                                               C.c_int, dbl, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kvqo_rate_at.restype = dbl
         L.kvqo_rate_at.argtypes = [vp, vp, i64, i64, C.c_int, C.c_int, vp, i64,
                                    C.c_int, dbl]
@@ -206,6 +209,26 @@ def allocate_at(x, G, s, lam, eta=0.0, budget_bits=0.0, ids=None, w=None):
         _p(out["D_r"]), _p(out["H_r"]), _p(out["gap"]), _p(out["mask"]),
         _p(out["totals"]))
     out.update(status=st, lambda_next=float(nxt[0]), **{"lambda": float(lam)})
+    return out
+
+
+def allocate_fixed_rate(x, G, s, bits_per_entry, ids=None, w=None):
+    """The fixed-rate comparator: every block gets its own lambda_r from the
+    40-step bisection applied to that block alone with budget
+    bits_per_entry * d_r, so each block (not only the total) meets the rate.
+    Returns the per-block arrays (ids order), "lambdas" and the status."""
+    x = _x(x)
+    w = _w(w, x)
+    S, T, D = x.shape
+    ids = _ids(ids)
+    nb = num_blocks(S, T, D, G) if ids is None else len(ids)
+    out = _alloc_out(nb)
+    lams = np.zeros(nb)
+    st = lib().kvqo_allocate_fixed_rate(
+        _p(x), _p(w), S, T, D, G, _p(ids), nb, s, float(bits_per_entry), _p(lams),
+        _p(out["codebook"]), _p(out["k"]), _p(out["D_r"]), _p(out["H_r"]), _p(out["gap"]),
+        _p(out["mask"]), _p(out["totals"]))
+    out.update(status=st, lambdas=lams)
     return out
 
 

@@ -584,6 +584,104 @@ int kvqo_allocate_bisect(const uint16_t *x, const float *wt, int64_t S,
     return status;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Fixed-rate comparator ("Implementation notes": compare against fixed-rate  */
+/* entropy coding at equal total cache bytes).                               */
+/* Reading: the same per-block quantizer, but every block r holds the same   */
+/* rate, d_r H_r <= b d_r with b = the budget per entry, through its own      */
+/* lambda_r found by the bisection above applied to that block alone (R_r(0) */
+/* <= b d_r -> lambda_r = 0; hi = (c_max - c_min)^2 (times the block's       */
+/* largest weight) doubled at most 30 times; 40 steps; lambda_r = hi).  The  */
+/* total rate then meets the same total budget b * entries, so the stored    */
+/* bytes are equal and only the allocation across blocks differs.  A block   */
+/* still infeasible at hi * 2^30 keeps its choice there (status 4).          */
+/* ------------------------------------------------------------------------ */
+
+static int block_bisect(const kvqo_block_t *B, int s, double budget,
+                        double *lambda_out)
+{
+    kvqo_choice_t ch;
+    block_choose(B, s, 0.0, 0, &ch);
+    if (ch.Rr <= budget) { *lambda_out = 0.0; return KVQO_OK; }
+    double w = B->c[B->mp - 1] - B->c[0];
+    double lo = 0.0, hi = (w * w) * B->wmax;
+    int n = 0;
+    block_choose(B, s, hi, 0, &ch);
+    int feas = ch.Rr <= budget;
+    while (!feas && n < 30) {
+        hi *= 2.0;
+        n++;
+        block_choose(B, s, hi, 0, &ch);
+        feas = ch.Rr <= budget;
+    }
+    if (!feas) { *lambda_out = hi; return KVQO_INFEASIBLE; }
+    for (int step = 0; step < 40; step++) {
+        double mid = 0.5 * (lo + hi);
+        block_choose(B, s, mid, 0, &ch);
+        if (ch.Rr <= budget) hi = mid;
+        else lo = mid;
+    }
+    *lambda_out = hi;
+    return KVQO_OK;
+}
+
+int kvqo_allocate_fixed_rate(const uint16_t *x, const float *wt, int64_t S,
+                             int64_t T, int D, int G, const int64_t *ids, int64_t nb,
+                             int s, double bits_per_entry, double *lambdas,
+                             float *codebook, uint8_t *kout, double *Dr,
+                             double *Hr, double *gap, uint32_t *masks,
+                             double *totals)
+{
+    (void)S;
+    kvqo_set_t st;
+    set_build(x, wt, T, D, G, ids, nb, &st);
+    int status = set_status(&st);
+    int infeasible = 0;
+    double *rr = (double *)malloc(sizeof(double) * (size_t)(nb ? nb : 1));
+    double *dd = (double *)malloc(sizeof(double) * (size_t)(nb ? nb : 1));
+#pragma omp parallel for schedule(dynamic, 4) reduction(|:infeasible)
+    for (int64_t i = 0; i < nb; i++) {
+        const kvqo_block_t *B = &st.blk[i];
+        double lam = 0.0;
+        if (block_bisect(B, s, bits_per_entry * (double)B->d, &lam) != KVQO_OK) infeasible = 1;
+        lambdas[i] = lam;
+        kvqo_choice_t ch;
+        block_choose(B, s, lam, 1, &ch);
+        int k = 0;
+        float q[KVQO_SMAX];
+        for (int j = 0; j < B->mp; j++)
+            if (ch.mask >> j & 1u) q[k++] = (float)B->c[j];
+        for (int j = k; j < KVQO_SMAX; j++) q[j] = q[k - 1];
+        if (codebook) memcpy(codebook + i * KVQO_SMAX, q, sizeof q);
+        if (kout) kout[i] = (uint8_t)k;
+        if (Dr) Dr[i] = ch.Dr;
+        if (Hr) Hr[i] = ch.Rr / (double)B->d;
+        if (masks) masks[i] = ch.mask;
+        if (gap) {
+            if (!(ch.obj2 < INFINITY)) gap[i] = INFINITY;
+            else if (ch.obj == 0.0) gap[i] = ch.obj2 > 0.0 ? INFINITY : 0.0;
+            else gap[i] = (ch.obj2 - ch.obj) / fabs(ch.obj);
+        }
+        rr[i] = ch.Rr;
+        dd[i] = ch.Dr;
+    }
+    if (totals) {
+        double R = 0, Dsum = 0;
+        for (int64_t i = 0; i < nb; i++) {   /* block order */
+            R += rr[i];
+            Dsum += dd[i];
+        }
+        totals[0] = R;
+        totals[1] = Dsum;
+        totals[2] = 0.0;
+    }
+    free(rr);
+    free(dd);
+    set_free(&st);
+    if (status == KVQO_OK && infeasible) status = KVQO_INFEASIBLE;
+    return status;
+}
+
 /* Choice at a fixed lambda (used for the one-step subgradient map, and to
  * check the codebooks at a given lambda).  *lambda_next receives
  * max(0, lambda + eta (R - budget_bits)). */

@@ -123,7 +123,8 @@ constexpr int64_t kPilotMinBlocks = 1024;
 constexpr int kPilotStride = 16;
 
 __global__ void ctrl_init_kernel(Ctrl *c, const StatsHeader *hdr, double budget, double eta,
-                                 int mode, const double *lambda_in, int64_t nb) {
+                                 int mode, const double *lambda_in, int64_t nb,
+                                 unsigned long long wait_ns, uint32_t spin_limit) {
     if (threadIdx.x != 0) return;
     search_init(c->s);
     c->s.hi0 = __longlong_as_double((long long)hdr->hi0_bits);
@@ -151,6 +152,8 @@ __global__ void ctrl_init_kernel(Ctrl *c, const StatsHeader *hdr, double budget,
     c->Rxb_fx = 0;
     c->cnt[0] = c->cnt[1] = 0u;
     c->t_start = c->t_end = 0ull;
+    c->wait_ns = wait_ns;
+    c->spin_limit = spin_limit;
     for (int i = 0; i < 16; ++i) c->t_dp[i] = c->t_ctl[i] = 0ull;
 }
 
@@ -592,8 +595,10 @@ __device__ __forceinline__ void publish_search(Ctrl *ctrl, const SearchState &S,
 __device__ __forceinline__ bool wait_gen(const Ctrl *ctrl, uint32_t target) {
     uint32_t spins = 0;
     const unsigned long long t0 = global_ns();
+    const unsigned long long lim = ctrl->wait_ns;
+    const uint32_t slim = ctrl->spin_limit;
     while (ld_acquire_u32(&ctrl->gen) < target) {
-        if (++spins > kSpinLimit || global_ns() - t0 > kWaitLimitNs) return false;
+        if (++spins > slim || global_ns() - t0 > lim) return false;
         __nanosleep(64);
     }
     return true;
@@ -623,6 +628,7 @@ __device__ __noinline__ void run_queue(const Ctrl *ctrl, uint32_t target, uint64
                                        float *scratch, int lane, uint64_t total_warps,
                                        uint64_t &qj, int &qpart) {
     const unsigned long long t0 = global_ns();
+    const unsigned long long lim = ctrl->wait_ns;
     bool prepared = false;
     int64_t b = 0;
     uint32_t T[16];
@@ -636,7 +642,7 @@ __device__ __noinline__ void run_queue(const Ctrl *ctrl, uint32_t target, uint64
         if (gcur >= target) break;
         if (lane == 0) gpoll = ld_relaxed_u32(&ctrl->gen);
         if (qj >= avail) {
-            if (global_ns() - t0 > kWaitLimitNs) break;
+            if (global_ns() - t0 > lim) break;
             __nanosleep(100);
             continue;
         }
@@ -1284,6 +1290,182 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
     ctrl->t_end = global_ns();
 }
 
+// ------------------------------------------------ fixed-rate comparator
+// Every block on its own lambda_r ("Implementation notes": the comparison
+// against fixed-rate entropy coding at equal total cache bytes): one warp per
+// block runs the 40-step bisection above on that block alone, budget
+// bits_per_entry * d_r, with the same exact DP (one lane per probe lambda)
+// and the same search control (kvq_search.h) walking 5 levels per round;
+// then the chain at the smallest feasible lambda evaluated is emitted.
+template <bool GENERAL>
+__global__ void __launch_bounds__(RoundCfg<GENERAL>::kWarps * 32)
+fixed_rate_kernel(const float *__restrict__ tables, int64_t nb, int s, double bits_per_entry,
+                  float *__restrict__ codebook, uint8_t *__restrict__ kout, float *__restrict__ Dr,
+                  float *__restrict__ Hr, double *__restrict__ lambdas,
+                  int32_t *__restrict__ status) {
+    using Cfg = RoundCfg<GENERAL>;
+    constexpr int W = Cfg::kWarps;
+    extern __shared__ __align__(16) float smem[];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    float *sTbl = smem + w * kTblStride;
+    float *sState = smem + W * kTblStride + w * Cfg::kStateFloats;
+    float *sDiag = smem + W * (kTblStride + Cfg::kStateFloats) + w * 32;
+    __shared__ __align__(16) SearchState sS[W];
+    __shared__ long long sR[W][32];
+    __shared__ double sProbe[W][32];
+    const int64_t b = (int64_t)blockIdx.x * W + w;
+    if (b >= nb) return;                      // warp-level work only below
+    {
+        const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
+        float4 *dst = reinterpret_cast<float4 *>(sTbl);
+        for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
+    }
+    __syncwarp();
+    const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
+    const int d = __float_as_int(sTbl[kTblHdr + 1]);
+    const int bflags = __float_as_int(sTbl[kTblHdr + 2]);
+    SearchState &S = sS[w];
+    if (lane == 0) {
+        search_init(S);
+        const double wd = (double)sTbl[kTblC + 16] - (double)sTbl[kTblC];
+        S.hi0 = wd * wd;
+        S.f32_lambda = 1;                     // the DP runs at float(lambda)
+    }
+    __syncwarp();
+    const long long Bfx = budget_fx(bits_per_entry * (double)d);
+    uint32_t xb_mask = 1u;
+    float xb_rate = 0.f;
+    if (mp > 1) {
+        const int C = mp > s ? mp - s : 0;
+        for (int round = 0; round < kMaxRounds && S.phase != kSearchDone; ++round) {
+            const double v = search_probe(S, lane);
+            const float lam = (float)v;
+            float rate;
+            uint32_t mask;
+            if (!GENERAL || C == 0 || (C == 1 && mp == 17)) {
+                dp_a_diag(sTbl, sDiag, lane);
+                dp_path_a(sTbl, lam, C, sState, sState + kPairs * 32, sDiag, lane, rate, mask);
+            } else {
+                dp_path_b(sTbl, lam, s, sState, sState + kPairs * 32,
+                          reinterpret_cast<uint32_t *>(sState + 2 * kPairs * 32), lane, rate, mask);
+            }
+            const long long R = llrint((double)rate * kRateScale);
+            sR[w][lane] = R;
+            __syncwarp();
+            // the round's evaluations into the window: smallest feasible probe,
+            // largest infeasible one below it (order keys; first lane on ties)
+            const bool inr = lane < S.nprobe;
+            const uint64_t kv = okey(v);
+            const bool feas = inr && R <= Bfx;
+            uint64_t kb = feas ? kv : ~0ull;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const uint64_t y = __shfl_xor_sync(0xffffffffu, kb, o);
+                kb = y < kb ? y : kb;
+            }
+            const uint32_t mb = __ballot_sync(0xffffffffu, feas && kv == kb);
+            const int ib = mb ? __ffs(mb) - 1 : -1;
+            const double vb = __shfl_sync(0xffffffffu, v, ib >= 0 ? ib : 0);
+            const uint64_t kxb = okey(S.xb);
+            const uint64_t kxbn = (ib >= 0 && kb < kxb) ? kb : kxb;
+            const bool inf = inr && !feas && kv < kxbn;
+            uint64_t ka = inf ? kv : 0ull;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const uint64_t y = __shfl_xor_sync(0xffffffffu, ka, o);
+                ka = y > ka ? y : ka;
+            }
+            const uint32_t ma = __ballot_sync(0xffffffffu, inf && kv == ka);
+            const int ia = ma ? __ffs(ma) - 1 : -1;
+            const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
+            SearchState st;                    // every lane the same copy
+            search_copy_scalars(st, S);
+            search_window(st, ib >= 0 ? vb : INFINITY, ib, ib >= 0 ? sR[w][ib] : 0, va, ia);
+            const int walk_on = search_decide(st, sR[w], Bfx);
+            const int xp = st.xb_probe;        // lane-uniform
+            const uint32_t mk = __shfl_sync(0xffffffffu, mask, xp >= 0 ? xp : 0);
+            const float rk = __shfl_sync(0xffffffffu, rate, xp >= 0 ? xp : 0);
+            if (xp >= 0) {
+                xb_mask = mk;
+                xb_rate = rk;
+            }
+            if (walk_on) {
+                const SearchWindow win = search_window_of(st);
+                const int go = search_walk_w(st, win);
+                __syncwarp();
+                if (go) {
+                    sProbe[w][lane] = search_first_unknown(st);
+                    __syncwarp();
+                    search_path_w(st, win, lane, sProbe[w]);
+                    __syncwarp();
+                    S.probe[lane] = sProbe[w][lane];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) search_copy_scalars(S, st);
+            __syncwarp();
+        }
+    }
+    // emit (lane 0): levels in slot order, D_r along the chain, H_r
+    if (lane == 0) {
+        uint32_t mask = xb_mask & 0x1ffffu;
+        if (mp <= 1 || mask == 0u) mask = 1u;
+        const int k = min(__popc(mask), 16);
+        float dv = 0.f, top = sTbl[kTblC];
+        int prev = 0, pos = 0;
+        for (int t = 0; t < 17; ++t) {
+            if (!((mask >> t) & 1u)) continue;
+            if (t > 0) dv += sTbl[kTblD + dp_off(prev) + t - prev - 1];
+            top = sTbl[kTblC + t];
+            if (pos < 16) codebook[b * 16 + pos] = top;
+            ++pos;
+            prev = t;
+        }
+        for (int t = k; t < 16; ++t) codebook[b * 16 + t] = top;
+        kout[b] = (uint8_t)k;
+        Dr[b] = dv;
+        Hr[b] = mp > 1 ? xb_rate / (float)d : 0.f;
+        lambdas[b] = mp > 1 ? S.lambda : 0.0;
+        if (S.infeasible) atomicMax(status, (int32_t)KVQ_ERR_INFEASIBLE);
+        if (bflags & kFlagWeighted) atomicMax(status, (int32_t)KVQ_ERR_INVALID_ARG + 100);
+    }
+}
+
+// Totals of the fixed-rate comparator in a fixed order: each thread a
+// contiguous run of blocks, then a fixed tree; the status of the data.
+__global__ void fixed_rate_totals_kernel(const StatsHeader *__restrict__ hdr, int64_t nb, int d,
+                                         const float *__restrict__ Dr,
+                                         const float *__restrict__ Hr, double *__restrict__ totals,
+                                         int32_t *__restrict__ status) {
+    __shared__ double sR[256], sD[256];
+    const int t = threadIdx.x;
+    const int64_t chunk = (nb + 255) / 256;
+    double r = 0.0, dd = 0.0;
+    for (int64_t i = (int64_t)t * chunk; i < nb && i < (int64_t)(t + 1) * chunk; ++i) {
+        r += (double)Hr[i] * (double)d;
+        dd += (double)Dr[i];
+    }
+    sR[t] = r;
+    sD[t] = dd;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (t < o) {
+            sR[t] += sR[t + o];
+            sD[t] += sD[t + o];
+        }
+        __syncthreads();
+    }
+    if (t == 0) {
+        totals[0] = sR[0];
+        totals[1] = sD[0];
+        totals[2] = 0.0;
+        int st = *status;
+        if (st == KVQ_ERR_INVALID_ARG + 100) st = KVQ_ERR_INVALID_ARG;   // weighted stats
+        if (hdr->flags & kFlagNonfinite) st = KVQ_ERR_NONFINITE;
+        *status = st;
+    }
+}
+
 __global__ void empty_alloc_kernel(double *totals, double *lambda_out, int32_t *status, int mode,
                                    double eta, double budget) {
     if (threadIdx.x != 0) return;
@@ -1313,7 +1495,11 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
     const StatsHeader *hdr = static_cast<const StatsHeader *>(stats);
     const float *recs = reinterpret_cast<const float *>(static_cast<const char *>(stats) +
                                                         sizeof(StatsHeader));
-    ctrl_init_kernel<<<1, 32, 0, st>>>(ws.ctrl, hdr, budget, eta, mode, lambda, nb);
+    unsigned long long wait_ns = kWaitLimitNs;
+    uint32_t spin_limit = kSpinLimit;
+    if (test_wait_limit(&wait_ns)) spin_limit = 1u;
+    ctrl_init_kernel<<<1, 32, 0, st>>>(ws.ctrl, hdr, budget, eta, mode, lambda, nb, wait_ns,
+                                       spin_limit);
     if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
     const bool general = s < 16;
     const bool quant = codes != nullptr;
@@ -1357,6 +1543,33 @@ int launch_allocate(const void *stats, const kvq_layout &L, int s, double budget
                              : (quant ? (const void *)search_kernel<false, true>
                                       : (const void *)search_kernel<false, false>);
     if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return KVQ_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+int launch_fixed_rate(const void *stats, const kvq_layout &L, int s, double bits_per_entry,
+                      float *codebook, uint8_t *k, float *Dr, float *Hr, double *lambdas,
+                      double *totals, int32_t *status, cudaStream_t st) {
+    const int64_t nb = num_blocks(L);
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return KVQ_ERR_CUDA;
+    const StatsHeader *hdr = static_cast<const StatsHeader *>(stats);
+    if (nb > 0) {
+        const float *recs = reinterpret_cast<const float *>(static_cast<const char *>(stats) +
+                                                            sizeof(StatsHeader));
+        const bool general = s < 16;
+        const int W = general ? RoundCfg<true>::kWarps : RoundCfg<false>::kWarps;
+        const unsigned grid = (unsigned)((nb + W - 1) / W);
+        const size_t smem = general ? RoundCfg<true>::kSmem : RoundCfg<false>::kSmem;
+        if (general)
+            fixed_rate_kernel<true><<<grid, W * 32, smem, st>>>(recs, nb, s, bits_per_entry,
+                                                                 codebook, k, Dr, Hr, lambdas,
+                                                                 status);
+        else
+            fixed_rate_kernel<false><<<grid, W * 32, smem, st>>>(recs, nb, s, bits_per_entry,
+                                                                  codebook, k, Dr, Hr, lambdas,
+                                                                  status);
+        if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+    }
+    fixed_rate_totals_kernel<<<1, 256, 0, st>>>(hdr, nb, 32 * L.group, Dr, Hr, totals, status);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
@@ -1406,6 +1619,13 @@ int allocate_init() {
         setup_search_kernel<false, true>(sms, r[0][1]) != KVQ_OK ||
         setup_search_kernel<true, false>(sms, r[1][0]) != KVQ_OK ||
         setup_search_kernel<true, true>(sms, r[1][1]) != KVQ_OK)
+        return KVQ_ERR_CUDA;
+    if (cudaFuncSetAttribute((const void *)fixed_rate_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)RoundCfg<false>::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute((const void *)fixed_rate_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)RoundCfg<true>::kSmem) != cudaSuccess)
         return KVQ_ERR_CUDA;
     // the module is loaded on this device now (the attributes above needed
     // it), so the static scratch exists: take its device address

@@ -38,6 +38,9 @@ int allocate_init();
 int weights_init();
 int allocate_report(const void *workspace, kvq_report *r);
 void *static_workspace_address(int dev);
+int launch_fixed_rate(const void *stats, const kvq_layout &L, int s, double bits_per_entry,
+                      float *codebook, uint8_t *k, float *Dr, float *Hr, double *lambdas,
+                      double *totals, int32_t *status, cudaStream_t st);
 
 static bool layout_ok(const kvq_layout &L) {
     if (L.S < 0 || L.T < 0 || L.T % 32 != 0) return false;
@@ -181,6 +184,24 @@ int kvq_allocate_static(const void *stats, kvq_layout L, int s, double budget_bi
     // kernel of kvq_allocate; nothing else in it is read before it is written
     return kvq_allocate(stats, L, s, budget_bits, mode, eta, lambda, ws, codebook, k, D_r, H_r,
                         totals, status, stream);
+}
+
+int kvq_allocate_fixed_rate(const void *stats, kvq_layout L, int s, double bits_per_entry,
+                            float *codebook, uint8_t *k, float *D_r, float *H_r,
+                            double *lambda_r, double *totals, int32_t *status, void *stream) {
+    if (!layout_ok(L) || s < 2 || s > kMaxLev) return KVQ_ERR_INVALID_ARG;
+    if (!(bits_per_entry >= 0.0) || !isfinite(bits_per_entry)) return KVQ_ERR_INVALID_ARG;
+    if (!totals || !status) return KVQ_ERR_INVALID_ARG;
+    const int64_t nb = num_blocks(L);
+    if (nb > 0) {
+        if (!stats || !codebook || !k || !D_r || !H_r || !lambda_r) return KVQ_ERR_INVALID_ARG;
+        if (!aligned16(stats) || !aligned16(codebook)) return KVQ_ERR_INVALID_ARG;
+        if (nb > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
+    }
+    if (!stats) return KVQ_ERR_INVALID_ARG;
+    if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
+    return launch_fixed_rate(stats, L, s, bits_per_entry, codebook, k, D_r, H_r, lambda_r, totals,
+                             status, static_cast<cudaStream_t>(stream));
 }
 
 int kvq_quantize(const uint16_t *x, kvq_layout L, const float *codebook, const uint8_t *k,

@@ -71,7 +71,7 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
                     const float *__restrict__ kcb, const uint8_t *__restrict__ vc,
                     const float *__restrict__ vcb, int64_t ntb, int G, int64_t T_valid,
                     float scale2, int bps, int chunk, float *__restrict__ part,
-                    int32_t *__restrict__ status) {
+                    int32_t *__restrict__ status, uint32_t wait_polls) {
     constexpr int D = kAttnD;
     const float NEG = __int_as_float(0xff800000);   // -inf
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -144,7 +144,7 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
 
     int cfail = nchunks;
     for (int c = 0; c < nchunks; ++c) {
-        if (tid == 0 && !mbar_wait(&bars[c & 1], (uint32_t)(c >> 1) & 1u, kAttnWaitLimit))
+        if (tid == 0 && !mbar_wait(&bars[c & 1], (uint32_t)(c >> 1) & 1u, wait_polls))
             failed = true;
         __syncthreads();
         if (failed) {
@@ -387,18 +387,23 @@ int launch_decode_attention(const float *q, int n_rep, const kvq_layout &L, cons
         // ring of two stages of 8
         const int chunk = (int)(bps < kAttnChunkMax ? bps : kAttnChunkMax);
         const size_t smem = (bps > chunk ? 2 : 1) * (size_t)attn_stage_bytes(chunk, L.D / L.group);
+        unsigned long long tw = 0;
+        const uint32_t wait_polls = test_wait_limit(&tw) ? 0u : kAttnWaitLimit;
         switch (n_rep) {
         case 1:
             attn_partial_kernel<1><<<grid, kAttnThreads, smem, st>>>(
-                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, status);
+                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, status,
+                wait_polls);
             break;
         case 2:
             attn_partial_kernel<2><<<grid, kAttnThreads, smem, st>>>(
-                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, status);
+                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, status,
+                wait_polls);
             break;
         default:
             attn_partial_kernel<4><<<grid, kAttnThreads, smem, st>>>(
-                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, status);
+                q, kc, kcb, vc, vcb, ntb, L.group, T_valid, scale2, (int)bps, chunk, part, status,
+                wait_polls);
             break;
         }
         if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;

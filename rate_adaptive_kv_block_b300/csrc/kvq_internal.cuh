@@ -3,11 +3,26 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "kvq.h"
 #include "kvq_search.h"
 
 namespace kvq {
+
+// Test hook for the error paths of the kernels' bounded waits: with
+// KVQ_TEST_WAIT_LIMIT_NS set in the environment when a call is made, the
+// search kernel's hand-over waits give up after that many nanoseconds and
+// the quantize and attention kernels' waits for their bulk copies without
+// polling, so that those calls return KVQ_ERR_TIMEOUT in their status
+// instead of their results.  (The waits for copies still in flight when a
+// kernel leaves keep their normal limit.)  Unset: the normal limits.
+inline bool test_wait_limit(unsigned long long *ns) {
+    const char *e = getenv("KVQ_TEST_WAIT_LIMIT_NS");
+    if (!e || !*e) return false;
+    *ns = strtoull(e, nullptr, 10);
+    return true;
+}
 
 constexpr int kCand = 17;       // order-statistic candidates per block
 constexpr int kMaxLev = 16;     // levels per block (4-bit codes)
@@ -165,6 +180,9 @@ struct alignas(16) Ctrl {
     // round's DP (the last CTA's ticket), its control's second publication,
     // and the end of the emit
     unsigned long long t_start, t_end, t_dp[16], t_ctl[16];
+    unsigned long long wait_ns;    // limit of each grid hand-over wait
+    uint32_t spin_limit;           // and of its polls
+    uint32_t pad_w;
 };
 static_assert(sizeof(Ctrl) % 16 == 0, "control block in 16-byte pieces");
 constexpr double kRateScale = 1048576.0;   // 2^20

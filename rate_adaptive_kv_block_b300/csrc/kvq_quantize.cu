@@ -226,15 +226,19 @@ __device__ __forceinline__ uint32_t quant8_table(const uint4 raw, uint32_t binba
 __global__ void __launch_bounds__(kTThreads, KVQ_QT_MINB)
 quantize_table_kernel(const uint16_t *__restrict__ x, const float *__restrict__ codebook,
                       TGeom g, PhiloxKey K, uint64_t index_base, uint8_t *__restrict__ codes,
-                      int32_t *__restrict__ status) {
+                      int32_t *__restrict__ status, uint32_t wait_polls) {
     extern __shared__ __align__(128) char qsm[];
     __shared__ __align__(8) uint64_t bars[kTStages];
     __shared__ __align__(1024) TTables tb;
     __shared__ int failed;
+    __shared__ uint32_t issued[kTStages];      // copies issued into each stage buffer
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int kWarps = kTThreads / 32;
     if (tid == 0) {
-        for (int s = 0; s < kTStages; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < kTStages; ++s) {
+            mbar_init(&bars[s], 1);
+            issued[s] = 0u;
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         failed = 0;
     }
@@ -243,7 +247,10 @@ quantize_table_kernel(const uint16_t *__restrict__ x, const float *__restrict__ 
     if (tid == 0) {
         for (int i = 0; i < kTStages; ++i) {
             const int64_t s = s0 + (int64_t)i * sstep;
-            if (s < g.nstages) t_issue(g, s, x, codebook, qsm + i * g.stage_bytes, &bars[i]);
+            if (s < g.nstages) {
+                t_issue(g, s, x, codebook, qsm + i * g.stage_bytes, &bars[i]);
+                issued[i] = 1u;
+            }
         }
     }
     // this thread's units: column cu, rows rg * upt .. rg * upt + upt - 1 (one slab)
@@ -262,7 +269,7 @@ quantize_table_kernel(const uint16_t *__restrict__ x, const float *__restrict__ 
     const int cbstep = g.G / 2;
     // tables of the first stage
     if (s0 < g.nstages) {
-        if (!mbar_wait(&bars[0], 0u, kQWaitLimit)) atomicOr(&failed, 1);
+        if (!mbar_wait(&bars[0], 0u, wait_polls)) atomicOr(&failed, 1);
         const float *cb = reinterpret_cast<const float *>(qsm + g.x_bytes);
         const int ntask = 4 * t_blocks(g, s0);
         for (int q = warp; q < ntask; q += kWarps) t_build(tb, 0, q >> 2, q & 3, cb, lane);
@@ -273,7 +280,7 @@ quantize_table_kernel(const uint16_t *__restrict__ x, const float *__restrict__ 
         const uint32_t st = n % kTStages, par = n & 1u;
         char *buf = qsm + st * g.stage_bytes;
         // this stage: every thread observes its copy's completion
-        if (!mbar_wait(&bars[st], (n / kTStages) & 1u, kQWaitLimit)) atomicOr(&failed, 1);
+        if (!mbar_wait(&bars[st], (n / kTStages) & 1u, wait_polls)) atomicOr(&failed, 1);
         int64_t slab_g;
         int col;
         if (g.Dc == g.D) {
@@ -326,7 +333,7 @@ quantize_table_kernel(const uint16_t *__restrict__ x, const float *__restrict__ 
             const uint32_t nn = n + 1;
             const int ntask = 4 * t_blocks(g, sn);
             if (warp < ntask) {
-                if (!mbar_wait(&bars[nn % kTStages], (nn / kTStages) & 1u, kQWaitLimit))
+                if (!mbar_wait(&bars[nn % kTStages], (nn / kTStages) & 1u, wait_polls))
                     atomicOr(&failed, 1);
                 const float *cb = reinterpret_cast<const float *>(qsm + (nn % kTStages) * g.stage_bytes +
                                                                   g.x_bytes);
@@ -335,25 +342,24 @@ quantize_table_kernel(const uint16_t *__restrict__ x, const float *__restrict__ 
             }
         }
         __syncthreads();            // stage buffer and this parity's tables are free
-        if (tid == 0) {
+        if (tid == 0 && !failed) {  // after a failed wait nothing more is issued
             const int64_t sf = s + (int64_t)kTStages * sstep;
             if (sf < g.nstages) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 t_issue(g, sf, x, codebook, buf, &bars[st]);
+                ++issued[st];
             }
         }
     }
     if (failed) {
-        // a copy never completed: report it, and give the copies this CTA
-        // issued a bounded chance to land before the shared memory is released
+        // a wait gave up: report it, and give the last copy issued into each
+        // stage buffer a bounded chance (the normal limit) to land before the
+        // shared memory is released
         __syncthreads();
         if (tid == 0) {
             if (status) atomicExch(status, KVQ_ERR_TIMEOUT);
-            for (uint32_t i = 0; i < kTStages; ++i) {
-                const uint32_t ni = n + i;
-                const int64_t si = s0 + (int64_t)ni * sstep;
-                if (si < g.nstages) mbar_wait(&bars[ni % kTStages], (ni / kTStages) & 1u, kQWaitLimit);
-            }
+            for (int i = 0; i < kTStages; ++i)
+                if (issued[i]) mbar_wait(&bars[i], (issued[i] - 1u) & 1u, kQWaitLimit);
         }
         __syncthreads();
     }
@@ -404,7 +410,7 @@ template <bool NEAREST>
 __global__ void __launch_bounds__(kQThreads, 6)
 quantize_kernel(const uint16_t *__restrict__ x, const float *__restrict__ codebook, QGeom g,
                 int64_t ntiles, PhiloxKey K, uint64_t index_base, uint8_t *__restrict__ codes,
-                int32_t *__restrict__ status) {
+                int32_t *__restrict__ status, uint32_t wait_polls) {
     extern __shared__ __align__(128) char qsm[];
     __shared__ __align__(8) uint64_t bars[kQStages];
     __shared__ __align__(16) QTables tb;
@@ -433,7 +439,7 @@ quantize_kernel(const uint16_t *__restrict__ x, const float *__restrict__ codebo
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++n) {
         const uint32_t s = n % kQStages;
         char *buf = qsm + s * g.stage_bytes;
-        if (!mbar_wait(&bars[s], (n / kQStages) & 1u, kQWaitLimit)) {
+        if (!mbar_wait(&bars[s], (n / kQStages) & 1u, wait_polls)) {
             if (tid == 0) failed = true;
         }
         __syncthreads();
@@ -620,6 +626,8 @@ int launch_quantize(const uint16_t *x, const kvq_layout &L, const float *codeboo
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
     const PhiloxKey K = philox_key(seed);
+    unsigned long long tw = 0;
+    const uint32_t wait_polls = test_wait_limit(&tw) ? 0u : kQWaitLimit;
     if (!nearest) {
         const TGeom tg = table_geometry(L);
         if (table_ok(tg)) {
@@ -628,7 +636,7 @@ int launch_quantize(const uint16_t *x, const kvq_layout &L, const float *codeboo
             const size_t smem = (size_t)kTStages * tg.stage_bytes;
             quantize_table_kernel<<<(unsigned)grid, kTThreads, smem, st>>>(x, codebook, tg, K,
                                                                             index_base, codes,
-                                                                            status);
+                                                                            status, wait_polls);
             return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
         }
     }
@@ -639,10 +647,12 @@ int launch_quantize(const uint16_t *x, const kvq_layout &L, const float *codeboo
     const size_t smem = (size_t)kQStages * g.stage_bytes;
     if (nearest)
         quantize_kernel<true><<<(unsigned)grid, kQThreads, smem, st>>>(x, codebook, g, ntiles, K,
-                                                                       index_base, codes, status);
+                                                                       index_base, codes, status,
+                                                                       wait_polls);
     else
         quantize_kernel<false><<<(unsigned)grid, kQThreads, smem, st>>>(x, codebook, g, ntiles, K,
-                                                                        index_base, codes, status);
+                                                                        index_base, codes, status,
+                                                                        wait_polls);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

@@ -102,6 +102,9 @@ def lib():
         L.kvq_allocate_static.restype = C.c_int
         L.kvq_allocate_static.argtypes = [vp, _Layout, C.c_int, dbl, C.c_int, dbl, vp, vp, vp,
                                           vp, vp, vp, vp, vp]
+        L.kvq_allocate_fixed_rate.restype = C.c_int
+        L.kvq_allocate_fixed_rate.argtypes = [vp, _Layout, C.c_int, dbl, vp, vp, vp, vp, vp, vp,
+                                              vp, vp]
         L.kvq_quantize.restype = C.c_int
         L.kvq_quantize.argtypes = [vp, _Layout, vp, vp, u64, u64, vp, vp, vp]
         L.kvq_dequantize.restype = C.c_int
@@ -206,6 +209,14 @@ def kvq_allocate_static(stats, L: Layout, s: int, budget_bits: float, mode: int,
                                      float(eta), _ptr(lam), _ptr(codebook), _ptr(k), _ptr(D_r),
                                      _ptr(H_r), _ptr(totals), _ptr(status), _stream(stream)),
            "kvq_allocate_static")
+
+
+def kvq_allocate_fixed_rate(stats, L: Layout, s: int, bits_per_entry: float, codebook, k, D_r,
+                            H_r, lambda_r, totals, status, stream=None):
+    _check(lib().kvq_allocate_fixed_rate(_ptr(stats), L.c(), int(s), float(bits_per_entry),
+                                         _ptr(codebook), _ptr(k), _ptr(D_r), _ptr(H_r),
+                                         _ptr(lambda_r), _ptr(totals), _ptr(status),
+                                         _stream(stream)), "kvq_allocate_fixed_rate")
 
 
 def kvq_quantize(x, L: Layout, codebook, k, seed: int, index_base: int, codes, status=None,
