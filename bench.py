@@ -596,6 +596,125 @@ def other_configs_bench(dev, hbm, src):
     return out
 
 
+def run_sharded(args, rank, world, local):
+    """Several GPUs on one tensor under one global lambda: rank r holds the
+    layer-shaped shard r (the same workload, drawn with seed r), the total
+    budget is 2.5 bits per entry over every shard, and the lambda search runs
+    in rounds with one all-reduce of 32 integer rate sums per round
+    (sharded.allocate); stats, the final choice and quantize are local.  The
+    step is timed eagerly (host round trips between rounds), L2 flushed
+    before it, between barriers; value = all ranks' bytes / the slowest
+    rank's time."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from rate_adaptive_kv_block_b300 import kvq, sharded, synth
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    use_dist = world > 1 or "RANK" in os.environ     # torchrun: NCCL even for one rank
+    if use_dist and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    w = synth.workload(WORKLOAD)
+    x_np = synth.make_numpy(w, seed=rank)
+    x = torch.from_numpy(x_np.view(np.int16)).view(torch.float16).to(dev)
+    L = kvq.Layout(w.S, w.T, w.D, w.G)
+    B = w.budgets[0] * w.entries * world
+    buf = kvq.Buffers(L, w.s, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    in_bytes = x.numel() * 2
+
+    def step(xin):
+        kvq.kvq_stats(xin, L, buf.stats, buf.status_stats)
+        lam, st, rounds = sharded.allocate(buf.stats, L, w.s, B, buf)
+        kvq.kvq_quantize(xin, L, buf.codebook, buf.k, 0, 0, buf.codes, buf.status_quant)
+        return lam, st, rounds
+
+    def barrier():
+        if use_dist:
+            dist.barrier()
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xff)
+        info = step(x)
+    torch.cuda.synchronize()
+    if info[1] != 0 or int(buf.status.item()) != 0:
+        raise SystemExit("sharded allocation status %d / %d" % (info[1], int(buf.status.item())))
+    with ClockSampler(local) as clk:
+        ts = []
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            torch.cuda.synchronize()
+            barrier()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            info = step(x)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        # end to end: the input from pinned host memory, the codes, codebooks,
+        # k and totals back, inside the timed interval
+        x_host = torch.from_numpy(x_np.view(np.int16)).view(torch.float16).pin_memory()
+        xe = torch.empty_like(x)
+        outs = dict(codes=torch.empty(buf.codes.shape, dtype=torch.uint8).pin_memory(),
+                    codebook=torch.empty(buf.codebook.shape, dtype=torch.float32).pin_memory(),
+                    k=torch.empty(buf.k.shape, dtype=torch.uint8).pin_memory(),
+                    totals=torch.empty(3, dtype=torch.float64).pin_memory())
+        te = []
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            torch.cuda.synchronize()
+            barrier()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            xe.copy_(x_host, non_blocking=True)
+            step(xe)
+            for key, t in outs.items():
+                t.copy_(getattr(buf, key), non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            te.append(a.elapsed_time(b))
+    tot = torch.tensor([sum(ts), sum(te)], dtype=torch.float64, device=dev)
+    if use_dist:
+        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
+    tot_ms, tot_e2e = float(tot[0].item()), float(tot[1].item())
+    value = world * args.steps * in_bytes / (tot_ms * 1e-3) / 1e9
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, dt, thr, desc = cpu_baseline(w, x_np, w.budgets[0])
+        cpu = {"value": gbs, "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc,
+               "seconds": dt, "cpu_model": cpu_model()}
+    if rank == 0:
+        h2d = x_host.numel() * 2
+        d2h = sum(t.numel() * t.element_size() for t in outs.values())
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC + "; rank r holds shard r (seed r), one global "
+                                                   "lambda over all shards",
+                       "l2": "flushed before each step (256 MB write, outside the timed interval)",
+                       "launch": "eager (the lambda search's rounds return to the host)",
+                       "parallelism": "sharded lambda over %d GPUs (all-reduce of 32 int64 "
+                                      "rate sums per search round)" % world},
+            "tokens_per_s": world * args.steps * w.T / (tot_ms * 1e-3),
+            "lambda": info[0], "search_rounds": info[2],
+            "e2e": {"value": world * args.steps * in_bytes / (tot_e2e * 1e-3) / 1e9,
+                    "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "how": "C-ABI calls with the input copied from pinned host memory and the "
+                           "codes, codebooks, k and totals copied back inside each step"},
+            "gpu_launches": args.steps * (4 + info[2]),   # stats, a rate-sum kernel per round, control init + search kernel, quantize
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if use_dist:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -605,6 +724,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-blocks", type=int, default=CPU_SAMPLE_BLOCKS)
     ap.add_argument("--no-other-configs", action="store_true")
+    ap.add_argument("--sharded", action="store_true",
+                    help="the multi-GPU mode (one global lambda over every rank's shard) also "
+                         "at one GPU")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -615,6 +737,9 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if world > 1 or args.sharded:
+        run_sharded(args, rank, world, local)
         return
 
     import numpy as np

@@ -388,6 +388,56 @@ int kvq_decode_attention(const float *q, int n_rep, kvq_layout L, const uint8_t 
                          float *out, int32_t *status, void *stream);
 
 /*
+ * One global lambda over a tensor whose blocks are split across devices
+ * ("Mathematical statement": the blocks are coupled only through lambda).
+ * Each device holds some of the blocks (any split: streams, layers, ...) and
+ * their kvq_stats record.  The 40-step bisection of kvq_allocate then runs as
+ * rounds: every rank asks kvq_search_probes for the round's lambdas (up to
+ * 32), evaluates its own blocks there with kvq_rate_sums, the ranks add the
+ * 32 integer sums (an all-reduce; integer adds are exact, so the result does
+ * not depend on the split or the order), and every rank feeds the same sums
+ * to kvq_search_advance, so all ranks hold the same search state.  When
+ * kvq_search_probes returns 0 the search is done: kvq_search_result gives
+ * lambda, and each rank takes its blocks' choice there with kvq_allocate in
+ * KVQ_SUBGRADIENT mode with eta = 0.  The result does not depend on how the
+ * blocks are split (bit for bit), and it is the bisection of kvq_allocate
+ * with the same control and rate sums; kvq_allocate's own search evaluates
+ * other probes (a sampled pilot round places its first ones), so the two
+ * lambdas agree within the binary32 DP's rounding (both within the parity
+ * tolerance of the exact bisection).
+ *
+ * kvq_search_state_bytes  size of the state (host memory, caller-owned).
+ * kvq_search_begin        start: hi0 = the largest (c_max - c_min)^2 over all
+ *                         ranks' blocks (kvq_stats_hi0 on each, then the max),
+ *                         budget_bits the total budget over all ranks.
+ * kvq_search_probes       the round's lambdas into lambdas[0 .. n-1]; returns
+ *                         n, 0 when the search is done, -1 on a bad argument.
+ * kvq_search_advance      feed the round's total fixed-point rate sums
+ *                         (rate_sums[p] for probe p, the all-reduced output
+ *                         of kvq_rate_sums).
+ * kvq_search_result       lambda and the number of rounds; KVQ_OK,
+ *                         KVQ_ERR_INFEASIBLE (lambda then is the largest
+ *                         bracket), KVQ_ERR_INVALID_ARG if not done.
+ * kvq_stats_hi0           the largest (c_max - c_min)^2 of one kvq_stats
+ *                         record (synchronous copy to the host); returns
+ *                         KVQ_ERR_NONFINITE if a block holds NaN or +-Inf.
+ * kvq_rate_sums           device int64 sums[32]: sums[p] = sum over the
+ *                         layout's blocks of d_r H_r at float(lambdas[p]) in
+ *                         units of 2^-20 bit (each block rounded once), the
+ *                         exact DP of kvq_allocate; sums[p] = 0 for p >= n.
+ *                         lambdas is host memory (n <= 32, each finite, >= 0).
+ * All but kvq_stats_hi0 and kvq_rate_sums are host computations.
+ */
+size_t kvq_search_state_bytes(void);
+int kvq_search_begin(double hi0, double budget_bits, void *state);
+int kvq_search_probes(const void *state, double *lambdas);
+int kvq_search_advance(void *state, const int64_t *rate_sums, double budget_bits);
+int kvq_search_result(const void *state, double *lambda, int32_t *rounds);
+int kvq_stats_hi0(const void *stats, double *hi0);
+int kvq_rate_sums(const void *stats, kvq_layout L, int s, const double *lambdas, int nprobe,
+                  int64_t *sums, void *stream);
+
+/*
  * kvq_allocate_report -- what the last kvq_allocate on this workspace did
  * (diagnostics; no counterpart on the method's page).  Synchronous: waits
  * for the copy of the control block to the host.

@@ -59,6 +59,12 @@ static int g_resident[kMaxDevices][2][2];   // [device][s < 16][fused]
 static __device__ __align__(256) unsigned char g_static_workspace[KVQ_STATIC_WORKSPACE_BYTES];
 static void *g_static_addr[kMaxDevices];
 
+// lambdas of one evaluation of the global search (kernel parameter)
+struct ProbeSet {
+    double lambda[kSearchProbes];
+    int n;
+};
+
 // ---------------------------------------------------------------- workspace
 struct Workspace {
     Ctrl *ctrl;
@@ -1431,6 +1437,57 @@ fixed_rate_kernel(const float *__restrict__ tables, int64_t nb, int s, double bi
     }
 }
 
+// --------------------------------------------------- per-probe rate sums
+// Sum over the layout's blocks of d_r H_r at up to 32 lambdas (one lane per
+// lambda, the exact DP at float(lambda)), in fixed point (2^-20 bit units,
+// each block's rate rounded once): the quantity one evaluation of the global
+// lambda search needs.  Integer sums are exact and do not depend on the order
+// of the adds, so the sums of blocks split across devices add up to the sum
+// over all of them bit for bit.
+template <bool GENERAL>
+__global__ void __launch_bounds__(RoundCfg<GENERAL>::kWarps * 32)
+rate_sums_kernel(const float *__restrict__ tables, int64_t nb, int s, ProbeSet probes,
+                 unsigned long long *__restrict__ sums) {
+    using Cfg = RoundCfg<GENERAL>;
+    constexpr int W = Cfg::kWarps;
+    extern __shared__ __align__(16) float smem[];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    float *sTbl = smem + w * kTblStride;
+    float *sState = smem + W * kTblStride + w * Cfg::kStateFloats;
+    float *sDiag = smem + W * (kTblStride + Cfg::kStateFloats) + w * 32;
+    __shared__ long long sSum[W][32];
+    const float lam = lane < probes.n ? (float)probes.lambda[lane] : 0.f;
+    long long acc = 0;
+    for (int64_t b = (int64_t)blockIdx.x * W + w; b < nb; b += (int64_t)gridDim.x * W) {
+        const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
+        float4 *dst = reinterpret_cast<float4 *>(sTbl);
+        for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
+        __syncwarp();
+        const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
+        float rate = 0.f;
+        uint32_t mask = 1u;
+        if (mp > 1) {
+            const int C = mp > s ? mp - s : 0;
+            if (!GENERAL || C == 0 || (C == 1 && mp == 17)) {
+                dp_a_diag(sTbl, sDiag, lane);
+                dp_path_a(sTbl, lam, C, sState, sState + kPairs * 32, sDiag, lane, rate, mask);
+            } else {
+                dp_path_b(sTbl, lam, s, sState, sState + kPairs * 32,
+                          reinterpret_cast<uint32_t *>(sState + 2 * kPairs * 32), lane, rate, mask);
+            }
+        }
+        acc += llrint((double)rate * kRateScale);
+        __syncwarp();
+    }
+    sSum[w][lane] = acc;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        long long t = 0;
+        for (int k = 0; k < W; ++k) t += sSum[k][threadIdx.x];
+        if (t && threadIdx.x < probes.n) atomicAdd(&sums[threadIdx.x], (unsigned long long)t);
+    }
+}
+
 // Totals of the fixed-rate comparator in a fixed order: each thread a
 // contiguous run of blocks, then a fixed tree; the status of the data.
 __global__ void fixed_rate_totals_kernel(const StatsHeader *__restrict__ hdr, int64_t nb, int d,
@@ -1573,6 +1630,40 @@ int launch_fixed_rate(const void *stats, const kvq_layout &L, int s, double bits
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
+int launch_rate_sums(const void *stats, const kvq_layout &L, int s, const double *lambdas,
+                     int nprobe, unsigned long long *sums, cudaStream_t st) {
+    if (cudaMemsetAsync(sums, 0, kSearchProbes * sizeof(unsigned long long), st) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    const int64_t nb = num_blocks(L);
+    if (nb == 0 || nprobe == 0) return KVQ_OK;
+    ProbeSet ps = {};
+    for (int p = 0; p < nprobe; ++p) ps.lambda[p] = lambdas[p];
+    ps.n = nprobe;
+    const float *recs = reinterpret_cast<const float *>(static_cast<const char *>(stats) +
+                                                        sizeof(StatsHeader));
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+    const bool general = s < 16;
+    const int W = general ? RoundCfg<true>::kWarps : RoundCfg<false>::kWarps;
+    int64_t grid = (nb + W - 1) / W;
+    const int64_t cap = 8 * (int64_t)g_resident[dev][general ? 1 : 0][0];
+    if (cap > 0 && grid > cap) grid = cap;
+    const size_t smem = general ? RoundCfg<true>::kSmem : RoundCfg<false>::kSmem;
+    if (general)
+        rate_sums_kernel<true><<<(unsigned)grid, W * 32, smem, st>>>(recs, nb, s, ps, sums);
+    else
+        rate_sums_kernel<false><<<(unsigned)grid, W * 32, smem, st>>>(recs, nb, s, ps, sums);
+    return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+int stats_hi0(const void *stats, double *hi0) {
+    StatsHeader h;
+    if (cudaMemcpy(&h, stats, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return KVQ_ERR_CUDA;
+    uint64_t b = h.hi0_bits;
+    memcpy(hi0, &b, 8);
+    return (h.flags & kFlagNonfinite) ? KVQ_ERR_NONFINITE : KVQ_OK;
+}
+
 int allocate_report(const void *workspace, kvq_report *r) {
     Ctrl c;
     if (cudaMemcpy(&c, workspace, sizeof(Ctrl), cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -1619,6 +1710,13 @@ int allocate_init() {
         setup_search_kernel<false, true>(sms, r[0][1]) != KVQ_OK ||
         setup_search_kernel<true, false>(sms, r[1][0]) != KVQ_OK ||
         setup_search_kernel<true, true>(sms, r[1][1]) != KVQ_OK)
+        return KVQ_ERR_CUDA;
+    if (cudaFuncSetAttribute((const void *)rate_sums_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)RoundCfg<false>::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute((const void *)rate_sums_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)RoundCfg<true>::kSmem) != cudaSuccess)
         return KVQ_ERR_CUDA;
     if (cudaFuncSetAttribute((const void *)fixed_rate_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -1,6 +1,7 @@
 // C ABI of libkvq (declared in include/kvq.h): argument validation on the
 // host, then stream-ordered launches.  Nothing here allocates memory.
 #include <math.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -38,6 +39,9 @@ int allocate_init();
 int weights_init();
 int allocate_report(const void *workspace, kvq_report *r);
 void *static_workspace_address(int dev);
+int launch_rate_sums(const void *stats, const kvq_layout &L, int s, const double *lambdas,
+                     int nprobe, unsigned long long *sums, cudaStream_t st);
+int stats_hi0(const void *stats, double *hi0);
 int launch_fixed_rate(const void *stats, const kvq_layout &L, int s, double bits_per_entry,
                       float *codebook, uint8_t *k, float *Dr, float *Hr, double *lambdas,
                       double *totals, int32_t *status, cudaStream_t st);
@@ -202,6 +206,72 @@ int kvq_allocate_fixed_rate(const void *stats, kvq_layout L, int s, double bits_
     if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
     return launch_fixed_rate(stats, L, s, bits_per_entry, codebook, k, D_r, H_r, lambda_r, totals,
                              status, static_cast<cudaStream_t>(stream));
+}
+
+size_t kvq_search_state_bytes(void) { return sizeof(SearchState); }
+
+int kvq_search_begin(double hi0, double budget_bits, void *state) {
+    if (!state || !(hi0 >= 0.0) || !isfinite(hi0)) return KVQ_ERR_INVALID_ARG;
+    if (!(budget_bits >= 0.0) || !isfinite(budget_bits)) return KVQ_ERR_INVALID_ARG;
+    SearchState s;
+    search_init(s);
+    s.hi0 = hi0;
+    s.f32_lambda = 1;     // kvq_rate_sums evaluates the DP at float(lambda)
+    memcpy(state, &s, sizeof(s));
+    return KVQ_OK;
+}
+
+int kvq_search_probes(const void *state, double *lambdas) {
+    if (!state || !lambdas) return -1;
+    SearchState s;
+    memcpy(&s, state, sizeof(s));
+    if (s.phase == kSearchDone) return 0;
+    for (int p = 0; p < s.nprobe; ++p) lambdas[p] = search_probe(s, p);
+    return s.nprobe;
+}
+
+int kvq_search_advance(void *state, const int64_t *rate_sums, double budget_bits) {
+    if (!state || !rate_sums) return KVQ_ERR_INVALID_ARG;
+    if (!(budget_bits >= 0.0) || !isfinite(budget_bits)) return KVQ_ERR_INVALID_ARG;
+    SearchState s;
+    memcpy(&s, state, sizeof(s));
+    if (s.phase == kSearchDone) return KVQ_OK;
+    long long R[kSearchProbes];
+    for (int p = 0; p < kSearchProbes; ++p) R[p] = p < s.nprobe ? (long long)rate_sums[p] : 0;
+    search_update(s, R, budget_bits);
+    memcpy(state, &s, sizeof(s));
+    return KVQ_OK;
+}
+
+int kvq_search_result(const void *state, double *lambda, int32_t *rounds) {
+    if (!state || !lambda) return KVQ_ERR_INVALID_ARG;
+    SearchState s;
+    memcpy(&s, state, sizeof(s));
+    if (s.phase != kSearchDone) return KVQ_ERR_INVALID_ARG;
+    *lambda = s.lambda;
+    if (rounds) *rounds = s.rounds;
+    return s.infeasible ? KVQ_ERR_INFEASIBLE : KVQ_OK;
+}
+
+int kvq_stats_hi0(const void *stats, double *hi0) {
+    if (!stats || !hi0) return KVQ_ERR_INVALID_ARG;
+    return stats_hi0(stats, hi0);
+}
+
+int kvq_rate_sums(const void *stats, kvq_layout L, int s, const double *lambdas, int nprobe,
+                  int64_t *sums, void *stream) {
+    if (!layout_ok(L) || s < 2 || s > kMaxLev) return KVQ_ERR_INVALID_ARG;
+    if (nprobe < 0 || nprobe > kSearchProbes || (nprobe > 0 && !lambdas) || !sums)
+        return KVQ_ERR_INVALID_ARG;
+    for (int p = 0; p < nprobe; ++p)
+        if (!(lambdas[p] >= 0.0) || !isfinite(lambdas[p])) return KVQ_ERR_INVALID_ARG;
+    const int64_t nb = num_blocks(L);
+    if (nb > 0 && (!stats || !aligned16(stats))) return KVQ_ERR_INVALID_ARG;
+    if (nb > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
+    if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
+    return launch_rate_sums(stats, L, s, lambdas, nprobe,
+                            reinterpret_cast<unsigned long long *>(sums),
+                            static_cast<cudaStream_t>(stream));
 }
 
 int kvq_quantize(const uint16_t *x, kvq_layout L, const float *codebook, const uint8_t *k,

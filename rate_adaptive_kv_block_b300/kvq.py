@@ -105,6 +105,20 @@ def lib():
         L.kvq_allocate_fixed_rate.restype = C.c_int
         L.kvq_allocate_fixed_rate.argtypes = [vp, _Layout, C.c_int, dbl, vp, vp, vp, vp, vp, vp,
                                               vp, vp]
+        L.kvq_search_state_bytes.restype = C.c_size_t
+        L.kvq_search_state_bytes.argtypes = []
+        L.kvq_search_begin.restype = C.c_int
+        L.kvq_search_begin.argtypes = [dbl, dbl, vp]
+        L.kvq_search_probes.restype = C.c_int
+        L.kvq_search_probes.argtypes = [vp, vp]
+        L.kvq_search_advance.restype = C.c_int
+        L.kvq_search_advance.argtypes = [vp, vp, dbl]
+        L.kvq_search_result.restype = C.c_int
+        L.kvq_search_result.argtypes = [vp, vp, vp]
+        L.kvq_stats_hi0.restype = C.c_int
+        L.kvq_stats_hi0.argtypes = [vp, vp]
+        L.kvq_rate_sums.restype = C.c_int
+        L.kvq_rate_sums.argtypes = [vp, _Layout, C.c_int, vp, C.c_int, vp, vp]
         L.kvq_quantize.restype = C.c_int
         L.kvq_quantize.argtypes = [vp, _Layout, vp, vp, u64, u64, vp, vp, vp]
         L.kvq_dequantize.restype = C.c_int
@@ -217,6 +231,51 @@ def kvq_allocate_fixed_rate(stats, L: Layout, s: int, bits_per_entry: float, cod
                                          _ptr(codebook), _ptr(k), _ptr(D_r), _ptr(H_r),
                                          _ptr(lambda_r), _ptr(totals), _ptr(status),
                                          _stream(stream)), "kvq_allocate_fixed_rate")
+
+
+class SearchState:
+    """Host state of the global lambda search driven round by round
+    (kvq_search_* in include/kvq.h)."""
+
+    def __init__(self, hi0: float, budget_bits: float):
+        self.buf = (C.c_char * lib().kvq_search_state_bytes())()
+        self.budget = float(budget_bits)
+        _check(lib().kvq_search_begin(float(hi0), self.budget, self.buf), "kvq_search_begin")
+
+    def probes(self):
+        lam = (C.c_double * 32)()
+        n = lib().kvq_search_probes(self.buf, lam)
+        if n < 0:
+            raise KvqError("kvq_search_probes: bad argument")
+        return list(lam)[:n]
+
+    def advance(self, rate_sums):
+        arr = (C.c_int64 * 32)(*[int(v) for v in list(rate_sums)[:32]] +
+                               [0] * (32 - min(32, len(rate_sums))))
+        _check(lib().kvq_search_advance(self.buf, arr, self.budget), "kvq_search_advance")
+
+    def result(self):
+        lam = C.c_double(0.0)
+        rounds = C.c_int32(0)
+        st = lib().kvq_search_result(self.buf, C.byref(lam), C.byref(rounds))
+        if st == KVQ_ERR_INVALID_ARG:
+            raise KvqError("kvq_search_result: the search is not done")
+        return lam.value, st, rounds.value
+
+
+def kvq_stats_hi0(stats) -> float:
+    v = C.c_double(0.0)
+    rc = lib().kvq_stats_hi0(_ptr(stats), C.byref(v))
+    if rc not in (KVQ_OK, KVQ_ERR_NONFINITE):
+        _check(rc, "kvq_stats_hi0")
+    return v.value
+
+
+def kvq_rate_sums(stats, L: Layout, s: int, lambdas, sums, stream=None):
+    """sums: device int64 [32]; lambdas: up to 32 host floats."""
+    lam = (C.c_double * 32)(*list(lambdas)[:32])
+    _check(lib().kvq_rate_sums(_ptr(stats), L.c(), int(s), lam, len(lambdas), _ptr(sums),
+                               _stream(stream)), "kvq_rate_sums")
 
 
 def kvq_quantize(x, L: Layout, codebook, k, seed: int, index_base: int, codes, status=None,
