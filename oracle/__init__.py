@@ -419,6 +419,78 @@ def entropy_decode(slot, d):
     return (sym[0::2] | (sym[1::2] << 4)).astype(np.uint8)
 
 
+def entropy_encode_segments(codes, d, nseg):
+    """Entropy coding across adjacent blocks ("Rate-adaptive KV-cache
+    quantizer", "Implementation notes": arithmetic coding across adjacent
+    blocks): the blocks in runs (segments) of nseg consecutive blocks (the
+    last run may be shorter), each run coded as 32 interleaved rANS streams
+    whose state continues from block to block; stream l holds entries l, l+32,
+    .. of the run's first block, then of its second, and so on; every symbol
+    is coded with its own block's exact counts (total d), the rANS of
+    entropy_encode otherwise (32-bit state in [L, 256 L), L = 2^23, byte
+    renormalisation, encoded last symbol first).  Segment slot = the m blocks'
+    16 u16 counts each, 32 u16 stream lengths, the streams (each: final state
+    4 bytes little-endian, then its bytes in the order the decoder reads
+    them).  Returns a list of bytes objects (one per segment)."""
+    lg = int(d).bit_length() - 1
+    n = d // 32
+    rows = np.asarray(codes, dtype=np.uint8)
+    out = []
+    for s0 in range(0, rows.shape[0], nseg):
+        blocks = rows[s0:s0 + nseg]
+        syms = [_unpack(r) for r in blocks]
+        cnts = [np.bincount(sy, minlength=16) for sy in syms]
+        cums = [np.concatenate([[0], np.cumsum(c)]) for c in cnts]
+        streams = []
+        for lane in range(32):
+            x, emitted = RANS_L, []
+            for bi in range(len(blocks) - 1, -1, -1):
+                sym, cnt, cum = syms[bi], cnts[bi], cums[bi]
+                for j in range(n - 1, -1, -1):
+                    c = int(sym[lane + 32 * j])
+                    f, bc = int(cnt[c]), int(cum[c])
+                    xmax = ((RANS_L >> lg) << 8) * f
+                    while x >= xmax:
+                        emitted.append(x & 255)
+                        x >>= 8
+                    x = ((x // f) << lg) + (x % f) + bc
+            streams.append(bytes([x & 255, (x >> 8) & 255, (x >> 16) & 255, (x >> 24) & 255]
+                                 + emitted[::-1]))
+        head = b"".join(int(v).to_bytes(2, "little") for cnt in cnts for v in cnt)
+        head += b"".join(len(st).to_bytes(2, "little") for st in streams)
+        out.append(head + b"".join(streams))
+    return out
+
+
+def entropy_decode_segments(slot, d, m):
+    """The packed codes [m, d/2] of one segment slot of m blocks written by
+    entropy_encode_segments."""
+    lg = int(d).bit_length() - 1
+    n = d // 32
+    cnts = [[int.from_bytes(slot[32 * b + 2 * t:32 * b + 2 * t + 2], "little") for t in range(16)]
+            for b in range(m)]
+    cums = [np.concatenate([[0], np.cumsum(c)]) for c in cnts]
+    h = 32 * m
+    lens = [int.from_bytes(slot[h + 2 * l:h + 2 * l + 2], "little") for l in range(32)]
+    sym = np.zeros((m, d), dtype=np.int64)
+    p = h + 64
+    for lane in range(32):
+        st = slot[p:p + lens[lane]]
+        p += lens[lane]
+        x = int.from_bytes(st[:4], "little")
+        q = 4
+        for b in range(m):
+            for j in range(n):
+                s = x & (d - 1)
+                c = int(np.searchsorted(cums[b], s, side="right") - 1)
+                x = cnts[b][c] * (x >> lg) + s - int(cums[b][c])
+                while x < RANS_L:
+                    x = (x << 8) | st[q]
+                    q += 1
+                sym[b, lane + 32 * j] = c
+    return (sym[:, 0::2] | (sym[:, 1::2] << 4)).astype(np.uint8)
+
+
 def decode_attention(q, k_codes, k_codebook, v_codes, v_codebook, S, T, D, G, n_rep, T_valid,
                      scale):
     """One decoding step of attention over the stored cache, in fp64 ("Rate-

@@ -53,6 +53,47 @@ def test_oracle_round_trip_and_size_bounds(case, d):
         assert abs(payload - d / 2) <= 32 * 6          # exactly 4 bits a symbol, plus the states
 
 
+def _segment_blocks(r, d, m):
+    names = sorted(CASES)
+    return np.stack([CASES[names[(i * 3) % len(names)]](r, d) for i in range(m)]).astype(np.int64)
+
+
+@pytest.mark.parametrize("d,m,nseg", [(256, 7, 3), (1024, 5, 1), (256, 16, 16), (4096, 3, 2)])
+def test_oracle_segments_round_trip_and_size_bounds(d, m, nseg):
+    # runs of adjacent blocks with different distributions, a ragged last run
+    r = np.random.default_rng(d * 131 + m * 7 + nseg)
+    sym = _segment_blocks(r, d, m)
+    codes = _pack(sym)
+    slots = oracle.entropy_encode_segments(codes, d, nseg)
+    assert len(slots) == -(-m // nseg)
+    for i, slot in enumerate(slots):
+        blk = sym[i * nseg:(i + 1) * nseg]
+        mb = blk.shape[0]
+        assert np.array_equal(oracle.entropy_decode_segments(slot, d, mb),
+                              codes[i * nseg:i * nseg + mb])
+        # rANS bounds of the run: at least the blocks' empirical entropy, at
+        # most that plus each stream's state and one byte of slack
+        payload = len(slot) - 32 * mb - 64
+        h = sum(_entropy_bits(b) for b in blk)
+        assert h / 8 <= payload + 1e-9
+        assert payload <= h / 8 + 32 * 6
+
+
+def test_oracle_segments_share_the_state_and_cost_less():
+    # one block per run: the streams are those of the per-block coder; longer
+    # runs store the 32 states and lengths once per run
+    r = np.random.default_rng(3)
+    d, m = 1024, 12
+    sym = _segment_blocks(r, d, m)
+    codes = _pack(sym)
+    per_block = oracle.entropy_encode(codes, d)
+    one = oracle.entropy_encode_segments(codes, d, 1)
+    for a, b in zip(per_block, one):
+        assert a[96:] == b[96:]                       # the same streams
+    runs = oracle.entropy_encode_segments(codes, d, 6)
+    assert sum(map(len, runs)) < sum(map(len, per_block)) - (m - 2) * 96
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("name,T,S,G", [("llama3_8b_layer", 256, 16, 128),
                                         ("hadamard_groups", 256, 8, 32),
