@@ -354,10 +354,32 @@ def entropy_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, de
     assert torch.equal(back, buf.codes) and int(st.item()) == 0
     stored = float(nbytes.double().sum())
     n = x.numel()
+    # coding across adjacent blocks: runs of 16 consecutive blocks
+    nseg = 16
+    nruns = -(-nb // nseg)
+    rcap = kvq.kvq_entropy_run_bytes(L, nseg)
+    rout = torch.zeros((nruns, rcap), dtype=torch.uint8, device=dev)
+    rbytes = torch.zeros(nruns, dtype=torch.int32, device=dev)
+    rback = torch.empty_like(buf.codes)
+    g_re = graph_of(lambda: (flush_l2(1), kvq.kvq_entropy_encode_runs(buf.codes, L, nseg, rout, rbytes)))
+    g_rd = graph_of(lambda: (flush_l2(1), kvq.kvq_entropy_decode_runs(rout, L, nseg, rback, st)))
+    device_ms(g_re, 2)
+    device_ms(g_rd, 2)
+    t_re = device_ms(g_re, nrep) - t_flush
+    t_rd = device_ms(g_rd, nrep) - t_flush
+    torch.cuda.synchronize()
+    assert torch.equal(rback, buf.codes) and int(st.item()) == 0
+    rstored = float(rbytes.double().sum())
     return {"what": "the layer's 4-bit codes entropy-coded per block (rANS, exact counts, 32 "
                     "streams per block); bits per entry include the 96-byte block headers, not "
                     "the 64-byte codebooks",
             "stored_bits_per_entry": stored * 8 / n, "rate_target_bits": float(buf.totals[0]) / n,
+            "runs_of_adjacent_blocks": {"blocks_per_run": nseg,
+                                        "stored_bits_per_entry": rstored * 8 / n,
+                                        "encode_ms": t_re, "decode_ms": t_rd,
+                                        "what": "32 rANS streams per run of 16 consecutive blocks, "
+                                                "states carried across the blocks; counts "
+                                                "(32 B) per block, states and lengths per run"},
             "packed_bits_per_entry": 4.0,
             "encode_ms": t_e, "decode_ms": t_d,
             "encode_GBps_of_codes": (n / 2) / (t_e * 1e-3) / 1e9,

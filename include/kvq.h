@@ -349,6 +349,35 @@ int kvq_entropy_decode(const uint8_t *in, kvq_layout L, uint8_t *codes, int32_t 
                        void *stream);
 
 /*
+ * kvq_entropy_encode_runs / kvq_entropy_decode_runs -- coding across adjacent
+ * blocks ("Implementation notes": arithmetic coding across adjacent blocks).
+ * The blocks in runs of nseg consecutive blocks (1 <= nseg <= 32; the last
+ * run may be shorter): a run is one set of 32 interleaved rANS streams whose
+ * state continues from block to block (stream l: entries l, l+32, .. of the
+ * run's first block, then of its second, ..), every symbol coded with its own
+ * block's exact counts, the rANS of kvq_entropy_encode otherwise.  The 32
+ * states and lengths are stored once per run instead of once per block; a
+ * run decodes as a whole.
+ * Run slot r at out + r * kvq_entropy_run_bytes(L, nseg) (little-endian):
+ *   [0, 32 m)          16 x u16 counts of each of its m blocks
+ *   [32 m, 32 m + 64)  32 x u16: bytes of each stream
+ *   then the streams in order, each its final state (4 bytes) and its bytes
+ *   in the order the decoder reads them.
+ *   codes   device uint8 [nblocks][16 group] (kvq_quantize's layout).
+ *   out     device, ceil(nblocks / nseg) slots; nbytes device uint32 per run:
+ *           the run's stored size.
+ *   status  (decode) device int32: KVQ_ERR_CORRUPT for a malformed slot
+ *           (every read is checked against the slot; the codes of such a
+ *           run are unspecified).
+ * kvq_entropy_run_bytes returns 0 for an invalid layout or nseg.
+ */
+size_t kvq_entropy_run_bytes(kvq_layout L, int nseg);
+int kvq_entropy_encode_runs(const uint8_t *codes, kvq_layout L, int nseg, uint8_t *out,
+                            uint32_t *nbytes, void *stream);
+int kvq_entropy_decode_runs(const uint8_t *in, kvq_layout L, int nseg, uint8_t *codes,
+                            int32_t *status, void *stream);
+
+/*
  * kvq_decode_attention -- one decoding step of attention over the quantized
  * cache, with the codes decoded in registers ("Implementation notes": decode
  * before attention; the page records attention latency).  For query head hq

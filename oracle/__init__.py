@@ -419,19 +419,19 @@ def entropy_decode(slot, d):
     return (sym[0::2] | (sym[1::2] << 4)).astype(np.uint8)
 
 
-def entropy_encode_segments(codes, d, nseg):
+def entropy_encode_runs(codes, d, nseg):
     """Entropy coding across adjacent blocks ("Rate-adaptive KV-cache
     quantizer", "Implementation notes": arithmetic coding across adjacent
-    blocks): the blocks in runs (segments) of nseg consecutive blocks (the
+    blocks): the blocks in runs of nseg consecutive blocks (the
     last run may be shorter), each run coded as 32 interleaved rANS streams
     whose state continues from block to block; stream l holds entries l, l+32,
     .. of the run's first block, then of its second, and so on; every symbol
     is coded with its own block's exact counts (total d), the rANS of
     entropy_encode otherwise (32-bit state in [L, 256 L), L = 2^23, byte
-    renormalisation, encoded last symbol first).  Segment slot = the m blocks'
+    renormalisation, encoded last symbol first).  Run slot = the m blocks'
     16 u16 counts each, 32 u16 stream lengths, the streams (each: final state
     4 bytes little-endian, then its bytes in the order the decoder reads
-    them).  Returns a list of bytes objects (one per segment)."""
+    them).  Returns a list of bytes objects (one per run)."""
     lg = int(d).bit_length() - 1
     n = d // 32
     rows = np.asarray(codes, dtype=np.uint8)
@@ -462,9 +462,9 @@ def entropy_encode_segments(codes, d, nseg):
     return out
 
 
-def entropy_decode_segments(slot, d, m):
-    """The packed codes [m, d/2] of one segment slot of m blocks written by
-    entropy_encode_segments."""
+def entropy_decode_runs(slot, d, m):
+    """The packed codes [m, d/2] of one run slot of m blocks written by
+    entropy_encode_runs."""
     lg = int(d).bit_length() - 1
     n = d // 32
     cnts = [[int.from_bytes(slot[32 * b + 2 * t:32 * b + 2 * t + 2], "little") for t in range(16)]

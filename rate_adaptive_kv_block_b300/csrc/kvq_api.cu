@@ -35,6 +35,12 @@ int launch_entropy_encode(const uint8_t *codes, const kvq_layout &L, uint8_t *ou
 int launch_entropy_decode(const uint8_t *in, const kvq_layout &L, uint8_t *codes, int32_t *status,
                           cudaStream_t st);
 size_t entropy_slot(const kvq_layout &L);
+int launch_entropy_encode_runs(const uint8_t *codes, const kvq_layout &L, int nseg, uint8_t *out,
+                               uint32_t *nbytes, cudaStream_t st);
+int launch_entropy_decode_runs(const uint8_t *in, const kvq_layout &L, int nseg, uint8_t *codes,
+                               int32_t *status, cudaStream_t st);
+size_t entropy_run_slot(const kvq_layout &L, int nseg);
+int entropy_run_max_blocks();
 int allocate_init();
 int weights_init();
 int allocate_report(const void *workspace, kvq_report *r);
@@ -347,6 +353,32 @@ int kvq_entropy_decode(const uint8_t *in, kvq_layout L, uint8_t *codes, int32_t 
     if (!status || (num_blocks(L) > 0 && (!in || !codes || !aligned16(in) || !aligned16(codes))))
         return KVQ_ERR_INVALID_ARG;
     return launch_entropy_decode(in, L, codes, status, static_cast<cudaStream_t>(stream));
+}
+
+static bool runs_ok(const kvq_layout &L, int nseg) {
+    return layout_ok(L) && nseg >= 1 && nseg <= entropy_run_max_blocks();
+}
+
+size_t kvq_entropy_run_bytes(kvq_layout L, int nseg) {
+    return runs_ok(L, nseg) ? entropy_run_slot(L, nseg) : 0;
+}
+
+int kvq_entropy_encode_runs(const uint8_t *codes, kvq_layout L, int nseg, uint8_t *out,
+                            uint32_t *nbytes, void *stream) {
+    if (!runs_ok(L, nseg)) return KVQ_ERR_INVALID_ARG;
+    if (num_blocks(L) > 0 && (!codes || !out || !nbytes || !aligned16(codes) || !aligned16(out)))
+        return KVQ_ERR_INVALID_ARG;
+    return launch_entropy_encode_runs(codes, L, nseg, out, nbytes,
+                                      static_cast<cudaStream_t>(stream));
+}
+
+int kvq_entropy_decode_runs(const uint8_t *in, kvq_layout L, int nseg, uint8_t *codes,
+                            int32_t *status, void *stream) {
+    if (!runs_ok(L, nseg) || !status) return KVQ_ERR_INVALID_ARG;
+    if (num_blocks(L) > 0 && (!in || !codes || !aligned16(in) || !aligned16(codes)))
+        return KVQ_ERR_INVALID_ARG;
+    return launch_entropy_decode_runs(in, L, nseg, codes, status,
+                                      static_cast<cudaStream_t>(stream));
 }
 
 static bool attention_layout_ok(const kvq_layout &L, int n_rep) {

@@ -252,6 +252,237 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
         cout[i] = (uint8_t)(sym[w][2 * i] | (sym[w][2 * i + 1] << 4));
 }
 
+// ------------------------------------------- runs of adjacent blocks
+// Coding across adjacent blocks ("Implementation notes": arithmetic coding
+// across adjacent blocks): a run of nseg consecutive blocks is one set of 32
+// interleaved rANS streams whose state continues from block to block (stream
+// l: entries l, l+32, .. of the run's first block, then of the next, ..);
+// each symbol is coded with its own block's exact counts, so blocks keep
+// their models while the 32 states and lengths are stored once per run.
+// Run slot (capacity kvq_entropy_run_bytes, little-endian):
+//   [0, 32 m)          16 x u16 counts of each of the m blocks
+//   [32 m, 32 m + 64)  32 x u16: bytes of each stream
+//   then the streams in lane order, each its final state (4 bytes) and its
+//   renormalisation bytes in the order the decoder reads them.
+// One warp per run.  The encoder makes two passes over the run: the first
+// only counts each stream's bytes, the second writes them downwards from
+// the stream's end (known from the first), so no worst-case scratch is held.
+constexpr int kRunMaxBlocks = 32;
+constexpr int kRunWarps = 4;
+
+__host__ __device__ constexpr uint64_t run_slot_bytes(int d, int nseg) {
+    // at most 4 bits a symbol (exact counts), the counts, the lengths, and per
+    // stream its state and one byte of renormalisation slack
+    return ((uint64_t)nseg * (uint64_t)(d / 2 + 32) + 64u + 32u * 6u + 15u) & ~(uint64_t)15u;
+}
+
+__device__ __forceinline__ uint32_t nibble_at(const uint8_t *__restrict__ cb, int e) {
+    return (cb[e >> 1] >> ((e & 1) * 4)) & 15u;
+}
+
+__global__ void __launch_bounds__(kRunWarps * 32)
+entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d, int nseg,
+                           uint8_t *__restrict__ out, uint32_t *__restrict__ nbytes) {
+    __shared__ uint4 smodel[kRunWarps][kRunMaxBlocks][16];   // count, cumulative, reciprocal
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t nruns = (nb + nseg - 1) / nseg;
+    const int64_t rn = (int64_t)blockIdx.x * kRunWarps + w;
+    if (rn >= nruns) return;
+    const int64_t b0 = rn * nseg;
+    const int m = (int)min((int64_t)nseg, nb - b0);
+    const int n = d / 32, lg = ilog2(d);
+    const int half = d / 2;
+    uint8_t *slot = out + rn * (int64_t)run_slot_bytes(d, nseg);
+    const uint8_t *src = codes + b0 * half;
+    // the blocks' models: counts (lane-private, then warp sums), cumulative
+    // counts, reciprocals; the counts also go to the slot
+    for (int bi = 0; bi < m; ++bi) {
+        const uint8_t *cb = src + (int64_t)bi * half;
+        uint32_t cnt[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) cnt[t] = 0;
+        for (int j = 0; j < n; ++j) {
+            const uint32_t c = nibble_at(cb, lane + 32 * j);
+#pragma unroll
+            for (int t = 0; t < 16; ++t) cnt[t] += (c == (uint32_t)t) ? 1u : 0u;
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cnt[t] += __shfl_xor_sync(0xffffffffu, cnt[t], o);
+        if (lane < 16) {
+            uint32_t f = 0, bc = 0, acc = 0;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                if (t == lane) { f = cnt[t]; bc = acc; }
+                acc += cnt[t];
+            }
+            const Recip r = recip_of(f > 0 ? f : 1u);
+            smodel[w][bi][lane] = make_uint4(f, bc, r.m, r.sh);
+            slot[32 * bi + 2 * lane] = (uint8_t)f;
+            slot[32 * bi + 2 * lane + 1] = (uint8_t)(f >> 8);
+        }
+    }
+    __syncwarp();
+    const uint32_t xmax0 = (kRansL >> lg) << 8;
+    // pass 1: the length of this lane's stream
+    uint32_t x = kRansL, len = 4;
+    for (int bi = m - 1; bi >= 0; --bi) {
+        const uint8_t *cb = src + (int64_t)bi * half;
+        for (int j = n - 1; j >= 0; --j) {
+            const uint4 md = smodel[w][bi][nibble_at(cb, lane + 32 * j)];
+            const uint32_t xmax = xmax0 * md.x;
+            while (x >= xmax) {
+                ++len;
+                x >>= 8;
+            }
+            const uint32_t qd = div_by(x, Recip{md.z, md.w});
+            x = (qd << lg) + (x - qd * md.x) + md.y;
+        }
+    }
+    uint32_t off = len;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, off, o);
+        if (lane >= o) off += y;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, off, 31);
+    off -= len;
+    const uint32_t hdr = 32u * (uint32_t)m + 64u;
+    slot[32 * m + 2 * lane] = (uint8_t)len;
+    slot[32 * m + 2 * lane + 1] = (uint8_t)(len >> 8);
+    if (lane == 0) nbytes[rn] = hdr + total;
+    // pass 2: the same steps, the bytes written downwards from the stream's end
+    uint8_t *st = slot + hdr + off;
+    uint32_t pos = len;
+    x = kRansL;
+    for (int bi = m - 1; bi >= 0; --bi) {
+        const uint8_t *cb = src + (int64_t)bi * half;
+        for (int j = n - 1; j >= 0; --j) {
+            const uint4 md = smodel[w][bi][nibble_at(cb, lane + 32 * j)];
+            const uint32_t xmax = xmax0 * md.x;
+            while (x >= xmax) {
+                st[--pos] = (uint8_t)(x & 255u);
+                x >>= 8;
+            }
+            const uint32_t qd = div_by(x, Recip{md.z, md.w});
+            x = (qd << lg) + (x - qd * md.x) + md.y;
+        }
+    }
+    st[0] = (uint8_t)x;          // pos == 4 here: the state opens the stream
+    st[1] = (uint8_t)(x >> 8);
+    st[2] = (uint8_t)(x >> 16);
+    st[3] = (uint8_t)(x >> 24);
+}
+
+__global__ void __launch_bounds__(kRunWarps * 32)
+entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, int nseg,
+                           uint8_t *__restrict__ codes, int32_t *__restrict__ status) {
+    __shared__ uint32_t scum[kRunWarps][17], scnt[kRunWarps][16];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t nruns = (nb + nseg - 1) / nseg;
+    const int64_t rn = (int64_t)blockIdx.x * kRunWarps + w;
+    if (rn >= nruns) return;
+    const int64_t b0 = rn * nseg;
+    const int m = (int)min((int64_t)nseg, nb - b0);
+    const int n = d / 32, lg = ilog2(d);
+    const int half = d / 2;
+    const uint64_t cap = run_slot_bytes(d, nseg);
+    const uint8_t *slot = in + rn * (int64_t)cap;
+    const uint32_t hdr = 32u * (uint32_t)m + 64u;
+    const uint32_t len = (uint32_t)slot[32 * m + 2 * lane] | ((uint32_t)slot[32 * m + 2 * lane + 1] << 8);
+    uint32_t off = len;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, off, o);
+        if (lane >= o) off += y;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, off, 31);
+    off -= len;
+    // a slot that does not hold m blocks of d symbols: status, codes 0
+    bool bad = __any_sync(0xffffffffu, (uint64_t)hdr + total > cap || len < 4);
+    uint32_t p = hdr + off;
+    const uint32_t end = p + len;
+    uint32_t x = 0;
+    if (!bad) {
+        x = (uint32_t)slot[p] | ((uint32_t)slot[p + 1] << 8) | ((uint32_t)slot[p + 2] << 16) |
+            ((uint32_t)slot[p + 3] << 24);
+        p += 4;
+    }
+    bool overrun = false;
+    uint8_t *dst = codes + b0 * half;
+    for (int bi = 0; bi < m; ++bi) {
+        // this block's model: counts from the slot, cumulative counts by a scan
+        const uint32_t mycnt = lane < 16 ? ((uint32_t)slot[32 * bi + 2 * lane] |
+                                            ((uint32_t)slot[32 * bi + 2 * lane + 1] << 8))
+                                         : 0u;
+        uint32_t incl = mycnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        __syncwarp();                              // the previous block's model is done with
+        if (lane < 16) {
+            scnt[w][lane] = mycnt;
+            scum[w][lane] = incl - mycnt;
+        }
+        if (lane == 16) scum[w][16] = incl;
+        __syncwarp();
+        const bool badm = __any_sync(0xffffffffu, scum[w][16] != (uint32_t)d);
+        bad = bad || badm;
+        const uint32_t *cum = scum[w];
+        uint8_t *db = dst + (int64_t)bi * half;
+        for (int j = 0; j < n; ++j) {
+            uint32_t c = 0;
+            if (!bad && !overrun) {
+                const uint32_t s = x & ((1u << lg) - 1u);
+                c = (uint32_t)rans_symbol(cum, s);
+                x = scnt[w][c] * (x >> lg) + s - cum[c];
+                while (x < kRansL) {
+                    if (p >= end) { overrun = true; break; }   // never reads past its stream
+                    x = (x << 8) | slot[p++];
+                }
+            }
+            const uint32_t hi = __shfl_xor_sync(0xffffffffu, c, 1);
+            const int e = lane + 32 * j;
+            if ((lane & 1) == 0) db[e >> 1] = (uint8_t)(c | (hi << 4));
+        }
+    }
+    overrun = overrun || (!bad && p != end);
+    if (__any_sync(0xffffffffu, bad || overrun) && lane == 0) atomicMax(status, (int32_t)KVQ_ERR_CORRUPT);
+}
+
+int launch_entropy_encode_runs(const uint8_t *codes, const kvq_layout &L, int nseg, uint8_t *out,
+                               uint32_t *nbytes, cudaStream_t st) {
+    const int64_t nb = num_blocks(L);
+    if (nb == 0) return KVQ_OK;
+    const int d = 32 * L.group;
+    const int64_t nruns = (nb + nseg - 1) / nseg;
+    const int64_t ctas = (nruns + kRunWarps - 1) / kRunWarps;
+    entropy_encode_runs_kernel<<<(unsigned)ctas, kRunWarps * 32, 0, st>>>(codes, nb, d, nseg, out,
+                                                                          nbytes);
+    return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+int launch_entropy_decode_runs(const uint8_t *in, const kvq_layout &L, int nseg, uint8_t *codes,
+                               int32_t *status, cudaStream_t st) {
+    const int64_t nb = num_blocks(L);
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (nb == 0) return KVQ_OK;
+    const int d = 32 * L.group;
+    const int64_t nruns = (nb + nseg - 1) / nseg;
+    const int64_t ctas = (nruns + kRunWarps - 1) / kRunWarps;
+    entropy_decode_runs_kernel<<<(unsigned)ctas, kRunWarps * 32, 0, st>>>(in, nb, d, nseg, codes,
+                                                                          status);
+    return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+size_t entropy_run_slot(const kvq_layout &L, int nseg) {
+    return (size_t)run_slot_bytes(32 * L.group, nseg);
+}
+int entropy_run_max_blocks() { return kRunMaxBlocks; }
+
 int launch_entropy_encode(const uint8_t *codes, const kvq_layout &L, uint8_t *out,
                           uint32_t *nbytes, cudaStream_t st) {
     const int64_t nb = num_blocks(L);

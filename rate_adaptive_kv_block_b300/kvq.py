@@ -133,6 +133,12 @@ def lib():
         L.kvq_entropy_encode.argtypes = [vp, _Layout, vp, vp, vp]
         L.kvq_entropy_decode.restype = C.c_int
         L.kvq_entropy_decode.argtypes = [vp, _Layout, vp, vp, vp]
+        L.kvq_entropy_run_bytes.restype = C.c_size_t
+        L.kvq_entropy_run_bytes.argtypes = [_Layout, C.c_int]
+        L.kvq_entropy_encode_runs.restype = C.c_int
+        L.kvq_entropy_encode_runs.argtypes = [vp, _Layout, C.c_int, vp, vp, vp]
+        L.kvq_entropy_decode_runs.restype = C.c_int
+        L.kvq_entropy_decode_runs.argtypes = [vp, _Layout, C.c_int, vp, vp, vp]
         L.kvq_attention_workspace_bytes.restype = C.c_size_t
         L.kvq_attention_workspace_bytes.argtypes = [_Layout, C.c_int]
         L.kvq_decode_attention.restype = C.c_int
@@ -317,6 +323,20 @@ def kvq_entropy_decode(inp, L: Layout, codes, status, stream=None):
     """Decode the slots of kvq_entropy_encode back into packed codes."""
     _check(lib().kvq_entropy_decode(_ptr(inp), L.c(), _ptr(codes), _ptr(status), _stream(stream)),
            "kvq_entropy_decode")
+
+
+def kvq_entropy_run_bytes(L: Layout, nseg: int) -> int:
+    return lib().kvq_entropy_run_bytes(L.c(), int(nseg))
+
+
+def kvq_entropy_encode_runs(codes, L: Layout, nseg: int, out, nbytes, stream=None):
+    _check(lib().kvq_entropy_encode_runs(_ptr(codes), L.c(), int(nseg), _ptr(out), _ptr(nbytes),
+                                         _stream(stream)), "kvq_entropy_encode_runs")
+
+
+def kvq_entropy_decode_runs(inp, L: Layout, nseg: int, codes, status, stream=None):
+    _check(lib().kvq_entropy_decode_runs(_ptr(inp), L.c(), int(nseg), _ptr(codes), _ptr(status),
+                                         _stream(stream)), "kvq_entropy_decode_runs")
 
 
 def kvq_attention_workspace_bytes(L: Layout, n_rep: int) -> int:

@@ -53,23 +53,23 @@ def test_oracle_round_trip_and_size_bounds(case, d):
         assert abs(payload - d / 2) <= 32 * 6          # exactly 4 bits a symbol, plus the states
 
 
-def _segment_blocks(r, d, m):
+def _run_blocks(r, d, m):
     names = sorted(CASES)
     return np.stack([CASES[names[(i * 3) % len(names)]](r, d) for i in range(m)]).astype(np.int64)
 
 
 @pytest.mark.parametrize("d,m,nseg", [(256, 7, 3), (1024, 5, 1), (256, 16, 16), (4096, 3, 2)])
-def test_oracle_segments_round_trip_and_size_bounds(d, m, nseg):
+def test_oracle_runs_round_trip_and_size_bounds(d, m, nseg):
     # runs of adjacent blocks with different distributions, a ragged last run
     r = np.random.default_rng(d * 131 + m * 7 + nseg)
-    sym = _segment_blocks(r, d, m)
+    sym = _run_blocks(r, d, m)
     codes = _pack(sym)
-    slots = oracle.entropy_encode_segments(codes, d, nseg)
+    slots = oracle.entropy_encode_runs(codes, d, nseg)
     assert len(slots) == -(-m // nseg)
     for i, slot in enumerate(slots):
         blk = sym[i * nseg:(i + 1) * nseg]
         mb = blk.shape[0]
-        assert np.array_equal(oracle.entropy_decode_segments(slot, d, mb),
+        assert np.array_equal(oracle.entropy_decode_runs(slot, d, mb),
                               codes[i * nseg:i * nseg + mb])
         # rANS bounds of the run: at least the blocks' empirical entropy, at
         # most that plus each stream's state and one byte of slack
@@ -79,18 +79,18 @@ def test_oracle_segments_round_trip_and_size_bounds(d, m, nseg):
         assert payload <= h / 8 + 32 * 6
 
 
-def test_oracle_segments_share_the_state_and_cost_less():
+def test_oracle_runs_share_the_state_and_cost_less():
     # one block per run: the streams are those of the per-block coder; longer
     # runs store the 32 states and lengths once per run
     r = np.random.default_rng(3)
     d, m = 1024, 12
-    sym = _segment_blocks(r, d, m)
+    sym = _run_blocks(r, d, m)
     codes = _pack(sym)
     per_block = oracle.entropy_encode(codes, d)
-    one = oracle.entropy_encode_segments(codes, d, 1)
+    one = oracle.entropy_encode_runs(codes, d, 1)
     for a, b in zip(per_block, one):
         assert a[96:] == b[96:]                       # the same streams
-    runs = oracle.entropy_encode_segments(codes, d, 6)
+    runs = oracle.entropy_encode_runs(codes, d, 6)
     assert sum(map(len, runs)) < sum(map(len, per_block)) - (m - 2) * 96
 
 
@@ -151,5 +151,77 @@ def test_entropy_decode_reports_a_damaged_slot():
             bad[3, 32] = 3                      # stream 0 shorter than its state
             bad[3, 33] = 0
         kvq.kvq_entropy_decode(bad, L, back, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == kvq.KVQ_ERR_CORRUPT, damage
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,T,S,G,nseg", [("llama3_8b_layer", 256, 16, 128, 16),
+                                             ("llama3_8b_layer", 96, 16, 128, 5),
+                                             ("hadamard_groups", 256, 8, 32, 32),
+                                             ("k_head_small", 128, 4, 8, 3)])
+def test_run_coder_matches_oracle_and_round_trips(name, T, S, G, nseg):
+    """Coding across adjacent blocks: the runs' slots and sizes equal the
+    oracle's byte for byte (ragged last runs included), decode inverts
+    encode, and the stored bytes are below the per-block coder's."""
+    import torch
+    from rate_adaptive_kv_block_b300 import kvq, synth
+    w = synth.workload(name, T=T, S=S)
+    x = synth.make_torch(w, seed=4, device="cuda")
+    L = kvq.Layout(w.S, w.T, w.D, G)
+    buf = kvq.Buffers(L, 16)
+    kvq.quantize(x, L, 2.5 * w.entries, 16, buf=buf)
+    nb, d = L.nblocks, 32 * G
+    nruns = -(-nb // nseg)
+    cap = kvq.kvq_entropy_run_bytes(L, nseg)
+    assert cap >= nseg * (d // 2 + 32) + 64 and cap % 16 == 0
+    out = torch.zeros((nruns, cap), dtype=torch.uint8, device="cuda")
+    nbytes = torch.zeros(nruns, dtype=torch.int32, device="cuda")
+    kvq.kvq_entropy_encode_runs(buf.codes, L, nseg, out, nbytes)
+    back = torch.empty_like(buf.codes)
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    kvq.kvq_entropy_decode_runs(out, L, nseg, back, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvq.KVQ_OK
+    assert torch.equal(back, buf.codes)
+    want = oracle.entropy_encode_runs(buf.codes.cpu().numpy(), d, nseg)
+    got, sizes = out.cpu().numpy(), nbytes.cpu().numpy()
+    for r in range(nruns):
+        assert sizes[r] == len(want[r])
+        assert bytes(got[r, :sizes[r]]) == want[r]
+    per_block = sum(len(s) for s in oracle.entropy_encode(buf.codes.cpu().numpy(), d))
+    if nseg > 1:
+        assert int(sizes.sum()) < per_block
+
+
+@pytest.mark.gpu
+def test_run_decode_reports_a_damaged_slot():
+    import torch
+    from rate_adaptive_kv_block_b300 import kvq, synth
+    w = synth.workload("llama3_8b_layer", T=128, S=4)
+    x = synth.make_torch(w, seed=5, device="cuda")
+    L = kvq.Layout(w.S, w.T, w.D, w.G)
+    buf = kvq.Buffers(L, 16)
+    kvq.quantize(x, L, 2.5 * w.entries, 16, buf=buf)
+    nseg = 4
+    nruns = -(-L.nblocks // nseg)
+    cap = kvq.kvq_entropy_run_bytes(L, nseg)
+    out = torch.zeros((nruns, cap), dtype=torch.uint8, device="cuda")
+    nbytes = torch.zeros(nruns, dtype=torch.int32, device="cuda")
+    kvq.kvq_entropy_encode_runs(buf.codes, L, nseg, out, nbytes)
+    torch.cuda.synchronize()
+    back = torch.empty_like(buf.codes)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h = 32 * nseg
+    for damage in ("counts", "lengths", "stream"):
+        bad = out.clone()
+        if damage == "counts":
+            bad[1, 32 * 2] ^= 1                 # block 2's counts no longer add up to d
+        elif damage == "lengths":
+            bad[2, h + 1] = 0xFF                # a stream longer than the slot
+        else:
+            bad[3, h] = 3                       # stream 0 shorter than its state
+            bad[3, h + 1] = 0
+        kvq.kvq_entropy_decode_runs(bad, L, nseg, back, st)
         torch.cuda.synchronize()
         assert int(st.item()) == kvq.KVQ_ERR_CORRUPT, damage
