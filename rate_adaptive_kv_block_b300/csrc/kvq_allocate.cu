@@ -18,9 +18,9 @@
 //                  DP at its own lambda, so the warp evaluates 32 lambdas
 //                  with no cross-lane traffic and the table reads are
 //                  shared-memory broadcasts.  Per-probe rate sums are exact
-//                  fixed-point integer atomics; the last CTA to finish the
-//                  round advances the search (kvq_search.h) and releases the
-//                  grid for the next round:
+//                  fixed-point integer atomics; once every CTA is in, CTA 0
+//                  advances the search (kvq_search.h) and releases the grid
+//                  for the next round:
 //                    pilot round (large tensors): a sample of the blocks at
 //                    the bracket probes, for an estimate of lambda;
 //                    round 0: probes 0, hi0 * 2^{0,1,2} and a grid (around
@@ -548,8 +548,8 @@ struct RoundCfg {
         (size_t)kWarps * 32 * sizeof(long long) + (size_t)kWarps * 32 * sizeof(float);
 };
 
-// Grid-wide hand-over between rounds: the last CTA of a round publishes the
-// next round's state and then the generation number with a release store;
+// Grid-wide hand-over between rounds: CTA 0, once every CTA's ticket is in,
+// publishes the next round's state and then the generation number with a release store;
 // the other CTAs wait for it with acquire loads.  Every CTA of the grid is
 // resident (cooperative launch), and the wait is bounded all the same.
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
@@ -726,9 +726,9 @@ __device__ __noinline__ void finish_blocks(const Ctrl *ctrl, int64_t nb, int xb_
 // bracket rounds, a sample in the pilot round, in the walk only the blocks
 // evaluated in the previous round -- a block that was not is constant across
 // the window and stays so).  Each lane accumulates, per probe, the change of
-// its blocks' d_r H_r against their value at xb, in fixed point; the last
-// CTA to finish adds the sums to the total at xb and advances the search;
-// the next round starts when it publishes the new state.
+// its blocks' d_r H_r against their value at xb, in fixed point; CTA 0,
+// once every CTA has taken its ticket, adds the sums to the total at xb and
+// advances the search; the next round starts when it publishes the new state.
 //
 // Emit (after the last round), one warp per block, lane t = slot t: the
 // chain at the final lambda becomes the codebook (levels in slot order), k,
@@ -965,12 +965,33 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
             // acquire-release ticket: orders this CTA's sums (made before the
             // barrier) before it, and the last CTA sees every CTA's sums
             const unsigned t = atom_add_acq_rel_u32(&ctrl->ticket, 1u);
-            is_last = (t == gridDim.x - 1);
             timed_out = false;
+            // CTA 0 runs every round's control, once every CTA's ticket is in
+            // (spinning, bounded): the control code then stays in the
+            // instruction cache of one SM instead of being fetched cold by
+            // whichever CTA happens to finish last
+            is_last = blockIdx.x == 0;
+            if (is_last && t != gridDim.x - 1) {
+                uint32_t spins = 0;
+                const unsigned long long t0 = global_ns();
+                while (ld_acquire_u32(&ctrl->ticket) < gridDim.x) {
+                    if (++spins > ctrl->spin_limit || global_ns() - t0 > ctrl->wait_ns) {
+                        timed_out = true;
+                        break;
+                    }
+                }
+            }
         }
         __syncthreads();
+        if (timed_out) {
+            if (threadIdx.x == 0) {
+                atomicExch(&ctrl->err, 1u);
+                *status = KVQ_ERR_TIMEOUT;
+            }
+            return;
+        }
         if (is_last) {
-            // ---- last CTA: stage the control block again (the sums are
+            // ---- CTA 0: stage the control block again (the sums are
             // final now), advance the search in shared memory, write back
             // what changed, then release the other CTAs
             if (threadIdx.x == 0) ctrl->t_dp[min(round, 15)] = global_ns();
