@@ -39,6 +39,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fp16 KV GB/s quantized at budget B (1 B300) and fraction of HBM roofline"
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# layer workload's search and quantize kernels from one ncu capture each
+# (cache control on: cold L2), as summarised in
+# profiles/kernels_llama3_8b_layer.md; to be taken again whenever either
+# kernel changes
+SEARCH_DRAM_BYTES = 18502912
+QUANT_DRAM_BYTES = 33873408 + 1024000
+TRAFFIC_NOTE = "bytes per launch, ncu capture with a cold L2"
 WORKLOAD = "llama3_8b_layer"
 WORKLOAD_DESC = ("Llama-3-8B-shaped single-layer prefill: K and V, 8 KV heads x 8192 tokens x "
                  "128 dims fp16 (S=16 streams); K = N(0,1) x per-channel lognormal(0,0.5) with 4 "
@@ -252,6 +260,32 @@ def comparator_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep,
     t_f = device_ms(g_f, max(3, nrep // 4)) - t_flush
     mse_fixed = mse(bf_.codes, bf_.codebook)
     n = x.numel()
+    fixed_budget = {"rate_bits": float(bf_.totals[0].item()) / n,
+                    "expected_distortion_per_entry": float(bf_.totals[1].item()) / n}
+    # the same comparator at equal total rate: the per-block budget b' raised
+    # (bisection, 14 steps) until the blocks' total rate is the rate-adaptive
+    # allocation's (each block's rate moves in steps, so a cap of b leaves part
+    # of b unspent)
+    target = float(buf.totals[0].item())
+    lo_b, hi_b = bpe, 4.0
+    for _ in range(14):
+        mid_b = 0.5 * (lo_b + hi_b)
+        kvq.kvq_allocate_fixed_rate(bf_.stats, L, w.s, mid_b, bf_.codebook, bf_.k, bf_.D_r,
+                                    bf_.H_r, lam_r, bf_.totals, bf_.status)
+        if float(bf_.totals[0].item()) <= target:
+            lo_b = mid_b
+        else:
+            hi_b = mid_b
+    kvq.kvq_allocate_fixed_rate(bf_.stats, L, w.s, lo_b, bf_.codebook, bf_.k, bf_.D_r, bf_.H_r,
+                                lam_r, bf_.totals, bf_.status)
+    kvq.kvq_quantize(x, L, bf_.codebook, bf_.k, 0, 0, bf_.codes)
+    torch.cuda.synchronize()
+    fixed_equal = {"what": "every block at <= b' bits/entry on its own lambda, b' raised until the "
+                           "total rate equals the rate-adaptive allocation's",
+                   "block_budget_bits": lo_b, "mse": mse(bf_.codes, bf_.codebook),
+                   "rate_bits": float(bf_.totals[0].item()) / n,
+                   "expected_distortion_per_entry": float(bf_.totals[1].item()) / n,
+                   "status": int(bf_.status.item())}
     return {"what": "mean squared error of the binary16 decode and rate in bits/entry on this "
                     "layer; uniform = 16 equally spaced levels per block from its minimum to its "
                     "maximum; uniform rates are the per-block entropies of the codes",
@@ -265,12 +299,13 @@ def comparator_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep,
                                              "(kvq_allocate_fixed_rate): the same total budget as "
                                              "the rate-adaptive allocation" % bpe,
                                      "mse": mse_fixed,
-                                     "rate_bits": float(bf_.totals[0].item()) / n,
-                                     "expected_distortion_per_entry": float(bf_.totals[1].item()) / n,
+                                     "rate_bits": fixed_budget["rate_bits"],
+                                     "expected_distortion_per_entry":
+                                         fixed_budget["expected_distortion_per_entry"],
                                      "rate_adaptive_expected_distortion_per_entry":
                                          float(buf.totals[1].item()) / n,
-                                     "status": int(bf_.status.item()),
                                      "allocate_ms": t_f},
+            "fixed_rate_at_equal_rate": fixed_equal,
             "uniform_int4_ms": t_u,
             "uniform_int4_GBps": (x.numel() * 2 + x.numel() // 2 + nb * 65) / (t_u * 1e-3) / 1e9}
 
@@ -1008,6 +1043,7 @@ def main():
     kern["quantize_roofline"] = {"bound": "hbm", "achieved": kern["quantize_cold_GBps"],
                                  "peak": hbm, "unit": "GB/s",
                                  "frac": kern["quantize_cold_GBps"] / hbm,
+                                 "traffic": QUANT_DRAM_BYTES, "traffic_unit": TRAFFIC_NOTE,
                                  "peak_source": src}
     shares = {"stats": t_scold, "allocate": t_acold, "quantize": t_qcold}
     dominant = max(shares, key=shares.get)
@@ -1030,7 +1066,8 @@ def main():
         peak = n_sm * 128 * sm_mhz * 1e6 / 1e12         # fp32 lane ops, T/s
         a = dp_ops / (t_acold * 1e-3) / 1e12
         roof = {"kernel": "kvq_allocate (search rounds)", "bound": "alu", "achieved": a,
-                "peak": peak, "unit": "T fp32 lane-op/s", "frac": a / peak, "traffic": None,
+                "peak": peak, "unit": "T fp32 lane-op/s", "frac": a / peak,
+                "traffic": SEARCH_DRAM_BYTES, "traffic_unit": TRAFFIC_NOTE,
                 "work": "%d DP block-lambda evaluations x 680 triples x 2 ops" % (sum(rep["active"]) * 32),
                 "peak_source": "%d SMs x 128 fp32 lanes x median SM clock" % n_sm}
     elif dominant == "stats":
