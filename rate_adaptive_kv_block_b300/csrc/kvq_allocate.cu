@@ -617,6 +617,45 @@ __device__ __forceinline__ void stage_search(SearchState &dst, const SearchState
     for (int i = threadIdx.x; i < (int)(sizeof(SearchState) / 16); i += blockDim.x) d4[i] = __ldcg(s4 + i);
 }
 
+// The emit of one block by one thread: the chain `mask` (slot bits) becomes
+// the codebook (levels in slot order, padded with the largest), k, D_r (the
+// chain's interval distortions added slot by slot, in order) and H_r =
+// rate / d.  Table addresses depend on the mask alone, so every load issues
+// at once.  Returns D_r.
+__device__ __forceinline__ float emit_block(const float *__restrict__ tables, int64_t b,
+                                            uint32_t mask, float rate, float *__restrict__ codebook,
+                                            uint8_t *__restrict__ kout, float *__restrict__ Dr,
+                                            float *__restrict__ Hr) {
+    const float *tb = tables + b * kRecFloats + kRecTbl;
+    float qv[17];
+#pragma unroll
+    for (int t = 0; t < 17; ++t) qv[t] = tb[kTblC + t];
+    const int d = __float_as_int(tb[kTblHdr + 1]);
+    mask &= 0x1ffffu;
+    if (mask == 0u) mask = 1u;
+    const int k = min(__popc(mask), 16);
+    float dv = 0.f, top = qv[0];
+    int prev = 0;
+#pragma unroll
+    for (int t = 0; t < 17; ++t) {
+        const bool in = (mask >> t) & 1u;
+        const bool link = in && t > 0;
+        const float dd = tb[kTblD + (link ? dp_off(prev) + t - prev - 1 : 0)];
+        if (link) dv += dd;
+        const int pos = __popc(mask & ((1u << t) - 1u));
+        if (in && pos < 16) codebook[b * 16 + pos] = qv[t];
+        if (in) {
+            top = qv[t];
+            prev = t;
+        }
+    }
+    for (int t = k; t < 16; ++t) codebook[b * 16 + t] = top;
+    kout[b] = (uint8_t)k;
+    Dr[b] = dv;
+    Hr[b] = rate / (float)d;
+    return dv;
+}
+
 // Work the fused path's queue (positions below `avail`) for one warp until
 // the release generation reaches `target`: the warp's share is queue
 // positions qj, qj + total_warps, ..., each block in 8 parts of 4 rows (qpart
@@ -730,11 +769,11 @@ __device__ __noinline__ void finish_blocks(const Ctrl *ctrl, int64_t nb, int xb_
 // once every CTA has taken its ticket, adds the sums to the total at xb and
 // advances the search; the next round starts when it publishes the new state.
 //
-// Emit (after the last round), one warp per block, lane t = slot t: the
-// chain at the final lambda becomes the codebook (levels in slot order), k,
-// D_r (sum of the chain's interval distortions, reduced in a fixed tree) and
-// H_r.  Sum D_r: per CTA in warp and block order, then the last CTA adds the
-// CTA partials in a fixed pattern and a fixed shuffle tree.
+// Emit (after the last round), a thread per block: the chain at the final
+// lambda becomes the codebook (levels in slot order), k, D_r (the chain's
+// interval distortions added slot by slot) and H_r; each warp sums 32
+// consecutive blocks' D_r in a fixed shuffle tree, and the last CTA adds the
+// chunk sums in a fixed pattern.
 template <bool GENERAL, bool QUANT>
 __global__ void __launch_bounds__(RoundCfg<GENERAL>::kWarps * 32, 1)
 search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restrict__ ctrl,
@@ -1186,46 +1225,15 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
             const int64_t b = g * 32 + lane;
             float dv = 0.f;
             if (b < nb) {
-                const float *tb = tables + b * kRecFloats + kRecTbl;
-                // every load that does not depend on the chosen chain, at once
                 const int32_t ev = __ldcg(&evr[b]);
                 const int xp = xb_probe >= 0 ? xb_probe : 0;
                 const uint32_t m_last = __ldcg(&masks[b * 32 + xp]);
                 const float r_last = __ldcg(&rates[b * 32 + xp]);
                 const uint32_t m_hi = __ldcg(&mask_hi[b]);
                 const float r_hi = __ldcg(&rate_hi[b]);
-                float qv[17];
-#pragma unroll
-                for (int t = 0; t < 17; ++t) qv[t] = tb[kTblC + t];
-                const int d = __float_as_int(tb[kTblHdr + 1]);
                 const bool from_last = xb_probe >= 0 && ev == last_round;
-                uint32_t mask = from_last ? m_last : m_hi;
-                const float rate = from_last ? r_last : r_hi;
-                mask &= 0x1ffffu;
-                if (mask == 0u) mask = 1u;
-                const int k = min(__popc(mask), 16);
-                // the chain's levels in slot order, and the sum of its interval
-                // distortions (slot by slot, in order); table addresses come from
-                // the mask alone, so the loads issue together
-                float top = qv[0];
-                int prev = 0;
-#pragma unroll
-                for (int t = 0; t < 17; ++t) {
-                    const bool in = (mask >> t) & 1u;
-                    const bool link = in && t > 0;
-                    const float dd = tb[kTblD + (link ? dp_off(prev) + t - prev - 1 : 0)];
-                    if (link) dv += dd;
-                    const int pos = __popc(mask & ((1u << t) - 1u));
-                    if (in && pos < 16) codebook[b * 16 + pos] = qv[t];
-                    if (in) {
-                        top = qv[t];
-                        prev = t;
-                    }
-                }
-                for (int t = k; t < 16; ++t) codebook[b * 16 + t] = top;
-                kout[b] = (uint8_t)k;
-                Dr[b] = dv;
-                Hr[b] = rate / (float)d;
+                dv = emit_block(tables, b, from_last ? m_last : m_hi, from_last ? r_last : r_hi,
+                                codebook, kout, Dr, Hr);
             }
             double t = (double)dv;          // lanes past the last block add 0
 #pragma unroll
@@ -1234,9 +1242,9 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
         }
     }
     // ---- totals, by the last CTA to finish: D = the chunk sums (32
-    // consecutive blocks each, a fixed shuffle tree) added in index order in a
-    // fixed pattern (contiguous runs of four interleaved accumulators, then a
-    // fixed tree)
+    // consecutive blocks each, a fixed shuffle tree) added in a fixed pattern
+    // (thread t sums chunks t, t + blockDim.x, .. in order; then the threads'
+    // sums in a fixed tree)
     __syncthreads();
     if (threadIdx.x == 0) {
         const unsigned t = atom_add_acq_rel_u32(&ctrl->ticket_emit, 1u);   // orders this CTA's D_r
@@ -1270,21 +1278,11 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
     }
     __shared__ double sPart[W * 32];
     {
-        const int64_t chunk = (nch + W * 32 - 1) / (W * 32);
-        const int64_t b0 = (int64_t)threadIdx.x * chunk;
-        const int64_t b1 = b0 + chunk < nch ? b0 + chunk : nch;
-        // chunk sum b0 + 4m + j goes to accumulator j, in order of m; the
-        // loads of 32 of them are issued before their adds
-        double acc[4] = {0.0, 0.0, 0.0, 0.0};
-        for (int64_t i = b0; i < b1; i += 32) {
-            double v[32];
-#pragma unroll
-            for (int u = 0; u < 32; ++u) v[u] = i + u < b1 ? __ldcg(&epartial[i + u]) : 0.0;
-#pragma unroll
-            for (int u = 0; u < 32; ++u)
-                if (i + u < b1) acc[u & 3] += v[u];
-        }
-        sPart[threadIdx.x] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        // thread t adds the chunk sums t, t + blockDim.x, .. in order
+        double a = 0.0;
+#pragma unroll 4
+        for (int64_t i = threadIdx.x; i < nch; i += blockDim.x) a += __ldcg(&epartial[i]);
+        sPart[threadIdx.x] = a;
     }
     __syncthreads();
     if (threadIdx.x >= 32) return;
