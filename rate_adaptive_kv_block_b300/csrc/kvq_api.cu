@@ -43,6 +43,7 @@ size_t entropy_run_slot(const kvq_layout &L, int nseg);
 int entropy_run_max_blocks();
 int allocate_init();
 int weights_init();
+int entropy_init();
 int allocate_report(const void *workspace, kvq_report *r);
 void *static_workspace_address(int dev);
 int launch_rate_sums(const void *stats, const kvq_layout &L, int s, const double *lambdas,
@@ -81,6 +82,7 @@ static int init_once() {
     if (st == KVQ_OK) st = quantize_init();
     if (st == KVQ_OK) st = attention_init();
     if (st == KVQ_OK) st = weights_init();
+    if (st == KVQ_OK) st = entropy_init();
     if (st != KVQ_OK) {
         (void)cudaGetLastError();
         return st;
@@ -368,6 +370,7 @@ int kvq_entropy_encode_runs(const uint8_t *codes, kvq_layout L, int nseg, uint8_
     if (!runs_ok(L, nseg)) return KVQ_ERR_INVALID_ARG;
     if (num_blocks(L) > 0 && (!codes || !out || !nbytes || !aligned16(codes) || !aligned16(out)))
         return KVQ_ERR_INVALID_ARG;
+    if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
     return launch_entropy_encode_runs(codes, L, nseg, out, nbytes,
                                       static_cast<cudaStream_t>(stream));
 }
@@ -377,6 +380,7 @@ int kvq_entropy_decode_runs(const uint8_t *in, kvq_layout L, int nseg, uint8_t *
     if (!runs_ok(L, nseg) || !status) return KVQ_ERR_INVALID_ARG;
     if (num_blocks(L) > 0 && (!in || !codes || !aligned16(in) || !aligned16(codes)))
         return KVQ_ERR_INVALID_ARG;
+    if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
     return launch_entropy_decode_runs(in, L, nseg, codes, status,
                                       static_cast<cudaStream_t>(stream));
 }

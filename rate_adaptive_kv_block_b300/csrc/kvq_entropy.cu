@@ -264,40 +264,61 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
 //   [32 m, 32 m + 64)  32 x u16: bytes of each stream
 //   then the streams in lane order, each its final state (4 bytes) and its
 //   renormalisation bytes in the order the decoder reads them.
-// One warp per run.  The encoder makes two passes over the run: the first
-// only counts each stream's bytes, the second writes them downwards from
-// the stream's end (known from the first), so no worst-case scratch is held.
+// One warp per run and per CTA, so the runs spread over every SM.  The
+// encoder first stages the run's codes and models in shared memory, then
+// makes two passes over the run: the first only counts each stream's bytes,
+// the second writes them downwards from the stream's end (known from the
+// first), so no worst-case scratch is held.  The decoder stages the run's
+// slot (as far as its stream lengths reach) and assembles each block's packed
+// codes in shared memory before one coalesced store.  Both serial per-lane
+// loops then touch shared memory only.
 constexpr int kRunMaxBlocks = 32;
-constexpr int kRunWarps = 4;
 
 __host__ __device__ constexpr uint64_t run_slot_bytes(int d, int nseg) {
     // at most 4 bits a symbol (exact counts), the counts, the lengths, and per
     // stream its state and one byte of renormalisation slack
     return ((uint64_t)nseg * (uint64_t)(d / 2 + 32) + 64u + 32u * 6u + 15u) & ~(uint64_t)15u;
 }
+// dynamic shared memory of the two kernels
+__host__ __device__ constexpr size_t run_enc_smem(int d, int nseg) {
+    return (size_t)nseg * (16 * sizeof(uint4) + (size_t)(d / 2));
+}
+__host__ __device__ constexpr size_t run_dec_smem(int d, int nseg) {
+    return 144 + (size_t)(d / 2) + (size_t)run_slot_bytes(d, nseg);
+}
+constexpr size_t kRunSmemMax = run_enc_smem(4096, kRunMaxBlocks) > run_dec_smem(4096, kRunMaxBlocks)
+                                   ? run_enc_smem(4096, kRunMaxBlocks)
+                                   : run_dec_smem(4096, kRunMaxBlocks);
 
-__device__ __forceinline__ uint32_t nibble_at(const uint8_t *__restrict__ cb, int e) {
+__device__ __forceinline__ uint32_t nibble_at(const uint8_t *cb, int e) {
     return (cb[e >> 1] >> ((e & 1) * 4)) & 15u;
 }
 
-__global__ void __launch_bounds__(kRunWarps * 32)
+__global__ void __launch_bounds__(32)
 entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d, int nseg,
                            uint8_t *__restrict__ out, uint32_t *__restrict__ nbytes) {
-    __shared__ uint4 smodel[kRunWarps][kRunMaxBlocks][16];   // count, cumulative, reciprocal
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t nruns = (nb + nseg - 1) / nseg;
-    const int64_t rn = (int64_t)blockIdx.x * kRunWarps + w;
-    if (rn >= nruns) return;
+    extern __shared__ __align__(16) uint8_t rsm[];
+    uint4 *smodel = reinterpret_cast<uint4 *>(rsm);            // [block][symbol]: count,
+                                                               // cumulative, reciprocal
+    uint8_t *scodes = rsm + (size_t)nseg * 16 * sizeof(uint4);   // the run's codes
+    const int lane = threadIdx.x;
+    const int64_t rn = blockIdx.x;
     const int64_t b0 = rn * nseg;
     const int m = (int)min((int64_t)nseg, nb - b0);
     const int n = d / 32, lg = ilog2(d);
     const int half = d / 2;
     uint8_t *slot = out + rn * (int64_t)run_slot_bytes(d, nseg);
-    const uint8_t *src = codes + b0 * half;
+    {
+        // 16-byte copies: codes is 16-byte aligned and half a multiple of 16
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(codes + b0 * half);
+        uint4 *d4 = reinterpret_cast<uint4 *>(scodes);
+        for (int i = lane; i < m * half / 16; i += 32) d4[i] = __ldg(s4 + i);
+    }
+    __syncwarp();
     // the blocks' models: counts (lane-private, then warp sums), cumulative
     // counts, reciprocals; the counts also go to the slot
     for (int bi = 0; bi < m; ++bi) {
-        const uint8_t *cb = src + (int64_t)bi * half;
+        const uint8_t *cb = scodes + bi * half;
         uint32_t cnt[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) cnt[t] = 0;
@@ -318,27 +339,34 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
                 acc += cnt[t];
             }
             const Recip r = recip_of(f > 0 ? f : 1u);
-            smodel[w][bi][lane] = make_uint4(f, bc, r.m, r.sh);
+            smodel[bi * 16 + lane] = make_uint4(f, bc, r.m, r.sh);
             slot[32 * bi + 2 * lane] = (uint8_t)f;
             slot[32 * bi + 2 * lane + 1] = (uint8_t)(f >> 8);
         }
     }
     __syncwarp();
     const uint32_t xmax0 = (kRansL >> lg) << 8;
-    // pass 1: the length of this lane's stream
+    // pass 1: the length of this lane's stream.  The symbols are taken last
+    // first, run position k = bi * n + j from m n - 1 down to 0; the next
+    // symbol's model entry does not depend on the state, so it is loaded one
+    // step ahead (the state's chain then holds only the arithmetic)
+    const int nk = m * n;
+    auto model_at = [&](int k) {
+        const int bi = k >> (lg - 5), j = k & (n - 1);     // n = d / 32, a power of two
+        return smodel[bi * 16 + nibble_at(scodes + bi * half, lane + 32 * j)];
+    };
     uint32_t x = kRansL, len = 4;
-    for (int bi = m - 1; bi >= 0; --bi) {
-        const uint8_t *cb = src + (int64_t)bi * half;
-        for (int j = n - 1; j >= 0; --j) {
-            const uint4 md = smodel[w][bi][nibble_at(cb, lane + 32 * j)];
-            const uint32_t xmax = xmax0 * md.x;
-            while (x >= xmax) {
-                ++len;
-                x >>= 8;
-            }
-            const uint32_t qd = div_by(x, Recip{md.z, md.w});
-            x = (qd << lg) + (x - qd * md.x) + md.y;
+    uint4 nxt = model_at(nk - 1);
+    for (int k = nk - 1; k >= 0; --k) {
+        const uint4 md = nxt;
+        if (k > 0) nxt = model_at(k - 1);
+        const uint32_t xmax = xmax0 * md.x;
+        while (x >= xmax) {
+            ++len;
+            x >>= 8;
         }
+        const uint32_t qd = div_by(x, Recip{md.z, md.w});
+        x = (qd << lg) + (x - qd * md.x) + md.y;
     }
     uint32_t off = len;
 #pragma unroll
@@ -356,18 +384,17 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     uint8_t *st = slot + hdr + off;
     uint32_t pos = len;
     x = kRansL;
-    for (int bi = m - 1; bi >= 0; --bi) {
-        const uint8_t *cb = src + (int64_t)bi * half;
-        for (int j = n - 1; j >= 0; --j) {
-            const uint4 md = smodel[w][bi][nibble_at(cb, lane + 32 * j)];
-            const uint32_t xmax = xmax0 * md.x;
-            while (x >= xmax) {
-                st[--pos] = (uint8_t)(x & 255u);
-                x >>= 8;
-            }
-            const uint32_t qd = div_by(x, Recip{md.z, md.w});
-            x = (qd << lg) + (x - qd * md.x) + md.y;
+    nxt = model_at(nk - 1);
+    for (int k = nk - 1; k >= 0; --k) {
+        const uint4 md = nxt;
+        if (k > 0) nxt = model_at(k - 1);
+        const uint32_t xmax = xmax0 * md.x;
+        while (x >= xmax) {
+            st[--pos] = (uint8_t)(x & 255u);
+            x >>= 8;
         }
+        const uint32_t qd = div_by(x, Recip{md.z, md.w});
+        x = (qd << lg) + (x - qd * md.x) + md.y;
     }
     st[0] = (uint8_t)x;          // pos == 4 here: the state opens the stream
     st[1] = (uint8_t)(x >> 8);
@@ -375,18 +402,19 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     st[3] = (uint8_t)(x >> 24);
 }
 
-__global__ void __launch_bounds__(kRunWarps * 32)
+__global__ void __launch_bounds__(32)
 entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, int nseg,
                            uint8_t *__restrict__ codes, int32_t *__restrict__ status) {
-    __shared__ uint32_t scum[kRunWarps][17], scnt[kRunWarps][16];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t nruns = (nb + nseg - 1) / nseg;
-    const int64_t rn = (int64_t)blockIdx.x * kRunWarps + w;
-    if (rn >= nruns) return;
+    extern __shared__ __align__(16) uint8_t rsm[];
+    uint32_t *scum = reinterpret_cast<uint32_t *>(rsm);      // [16]: cumulative | count << 16
+    uint8_t *sout = rsm + 144;                               // one block's packed codes
+    const int lane = threadIdx.x;
+    const int64_t rn = blockIdx.x;
     const int64_t b0 = rn * nseg;
     const int m = (int)min((int64_t)nseg, nb - b0);
     const int n = d / 32, lg = ilog2(d);
     const int half = d / 2;
+    uint8_t *sslot = sout + half;                            // the run's slot
     const uint64_t cap = run_slot_bytes(d, nseg);
     const uint8_t *slot = in + rn * (int64_t)cap;
     const uint32_t hdr = 32u * (uint32_t)m + 64u;
@@ -401,20 +429,30 @@ entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, in
     off -= len;
     // a slot that does not hold m blocks of d symbols: status, codes 0
     bool bad = __any_sync(0xffffffffu, (uint64_t)hdr + total > cap || len < 4);
+    {
+        // stage what the streams reach (16-byte copies; cap and the slots'
+        // offsets are multiples of 16), never more than the slot
+        const uint64_t used = bad ? (uint64_t)hdr : (uint64_t)hdr + total;
+        const uint32_t nq = (uint32_t)((used + 15u) / 16u);
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(slot);
+        uint4 *d4 = reinterpret_cast<uint4 *>(sslot);
+        for (uint32_t i = lane; i < nq; i += 32) d4[i] = __ldg(s4 + i);
+    }
+    __syncwarp();
     uint32_t p = hdr + off;
     const uint32_t end = p + len;
     uint32_t x = 0;
     if (!bad) {
-        x = (uint32_t)slot[p] | ((uint32_t)slot[p + 1] << 8) | ((uint32_t)slot[p + 2] << 16) |
-            ((uint32_t)slot[p + 3] << 24);
+        x = (uint32_t)sslot[p] | ((uint32_t)sslot[p + 1] << 8) | ((uint32_t)sslot[p + 2] << 16) |
+            ((uint32_t)sslot[p + 3] << 24);
         p += 4;
     }
     bool overrun = false;
     uint8_t *dst = codes + b0 * half;
     for (int bi = 0; bi < m; ++bi) {
         // this block's model: counts from the slot, cumulative counts by a scan
-        const uint32_t mycnt = lane < 16 ? ((uint32_t)slot[32 * bi + 2 * lane] |
-                                            ((uint32_t)slot[32 * bi + 2 * lane + 1] << 8))
+        const uint32_t mycnt = lane < 16 ? ((uint32_t)sslot[32 * bi + 2 * lane] |
+                                            ((uint32_t)sslot[32 * bi + 2 * lane + 1] << 8))
                                          : 0u;
         uint32_t incl = mycnt;
 #pragma unroll
@@ -422,35 +460,55 @@ entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, in
             const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
-        __syncwarp();                              // the previous block's model is done with
-        if (lane < 16) {
-            scnt[w][lane] = mycnt;
-            scum[w][lane] = incl - mycnt;
-        }
-        if (lane == 16) scum[w][16] = incl;
+        __syncwarp();                              // the previous block is done with
+        if (lane < 16) scum[lane] = (incl - mycnt) | (mycnt << 16);   // cumulative | count
         __syncwarp();
-        const bool badm = __any_sync(0xffffffffu, scum[w][16] != (uint32_t)d);
+        const uint32_t tot = __shfl_sync(0xffffffffu, incl, 15);
+        const bool badm = __any_sync(0xffffffffu, tot != (uint32_t)d);
         bad = bad || badm;
-        const uint32_t *cum = scum[w];
-        uint8_t *db = dst + (int64_t)bi * half;
+        // the cumulative counts b_1 .. b_15 in every lane's registers: the
+        // symbol of slot s is the number of them at or below s (the same c as
+        // the search over b: symbols with count 0 have b_c = b_{c+1})
+        uint32_t bcum[15];
+#pragma unroll
+        for (int t = 0; t < 15; ++t) bcum[t] = __shfl_sync(0xffffffffu, incl, t);
         for (int j = 0; j < n; ++j) {
             uint32_t c = 0;
             if (!bad && !overrun) {
                 const uint32_t s = x & ((1u << lg) - 1u);
-                c = (uint32_t)rans_symbol(cum, s);
-                x = scnt[w][c] * (x >> lg) + s - cum[c];
+#pragma unroll
+                for (int t = 0; t < 15; ++t) c += bcum[t] <= s ? 1u : 0u;
+                const uint32_t e = scum[c];
+                x = (e >> 16) * (x >> lg) + s - (e & 0xffffu);
                 while (x < kRansL) {
                     if (p >= end) { overrun = true; break; }   // never reads past its stream
-                    x = (x << 8) | slot[p++];
+                    x = (x << 8) | sslot[p++];
                 }
             }
             const uint32_t hi = __shfl_xor_sync(0xffffffffu, c, 1);
             const int e = lane + 32 * j;
-            if ((lane & 1) == 0) db[e >> 1] = (uint8_t)(c | (hi << 4));
+            if ((lane & 1) == 0) sout[e >> 1] = (uint8_t)(c | (hi << 4));
+        }
+        __syncwarp();
+        {
+            uint4 *o4 = reinterpret_cast<uint4 *>(dst + (int64_t)bi * half);
+            const uint4 *s4 = reinterpret_cast<const uint4 *>(sout);
+            for (int i = lane; i < half / 16; i += 32) o4[i] = s4[i];
         }
     }
     overrun = overrun || (!bad && p != end);
     if (__any_sync(0xffffffffu, bad || overrun) && lane == 0) atomicMax(status, (int32_t)KVQ_ERR_CORRUPT);
+}
+
+int entropy_init() {
+    if (cudaFuncSetAttribute((const void *)entropy_encode_runs_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRunSmemMax) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute((const void *)entropy_decode_runs_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRunSmemMax) !=
+            cudaSuccess)
+        return KVQ_ERR_CUDA;
+    return KVQ_OK;
 }
 
 int launch_entropy_encode_runs(const uint8_t *codes, const kvq_layout &L, int nseg, uint8_t *out,
@@ -459,9 +517,8 @@ int launch_entropy_encode_runs(const uint8_t *codes, const kvq_layout &L, int ns
     if (nb == 0) return KVQ_OK;
     const int d = 32 * L.group;
     const int64_t nruns = (nb + nseg - 1) / nseg;
-    const int64_t ctas = (nruns + kRunWarps - 1) / kRunWarps;
-    entropy_encode_runs_kernel<<<(unsigned)ctas, kRunWarps * 32, 0, st>>>(codes, nb, d, nseg, out,
-                                                                          nbytes);
+    entropy_encode_runs_kernel<<<(unsigned)nruns, 32, run_enc_smem(d, nseg), st>>>(codes, nb, d,
+                                                                                 nseg, out, nbytes);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
@@ -472,9 +529,8 @@ int launch_entropy_decode_runs(const uint8_t *in, const kvq_layout &L, int nseg,
     if (nb == 0) return KVQ_OK;
     const int d = 32 * L.group;
     const int64_t nruns = (nb + nseg - 1) / nseg;
-    const int64_t ctas = (nruns + kRunWarps - 1) / kRunWarps;
-    entropy_decode_runs_kernel<<<(unsigned)ctas, kRunWarps * 32, 0, st>>>(in, nb, d, nseg, codes,
-                                                                          status);
+    entropy_decode_runs_kernel<<<(unsigned)nruns, 32, run_dec_smem(d, nseg), st>>>(in, nb, d, nseg,
+                                                                                 codes, status);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
