@@ -165,6 +165,15 @@ def cpu_baseline(w, x_np, budget_per_entry, nblocks=CPU_SAMPLE_BLOCKS, seed=0):
         % (len(sel), per, per, w.nblocks, sl.nbytes))
 
 
+def step_config(world):
+    """The bench step's workload and launch, the same object on both arms."""
+    return {"workload": WORKLOAD_DESC,
+            "l2": "flushed before each step (256 MB write then 256 MB read, outside the timed "
+                  "interval)",
+            "launch": "whole step as one CUDA graph replay",
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def run_reference(args, rank, world):
     """Reference arm: the CPU oracle on bounded samples (rank 0 only)."""
     if rank != 0:
@@ -187,7 +196,7 @@ def run_reference(args, rank, world):
         "warmup": args.warmup, "ms_per_step": 1e3 * sum(secs) / len(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": WORKLOAD_DESC, "sample": desc},
+        "config": step_config(world),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": thr, "kind": "oracle",
                          "sample": desc, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -1093,9 +1102,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "l2": "flushed before each step (256 MB write then 256 MB read, outside the timed interval)",
-                       "launch": "whole step as one CUDA graph replay",
-                       "parallelism": "replicas" if world > 1 else "single"},
+            "config": step_config(world),
             "tokens_per_s": world * args.steps * w.T / (tot_ms * 1e-3),
             "lambda": float(buf.lam.item()), "rate_bits_per_entry": float(buf.totals[0].item()) / w.entries,
             "kernels": kern,
