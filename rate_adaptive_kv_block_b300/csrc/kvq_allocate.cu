@@ -426,6 +426,28 @@ __device__ void dp_path_b(const float *__restrict__ tb, float lam, int s,
     mask = sM[p * 32 + lane];
 }
 
+// A block's DP tables (kTblStride floats) into the warp's shared memory:
+// every lane's 16-byte loads issued before any store, so the copy costs one
+// L2 round trip (L2 only: the stats kernel wrote them).
+__device__ __forceinline__ void load_tables(float *__restrict__ sTbl, const float *__restrict__ tables,
+                                            int64_t b, int lane) {
+    constexpr int kN4 = kTblStride / 4;
+    constexpr int kPer = (kN4 + 31) / 32;
+    const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
+    float4 *dst = reinterpret_cast<float4 *>(sTbl);
+    float4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int i = lane + 32 * k;
+        if (i < kN4) v[k] = __ldcg(src + i);
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int i = lane + 32 * k;
+        if (i < kN4) dst[i] = v[k];
+    }
+}
+
 // ------------------------------------------------- fused emit + quantize
 // The allocate-and-quantize path quantizes each block as soon as its chain is
 // final -- a block whose rate is equal at both ends of the window is constant
@@ -909,12 +931,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
             if (!ready) {
                 // phase A ran on the published window: load each warp's first
                 // table while the control finishes the round's probes
-                if (w < (int)sN) {
-                    const float4 *src = reinterpret_cast<const float4 *>(
-                        tables + (int64_t)sList[w] * kRecFloats + kRecTbl);
-                    float4 *dst = reinterpret_cast<float4 *>(sTbl);
-                    for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
-                }
+                if (w < (int)sN) load_tables(sTbl, tables, (int64_t)sList[w], lane);
                 if constexpr (QUANT)
                     run_queue(ctrl, 2u * (uint32_t)iter, (uint64_t)sC.fin_avail, fin, mask_hi, rate_hi,
                               tables, qa, codebook, kout, Dr, Hr, scratch, lane, total_warps, qj,
@@ -935,11 +952,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
             for (uint32_t q = w; q < n; q += W) {
                 const int64_t b = sList[q];
                 const float rb = sRb[q];
-                if (!(prefetched && q == (uint32_t)w)) {
-                    const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
-                    float4 *dst = reinterpret_cast<float4 *>(sTbl);
-                    for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
-                }
+                if (!(prefetched && q == (uint32_t)w)) load_tables(sTbl, tables, b, lane);
                 __syncwarp();
                 const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
                 float rate;
@@ -1340,11 +1353,7 @@ fixed_rate_kernel(const float *__restrict__ tables, int64_t nb, int s, double bi
     __shared__ double sProbe[W][32];
     const int64_t b = (int64_t)blockIdx.x * W + w;
     if (b >= nb) return;                      // warp-level work only below
-    {
-        const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
-        float4 *dst = reinterpret_cast<float4 *>(sTbl);
-        for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
-    }
+    load_tables(sTbl, tables, b, lane);
     __syncwarp();
     const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
     const int d = __float_as_int(sTbl[kTblHdr + 1]);
@@ -1478,9 +1487,7 @@ rate_sums_kernel(const float *__restrict__ tables, int64_t nb, int s, ProbeSet p
     const float lam = lane < probes.n ? (float)probes.lambda[lane] : 0.f;
     long long acc = 0;
     for (int64_t b = (int64_t)blockIdx.x * W + w; b < nb; b += (int64_t)gridDim.x * W) {
-        const float4 *src = reinterpret_cast<const float4 *>(tables + b * kRecFloats + kRecTbl);
-        float4 *dst = reinterpret_cast<float4 *>(sTbl);
-        for (int i = lane; i < kTblStride / 4; i += 32) dst[i] = src[i];
+        load_tables(sTbl, tables, b, lane);
         __syncwarp();
         const int mp = min(max(__float_as_int(sTbl[kTblHdr]), 1), kCand);
         float rate = 0.f;
