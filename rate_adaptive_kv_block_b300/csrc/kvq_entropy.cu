@@ -71,6 +71,26 @@ __device__ __forceinline__ uint32_t div_by(uint32_t x, Recip r) {
     return (uint32_t)(((uint64_t)x * r.m) >> r.sh);
 }
 
+// n16 16-byte words from global to shared memory by one warp, in batches of
+// eight per lane: each batch's loads are in flight together (a sequential
+// load-store loop would wait one memory round trip per iteration).
+__device__ __forceinline__ void stage16(uint4 *__restrict__ dst, const uint4 *__restrict__ src,
+                                        int n16, int lane) {
+    for (int base = 0; base < n16; base += 8 * 32) {
+        uint4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = base + lane + 32 * k;
+            if (i < n16) v[k] = __ldg(src + i);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = base + lane + 32 * k;
+            if (i < n16) dst[i] = v[k];
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kEntWarps * 32)
 entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
                       uint8_t *__restrict__ out, uint32_t *__restrict__ nbytes) {
@@ -83,8 +103,8 @@ entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     const int n = d / 32, lg = ilog2(d);
     // the block's codes in shared memory (coalesced 16-byte loads)
     uint8_t *cb = sslot[w];
-    for (int i = lane; i < d / 32; i += 32)
-        reinterpret_cast<uint4 *>(cb)[i] = reinterpret_cast<const uint4 *>(codes + b * (d / 2))[i];
+    stage16(reinterpret_cast<uint4 *>(cb), reinterpret_cast<const uint4 *>(codes + b * (d / 2)),
+            d / 32, lane);
     __syncwarp();
     // the block's counts (lane-private, then a warp sum)
     uint32_t cnt[16];
@@ -127,8 +147,10 @@ entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     uint8_t *buf = scratch[w][lane];
     int pos = kEntLaneCap;
     uint32_t x = kRansL;
+    uint4 nxt = smodel[w][mysym[n - 1]];      // the next symbol's model, one step ahead
     for (int j = n - 1; j >= 0; --j) {
-        const uint4 md = smodel[w][mysym[j]];
+        const uint4 md = nxt;
+        if (j > 0) nxt = smodel[w][mysym[j - 1]];
         const uint32_t f = md.x, bc = md.y;
         const Recip r{md.z, md.w};
         const uint32_t xmax = ((kRansL >> lg) << 8) * f;
@@ -189,9 +211,8 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
     const uint32_t cap = entropy_slot_bytes(d);
     // the whole slot in shared memory (16-byte loads; the capacity is a
     // multiple of 16)
-    for (uint32_t i = lane; i < cap / 16; i += 32)
-        reinterpret_cast<uint4 *>(sslot[w])[i] =
-            reinterpret_cast<const uint4 *>(in + b * (int64_t)cap)[i];
+    stage16(reinterpret_cast<uint4 *>(sslot[w]), reinterpret_cast<const uint4 *>(in + b * (int64_t)cap),
+            (int)(cap / 16), lane);
     __syncwarp();
     const uint8_t *slot = sslot[w];
     // counts and cumulative counts in shared memory (lane t < 16 reads
@@ -308,12 +329,9 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     const int n = d / 32, lg = ilog2(d);
     const int half = d / 2;
     uint8_t *slot = out + rn * (int64_t)run_slot_bytes(d, nseg);
-    {
-        // 16-byte copies: codes is 16-byte aligned and half a multiple of 16
-        const uint4 *s4 = reinterpret_cast<const uint4 *>(codes + b0 * half);
-        uint4 *d4 = reinterpret_cast<uint4 *>(scodes);
-        for (int i = lane; i < m * half / 16; i += 32) d4[i] = __ldg(s4 + i);
-    }
+    // 16-byte copies: codes is 16-byte aligned and half a multiple of 16
+    stage16(reinterpret_cast<uint4 *>(scodes), reinterpret_cast<const uint4 *>(codes + b0 * half),
+            m * half / 16, lane);
     __syncwarp();
     // the blocks' models: counts (lane-private, then warp sums), cumulative
     // counts, reciprocals; the counts also go to the slot
@@ -433,10 +451,8 @@ entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, in
         // stage what the streams reach (16-byte copies; cap and the slots'
         // offsets are multiples of 16), never more than the slot
         const uint64_t used = bad ? (uint64_t)hdr : (uint64_t)hdr + total;
-        const uint32_t nq = (uint32_t)((used + 15u) / 16u);
-        const uint4 *s4 = reinterpret_cast<const uint4 *>(slot);
-        uint4 *d4 = reinterpret_cast<uint4 *>(sslot);
-        for (uint32_t i = lane; i < nq; i += 32) d4[i] = __ldg(s4 + i);
+        const int nq = (int)((used + 15u) / 16u);
+        stage16(reinterpret_cast<uint4 *>(sslot), reinterpret_cast<const uint4 *>(slot), nq, lane);
     }
     __syncwarp();
     uint32_t p = hdr + off;
