@@ -781,6 +781,169 @@ __device__ __noinline__ void finish_blocks(const Ctrl *ctrl, int64_t nb, int xb_
     }
 }
 
+// The search kernel's copy of the control block in shared memory; at file
+// scope so that the out-of-line control addresses it as shared memory.
+__shared__ __align__(16) Ctrl s_ctrl;
+
+// One round's control, run by one warp of CTA 0 once every CTA's ticket is
+// in: fold the round's per-probe rate sums into the search state S, publish
+// the window (first release), then walk and publish the next probes (second
+// release).  Out of line so that one copy of its code serves two calls:
+// `dry` runs the same instructions with a decreasing stand-in for the sums
+// and writes nothing to global memory (only the staged state, which CTA 0
+// stages again before its real control).  CTA 0 makes that call while the
+// other CTAs evaluate each round, so the control's code is in the SM's
+// instruction cache when the real control runs.  Fetched cold (from DRAM in
+// the launch's first rounds, from L2 once a DP wave has evicted it) the
+// control takes about twice as long.
+__device__ __noinline__ void round_control(Ctrl *ctrl, bool walk, int iter, int round, bool dry) {
+    const Ctrl &sC = s_ctrl;
+    SearchState &S = s_ctrl.s;
+    const int L = threadIdx.x & 31;
+    __shared__ long long Rfx[32];
+    __shared__ double sProbe[kSearchProbes];
+    long long myR;
+    if (!dry) {
+        myR = (walk ? sC.Rxb_fx : 0) + (long long)sC.acc[L];
+        ctrl->acc[L] = 0ull;
+    } else {
+        // R(v) = B vm / v (4 B at v = 0), vm the middle probe; the pilot's
+        // sums cover its sample only
+        const double v = search_probe(S, L), vm = search_probe(S, kSearchProbes / 2);
+        const double r = (v > 0.0 && vm > 0.0) ? fmin(sC.budget * (vm / v), 4.0 * sC.budget)
+                                                : 4.0 * sC.budget;
+        const double part = S.phase == kSearchPilot
+                                ? (double)(S.pilot_blocks > 0 ? S.pilot_blocks : 1) / (double)sC.nb
+                                : 1.0;
+        myR = llrint(r * part * kRateScale);
+    }
+    Rfx[L] = myR;
+    const long long Bfx = sC.budget_fx;
+    if (L == 0) S.hi0 = __longlong_as_double((long long)sC.hi0_bits);
+    __syncwarp();
+    SearchState st;              // every lane keeps the same copy
+    bool walk_on = false;        // a walk follows the first publication
+    if (sC.fixed) {
+        if (L == 0) {
+            S.xb_probe = 0;
+            S.R_xb = myR;
+            S.lambda = sC.lambda_fixed;
+            S.phase = kSearchDone;
+            S.rounds += 1;
+        }
+    } else if (S.phase == kSearchPilot) {
+        // one lane per probe: the sample's rates scaled to all blocks, the
+        // smallest feasible probe and the largest infeasible one below it
+        // (first lane on ties, as a sequential scan)
+        const double B = sC.budget;
+        const double scale =
+            (double)sC.nb / (double)(S.pilot_blocks > 0 ? S.pilot_blocks : 1) / kRateScale;
+        const double v = search_probe(S, L), r = (double)myR * scale;
+        const bool feas = r <= B;
+        const uint64_t kv = okey(v);
+        uint64_t kb = feas ? kv : ~0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t y = __shfl_xor_sync(0xffffffffu, kb, o);
+            kb = y < kb ? y : kb;
+        }
+        const uint32_t mb = __ballot_sync(0xffffffffu, feas && kv == kb);
+        const int ib = mb ? __ffs(mb) - 1 : -1;
+        const bool cand = !feas && v > -1.0 && (ib < 0 || kv < kb);
+        uint64_t ka = cand ? kv : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t y = __shfl_xor_sync(0xffffffffu, ka, o);
+            ka = y > ka ? y : ka;
+        }
+        const uint32_t ma = __ballot_sync(0xffffffffu, cand && kv == ka);
+        const int ia = ma ? __ffs(ma) - 1 : -1;
+        const double vb = __shfl_sync(0xffffffffu, v, ib >= 0 ? ib : 0);
+        const double Rb = __shfl_sync(0xffffffffu, r, ib >= 0 ? ib : 0);
+        const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
+        const double Ra = __shfl_sync(0xffffffffu, r, ia >= 0 ? ia : 0);
+        search_copy_scalars(st, S);        // every lane computes the same estimate
+        const double est = search_pilot_finish(st, ib, ib >= 0 ? vb : INFINITY, ib >= 0 ? Rb : 0.0,
+                                               ia, ia >= 0 ? va : -1.0, ia >= 0 ? Ra : 0.0, B);
+        __syncwarp();
+        if (st.have_grid && L > kSearchFirstDoublings) S.probe[L] = search_pilot_probe(est, L);
+        __syncwarp();
+        if (L == 0) search_copy_scalars(S, st);
+    } else {
+        // one lane per probe folds the evaluations into the window (exact
+        // min / max of order keys), every lane walks, and lane L generates
+        // the probes along decision path L
+        const bool inr = L < S.nprobe;
+        const double v = search_probe(S, L);
+        const uint64_t kv = okey(v);
+        const bool feas = inr && myR <= Bfx;
+        uint64_t kb = feas ? kv : ~0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t y = __shfl_xor_sync(0xffffffffu, kb, o);
+            kb = y < kb ? y : kb;
+        }
+        const uint32_t mb = __ballot_sync(0xffffffffu, feas && kv == kb);
+        const int ib = mb ? __ffs(mb) - 1 : -1;
+        const double vb = __shfl_sync(0xffffffffu, v, ib >= 0 ? ib : 0);
+        const uint64_t kxb = okey(S.xb);
+        const uint64_t kxbn = (ib >= 0 && kb < kxb) ? kb : kxb;
+        const bool inf = inr && !feas && kv < kxbn;
+        uint64_t ka = inf ? kv : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t y = __shfl_xor_sync(0xffffffffu, ka, o);
+            ka = y > ka ? y : ka;
+        }
+        const uint32_t ma = __ballot_sync(0xffffffffu, inf && kv == ka);
+        const int ia = ma ? __ffs(ma) - 1 : -1;
+        const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
+        search_copy_scalars(st, S);
+        search_window(st, ib >= 0 ? vb : INFINITY, ib, ib >= 0 ? Rfx[ib] : 0, va, ia);
+        walk_on = search_decide(st, Rfx, Bfx);
+        __syncwarp();
+        if (L == 0) {
+            search_copy_scalars(S, st);
+            if (st.infeasible && !dry) ctrl->status = KVQ_ERR_INFEASIBLE;
+        }
+    }
+    // first publication: the window and the next round's kind
+    __syncwarp();
+    if (!dry) {
+        if (L == 0) {
+            if (!sC.fixed && S.xb_probe >= 0) ctrl->Rxb_fx = Rfx[S.xb_probe];
+            ctrl->cnt[round & 1] = 0u;     // consumed; the next round appends here
+            ctrl->ticket = 0u;
+            ctrl->fin_avail = sC.fin_tail;  // every queue append of this round is in
+        }
+        publish_search(ctrl, S, L);
+        __syncwarp();            // the warp's writes, then one release store
+        if (L == 0) st_release_u32(&ctrl->gen, 2u * (uint32_t)iter + 1u);
+    }
+    // second publication: the walk and the next round's probes
+    if (walk_on) {
+        const SearchWindow win = search_window_of(st);   // the walk keeps it
+        const int go = search_walk_w(st, win);
+        __syncwarp();
+        if (go) {
+            sProbe[L] = search_first_unknown(st);
+            __syncwarp();
+            search_path_w(st, win, L, sProbe);
+            __syncwarp();
+            S.probe[L] = sProbe[L];
+        }
+        __syncwarp();
+        if (L == 0) search_copy_scalars(S, st);
+        __syncwarp();
+        if (!dry) publish_search(ctrl, S, L);
+    }
+    __syncwarp();
+    if (L == 0 && !dry) {
+        ctrl->t_ctl[min(round, 15)] = global_ns();
+        st_release_u32(&ctrl->gen, 2u * (uint32_t)iter + 2u);
+    }
+}
+
 // The whole search and the emit in one persistent, cooperative launch.
 //
 // Each round: the grid's warps take the round's blocks (all blocks in the
@@ -815,7 +978,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
     float *sState = smem + W * kTblStride + w * Cfg::kStateFloats;
     long long *sSum = reinterpret_cast<long long *>(smem + W * (kTblStride + Cfg::kStateFloats));
     float *sDiag = reinterpret_cast<float *>(sSum + W * 32) + w * 32;
-    __shared__ __align__(16) Ctrl sC;
+    Ctrl &sC = s_ctrl;
     __shared__ bool is_last, timed_out;
     __shared__ uint32_t sAct, sN;
     __shared__ int32_t sList[W * 32];
@@ -858,16 +1021,21 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
         float lam = ready ? (float)(fixed ? sC.lambda_fixed : search_probe(sC.s, lane)) : 0.f;
         long long my_sum = 0;
         bool done = false;
-        // Items in chunks of one per thread: item it = blockIdx.x + gridDim.x
-        // * (c * blockDim.x + threadIdx.x), so consecutive CTAs take
-        // consecutive items.  Phase A (a thread per item) carries the walk's
-        // per-block state to the new window ends and keeps the blocks whose
-        // rate can still change; phase B (a warp per kept block) runs the DP.
-        for (int64_t c0 = 0; (int64_t)blockIdx.x + (int64_t)gridDim.x * c0 < nitems;
-             c0 += blockDim.x) {
+        // CTA 0 takes no items in the search's rounds: while the other CTAs
+        // evaluate, it runs the control once with a stand-in for the sums
+        // (round_control), so the real control finds its code cached
+        const bool warm = !fixed && gridDim.x > 1;
+        const int64_t cta = warm ? (int64_t)blockIdx.x - 1 : (int64_t)blockIdx.x;
+        const int64_t ncta = warm ? (int64_t)gridDim.x - 1 : (int64_t)gridDim.x;
+        // Items in chunks of one per thread: item it = cta + ncta * (c *
+        // blockDim.x + threadIdx.x), so consecutive CTAs take consecutive
+        // items.  Phase A (a thread per item) carries the walk's per-block
+        // state to the new window ends and keeps the blocks whose rate can
+        // still change; phase B (a warp per kept block) runs the DP.
+        for (int64_t c0 = 0; cta >= 0 && cta + ncta * c0 < nitems; c0 += blockDim.x) {
             if (threadIdx.x == 0) sN = 0u;
             __syncthreads();
-            const int64_t it = (int64_t)blockIdx.x + (int64_t)gridDim.x * (c0 + threadIdx.x);
+            const int64_t it = cta + ncta * (c0 + threadIdx.x);
             bool act = false;
             int32_t bsel = 0;
             if (it < nitems) {
@@ -1004,6 +1172,9 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
             return;
         }
         if (done) break;
+        // (the dry control changes only the staged search state, which CTA 0
+        // reads again before its real control)
+        if (warm && blockIdx.x == 0 && w == 0) round_control(ctrl, false, iter, round, true);
         sSum[w * 32 + lane] = my_sum;
         __syncthreads();
         if (threadIdx.x < 32) {
@@ -1049,140 +1220,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
             if (threadIdx.x == 0) ctrl->t_dp[min(round, 15)] = global_ns();
             stage_ctrl(sC, ctrl);
             __syncthreads();
-            if (threadIdx.x < 32) {
-                const int L = threadIdx.x;
-                SearchState &S = sC.s;
-                __shared__ long long Rfx[32];
-                const long long myR = (walk ? sC.Rxb_fx : 0) + (long long)sC.acc[L];
-                Rfx[L] = myR;
-                ctrl->acc[L] = 0ull;
-                const long long Bfx = sC.budget_fx;
-                if (L == 0) S.hi0 = __longlong_as_double((long long)sC.hi0_bits);
-                __syncwarp();
-                SearchState st;              // every lane keeps the same copy
-                bool walk_on = false;        // a walk follows the first publication
-                if (sC.fixed) {
-                    if (L == 0) {
-                        S.xb_probe = 0;
-                        S.R_xb = myR;
-                        S.lambda = sC.lambda_fixed;
-                        S.phase = kSearchDone;
-                        S.rounds += 1;
-                    }
-                } else if (S.phase == kSearchPilot) {
-                    // one lane per probe: the sample's rates scaled to all blocks, the
-                    // smallest feasible probe and the largest infeasible one below it
-                    // (first lane on ties, as a sequential scan)
-                    const double B = sC.budget;
-                    const double scale =
-                        (double)sC.nb / (double)(S.pilot_blocks > 0 ? S.pilot_blocks : 1) / kRateScale;
-                    const double v = search_probe(S, L), r = (double)myR * scale;
-                    const bool feas = r <= B;
-                    const uint64_t kv = okey(v);
-                    uint64_t kb = feas ? kv : ~0ull;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const uint64_t y = __shfl_xor_sync(0xffffffffu, kb, o);
-                        kb = y < kb ? y : kb;
-                    }
-                    const uint32_t mb = __ballot_sync(0xffffffffu, feas && kv == kb);
-                    const int ib = mb ? __ffs(mb) - 1 : -1;
-                    const bool cand = !feas && v > -1.0 && (ib < 0 || kv < kb);
-                    uint64_t ka = cand ? kv : 0ull;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const uint64_t y = __shfl_xor_sync(0xffffffffu, ka, o);
-                        ka = y > ka ? y : ka;
-                    }
-                    const uint32_t ma = __ballot_sync(0xffffffffu, cand && kv == ka);
-                    const int ia = ma ? __ffs(ma) - 1 : -1;
-                    const double vb = __shfl_sync(0xffffffffu, v, ib >= 0 ? ib : 0);
-                    const double Rb = __shfl_sync(0xffffffffu, r, ib >= 0 ? ib : 0);
-                    const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
-                    const double Ra = __shfl_sync(0xffffffffu, r, ia >= 0 ? ia : 0);
-                    search_copy_scalars(st, S);        // every lane computes the same estimate
-                    const double est = search_pilot_finish(st, ib, ib >= 0 ? vb : INFINITY, ib >= 0 ? Rb : 0.0,
-                                                           ia, ia >= 0 ? va : -1.0, ia >= 0 ? Ra : 0.0, B);
-                    __syncwarp();
-                    if (st.have_grid && L > kSearchFirstDoublings) S.probe[L] = search_pilot_probe(est, L);
-                    __syncwarp();
-                    if (L == 0) search_copy_scalars(S, st);
-                } else {
-                    // one lane per probe folds the evaluations into the window (exact
-                    // min / max of order keys), every lane walks, and lane L generates
-                    // the probes along decision path L
-                    const bool inr = L < S.nprobe;
-                    const double v = search_probe(S, L);
-                    const uint64_t kv = okey(v);
-                    const bool feas = inr && myR <= Bfx;
-                    uint64_t kb = feas ? kv : ~0ull;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const uint64_t y = __shfl_xor_sync(0xffffffffu, kb, o);
-                        kb = y < kb ? y : kb;
-                    }
-                    const uint32_t mb = __ballot_sync(0xffffffffu, feas && kv == kb);
-                    const int ib = mb ? __ffs(mb) - 1 : -1;
-                    const double vb = __shfl_sync(0xffffffffu, v, ib >= 0 ? ib : 0);
-                    const uint64_t kxb = okey(S.xb);
-                    const uint64_t kxbn = (ib >= 0 && kb < kxb) ? kb : kxb;
-                    const bool inf = inr && !feas && kv < kxbn;
-                    uint64_t ka = inf ? kv : 0ull;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const uint64_t y = __shfl_xor_sync(0xffffffffu, ka, o);
-                        ka = y > ka ? y : ka;
-                    }
-                    const uint32_t ma = __ballot_sync(0xffffffffu, inf && kv == ka);
-                    const int ia = ma ? __ffs(ma) - 1 : -1;
-                    const double va = __shfl_sync(0xffffffffu, v, ia >= 0 ? ia : 0);
-                    search_copy_scalars(st, S);
-                    search_window(st, ib >= 0 ? vb : INFINITY, ib, ib >= 0 ? Rfx[ib] : 0, va, ia);
-                    walk_on = search_decide(st, Rfx, Bfx);
-                    __syncwarp();
-                    if (L == 0) {
-                        search_copy_scalars(S, st);
-                        if (st.infeasible) ctrl->status = KVQ_ERR_INFEASIBLE;
-                    }
-                }
-                // first publication: the window and the next round's kind
-                __syncwarp();
-                if (L == 0) {
-                    if (!sC.fixed && S.xb_probe >= 0) ctrl->Rxb_fx = Rfx[S.xb_probe];
-                    ctrl->cnt[round & 1] = 0u;     // consumed; the next round appends here
-                    ctrl->ticket = 0u;
-                    ctrl->fin_avail = sC.fin_tail;  // every queue append of this round is in
-                }
-                publish_search(ctrl, S, L);
-                __syncwarp();            // the warp's writes, then one release store
-                if (L == 0) st_release_u32(&ctrl->gen, 2u * (uint32_t)iter + 1u);
-                
-                // second publication: the walk and the next round's probes
-                if (walk_on) {
-                    const SearchWindow win = search_window_of(st);   // the walk keeps it
-                    const int go = search_walk_w(st, win);
-                    __syncwarp();
-                    
-                    if (go) {
-                        __shared__ double sProbe[kSearchProbes];
-                        sProbe[L] = search_first_unknown(st);
-                        __syncwarp();
-                        search_path_w(st, win, L, sProbe);
-                        __syncwarp();
-                        
-                        S.probe[L] = sProbe[L];
-                    }
-                    __syncwarp();
-                    if (L == 0) search_copy_scalars(S, st);
-                    __syncwarp();
-                    publish_search(ctrl, S, L);
-                }
-                __syncwarp();
-                if (L == 0) {
-                    ctrl->t_ctl[min(round, 15)] = global_ns();
-                    st_release_u32(&ctrl->gen, 2u * (uint32_t)iter + 2u);
-                }
-            }
+            if (threadIdx.x < 32) round_control(ctrl, walk, iter, round, false);
             __syncthreads();
             ready = true;
         } else {
