@@ -959,58 +959,43 @@ def main():
     wtd = weighted_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, dev)
     others = None if args.no_other_configs else other_configs_bench(dev, *peaks())
 
-    # End to end through the C ABI from pinned host memory, pipelined over
-    # three streams the way a serving loop would run it: step i's input copy
-    # overlaps step i-1's kernels and step i-2's result copy.  Every step
-    # copies its whole input in and its codes, codebooks, k and totals out;
-    # the L2 flush runs on the compute stream before each step, inside the
-    # timed interval.  Two sets of device and host buffers alternate.
+    # End to end through the C ABI from pinned host memory: one
+    # kvq_encode_host call per step (the input copied in by four copy
+    # engines at once, the three kernels, the codes, codebooks, k and totals
+    # copied out), steps alternating between two streams and two sets of
+    # buffers the way a serving loop would run them, so that step i's copy in
+    # overlaps step i-1's kernels and result copy.  The L2 flush runs on the
+    # step's stream before its call, inside the timed interval.
     x_host = torch.from_numpy(x_np.view(np.int16)).view(torch.float16).pin_memory()
     bufs = [buf, kvq.Buffers(L, s, dev)]
     xes = [torch.empty_like(x), torch.empty_like(x)]
+    sts = [torch.zeros(3, dtype=torch.int32, device=dev) for _ in range(2)]
     outs_h = [dict(codes=torch.empty(buf.codes.shape, dtype=torch.uint8).pin_memory(),
                    codebook=torch.empty(buf.codebook.shape, dtype=torch.float32).pin_memory(),
                    k=torch.empty(buf.k.shape, dtype=torch.uint8).pin_memory(),
                    totals=torch.empty(3, dtype=torch.float64).pin_memory()) for _ in range(2)]
     h2d = x_host.numel() * 2
     d2h = sum(t.numel() * t.element_size() for t in outs_h[0].values())
-    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_cmp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    e2e_streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
 
     def e2e_run(n):
         torch.cuda.synchronize()
+        cur = torch.cuda.current_stream()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(s_in)
-        s_cmp.wait_event(t0)
-        s_out.wait_event(t0)
+        t0.record(cur)
+        for st_ in e2e_streams:
+            st_.wait_event(t0)
         for i in range(n):
             j = i & 1
-            b, xe, oh = bufs[j], xes[j], outs_h[j]
-            with torch.cuda.stream(s_in):
-                if i >= 2:
-                    s_in.wait_event(ev_cmp[j])         # step i-2 is done reading xe
-                xe.copy_(x_host, non_blocking=True)
-                ev_in[j].record(s_in)
-            with torch.cuda.stream(s_cmp):
-                s_cmp.wait_event(ev_in[j])
-                if i >= 2:
-                    s_cmp.wait_event(ev_out[j])       # step i-2's results are copied out
+            st_, oh = e2e_streams[j], outs_h[j]
+            with torch.cuda.stream(st_):
                 flush_l2(i)
-                kvq.kvq_stats(xe, L, b.stats, b.status_stats, stream=s_cmp)
-                kvq.kvq_allocate(b.stats, L, s, B, kvq.KVQ_BISECT40, 0.0, b.lam, b.workspace,
-                                 b.codebook, b.k, b.D_r, b.H_r, b.totals, b.status, stream=s_cmp)
-                kvq.kvq_quantize(xe, L, b.codebook, b.k, 0, 0, b.codes, b.status_quant,
-                                 stream=s_cmp)
-                ev_cmp[j].record(s_cmp)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_cmp[j])
-                for key in ("codes", "codebook", "k", "totals"):
-                    oh[key].copy_(getattr(b, key), non_blocking=True)
-                ev_out[j].record(s_out)
-        t1.record(s_out)                              # after the last result copy
+                kvq.kvq_encode_host(x_host, L, s, B, 0, 0, xes[j], bufs[j], sts[j], oh["codes"],
+                                    oh["codebook"], oh["k"], oh["totals"], stream=st_)
+        for st_ in e2e_streams:
+            cur.wait_stream(st_)
+        t1.record(cur)                                # after the last result copy
         torch.cuda.synchronize()
         return t0.elapsed_time(t1)
 
@@ -1024,6 +1009,8 @@ def main():
     e2e_val = world * args.steps * in_bytes / (t_e2e * 1e-3) / 1e9
     if not torch.equal(outs_h[(args.steps - 1) & 1]["codes"], ref_codes):
         raise SystemExit("end-to-end codes differ from the device-resident run")
+    if any(v != 0 for st_ in sts for v in st_.tolist()):
+        raise SystemExit("end-to-end statuses %s" % [st_.tolist() for st_ in sts])
 
     hbm, src = peaks()
     mean = lambda v: sum(v) / len(v)
@@ -1109,8 +1096,9 @@ def main():
             "roofline": roof,
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
-                    "how": "C-ABI calls from pinned host memory, input copy / kernels / result "
-                           "copy pipelined on 3 streams, L2 flush inside each step"},
+                    "how": "kvq_encode_host per step from pinned host memory (input copied in "
+                           "4 pieces on 4 copy streams, codes / codebooks / k / totals copied "
+                           "out), steps alternating over 2 streams, L2 flush inside each step"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk_summary,
             "cpu_baseline": cpu,

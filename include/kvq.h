@@ -288,6 +288,45 @@ int kvq_dequantize(const uint8_t *codes, const float *codebook, kvq_layout L,
                    uint16_t *y, void *stream);
 
 /*
+ * kvq_encode_host -- the whole write path for a tensor held in host memory:
+ * the copy in, kvq_stats, kvq_allocate (KVQ_BISECT40), kvq_quantize, and the
+ * copy out of what a cache stores (codes, codebook, k) and of the totals.
+ * The method's page describes the computation on the device; this is the
+ * call a serving loop makes when the new keys or values are staged in host
+ * memory.
+ *   x_host      host [S,T,D] binary16; page-locked (cudaHostAlloc or
+ *               cudaHostRegister) for the call to be asynchronous -- it is
+ *               read until the stream has passed the copy in.
+ *   x_dev       device [S,T,D] binary16: where the input is copied.
+ *   stats, lambda, workspace, codebook, k, D_r, H_r, totals
+ *               device, as kvq_stats / kvq_allocate (s, budget_bits too).
+ *   seed, index_base, codes   as kvq_quantize.
+ *   status      device int32 [3]: the status words of the stats, the
+ *               allocation and the quantization, in that order (the last is
+ *               set to KVQ_OK first, then to KVQ_ERR_TIMEOUT if a copy into
+ *               shared memory never completed).
+ *   codes_host, codebook_host, k_host, totals_host
+ *               host (page-locked, as x_host), each written with its device
+ *               counterpart, or NULL to skip that copy.
+ *   stream      everything is ordered on `stream` and asynchronous; the host
+ *               outputs are valid once the stream has reached the end of the
+ *               call.  The copy in is split into up to 4 pieces, each on one
+ *               of the library's own copy streams (created per device by the
+ *               first call, which should therefore be made outside any
+ *               stream capture): they start after the work already queued on
+ *               `stream`, and `stream` waits for all of them, so several copy
+ *               engines move the input at once.
+ * Every argument is checked before anything is issued; KVQ_ERR_CUDA if the
+ * runtime refused a copy or a launch.
+ */
+int kvq_encode_host(const uint16_t *x_host, kvq_layout L, int s, double budget_bits,
+                    uint64_t seed, uint64_t index_base, uint16_t *x_dev, void *stats,
+                    double *lambda, void *workspace, float *codebook, uint8_t *k, float *D_r,
+                    float *H_r, double *totals, uint8_t *codes, int32_t *status,
+                    uint8_t *codes_host, float *codebook_host, uint8_t *k_host,
+                    double *totals_host, void *stream);
+
+/*
  * kvq_uniform_codebook -- codebooks of the uniform comparator ("Implementation
  * notes": compare uniform INT4 and uniform stochastic quantization at equal
  * cache bytes): per block, from its minimum m and maximum M,

@@ -90,6 +90,65 @@ static int init_once() {
     done[dev] = true;
     return KVQ_OK;
 }
+
+// kvq_encode_host's copy lanes: per device, kCopyLanes non-blocking streams
+// that each take one piece of the host-to-device copy, so that several copy
+// engines run at once (one engine moves about 28 GB/s from page-locked host
+// memory on a B300 host, four about 44 GB/s); an event forks them from the
+// caller's stream and one event per lane joins them back.  Created on the
+// first call on the device, under the lock that also orders each call's
+// record / wait sequence against other host threads.
+constexpr int kCopyLanes = 4;
+struct CopyLanes {
+    cudaStream_t st[kCopyLanes];
+    cudaEvent_t fork, join[kCopyLanes];
+    bool ready;
+};
+static std::mutex g_lanes_mu;
+static CopyLanes g_lanes[64];
+
+static int lanes_ready(int dev) {
+    CopyLanes &C = g_lanes[dev];
+    if (C.ready) return KVQ_OK;
+    bool ok = cudaEventCreateWithFlags(&C.fork, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < kCopyLanes; ++i) {
+        ok = cudaStreamCreateWithFlags(&C.st[i], cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&C.join[i], cudaEventDisableTiming) == cudaSuccess;
+    }
+    if (!ok) {
+        (void)cudaGetLastError();
+        return KVQ_ERR_CUDA;   // what was created stays, unused; the next call tries again
+    }
+    C.ready = true;
+    return KVQ_OK;
+}
+
+// Copy `bytes` from host to device in up to kCopyLanes pieces (multiples of
+// 64 KiB but the last), each on its own lane, ordered after and before the
+// work of `st`.
+static int copy_in_lanes(void *dst, const void *src, size_t bytes, cudaStream_t st) {
+    if (bytes == 0) return KVQ_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
+    std::lock_guard<std::mutex> g(g_lanes_mu);
+    if (lanes_ready(dev) != KVQ_OK) return KVQ_ERR_CUDA;
+    CopyLanes &C = g_lanes[dev];
+    const size_t unit = (size_t)1 << 16;
+    const size_t piece = ((bytes + kCopyLanes - 1) / kCopyLanes + unit - 1) / unit * unit;
+    if (cudaEventRecord(C.fork, st) != cudaSuccess) return KVQ_ERR_CUDA;
+    for (int i = 0; i < kCopyLanes; ++i) {
+        const size_t off = (size_t)i * piece;
+        if (off >= bytes) break;
+        const size_t len = bytes - off < piece ? bytes - off : piece;
+        if (cudaStreamWaitEvent(C.st[i], C.fork, 0) != cudaSuccess ||
+            cudaMemcpyAsync(static_cast<char *>(dst) + off, static_cast<const char *>(src) + off,
+                            len, cudaMemcpyHostToDevice, C.st[i]) != cudaSuccess ||
+            cudaEventRecord(C.join[i], C.st[i]) != cudaSuccess ||
+            cudaStreamWaitEvent(st, C.join[i], 0) != cudaSuccess)
+            return KVQ_ERR_CUDA;
+    }
+    return KVQ_OK;
+}
 }  // namespace kvq
 
 using namespace kvq;
@@ -414,6 +473,55 @@ int kvq_decode_attention(const float *q, int n_rep, kvq_layout L, const uint8_t 
     return launch_decode_attention(q, n_rep, L, k_codes, k_codebook, v_codes, v_codebook, T_valid,
                                    scale, workspace, out, status,
                                    static_cast<cudaStream_t>(stream));
+}
+
+int kvq_encode_host(const uint16_t *x_host, kvq_layout L, int s, double budget_bits,
+                    uint64_t seed, uint64_t index_base, uint16_t *x_dev, void *stats,
+                    double *lambda, void *workspace, float *codebook, uint8_t *k, float *D_r,
+                    float *H_r, double *totals, uint8_t *codes, int32_t *status,
+                    uint8_t *codes_host, float *codebook_host, uint8_t *k_host,
+                    double *totals_host, void *stream) {
+    // every argument of the three calls is checked before anything is issued
+    if (!layout_ok(L) || s < 2 || s > kMaxLev) return KVQ_ERR_INVALID_ARG;
+    if (!(budget_bits >= 0.0) || !isfinite(budget_bits)) return KVQ_ERR_INVALID_ARG;
+    if (!lambda || !totals || !status) return KVQ_ERR_INVALID_ARG;
+    if (index_base & 3u) return KVQ_ERR_INVALID_ARG;
+    const uint64_t n = (uint64_t)L.S * (uint64_t)L.T * (uint64_t)L.D;
+    if (index_base > (1ull << 40) || n > (1ull << 40) - index_base) return KVQ_ERR_INVALID_ARG;
+    const int64_t nb = num_blocks(L);
+    if (nb > 0) {
+        if (!x_host || !x_dev || !stats || !workspace || !codebook || !k || !D_r || !H_r || !codes)
+            return KVQ_ERR_INVALID_ARG;
+        if (!aligned16(x_dev) || !aligned16(stats) || !aligned16(workspace) ||
+            !aligned16(codebook) || !aligned16(codes))
+            return KVQ_ERR_INVALID_ARG;
+        if (nb > 0x7fffffffll) return KVQ_ERR_INVALID_ARG;
+    }
+    if (init_once() != KVQ_OK) return KVQ_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = copy_in_lanes(x_dev, x_host, (size_t)n * sizeof(uint16_t), st);
+    if (rc == KVQ_OK) rc = kvq_stats(x_dev, L, kCand, stats, status, stream);
+    if (rc == KVQ_OK)
+        rc = kvq_allocate(stats, L, s, budget_bits, KVQ_BISECT40, 0.0, lambda, workspace, codebook,
+                          k, D_r, H_r, totals, status + 1, stream);
+    // kvq_quantize writes its status only when a copy times out
+    if (rc == KVQ_OK && cudaMemsetAsync(status + 2, 0, sizeof(int32_t), st) != cudaSuccess)
+        rc = KVQ_ERR_CUDA;
+    if (rc == KVQ_OK)
+        rc = kvq_quantize(x_dev, L, codebook, k, seed, index_base, codes, status + 2, stream);
+    if (rc != KVQ_OK) return rc;
+    // what a cache stores, and the totals, back to the host
+    struct { void *dst; const void *src; size_t bytes; } out[4] = {
+        {codes_host, codes, (size_t)nb * 16 * (size_t)L.group},
+        {codebook_host, codebook, (size_t)nb * 16 * sizeof(float)},
+        {k_host, k, (size_t)nb},
+        {totals_host, totals, 3 * sizeof(double)},
+    };
+    for (const auto &o : out)
+        if (o.dst && o.bytes &&
+            cudaMemcpyAsync(o.dst, o.src, o.bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            return KVQ_ERR_CUDA;
+    return KVQ_OK;
 }
 
 int kvq_allocate_report(const void *workspace, kvq_report *report) {

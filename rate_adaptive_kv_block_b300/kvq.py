@@ -123,6 +123,9 @@ def lib():
         L.kvq_quantize.argtypes = [vp, _Layout, vp, vp, u64, u64, vp, vp, vp]
         L.kvq_dequantize.restype = C.c_int
         L.kvq_dequantize.argtypes = [vp, vp, _Layout, vp, vp]
+        L.kvq_encode_host.restype = C.c_int
+        L.kvq_encode_host.argtypes = [vp, _Layout, C.c_int, dbl, u64, u64, vp, vp, vp, vp, vp, vp,
+                                      vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kvq_uniform_codebook.restype = C.c_int
         L.kvq_uniform_codebook.argtypes = [vp, _Layout, vp, vp, vp, vp]
         L.kvq_quantize_nearest.restype = C.c_int
@@ -294,6 +297,21 @@ def kvq_quantize(x, L: Layout, codebook, k, seed: int, index_base: int, codes, s
 def kvq_dequantize(codes, codebook, L: Layout, y, stream=None):
     _check(lib().kvq_dequantize(_ptr(codes), _ptr(codebook), L.c(), _ptr(y), _stream(stream)),
            "kvq_dequantize")
+
+
+def kvq_encode_host(x_host, L: Layout, s: int, budget_bits: float, seed: int, index_base: int,
+                    x_dev, buf: "Buffers", status, codes_host=None, codebook_host=None,
+                    k_host=None, totals_host=None, stream=None):
+    """The write path from host memory (see include/kvq.h): x_host a pinned
+    [S,T,D] float16 CPU tensor, x_dev its device destination, buf the device
+    buffers, status a device int32 [3]; the *_host outputs are pinned CPU
+    tensors or None."""
+    _check(lib().kvq_encode_host(
+        _ptr(x_host), L.c(), int(s), float(budget_bits), int(seed), int(index_base), _ptr(x_dev),
+        _ptr(buf.stats), _ptr(buf.lam), _ptr(buf.workspace), _ptr(buf.codebook), _ptr(buf.k),
+        _ptr(buf.D_r), _ptr(buf.H_r), _ptr(buf.totals), _ptr(buf.codes), _ptr(status),
+        _ptr(codes_host), _ptr(codebook_host), _ptr(k_host), _ptr(totals_host), _stream(stream)),
+        "kvq_encode_host")
 
 
 def kvq_uniform_codebook(x, L: Layout, codebook, k, status, stream=None):

@@ -118,3 +118,27 @@ def test_decode_attention_host_validation():
     assert call(kc=None) == bad and call(kc=C.c_void_p(odd.p)) == bad
     with pytest.raises(kvq.KvqError):
         kvq.kvq_decode_attention(p, 3, L, p, p, p, p, 8192, 0.088, p, p, stream=s)
+
+
+def test_encode_host_validation():
+    """kvq_encode_host checks every argument of its three calls before it
+    issues anything (no GPU is touched: each case is rejected on the host)."""
+    L = kvq.Layout(2, 64, 128, 128)
+    lib = kvq.lib()
+    bad = kvq.KVQ_ERR_INVALID_ARG
+    v, odd = C.c_void_p(1 << 20), C.c_void_p((1 << 20) + 8)
+
+    def call(x_host=v, L_=L, s=8, B=1.0, seed=0, base=0, x_dev=v, stats=v, lam=v, ws=v, cb=v,
+             k=v, Dr=v, Hr=v, tot=v, codes=v, status=v):
+        return lib.kvq_encode_host(x_host, L_.c(), s, B, seed, base, x_dev, stats, lam, ws, cb, k,
+                                   Dr, Hr, tot, codes, status, None, None, None, None,
+                                   kvq._stream(_Stream()))
+
+    assert call(L_=kvq.Layout(2, 65, 128, 128)) == bad          # T % 32
+    assert call(s=1) == bad and call(s=17) == bad
+    assert call(B=-1.0) == bad and call(B=float("inf")) == bad
+    assert call(base=2) == bad                                   # index_base % 4
+    assert call(x_host=None) == bad and call(x_dev=None) == bad
+    assert call(x_dev=odd) == bad and call(codes=odd) == bad and call(stats=odd) == bad
+    assert call(status=None) == bad and call(lam=None) == bad and call(tot=None) == bad
+    assert call(ws=None) == bad and call(cb=None) == bad

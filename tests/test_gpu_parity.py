@@ -404,3 +404,53 @@ def test_search_needs_one_round_over_every_block(name, T, S, bpe):
     assert all(a < nb // 2 for a in active[2:]), active
     want = oracle.allocate_bisect(x.view(np.float16), w.G, 16, bpe * w.entries)["lambda"]
     assert abs(float(buf.lam.item()) - want) <= 1e-4 * want
+
+
+# ------------------------------------------- the write path from host memory
+
+@pytest.mark.parametrize("name,T,S", [("k_head_small", 64, None), ("hadamard_groups", 256, None),
+                                      ("llama3_8b_layer", 512, None)])
+def test_encode_host_matches_oracle_and_device_calls(name, T, S):
+    """kvq_encode_host (host input copied in pieces on several streams, host
+    outputs) gives the oracle's lambda and codes, and the device-resident
+    calls' results byte for byte."""
+    _need_gpu()
+    w = synth.workload(name, T=T, S=S)
+    x = synth.make_numpy(w, seed=12)
+    L = kvq.Layout(*x.shape, w.G)
+    B = w.budgets[0] * x.size
+    xh = torch.from_numpy(x.view(np.int16)).view(torch.float16).pin_memory()
+    xd = torch.empty(x.shape, dtype=torch.float16, device="cuda")
+    buf = kvq.Buffers(L, w.s)
+    status = torch.full((3,), 9, dtype=torch.int32, device="cuda")
+    out = dict(codes=torch.empty(buf.codes.shape, dtype=torch.uint8).pin_memory(),
+               codebook=torch.empty(buf.codebook.shape, dtype=torch.float32).pin_memory(),
+               k=torch.empty(buf.k.shape, dtype=torch.uint8).pin_memory(),
+               totals=torch.empty(3, dtype=torch.float64).pin_memory())
+    side = torch.cuda.Stream()
+    kvq.kvq_encode_host(xh, L, w.s, B, 7, 1 << 20, xd, buf, status, out["codes"], out["codebook"],
+                        out["k"], out["totals"], stream=side)
+    side.synchronize()
+    assert status.tolist() == [0, 0, 0]
+    assert torch.equal(xd.view(torch.int16).cpu(), xh.view(torch.int16))      # the copy in
+    ref = kvq.quantize(gc.to_dev(x), L, B, w.s, seed=7, index_base=1 << 20)
+    torch.cuda.synchronize()
+    for key in ("codes", "codebook", "k", "totals"):
+        assert torch.equal(out[key].view(torch.uint8), getattr(ref, key).cpu().view(torch.uint8)), key
+    lam = float(out["totals"][2])
+    ob = oracle.allocate_bisect(x, w.G, w.s, B)
+    assert abs(lam - ob["lambda"]) <= gc.LAM_REL * abs(ob["lambda"]), (lam, ob["lambda"])
+    codes_o = oracle.quantize(x, w.G, out["codebook"].numpy(), out["k"].numpy(), 7, 1 << 20)
+    assert np.array_equal(codes_o, out["codes"].numpy())
+
+
+def test_encode_host_empty_layout_and_skipped_outputs():
+    _need_gpu()
+    L = kvq.Layout(0, 64, 128, 128)
+    buf = kvq.Buffers(L, 16)
+    status = torch.full((3,), 9, dtype=torch.int32, device="cuda")
+    xh = torch.empty((0, 64, 128), dtype=torch.float16).pin_memory()
+    xd = torch.empty((0, 64, 128), dtype=torch.float16, device="cuda")
+    kvq.kvq_encode_host(xh, L, 16, 100.0, 0, 0, xd, buf, status)
+    torch.cuda.synchronize()
+    assert status.tolist() == [0, 0, 0] and float(buf.totals[0].item()) == 0.0
