@@ -14,10 +14,10 @@
 //   scan    bin prefix counts locate the bin of each of the 17 ranks;
 //   pass 2  entries of those (<= 17) bins count their low byte in a second
 //           histogram (two 16-bit counters per 32-bit word);
-//   select  one warp per selected bin finds the exact key of each rank and
-//           the prefix sums of (1, j, j^2) below it (a count scan, then
-//           warp reductions over the keys whose prefix stays at or below the
-//           rank).
+//   select  one warp per selected bin sums (1, j, j^2) over each chunk of 8
+//           keys and scans the chunk sums; then one lane per rank finds its
+//           chunk by a binary search of the prefix counts and its key inside
+//           the chunk, with the prefix sums of (1, j, j^2) below it.
 // Inside a bin the value is affine in j (one binade quarter: fixed sign and
 // exponent), so the atom moments follow from those exact integer sums without
 // touching the entries again: half a warp per atom sums its bins with a
@@ -39,16 +39,18 @@ struct StatsSmem {
             uint32_t h1a[kStatsWarps][256];   // per warp: (count << 22) | sum j
             uint32_t h1b[kStatsWarps][256];   // per warp: sum j^2
         };
-        uint32_t l2[17][128];                 // after the merge: low-byte counts
+        struct {
+            uint32_t l2[17][128];             // after the merge: low-byte counts
+            // per selected bin and 8-key chunk: counts, sum j and sum j^2
+            // of the keys in the chunks before it
+            uint32_t cpn[17][32], cps1[17][32], cps2[17][32];
+        };
     };
     int32_t cnt[256];
     uint32_t s1[256], s2[256];
     uint8_t binslot[256];
     int32_t warp_tot[kStatsWarps];
-    int32_t rank_bin[17], rank_res[17], rank_slot[17];
-    int32_t slot_first[17], slot_nrank[17];
-    int32_t rank_key[17], rank_p0[17], rank_cnt[17];
-    uint32_t rank_p1[17], rank_p2[17];
+    int32_t rank_bin[17], rank_res[17];
     int32_t dkey[17], dp0[17], dcnt[17];
     uint32_t dp1[17], dp2[17];
     float dc[17];
@@ -209,10 +211,6 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
     int nslots;
     const int slot = block_excl_scan(tgt ? 1 : 0, sm.warp_tot, nslots);
     sm.binslot[tid] = tgt ? (uint8_t)slot : (uint8_t)0xff;
-    if (tgt) {
-        sm.slot_first[slot] = jlo;
-        sm.slot_nrank[slot] = jhi - jlo + 1;
-    }
     if (tid == 0) sm.nslots = nslots;
     __syncthreads();
 
@@ -230,80 +228,93 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
     }
     __syncthreads();
 
-    // ---- exact key of every rank + prefix sums (count, sum j, sum j^2) of
-    //      the keys below it inside its bin: one warp per selected bin, lane l
-    //      holds keys 8l .. 8l+7
+    // ---- per selected bin, a warp with one lane per chunk of 8 keys (lane l
+    //      holds keys 8l .. 8l+7): the chunk's count, sum j and sum j^2, and
+    //      their exclusive prefixes over the chunks
     for (int sl = warp; sl < sm.nslots; sl += kStatsWarps) {
         const uint4 wd = reinterpret_cast<const uint4 *>(sm.l2[sl])[lane];
-        const uint32_t c8[8] = {wd.x & 0xffffu, wd.x >> 16, wd.y & 0xffffu, wd.y >> 16,
-                                wd.z & 0xffffu, wd.z >> 16, wd.w & 0xffffu, wd.w >> 16};
-        const uint32_t pairsum = wd.x + wd.y + wd.z + wd.w;   // two 16-bit sums
-        const uint32_t n = (pairsum & 0xffffu) + (pairsum >> 16);
-        uint32_t en = n;
+        const uint32_t w4[4] = {wd.x, wd.y, wd.z, wd.w};
+        uint32_t n = 0, s1 = 0, s2 = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint32_t c = (w4[q >> 1] >> ((q & 1) * 16)) & 0xffffu;
+            const uint32_t jj = (uint32_t)(lane * 8 + q);
+            n += c;
+            s1 += c * jj;
+            s2 += c * jj * jj;
+        }
+        uint32_t en = n, e1 = s1, e2 = s2;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t a = __shfl_up_sync(0xffffffffu, en, o);
-            if (lane >= o) en += a;
-        }
-        en -= n;                                                // exclusive
-        // inclusive prefix count at each of the lane's keys, and the key's
-        // (count, count j, count j^2)
-        uint32_t ci[8], pj[8], pjj[8];
-        {
-            uint32_t run = en;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint32_t jj = (uint32_t)(lane * 8 + q);
-                run += c8[q];
-                ci[q] = run;
-                pj[q] = c8[q] * jj;
-                pjj[q] = c8[q] * jj * jj;
+            const uint32_t b = __shfl_up_sync(0xffffffffu, e1, o);
+            const uint32_t c = __shfl_up_sync(0xffffffffu, e2, o);
+            if (lane >= o) {
+                en += a;
+                e1 += b;
+                e2 += c;
             }
         }
-        const int j0 = sm.slot_first[sl], nr = sm.slot_nrank[sl];
-        for (int j = j0; j < j0 + nr; ++j) {
-            // the rank's key is the first whose inclusive prefix exceeds the
-            // residual: count (and sum over) the keys whose prefix does not
-            const uint32_t res = (uint32_t)sm.rank_res[j];
-            uint32_t kb = 0, c0 = 0, p1 = 0, p2 = 0, cle = 0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const bool below = ci[q] <= res;
-                kb += below ? 1u : 0u;
-                c0 += below ? c8[q] : 0u;
-                p1 += below ? pj[q] : 0u;
-                p2 += below ? pjj[q] : 0u;
-                cle += (ci[q] - c8[q] <= res) ? c8[q] : 0u;     // keys at or below
-            }
-            const uint32_t key = __reduce_add_sync(0xffffffffu, kb);
-            const uint32_t P0 = __reduce_add_sync(0xffffffffu, c0);
-            const uint32_t P1 = __reduce_add_sync(0xffffffffu, p1);
-            const uint32_t P2 = __reduce_add_sync(0xffffffffu, p2);
-            const uint32_t CL = __reduce_add_sync(0xffffffffu, cle);
-            if (lane == 0) {
-                sm.rank_key[j] = (sm.rank_bin[j] << 8) | (int)key;
-                sm.rank_p0[j] = (int)P0;
-                sm.rank_p1[j] = P1;
-                sm.rank_p2[j] = P2;
-                sm.rank_cnt[j] = (int)(CL - P0);
-            }
-        }
+        sm.cpn[sl][lane] = en - n;
+        sm.cps1[sl][lane] = e1 - s1;
+        sm.cps2[sl][lane] = e2 - s2;
     }
     __syncthreads();
 
-    // ---- merge equal candidates (warp 0, lane j = rank j)
+    // ---- warp 0, lane j = rank j: its key is the first of its bin whose
+    //      inclusive prefix count exceeds the rank's residual; the chunk that
+    //      holds it is the last whose exclusive prefix does not, then the keys
+    //      of that chunk in order.  P0, P1, P2: count, sum j, sum j^2 of the
+    //      bin's entries below the key; cnt: the entries equal to it.  Equal
+    //      candidates are then merged.
     if (warp == 0) {
-        const int key = lane < kCand ? sm.rank_key[lane] : -1;
-        const int prev = (lane >= 1 && lane < kCand) ? sm.rank_key[lane - 1] : -2;
+        int key = -1;
+        uint32_t P0 = 0, P1 = 0, P2 = 0, cnt = 0;
+        if (lane < kCand) {
+            const int bin = sm.rank_bin[lane];
+            const uint32_t res = (uint32_t)sm.rank_res[lane];
+            const int sl = sm.binslot[bin];
+            int ch = 0;                       // cpn[sl][0] = 0 <= res; ch + step <= 31
+#pragma unroll
+            for (int step = 16; step > 0; step >>= 1)
+                if (sm.cpn[sl][ch + step] <= res) ch += step;
+            const uint4 wd = reinterpret_cast<const uint4 *>(sm.l2[sl])[ch];
+            const uint32_t w4[4] = {wd.x, wd.y, wd.z, wd.w};
+            uint32_t e = sm.cpn[sl][ch], p1 = sm.cps1[sl][ch], p2 = sm.cps2[sl][ch];
+            int kq = 7;
+            bool found = false;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t c = (w4[q >> 1] >> ((q & 1) * 16)) & 0xffffu;
+                const uint32_t jj = (uint32_t)(ch * 8 + q);
+                if (!found) {
+                    if (e + c > res) {
+                        found = true;
+                        kq = q;
+                        cnt = c;
+                    } else {
+                        e += c;
+                        p1 += c * jj;
+                        p2 += c * jj * jj;
+                    }
+                }
+            }
+            key = (bin << 8) | (ch * 8 + kq);
+            P0 = e;
+            P1 = p1;
+            P2 = p2;
+        }
+        const int prev_raw = __shfl_up_sync(0xffffffffu, key, 1);
+        const int prev = (lane >= 1 && lane < kCand) ? prev_raw : -2;
         const bool first = lane < kCand && key != prev;
         const uint32_t bal = __ballot_sync(0xffffffffu, first);
         if (first) {
             const int p = __popc(bal & ((1u << lane) - 1u));
             sm.dkey[p] = key;
-            sm.dp0[p] = sm.rank_p0[lane];
-            sm.dp1[p] = sm.rank_p1[lane];
-            sm.dp2[p] = sm.rank_p2[lane];
-            sm.dcnt[p] = sm.rank_cnt[lane];
+            sm.dp0[p] = (int)P0;
+            sm.dp1[p] = P1;
+            sm.dp2[p] = P2;
+            sm.dcnt[p] = (int)cnt;
             sm.dc[p] = key_value((uint32_t)key);
         }
         if (lane == 0) sm.mprime = __popc(bal);
@@ -375,11 +386,16 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
     //        Mup = sum (s1 + n A) / (b - a)        (expected count sent to b)
     //        Mdn = sum (t1 + n B) / (b - a)        (expected count sent to a)
     //      every term non-negative
+    //      Pairs in order of decreasing length Q - P, so that the threads of
+    //      a warp run loops of similar length: thread t takes the P-th of the
+    //      u pairs of length m' - u, u(u-1)/2 <= t < u(u+1)/2.
     const int npr = mp * (mp - 1) / 2;
     if (tid < npr) {
-        int P = 0, rem = tid;
-        while (rem >= mp - 1 - P) { rem -= mp - 1 - P; ++P; }
-        const int Q = P + 1 + rem;
+        int u = (int)((1.0f + sqrtf(1.0f + 8.0f * (float)tid)) * 0.5f);
+        if (u * (u - 1) / 2 > tid) --u;
+        if ((u + 1) * u / 2 <= tid) ++u;
+        const int P = tid - u * (u - 1) / 2;
+        const int Q = P + mp - u;
         const float a = sm.dc[P], bq = sm.dc[Q];
         float Dv = 0.f, Us = 0.f, Ls = 0.f;
         for (int p = P; p < Q; ++p) {
