@@ -194,6 +194,16 @@ __device__ __forceinline__ uint32_t f16_key(uint32_t h) {
     h = (h == 0x8000u) ? 0u : h;
     return (h & 0x8000u) ? (~h & 0xffffu) : (h | 0x8000u);
 }
+// The keys of the two binary16 values packed in w (low half first), packed
+// the same way: both zeros fold into +0 (one packed compare), then each half
+// flips its sign bit, or all its bits when it is negative.
+__device__ __forceinline__ uint32_t f16_key2(uint32_t w) {
+    __half2 h;
+    memcpy(&h, &w, sizeof(w));
+    w &= ~__heq2_mask(h, __float2half2_rn(0.0f));
+    const uint32_t neg = (w >> 15) & 0x00010001u;
+    return w ^ 0x80008000u ^ (neg * 0x7fffu);
+}
 __device__ __forceinline__ uint32_t key_to_bits(uint32_t key) {
     return (key & 0x8000u) ? (key & 0x7fffu) : (~key & 0xffffu);
 }

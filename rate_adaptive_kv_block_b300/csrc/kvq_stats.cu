@@ -48,6 +48,7 @@ struct StatsSmem {
     };
     int32_t cnt[256];
     uint32_t s1[256], s2[256];
+    float bv0[256], bu[256];      // per bin: value of low byte 0, spacing of keys
     uint8_t binslot[256];
     int32_t warp_tot[kStatsWarps];
     int32_t rank_bin[17], rank_res[17];
@@ -81,15 +82,16 @@ __device__ __forceinline__ int block_excl_scan(int v, int32_t *warp_tot, int &to
     return off + x - v;
 }
 
-// Add one piece (entries of bin b with key low byte in [j0, j1], integer sums
-// n, S1 = sum j, S2 = sum j^2) to the moments of the atom [cp, cq).
-__device__ __forceinline__ void add_piece(uint32_t b, int j0, int j1, uint32_t n,
+// Add one piece (entries of a bin with key low byte in [j0, j1], integer sums
+// n, S1 = sum j, S2 = sum j^2) to the moments of the atom [cp, cq).  v0, u:
+// the bin's value at low byte 0 and its key spacing; the value at low byte j
+// is v0 + j u, exact in binary32 (a binary16 value of the bin).
+__device__ __forceinline__ void add_piece(float v0, float u, int j0, int j1, uint32_t n,
                                           uint32_t S1, uint32_t S2, float cp, float cq,
                                           float &an, float &as1, float &at1, float &ae) {
     if (n == 0) return;
-    const float u = bin_ulp(b);
-    const float Y0 = key_value((b << 8) | (uint32_t)j0) - cp;   // >= 0
-    const float T1 = cq - key_value((b << 8) | (uint32_t)j1);   // >= 0
+    const float Y0 = fmaf((float)j0, u, v0) - cp;   // >= 0
+    const float T1 = cq - fmaf((float)j1, u, v0);   // >= 0
     // integer sums of i = j - j0 over the piece; every true value lies in
     // [0, 2^32), so 32-bit modular arithmetic gives it exactly
     const uint32_t L = (uint32_t)(j1 - j0), u0 = (uint32_t)j0;
@@ -152,13 +154,15 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
         const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint32_t k0 = f16_key(w4[q] & 0xffffu), k1 = f16_key(w4[q] >> 16);
-            keys[k][q] = k0 | (k1 << 16);
+            const uint32_t kk = f16_key2(w4[q]);
+            keys[k][q] = kk;
             if (u < units) {
-                atomicAdd(&sm.h1a[warp][k0 >> 8], (1u << 22) | (k0 & 255u));
-                atomicAdd(&sm.h1b[warp][k0 >> 8], (k0 & 255u) * (k0 & 255u));
-                atomicAdd(&sm.h1a[warp][k1 >> 8], (1u << 22) | (k1 & 255u));
-                atomicAdd(&sm.h1b[warp][k1 >> 8], (k1 & 255u) * (k1 & 255u));
+                const uint32_t b0 = (kk >> 8) & 255u, j0 = kk & 255u;
+                const uint32_t b1 = kk >> 24, j1 = (kk >> 16) & 255u;
+                atomicAdd(&sm.h1a[warp][b0], (1u << 22) | j0);
+                atomicAdd(&sm.h1b[warp][b0], j0 * j0);
+                atomicAdd(&sm.h1a[warp][b1], (1u << 22) | j1);
+                atomicAdd(&sm.h1b[warp][b1], j1 * j1);
             }
         }
     }
@@ -177,6 +181,8 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
     sm.cnt[tid] = cnt;
     sm.s1[tid] = S1;
     sm.s2[tid] = S2;
+    sm.bv0[tid] = key_value((uint32_t)tid << 8);     // bin tid: value at j = 0 and spacing
+    sm.bu[tid] = bin_ulp((uint32_t)tid);
     int total;
     const int pre = block_excl_scan(cnt, sm.warp_tot, total);
     // every warp table has been read: its memory becomes the low-byte table
@@ -335,10 +341,16 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
             const uint32_t Klo = (uint32_t)sm.dkey[p], Khi = (uint32_t)sm.dkey[p + 1];
             const uint32_t blo = Klo >> 8, bhi = Khi >> 8;
             const float cp = sm.dc[p], cq = sm.dc[p + 1];
+            // this sub-lane's first piece (n = 0: none)
+            uint32_t b = blo, n = 0, S1 = 0, S2 = 0;
+            int j0 = 0, j1 = 255;
             if (sub >= 2) {
-                for (uint32_t b = blo + (uint32_t)sub - 1u; b < bhi; b += 14u) {
-                    const int c = sm.cnt[b];
-                    if (c) add_piece(b, 0, 255, (uint32_t)c, sm.s1[b], sm.s2[b], cp, cq, an, as1, at1, ae);
+                const uint32_t bb = blo + (uint32_t)sub - 1u;
+                if (bb < bhi) {
+                    b = bb;
+                    n = (uint32_t)sm.cnt[b];
+                    S1 = sm.s1[b];
+                    S2 = sm.s2[b];
                 }
             } else {
                 const int jlo = (int)(Klo & 255u), jhi = (int)(Khi & 255u);
@@ -353,13 +365,31 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
                     jend = jhi;
                 }
                 if (sub == 0) {
-                    if (blo == bhi)
-                        add_piece(blo, jlo, jend, hi0 - lo0, hi1 - lo1, hi2 - lo2, cp, cq, an, as1, at1, ae);
-                    else
-                        add_piece(blo, jlo, 255, (uint32_t)sm.cnt[blo] - lo0, sm.s1[blo] - lo1,
-                                  sm.s2[blo] - lo2, cp, cq, an, as1, at1, ae);
+                    j0 = jlo;
+                    if (blo == bhi) {
+                        j1 = jend;
+                        n = hi0 - lo0;
+                        S1 = hi1 - lo1;
+                        S2 = hi2 - lo2;
+                    } else {
+                        n = (uint32_t)sm.cnt[blo] - lo0;
+                        S1 = sm.s1[blo] - lo1;
+                        S2 = sm.s2[blo] - lo2;
+                    }
                 } else if (blo != bhi && jend >= 0) {
-                    add_piece(bhi, 0, jend, hi0, hi1, hi2, cp, cq, an, as1, at1, ae);
+                    b = bhi;
+                    j1 = jend;
+                    n = hi0;
+                    S1 = hi1;
+                    S2 = hi2;
+                }
+            }
+            add_piece(sm.bv0[b], sm.bu[b], j0, j1, n, S1, S2, cp, cq, an, as1, at1, ae);
+            if (sub >= 2) {   // the rest of the bins strictly between, 14 apart
+                for (uint32_t bb = blo + (uint32_t)sub + 13u; bb < bhi; bb += 14u) {
+                    const uint32_t c = (uint32_t)sm.cnt[bb];
+                    if (c) add_piece(sm.bv0[bb], sm.bu[bb], 0, 255, c, sm.s1[bb], sm.s2[bb], cp, cq,
+                                     an, as1, at1, ae);
                 }
             }
         }
