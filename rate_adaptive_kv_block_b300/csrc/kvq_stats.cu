@@ -181,6 +181,7 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
     sm.cnt[tid] = cnt;
     sm.s1[tid] = S1;
     sm.s2[tid] = S2;
+    sm.binslot[tid] = 0xff;                          // not selected (yet)
     sm.bv0[tid] = key_value((uint32_t)tid << 8);     // bin tid: value at j = 0 and spacing
     sm.bu[tid] = bin_ulp((uint32_t)tid);
     int total;
@@ -209,15 +210,21 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
         jlo = a <= 0 ? 0 : fdiv(a + dm1 - 1);
         jhi = bnd < 0 ? -1 : min(fdiv(bnd), kCand - 1);
     }
-    const bool tgt = jlo <= jhi;
     for (int j = jlo; j <= jhi; ++j) {
         sm.rank_bin[j] = tid;
         sm.rank_res[j] = ((j * (d - 1) + 8) >> 4) - pre;
     }
-    int nslots;
-    const int slot = block_excl_scan(tgt ? 1 : 0, sm.warp_tot, nslots);
-    sm.binslot[tid] = tgt ? (uint8_t)slot : (uint8_t)0xff;
-    if (tid == 0) sm.nslots = nslots;
+    __syncthreads();
+    // the selected bins get slots 0, 1, .. in bin order: lane j = rank j (the
+    // ranks' bins are non-decreasing), a slot for each first lane of a bin
+    if (warp == 0) {
+        const int bin = lane < kCand ? sm.rank_bin[lane] : -1;
+        const int prev = __shfl_up_sync(0xffffffffu, bin, 1);
+        const bool first = lane < kCand && (lane == 0 || bin != prev);
+        const uint32_t bal = __ballot_sync(0xffffffffu, first);
+        if (first) sm.binslot[bin] = (uint8_t)__popc(bal & ((1u << lane) - 1u));
+        if (lane == 0) sm.nslots = __popc(bal);
+    }
     __syncthreads();
 
     // ---- pass 2: per-key counts inside the selected bins
@@ -469,20 +476,38 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
     // d_r H_r moves by less than 2^-22 d_r bits, far inside the DP's fp32
     // rounding of the same sums
     auto hterm = [&](float M) { return M > 0.f ? -M * __log2f(M * inv_d) : 0.f; };
-    for (int idx = tid; idx < kDpFloats; idx += kStatsThreads) {
-        const uint32_t dcd = kDecode.pair[idx];
-        const int j = dcd & 255, l = dcd >> 8;
-        tb[kTblD + idx] = l < 17 ? sm.pDp[pidx(j, l)] : __int_as_float(0x7f800000);
-    }
     // slots that hold a candidate (0 .. m'-2, and 16 for the maximum)
     const uint32_t realm = mp > 1 ? (((1u << (mp - 1)) - 1u) | (1u << 16)) : 0u;
-    for (int idx = tid; idx < kHHFloats; idx += kStatsThreads) {
-        const uint32_t dcd = kDecode.trip[idx];
-        const uint32_t i = (dcd >> 16) & 31u, j = (dcd >> 21) & 31u, l = dcd >> 26;
-        float v = 0.f;
-        if (l < 17u && ((realm >> i) & (realm >> j) & (realm >> l) & 1u))
-            v = hterm(sm.pUp[dcd & 255u] + sm.pDn[(dcd >> 8) & 255u]);
-        tb[kTblHH + idx] = v;
+    // the hh and D tables in 16-byte pieces: rows are padded to multiples of
+    // 4, so the 4 entries of a piece share one row -- i and j (hh) or j (D),
+    // with l = l0 .. l0+3 and consecutive pair indices
+    constexpr int kHHq = kHHFloats / 4, kDq = kDpFloats / 4;
+    for (int q = tid; q < kHHq + kDq; q += kStatsThreads) {
+        float v[4];
+        if (q < kHHq) {
+            const uint32_t dcd = kDecode.trip[4 * q];
+            const uint32_t i = (dcd >> 16) & 31u, j = (dcd >> 21) & 31u, l0 = dcd >> 26;
+            const bool ij = ((realm >> i) & (realm >> j) & 1u) != 0u;
+            const float up = sm.pUp[dcd & 255u];
+            const uint32_t pj = (dcd >> 8) & 255u;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t l = l0 + (uint32_t)k;
+                v[k] = 0.f;
+                if (ij && l < 17u && ((realm >> l) & 1u))
+                    v[k] = hterm(up + sm.pDn[min(pj + (uint32_t)k, (uint32_t)kPairs - 1u)]);
+            }
+            *reinterpret_cast<float4 *>(tb + kTblHH + 4 * q) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+            const int r = q - kHHq;
+            const uint32_t dcd = kDecode.pair[4 * r];
+            const int j = dcd & 255, l0 = dcd >> 8;
+            const int base = l0 < 17 ? pidx(j, l0) : 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                v[k] = l0 + k < 17 ? sm.pDp[min(base + k, kPairs - 1)] : __int_as_float(0x7f800000);
+            *reinterpret_cast<float4 *>(tb + kTblD + 4 * r) = make_float4(v[0], v[1], v[2], v[3]);
+        }
     }
     if (tid < 20) {
         const int t = tid;
