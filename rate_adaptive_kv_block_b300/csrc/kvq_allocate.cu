@@ -160,6 +160,7 @@ __global__ void ctrl_init_kernel(Ctrl *c, const StatsHeader *hdr, double budget,
     c->t_start = c->t_end = 0ull;
     c->wait_ns = wait_ns;
     c->spin_limit = spin_limit;
+    c->phase1 = c->s.phase;
     for (int i = 0; i < 16; ++i) c->t_dp[i] = c->t_ctl[i] = 0ull;
 }
 
@@ -911,8 +912,9 @@ __device__ __noinline__ void round_control(Ctrl *ctrl, bool walk, int iter, int 
     __syncwarp();
     if (!dry) {
         if (L == 0) {
+            ctrl->phase1 = S.phase;
             if (!sC.fixed && S.xb_probe >= 0) ctrl->Rxb_fx = Rfx[S.xb_probe];
-            ctrl->cnt[round & 1] = 0u;     // consumed; the next round appends here
+            ctrl->cnt[iter & 1] = 0u;      // consumed; the next round appends here
             ctrl->ticket = 0u;
             ctrl->fin_avail = sC.fin_tail;  // every queue append of this round is in
         }
@@ -1003,30 +1005,38 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
     }
 
     if (blockIdx.x == 0 && threadIdx.x == 0) ctrl->t_start = global_ns();
+    // CTA 0 takes no items in the search's rounds (round_control): item it
+    // goes to CTA 1 + it mod (grid - 1)
+    const bool warm = !ctrl->fixed && gridDim.x > 1;
+    const int64_t cta = warm ? (int64_t)blockIdx.x - 1 : (int64_t)blockIdx.x;
+    const int64_t ncta = warm ? (int64_t)gridDim.x - 1 : (int64_t)gridDim.x;
     for (int iter = 0; iter < kMaxRounds; ++iter) {
+        // the candidate lists alternate by round; this thread's first item of
+        // a walk round is fetched while the control block is staged
+        const int32_t *lin = list + (size_t)(iter & 1) * nb;
+        int32_t *lout = list + (size_t)((iter + 1) & 1) * nb;
+        const int64_t it0 = cta + ncta * (int64_t)threadIdx.x;
+        const int32_t b0 = (iter > 0 && cta >= 0 && it0 < nb) ? __ldcg(&lin[it0]) : 0;
         stage_ctrl(sC, ctrl);
         if (threadIdx.x == 0) sAct = 0u;
         __syncthreads();
-        if (sC.s.phase == kSearchDone) break;
-        const int fixed = sC.fixed, phase = sC.s.phase;
+        // The other CTAs have acquired only the control's first publication:
+        // its second may be landing while they stage, so they take the round
+        // kind from phase1 (a walk that ends reaches them as the second
+        // publication, below).  CTA 0 reads the state it wrote itself.
+        const int phase = blockIdx.x == 0 ? sC.s.phase : sC.phase1;
+        if (phase == kSearchDone) break;
+        const int fixed = sC.fixed;
         const int xa_probe = sC.s.xa_probe, xb_probe = sC.s.xb_probe;
         const int round = sC.s.rounds;
         const bool walk = !fixed && phase == kSearchWalk;
         const bool pilot = !fixed && phase == kSearchPilot;
         const int stride = sC.s.pilot_stride;
-        const int32_t *lin = list + (size_t)(round & 1) * nb;
-        int32_t *lout = list + (size_t)((round + 1) & 1) * nb;
-        const int64_t nitems = walk ? (int64_t)sC.cnt[round & 1]
+        const int64_t nitems = walk ? (int64_t)sC.cnt[iter & 1]
                                     : pilot ? (int64_t)sC.s.pilot_blocks : nb;
         float lam = ready ? (float)(fixed ? sC.lambda_fixed : search_probe(sC.s, lane)) : 0.f;
         long long my_sum = 0;
         bool done = false;
-        // CTA 0 takes no items in the search's rounds: while the other CTAs
-        // evaluate, it runs the control once with a stand-in for the sums
-        // (round_control), so the real control finds its code cached
-        const bool warm = !fixed && gridDim.x > 1;
-        const int64_t cta = warm ? (int64_t)blockIdx.x - 1 : (int64_t)blockIdx.x;
-        const int64_t ncta = warm ? (int64_t)gridDim.x - 1 : (int64_t)gridDim.x;
         // Items in chunks of one per thread: item it = cta + ncta * (c *
         // blockDim.x + threadIdx.x), so consecutive CTAs take consecutive
         // items.  Phase A (a thread per item) carries the walk's per-block
@@ -1045,7 +1055,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                     // window ends; the rate is non-increasing in lambda, so
                     // equal rates at both ends mean the chain is constant
                     // inside the window
-                    const int32_t b = __ldcg(&lin[it]);
+                    const int32_t b = c0 == 0 ? b0 : __ldcg(&lin[it]);
                     float ra = __ldcg(&rate_lo[b]), rb = __ldcg(&rate_hi[b]);
                     if (xa_probe >= 0) ra = __ldcg(&rates[(int64_t)b * 32 + xa_probe]);
                     if (xb_probe >= 0) {
@@ -1091,7 +1101,7 @@ search_kernel(const float *__restrict__ tables, int64_t nb, int s, Ctrl *__restr
                 const uint32_t am = __ballot_sync(0xffffffffu, act);
                 lrank = __popc(am & ((1u << lane) - 1u));
                 if (lane == 0 && am)
-                    lbase = atomicAdd(&ctrl->cnt[(round + 1) & 1], (uint32_t)__popc(am));
+                    lbase = atomicAdd(&ctrl->cnt[(iter + 1) & 1], (uint32_t)__popc(am));
                 lbase = __shfl_sync(0xffffffffu, lbase, 0);
             }
             __syncthreads();

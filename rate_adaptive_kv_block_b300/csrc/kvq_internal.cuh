@@ -182,7 +182,10 @@ struct alignas(16) Ctrl {
     unsigned long long t_start, t_end, t_dp[16], t_ctl[16];
     unsigned long long wait_ns;    // limit of each grid hand-over wait
     uint32_t spin_limit;           // and of its polls
-    uint32_t pad_w;
+    // the search phase as of a control's first publication (the round kind
+    // the other CTAs act on); the second publication does not change it, so
+    // a CTA that has only seen the first never reads a phase the walk set
+    int32_t phase1;
 };
 static_assert(sizeof(Ctrl) % 16 == 0, "control block in 16-byte pieces");
 constexpr double kRateScale = 1048576.0;   // 2^20
