@@ -6,11 +6,11 @@
 // One CTA of 256 threads per block.  The block's binary16 entries are read
 // once from HBM with 16-byte loads; their order-preserving 16-bit keys stay in
 // registers.  Order statistics come from a two-level radix select:
-//   pass 1  each warp histograms its own entries by the key's high byte into a
-//           private 256-bin table: one 32-bit shared atomic adds
-//           (1 << 22) | j (count in bits 22..31, sum of the low byte j in
-//           0..21; a warp holds at most 512 entries, so neither field can
-//           overflow) and a second adds j^2.  The 8 tables are merged per bin;
+//   pass 1  each half of the CTA (4 warps) histograms its entries by the key's
+//           high byte into its own 256-bin table: one 32-bit shared atomic
+//           adds (1 << 20) | j (count in bits 20..31, sum of the low byte j in
+//           0..19; a half holds at most 2048 entries, so neither field can
+//           overflow) and a second adds j^2.  The 2 tables are merged per bin;
 //   scan    bin prefix counts locate the bin of each of the 17 ranks;
 //   pass 2  entries of those (<= 17) bins count their low byte in a second
 //           histogram (two 16-bit counters per 32-bit word);
@@ -32,12 +32,13 @@ namespace kvq {
 
 constexpr int kStatsThreads = 256;
 constexpr int kStatsWarps = kStatsThreads / 32;
+constexpr int kHistTables = 2;      // first-pass histograms, one per 4 warps
 
 struct StatsSmem {
     union {
         struct {
-            uint32_t h1a[kStatsWarps][256];   // per warp: (count << 22) | sum j
-            uint32_t h1b[kStatsWarps][256];   // per warp: sum j^2
+            uint32_t h1a[kHistTables][256];   // per half of the CTA: (count << 20) | sum j
+            uint32_t h1b[kHistTables][256];   // per half of the CTA: sum j^2
         };
         struct {
             uint32_t l2[17][128];             // after the merge: low-byte counts
@@ -56,7 +57,7 @@ struct StatsSmem {
     uint32_t dp1[17], dp2[17];
     float dc[17];
     int32_t mprime, nslots;
-    float an[16], as1[16], at1[16], ae[16];
+    float4 atom[16];                  // per atom: n, s1, t1, e
     float pDp[kPairs], pUp[kPairs], pDn[kPairs];   // pair tables, slot space
 };
 
@@ -137,7 +138,7 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
     // zero the tables while the loads are in flight
     {
         uint4 *z = reinterpret_cast<uint4 *>(&sm.h1a[0][0]);
-        for (int i = tid; i < 2 * kStatsWarps * 256 / 4; i += kStatsThreads) z[i] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < 2 * kHistTables * 256 / 4; i += kStatsThreads) z[i] = make_uint4(0, 0, 0, 0);
         if (tid < kPairs) {
             sm.pDp[tid] = __int_as_float(0x7f800000);   // +inf: no such pair
             sm.pUp[tid] = 0.f;
@@ -146,8 +147,9 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
     }
     __syncthreads();
 
-    // ---- keys (two per register) and pass 1 into the warp's own table
+    // ---- keys (two per register) and pass 1 into the half's table
     uint32_t keys[UNITS][4];
+    const int ht = warp / (kStatsWarps / kHistTables);
 #pragma unroll
     for (int k = 0; k < UNITS; ++k) {
         const int u = tid + k * kStatsThreads;
@@ -159,24 +161,24 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
             if (u < units) {
                 const uint32_t b0 = (kk >> 8) & 255u, j0 = kk & 255u;
                 const uint32_t b1 = kk >> 24, j1 = (kk >> 16) & 255u;
-                atomicAdd(&sm.h1a[warp][b0], (1u << 22) | j0);
-                atomicAdd(&sm.h1b[warp][b0], j0 * j0);
-                atomicAdd(&sm.h1a[warp][b1], (1u << 22) | j1);
-                atomicAdd(&sm.h1b[warp][b1], j1 * j1);
+                atomicAdd(&sm.h1a[ht][b0], (1u << 20) | j0);
+                atomicAdd(&sm.h1b[ht][b0], j0 * j0);
+                atomicAdd(&sm.h1a[ht][b1], (1u << 20) | j1);
+                atomicAdd(&sm.h1b[ht][b1], j1 * j1);
             }
         }
     }
     __syncthreads();
 
-    // ---- merge the warp tables (thread = bin), prefix counts, rank -> bin
+    // ---- merge the two tables (thread = bin), prefix counts, rank -> bin
     int cnt = 0;
     uint32_t S1 = 0, S2 = 0;
 #pragma unroll
-    for (int w = 0; w < kStatsWarps; ++w) {
-        const uint32_t a = sm.h1a[w][tid];
-        cnt += (int)(a >> 22);
-        S1 += a & 0x3fffffu;
-        S2 += sm.h1b[w][tid];
+    for (int h = 0; h < kHistTables; ++h) {
+        const uint32_t a = sm.h1a[h][tid];
+        cnt += (int)(a >> 20);
+        S1 += a & 0xfffffu;
+        S2 += sm.h1b[h][tid];
     }
     sm.cnt[tid] = cnt;
     sm.s1[tid] = S1;
@@ -186,7 +188,7 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
     sm.bu[tid] = bin_ulp((uint32_t)tid);
     int total;
     const int pre = block_excl_scan(cnt, sm.warp_tot, total);
-    // every warp table has been read: its memory becomes the low-byte table
+    // both tables have been read: their memory becomes the low-byte table
     {
         uint4 *z2 = reinterpret_cast<uint4 *>(&sm.l2[0][0]);
         for (int i = tid; i < 17 * 128 / 4; i += kStatsThreads) z2[i] = make_uint4(0, 0, 0, 0);
@@ -407,12 +409,7 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
             at1 += __shfl_down_sync(0xffffffffu, at1, o, 16);
             ae += __shfl_down_sync(0xffffffffu, ae, o, 16);
         }
-        if (sub == 0 && p < 16) {
-            sm.an[p] = an;
-            sm.as1[p] = as1;
-            sm.at1[p] = at1;
-            sm.ae[p] = ae;
-        }
+        if (sub == 0 && p < 16) sm.atom[p] = make_float4(an, as1, at1, ae);
     }
     __syncthreads();
 
@@ -436,7 +433,8 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
         const float a = sm.dc[P], bq = sm.dc[Q];
         float Dv = 0.f, Us = 0.f, Ls = 0.f;
         for (int p = P; p < Q; ++p) {
-            const float n = sm.an[p], s1 = sm.as1[p], t1 = sm.at1[p], e = sm.ae[p];
+            const float4 at = sm.atom[p];
+            const float n = at.x, s1 = at.y, t1 = at.z, e = at.w;
             const float A = sm.dc[p] - a, Bq = bq - sm.dc[p + 1];
             Dv += n * A * Bq + A * t1 + Bq * s1 + e;
             Us += s1 + n * A;
@@ -462,10 +460,10 @@ stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr
         else if (tid == 17) v = __int_as_float(mp);
         else if (tid == 18) v = __int_as_float(bad ? kFlagNonfinite : 0);
         else if (tid == 19) v = __int_as_float(d);
-        else if (tid < 36) v = sm.an[tid - 20];
-        else if (tid < 52) v = sm.as1[tid - 36];
-        else if (tid < 68) v = sm.at1[tid - 52];
-        else if (tid < 84) v = sm.ae[tid - 68];
+        else if (tid < 36) v = sm.atom[tid - 20].x;
+        else if (tid < 52) v = sm.atom[tid - 36].y;
+        else if (tid < 68) v = sm.atom[tid - 52].z;
+        else if (tid < 84) v = sm.atom[tid - 68].w;
         rec[tid] = v;
     }
     float *tb = rec + kRecTbl;
