@@ -432,7 +432,7 @@ def entropy_bench(w, L, x, buf, flush_l2, graph_of, device_ms, t_flush, nrep, de
 
 def attention_bench(w, L, buf, flush_l2, graph_of, device_ms, t_flush, nrep, hbm, src, dev):
     """kvq_decode_attention on the quantized layer, L2 flushed before every
-    launch: its time (median of single graph replays), the bytes it must read
+    launch: its time (by subtraction of flush-only replays), the bytes it must read
     (codes, codebooks, queries) and the fraction of the HBM roofline;
     PyTorch's attention on the binary16 decode of the same cache, timed the
     same way, for comparison."""
@@ -454,27 +454,17 @@ def attention_bench(w, L, buf, flush_l2, graph_of, device_ms, t_flush, nrep, hbm
     def run():
         kvq.kvq_decode_attention(qa, n_rep, L_kv, kc, kcb, vc, vcb, w.T, scale, ws, out)
 
-    # a kernel this short is timed on its own: the L2 flush, then events
-    # around one replay of a graph of the call alone; the median over the
-    # replays (subtracting two flush-dominated graph times is too noisy here)
-    stream = torch.cuda.current_stream()
-
+    # a call this short is timed by subtraction over many replays: a graph of
+    # (L2 flush, call) and a graph of the flush alone, each replayed 200
+    # times between events, five times over; the median of the differences
+    # (events around one short replay move in 2.048 us steps on this GPU)
     def median_cold_ms(fn, n):
-        gk = graph_of(fn)
-        ts = []
-        for i in range(n + 3):
-            flush_l2(i)
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            gk.replay()
-            b.record(stream)
-            torch.cuda.synchronize()
-            if i >= 3:
-                ts.append(a.elapsed_time(b))
-        ts.sort()
+        gf = graph_of(lambda: flush_l2(0))
+        gk = graph_of(lambda: (flush_l2(0), fn()))
+        device_ms(gk, 3)
+        ts = sorted(device_ms(gk, n) - device_ms(gf, n) for _ in range(5))
         return ts[len(ts) // 2]
-    t_att = median_cold_ms(run, max(nrep, 30))
+    t_att = median_cold_ms(run, 200)
     nbytes = 2 * half * 16 * w.G + 2 * half * 64 + 2 * qa.numel() * 4
     res = {"what": "one decoding step: %d query heads, %d KV heads x %d tokens x %d, read from "
                    "the 4-bit codes" % (S_kv * n_rep, S_kv, w.T, D),
@@ -493,7 +483,7 @@ def attention_bench(w, L, buf, flush_l2, graph_of, device_ms, t_flush, nrep, hbm
         def sdpa():
             ref["o"] = F.scaled_dot_product_attention(qh, Kf, Vf, scale=scale, enable_gqa=True)
         sdpa()
-        t_sdpa = median_cold_ms(sdpa, max(nrep, 30))
+        t_sdpa = median_cold_ms(sdpa, 200)
         run()
         torch.cuda.synchronize()
         diff = (ref["o"].view(-1, D).float() - out).abs().max().item()

@@ -79,9 +79,6 @@ attn_partial_kernel(const float *__restrict__ q, const uint8_t *__restrict__ kc,
     const int split = blockIdx.x, nsplit = gridDim.x;
     const int nG = D / G;
     const int64_t ntb_valid = (T_valid + 31) / 32;
-    // the combine launch may be scheduled now; it waits for this grid to
-    // finish before it reads anything (programmatic dependent launch)
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t tb0 = (int64_t)split * bps;
     const int64_t tb1 = min(tb0 + bps, ntb_valid);
     const int nchunks = tb1 > tb0 ? (int)((tb1 - tb0 + chunk - 1) / chunk) : 0;
@@ -310,9 +307,6 @@ attn_combine_kernel(const float *__restrict__ part, int nsplit, float *__restric
     __shared__ float sM;
     const int hq = blockIdx.x, f = threadIdx.x;
     const float NEG = __int_as_float(0xff800000);
-    // launched as a programmatic dependent of the partial kernel: wait until
-    // that grid has finished and its writes are visible
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float *base = part + (int64_t)hq * nsplit * (D + 2);
     float o[kAttnMaxSplits];
 #pragma unroll
@@ -414,21 +408,7 @@ int launch_decode_attention(const float *q, int n_rep, const kvq_layout &L, cons
         }
         if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
     }
-    // the combine as a programmatic dependent launch: its CTAs are scheduled
-    // while the partial kernel runs and wait in griddepcontrol.wait, so the
-    // launch gap between the two kernels is hidden
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(H * n_rep));
-    cfg.blockDim = dim3(kAttnD);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, attn_combine_kernel, (const float *)part, nsplit, out) != cudaSuccess)
-        return KVQ_ERR_CUDA;
+    attn_combine_kernel<<<(unsigned)(H * n_rep), kAttnD, 0, st>>>(part, nsplit, out);
     return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
