@@ -454,3 +454,42 @@ def test_encode_host_empty_layout_and_skipped_outputs():
     kvq.kvq_encode_host(xh, L, 16, 100.0, 0, 0, xd, buf, status)
     torch.cuda.synchronize()
     assert status.tolist() == [0, 0, 0] and float(buf.totals[0].item()) == 0.0
+
+
+def test_encode_host_in_a_cuda_graph():
+    """kvq_encode_host captured in a CUDA graph (its copy streams join the
+    capture through events) and replayed on new host data gives the eager
+    call's outputs byte for byte."""
+    _need_gpu()
+    w = synth.workload("llama3_8b_layer", T=512)
+    L = kvq.Layout(w.S, w.T, w.D, w.G)
+    B = w.budgets[0] * w.entries
+    x0 = synth.make_numpy(w, seed=21)
+    xh = torch.from_numpy(x0.view(np.int16)).view(torch.float16).pin_memory()
+    xd = torch.empty(x0.shape, dtype=torch.float16, device="cuda")
+    buf = kvq.Buffers(L, w.s)
+    status = torch.zeros(3, dtype=torch.int32, device="cuda")
+    outs = dict(codes=torch.empty(buf.codes.shape, dtype=torch.uint8).pin_memory(),
+                codebook=torch.empty(buf.codebook.shape, dtype=torch.float32).pin_memory(),
+                k=torch.empty(buf.k.shape, dtype=torch.uint8).pin_memory(),
+                totals=torch.empty(3, dtype=torch.float64).pin_memory())
+
+    def call(stream=None):
+        kvq.kvq_encode_host(xh, L, w.s, B, 9, 0, xd, buf, status, outs["codes"], outs["codebook"],
+                            outs["k"], outs["totals"], stream=stream)
+    call()                                   # first call outside the capture (set-up)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for sd in (22, 23):
+        xn = synth.make_numpy(w, seed=sd)
+        xh.copy_(torch.from_numpy(xn.view(np.int16)).view(torch.float16))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = {k: v.clone() for k, v in outs.items()}
+        ref = kvq.quantize(gc.to_dev(xn), L, B, w.s, seed=9)
+        torch.cuda.synchronize()
+        assert status.tolist() == [0, 0, 0]
+        for key in ("codes", "codebook", "k", "totals"):
+            assert torch.equal(got[key].view(torch.uint8), getattr(ref, key).cpu().view(torch.uint8)), key
