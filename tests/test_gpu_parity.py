@@ -63,6 +63,31 @@ def test_stats_edge_blocks():
     assert ora["mprime"][0] == 1 and ora["mprime"][1] == 2
 
 
+def _boundary_tensor(nb=96, seed=7):
+    """Blocks whose entries take a few keys each, at the edges of 8-key
+    chunks and of 256-key bins (low bytes 0, 1, 7, 8, .., 255), in one to five
+    bins, with skewed frequencies: several ranks share a bin or a key, and
+    ranks land on chunk and bin edges."""
+    r = np.random.default_rng(seed)
+    lows = np.array([0, 1, 7, 8, 9, 15, 16, 31, 32, 127, 128, 200, 247, 248, 254, 255])
+    out = np.empty((nb, 32, 128), dtype=np.uint16)
+    for b in range(nb):
+        bins = r.choice(np.arange(8, 248), size=int(r.integers(1, 6)), replace=False)
+        keys = (bins[:, None] * 256 + lows[None, :]).ravel()
+        k = r.choice(keys, size=32 * 128, p=r.dirichlet(np.full(keys.size, 0.3)))
+        bits = np.where(k & 0x8000, k & 0x7fff, ~k & 0xffff).astype(np.uint16)   # key -> binary16
+        out[b] = bits.reshape(32, 128)
+    return out
+
+
+def test_stats_ranks_on_chunk_and_bin_edges():
+    _need_gpu()
+    x = _boundary_tensor()
+    g = gc.run(x, 128, 16, 2.0 * x.size)
+    gc.check_stats(g, oracle.stats(x, 128))
+    assert g["status_stats"] == 0
+
+
 # --------------------------------------------------- quantize / dequantize
 
 @pytest.mark.parametrize("name,T,G", [("llama3_8b_layer", 512, 128), ("hadamard_groups", 256, 32)])
