@@ -168,12 +168,17 @@ stats_weight_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt
     __syncthreads();
 
     // weighted distortion of every candidate pair, in slot space (the maximum
-    // in slot 16), every term non-negative
+    // in slot 16), every term non-negative; pairs in order of decreasing
+    // length Q - P, so that a warp's threads run loops of similar length:
+    // thread t takes the P-th of the u pairs of length m' - u,
+    // u(u-1)/2 <= t < u(u+1)/2
     const int npr = mp * (mp - 1) / 2;
     if (tid < npr) {
-        int P = 0, rem = tid;
-        while (rem >= mp - 1 - P) { rem -= mp - 1 - P; ++P; }
-        const int Q = P + 1 + rem;
+        int u = (int)((1.0f + sqrtf(1.0f + 8.0f * (float)tid)) * 0.5f);
+        if (u * (u - 1) / 2 > tid) --u;
+        if ((u + 1) * u / 2 <= tid) ++u;
+        const int P = tid - u * (u - 1) / 2;
+        const int Q = P + mp - u;
         const float a = sc[P], bq = sc[Q];
         float Dv = 0.f;
         for (int p = P; p < Q; ++p) {
@@ -187,10 +192,15 @@ stats_weight_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wt
 
     const bool wbad = s_wbad != 0u;
     const int addf = kFlagWeighted | (wbad ? kFlagBadWeight : 0);
-    for (int idx = tid; idx < kDpFloats; idx += kWThreads) {
-        const uint32_t dcd = kDecode.pair[idx];
-        const int j = dcd & 255, l = dcd >> 8;
-        tb[kTblD + idx] = l < 17 ? pD[pidx(j, l)] : inf;
+    // the D table in 16-byte pieces (a padded row piece shares j)
+    if (tid < kDpFloats / 4) {
+        const uint32_t dcd = kDecode.pair[4 * tid];
+        const int j = dcd & 255, l0 = dcd >> 8;
+        const int base = l0 < 17 ? pidx(j, l0) : 0;
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = l0 + k < 17 ? pD[min(base + k, kPairs - 1)] : inf;
+        *reinterpret_cast<float4 *>(tb + kTblD + 4 * tid) = make_float4(v[0], v[1], v[2], v[3]);
     }
     if (tid >= 20 && tid < 84) {
         const int q = (tid - 20) >> 4, p = (tid - 20) & 15;
