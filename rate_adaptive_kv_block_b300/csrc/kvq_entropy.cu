@@ -91,6 +91,36 @@ __device__ __forceinline__ void stage16(uint4 *__restrict__ dst, const uint4 *__
     }
 }
 
+// Counts of the 16 symbols over a warp: each lane counts its n <= 128
+// symbols in four registers of four 8-bit counters (symbol c adds 1 to byte
+// c & 3 of register c >> 2), then the counts go to eight registers of two
+// 16-bit counters (a warp's count is at most 4096) for the warp sum.
+template <typename SymAt>
+__device__ __forceinline__ void warp_counts(int n, SymAt sym_at, uint32_t (&cnt)[16]) {
+    uint32_t pk[4] = {0u, 0u, 0u, 0u};
+    for (int j = 0; j < n; ++j) {
+        const uint32_t c = sym_at(j);
+        const uint32_t inc = 1u << ((c & 3u) << 3);
+        const uint32_t g = c >> 2;
+        pk[0] += g == 0u ? inc : 0u;
+        pk[1] += g == 1u ? inc : 0u;
+        pk[2] += g == 2u ? inc : 0u;
+        pk[3] += g == 3u ? inc : 0u;
+    }
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t w = pk[k >> 1] >> ((k & 1) * 16);        // counters 2k, 2k+1
+        h[k] = (w & 0xffu) | ((w & 0xff00u) << 8);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) h[k] += __shfl_xor_sync(0xffffffffu, h[k], o);
+#pragma unroll
+    for (int t = 0; t < 16; ++t) cnt[t] = (h[t >> 1] >> ((t & 1) * 16)) & 0xffffu;
+}
+
 __global__ void __launch_bounds__(kEntWarps * 32)
 entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
                       uint8_t *__restrict__ out, uint32_t *__restrict__ nbytes) {
@@ -108,18 +138,10 @@ entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     __syncwarp();
     // the block's counts (lane-private, then a warp sum)
     uint32_t cnt[16];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) cnt[c] = 0;
-    for (int j = 0; j < n; ++j) {
+    warp_counts(n, [&](int j) {
         const int e = lane + 32 * j;
-        const uint32_t c = (cb[e >> 1] >> ((e & 1) * 4)) & 15u;
-#pragma unroll
-        for (int t = 0; t < 16; ++t) cnt[t] += (c == (uint32_t)t) ? 1u : 0u;
-    }
-#pragma unroll
-    for (int t = 0; t < 16; ++t)
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cnt[t] += __shfl_xor_sync(0xffffffffu, cnt[t], o);
+        return (uint32_t)((cb[e >> 1] >> ((e & 1) * 4)) & 15u);
+    }, cnt);
     uint32_t cum[17];
     cum[0] = 0;
 #pragma unroll
@@ -338,17 +360,7 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     for (int bi = 0; bi < m; ++bi) {
         const uint8_t *cb = scodes + bi * half;
         uint32_t cnt[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) cnt[t] = 0;
-        for (int j = 0; j < n; ++j) {
-            const uint32_t c = nibble_at(cb, lane + 32 * j);
-#pragma unroll
-            for (int t = 0; t < 16; ++t) cnt[t] += (c == (uint32_t)t) ? 1u : 0u;
-        }
-#pragma unroll
-        for (int t = 0; t < 16; ++t)
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) cnt[t] += __shfl_xor_sync(0xffffffffu, cnt[t], o);
+        warp_counts(n, [&](int j) { return nibble_at(cb, lane + 32 * j); }, cnt);
         if (lane < 16) {
             uint32_t f = 0, bc = 0, acc = 0;
 #pragma unroll
