@@ -176,10 +176,16 @@ entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
         const uint32_t f = md.x, bc = md.y;
         const Recip r{md.z, md.w};
         const uint32_t xmax = ((kRansL >> lg) << 8) * f;
-        while (x >= xmax) {
-            buf[--pos] = (uint8_t)(x & 255u);
-            x >>= 8;
-        }
+        // at most two bytes leave per symbol (x < 2^31, xmax >= 2^19): two
+        // predicated steps instead of a loop whose trip count differs by lane
+        const bool e1 = x >= xmax;
+        if (e1) buf[pos - 1] = (uint8_t)(x & 255u);
+        pos -= e1 ? 1 : 0;
+        x = e1 ? x >> 8 : x;
+        const bool e2 = x >= xmax;
+        if (e2) buf[pos - 1] = (uint8_t)(x & 255u);
+        pos -= e2 ? 1 : 0;
+        x = e2 ? x >> 8 : x;
         const uint32_t qd = div_by(x, r);
         x = (qd << lg) + (x - qd * f) + bc;
     }
@@ -391,10 +397,12 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
         const uint4 md = nxt;
         if (k > 0) nxt = model_at(k - 1);
         const uint32_t xmax = xmax0 * md.x;
-        while (x >= xmax) {
-            ++len;
-            x >>= 8;
-        }
+        // at most two bytes leave per symbol (x < 2^31, xmax >= 2^19)
+        const uint32_t e1 = x >= xmax ? 1u : 0u;
+        x >>= 8 * e1;
+        const uint32_t e2 = x >= xmax ? 1u : 0u;
+        x >>= 8 * e2;
+        len += e1 + e2;
         const uint32_t qd = div_by(x, Recip{md.z, md.w});
         x = (qd << lg) + (x - qd * md.x) + md.y;
     }
@@ -419,10 +427,14 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
         const uint4 md = nxt;
         if (k > 0) nxt = model_at(k - 1);
         const uint32_t xmax = xmax0 * md.x;
-        while (x >= xmax) {
-            st[--pos] = (uint8_t)(x & 255u);
-            x >>= 8;
-        }
+        const bool e1 = x >= xmax;
+        if (e1) st[pos - 1] = (uint8_t)(x & 255u);
+        pos -= e1 ? 1u : 0u;
+        x = e1 ? x >> 8 : x;
+        const bool e2 = x >= xmax;
+        if (e2) st[pos - 1] = (uint8_t)(x & 255u);
+        pos -= e2 ? 1u : 0u;
+        x = e2 ? x >> 8 : x;
         const uint32_t qd = div_by(x, Recip{md.z, md.w});
         x = (qd << lg) + (x - qd * md.x) + md.y;
     }
