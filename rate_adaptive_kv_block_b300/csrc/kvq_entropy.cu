@@ -286,10 +286,17 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
             c = rans_symbol(cum, s);
             const uint32_t f = scnt[w][c], bc = cum[c];
             x = f * (x >> lg) + s - bc;
-            while (x < kRansL) {
-                if (p >= end) { overrun = true; break; }   // never reads past its stream
-                x = (x << 8) | slot[p++];
+            // a stream this coder wrote refills at most two bytes per symbol
+            // (the encoder's bound); never read past the stream
+            if (x < kRansL) {
+                if (p < end) x = (x << 8) | slot[p++];
+                else overrun = true;
             }
+            if (x < kRansL) {
+                if (p < end) x = (x << 8) | slot[p++];
+                else overrun = true;
+            }
+            if (x < kRansL) overrun = true;            // a third: not such a stream
         }
         sym[w][lane + 32 * j] = (uint8_t)c;
     }
@@ -520,10 +527,16 @@ entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, in
                 for (int t = 0; t < 15; ++t) c += bcum[t] <= s ? 1u : 0u;
                 const uint32_t e = scum[c];
                 x = (e >> 16) * (x >> lg) + s - (e & 0xffffu);
-                while (x < kRansL) {
-                    if (p >= end) { overrun = true; break; }   // never reads past its stream
-                    x = (x << 8) | sslot[p++];
+                // at most two refill bytes per symbol, as in the per-block decoder
+                if (x < kRansL) {
+                    if (p < end) x = (x << 8) | sslot[p++];
+                    else overrun = true;
                 }
+                if (x < kRansL) {
+                    if (p < end) x = (x << 8) | sslot[p++];
+                    else overrun = true;
+                }
+                if (x < kRansL) overrun = true;
             }
             const uint32_t hi = __shfl_xor_sync(0xffffffffu, c, 1);
             const int e = lane + 32 * j;
