@@ -109,7 +109,7 @@ __device__ __forceinline__ void add_piece(float v0, float u, int j0, int j1, uin
 }
 
 template <int UNITS>
-__global__ void __launch_bounds__(kStatsThreads, 6)
+__global__ void __launch_bounds__(kStatsThreads, 8)
 stats_kernel(const uint16_t *__restrict__ x, kvq_layout L, int lg_ng, int lg_upr,
              StatsHeader *__restrict__ hdr, float *__restrict__ recs,
              int32_t *__restrict__ status) {
