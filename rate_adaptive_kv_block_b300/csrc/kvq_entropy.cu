@@ -44,16 +44,6 @@ __host__ __device__ constexpr uint32_t entropy_slot_bytes(int d) {
 
 __device__ __forceinline__ int ilog2(int v) { return 31 - __clz(v); }
 
-// symbol of slot s: the c with b_c <= s < b_{c+1} (cum[0] = 0, cum[16] = d;
-// symbols with count 0 have b_c = b_{c+1} and are never found)
-__device__ __forceinline__ int rans_symbol(const uint32_t *cum, uint32_t s) {
-    int c = 0;
-#pragma unroll
-    for (int step = 8; step > 0; step >>= 1)
-        if (cum[c + step] <= s) c += step;
-    return c;
-}
-
 // x / f for x < 2^31 and 1 <= f <= 4096 by one 64-bit product: with
 // l = ceil(log2 f) and m = floor(2^(31+l) / f) + 1 (at most 32 bits),
 // floor(x m / 2^(31+l)) = floor(x / f) for every 31-bit x (Granlund and
@@ -229,9 +219,12 @@ entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
 __global__ void __launch_bounds__(kEntWarps * 32)
 entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
                       uint8_t *__restrict__ codes, int32_t *__restrict__ status) {
-    __shared__ uint8_t sym[kEntWarps][4096];
+    // per warp: the symbol of every slot s < d.  With exact counts the slot
+    // table is the block's symbols in symbol order (b_c .. b_{c+1} - 1 hold c),
+    // so one lookup replaces the search over the cumulative counts.
+    __shared__ __align__(16) uint8_t smap[kEntWarps][4096];
     __shared__ __align__(16) uint8_t sslot[kEntWarps][entropy_slot_bytes(4096)];
-    __shared__ uint32_t scum[kEntWarps][17], scnt[kEntWarps][16];
+    __shared__ uint32_t sent[kEntWarps][16];        // per symbol: b_c | f_c << 16
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t b = (int64_t)blockIdx.x * kEntWarps + w;
     if (b >= nb) return;
@@ -243,22 +236,17 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
             (int)(cap / 16), lane);
     __syncwarp();
     const uint8_t *slot = sslot[w];
-    // counts and cumulative counts in shared memory (lane t < 16 reads
-    // count t; a warp scan gives the cumulative counts)
-    uint32_t mycnt = lane < 16 ? ((uint32_t)slot[2 * lane] | ((uint32_t)slot[2 * lane + 1] << 8)) : 0u;
+    // counts and cumulative counts (lane t < 16 reads count t; a warp scan
+    // gives the cumulative counts)
+    const uint32_t mycnt = lane < 16 ? ((uint32_t)slot[2 * lane] | ((uint32_t)slot[2 * lane + 1] << 8)) : 0u;
     uint32_t incl = mycnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
     }
-    if (lane < 16) {
-        scnt[w][lane] = mycnt;
-        scum[w][lane] = incl - mycnt;
-    }
-    if (lane == 16) scum[w][16] = incl;            // lanes >= 16 add nothing: the total
-    __syncwarp();
-    const uint32_t *cum = scum[w];
+    const uint32_t nsym = __shfl_sync(0xffffffffu, incl, 15);
+    if (lane < 16) sent[w][lane] = (incl - mycnt) | (mycnt << 16);
     const uint32_t len = (uint32_t)slot[32 + 2 * lane] | ((uint32_t)slot[32 + 2 * lane + 1] << 8);
     uint32_t off = len;
 #pragma unroll
@@ -269,8 +257,28 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
     const uint32_t total = __shfl_sync(0xffffffffu, off, 31);
     off -= len;
     // a slot that does not describe a block of d symbols: status, codes 0
-    bool bad = cum[16] != (uint32_t)d || kEntHeader + total > cap || len < 4;
+    bool bad = nsym != (uint32_t)d || kEntHeader + total > cap || len < 4;
     bad = __any_sync(0xffffffffu, bad);
+    __syncwarp();
+    uint8_t *map = smap[w];
+    const uint32_t *ent = sent[w];
+    if (!bad) {
+        // symbol c fills slots [a, a + f): whole 4-byte words with the
+        // repeated byte, then at most three bytes at either end (every b_c
+        // and f_c is at most d <= 4096 once the counts sum to d)
+        uint32_t *m32 = reinterpret_cast<uint32_t *>(map);
+        for (int c = 0; c < 16; ++c) {
+            const uint32_t e = ent[c], a = e & 0xffffu, z = a + (e >> 16);
+            const uint32_t wa = (a + 3u) >> 2, wz = z >> 2;
+            for (uint32_t i = wa + (uint32_t)lane; i < wz; i += 32) m32[i] = (uint32_t)c * 0x01010101u;
+            if (lane < 6) {
+                const uint32_t q = lane < 3 ? a + (uint32_t)lane : z - 1u - (uint32_t)(lane - 3);
+                const uint32_t wq = q >> 2;
+                if (q >= a && q < z && !(wq >= wa && wq < wz)) map[q] = (uint8_t)c;
+            }
+        }
+    }
+    __syncwarp();
     uint32_t p = kEntHeader + off, end = p + len;
     uint32_t x = 0;
     if (!bad) {
@@ -279,13 +287,16 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
         p += 4;
     }
     bool overrun = false;
+    // entry lane + 32 j is the low nibble of code byte 16 j + lane / 2 when
+    // the lane is even, the high nibble of that byte when it is odd
+    uint8_t *cout = codes + b * (d / 2) + (lane >> 1);
     for (int j = 0; j < n; ++j) {
-        int c = 0;
+        uint32_t c = 0;
         if (!bad) {
             const uint32_t s = x & ((1u << lg) - 1u);
-            c = rans_symbol(cum, s);
-            const uint32_t f = scnt[w][c], bc = cum[c];
-            x = f * (x >> lg) + s - bc;
+            c = map[s];
+            const uint32_t e = ent[c];
+            x = (e >> 16) * (x >> lg) + s - (e & 0xffffu);
             // a stream this coder wrote refills at most two bytes per symbol
             // (the encoder's bound); never read past the stream
             if (x < kRansL) {
@@ -298,14 +309,11 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
             }
             if (x < kRansL) overrun = true;            // a third: not such a stream
         }
-        sym[w][lane + 32 * j] = (uint8_t)c;
+        const uint32_t hi = __shfl_xor_sync(0xffffffffu, c, 1);
+        if ((lane & 1) == 0) cout[16 * j] = (uint8_t)(c | (hi << 4));
     }
     overrun |= !bad && p != end;
     if (__any_sync(0xffffffffu, bad || overrun) && lane == 0) atomicMax(status, (int32_t)KVQ_ERR_CORRUPT);
-    __syncwarp();
-    uint8_t *cout = codes + b * (d / 2);
-    for (int i = lane; i < d / 2; i += 32)
-        cout[i] = (uint8_t)(sym[w][2 * i] | (sym[w][2 * i + 1] << 4));
 }
 
 // ------------------------------------------- runs of adjacent blocks
@@ -340,7 +348,7 @@ __host__ __device__ constexpr size_t run_enc_smem(int d, int nseg) {
     return (size_t)nseg * (16 * sizeof(uint4) + (size_t)(d / 2));
 }
 __host__ __device__ constexpr size_t run_dec_smem(int d, int nseg) {
-    return 144 + (size_t)(d / 2) + (size_t)run_slot_bytes(d, nseg);
+    return 144 + (size_t)(d / 2) + (size_t)run_slot_bytes(d, nseg) + 4 * (size_t)d;
 }
 constexpr size_t kRunSmemMax = run_enc_smem(4096, kRunMaxBlocks) > run_dec_smem(4096, kRunMaxBlocks)
                                    ? run_enc_smem(4096, kRunMaxBlocks)
@@ -465,6 +473,7 @@ entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, in
     const int half = d / 2;
     uint8_t *sslot = sout + half;                            // the run's slot
     const uint64_t cap = run_slot_bytes(d, nseg);
+    uint32_t *smap = reinterpret_cast<uint32_t *>(sslot + cap);   // one block's slot table
     const uint8_t *slot = in + rn * (int64_t)cap;
     const uint32_t hdr = 32u * (uint32_t)m + 64u;
     const uint32_t len = (uint32_t)slot[32 * m + 2 * lane] | ((uint32_t)slot[32 * m + 2 * lane + 1] << 8);
@@ -513,20 +522,24 @@ entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, in
         const uint32_t tot = __shfl_sync(0xffffffffu, incl, 15);
         const bool badm = __any_sync(0xffffffffu, tot != (uint32_t)d);
         bad = bad || badm;
-        // the cumulative counts b_1 .. b_15 in every lane's registers: the
-        // symbol of slot s is the number of them at or below s (the same c as
-        // the search over b: symbols with count 0 have b_c = b_{c+1})
-        uint32_t bcum[15];
-#pragma unroll
-        for (int t = 0; t < 15; ++t) bcum[t] = __shfl_sync(0xffffffffu, incl, t);
+        // this block's slot table: slot b_c + q (q < f_c) holds
+        // c << 28 | f_c << 13 | q, all that decoding a symbol there needs
+        // (exact counts: slots b_c .. b_{c+1} - 1 belong to symbol c; once
+        // the counts sum to d, every b_c + q is below d)
+        if (!bad) {
+            for (int c = 0; c < 16; ++c) {
+                const uint32_t e = scum[c], a = e & 0xffffu, f = e >> 16;
+                const uint32_t hi = ((uint32_t)c << 28) | (f << 13);
+                for (uint32_t q = (uint32_t)lane; q < f; q += 32) smap[a + q] = hi | q;
+            }
+        }
+        __syncwarp();
         for (int j = 0; j < n; ++j) {
             uint32_t c = 0;
             if (!bad && !overrun) {
-                const uint32_t s = x & ((1u << lg) - 1u);
-#pragma unroll
-                for (int t = 0; t < 15; ++t) c += bcum[t] <= s ? 1u : 0u;
-                const uint32_t e = scum[c];
-                x = (e >> 16) * (x >> lg) + s - (e & 0xffffu);
+                const uint32_t e = smap[x & ((1u << lg) - 1u)];
+                c = e >> 28;
+                x = ((e >> 13) & 0x1fffu) * (x >> lg) + (e & 0x1fffu);
                 // at most two refill bytes per symbol, as in the per-block decoder
                 if (x < kRansL) {
                     if (p < end) x = (x << 8) | sslot[p++];
