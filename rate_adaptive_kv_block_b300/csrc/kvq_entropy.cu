@@ -329,13 +329,16 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
 //   then the streams in lane order, each its final state (4 bytes) and its
 //   renormalisation bytes in the order the decoder reads them.
 // One warp per run and per CTA, so the runs spread over every SM.  The
-// encoder first stages the run's codes and models in shared memory, then
-// makes two passes over the run: the first only counts each stream's bytes,
-// the second writes them downwards from the stream's end (known from the
+// encoder first stages the run's codes and models in shared memory.  Its
+// pass over the run counts each stream's bytes and keeps them, up to 4 bits a
+// symbol and some slack, in shared memory; once a warp scan of the lengths
+// has placed the streams, the kept bytes go out last first.  Only when some
+// stream is longer than what it could keep does a second pass recompute the
+// chain and write the bytes downwards from the stream's end (known from the
 // first), so no worst-case scratch is held.  The decoder stages the run's
-// slot (as far as its stream lengths reach) and assembles each block's packed
-// codes in shared memory before one coalesced store.  Both serial per-lane
-// loops then touch shared memory only.
+// slot (as far as its stream lengths reach), builds each block's slot table
+// and assembles its packed codes in shared memory before one coalesced store.
+// Both serial per-lane loops then touch shared memory only.
 constexpr int kRunMaxBlocks = 32;
 
 __host__ __device__ constexpr uint64_t run_slot_bytes(int d, int nseg) {
@@ -343,9 +346,15 @@ __host__ __device__ constexpr uint64_t run_slot_bytes(int d, int nseg) {
     // stream its state and one byte of renormalisation slack
     return ((uint64_t)nseg * (uint64_t)(d / 2 + 32) + 64u + 32u * 6u + 15u) & ~(uint64_t)15u;
 }
+// bytes of one lane's stream the run encoder keeps from its first pass: 4
+// bits per symbol and some slack (a stream longer than that is written by a
+// second pass instead)
+__host__ __device__ constexpr uint32_t run_keep_bytes(int d, int nseg) {
+    return ((uint32_t)(d / 32) * (uint32_t)nseg / 2u + 64u + 15u) & ~15u;
+}
 // dynamic shared memory of the two kernels
 __host__ __device__ constexpr size_t run_enc_smem(int d, int nseg) {
-    return (size_t)nseg * (16 * sizeof(uint4) + (size_t)(d / 2));
+    return (size_t)nseg * (16 * sizeof(uint4) + (size_t)(d / 2)) + 32 * (size_t)run_keep_bytes(d, nseg);
 }
 __host__ __device__ constexpr size_t run_dec_smem(int d, int nseg) {
     return 144 + (size_t)(d / 2) + (size_t)run_slot_bytes(d, nseg) + 4 * (size_t)d;
@@ -397,16 +406,19 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     }
     __syncwarp();
     const uint32_t xmax0 = (kRansL >> lg) << 8;
-    // pass 1: the length of this lane's stream.  The symbols are taken last
-    // first, run position k = bi * n + j from m n - 1 down to 0; the next
-    // symbol's model entry does not depend on the state, so it is loaded one
-    // step ahead (the state's chain then holds only the arithmetic)
+    // pass 1: the length of this lane's stream, and its bytes in the order
+    // they leave (up to `keep` of them).  The symbols are taken last first,
+    // run position k = bi * n + j from m n - 1 down to 0; the next symbol's
+    // model entry does not depend on the state, so it is loaded one step
+    // ahead (the state's chain then holds only the arithmetic)
+    const uint32_t keep = run_keep_bytes(d, nseg);
+    uint8_t *kept = scodes + (size_t)nseg * half + (size_t)lane * keep;
     const int nk = m * n;
     auto model_at = [&](int k) {
         const int bi = k >> (lg - 5), j = k & (n - 1);     // n = d / 32, a power of two
         return smodel[bi * 16 + nibble_at(scodes + bi * half, lane + 32 * j)];
     };
-    uint32_t x = kRansL, len = 4;
+    uint32_t x = kRansL, nout = 0;
     uint4 nxt = model_at(nk - 1);
     for (int k = nk - 1; k >= 0; --k) {
         const uint4 md = nxt;
@@ -414,13 +426,17 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
         const uint32_t xmax = xmax0 * md.x;
         // at most two bytes leave per symbol (x < 2^31, xmax >= 2^19)
         const uint32_t e1 = x >= xmax ? 1u : 0u;
+        if (e1 && nout < keep) kept[nout] = (uint8_t)x;
+        nout += e1;
         x >>= 8 * e1;
         const uint32_t e2 = x >= xmax ? 1u : 0u;
+        if (e2 && nout < keep) kept[nout] = (uint8_t)x;
+        nout += e2;
         x >>= 8 * e2;
-        len += e1 + e2;
         const uint32_t qd = div_by(x, Recip{md.z, md.w});
         x = (qd << lg) + (x - qd * md.x) + md.y;
     }
+    const uint32_t len = nout + 4;
     uint32_t off = len;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -433,27 +449,32 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     slot[32 * m + 2 * lane] = (uint8_t)len;
     slot[32 * m + 2 * lane + 1] = (uint8_t)(len >> 8);
     if (lane == 0) nbytes[rn] = hdr + total;
-    // pass 2: the same steps, the bytes written downwards from the stream's end
     uint8_t *st = slot + hdr + off;
-    uint32_t pos = len;
-    x = kRansL;
-    nxt = model_at(nk - 1);
-    for (int k = nk - 1; k >= 0; --k) {
-        const uint4 md = nxt;
-        if (k > 0) nxt = model_at(k - 1);
-        const uint32_t xmax = xmax0 * md.x;
-        const bool e1 = x >= xmax;
-        if (e1) st[pos - 1] = (uint8_t)(x & 255u);
-        pos -= e1 ? 1u : 0u;
-        x = e1 ? x >> 8 : x;
-        const bool e2 = x >= xmax;
-        if (e2) st[pos - 1] = (uint8_t)(x & 255u);
-        pos -= e2 ? 1u : 0u;
-        x = e2 ? x >> 8 : x;
-        const uint32_t qd = div_by(x, Recip{md.z, md.w});
-        x = (qd << lg) + (x - qd * md.x) + md.y;
+    if (!__any_sync(0xffffffffu, nout > keep)) {
+        // every lane kept its bytes: the stream holds them last first
+        for (uint32_t i = 0; i < nout; ++i) st[4 + i] = kept[nout - 1 - i];
+    } else {
+        // pass 2: the same steps, the bytes written downwards from the stream's end
+        uint32_t pos = len;
+        x = kRansL;
+        nxt = model_at(nk - 1);
+        for (int k = nk - 1; k >= 0; --k) {
+            const uint4 md = nxt;
+            if (k > 0) nxt = model_at(k - 1);
+            const uint32_t xmax = xmax0 * md.x;
+            const bool e1 = x >= xmax;
+            if (e1) st[pos - 1] = (uint8_t)(x & 255u);
+            pos -= e1 ? 1u : 0u;
+            x = e1 ? x >> 8 : x;
+            const bool e2 = x >= xmax;
+            if (e2) st[pos - 1] = (uint8_t)(x & 255u);
+            pos -= e2 ? 1u : 0u;
+            x = e2 ? x >> 8 : x;
+            const uint32_t qd = div_by(x, Recip{md.z, md.w});
+            x = (qd << lg) + (x - qd * md.x) + md.y;
+        }
     }
-    st[0] = (uint8_t)x;          // pos == 4 here: the state opens the stream
+    st[0] = (uint8_t)x;          // the state opens the stream
     st[1] = (uint8_t)(x >> 8);
     st[2] = (uint8_t)(x >> 16);
     st[3] = (uint8_t)(x >> 24);

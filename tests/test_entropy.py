@@ -195,6 +195,49 @@ def test_run_coder_matches_oracle_and_round_trips(name, T, S, G, nseg):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("G,nseg,nb", [(128, 16, 40), (64, 4, 9)])
+def test_run_coder_with_one_stream_far_above_four_bits_a_symbol(G, nseg, nb):
+    """In the first run, stream 0 (entries 0, 32, 64, .. of each block) holds
+    only rare symbols, so it needs far more than 4 bits a symbol while the run
+    as a whole stays small; the other runs are ordinary.  Both kinds of run
+    equal the oracle's slots byte for byte and decode back."""
+    import torch
+    from rate_adaptive_kv_block_b300 import kvq
+    d = 32 * G
+    e = np.arange(d)
+    r = np.random.default_rng(11)
+    sym = np.empty((nb, d), dtype=np.uint8)
+    for b in range(nb):
+        if b < nseg:
+            sym[b] = np.where(e % 32 == 0, 1 + (e // 32 + b) % 15, 0)
+        else:
+            sym[b] = CASES["skewed"](r, d)
+    codes_np = _pack(sym)
+    want = oracle.entropy_encode_runs(codes_np, d, nseg)
+    n = d // 32
+    len0 = want[0][32 * nseg] | (want[0][32 * nseg + 1] << 8)
+    assert len0 - 4 > n * nseg // 2 + 79          # well above 4 bits a symbol
+    L = kvq.Layout(1, 32 * nb, G, G)
+    assert L.nblocks == nb
+    codes = torch.from_numpy(codes_np).cuda()
+    nruns = -(-nb // nseg)
+    cap = kvq.kvq_entropy_run_bytes(L, nseg)
+    out = torch.zeros((nruns, cap), dtype=torch.uint8, device="cuda")
+    nbytes = torch.zeros(nruns, dtype=torch.int32, device="cuda")
+    kvq.kvq_entropy_encode_runs(codes, L, nseg, out, nbytes)
+    back = torch.empty_like(codes)
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    kvq.kvq_entropy_decode_runs(out, L, nseg, back, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvq.KVQ_OK
+    assert torch.equal(back, codes)
+    got, sizes = out.cpu().numpy(), nbytes.cpu().numpy()
+    for rr in range(nruns):
+        assert sizes[rr] == len(want[rr])
+        assert bytes(got[rr, :sizes[rr]]) == want[rr]
+
+
+@pytest.mark.gpu
 def test_run_decode_reports_a_damaged_slot():
     import torch
     from rate_adaptive_kv_block_b300 import kvq, synth
