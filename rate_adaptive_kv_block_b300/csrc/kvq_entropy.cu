@@ -31,10 +31,11 @@ namespace kvq {
 constexpr uint32_t kRansL = 1u << 23;
 constexpr int kEntWarps = 4;
 constexpr int kEntHeader = 96;
-// per-lane scratch of the encoder: a symbol emits at most ceil(log2 d / 8)
-// <= 2 bytes (the state stays below 2^31 and the bound is 2^(31 - log2 d) f),
-// plus the 4-byte state
-constexpr int kEntLaneCap = 2 * (4096 / 32) + 8;
+// bytes of a stream the per-block encoder keeps from its first pass: 4 bits
+// a symbol of a 4096-entry block and 32 bytes of slack (a symbol emits at
+// most two bytes, so a longer stream exists; its block is written by a
+// second pass)
+constexpr int kEntKeep = 4096 / 32 / 2 + 32;
 
 __host__ __device__ constexpr uint32_t entropy_slot_bytes(int d) {
     // the payload is at most d * 4 bits (16 symbols) plus, per stream, the
@@ -114,7 +115,7 @@ __device__ __forceinline__ void warp_counts(int n, SymAt sym_at, uint32_t (&cnt)
 __global__ void __launch_bounds__(kEntWarps * 32)
 entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
                       uint8_t *__restrict__ out, uint32_t *__restrict__ nbytes) {
-    __shared__ uint8_t scratch[kEntWarps][32][kEntLaneCap];
+    __shared__ uint8_t scratch[kEntWarps][32][kEntKeep];
     __shared__ __align__(16) uint8_t sslot[kEntWarps][entropy_slot_bytes(4096)];
     __shared__ uint4 smodel[kEntWarps][16];        // per symbol: count, cumulative, reciprocal
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -139,52 +140,46 @@ entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     // the model, one entry per symbol in shared memory (lane t < 16: its
     // count, cumulative count and the count's reciprocal, a 64-bit division
     // once per block)
+    uint32_t myf = 0;                             // lane t < 16: count of symbol t
     if (lane < 16) {
-        uint32_t f = 0, bc = 0;
+        uint32_t bc = 0;
 #pragma unroll
         for (int t = 0; t < 16; ++t)
-            if (t == lane) { f = cnt[t]; bc = cum[t]; }
-        const Recip r = recip_of(f > 0 ? f : 1u);
-        smodel[w][lane] = make_uint4(f, bc, r.m, r.sh);
-    }
-    // the symbols of this lane's stream (the codes' buffer is reused for the
-    // slot below)
-    uint8_t mysym[4096 / 32];
-    for (int j = 0; j < n; ++j) {
-        const int e = lane + 32 * j;
-        mysym[j] = (cb[e >> 1] >> ((e & 1) * 4)) & 15;
+            if (t == lane) { myf = cnt[t]; bc = cum[t]; }
+        const Recip r = recip_of(myf > 0 ? myf : 1u);
+        smodel[w][lane] = make_uint4(myf, bc, r.m, r.sh);
     }
     __syncwarp();
-    // this lane's stream, last entry first, bytes written downwards
-    uint8_t *buf = scratch[w][lane];
-    int pos = kEntLaneCap;
-    uint32_t x = kRansL;
-    uint4 nxt = smodel[w][mysym[n - 1]];      // the next symbol's model, one step ahead
+    // this lane's stream, last entry first.  Its symbol j (entry lane + 32 j)
+    // is the nibble (lane & 1) of code byte 16 j + lane / 2, read from the
+    // staged codes.  The bytes that leave are kept in the order they leave
+    // (up to kEntKeep of them); the state's final value opens the stream and
+    // the decoder reads the bytes last first.
+    const uint8_t *mine = cb + (lane >> 1);
+    const int nsh = 4 * (lane & 1);
+    auto sym_at = [&](int j) { return (uint32_t)(mine[16 * j] >> nsh) & 15u; };
+    const uint32_t xmax0 = (kRansL >> lg) << 8;
+    uint8_t *kept = scratch[w][lane];
+    uint32_t nout = 0, x = kRansL;
+    uint4 nxt = smodel[w][sym_at(n - 1)];     // the next symbol's model, one step ahead
     for (int j = n - 1; j >= 0; --j) {
         const uint4 md = nxt;
-        if (j > 0) nxt = smodel[w][mysym[j - 1]];
-        const uint32_t f = md.x, bc = md.y;
-        const Recip r{md.z, md.w};
-        const uint32_t xmax = ((kRansL >> lg) << 8) * f;
+        if (j > 0) nxt = smodel[w][sym_at(j - 1)];
+        const uint32_t xmax = xmax0 * md.x;
         // at most two bytes leave per symbol (x < 2^31, xmax >= 2^19): two
         // predicated steps instead of a loop whose trip count differs by lane
-        const bool e1 = x >= xmax;
-        if (e1) buf[pos - 1] = (uint8_t)(x & 255u);
-        pos -= e1 ? 1 : 0;
-        x = e1 ? x >> 8 : x;
-        const bool e2 = x >= xmax;
-        if (e2) buf[pos - 1] = (uint8_t)(x & 255u);
-        pos -= e2 ? 1 : 0;
-        x = e2 ? x >> 8 : x;
-        const uint32_t qd = div_by(x, r);
-        x = (qd << lg) + (x - qd * f) + bc;
+        const uint32_t e1 = x >= xmax ? 1u : 0u;
+        if (e1 && nout < kEntKeep) kept[nout] = (uint8_t)x;
+        nout += e1;
+        x >>= 8 * e1;
+        const uint32_t e2 = x >= xmax ? 1u : 0u;
+        if (e2 && nout < kEntKeep) kept[nout] = (uint8_t)x;
+        nout += e2;
+        x >>= 8 * e2;
+        const uint32_t qd = div_by(x, Recip{md.z, md.w});
+        x = (qd << lg) + (x - qd * md.x) + md.y;
     }
-    pos -= 4;
-    buf[pos] = (uint8_t)x;
-    buf[pos + 1] = (uint8_t)(x >> 8);
-    buf[pos + 2] = (uint8_t)(x >> 16);
-    buf[pos + 3] = (uint8_t)(x >> 24);
-    const uint32_t len = (uint32_t)(kEntLaneCap - pos);
+    const uint32_t len = nout + 4;
     // offsets of the streams (exclusive scan over the lanes)
     uint32_t off = len;
 #pragma unroll
@@ -194,24 +189,66 @@ entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     }
     const uint32_t total = __shfl_sync(0xffffffffu, off, 31);
     off -= len;
-    // the slot assembled in shared memory, then stored with 16-byte writes
-    uint8_t *ss = sslot[w];
-    if (lane < 16) {
-        ss[2 * lane] = (uint8_t)cnt[lane];
-        ss[2 * lane + 1] = (uint8_t)(cnt[lane] >> 8);
-    }
-    ss[32 + 2 * lane] = (uint8_t)len;
-    ss[32 + 2 * lane + 1] = (uint8_t)(len >> 8);
-    for (uint32_t i = 0; i < len; ++i) ss[kEntHeader + off + i] = buf[pos + i];
-    __syncwarp();
     const uint32_t size = kEntHeader + total;
     uint8_t *slot = out + b * (int64_t)entropy_slot_bytes(d);
-    for (uint32_t i = 16 * lane; i < size; i += 16 * 32) {
-        if (i + 16 <= size) {
-            *reinterpret_cast<uint4 *>(slot + i) = *reinterpret_cast<const uint4 *>(ss + i);
-        } else {
-            for (uint32_t k = i; k < size; ++k) slot[k] = ss[k];
+    if (!__any_sync(0xffffffffu, nout > (uint32_t)kEntKeep)) {
+        // every lane kept its bytes: the slot assembled in shared memory (the
+        // codes are no longer needed), then stored with 16-byte writes
+        __syncwarp();
+        uint8_t *ss = sslot[w];
+        if (lane < 16) {
+            ss[2 * lane] = (uint8_t)myf;
+            ss[2 * lane + 1] = (uint8_t)(myf >> 8);
         }
+        ss[32 + 2 * lane] = (uint8_t)len;
+        ss[32 + 2 * lane + 1] = (uint8_t)(len >> 8);
+        uint8_t *st = ss + kEntHeader + off;
+        st[0] = (uint8_t)x;
+        st[1] = (uint8_t)(x >> 8);
+        st[2] = (uint8_t)(x >> 16);
+        st[3] = (uint8_t)(x >> 24);
+        for (uint32_t i = 0; i < nout; ++i) st[4 + i] = kept[nout - 1 - i];
+        __syncwarp();
+        for (uint32_t i = 16 * lane; i < size; i += 16 * 32) {
+            if (i + 16 <= size) {
+                *reinterpret_cast<uint4 *>(slot + i) = *reinterpret_cast<const uint4 *>(ss + i);
+            } else {
+                for (uint32_t k = i; k < size; ++k) slot[k] = ss[k];
+            }
+        }
+    } else {
+        // some stream is longer than what it kept: the same steps again, each
+        // byte written straight to its place in the slot (from the stream's
+        // end downwards), and the header beside them
+        if (lane < 16) {
+            slot[2 * lane] = (uint8_t)myf;
+            slot[2 * lane + 1] = (uint8_t)(myf >> 8);
+        }
+        slot[32 + 2 * lane] = (uint8_t)len;
+        slot[32 + 2 * lane + 1] = (uint8_t)(len >> 8);
+        uint8_t *st = slot + kEntHeader + off;
+        uint32_t pos = len;
+        x = kRansL;
+        nxt = smodel[w][sym_at(n - 1)];
+        for (int j = n - 1; j >= 0; --j) {
+            const uint4 md = nxt;
+            if (j > 0) nxt = smodel[w][sym_at(j - 1)];
+            const uint32_t xmax = xmax0 * md.x;
+            const bool e1 = x >= xmax;
+            if (e1) st[pos - 1] = (uint8_t)(x & 255u);
+            pos -= e1 ? 1u : 0u;
+            x = e1 ? x >> 8 : x;
+            const bool e2 = x >= xmax;
+            if (e2) st[pos - 1] = (uint8_t)(x & 255u);
+            pos -= e2 ? 1u : 0u;
+            x = e2 ? x >> 8 : x;
+            const uint32_t qd = div_by(x, Recip{md.z, md.w});
+            x = (qd << lg) + (x - qd * md.x) + md.y;
+        }
+        st[0] = (uint8_t)x;
+        st[1] = (uint8_t)(x >> 8);
+        st[2] = (uint8_t)(x >> 16);
+        st[3] = (uint8_t)(x >> 24);
     }
     if (lane == 0) nbytes[b] = size;
 }

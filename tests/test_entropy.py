@@ -126,6 +126,48 @@ def test_entropy_coder_matches_oracle_and_round_trips(name, T, S, G):
 
 
 @pytest.mark.gpu
+def test_entropy_coder_with_one_stream_far_above_four_bits_a_symbol():
+    """Blocks whose stream 0 (entries 0, 32, 64, ..) holds only rare symbols,
+    so that it needs far more than 4 bits a symbol, between ordinary blocks
+    (distributions of the oracle pins): every slot equals the oracle's byte
+    for byte and decodes back."""
+    import torch
+    from rate_adaptive_kv_block_b300 import kvq
+    G, nb = 128, 37
+    d = 32 * G
+    e = np.arange(d)
+    r = np.random.default_rng(12)
+    names = sorted(CASES)
+    sym = np.empty((nb, d), dtype=np.uint8)
+    for b in range(nb):
+        if b % 3 == 0:
+            sym[b] = np.where(e % 32 == 0, 1 + (e // 32 + b) % 15, 0)
+        else:
+            sym[b] = CASES[names[b % len(names)]](r, d)
+    codes_np = _pack(sym)
+    want = oracle.entropy_encode(codes_np, d)
+    len0 = want[0][32] | (want[0][33] << 8)
+    assert len0 - 4 > d // 32 // 2 + 32           # well above 4 bits a symbol
+    L = kvq.Layout(1, 32 * nb, G, G)
+    assert L.nblocks == nb
+    codes = torch.from_numpy(codes_np).cuda()
+    cap = kvq.kvq_entropy_slot_bytes(L)
+    out = torch.zeros((nb, cap), dtype=torch.uint8, device="cuda")
+    nbytes = torch.zeros(nb, dtype=torch.int32, device="cuda")
+    kvq.kvq_entropy_encode(codes, L, out, nbytes)
+    back = torch.empty_like(codes)
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    kvq.kvq_entropy_decode(out, L, back, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvq.KVQ_OK
+    assert torch.equal(back, codes)
+    got, sizes = out.cpu().numpy(), nbytes.cpu().numpy()
+    for b in range(nb):
+        assert sizes[b] == len(want[b])
+        assert bytes(got[b, :sizes[b]]) == want[b]
+
+
+@pytest.mark.gpu
 def test_entropy_decode_reports_a_damaged_slot():
     import torch
     from rate_adaptive_kv_block_b300 import kvq, synth
