@@ -335,7 +335,10 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
             const uint32_t e = ent[c];
             x = (e >> 16) * (x >> lg) + s - (e & 0xffffu);
             // a stream this coder wrote refills at most two bytes per symbol
-            // (the encoder's bound); never read past the stream
+            // (the encoder's bound); never read past the stream.  (Issue
+            // bound with eight CTAs per SM, this kernel takes the refills as
+            // branches; the run decoder, one warp per SM, loads both bytes
+            // ahead instead.)
             if (x < kRansL) {
                 if (p < end) x = (x << 8) | slot[p++];
                 else overrun = true;
@@ -562,6 +565,7 @@ entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, in
         p += 4;
     }
     bool overrun = false;
+    const uint32_t last = end - 1;                   // len >= 4 when the slot is good
     uint8_t *dst = codes + b0 * half;
     for (int bi = 0; bi < m; ++bi) {
         // this block's model: counts from the slot, cumulative counts by a scan
@@ -594,20 +598,21 @@ entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, in
         __syncwarp();
         for (int j = 0; j < n; ++j) {
             uint32_t c = 0;
-            if (!bad && !overrun) {
+            if (!bad) {
+                // the stream's next two bytes, loaded before the state is
+                // known (clamped to the stream: one that runs out is reported
+                // at the end), so that the chain from one state to the next
+                // holds one shared-memory load; at most two refills
+                const uint32_t b1 = sslot[min(p, last)], b2 = sslot[min(p + 1, last)];
                 const uint32_t e = smap[x & ((1u << lg) - 1u)];
                 c = e >> 28;
                 x = ((e >> 13) & 0x1fffu) * (x >> lg) + (e & 0x1fffu);
-                // at most two refill bytes per symbol, as in the per-block decoder
-                if (x < kRansL) {
-                    if (p < end) x = (x << 8) | sslot[p++];
-                    else overrun = true;
-                }
-                if (x < kRansL) {
-                    if (p < end) x = (x << 8) | sslot[p++];
-                    else overrun = true;
-                }
-                if (x < kRansL) overrun = true;
+                const uint32_t k1 = x < kRansL ? 1u : 0u;
+                x = k1 ? (x << 8) | b1 : x;
+                const uint32_t k2 = x < kRansL ? 1u : 0u;
+                x = k2 ? (x << 8) | b2 : x;
+                overrun |= x < kRansL;
+                p += k1 + k2;
             }
             const uint32_t hi = __shfl_xor_sync(0xffffffffu, c, 1);
             const int e = lane + 32 * j;
@@ -620,6 +625,7 @@ entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, in
             for (int i = lane; i < half / 16; i += 32) o4[i] = s4[i];
         }
     }
+    // p beyond the end: the stream ran out; before it: bytes left over
     overrun = overrun || (!bad && p != end);
     if (__any_sync(0xffffffffu, bad || overrun) && lane == 0) atomicMax(status, (int32_t)KVQ_ERR_CORRUPT);
 }
