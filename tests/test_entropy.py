@@ -183,15 +183,21 @@ def test_entropy_decode_reports_a_damaged_slot():
     torch.cuda.synchronize()
     back = torch.empty_like(buf.codes)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for damage in ("counts", "lengths", "stream"):
+    for damage in ("counts", "lengths", "stream", "short"):
         bad = out.clone()
         if damage == "counts":
             bad[1, 0] ^= 1                      # counts no longer add up to d
         elif damage == "lengths":
             bad[2, 33] = 0xFF                   # a stream longer than the slot
-        else:
+        elif damage == "stream":
             bad[3, 32] = 3                      # stream 0 shorter than its state
             bad[3, 33] = 0
+        else:
+            # stream 0 one byte short: it runs out just before its last symbols
+            n0 = int(bad[4, 32]) | (int(bad[4, 33]) << 8)
+            assert n0 > 4
+            bad[4, 32] = (n0 - 1) & 0xFF
+            bad[4, 33] = (n0 - 1) >> 8
         kvq.kvq_entropy_decode(bad, L, back, st)
         torch.cuda.synchronize()
         assert int(st.item()) == kvq.KVQ_ERR_CORRUPT, damage
@@ -298,15 +304,21 @@ def test_run_decode_reports_a_damaged_slot():
     back = torch.empty_like(buf.codes)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     h = 32 * nseg
-    for damage in ("counts", "lengths", "stream"):
+    for damage in ("counts", "lengths", "stream", "short"):
         bad = out.clone()
         if damage == "counts":
             bad[1, 32 * 2] ^= 1                 # block 2's counts no longer add up to d
         elif damage == "lengths":
             bad[2, h + 1] = 0xFF                # a stream longer than the slot
-        else:
+        elif damage == "stream":
             bad[3, h] = 3                       # stream 0 shorter than its state
             bad[3, h + 1] = 0
+        else:
+            # stream 0 one byte short: it runs out just before the run's end
+            n0 = int(bad[0, h]) | (int(bad[0, h + 1]) << 8)
+            assert n0 > 4
+            bad[0, h] = (n0 - 1) & 0xFF
+            bad[0, h + 1] = (n0 - 1) >> 8
         kvq.kvq_entropy_decode_runs(bad, L, nseg, back, st)
         torch.cuda.synchronize()
         assert int(st.item()) == kvq.KVQ_ERR_CORRUPT, damage
