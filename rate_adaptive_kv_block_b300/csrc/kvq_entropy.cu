@@ -454,9 +454,13 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     const uint32_t keep = run_keep_bytes(d, nseg);
     uint8_t *kept = scodes + (size_t)nseg * half + (size_t)lane * keep;
     const int nk = m * n;
+    // run position k = bi n + j (n = d / 32 = 2^(lg - 5)) is entry lane + 32 j
+    // of block bi: nibble (lane & 1) of code byte bi d / 2 + 16 j + lane / 2
+    // = 16 k + lane / 2 of the staged run
+    const uint8_t *mine = scodes + (lane >> 1);
+    const int nsh = 4 * (lane & 1), lgn = lg - 5;
     auto model_at = [&](int k) {
-        const int bi = k >> (lg - 5), j = k & (n - 1);     // n = d / 32, a power of two
-        return smodel[bi * 16 + nibble_at(scodes + bi * half, lane + 32 * j)];
+        return smodel[((k >> lgn) << 4) + ((mine[16 * k] >> nsh) & 15)];
     };
     uint32_t x = kRansL, nout = 0;
     uint4 nxt = model_at(nk - 1);
