@@ -469,12 +469,18 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
         if (k > 0) nxt = model_at(k - 1);
         const uint32_t xmax = xmax0 * md.x;
         // at most two bytes leave per symbol (x < 2^31, xmax >= 2^19)
+        // the low byte is stored whether or not it leaves: a byte that stays
+        // is overwritten by the next one that leaves (or lies past the
+        // stream's end); the index is clamped only once nout reaches keep,
+        // and such a stream takes the second pass.  (With one warp per SM
+        // the store is cheaper than the predicate; the per-block encoder,
+        // issue-bound, keeps its predicated store.)
         const uint32_t e1 = x >= xmax ? 1u : 0u;
-        if (e1 && nout < keep) kept[nout] = (uint8_t)x;
+        kept[min(nout, keep - 1u)] = (uint8_t)x;
         nout += e1;
         x >>= 8 * e1;
         const uint32_t e2 = x >= xmax ? 1u : 0u;
-        if (e2 && nout < keep) kept[nout] = (uint8_t)x;
+        kept[min(nout, keep - 1u)] = (uint8_t)x;
         nout += e2;
         x >>= 8 * e2;
         const uint32_t qd = div_by(x, Recip{md.z, md.w});
@@ -494,7 +500,7 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     slot[32 * m + 2 * lane + 1] = (uint8_t)(len >> 8);
     if (lane == 0) nbytes[rn] = hdr + total;
     uint8_t *st = slot + hdr + off;
-    if (!__any_sync(0xffffffffu, nout > keep)) {
+    if (!__any_sync(0xffffffffu, nout >= keep)) {      // below keep the index was never clamped
         // every lane kept its bytes: the stream holds them last first
         for (uint32_t i = 0; i < nout; ++i) st[4 + i] = kept[nout - 1 - i];
     } else {
