@@ -606,16 +606,20 @@ entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, in
             }
         }
         __syncwarp();
-        for (int j = 0; j < n; ++j) {
-            uint32_t c = 0;
-            if (!bad) {
+        if (bad) {
+            for (int i = lane; i < half; i += 32) sout[i] = 0;
+        } else {
+            for (int j = 0; j < n; ++j) {
                 // the stream's next two bytes, loaded before the state is
-                // known (clamped to the stream: one that runs out is reported
-                // at the end), so that the chain from one state to the next
-                // holds one shared-memory load; at most two refills
-                const uint32_t b1 = sslot[min(p, last)], b2 = sslot[min(p + 1, last)];
+                // known (one clamp to the stream: the byte after it is still
+                // inside this kernel's shared memory, and a stream that runs
+                // out is reported at the end), so that the chain from one
+                // state to the next holds one shared-memory load; at most two
+                // refills
+                const uint32_t pc = min(p, last);
+                const uint32_t b1 = sslot[pc], b2 = sslot[pc + 1];
                 const uint32_t e = smap[x & ((1u << lg) - 1u)];
-                c = e >> 28;
+                const uint32_t c = e >> 28;
                 x = ((e >> 13) & 0x1fffu) * (x >> lg) + (e & 0x1fffu);
                 const uint32_t k1 = x < kRansL ? 1u : 0u;
                 x = k1 ? (x << 8) | b1 : x;
@@ -623,10 +627,9 @@ entropy_decode_runs_kernel(const uint8_t *__restrict__ in, int64_t nb, int d, in
                 x = k2 ? (x << 8) | b2 : x;
                 overrun |= x < kRansL;
                 p += k1 + k2;
+                const uint32_t hi = __shfl_xor_sync(0xffffffffu, c, 1);
+                if ((lane & 1) == 0) sout[16 * j + (lane >> 1)] = (uint8_t)(c | (hi << 4));
             }
-            const uint32_t hi = __shfl_xor_sync(0xffffffffu, c, 1);
-            const int e = lane + 32 * j;
-            if ((lane & 1) == 0) sout[e >> 1] = (uint8_t)(c | (hi << 4));
         }
         __syncwarp();
         {
