@@ -327,11 +327,12 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
     // entry lane + 32 j is the low nibble of code byte 16 j + lane / 2 when
     // the lane is even, the high nibble of that byte when it is odd
     uint8_t *cout = codes + b * (d / 2) + (lane >> 1);
-    for (int j = 0; j < n; ++j) {
-        uint32_t c = 0;
-        if (!bad) {
+    if (bad) {
+        for (int i = lane; i < d / 2; i += 32) codes[b * (d / 2) + i] = 0;
+    } else {
+        for (int j = 0; j < n; ++j) {
             const uint32_t s = x & ((1u << lg) - 1u);
-            c = map[s];
+            const uint32_t c = map[s];
             const uint32_t e = ent[c];
             x = (e >> 16) * (x >> lg) + s - (e & 0xffffu);
             // a stream this coder wrote refills at most two bytes per symbol
@@ -348,9 +349,9 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
                 else overrun = true;
             }
             if (x < kRansL) overrun = true;            // a third: not such a stream
+            const uint32_t hi = __shfl_xor_sync(0xffffffffu, c, 1);
+            if ((lane & 1) == 0) cout[16 * j] = (uint8_t)(c | (hi << 4));
         }
-        const uint32_t hi = __shfl_xor_sync(0xffffffffu, c, 1);
-        if ((lane & 1) == 0) cout[16 * j] = (uint8_t)(c | (hi << 4));
     }
     overrun |= !bad && p != end;
     if (__any_sync(0xffffffffu, bad || overrun) && lane == 0) atomicMax(status, (int32_t)KVQ_ERR_CORRUPT);
@@ -466,7 +467,7 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     uint4 nxt = model_at(nk - 1);
     for (int k = nk - 1; k >= 0; --k) {
         const uint4 md = nxt;
-        if (k > 0) nxt = model_at(k - 1);
+        nxt = model_at(max(k - 1, 0));          // the last step reloads its own
         const uint32_t xmax = xmax0 * md.x;
         // at most two bytes leave per symbol (x < 2^31, xmax >= 2^19)
         // the low byte is stored whether or not it leaves: a byte that stays
