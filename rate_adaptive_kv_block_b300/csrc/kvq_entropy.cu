@@ -164,7 +164,7 @@ entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
     uint4 nxt = smodel[w][sym_at(n - 1)];     // the next symbol's model, one step ahead
     for (int j = n - 1; j >= 0; --j) {
         const uint4 md = nxt;
-        if (j > 0) nxt = smodel[w][sym_at(j - 1)];
+        nxt = smodel[w][sym_at(max(j - 1, 0))];   // the last step reloads its own
         const uint32_t xmax = xmax0 * md.x;
         // at most two bytes leave per symbol (x < 2^31, xmax >= 2^19): two
         // predicated steps instead of a loop whose trip count differs by lane
@@ -232,7 +232,7 @@ entropy_encode_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
         nxt = smodel[w][sym_at(n - 1)];
         for (int j = n - 1; j >= 0; --j) {
             const uint4 md = nxt;
-            if (j > 0) nxt = smodel[w][sym_at(j - 1)];
+            nxt = smodel[w][sym_at(max(j - 1, 0))];
             const uint32_t xmax = xmax0 * md.x;
             const bool e1 = x >= xmax;
             if (e1) st[pos - 1] = (uint8_t)(x & 255u);
@@ -511,7 +511,7 @@ entropy_encode_runs_kernel(const uint8_t *__restrict__ codes, int64_t nb, int d,
         nxt = model_at(nk - 1);
         for (int k = nk - 1; k >= 0; --k) {
             const uint4 md = nxt;
-            if (k > 0) nxt = model_at(k - 1);
+            nxt = model_at(max(k - 1, 0));
             const uint32_t xmax = xmax0 * md.x;
             const bool e1 = x >= xmax;
             if (e1) st[pos - 1] = (uint8_t)(x & 255u);
