@@ -374,7 +374,7 @@ entropy_decode_kernel(const uint8_t *__restrict__ in, int64_t nb, int d,
 // pass over the run counts each stream's bytes and keeps them, up to 4 bits a
 // symbol and some slack, in shared memory; once a warp scan of the lengths
 // has placed the streams, the kept bytes go out last first.  Only when some
-// stream is longer than what it could keep does a second pass recompute the
+// stream fills what it could keep does a second pass recompute the
 // chain and write the bytes downwards from the stream's end (known from the
 // first), so no worst-case scratch is held.  The decoder stages the run's
 // slot (as far as its stream lengths reach), builds each block's slot table
